@@ -1,0 +1,399 @@
+"""Benchmark: forward + backward of decayed causal linear attention on the
+Lightning-2 benchmark shape (batch 4, 32 heads, d = e = 128, bf16, ALiBi-style
+decay slopes, scale 1) at n = 32768 tokens per sequence.
+
+One step = la_fwd (o, final_state) + la_bwd (dq, dk, dv) over one batch.
+`value` is whole-job tokens/s (B*n per step per rank) with inputs resident in
+HBM (each 1.07 GB tensor is larger than the 129 MB L2, so no flush is
+needed); `e2e` is the same metric through the public Python API with pinned
+host buffers copied in and results copied out inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--n 32768] [--impl reference]
+
+`--impl reference` times the fp64 CPU oracle (the reference arm: there is no
+runnable reference implementation) on the host cores, on a bounded sample of
+the same workload.  Under torchrun (N > 1) every rank runs its own batch
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd tokens/s & % roofline at b4 h32 d=e=128 bf16, n=512..32768"
+# Lightning-Attention-2 README, Benchmark tables (hardware unstated): fwd 17.661427 ms and
+# bwd 74.594788 ms at n = 32768 -> 4*32768 / 92.256215 ms.
+PAGES_TOKENS_PER_S = {512: 4 * 512 / ((0.351540 + 1.169621) * 1e-3),
+                      1024: 4 * 1024 / ((0.585876 + 2.334296) * 1e-3),
+                      2048: 4 * 2048 / ((1.134238 + 4.657026) * 1e-3),
+                      4096: 4 * 4096 / ((2.240815 + 9.307817) * 1e-3),
+                      8192: 4 * 8192 / ((4.414397 + 18.617611) * 1e-3),
+                      16384: 4 * 16384 / ((8.832678 + 37.212578) * 1e-3),
+                      32768: 4 * 32768 / ((17.661427 + 74.594788) * 1e-3)}
+FALLBACK_HBM_GBS = 6800.0
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value, world_size, device=None):
+    """Max of a float over ranks (identity when world_size == 1)."""
+    if world_size == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_bench(args):
+    import torch
+    import linear_attention_head_gb300 as la
+    from linear_attention_head_gb300 import _native
+    import workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = W.sweep_bf16(args.n)
+    B, T, H, D, E = w.B, w.T, w.H, w.d, w.e
+    gen = torch.Generator(device=dev).manual_seed(1234 + rank)
+    q = torch.randn((B, T, H, D), generator=gen, device=dev).to(torch.bfloat16)
+    k = torch.randn((B, T, H, D), generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, T, H, E), generator=gen, device=dev).to(torch.bfloat16)
+    do = torch.randn((B, T, H, E), generator=gen, device=dev).to(torch.bfloat16)
+    g = w.g_gamma.to(dev)
+    scale = w.scale
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        o, fin = la.la_fwd(q, k, v, g, scale)
+        if ev is not None:
+            ev[1].record(stream)
+        dq = la.la_bwd_dq(q, k, v, do, g, scale)
+        if ev is not None:
+            ev[2].record(stream)
+        dk, dv, _ = la.la_bwd_dkdv(q, k, v, do, g, scale, want_d_initial_state=False)
+        if ev is not None:
+            ev[3].record(stream)
+        return o, dq, dk, dv
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    la.get_device_error(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    launches0 = _native.lib().la_launch_count()
+    t_wall0 = time.perf_counter()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = _native.lib().la_launch_count() - launches0
+    clocks = sampler.stop()
+    la.get_device_error(dev)
+    ms = start.elapsed_time(end)
+    ms = max_over_ranks(ms, ws, dev)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    dq_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    tokens_step = B * T
+    value = ws * tokens_step * args.steps / (ms * 1e-3)
+
+    # algorithmic bytes per launch (bf16 tokens, fp32 states): one unit = one token tensor
+    unit = B * T * H * D * 2
+    state_bytes = B * H * D * E * 4
+    bytes_fwd = 4 * unit + state_bytes          # read q, k, v; write o, final_state
+    bytes_dq = 4 * unit                         # read k, v, do; write dq
+    bytes_dkdv = 6 * unit                       # read q, k, v, do; write dk, dv
+    kern = {"la_fwd": (fwd_ms, bytes_fwd), "la_bwd_dq": (dq_ms, bytes_dq),
+            "la_bwd_dkdv": (dkdv_ms, bytes_dkdv)}
+    dom = max(kern, key=lambda n: kern[n][0])
+    dom_ms, dom_bytes = kern[dom]
+    peak, peak_src = peaks()
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            with open(tr_path) as f:
+                tr = json.load(f)
+            entry = tr.get(dom)
+            if entry and entry.get("source_sha") == source_sha() and entry.get("n") == T:
+                traffic = entry["bytes_per_launch"]
+        except Exception:
+            traffic = None
+    step_bytes = bytes_fwd + bytes_dq + bytes_dkdv
+    roof_ms = (4 * unit + 7 * unit + state_bytes) / (peak * 1e9) * 1e3
+
+    # end to end: pinned host buffers -> device -> fwd+bwd -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.to("cpu").pin_memory() for t in (q, k, v, do))
+        houts = [torch.empty((B, T, H, E), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((B, T, H, D), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((B, T, H, D), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((B, T, H, E), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((B, H, D, E), dtype=torch.float32).pin_memory()]
+
+        def e2e_step():
+            dq_, dk_, dv_ = (hq.to(dev, non_blocking=True), hk.to(dev, non_blocking=True),
+                             hv.to(dev, non_blocking=True))
+            ddo = hdo.to(dev, non_blocking=True)
+            o, fin = la.la_fwd(dq_, dk_, dv_, g, scale)
+            gq, gk, gv, _ = la.la_bwd(dq_, dk_, dv_, ddo, g, scale, want_d_initial_state=False)
+            for h, d_ in zip(houts, (o, gq, gk, gv, fin)):
+                h.copy_(d_, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 2))):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(1, min(args.steps, 10))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
+        bi = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        bo = sum(t.numel() * t.element_size() for t in houts)
+        e2e = {"value": ws * tokens_step * ke / (e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": ke}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGES_TOKENS_PER_S[T] if T in PAGES_TOKENS_PER_S else None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "fwd+bwd b%d h%d n%d d=e=%d bf16, ALiBi slopes, scale 1"
+                   % (B, H, T, D), "B": B, "H": H, "n": T, "d": D, "e": E,
+                   "l2": "inputs larger than L2 (%.2f GB per token tensor), no flush" %
+                   (unit / 1e9), "parallelism": "dp%d" % ws},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else peak_src,
+                     "step_frac": roof_ms / (ms / args.steps)},
+        "kernels_ms": {"la_fwd": fwd_ms, "la_bwd_dq": dq_ms, "la_bwd_dkdv": dkdv_ms},
+        "bytes_per_call": {"la_fwd": bytes_fwd, "la_bwd_dq": bytes_dq,
+                           "la_bwd_dkdv": bytes_dkdv},
+        "kernel_family": la.kernel_family(B, T, H, D, E),
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": e2e,
+        "wall_s_timed": t_wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.n, args.cpu_pairs)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_attention_head_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _oracle_sample(n, pairs, n_sample, seed=0):
+    """A bounded sample of the workload for the CPU oracle: `pairs` (batch, head)
+    streams (heads spread over the decay slopes) of the first n_sample tokens.  The
+    oracle's cost is linear in the tokens of each stream, so tokens/s of the sample
+    scales to the full job by the ratio of streams."""
+    import torch
+    import workloads as W
+    w = W.sweep_bf16(n)
+    H = w.H
+    heads = [int(round(i * (H - 1) / max(pairs - 1, 1))) for i in range(pairs)]
+    gen = torch.Generator().manual_seed(seed)
+    shp = (1, min(n, n_sample), pairs, w.d)
+    q, k, v, do = (torch.randn(shp, generator=gen).bfloat16() for _ in range(4))
+    g = w.g_gamma[heads].clone()
+    return w, q, k, v, do, g
+
+
+def _oracle_step(w, q, k, v, do, g, cores):
+    import oracle
+    oracle.forward(q, k, v, g, w.scale, threads=cores)
+    oracle.backward(q, k, v, g, w.scale, do, threads=cores)
+
+
+def cpu_baseline(n, pairs=None, n_sample=8192):
+    """The fp64 oracle as it stands, fwd+bwd, timed on the host cores on a bounded sample;
+    reported as the full workload's tokens/s."""
+    import oracle
+    cores = os.cpu_count() or 1
+    pairs = pairs or min(cores, 16)
+    w, q, k, v, do, g = _oracle_sample(n, pairs, n_sample)
+    oracle._load()
+    t0 = time.perf_counter()
+    _oracle_step(w, q, k, v, do, g, cores)
+    dt = time.perf_counter() - t0
+    ns = q.shape[1]
+    value = pairs * ns / dt / w.H          # tokens of one (all-heads) sequence per second
+    return {"value": value, "unit": "tokens/s", "cores": min(cores, pairs), "kind": "oracle",
+            "sample": "fwd+bwd of %d (batch, head) streams x %d tokens of the %d x %d-token "
+                      "workload in %.2f s on %d threads; tokens/s = streams*tokens/time/H"
+                      % (pairs, ns, w.B * w.H, n, dt, min(cores, pairs))}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cores = os.cpu_count() or 1
+    pairs = args.cpu_pairs or min(cores, 16)
+    w, q, k, v, do, g = _oracle_sample(args.n, pairs, 4096)
+    oracle._load()
+    for _ in range(max(0, min(args.warmup, 1))):
+        _oracle_step(w, q[:, :128], k[:, :128], v[:, :128], do[:, :128], g, cores)
+    dt = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _oracle_step(w, q, k, v, do, g, cores)
+        dt += time.perf_counter() - t0
+    ns = q.shape[1]
+    value = pairs * ns * args.steps / dt / w.H
+    sample = ("per step: fwd+bwd of %d (batch, head) streams x %d tokens of the %d x %d-token "
+              "workload on %d host threads; tokens/s = streams*tokens/time/H"
+              % (pairs, ns, w.B * w.H, args.n, min(cores, pairs)))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": w.B * args.n / value * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "fwd+bwd b%d h%d n%d d=e=%d bf16, ALiBi slopes, scale 1"
+                       % (w.B, w.H, args.n, w.d), "B": w.B, "H": w.H, "n": args.n,
+                       "d": w.d, "e": w.e, "parallelism": "dp%d" % ws},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, pairs),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--n", type=int, default=32768)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-pairs", type=int, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_bench(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) library for causal linear attention
+ * with a per-head scalar exponential decay (Lightning attention / the
+ * `g_gamma` path of ejkernel's `recurrent`).
+ *
+ * The operation (ejkernel docs, kernels/_xla/recurrent/_interface, `recurrent`
+ * docstring, "The core update", with the per-head `g_gamma` decay of its Args
+ * and of the kernels/_triton/lightning_attn/_interface page), per sequence n
+ * and head h, with gamma = exp(g_gamma[h]) and tokens t in processing order:
+ *
+ *     S_t = gamma * S_{t-1} + k_t^T v_t          (S: d x e, fp32)
+ *     o_t = (scale * q_t) S_t                    (an e-vector)
+ *
+ * S_0 = initial_state (or zeros); final_state = S after the last processed
+ * token.  With reverse != 0 the tokens of every sequence are processed from
+ * last to first (o is still written at each token's own position).  With
+ * cu_seqlens the batch is one packed row of sequences [cu[n], cu[n+1]), each
+ * with its own state.  The library evaluates this in the chunked form of
+ * Lightning Attention-2 (OpenNLPLab/lightning-attention README): per chunk an
+ * intra-chunk decay-masked (Q K^T) V product plus an inter-chunk carried state.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees, keeps or allocates them.  cu_seqlens_host is a HOST pointer.
+ *   - Token tensors are indexed [batch, token, head, channel] through element
+ *     strides (batch, token, head); the channel dimension must be contiguous.
+ *     q, k, dq, dk share qk_strides; v, o, do, dv share v_strides.  Both the
+ *     token-major layout [B,T,H,X] (ejkernel) and the head-major layout
+ *     [B,H,T,X] (Lightning-2's (b, h, n, d)) are expressible.  Outputs must
+ *     not overlap inputs or each other.
+ *   - State tensors (initial_state, final_state, d_final_state,
+ *     d_initial_state) are dense fp32 [N, H, D, E], N = B, or num_seqs when
+ *     cu_seqlens is given.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) of the current device.  No entry point
+ *     allocates device memory or synchronizes, except: when cu_seqlens is given
+ *     without cu_seqlens_host the library copies cu_seqlens to the host and
+ *     waits for that copy; and la_get_device_error synchronizes `stream`.
+ *   - Every argument is validated before anything is enqueued.  A failed
+ *     validation returns LA_ERR_INVALID_ARG or LA_ERR_UNSUPPORTED, launches
+ *     nothing and leaves every output untouched; la_last_error() describes it.
+ *   - Every output is fully overwritten (no accumulation into outputs).
+ */
+#ifndef LA_GB300_H
+#define LA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum la_status {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride or cu_seqlens        */
+    LA_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels handle  */
+    LA_ERR_CUDA = 3,          /* a CUDA runtime call or a launch failed         */
+    LA_ERR_TIMEOUT = 4        /* a bounded on-device wait ran out (device word) */
+} la_status;
+
+/* Element type of the token tensors q, k, v, o, do, dq, dk, dv.  g_gamma and
+ * every state tensor are always fp32. */
+typedef enum la_dtype {
+    LA_DTYPE_BF16 = 0,
+    LA_DTYPE_F32 = 1
+} la_dtype;
+
+/* Problem sizes and layout.
+ *   batch      B  >= 0; must be 1 when cu_seqlens is given (lightning_attn
+ *                 docstring, Raises: batch must be 1 with cu_seqlens)
+ *   seq_len    T  >= 0 tokens per batch row (total tokens when packed)
+ *   heads      H  1..65535; keys and values have the same head count as
+ *                 queries (the lightning_attn docstring's "Must have the same
+ *                 shape as q")
+ *   dim_qk     D  query/key channels, 1..256
+ *   dim_v      E  value channels, 1..256
+ *   num_seqs   N  number of packed sequences when cu_seqlens is given
+ *                 (ignored otherwise; N = B)
+ *   qk_strides element strides (batch, token, head) of q, k, dq, dk
+ *   v_strides  element strides (batch, token, head) of v, o, do, dv        */
+typedef struct la_dims {
+    int32_t batch;
+    int32_t seq_len;
+    int32_t heads;
+    int32_t dim_qk;
+    int32_t dim_v;
+    int32_t num_seqs;
+    int64_t qk_strides[3];
+    int64_t v_strides[3];
+} la_dims;
+
+/* Forward pass (ejkernel `recurrent` / `lightning_attn`: returns the output
+ * and the final hidden state).
+ *   q, k            [B,T,H,D] of `dtype`
+ *   v               [B,T,H,E] of `dtype`
+ *   g_gamma         [H] fp32 log-decay per head (gamma = exp(g_gamma[h]);
+ *                   values > 0 are accepted but grow the state)
+ *   scale           multiplies q only (the pages' softmax_scale; callers apply
+ *                   the default 1/sqrt(D) themselves)
+ *   initial_state   [N,H,D,E] fp32, or NULL for zeros
+ *   reverse         0: t = 0..L-1 per sequence; 1: t = L-1..0
+ *   cu_seqlens      device int32 [N+1] with cu[0] = 0, non-decreasing,
+ *                   cu[N] = T; or NULL for B independent rows of length T
+ *   cu_seqlens_host host copy of cu_seqlens, or NULL (then copied, see above)
+ *   o               [B,T,H,E] of `dtype` (output, v_strides)
+ *   final_state     [N,H,D,E] fp32 output, or NULL to skip it              */
+la_status la_fwd(const la_dims *dims, int32_t dtype,
+                 const void *q, const void *k, const void *v,
+                 const float *g_gamma, float scale,
+                 const float *initial_state, int32_t reverse,
+                 const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                 void *o, float *final_state, void *stream);
+
+/* Backward pass: gradients of  sum(o * d_o) + sum(final_state * d_final_state)
+ * (the custom VJP of ejkernel `recurrent`, `_recurrent_bwd`, with upstream
+ * grads (do, dfinal_state); g_gamma, scale, reverse and cu_seqlens are not
+ * differentiated, as on that page).  Nothing from the forward pass is needed:
+ * the states are recomputed.  Packed sequences are supported (the pages raise
+ * NotImplementedError there; here each sequence gets its own gradient).
+ *   q, k, v, g_gamma, scale, initial_state, reverse, cu_seqlens: as la_fwd
+ *   d_o             [B,T,H,E] of `dtype` (v_strides)
+ *   d_final_state   [N,H,D,E] fp32, or NULL for zeros
+ *   dq, dk          [B,T,H,D] of `dtype` outputs (qk_strides)
+ *   dv              [B,T,H,E] of `dtype` output (v_strides)
+ *   d_initial_state [N,H,D,E] fp32 output, or NULL to skip it
+ * la_bwd is exactly la_bwd_dq followed by la_bwd_dkdv on the same stream.  */
+la_status la_bwd(const la_dims *dims, int32_t dtype,
+                 const void *q, const void *k, const void *v, const void *d_o,
+                 const float *g_gamma, float scale,
+                 const float *initial_state, const float *d_final_state,
+                 int32_t reverse,
+                 const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                 void *dq, void *dk, void *dv, float *d_initial_state,
+                 void *stream);
+
+/* The first half of la_bwd: dq only (a sweep in processing order that
+ * recomputes the states; q and d_final_state are not read).  Arguments as
+ * la_bwd; q may be NULL. */
+la_status la_bwd_dq(const la_dims *dims, int32_t dtype,
+                    const void *q, const void *k, const void *v, const void *d_o,
+                    const float *g_gamma, float scale,
+                    const float *initial_state, int32_t reverse,
+                    const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                    void *dq, void *stream);
+
+/* The second half of la_bwd: dk, dv and d_initial_state (a sweep against
+ * the processing order carrying dL/dS; initial_state is not read).
+ * Arguments as la_bwd; d_initial_state may be NULL. */
+la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype,
+                      const void *q, const void *k, const void *v, const void *d_o,
+                      const float *g_gamma, float scale,
+                      const float *d_final_state, int32_t reverse,
+                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                      void *dk, void *dv, float *d_initial_state, void *stream);
+
+/* Reads and clears the device-side error word that bounded on-device waits
+ * set when they run out (LA_ERR_TIMEOUT), after synchronizing `stream`.
+ * Returns LA_OK when no wait ran out, LA_ERR_TIMEOUT when one did, or
+ * LA_ERR_CUDA when the synchronization itself failed.  The word is shared by
+ * every stream of the current device. */
+la_status la_get_device_error(void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *la_strerror(int32_t status);
+
+/* Human-readable detail of the last failed call on this host thread (empty
+ * string when none).  Valid until the next call on the same thread. */
+const char *la_last_error(void);
+
+/* Which kernel family la_fwd would launch for these sizes and dtype, assuming
+ * 16-byte aligned base pointers: 1 = tensor-core (tcgen05) chunked kernels,
+ * 0 = CUDA-core chunked kernels, -1 = invalid or unsupported.  Pure host
+ * function; launches nothing. */
+int32_t la_kernel_family(const la_dims *dims, int32_t dtype);
+
+/* Number of kernels this library has enqueued since it was loaded (all
+ * devices, all host threads).  Pure host counter; lets a caller count the
+ * launches inside a timed region. */
+uint64_t la_launch_count(void);
+
+/* ABI version, (major << 16) | minor. */
+int32_t la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LA_GB300_H */

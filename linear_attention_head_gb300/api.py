@@ -1,0 +1,334 @@
+"""Tensor-level API over the C ABI: argument marshalling only.
+
+Every step of the computation runs in the CUDA kernels of liblagb300.so; this
+module only checks devices/dtypes, allocates outputs with torch (device
+memory), and passes pointers, strides and the current CUDA stream.
+
+Entry points mirror the pages:
+  * `la_fwd` / `la_bwd` / `la_bwd_dq` / `la_bwd_dkdv`: the C ABI, one call each.
+  * `recurrent(query, key, value, g_gamma=..., ...)`: ejkernel's `recurrent`
+    restricted to the Lightning `g_gamma` gate, differentiable.
+  * `lightning_attn(query, key, value, layer_idx, num_layers, ...)`: ejkernel's
+    Lightning wrapper (layer-dependent g_gamma).
+  * `lightning_attn_func(q, k, v, s)`: the Lightning-Attention-2 README call,
+    layout (b, h, n, d), decay exp(-s).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native as N
+
+Tensor = torch.Tensor
+
+
+def lightning_g_gamma(num_heads: int, layer_idx: int, num_layers: int) -> Tensor:
+    """ejkernel lightning_attn, "Key innovation":
+    g_gamma = -(8 / num_heads) * (1 - layer_idx / num_layers) * arange(num_heads)."""
+    return -(8.0 / num_heads * (1.0 - layer_idx / num_layers)) * torch.arange(
+        num_heads, dtype=torch.float32)
+
+
+def _dtype_code(t: Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return N.LA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return N.LA_DTYPE_F32
+    raise TypeError("token tensors must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t: Optional[Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+class _Packed:
+    """cu_seqlens on the device plus a host copy (so the library never syncs)."""
+
+    def __init__(self, cu_seqlens, device):
+        self.dev = None
+        self.host = None
+        self.n = 0
+        if cu_seqlens is None:
+            return
+        cu = torch.as_tensor(cu_seqlens)
+        if cu.ndim != 1:
+            raise ValueError("cu_seqlens must be 1-D")
+        self.host = cu.detach().to("cpu", torch.int32).contiguous()
+        if cu.device.type == "cuda" and cu.dtype == torch.int32 and cu.is_contiguous():
+            self.dev = cu
+        else:
+            self.dev = self.host.to(device)
+        self.n = self.host.numel() - 1
+
+    def host_ptr(self):
+        return None if self.host is None else ctypes.c_void_p(self.host.data_ptr())
+
+
+def _check_tokens(q, k, v, extra=()):
+    if q.ndim != 4 or k.shape != q.shape or v.ndim != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B, T, H, D] and v [B, T, H, E] (got %s, %s, %s)"
+                         % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    for t in (q, k, v) + tuple(extra):
+        if t.device.type != "cuda":
+            raise ValueError("token tensors must be CUDA tensors")
+        if t.dtype != q.dtype:
+            raise TypeError("all token tensors must share one dtype")
+        if t.device != q.device:
+            raise ValueError("all tensors must be on one device")
+
+
+def _channel_contiguous(ts):
+    return [t if t.stride(-1) == 1 or t.shape[-1] == 1 else t.contiguous() for t in ts]
+
+
+def _same_strides(group):
+    """The ABI shares one stride triple per group; make the group agree."""
+    s0 = group[0].stride()[:3]
+    if all(t.stride()[:3] == s0 for t in group):
+        return group
+    return [t.contiguous() for t in group]
+
+
+def _dims(q, v, packed: _Packed) -> N.LaDims:
+    B, T, H, D = q.shape
+    E = v.shape[3]
+    d = N.LaDims()
+    d.batch, d.seq_len, d.heads, d.dim_qk, d.dim_v = B, T, H, D, E
+    d.num_seqs = packed.n
+    for i in range(3):
+        d.qk_strides[i] = q.stride(i)
+        d.v_strides[i] = v.stride(i)
+    return d
+
+
+def _state(x: Optional[Tensor], shape, device, name) -> Optional[Tensor]:
+    if x is None:
+        return None
+    if tuple(x.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(x.shape)))
+    return x.to(device=device, dtype=torch.float32).contiguous()
+
+
+def _g(g_gamma, H, device) -> Tensor:
+    g = torch.as_tensor(g_gamma, dtype=torch.float32)
+    if g.numel() == 1 and H != 1:
+        g = g.reshape(1).expand(H)
+    if tuple(g.shape) != (H,):
+        raise ValueError("g_gamma must have shape [num_heads] = [%d]" % H)
+    return g.to(device).contiguous()
+
+
+def _num_states(q, packed):
+    return packed.n if packed.dev is not None else q.shape[0]
+
+
+def _like(t: Tensor) -> Tensor:
+    """Uninitialised output with t's shape, dtype and (dense) strides."""
+    return torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
+
+
+def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = None,
+           initial_state: Optional[Tensor] = None, reverse: bool = False,
+           cu_seqlens=None, out: Optional[Tensor] = None,
+           final_state: Optional[Tensor] = None, want_final_state: bool = True
+           ) -> Tuple[Tensor, Optional[Tensor]]:
+    """Forward pass. q, k: [B,T,H,D]; v: [B,T,H,E]; returns (o [B,T,H,E], final [N,H,D,E])."""
+    _check_tokens(q, k, v)
+    q, k, v = _channel_contiguous((q, k, v))
+    q, k = _same_strides([q, k])
+    dev = q.device
+    packed = _Packed(cu_seqlens, dev)
+    B, T, H, D = q.shape
+    E = v.shape[3]
+    Nst = _num_states(q, packed)
+    g = _g(g_gamma, H, dev)
+    scale = float(D ** -0.5 if scale is None else scale)
+    init = _state(initial_state, (Nst, H, D, E), dev, "initial_state")
+    if out is None:
+        out = _like(v)
+    if out.shape != v.shape or out.stride()[:3] != v.stride()[:3] or out.dtype != v.dtype:
+        raise ValueError("out must match v in shape, strides and dtype")
+    if final_state is None and want_final_state:
+        final_state = torch.empty((Nst, H, D, E), device=dev, dtype=torch.float32)
+    dims = _dims(q, v, packed)
+    st = N.lib().la_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                        scale, _ptr(init), int(bool(reverse)), _ptr(packed.dev),
+                        packed.host_ptr(), _ptr(out), _ptr(final_state), _stream(dev))
+    N.check(st)
+    return out, final_state
+
+
+def _bwd_prep(q, k, v, do, g_gamma, scale, initial_state, d_final_state, cu_seqlens):
+    _check_tokens(q, k, v, (do,))
+    if do.shape != v.shape:
+        raise ValueError("do must have v's shape")
+    q, k, v, do = _channel_contiguous((q, k, v, do))
+    q, k = _same_strides([q, k])
+    v, do = _same_strides([v, do])
+    dev = q.device
+    packed = _Packed(cu_seqlens, dev)
+    B, T, H, D = q.shape
+    E = v.shape[3]
+    Nst = _num_states(q, packed)
+    g = _g(g_gamma, H, dev)
+    scale = float(D ** -0.5 if scale is None else scale)
+    init = _state(initial_state, (Nst, H, D, E), dev, "initial_state")
+    dfin = _state(d_final_state, (Nst, H, D, E), dev, "d_final_state")
+    return q, k, v, do, dev, packed, g, scale, init, dfin, Nst
+
+
+def la_bwd(q: Tensor, k: Tensor, v: Tensor, do: Tensor, g_gamma, scale: Optional[float] = None,
+           initial_state: Optional[Tensor] = None, d_final_state: Optional[Tensor] = None,
+           reverse: bool = False, cu_seqlens=None, want_d_initial_state: bool = True):
+    """Backward pass: returns (dq, dk, dv, d_initial_state) of
+    sum(o*do) + sum(final_state*d_final_state)."""
+    q, k, v, do, dev, packed, g, scale, init, dfin, Nst = _bwd_prep(
+        q, k, v, do, g_gamma, scale, initial_state, d_final_state, cu_seqlens)
+    dq, dk, dv = _like(q), _like(q), _like(v)
+    dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
+                         dtype=torch.float32) if want_d_initial_state else None)
+    dims = _dims(q, v, packed)
+    st = N.lib().la_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
+                        _ptr(g), scale, _ptr(init), _ptr(dfin), int(bool(reverse)),
+                        _ptr(packed.dev), packed.host_ptr(), _ptr(dq), _ptr(dk), _ptr(dv),
+                        _ptr(dinit), _stream(dev))
+    N.check(st)
+    return dq, dk, dv, dinit
+
+
+def la_bwd_dq(q, k, v, do, g_gamma, scale=None, initial_state=None, reverse=False,
+              cu_seqlens=None):
+    """dq only (one sweep in processing order)."""
+    q, k, v, do, dev, packed, g, scale, init, _, _ = _bwd_prep(
+        q, k, v, do, g_gamma, scale, initial_state, None, cu_seqlens)
+    dq = _like(q)
+    dims = _dims(q, v, packed)
+    st = N.lib().la_bwd_dq(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
+                           _ptr(do), _ptr(g), scale, _ptr(init), int(bool(reverse)),
+                           _ptr(packed.dev), packed.host_ptr(), _ptr(dq), _stream(dev))
+    N.check(st)
+    return dq
+
+
+def la_bwd_dkdv(q, k, v, do, g_gamma, scale=None, d_final_state=None, reverse=False,
+                cu_seqlens=None, want_d_initial_state=True):
+    """dk, dv and d_initial_state (one sweep against processing order)."""
+    q, k, v, do, dev, packed, g, scale, _, dfin, Nst = _bwd_prep(
+        q, k, v, do, g_gamma, scale, None, d_final_state, cu_seqlens)
+    dk, dv = _like(q), _like(v)
+    dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
+                         dtype=torch.float32) if want_d_initial_state else None)
+    dims = _dims(q, v, packed)
+    st = N.lib().la_bwd_dkdv(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
+                             _ptr(do), _ptr(g), scale, _ptr(dfin), int(bool(reverse)),
+                             _ptr(packed.dev), packed.host_ptr(), _ptr(dk), _ptr(dv),
+                             _ptr(dinit), _stream(dev))
+    N.check(st)
+    return dk, dv, dinit
+
+
+def get_device_error(device=None) -> None:
+    """Raises LaError(LA_ERR_TIMEOUT) if an on-device bounded wait ran out."""
+    N.check(N.lib().la_get_device_error(_stream(device)))
+
+
+def kernel_family(B, T, H, D, E, dtype=torch.bfloat16, layout="bthd") -> int:
+    """1 = tensor-core kernels, 0 = CUDA-core kernels, -1 = unsupported."""
+    d = N.LaDims()
+    d.batch, d.seq_len, d.heads, d.dim_qk, d.dim_v, d.num_seqs = B, T, H, D, E, 0
+    if layout == "bthd":
+        qs, vs = (T * H * D, H * D, D), (T * H * E, H * E, E)
+    else:  # bhtd
+        qs, vs = (H * T * D, D, T * D), (H * T * E, E, T * E)
+    for i in range(3):
+        d.qk_strides[i] = qs[i]
+        d.v_strides[i] = vs[i]
+    code = N.LA_DTYPE_BF16 if dtype == torch.bfloat16 else N.LA_DTYPE_F32
+    return int(N.lib().la_kernel_family(ctypes.byref(d), code))
+
+
+class _LinearAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, init, g, scale, reverse, cu):
+        o, fin = la_fwd(q, k, v, g, scale, init, reverse, cu)
+        ctx.save_for_backward(q, k, v, init, g)
+        ctx.scale, ctx.reverse, ctx.cu = scale, reverse, cu
+        ctx.has_init = init is not None
+        return o, fin
+
+    @staticmethod
+    def backward(ctx, do, dfin):
+        q, k, v, init, g = ctx.saved_tensors
+        if do is None:
+            do = torch.zeros_like(v)
+        dq, dk, dv, dinit = la_bwd(q, k, v, do.to(v.dtype), g, ctx.scale,
+                                   init if ctx.has_init else None, dfin, ctx.reverse, ctx.cu,
+                                   want_d_initial_state=ctx.has_init)
+        return dq, dk, dv, (dinit if ctx.has_init else None), None, None, None, None
+
+
+def recurrent(query: Tensor, key: Tensor, value: Tensor, g=None, g_gamma=None, gk=None, gv=None,
+              softmax_scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
+              reverse: bool = False, cu_seqlens=None):
+    """ejkernel `recurrent` with the Lightning per-head `g_gamma` gate (the only gate on
+    this path).  Accepts [B,T,H,D] or packed [T_total,H,D] with cu_seqlens.
+    Returns (o, final_state); differentiable in query, key, value, initial_state."""
+    if g is not None or gk is not None or gv is not None:
+        raise NotImplementedError("only the per-head g_gamma decay is implemented")
+    squeeze = False
+    if query.ndim == 3:
+        if cu_seqlens is None:
+            raise ValueError("3-D inputs need cu_seqlens")
+        query, key, value = query[None], key[None], value[None]
+        squeeze = True
+    if cu_seqlens is not None and query.shape[0] != 1:
+        raise ValueError("The batch size is expected to be 1 rather than %d when using "
+                         "`cu_seqlens`." % query.shape[0])
+    H = query.shape[2]
+    if g_gamma is None:
+        g_gamma = torch.zeros(H, dtype=torch.float32)
+    g = _g(g_gamma, H, query.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(query.shape[-1])
+    o, fin = _LinearAttention.apply(query, key, value, initial_state, g, softmax_scale,
+                                    bool(reverse), cu_seqlens)
+    return (o[0] if squeeze else o), fin
+
+
+def lightning_attn(query: Tensor, key: Tensor, value: Tensor, layer_idx: int, num_layers: int,
+                   softmax_scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
+                   reverse: bool = False, cu_seqlens=None):
+    """ejkernel `lightning_attn`: g_gamma from the layer position, then `recurrent`."""
+    if cu_seqlens is not None:
+        if query.ndim == 4 and query.shape[0] != 1:
+            raise ValueError("The batch size is expected to be 1 rather than %d when using "
+                             "`cu_seqlens`." % query.shape[0])
+        n = len(cu_seqlens) - 1
+        if initial_state is not None and initial_state.shape[0] != n:
+            raise ValueError("The number of initial states is expected to be equal to the "
+                             "number of input sequences, i.e., %d rather than %d."
+                             % (n, initial_state.shape[0]))
+    if softmax_scale is None:
+        softmax_scale = key.shape[-1] ** -0.5
+    H = query.shape[-2]
+    return recurrent(query, key, value, g_gamma=lightning_g_gamma(H, layer_idx, num_layers),
+                     softmax_scale=softmax_scale, initial_state=initial_state, reverse=reverse,
+                     cu_seqlens=cu_seqlens)
+
+
+def lightning_attn_func(q: Tensor, k: Tensor, v: Tensor, s: Tensor) -> Tensor:
+    """Lightning-Attention-2 README call: q, k [b,h,n,d], v [b,h,n,e], slopes s [h]
+    (decay exp(-s)), scale 1.  Returns o [b,h,n,e]; differentiable."""
+    g = -torch.as_tensor(s, dtype=torch.float32).reshape(-1)
+    # (b, h, n, d) -> (b, n, h, d) views: no copy, the ABI takes the strides.
+    o, _ = _LinearAttention.apply(q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2), None,
+                                  g.to(q.device), 1.0, False, None)
+    return o.transpose(1, 2)

@@ -1,0 +1,373 @@
+// la_api.cu -- the C ABI declared in include/la.h: argument validation, the
+// packed-sequence table, and the mapping of la_fwd / la_bwd onto the two
+// sweep shapes of la_internal.h.
+//
+// Backward by role swap (the gradient of the recurrence in the ejkernel
+// `recurrent` custom VJP, `_recurrent_bwd`, written out per token):
+//   dq_t = s * S_t do_t                  -> the forward-type sweep on
+//                                           (q, k, v) := (do, v, k), state S^T
+//   dv_u = sum_t ... (q_t . k_u) do_t + G^T k_u    -> backward-type sweep
+//   dk_u = sum_t ... (do_t . v_u) q_t + G v_u      -> backward-type sweep on
+//                                           (q, k, w) := (do, v, q), G^T
+// so the kernels never see the words "query" or "gradient"; the host decides
+// which tensors play which role.
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "../../include/la.h"
+#include "la_internal.h"
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+
+void la::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local std::string g_msg;
+
+la_status fail(la_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_msg = buf;
+    return st;
+}
+
+la_status cuda_fail(cudaError_t e, const char *where)
+{
+    return fail(LA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+struct Problem {
+    int B, T, H, D, E, N;
+    bool packed;
+};
+
+// Sizes, dtype and the packed-sequence table; fills *P.
+la_status check_dims(const la_dims *d, int32_t dtype, const int32_t *cu, const int32_t *cu_host,
+                     cudaStream_t stream, Problem *P)
+{
+    if (!d)
+        return fail(LA_ERR_INVALID_ARG, "dims is NULL");
+    if (dtype != LA_DTYPE_BF16 && dtype != LA_DTYPE_F32)
+        return fail(LA_ERR_INVALID_ARG, "dtype %d is neither LA_DTYPE_BF16 nor LA_DTYPE_F32",
+                    dtype);
+    if (d->batch < 0 || d->seq_len < 0)
+        return fail(LA_ERR_INVALID_ARG, "negative batch (%d) or seq_len (%d)", d->batch,
+                    d->seq_len);
+    if (d->heads < 1 || d->heads > 65535)
+        return fail(LA_ERR_INVALID_ARG, "heads = %d outside 1..65535", d->heads);
+    if (d->dim_qk < 1 || d->dim_qk > 256 || d->dim_v < 1 || d->dim_v > 256)
+        return fail(LA_ERR_UNSUPPORTED, "head dims D = %d, E = %d: supported range is 1..256",
+                    d->dim_qk, d->dim_v);
+    for (int i = 0; i < 3; ++i)
+        if (d->qk_strides[i] < 0 || d->v_strides[i] < 0)
+            return fail(LA_ERR_INVALID_ARG, "negative stride");
+    P->B = d->batch;
+    P->T = d->seq_len;
+    P->H = d->heads;
+    P->D = d->dim_qk;
+    P->E = d->dim_v;
+    P->packed = cu != nullptr;
+    if (!cu) {
+        if (cu_host)
+            return fail(LA_ERR_INVALID_ARG, "cu_seqlens_host given without cu_seqlens");
+        if (d->batch > (1 << 30))
+            return fail(LA_ERR_INVALID_ARG, "batch = %d", d->batch);
+        P->N = d->batch;
+        return LA_OK;
+    }
+    if (d->batch != 1)
+        return fail(LA_ERR_INVALID_ARG,
+                    "the batch size is expected to be 1 rather than %d when using cu_seqlens",
+                    d->batch);
+    if (d->num_seqs < 0 || d->num_seqs > (1 << 30))
+        return fail(LA_ERR_INVALID_ARG, "num_seqs = %d", d->num_seqs);
+    P->N = d->num_seqs;
+    std::vector<int32_t> copy;
+    if (!cu_host) {
+        copy.resize((size_t)P->N + 1);
+        cudaError_t e = cudaMemcpyAsync(copy.data(), cu, sizeof(int32_t) * copy.size(),
+                                        cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "copying cu_seqlens to the host");
+        cu_host = copy.data();
+    }
+    if (cu_host[0] != 0)
+        return fail(LA_ERR_INVALID_ARG, "cu_seqlens[0] = %d, expected 0", cu_host[0]);
+    for (int n = 0; n < P->N; ++n)
+        if (cu_host[n + 1] < cu_host[n])
+            return fail(LA_ERR_INVALID_ARG, "cu_seqlens decreases at %d (%d -> %d)", n,
+                        cu_host[n], cu_host[n + 1]);
+    if (cu_host[P->N] != d->seq_len)
+        return fail(LA_ERR_INVALID_ARG, "cu_seqlens[%d] = %d but seq_len = %d", P->N,
+                    cu_host[P->N], d->seq_len);
+    return LA_OK;
+}
+
+bool has_tokens(const Problem &P) { return (int64_t)P.B * P.T > 0; }
+bool has_states(const Problem &P) { return (int64_t)P.N * P.H > 0; }
+
+la_status need(const void *p, const char *name)
+{
+    return p ? LA_OK : fail(LA_ERR_INVALID_ARG, "%s is NULL", name);
+}
+
+la::Tok tok(const void *p, const int64_t *st) { return la::Tok{p, st[0], st[1], st[2]}; }
+la::TokOut tok_out(void *p, const int64_t *st) { return la::TokOut{p, st[0], st[1], st[2]}; }
+
+la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, const float *g,
+                        float scale, int32_t reverse)
+{
+    la::SweepArgs a{};
+    a.B = P.B;
+    a.T = P.T;
+    a.H = P.H;
+    a.N = P.N;
+    a.cu = cu;
+    a.g = g;
+    a.scale = scale;
+    a.reverse = reverse ? 1 : 0;
+    a.bf16 = dtype == LA_DTYPE_BF16;
+    return a;
+}
+
+la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
+{
+    cudaError_t e = la::tc_forward_supported(a) ? la::tc_forward_sweep(a, s)
+                                                : la::simt_forward_sweep(a, s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "forward-type sweep launch");
+}
+
+la_status run_backward_type(const la::SweepArgs &a, cudaStream_t s)
+{
+    cudaError_t e = la::simt_backward_sweep(a, s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "backward-type sweep launch");
+}
+
+la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *k, const void *v,
+                 const void *d_o, const float *g_gamma, float scale, const float *init,
+                 int32_t reverse, const int32_t *cu, void *dq, cudaStream_t s)
+{
+    // dq = forward-type sweep with (q, k, v) := (do, v, k); the state is S^T (E x D).
+    la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse);
+    a.D = P.E;
+    a.E = P.D;
+    a.q = tok(d_o, d->v_strides);
+    a.k = tok(v, d->v_strides);
+    a.v = tok(k, d->qk_strides);
+    a.out = tok_out(dq, d->qk_strides);
+    a.s_in = la::StateIn{init, 1, P.E};
+    a.s_out = la::StateOut{nullptr, 0, 0};
+    return run_forward_type(a, s);
+}
+
+la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void *q,
+                   const void *k, const void *v, const void *d_o, const float *g_gamma,
+                   float scale, const float *dfinal, int32_t reverse, const int32_t *cu,
+                   void *dk, void *dv, float *dinit, cudaStream_t s)
+{
+    la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse);
+    // dv: (q, k, w) as given, G = dL/dS (D x E)
+    a.D = P.D;
+    a.E = P.E;
+    a.q = tok(q, d->qk_strides);
+    a.k = tok(k, d->qk_strides);
+    a.v = tok(d_o, d->v_strides);
+    a.out = tok_out(dv, d->v_strides);
+    a.s_in = la::StateIn{dfinal, P.E, 1};
+    a.s_out = la::StateOut{dinit, P.E, 1};
+    la_status st = run_backward_type(a, s);
+    if (st != LA_OK)
+        return st;
+    // dk: (q, k, w) := (do, v, q), G^T (E x D)
+    a.D = P.E;
+    a.E = P.D;
+    a.q = tok(d_o, d->v_strides);
+    a.k = tok(v, d->v_strides);
+    a.v = tok(q, d->qk_strides);
+    a.out = tok_out(dk, d->qk_strides);
+    a.s_in = la::StateIn{dfinal, 1, P.E};
+    a.s_out = la::StateOut{nullptr, 0, 0};
+    return run_backward_type(a, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *k, const void *v,
+                 const float *g_gamma, float scale, const float *initial_state, int32_t reverse,
+                 const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, void *o,
+                 float *final_state, void *stream)
+{
+    g_msg.clear();
+    cudaStream_t s = (cudaStream_t)stream;
+    Problem P;
+    la_status st = check_dims(dims, dtype, cu_seqlens, cu_seqlens_host, s, &P);
+    if (st != LA_OK)
+        return st;
+    if (has_tokens(P)) {
+        if ((st = need(q, "q")) || (st = need(k, "k")) || (st = need(v, "v")) ||
+            (st = need(o, "o")))
+            return st;
+    }
+    if (!has_states(P))
+        return LA_OK;
+    if ((st = need(g_gamma, "g_gamma")))
+        return st;
+    la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
+    a.D = P.D;
+    a.E = P.E;
+    a.q = tok(q, dims->qk_strides);
+    a.k = tok(k, dims->qk_strides);
+    a.v = tok(v, dims->v_strides);
+    a.out = tok_out(o, dims->v_strides);
+    a.s_in = la::StateIn{initial_state, P.E, 1};
+    a.s_out = la::StateOut{final_state, P.E, 1};
+    return run_forward_type(a, s);
+}
+
+la_status la_bwd_dq(const la_dims *dims, int32_t dtype, const void *q, const void *k,
+                    const void *v, const void *d_o, const float *g_gamma, float scale,
+                    const float *initial_state, int32_t reverse, const int32_t *cu_seqlens,
+                    const int32_t *cu_seqlens_host, void *dq, void *stream)
+{
+    (void)q;
+    g_msg.clear();
+    cudaStream_t s = (cudaStream_t)stream;
+    Problem P;
+    la_status st = check_dims(dims, dtype, cu_seqlens, cu_seqlens_host, s, &P);
+    if (st != LA_OK)
+        return st;
+    if (has_tokens(P)) {
+        if ((st = need(k, "k")) || (st = need(v, "v")) || (st = need(d_o, "d_o")) ||
+            (st = need(dq, "dq")))
+            return st;
+    }
+    if (!has_states(P))
+        return LA_OK;
+    if ((st = need(g_gamma, "g_gamma")))
+        return st;
+    return bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens,
+                  dq, s);
+}
+
+la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype, const void *q, const void *k,
+                      const void *v, const void *d_o, const float *g_gamma, float scale,
+                      const float *d_final_state, int32_t reverse, const int32_t *cu_seqlens,
+                      const int32_t *cu_seqlens_host, void *dk, void *dv,
+                      float *d_initial_state, void *stream)
+{
+    g_msg.clear();
+    cudaStream_t s = (cudaStream_t)stream;
+    Problem P;
+    la_status st = check_dims(dims, dtype, cu_seqlens, cu_seqlens_host, s, &P);
+    if (st != LA_OK)
+        return st;
+    if (has_tokens(P)) {
+        if ((st = need(q, "q")) || (st = need(k, "k")) || (st = need(v, "v")) ||
+            (st = need(d_o, "d_o")) || (st = need(dk, "dk")) || (st = need(dv, "dv")))
+            return st;
+    }
+    if (!has_states(P))
+        return LA_OK;
+    if ((st = need(g_gamma, "g_gamma")))
+        return st;
+    return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
+                    cu_seqlens, dk, dv, d_initial_state, s);
+}
+
+la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k, const void *v,
+                 const void *d_o, const float *g_gamma, float scale, const float *initial_state,
+                 const float *d_final_state, int32_t reverse, const int32_t *cu_seqlens,
+                 const int32_t *cu_seqlens_host, void *dq, void *dk, void *dv,
+                 float *d_initial_state, void *stream)
+{
+    g_msg.clear();
+    cudaStream_t s = (cudaStream_t)stream;
+    Problem P;
+    la_status st = check_dims(dims, dtype, cu_seqlens, cu_seqlens_host, s, &P);
+    if (st != LA_OK)
+        return st;
+    if (has_tokens(P)) {
+        if ((st = need(q, "q")) || (st = need(k, "k")) || (st = need(v, "v")) ||
+            (st = need(d_o, "d_o")) || (st = need(dq, "dq")) || (st = need(dk, "dk")) ||
+            (st = need(dv, "dv")))
+            return st;
+    }
+    if (!has_states(P))
+        return LA_OK;
+    if ((st = need(g_gamma, "g_gamma")))
+        return st;
+    st = bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens, dq,
+                s);
+    if (st != LA_OK)
+        return st;
+    return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
+                    cu_seqlens, dk, dv, d_initial_state, s);
+}
+
+la_status la_get_device_error(void *stream)
+{
+    g_msg.clear();
+    int err = 0;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = la::tc_read_and_clear_error((cudaStream_t)stream, &err);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "la_get_device_error");
+    if (err)
+        return fail(LA_ERR_TIMEOUT, "an on-device wait ran out (code %d)", err);
+    return LA_OK;
+}
+
+const char *la_strerror(int32_t status)
+{
+    switch (status) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID_ARG: return "invalid argument";
+    case LA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LA_ERR_CUDA: return "CUDA error";
+    case LA_ERR_TIMEOUT: return "on-device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+const char *la_last_error(void) { return g_msg.c_str(); }
+
+int32_t la_kernel_family(const la_dims *dims, int32_t dtype)
+{
+    Problem P;
+    std::string keep = g_msg;
+    // The packed table does not change the kernel family.
+    la_status st = check_dims(dims, dtype, nullptr, nullptr, nullptr, &P);
+    g_msg = keep;
+    if (st != LA_OK)
+        return -1;
+    la::SweepArgs a = base_args(P, dtype, nullptr, nullptr, 1.f, 0);
+    a.D = P.D;
+    a.E = P.E;
+    a.q = tok(nullptr, dims->qk_strides);
+    a.k = tok(nullptr, dims->qk_strides);
+    a.v = tok(nullptr, dims->v_strides);
+    a.out = tok_out(nullptr, dims->v_strides);
+    return la::tc_forward_supported(a) ? 1 : 0;
+}
+
+uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int32_t la_version(void) { return (0 << 16) | 1; }
+
+}  // extern "C"

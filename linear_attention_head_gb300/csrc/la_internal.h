@@ -1,0 +1,76 @@
+// la_internal.h -- kernel-launch interface shared by the translation units of
+// the library (not part of the public ABI; include/la.h is that).
+//
+// Two kernel shapes cover the whole method:
+//
+//  * the "forward-type" sweep: per (sequence, head), chunks in processing order,
+//        out_i = sum_{p(j)<=p(i)} s*gamma^(p(i)-p(j)) (q_i . k_j) v_j
+//                + s*gamma^(p(i)+1) q_i^T S_in
+//        S_out = gamma^Lc S_in + sum_j gamma^(Lc-1-p(j)) k_j v_j^T
+//    (p = position in processing order inside the chunk, Lc = chunk length).
+//    It is the forward pass, and, with q := do, k := v, v := k and the state
+//    transposed, the dq half of the backward pass.
+//
+//  * the "backward-type" sweep: chunks against processing order, carrying
+//    G = dL/dS,
+//        out_j = sum_{p(i)>=p(j)} s*gamma^(p(i)-p(j)) (q_i . k_j) w_i
+//                + gamma^(Lc-1-p(j)) G_in^T k_j
+//        G_out = gamma^Lc G_in + s * sum_i gamma^(p(i)+1) q_i w_i^T
+//    (w = do).  It is the dv half of the backward pass, and, with q := do,
+//    k := v, w := q and G transposed, the dk half.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace la {
+
+// A token tensor: element (row, token, head, c) lives at
+// p + row*sb + token*st + head*sh + c   (elements of the token dtype).
+struct Tok {
+    const void *p;
+    int64_t sb, st, sh;
+};
+struct TokOut {
+    void *p;
+    int64_t sb, st, sh;
+};
+// A state tensor slice: element (a, b) of (sequence n, head h) lives at
+// p + (n*H + h)*D*E + a*rs + b*cs   (fp32).  Transposed views swap rs/cs.
+struct StateIn {
+    const float *p;
+    int64_t rs, cs;
+};
+struct StateOut {
+    float *p;
+    int64_t rs, cs;
+};
+
+struct SweepArgs {
+    int B, T, H, D, E, N;     // D: width of q and k; E: width of v (w) and out
+    const int32_t *cu;        // device [N+1] or nullptr (dense: N == B rows of T)
+    const float *g;           // [H] log-decay
+    float scale;
+    int reverse;
+    int bf16;                 // token dtype: 1 bf16, 0 fp32
+    Tok q, k, v;              // forward-type: q, k, v; backward-type: q, k, w
+    TokOut out;               // forward-type: o (or dq); backward-type: dv (or dk)
+    StateIn s_in;             // forward-type: initial state; backward-type: dL/dfinal
+    StateOut s_out;           // forward-type: final state; backward-type: dL/dinitial
+};
+
+// Host-side count of enqueued kernels (la_launch_count).
+void note_launch();
+
+// CUDA-core kernels: any D, E in 1..256, bf16 or fp32, every flag.
+cudaError_t simt_forward_sweep(const SweepArgs &a, cudaStream_t s);
+cudaError_t simt_backward_sweep(const SweepArgs &a, cudaStream_t s);
+
+// Tensor-core (tcgen05) kernels for bf16; eligibility is decided by the host.
+bool tc_forward_supported(const SweepArgs &a);
+cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s);
+
+// Device error word of the tensor-core kernels (bounded waits that ran out).
+cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err);
+
+}  // namespace la

@@ -1,0 +1,151 @@
+"""Host-only checks of the C ABI (no GPU, no kernel launches).
+
+* the library loads and exports every function include/la.h declares;
+* the ctypes prototypes cover exactly those functions;
+* every validation failure returns its status before anything touches CUDA
+  (these calls would otherwise need a device), and la_last_error explains it;
+* la_kernel_family and la_strerror are pure host functions.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import linear_attention_head_gb300 as la
+from linear_attention_head_gb300 import _native as N
+from linear_attention_head_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "la.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return N.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("la_fwd", "la_bwd", "la_bwd_dq", "la_bwd_dkdv", "la_strerror",
+                 "la_last_error", "la_get_device_error", "la_kernel_family", "la_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", libbuild.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s+(la_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_prototypes_match_header():
+    assert sorted(N.PROTOTYPES) == declared_functions()
+
+
+def test_dims_struct_layout():
+    # int32 x 6 then two int64[3]: 24 + 48 bytes, no padding
+    assert ctypes.sizeof(N.LaDims) == 72
+    assert N.LaDims.qk_strides.offset == 24
+    assert N.LaDims.v_strides.offset == 48
+
+
+def test_strerror_and_version(lib):
+    assert N.strerror(0) == "ok"
+    assert "invalid" in N.strerror(1)
+    assert N.strerror(99) == "unknown status"
+    assert lib.la_version() >= 1
+
+
+def _dims(B=2, T=16, H=2, D=64, E=64, N_=0, layout="bthd"):
+    d = N.LaDims()
+    d.batch, d.seq_len, d.heads, d.dim_qk, d.dim_v, d.num_seqs = B, T, H, D, E, N_
+    qs = (T * H * D, H * D, D) if layout == "bthd" else (H * T * D, D, T * D)
+    vs = (T * H * E, H * E, E) if layout == "bthd" else (H * T * E, E, T * E)
+    for i in range(3):
+        d.qk_strides[i], d.v_strides[i] = qs[i], vs[i]
+    return d
+
+
+FAKE = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
+
+
+def _fwd(lib, dims, dtype=0, cu=None, cu_host=None, q=FAKE, g=FAKE, o=FAKE):
+    return lib.la_fwd(ctypes.byref(dims) if dims is not None else None, dtype, q, FAKE, FAKE, g,
+                      1.0, None, 0, cu, cu_host, o, None, None)
+
+
+def test_validation_errors_return_before_any_launch(lib):
+    assert _fwd(lib, None) == N.LA_ERR_INVALID_ARG
+    assert "dims" in N.last_error()
+    assert _fwd(lib, _dims(), dtype=7) == N.LA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(B=-1)) == N.LA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(H=0)) == N.LA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(D=0)) == N.LA_ERR_UNSUPPORTED
+    assert _fwd(lib, _dims(E=300)) == N.LA_ERR_UNSUPPORTED
+    assert _fwd(lib, _dims(), q=None) == N.LA_ERR_INVALID_ARG
+    assert "q is NULL" in N.last_error()
+    assert _fwd(lib, _dims(), o=None) == N.LA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(), g=None) == N.LA_ERR_INVALID_ARG
+    d = _dims()
+    d.qk_strides[1] = -1
+    assert _fwd(lib, d) == N.LA_ERR_INVALID_ARG
+
+
+def _cu(vals):
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def test_packed_sequence_table_is_validated_on_the_host(lib):
+    good, gp = _cu([0, 5, 5, 16])
+    # batch must be 1 with cu_seqlens (lightning_attn docstring, Raises)
+    assert _fwd(lib, _dims(B=2, N_=3), cu=FAKE, cu_host=gp) == N.LA_ERR_INVALID_ARG
+    assert "batch size is expected to be 1" in N.last_error()
+    bad0, b0 = _cu([1, 5, 5, 16])
+    assert _fwd(lib, _dims(B=1, N_=3), cu=FAKE, cu_host=b0) == N.LA_ERR_INVALID_ARG
+    dec, dp = _cu([0, 6, 5, 16])
+    assert _fwd(lib, _dims(B=1, N_=3), cu=FAKE, cu_host=dp) == N.LA_ERR_INVALID_ARG
+    assert "decreases" in N.last_error()
+    last, lp = _cu([0, 5, 5, 15])
+    assert _fwd(lib, _dims(B=1, N_=3), cu=FAKE, cu_host=lp) == N.LA_ERR_INVALID_ARG
+    assert _fwd(lib, _dims(B=1, N_=-1), cu=FAKE, cu_host=gp) == N.LA_ERR_INVALID_ARG
+    # a host table without the device table is an error too
+    assert _fwd(lib, _dims(B=1, N_=3), cu=None, cu_host=gp) == N.LA_ERR_INVALID_ARG
+
+
+def test_backward_entry_points_validate(lib):
+    d = _dims()
+    st = lib.la_bwd(ctypes.byref(d), 0, FAKE, FAKE, FAKE, None, FAKE, 1.0, None, None, 0, None,
+                    None, FAKE, FAKE, FAKE, None, None)
+    assert st == N.LA_ERR_INVALID_ARG and "d_o" in N.last_error()
+    st = lib.la_bwd_dq(ctypes.byref(d), 0, None, FAKE, FAKE, FAKE, FAKE, 1.0, None, 0, None,
+                       None, None, None)
+    assert st == N.LA_ERR_INVALID_ARG and "dq" in N.last_error()
+    st = lib.la_bwd_dkdv(ctypes.byref(d), 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, 0, None,
+                         None, FAKE, None, None, None)
+    assert st == N.LA_ERR_INVALID_ARG and "dv" in N.last_error()
+
+
+def test_empty_problems_enqueue_nothing(lib):
+    # zero batch rows or zero packed sequences: nothing to compute, success
+    assert _fwd(lib, _dims(B=0), q=None, o=None) == N.LA_OK
+    empty, ep = _cu([0])
+    assert _fwd(lib, _dims(B=1, T=0, N_=0), cu=FAKE, cu_host=ep, q=None, o=None) == N.LA_OK
+
+
+def test_kernel_family_is_host_only():
+    assert la.kernel_family(4, 1024, 32, 128, 128) in (0, 1)
+    assert la.kernel_family(1, 256, 2, 32, 32, dtype="f32") == 0
+    assert la.kernel_family(1, 256, 2, 0, 32) == -1

@@ -1,0 +1,169 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+the same seeded inputs, element by element, at the tolerances of the workload
+definitions: max relative error <= 2e-2 for bf16 token tensors and <= 1e-4 for
+fp32 (per (sequence, head) slice, tests/parity.py), final and initial-state
+gradients included.  Full-size workloads compare a sample of heads that the
+oracle computes on its own; everything else compares every element.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_head_gb300 as la
+import workloads as W
+from parity import TOL, compare, gpu_run, oracle_run, take_heads, take_out
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_fp32_forward():
+    w = W.tiny_fp32()
+    x = W.make_inputs(w, seed=0)
+    got = gpu_run(x, backward=False)
+    compare(got, oracle_run(x, backward=False), TOL[torch.float32], label=w.name)
+
+
+@pytest.mark.parametrize("reverse", [False, True])
+def test_small_bf16_fwd_bwd(reverse):
+    w = W.small_bf16()
+    x = W.make_inputs(w, seed=0)
+    got = gpu_run(x, reverse)
+    compare(got, oracle_run(x, reverse), TOL[torch.bfloat16], label=w.name)
+
+
+@pytest.mark.parametrize("n", [512, 2048])
+def test_sweep_shape_full_compare(n):
+    w = W.sweep_bf16(n)
+    x = W.make_inputs(w, seed=0)
+    got = gpu_run(x)
+    heads = [0, 13, 31]
+    compare(take_out(got, heads), oracle_run(take_heads(x, heads)), TOL[torch.bfloat16],
+            label=w.name)
+
+
+@pytest.mark.parametrize("n", [8192, 32768])
+def test_sweep_shape_sampled(n):
+    w = W.sweep_bf16(n)
+    x = W.make_inputs(w, seed=0)
+    got = gpu_run(x)
+    heads, rows = [0, 31], [0, 3]
+    compare(take_out(got, heads, rows), oracle_run(take_heads(x, heads, rows)),
+            TOL[torch.bfloat16], label=w.name)
+
+
+def test_d192_fwd_bwd():
+    w = W.d192_bf16()
+    x = W.make_inputs(w, seed=0)
+    got = gpu_run(x)
+    heads = [0, 11]
+    compare(take_out(got, heads), oracle_run(take_heads(x, heads)), TOL[torch.bfloat16],
+            label=w.name)
+
+
+@pytest.mark.parametrize("reverse", [False, True])
+def test_varlen_with_states(reverse):
+    w = W.varlen_bf16(seed=0)
+    x = W.make_inputs(w, seed=0)
+    got = gpu_run(x, reverse)
+    heads = [0, 7, 15]
+    compare(take_out(got, heads), oracle_run(take_heads(x, heads), reverse),
+            TOL[torch.bfloat16], cu=x["cu_seqlens"], label=w.name)
+
+
+# ---- edge cases -------------------------------------------------------------
+
+def _custom(B, T, H, D, E, dtype, seqlens=None, init=0.0, dfin=0.0, g=None, scale=None):
+    g = W.alibi_g_gamma(H) if g is None else g
+    return W.Workload("custom", B, T if seqlens is None else sum(seqlens), H, D, E, dtype, g,
+                      scale if scale is not None else 1.0 / math.sqrt(D), seqlens=seqlens,
+                      init_std=init, dfinal_std=dfin)
+
+
+@pytest.mark.parametrize("T", [1, 5, 31, 32, 33, 127, 128, 129, 300])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ragged_lengths(T, dtype):
+    w = _custom(2, T, 3, 64, 64, dtype, init=0.3, dfin=0.3,
+                g=torch.tensor([0.0, -0.05, -1.0]))
+    x = W.make_inputs(w, seed=T)
+    for reverse in (False, True):
+        compare(gpu_run(x, reverse), oracle_run(x, reverse), TOL[dtype],
+                label="T=%d rev=%d" % (T, reverse))
+
+
+@pytest.mark.parametrize("D,E", [(32, 32), (64, 128), (128, 64), (128, 128), (192, 192),
+                                 (256, 256), (16, 48), (80, 96), (1, 1)])
+def test_head_dims(D, E):
+    w = _custom(1, 200, 2, D, E, torch.bfloat16, init=0.2, dfin=0.2)
+    x = W.make_inputs(w, seed=D * 1000 + E)
+    compare(gpu_run(x), oracle_run(x), TOL[torch.bfloat16], label="D=%d E=%d" % (D, E))
+
+
+def test_packed_with_empty_and_short_sequences():
+    lens = [0, 1, 130, 0, 64, 257, 3]
+    for dtype in (torch.bfloat16, torch.float32):
+        w = _custom(1, 0, 4, 64, 64, dtype, seqlens=lens, init=0.1, dfin=0.1)
+        x = W.make_inputs(w, seed=5)
+        for reverse in (False, True):
+            got = gpu_run(x, reverse)
+            ref = oracle_run(x, reverse)
+            compare(got, ref, TOL[dtype], cu=x["cu_seqlens"], label="packed rev=%d" % reverse)
+            # zero-length sequences pass their states through unchanged
+            for n in (0, 3):
+                assert torch.equal(got["final_state"][n], x["initial_state"][n])
+                assert torch.equal(got["d_initial_state"][n], x["d_final_state"][n])
+
+
+def test_head_major_layout_and_lightning2_call():
+    # OpenNLPLab README: q, k, v as (b, h, n, d), slopes s, o = lightning_attn_func(q, k, v, s)
+    b, h, n, d, e = 2, 4, 300, 64, 64
+    gen = torch.Generator().manual_seed(3)
+    q = torch.randn((b, h, n, d), generator=gen).bfloat16()
+    k = torch.randn((b, h, n, d), generator=gen).bfloat16()
+    v = torch.randn((b, h, n, e), generator=gen).bfloat16()
+    s = -W.alibi_g_gamma(h)
+    o = la.lightning_attn_func(q.cuda(), k.cuda(), v.cuda(), s.cuda())
+    ref, _ = oracle_run(dict(q=q.transpose(1, 2), k=k.transpose(1, 2), v=v.transpose(1, 2),
+                             g_gamma=-s, scale=1.0, initial_state=None, cu_seqlens=None),
+                        backward=False).values()
+    compare(dict(o=o.transpose(1, 2).cpu()), dict(o=ref), TOL[torch.bfloat16],
+            label="head-major")
+
+
+def test_autograd_matches_la_bwd():
+    w = _custom(1, 150, 2, 64, 64, torch.bfloat16, init=0.1, dfin=0.0)
+    x = W.make_inputs(w, seed=9)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    q, k, v = (d[n].clone().requires_grad_() for n in ("q", "k", "v"))
+    init = d["initial_state"].clone().requires_grad_()
+    o, fin = la.recurrent(q, k, v, g_gamma=d["g_gamma"], softmax_scale=w.scale,
+                          initial_state=init)
+    (o.float() * d["do"].float()).sum().backward()
+    ref = oracle_run(dict(x, d_final_state=None))
+    got = dict(o=o.detach().cpu(), final_state=fin.detach().cpu(), dq=q.grad.cpu(),
+               dk=k.grad.cpu(), dv=v.grad.cpu(), d_initial_state=init.grad.cpu())
+    compare(got, ref, TOL[torch.bfloat16], label="autograd")
+
+
+def test_lightning_attn_docstring_example_closed_form():
+    # ejkernel lightning_attn example: ones (2, 2048, 8, 64), layer 5 of 12
+    ones = torch.ones((2, 2048, 8, 64), dtype=torch.bfloat16, device="cuda")
+    o, fin = la.lightning_attn(ones, ones, ones, layer_idx=5, num_layers=12)
+    g = la.lightning_g_gamma(8, 5, 12).double().numpy()
+    t = np.arange(2048)
+    for h in range(8):
+        gam = math.exp(g[h])
+        ref = (64 ** -0.5) * 64 * ((t + 1) if gam == 1 else (1 - gam ** (t + 1)) / (1 - gam))
+        got = o[0, :, h, 0].float().cpu().double().numpy()
+        assert np.max(np.abs(got - ref)) / np.max(ref) < 2e-2
+
+
+def test_empty_batch_and_zero_length():
+    q = torch.zeros((0, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    o, fin = la.la_fwd(q, q, q, torch.zeros(2))
+    assert o.shape == q.shape and fin.shape == (0, 2, 64, 64)
+    q = torch.zeros((3, 0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    init = torch.randn((3, 2, 64, 64), device="cuda")
+    o, fin = la.la_fwd(q, q, q, torch.full((2,), -0.5), initial_state=init)
+    assert torch.equal(fin, init)
