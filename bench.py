@@ -321,7 +321,7 @@ def _oracle_step(w, q, k, v, do, g, cores):
     oracle.backward(q, k, v, g, w.scale, do, threads=cores)
 
 
-def cpu_baseline(n, pairs=None, n_sample=8192):
+def cpu_baseline(n, pairs=None, n_sample=32768):
     """The fp64 oracle as it stands, fwd+bwd, timed on the host cores on a bounded sample;
     reported as the full workload's tokens/s."""
     import oracle

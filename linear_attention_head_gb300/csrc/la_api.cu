@@ -145,8 +145,12 @@ la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, cons
 
 la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 {
-    cudaError_t e = la::tc_forward_supported(a) ? la::tc_forward_sweep(a, s)
-                                                : la::simt_forward_sweep(a, s);
+    cudaError_t e = cudaErrorNotSupported;
+    if (la::tc_forward_supported(a))
+        e = la::tc_forward_sweep(a, s);
+    // cudaErrorNotSupported: the tensor maps could not be encoded for this layout
+    if (e == cudaErrorNotSupported)
+        e = la::simt_forward_sweep(a, s);
     return e == cudaSuccess ? LA_OK : cuda_fail(e, "forward-type sweep launch");
 }
 

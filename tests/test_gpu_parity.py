@@ -81,10 +81,11 @@ def _custom(B, T, H, D, E, dtype, seqlens=None, init=0.0, dfin=0.0, g=None, scal
                       init_std=init, dfinal_std=dfin)
 
 
-@pytest.mark.parametrize("T", [1, 5, 31, 32, 33, 127, 128, 129, 300])
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_ragged_lengths(T, dtype):
-    w = _custom(2, T, 3, 64, 64, dtype, init=0.3, dfin=0.3,
+@pytest.mark.parametrize("T", [1, 5, 31, 32, 33, 127, 128, 129, 300, 1000])
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float32, 64),
+                                     (torch.bfloat16, 128)])
+def test_ragged_lengths(T, dtype, D):
+    w = _custom(2, T, 3, D, D, dtype, init=0.3, dfin=0.3,
                 g=torch.tensor([0.0, -0.05, -1.0]))
     x = W.make_inputs(w, seed=T)
     for reverse in (False, True):
@@ -100,10 +101,12 @@ def test_head_dims(D, E):
     compare(gpu_run(x), oracle_run(x), TOL[torch.bfloat16], label="D=%d E=%d" % (D, E))
 
 
-def test_packed_with_empty_and_short_sequences():
-    lens = [0, 1, 130, 0, 64, 257, 3]
-    for dtype in (torch.bfloat16, torch.float32):
-        w = _custom(1, 0, 4, 64, 64, dtype, seqlens=lens, init=0.1, dfin=0.1)
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 64), (torch.float32, 64),
+                                     (torch.bfloat16, 128)])
+def test_packed_with_empty_and_short_sequences(dtype, D):
+    lens = [0, 1, 130, 0, 64, 257, 3, 128, 129]
+    if True:
+        w = _custom(1, 0, 4, D, D, dtype, seqlens=lens, init=0.1, dfin=0.1)
         x = W.make_inputs(w, seed=5)
         for reverse in (False, True):
             got = gpu_run(x, reverse)
@@ -167,3 +170,40 @@ def test_empty_batch_and_zero_length():
     init = torch.randn((3, 2, 64, 64), device="cuda")
     o, fin = la.la_fwd(q, q, q, torch.full((2,), -0.5), initial_state=init)
     assert torch.equal(fin, init)
+
+
+def test_tensor_core_path_is_selected_for_the_benchmark_shape():
+    # bf16, d = e = 128, dense token-major: the tcgen05 kernels, not the CUDA-core ones
+    assert la.kernel_family(4, 32768, 32, 128, 128) == 1
+    assert la.kernel_family(1, 4096, 16, 128, 64) == 1
+    assert la.kernel_family(1, 256, 2, 32, 32, dtype=torch.float32) == 0
+
+
+def test_unaligned_layout_falls_back_and_matches():
+    # a channel-contiguous layout whose token stride is not a multiple of 16 bytes
+    # cannot be described by TMA; the CUDA-core kernel takes it and must agree.
+    w = _custom(2, 200, 3, 128, 128, torch.bfloat16, init=0.2, dfin=0.2)
+    x = W.make_inputs(w, seed=21)
+    big = {}
+    for n in ("q", "k", "v", "do"):
+        t = x[n]
+        pad = torch.zeros(t.shape[:2] + (t.shape[2] * t.shape[3] + 4,), dtype=t.dtype)
+        pad[..., : t.shape[2] * t.shape[3]] = t.reshape(t.shape[0], t.shape[1], -1)
+        big[n] = pad.cuda()[..., : t.shape[2] * t.shape[3]].reshape(t.shape)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o, fin = la.la_fwd(big["q"], big["k"], big["v"], d["g_gamma"], w.scale, d["initial_state"])
+    dq, dk, dv, dinit = la.la_bwd(big["q"], big["k"], big["v"], big["do"], d["g_gamma"], w.scale,
+                                  d["initial_state"], d["d_final_state"])
+    got = dict(o=o.cpu(), final_state=fin.cpu(), dq=dq.cpu(), dk=dk.cpu(), dv=dv.cpu(),
+               d_initial_state=dinit.cpu())
+    compare(got, oracle_run(x), TOL[torch.bfloat16], label="unaligned")
+
+
+def test_repeated_calls_are_deterministic_and_report_no_timeout():
+    w = W.sweep_bf16(1024)
+    x = W.make_inputs(w, seed=4)
+    a = gpu_run(x)
+    b = gpu_run(x)
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+    la.get_device_error()
