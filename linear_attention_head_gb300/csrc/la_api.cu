@@ -146,7 +146,7 @@ la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, cons
 la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    if (la::tc_forward_supported(a))
+    if (la::tc_sweep_supported(a))
         e = la::tc_forward_sweep(a, s);
     // cudaErrorNotSupported: the tensor maps could not be encoded for this layout
     if (e == cudaErrorNotSupported)
@@ -156,7 +156,11 @@ la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 
 la_status run_backward_type(const la::SweepArgs &a, cudaStream_t s)
 {
-    cudaError_t e = la::simt_backward_sweep(a, s);
+    cudaError_t e = cudaErrorNotSupported;
+    if (la::tc_sweep_supported(a))
+        e = la::tc_backward_sweep(a, s);
+    if (e == cudaErrorNotSupported)
+        e = la::simt_backward_sweep(a, s);
     return e == cudaSuccess ? LA_OK : cuda_fail(e, "backward-type sweep launch");
 }
 
@@ -367,7 +371,7 @@ int32_t la_kernel_family(const la_dims *dims, int32_t dtype)
     a.k = tok(nullptr, dims->qk_strides);
     a.v = tok(nullptr, dims->v_strides);
     a.out = tok_out(nullptr, dims->v_strides);
-    return la::tc_forward_supported(a) ? 1 : 0;
+    return la::tc_sweep_supported(a) ? 1 : 0;
 }
 
 uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

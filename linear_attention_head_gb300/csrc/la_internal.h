@@ -66,9 +66,11 @@ void note_launch();
 cudaError_t simt_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t simt_backward_sweep(const SweepArgs &a, cudaStream_t s);
 
-// Tensor-core (tcgen05) kernels for bf16; eligibility is decided by the host.
-bool tc_forward_supported(const SweepArgs &a);
+// Tensor-core (tcgen05) kernels for bf16, both sweep shapes; eligibility
+// (dtype, widths, 16-byte alignment) is the same for both.
+bool tc_sweep_supported(const SweepArgs &a);
 cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s);
+cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s);
 
 // Device error word of the tensor-core kernels (bounded waits that ran out).
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err);

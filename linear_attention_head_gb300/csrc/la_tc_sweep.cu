@@ -1,4 +1,4 @@
-// la_tc_fwd.cu -- tensor-core (tcgen05 + TMEM + TMA) forward-type sweep for
+// la_tc_sweep.cu -- tensor-core (tcgen05 + TMEM + TMA) sweeps (both shapes) for
 // bf16 tokens, key width D = 128, value width E in {64, 128}.
 //
 // Chunked form of the decayed recurrence (Lightning Attention-2, as named in
@@ -136,8 +136,8 @@ __device__ __forceinline__ void store_row_sw128(uint8_t *row_base, int row, cons
     }
 }
 
-template <int E>
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_constant__ TcParams P)
+template <int E, bool BWD>
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_constant__ TcParams P)
 {
     using L = TcLayout<E>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_
                 const int s = c % TC_NST;
                 if (c >= TC_NST && !bwait(&empty[s], ((c / TC_NST) - 1) & 1, abort_flag))
                     break;
-                const int cidx = a.reverse ? nc - 1 - c : c;
+                const int cidx = (a.reverse != 0) != BWD ? nc - 1 - c : c;
                 const int t0 = (int)(bos + (int64_t)cidx * TC_C);
                 uint8_t *st = sm + s * L::STAGE;
                 mbar_arrive_expect_tx(&full[s], L::STAGE);
@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_
         const float g = a.g[h];
         const float scale = a.scale;
         const bool rev = a.reverse != 0;
+        const bool flip = rev != BWD;   // mask / chunk order direction
         const bool cols = hh < E / 64;
         for (int m = et; m <= TC_C; m += TC_EPI)
             pw[m] = m == 0 ? 1.f : expf(g * (float)m);
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_
         bool ok = true;
         for (int c = 0; c < nc && ok; ++c) {
             const int s = c % TC_NST;
-            const int cidx = rev ? nc - 1 - c : c;
+            const int cidx = flip ? nc - 1 - c : c;
             const int64_t tc0 = (int64_t)cidx * TC_C;
             const int Lc = (int)(len - tc0 < TC_C ? len - tc0 : TC_C);
 
@@ -337,9 +338,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_
 #pragma unroll
                 for (int jj = 0; jj < 16; jj += 2) {
                     const int j = 64 * hh + 16 * part + jj;
-                    const int d0 = rev ? j - i : i - j, d1 = rev ? d0 + 1 : d0 - 1;
-                    const bool k0 = d0 >= 0 && (rev ? j : i) < Lc;
-                    const bool k1 = d1 >= 0 && (rev ? j + 1 : i) < Lc;
+                    const int d0 = flip ? j - i : i - j, d1 = flip ? d0 + 1 : d0 - 1;
+                    const bool k0 = d0 >= 0 && (flip ? j : i) < Lc;
+                    const bool k1 = d1 >= 0 && (flip ? j + 1 : i) < Lc;
                     const float v0 = k0 ? scale * __uint_as_float(r[jj]) * pw[k0 ? d0 : 0] : 0.f;
                     const float v1 = k1 ? scale * __uint_as_float(r[jj + 1]) * pw[k1 ? d1 : 0] : 0.f;
                     pk[jj / 2] = pack_bf16x2(v0, v1);
@@ -349,7 +350,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_
                 tmem_st8(tm + lane_off + TM_SC + 64 * hh + 8 * part, pk);
             }
             {
-                const float lk = i < Lc ? (rev ? pw[i] : pw[Lc - 1 - i]) : 0.f;
+                // column factor: gamma^(Lc-1-p(i)) forward, gamma^(p(i)+1) backward
+                const float lk = i >= Lc ? 0.f
+                                 : BWD ? (rev ? pw[Lc - i] : pw[i + 1])
+                                       : (rev ? pw[i] : pw[Lc - 1 - i]);
                 uint8_t *krow = sm + s * L::STAGE + L::QB + hh * (TC_C * 128) + i * 128;
 #pragma unroll
                 for (int c16 = 0; c16 < 8; ++c16) {
@@ -367,7 +371,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_
                 break;
             tc_fence_after();
             if (cols) {
-                const float lq = i < Lc ? scale * (rev ? pw[Lc - i] : pw[i + 1]) : 0.f;
+                // row factor: s*gamma^(p(i)+1) forward, gamma^(Lc-1-p(i)) backward
+                const float lq = i >= Lc ? 0.f
+                                 : BWD ? (rev ? pw[i] : pw[Lc - 1 - i])
+                                       : scale * (rev ? pw[Lc - i] : pw[i + 1]);
                 __nv_bfloat16 *orow = obase + (bos + tc0 + i) * a.out.st;
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
@@ -399,13 +406,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_forward_kernel(const __grid_
             tc_fence_after();
             if (cols) {
                 const float gl = pw[Lc];
+                const float ds_scale = BWD ? scale : 1.f;
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
                     uint32_t r[16];
                     tmem_ld16(tm + lane_off + TM_DS + 64 * hh + 16 * part, r);
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
-                        S[16 * part + k] = fmaf(gl, S[16 * part + k], __uint_as_float(r[k]));
+                        S[16 * part + k] = fmaf(gl, S[16 * part + k], ds_scale * __uint_as_float(r[k]));
                 }
                 store_row_sw128(srow, i, S);
                 fence_proxy_async_smem();
@@ -474,15 +482,19 @@ bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int E> cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s)
+// Tile roles: X rows (scores = X Y^T, inter term X S), Y columns (scaled in
+// place for the state update), Z values.  Forward: (X, Y, Z) = (q, k, v);
+// backward: (k, q, w).
+template <int E, bool BWD> cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s)
 {
     TcParams p;
-    if (!make_map(&p.mq, a.q.p, TC_D, a, a.q.sb, a.q.st, a.q.sh) ||
-        !make_map(&p.mk, a.k.p, TC_D, a, a.k.sb, a.k.st, a.k.sh) ||
+    const Tok &x = BWD ? a.k : a.q, &y = BWD ? a.q : a.k;
+    if (!make_map(&p.mq, x.p, TC_D, a, x.sb, x.st, x.sh) ||
+        !make_map(&p.mk, y.p, TC_D, a, y.sb, y.st, y.sh) ||
         !make_map(&p.mv, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh))
         return cudaErrorNotSupported;
     p.a = a;
-    auto kern = tc_forward_kernel<E>;
+    auto kern = tc_sweep_kernel<E, BWD>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            TcLayout<E>::DYN);
     if (err != cudaSuccess)
@@ -494,7 +506,7 @@ template <int E> cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s)
 
 }  // namespace
 
-bool tc_forward_supported(const SweepArgs &a)
+bool tc_sweep_supported(const SweepArgs &a)
 {
     if (!a.bf16 || a.D != TC_D || (a.E != 64 && a.E != 128) || a.T < 1 || a.B < 1)
         return false;
@@ -510,7 +522,14 @@ cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
-    return a.E == 128 ? launch_tc<128>(a, s) : launch_tc<64>(a, s);
+    return a.E == 128 ? launch_tc<128, false>(a, s) : launch_tc<64, false>(a, s);
+}
+
+cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s)
+{
+    if (a.N == 0)
+        return cudaSuccess;
+    return a.E == 128 ? launch_tc<128, true>(a, s) : launch_tc<64, true>(a, s);
 }
 
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err)
