@@ -3,29 +3,40 @@
 //
 // Chunked form of the decayed recurrence (Lightning Attention-2, as named in
 // the OpenNLPLab/lightning-attention README; the recurrence itself is the
-// ejkernel `recurrent` docstring's "core update"), per (sequence, head), chunk
-// of C = 128 tokens with valid length Lc, positions p in processing order:
-//     P      = s * (Q K^T) .* M,  M_ij = gamma^(p(i)-p(j)) if p(j) <= p(i), else 0
-//     O      = P V  +  diag(s * gamma^(p(i)+1)) (Q S_bf16)
-//     S     <- gamma^Lc S + (diag(gamma^(Lc-1-p(j))) K)^T V        (fp32 master)
+// ejkernel `recurrent` docstring's "core update").  Per (sequence, head) and
+// chunk of C = 128 tokens with valid length Lc and positions p(.) in
+// processing order, with three 128-token tiles X, Y, Z:
+//     P   = s * (X Y^T) .* M           M_rc = gamma^|p(r)-p(c)| on one side
+//     O   = P Z + diag(lrow) (X S_bf16)
+//     S  <- gamma^Lc S + (diag(lcol) Y)^T Z                  (fp32, in TMEM)
+//   forward  (X, Y, Z) = (q, k, v):   keep p(c) <= p(r), lrow = s*gamma^(p(r)+1),
+//                                     lcol = gamma^(Lc-1-p(c))
+//   backward (X, Y, Z) = (k, q, do):  keep p(c) >= p(r), lrow = gamma^(Lc-1-p(r)),
+//                                     lcol = s*gamma^(p(c)+1), chunks in
+//                                     reverse processing order (dv; dk swaps
+//                                     the tensors' roles on the host)
 // Every decay factor is gamma^m with m >= 0, so nothing overflows.
 //
-// One CTA per (sequence, head); 10 warps:
-//   warp 0      TMA producer: Q, K, V chunk boxes (128-byte swizzle) into a
-//               2-stage ring
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//   warps 2..9  epilogue: warp w owns TMEM lanes 32*(w%4).. (rows) and column
-//               half (w-2)/4; it turns scores into bf16 P (written back into
-//               TMEM as the A operand of P V), scales its K row by the decay
-//               in place, combines and stores o, and keeps its 64 columns of
-//               the fp32 state S in registers, rewriting the bf16 copy that
-//               the next chunk's Q S reads.
-// TMEM (512 columns): scores / P [0,128), Q S [128,256), P V [256,384),
-// K^T V [384,512).
+// One CTA per (sequence, head); 18 warps:
+//   warp 0        TMA producer: X, Y, Z boxes (128-byte swizzle), 2-stage ring
+//   warp 1        TMEM allocator; one thread issues every tcgen05.mma
+//   warps 2..9    P group: warp w owns TMEM lanes 32*(w%4).. and key half
+//                 (w-2)/4 of the scores; writes bf16 P back into TMEM (the A
+//                 operand of P Z) and scales its Y row in place by lcol
+//   warps 10..13  S group: one thread per state row; turns the state around
+//                 each chunk: S -> bf16 copy (B operand of the next X S) and
+//                 S * gamma^Lc(next) back into TMEM, where the next update
+//                 accumulates
+//   warps 14..17  O group: one thread per token row; o = P Z + lrow * X S
+// TMEM (512 columns): scores/P [0,128), X S [128,256), P Z [256,384),
+// S [384,512) (value columns: E of them).  MMA order per chunk: scores and
+// X S as soon as the tiles land; then, once P is written, the state update
+// and P Z.  A ring stage is held only from landing to that last MMA, which is
+// what bounds the memory pipeline with two 96 KB stages.
 //
 // Every mbarrier wait is bounded (2 s); on expiry the CTA raises a shared
-// abort flag, records LA_ERR_TIMEOUT in a device word, drains its own copies
-// and MMAs, frees TMEM and returns.
+// abort flag and records LA_ERR_TIMEOUT in a device word, drains its own
+// copies and MMAs, frees TMEM and returns.
 
 #include <climits>
 #include <cstdint>
@@ -45,24 +56,26 @@ using namespace sm100;
 
 __device__ int g_tc_error;
 
-constexpr int TC_C = 128;        // tokens per chunk (MMA M and the P V K-extent)
+constexpr int TC_C = 128;        // tokens per chunk (MMA M and the P Z K-extent)
 constexpr int TC_D = 128;        // key width
 constexpr int TC_NST = 2;        // TMA ring stages
-constexpr int TC_THREADS = 320;
-constexpr int TC_EPI = 256;      // epilogue threads
+constexpr int TC_THREADS = 576;  // 18 warps
+constexpr int TC_PG = 256;       // P group threads (warps 2..9)
+constexpr int TC_SG = 128;       // S group threads (warps 10..13)
+constexpr int TC_OG = 128;       // O group threads (warps 14..17)
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;
 constexpr int TC_ERR_TIMEOUT = 4;
-constexpr uint32_t TM_SC = 0, TM_OI = 128, TM_OA = 256, TM_DS = 384, TM_COLS = 512;
+constexpr uint32_t TM_SC = 0, TM_OI = 128, TM_OA = 256, TM_S = 384, TM_COLS = 512;
 
 template <int E> struct TcLayout {
-    static constexpr int QB = TC_C * TC_D * 2;
-    static constexpr int KB = TC_C * TC_D * 2;
-    static constexpr int VB = TC_C * E * 2;
-    static constexpr int STAGE = QB + KB + VB;
+    static constexpr int XB = TC_C * TC_D * 2;
+    static constexpr int YB = TC_C * TC_D * 2;
+    static constexpr int ZB = TC_C * E * 2;
+    static constexpr int STAGE = XB + YB + ZB;
     static constexpr int SOFF = TC_NST * STAGE;       // bf16 copy of S, [E/64][D][64]
     static constexpr int SB = TC_D * E * 2;
     static constexpr int MOFF = SOFF + SB;
-    static constexpr int NBAR = 2 * TC_NST + 7;
+    static constexpr int NBAR = 2 * TC_NST + 12;
     static constexpr int PWOFF = MOFF + NBAR * 8;
     static constexpr int SLOTOFF = PWOFF + (TC_C + 1) * 4;
     static constexpr int ABORTOFF = SLOTOFF + 4;
@@ -71,7 +84,7 @@ template <int E> struct TcLayout {
 };
 
 struct TcParams {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mx, my, mz;
     SweepArgs a;
 };
 
@@ -109,7 +122,7 @@ __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffff
 
 __device__ __forceinline__ void epi_bar_sync()
 {
-    asm volatile("bar.sync 1, %0;" ::"n"(TC_EPI) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(TC_PG + TC_SG + TC_OG) : "memory");
 }
 
 // 16 bytes = 8 bf16 scaled by f, in place.
@@ -122,18 +135,44 @@ __device__ __forceinline__ uint4 scale8(uint4 v, float f)
     return v;
 }
 
-// Writes 64 fp32 values as one 128-byte row of a 128B-swizzled bf16 tile.
-__device__ __forceinline__ void store_row_sw128(uint8_t *row_base, int row, const float *x)
+// One 128-byte row of a 128B-swizzled bf16 tile, scaled in place.
+__device__ __forceinline__ void scale_row_sw128(uint8_t *row_base, int row, float f)
 {
 #pragma unroll
     for (int c16 = 0; c16 < 8; ++c16) {
+        uint4 *p = reinterpret_cast<uint4 *>(row_base + ((c16 ^ (row & 7)) << 4));
+        *p = scale8(*p, f);
+    }
+}
+
+// 64 fp32 (as bits, lo = first 32 columns, hi = next 32) -> one 128-byte
+// row of a 128B-swizzled bf16 tile.
+__device__ __forceinline__ void store_row_sw128(uint8_t *row_base, int row,
+                                                const uint32_t (&lo)[32], const uint32_t (&hi)[32])
+{
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16) {
+        const uint32_t *x = c16 < 4 ? lo : hi;
+        const int o = 8 * (c16 & 3);
         uint4 v;
-        v.x = pack_bf16x2(x[8 * c16 + 0], x[8 * c16 + 1]);
-        v.y = pack_bf16x2(x[8 * c16 + 2], x[8 * c16 + 3]);
-        v.z = pack_bf16x2(x[8 * c16 + 4], x[8 * c16 + 5]);
-        v.w = pack_bf16x2(x[8 * c16 + 6], x[8 * c16 + 7]);
+        v.x = pack_bf16x2(__uint_as_float(x[o + 0]), __uint_as_float(x[o + 1]));
+        v.y = pack_bf16x2(__uint_as_float(x[o + 2]), __uint_as_float(x[o + 3]));
+        v.z = pack_bf16x2(__uint_as_float(x[o + 4]), __uint_as_float(x[o + 5]));
+        v.w = pack_bf16x2(__uint_as_float(x[o + 6]), __uint_as_float(x[o + 7]));
         *reinterpret_cast<uint4 *>(row_base + ((c16 ^ (row & 7)) << 4)) = v;
     }
+}
+
+// 32 fp32 (as bits) -> 32 bf16 at dst (4 x 16-byte stores).
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t (&x)[32])
+{
+#pragma unroll
+    for (int c16 = 0; c16 < 4; ++c16)
+        *reinterpret_cast<uint4 *>(dst + 8 * c16) = make_uint4(
+            pack_bf16x2(__uint_as_float(x[8 * c16 + 0]), __uint_as_float(x[8 * c16 + 1])),
+            pack_bf16x2(__uint_as_float(x[8 * c16 + 2]), __uint_as_float(x[8 * c16 + 3])),
+            pack_bf16x2(__uint_as_float(x[8 * c16 + 4]), __uint_as_float(x[8 * c16 + 5])),
+            pack_bf16x2(__uint_as_float(x[8 * c16 + 6]), __uint_as_float(x[8 * c16 + 7])));
 }
 
 template <int E, bool BWD>
@@ -146,9 +185,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     const SweepArgs &a = P.a;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::MOFF);
     uint64_t *full = bars, *empty = bars + TC_NST;
-    uint64_t *sc_full = bars + 2 * TC_NST, *p_ready = sc_full + 1, *o_full = sc_full + 2,
-             *o_free = sc_full + 3, *ds_full = sc_full + 4, *s_ready = sc_full + 5,
-             *drain = sc_full + 6;
+    uint64_t *sc_full = bars + 2 * TC_NST;   // scores of the chunk are in TMEM
+    uint64_t *pv_done = sc_full + 1;         // P consumed (scores columns free)
+    uint64_t *p_ready = sc_full + 2;         // P written, Y scaled
+    uint64_t *s_ready = sc_full + 3;         // bf16 S written, TMEM S pre-scaled
+    uint64_t *o_free = sc_full + 4;          // both O accumulators read
+    uint64_t *ds_full = sc_full + 5;         // state update (and X S) done
+    uint64_t *o_full = sc_full + 6;          // P Z (and X S) done
+    uint64_t *drain = sc_full + 7;
     float *pw = reinterpret_cast<float *>(sm + L::PWOFF);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::SLOTOFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::ABORTOFF);
@@ -166,6 +210,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         len = a.T;
     }
     const int nc = (int)((len + TC_C - 1) / TC_C);
+    const bool rev = a.reverse != 0;
+    const bool flip = rev != BWD;   // chunk order and mask direction
+    // first token and valid length of the chunk processed c-th
+    auto chunk_t0 = [&](int c) { return (int64_t)(flip ? nc - 1 - c : c) * TC_C; };
+    auto chunk_len = [&](int c) {
+        const int64_t t0 = chunk_t0(c);
+        return (int)(len - t0 < TC_C ? len - t0 : TC_C);
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < TC_NST; ++i) {
@@ -173,11 +225,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             mbar_init(&empty[i], 1);
         }
         mbar_init(sc_full, 1);
-        mbar_init(p_ready, TC_EPI);
-        mbar_init(o_full, 1);
-        mbar_init(o_free, TC_EPI);
+        mbar_init(pv_done, 1);
+        mbar_init(p_ready, TC_PG);
+        mbar_init(s_ready, TC_SG);
+        mbar_init(o_free, TC_OG);
         mbar_init(ds_full, 1);
-        mbar_init(s_ready, TC_EPI);
+        mbar_init(o_full, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -187,9 +240,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&P.mq);
-        prefetch_tmap(&P.mk);
-        prefetch_tmap(&P.mv);
+        prefetch_tmap(&P.mx);
+        prefetch_tmap(&P.my);
+        prefetch_tmap(&P.mz);
     }
     tc_fence_before();
     __syncthreads();
@@ -204,20 +257,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 const int s = c % TC_NST;
                 if (c >= TC_NST && !bwait(&empty[s], ((c / TC_NST) - 1) & 1, abort_flag))
                     break;
-                const int cidx = (a.reverse != 0) != BWD ? nc - 1 - c : c;
-                const int t0 = (int)(bos + (int64_t)cidx * TC_C);
+                const int t0 = (int)(bos + chunk_t0(c));
                 uint8_t *st = sm + s * L::STAGE;
                 mbar_arrive_expect_tx(&full[s], L::STAGE);
 #pragma unroll
                 for (int b = 0; b < TC_D / 64; ++b)
-                    tma_load_4d(st + b * (TC_C * 128), &P.mq, &full[s], 64 * b, h, t0, (int)row);
+                    tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, h, t0, (int)row);
 #pragma unroll
                 for (int b = 0; b < TC_D / 64; ++b)
-                    tma_load_4d(st + L::QB + b * (TC_C * 128), &P.mk, &full[s], 64 * b, h, t0,
+                    tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, h, t0,
                                 (int)row);
 #pragma unroll
                 for (int b = 0; b < E / 64; ++b)
-                    tma_load_4d(st + L::QB + L::KB + b * (TC_C * 128), &P.mv, &full[s], 64 * b, h,
+                    tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s], 64 * b, h,
                                 t0, (int)row);
                 ++issued;
             }
@@ -228,56 +280,58 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t id_qk = idesc_bf16_f32(128, 128, 0, 0);
-            const uint32_t id_qs = idesc_bf16_f32(128, E, 0, 1);
-            const uint32_t id_kv = idesc_bf16_f32(128, E, 1, 1);
+            const uint32_t id_xy = idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t id_xz = idesc_bf16_f32(128, E, 0, 1);
+            const uint32_t id_yz = idesc_bf16_f32(128, E, 1, 1);
             const uint32_t sbase = smem_u32(sm);
+            const uint32_t sa = sbase + L::SOFF;
             bool any = false;
             for (int c = 0; c < nc; ++c) {
                 const int s = c % TC_NST;
-                const uint32_t qa = sbase + s * L::STAGE, ka = qa + L::QB, va = ka + L::KB;
-                const uint32_t sa = sbase + L::SOFF;
+                const uint32_t xa = sbase + s * L::STAGE, ya = xa + L::XB, za = ya + L::YB;
                 if (!bwait(&full[s], (c / TC_NST) & 1, abort_flag))
                     break;
-                if (c > 0 && !bwait(o_full, (c - 1) & 1, abort_flag))   // P of c-1 consumed
+                if (c > 0 && !bwait(pv_done, (c - 1) & 1, abort_flag))
                     break;
                 tc_fence_after();
-                // scores = Q K^T  (both K-major, K = D)
+                // scores = X Y^T  (both K-major, K = D)
 #pragma unroll
                 for (int kk = 0; kk < TC_D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (TC_C * 128) + (kk & 3) * 32;
-                    mma_ss(tm + TM_SC, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
+                    mma_ss(tm + TM_SC, sdesc_sw128(xa + off, 16, 1024),
+                           sdesc_sw128(ya + off, 16, 1024), id_xy, kk > 0);
                 }
                 mma_commit(sc_full);
                 any = true;
+                // X S_bf16  (S: MN-major, N = E, K = D): needs this chunk's state
+                // copy and the previous chunk's O read
                 if (!bwait(s_ready, c & 1, abort_flag))
                     break;
                 if (c > 0 && !bwait(o_free, (c - 1) & 1, abort_flag))
                     break;
                 tc_fence_after();
-                // Q S_bf16  (S: MN-major, N = E, K = D)
 #pragma unroll
                 for (int kk = 0; kk < TC_D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (TC_C * 128) + (kk & 3) * 32;
-                    mma_ss(tm + TM_OI, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(sa + kk * 2048, TC_D * 128, 1024), id_qs, kk > 0);
+                    mma_ss(tm + TM_OI, sdesc_sw128(xa + off, 16, 1024),
+                           sdesc_sw128(sa + kk * 2048, TC_D * 128, 1024), id_xz, kk > 0);
                 }
                 if (!bwait(p_ready, c & 1, abort_flag))
                     break;
                 tc_fence_after();
-                // P V  (P from TMEM, V: MN-major, K = C tokens)
+                // S += (lcol Y)^T Z  (both MN-major, M = D, K = C tokens): the recurrence
+#pragma unroll
+                for (int kk = 0; kk < TC_C / 16; ++kk)
+                    mma_ss(tm + TM_S, sdesc_sw128(ya + kk * 2048, TC_C * 128, 1024),
+                           sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_yz, 1);
+                mma_commit(ds_full);
+                // P Z  (P from TMEM, Z: MN-major, K = C tokens)
 #pragma unroll
                 for (int kk = 0; kk < TC_C / 16; ++kk)
                     mma_ts(tm + TM_OA, tm + TM_SC + (kk >> 2) * 64 + (kk & 3) * 8,
-                           sdesc_sw128(va + kk * 2048, TC_C * 128, 1024), id_qs, kk > 0);
+                           sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_xz, kk > 0);
                 mma_commit(o_full);
-                // (Lambda K)^T V  (both MN-major, M = D, K = C tokens)
-#pragma unroll
-                for (int kk = 0; kk < TC_C / 16; ++kk)
-                    mma_ss(tm + TM_DS, sdesc_sw128(ka + kk * 2048, TC_C * 128, 1024),
-                           sdesc_sw128(va + kk * 2048, TC_C * 128, 1024), id_kv, kk > 0);
-                mma_commit(ds_full);
+                mma_commit(pv_done);
                 mma_commit(&empty[s]);
             }
             if (any) {   // every MMA has finished before TMEM is released
@@ -287,144 +341,209 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ epilogue
         const int et = threadIdx.x - 64;
-        const int q = warp & 3, hh = (warp - 2) >> 2;
-        const int i = 32 * q + lane;
-        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const float g = a.g[h];
         const float scale = a.scale;
-        const bool rev = a.reverse != 0;
-        const bool flip = rev != BWD;   // mask / chunk order direction
-        const bool cols = hh < E / 64;
-        for (int m = et; m <= TC_C; m += TC_EPI)
+        for (int m = et; m <= TC_C; m += TC_PG + TC_SG + TC_OG)
             pw[m] = m == 0 ? 1.f : expf(g * (float)m);
         epi_bar_sync();
+        const int q = warp & 3;
+        const int i = 32 * q + lane;   // TMEM lane = tile row
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
 
-        const int64_t sb = ((int64_t)n * a.H + h) * (int64_t)a.D * a.E;
-        uint8_t *srow = sm + L::SOFF + hh * (TC_D * 128) + i * 128;
-        float S[64];
+        if (warp < 10) {
+            // ------------------------------------------------------- P group
+            const int hh = (warp - 2) >> 2;
+            const int j0 = 64 * hh;
+            const float gam = pw[1];
+            for (int c = 0; c < nc; ++c) {
+                const int s = c % TC_NST;
+                const int Lc = chunk_len(c);
+                bool ok = warp_all(bwait(&full[s], (c / TC_NST) & 1, abort_flag));
+                if (ok)
+                    ok = warp_all(bwait(sc_full, c & 1, abort_flag));
+                if (!ok)
+                    break;
+                tc_fence_after();
+                uint32_t ra[32], rb[32];
+                const uint32_t col = tm + lane_off + TM_SC + j0;
+                tmem_ld32_issue(col, ra);
+                tmem_ld32_issue(col + 32, rb);
+                tmem_wait_ld(ra, rb);
+                // decay gamma^d, d = |p(i) - p(j)|, walked with a running product
+                // along the row (at most 127 steps) instead of a table load per
+                // element; masked entries are zero.  Each packed pair of P goes
+                // into the even register slot it was read from.
+                if (!flip) {
+                    // keep j <= i (< Lc); d = i - j grows as j falls
+                    int d = i - (j0 + 63);
+                    float w = pw[d > 0 ? d : 0];
+                    const float sc = i < Lc ? scale : 0.f;
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
-            S[k] = (cols && a.s_in.p) ? a.s_in.p[sb + i * a.s_in.rs + (64 * hh + k) * a.s_in.cs]
-                                      : 0.f;
-        if (cols) {
-            store_row_sw128(srow, i, S);
-            fence_proxy_async_smem();
-        }
-        tc_fence_before();
-        mbar_arrive(s_ready);
-
-        __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.out.p) + row * a.out.sb +
-                               (int64_t)h * a.out.sh + 64 * hh;
-        bool ok = true;
-        for (int c = 0; c < nc && ok; ++c) {
-            const int s = c % TC_NST;
-            const int cidx = flip ? nc - 1 - c : c;
-            const int64_t tc0 = (int64_t)cidx * TC_C;
-            const int Lc = (int)(len - tc0 < TC_C ? len - tc0 : TC_C);
-
-            // (a) decay-masked P (bf16, back into TMEM) and Lambda_k K in place
-            ok = warp_all(bwait(&full[s], (c / TC_NST) & 1, abort_flag));
-            if (ok)
-                ok = warp_all(bwait(sc_full, c & 1, abort_flag));
-            if (!ok)
-                break;
-            tc_fence_after();
+                    for (int jj = 63; jj >= 0; jj -= 2) {
+                        const float x1 = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
+                        const float x0 = __uint_as_float(jj < 32 ? ra[jj - 1] : rb[jj - 33]);
+                        const float v1 = d >= 0 ? sc * x1 * w : 0.f;
+                        w = d >= 0 ? w * gam : w;
+                        ++d;
+                        const float v0 = d >= 0 ? sc * x0 * w : 0.f;
+                        w = d >= 0 ? w * gam : w;
+                        ++d;
+                        const uint32_t pk = pack_bf16x2(v0, v1);
+                        if (jj < 32)
+                            ra[jj - 1] = pk;   // slot just consumed
+                        else
+                            rb[jj - 33] = pk;
+                    }
+                } else {
+                    // keep j >= i, j < Lc; d = j - i grows with j
+                    int d = j0 - i;
+                    float w = pw[d > 0 ? d : 0];
 #pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                uint32_t r[16], pk[8];
-                tmem_ld16(tm + lane_off + TM_SC + 64 * hh + 16 * part, r);
-#pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {
-                    const int j = 64 * hh + 16 * part + jj;
-                    const int d0 = flip ? j - i : i - j, d1 = flip ? d0 + 1 : d0 - 1;
-                    const bool k0 = d0 >= 0 && (flip ? j : i) < Lc;
-                    const bool k1 = d1 >= 0 && (flip ? j + 1 : i) < Lc;
-                    const float v0 = k0 ? scale * __uint_as_float(r[jj]) * pw[k0 ? d0 : 0] : 0.f;
-                    const float v1 = k1 ? scale * __uint_as_float(r[jj + 1]) * pw[k1 ? d1 : 0] : 0.f;
-                    pk[jj / 2] = pack_bf16x2(v0, v1);
-                }
-                // P for keys [64hh + 16part, +16) -> 8 packed columns inside this
-                // thread's own (already read) score columns
-                tmem_st8(tm + lane_off + TM_SC + 64 * hh + 8 * part, pk);
-            }
-            {
-                // column factor: gamma^(Lc-1-p(i)) forward, gamma^(p(i)+1) backward
-                const float lk = i >= Lc ? 0.f
-                                 : BWD ? (rev ? pw[Lc - i] : pw[i + 1])
-                                       : (rev ? pw[i] : pw[Lc - 1 - i]);
-                uint8_t *krow = sm + s * L::STAGE + L::QB + hh * (TC_C * 128) + i * 128;
-#pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16) {
-                    uint4 *p = reinterpret_cast<uint4 *>(krow + ((c16 ^ (i & 7)) << 4));
-                    *p = scale8(*p, lk);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(p_ready);
-
-            // (b) o = P V + s gamma^(p(i)+1) Q S
-            ok = warp_all(bwait(o_full, c & 1, abort_flag));
-            if (!ok)
-                break;
-            tc_fence_after();
-            if (cols) {
-                // row factor: s*gamma^(p(i)+1) forward, gamma^(Lc-1-p(i)) backward
-                const float lq = i >= Lc ? 0.f
-                                 : BWD ? (rev ? pw[i] : pw[Lc - 1 - i])
-                                       : scale * (rev ? pw[Lc - i] : pw[i + 1]);
-                __nv_bfloat16 *orow = obase + (bos + tc0 + i) * a.out.st;
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {
-                    uint32_t ra[16], ri[16];
-                    tmem_ld16(tm + lane_off + TM_OA + 64 * hh + 16 * part, ra);
-                    tmem_ld16(tm + lane_off + TM_OI + 64 * hh + 16 * part, ri);
-                    if (i < Lc) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            w[u] = pack_bf16x2(
-                                fmaf(lq, __uint_as_float(ri[2 * u]), __uint_as_float(ra[2 * u])),
-                                fmaf(lq, __uint_as_float(ri[2 * u + 1]),
-                                     __uint_as_float(ra[2 * u + 1])));
-                        *reinterpret_cast<uint4 *>(orow + 16 * part) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4 *>(orow + 16 * part + 8) =
-                            make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int jj = 0; jj < 64; jj += 2) {
+                        const float x0 = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
+                        const float x1 = __uint_as_float(jj < 32 ? ra[jj + 1] : rb[jj - 31]);
+                        const float v0 = d >= 0 && j0 + jj < Lc ? scale * x0 * w : 0.f;
+                        w = d >= 0 ? w * gam : w;
+                        ++d;
+                        const float v1 = d >= 0 && j0 + jj + 1 < Lc ? scale * x1 * w : 0.f;
+                        w = d >= 0 ? w * gam : w;
+                        ++d;
+                        const uint32_t pk = pack_bf16x2(v0, v1);
+                        if (jj < 32)
+                            ra[jj] = pk;   // slot just consumed
+                        else
+                            rb[jj - 32] = pk;
                     }
                 }
-            }
-            tc_fence_before();
-            mbar_arrive(o_free);
-
-            // (c) S = gamma^Lc S + (Lambda_k K)^T V; refresh the bf16 copy
-            ok = warp_all(bwait(ds_full, c & 1, abort_flag));
-            if (!ok)
-                break;
-            tc_fence_after();
-            if (cols) {
-                const float gl = pw[Lc];
-                const float ds_scale = BWD ? scale : 1.f;
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {
-                    uint32_t r[16];
-                    tmem_ld16(tm + lane_off + TM_DS + 64 * hh + 16 * part, r);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        S[16 * part + k] = fmaf(gl, S[16 * part + k], ds_scale * __uint_as_float(r[k]));
+                // P for the keys of this half: 32 packed columns inside the
+                // thread's own (already read) score columns
+                tmem_st16_even_issue(col, ra);
+                tmem_st16_even_issue(col + 16, rb);
+                tmem_wait_st();
+                {
+                    // column factor for the state update, applied to row i of Y
+                    float lc = 0.f;
+                    if (i < Lc) {
+                        const int pi = rev ? Lc - 1 - i : i;
+                        lc = BWD ? scale * pw[pi + 1] : pw[Lc - 1 - pi];
+                    }
+                    scale_row_sw128(sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128, i, lc);
                 }
-                store_row_sw128(srow, i, S);
                 fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_ready);
             }
-            tc_fence_before();
-            mbar_arrive(s_ready);
-        }
-        if (ok && cols && a.s_out.p && !*abort_flag) {
+        } else if (warp < 14) {
+            // ------------------------------------------------------- S group
+            const int64_t sb = ((int64_t)n * a.H + h) * (int64_t)a.D * a.E;
+            uint8_t *sbf = sm + L::SOFF + i * 128;
+            // initial state: bf16 copy and gamma^L0-scaled fp32 in TMEM
+            {
+                const float g0 = nc > 0 ? pw[chunk_len(0)] : 1.f;
+#pragma unroll 1
+                for (int eb = 0; eb < E / 64; ++eb) {
+                    uint32_t ra[32], rb[32];
+                    const float *src =
+                        a.s_in.p ? a.s_in.p + sb + i * a.s_in.rs + 64 * eb * a.s_in.cs : nullptr;
 #pragma unroll
-            for (int k = 0; k < 64; ++k)
-                a.s_out.p[sb + i * a.s_out.rs + (64 * hh + k) * a.s_out.cs] = S[k];
+                    for (int k = 0; k < 32; ++k) {
+                        ra[k] = __float_as_uint(src ? src[k * a.s_in.cs] : 0.f);
+                        rb[k] = __float_as_uint(src ? src[(k + 32) * a.s_in.cs] : 0.f);
+                    }
+                    if (nc == 0) {
+                        if (a.s_out.p) {
+                            float *dst = a.s_out.p + sb + i * a.s_out.rs + 64 * eb * a.s_out.cs;
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                dst[k * a.s_out.cs] = __uint_as_float(ra[k]);
+                                dst[(k + 32) * a.s_out.cs] = __uint_as_float(rb[k]);
+                            }
+                        }
+                        continue;
+                    }
+                    store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        ra[k] = __float_as_uint(g0 * __uint_as_float(ra[k]));
+                        rb[k] = __float_as_uint(g0 * __uint_as_float(rb[k]));
+                    }
+                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb, ra);
+                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb + 32, rb);
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(s_ready);
+            }
+            for (int c = 0; c < nc; ++c) {
+                if (!warp_all(bwait(ds_full, c & 1, abort_flag)))
+                    break;
+                tc_fence_after();
+                const bool last = c + 1 == nc;
+                const float gn = last ? 1.f : pw[chunk_len(c + 1)];
+#pragma unroll 1
+                for (int eb = 0; eb < E / 64; ++eb) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32_issue(tm + lane_off + TM_S + 64 * eb, ra);
+                    tmem_ld32_issue(tm + lane_off + TM_S + 64 * eb + 32, rb);
+                    tmem_wait_ld(ra, rb);
+                    if (last) {
+                        if (a.s_out.p && !*abort_flag) {
+                            float *dst = a.s_out.p + sb + i * a.s_out.rs + 64 * eb * a.s_out.cs;
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                dst[k * a.s_out.cs] = __uint_as_float(ra[k]);
+                                dst[(k + 32) * a.s_out.cs] = __uint_as_float(rb[k]);
+                            }
+                        }
+                        continue;
+                    }
+                    store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        ra[k] = __float_as_uint(gn * __uint_as_float(ra[k]));
+                        rb[k] = __float_as_uint(gn * __uint_as_float(rb[k]));
+                    }
+                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb, ra);
+                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb + 32, rb);
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(s_ready);
+            }
+        } else {
+            // ------------------------------------------------------- O group
+            __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.out.p) + row * a.out.sb +
+                                   (int64_t)h * a.out.sh;
+            for (int c = 0; c < nc; ++c) {
+                const int Lc = chunk_len(c);
+                if (!warp_all(bwait(o_full, c & 1, abort_flag)))
+                    break;
+                tc_fence_after();
+                float lr = 0.f;
+                if (i < Lc) {
+                    const int pi = rev ? Lc - 1 - i : i;
+                    lr = BWD ? pw[Lc - 1 - pi] : scale * pw[pi + 1];
+                }
+                __nv_bfloat16 *orow = obase + (bos + chunk_t0(c) + i) * a.out.st;
+#pragma unroll 1
+                for (int part = 0; part < E / 32; ++part) {
+                    uint32_t ra[32], ri[32];
+                    tmem_ld32_issue(tm + lane_off + TM_OA + 32 * part, ra);
+                    tmem_ld32_issue(tm + lane_off + TM_OI + 32 * part, ri);
+                    tmem_wait_ld(ra, ri);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        ra[k] = __float_as_uint(
+                            fmaf(lr, __uint_as_float(ri[k]), __uint_as_float(ra[k])));
+                    if (i < Lc)
+                        store_bf16x32(orow + 32 * part, ra);
+                }
+                tc_fence_before();
+                mbar_arrive(o_free);
+            }
         }
     }
 
@@ -489,9 +608,9 @@ template <int E, bool BWD> cudaError_t launch_tc(const SweepArgs &a, cudaStream_
 {
     TcParams p;
     const Tok &x = BWD ? a.k : a.q, &y = BWD ? a.q : a.k;
-    if (!make_map(&p.mq, x.p, TC_D, a, x.sb, x.st, x.sh) ||
-        !make_map(&p.mk, y.p, TC_D, a, y.sb, y.st, y.sh) ||
-        !make_map(&p.mv, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh))
+    if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh) ||
+        !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh) ||
+        !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh))
         return cudaErrorNotSupported;
     p.a = a;
     auto kern = tc_sweep_kernel<E, BWD>;
