@@ -135,14 +135,18 @@ __device__ __forceinline__ uint4 scale8(uint4 v, float f)
     return v;
 }
 
-// One 128-byte row of a 128B-swizzled bf16 tile, scaled in place.
+// One 128-byte row of a 128B-swizzled bf16 tile, scaled in place.  All eight
+// 16-byte chunks are loaded before any is stored, so the loads are not held
+// back behind stores the compiler cannot prove to be elsewhere.
 __device__ __forceinline__ void scale_row_sw128(uint8_t *row_base, int row, float f)
 {
+    uint4 v[8];
 #pragma unroll
-    for (int c16 = 0; c16 < 8; ++c16) {
-        uint4 *p = reinterpret_cast<uint4 *>(row_base + ((c16 ^ (row & 7)) << 4));
-        *p = scale8(*p, f);
-    }
+    for (int c16 = 0; c16 < 8; ++c16)
+        v[c16] = *reinterpret_cast<const uint4 *>(row_base + ((c16 ^ (row & 7)) << 4));
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16)
+        *reinterpret_cast<uint4 *>(row_base + ((c16 ^ (row & 7)) << 4)) = scale8(v[c16], f);
 }
 
 // 64 fp32 (as bits, lo = first 32 columns, hi = next 32) -> one 128-byte
