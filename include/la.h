@@ -31,6 +31,13 @@
  *   - State tensors (initial_state, final_state, d_final_state,
  *     d_initial_state) are dense fp32 [N, H, D, E], N = B, or num_seqs when
  *     cu_seqlens is given.
+ *   - Workspace (optional): with packed sequences the library schedules the
+ *     longest sequences first.  It needs la_workspace_size(N) bytes of device
+ *     memory for that schedule, passed as (workspace, workspace_bytes); the
+ *     schedule is copied there on `stream` and read by the kernels, so the
+ *     workspace must not be shared with another call in flight on another
+ *     stream.  NULL (or too small a workspace) runs the sequences in index
+ *     order; results are identical either way.  Dense batches ignore it.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) of the current device.  No entry point
  *     allocates device memory or synchronizes, except: when cu_seqlens is given
@@ -105,13 +112,15 @@ typedef struct la_dims {
  *                   cu[N] = T; or NULL for B independent rows of length T
  *   cu_seqlens_host host copy of cu_seqlens, or NULL (then copied, see above)
  *   o               [B,T,H,E] of `dtype` (output, v_strides)
- *   final_state     [N,H,D,E] fp32 output, or NULL to skip it              */
+ *   final_state     [N,H,D,E] fp32 output, or NULL to skip it
+ *   workspace       device scratch for the packed schedule, or NULL (above) */
 la_status la_fwd(const la_dims *dims, int32_t dtype,
                  const void *q, const void *k, const void *v,
                  const float *g_gamma, float scale,
                  const float *initial_state, int32_t reverse,
                  const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                 void *o, float *final_state, void *stream);
+                 void *o, float *final_state,
+                 void *workspace, size_t workspace_bytes, void *stream);
 
 /* Backward pass: gradients of  sum(o * d_o) + sum(final_state * d_final_state)
  * (the custom VJP of ejkernel `recurrent`, `_recurrent_bwd`, with upstream
@@ -133,7 +142,7 @@ la_status la_bwd(const la_dims *dims, int32_t dtype,
                  int32_t reverse,
                  const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                  void *dq, void *dk, void *dv, float *d_initial_state,
-                 void *stream);
+                 void *workspace, size_t workspace_bytes, void *stream);
 
 /* The first half of la_bwd: dq only (a sweep in processing order that
  * recomputes the states; q and d_final_state are not read).  Arguments as
@@ -143,7 +152,7 @@ la_status la_bwd_dq(const la_dims *dims, int32_t dtype,
                     const float *g_gamma, float scale,
                     const float *initial_state, int32_t reverse,
                     const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                    void *dq, void *stream);
+                    void *dq, void *workspace, size_t workspace_bytes, void *stream);
 
 /* The second half of la_bwd: dk, dv and d_initial_state (a sweep against
  * the processing order carrying dL/dS; initial_state is not read).
@@ -153,7 +162,12 @@ la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype,
                       const float *g_gamma, float scale,
                       const float *d_final_state, int32_t reverse,
                       const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                      void *dk, void *dv, float *d_initial_state, void *stream);
+                      void *dk, void *dv, float *d_initial_state,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace for the longest-first schedule of num_seqs packed
+ * sequences (0 when num_seqs < 1).  Pure host function. */
+size_t la_workspace_size(int32_t num_seqs);
 
 /* Reads and clears the device-side error word that bounded on-device waits
  * set when they run out (LA_ERR_TIMEOUT), after synchronizing `stream`.

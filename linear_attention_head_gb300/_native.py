@@ -51,19 +51,21 @@ class LaUnsupported(LaError, NotImplementedError):
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _f32 = ctypes.c_float
+_sz = ctypes.c_size_t
 _dims_p = ctypes.POINTER(LaDims)
 
 # name -> (restype, argtypes); mirrors include/la.h exactly (float* are passed
 # as void* addresses).
 PROTOTYPES = {
     "la_fwd": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _vp,
-                      _vp, _vp, _vp]),
+                      _vp, _vp, _vp, _sz, _vp]),
     "la_bwd": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _i32,
-                      _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "la_bwd_dq": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32,
-                         _vp, _vp, _vp, _vp]),
+                         _vp, _vp, _vp, _vp, _sz, _vp]),
     "la_bwd_dkdv": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32,
-                           _vp, _vp, _vp, _vp, _vp, _vp]),
+                           _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "la_workspace_size": (_sz, [_i32]),
     "la_get_device_error": (_i32, [_vp]),
     "la_strerror": (ctypes.c_char_p, [_i32]),
     "la_last_error": (ctypes.c_char_p, []),

@@ -50,12 +50,14 @@ def _stream(device) -> ctypes.c_void_p:
 
 
 class _Packed:
-    """cu_seqlens on the device plus a host copy (so the library never syncs)."""
+    """cu_seqlens on the device plus a host copy (so the library never syncs), and the
+    device workspace for the library's longest-first schedule of the sequences."""
 
     def __init__(self, cu_seqlens, device):
         self.dev = None
         self.host = None
         self.n = 0
+        self.ws = None
         if cu_seqlens is None:
             return
         cu = torch.as_tensor(cu_seqlens)
@@ -67,6 +69,14 @@ class _Packed:
         else:
             self.dev = self.host.to(device)
         self.n = self.host.numel() - 1
+        nbytes = int(N.lib().la_workspace_size(self.n))
+        if nbytes:
+            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def ws_args(self):
+        if self.ws is None:
+            return None, 0
+        return ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel()
 
     def host_ptr(self):
         return None if self.host is None else ctypes.c_void_p(self.host.data_ptr())
@@ -161,7 +171,8 @@ def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = No
     dims = _dims(q, v, packed)
     st = N.lib().la_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                         scale, _ptr(init), int(bool(reverse)), _ptr(packed.dev),
-                        packed.host_ptr(), _ptr(out), _ptr(final_state), _stream(dev))
+                        packed.host_ptr(), _ptr(out), _ptr(final_state), *packed.ws_args(),
+                        _stream(dev))
     N.check(st)
     return out, final_state
 
@@ -199,7 +210,7 @@ def la_bwd(q: Tensor, k: Tensor, v: Tensor, do: Tensor, g_gamma, scale: Optional
     st = N.lib().la_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
                         _ptr(g), scale, _ptr(init), _ptr(dfin), int(bool(reverse)),
                         _ptr(packed.dev), packed.host_ptr(), _ptr(dq), _ptr(dk), _ptr(dv),
-                        _ptr(dinit), _stream(dev))
+                        _ptr(dinit), *packed.ws_args(), _stream(dev))
     N.check(st)
     return dq, dk, dv, dinit
 
@@ -213,7 +224,8 @@ def la_bwd_dq(q, k, v, do, g_gamma, scale=None, initial_state=None, reverse=Fals
     dims = _dims(q, v, packed)
     st = N.lib().la_bwd_dq(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                            _ptr(do), _ptr(g), scale, _ptr(init), int(bool(reverse)),
-                           _ptr(packed.dev), packed.host_ptr(), _ptr(dq), _stream(dev))
+                           _ptr(packed.dev), packed.host_ptr(), _ptr(dq), *packed.ws_args(),
+                           _stream(dev))
     N.check(st)
     return dq
 
@@ -230,7 +242,7 @@ def la_bwd_dkdv(q, k, v, do, g_gamma, scale=None, d_final_state=None, reverse=Fa
     st = N.lib().la_bwd_dkdv(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                              _ptr(do), _ptr(g), scale, _ptr(dfin), int(bool(reverse)),
                              _ptr(packed.dev), packed.host_ptr(), _ptr(dk), _ptr(dv),
-                             _ptr(dinit), _stream(dev))
+                             _ptr(dinit), *packed.ws_args(), _stream(dev))
     N.check(st)
     return dk, dv, dinit
 

@@ -12,6 +12,7 @@
 // so the kernels never see the words "query" or "gradient"; the host decides
 // which tensors play which role.
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -50,6 +51,7 @@ la_status cuda_fail(cudaError_t e, const char *where)
 struct Problem {
     int B, T, H, D, E, N;
     bool packed;
+    std::vector<int32_t> cu_host;   // validated host copy of cu_seqlens (packed only)
 };
 
 // Sizes, dtype and the packed-sequence table; fills *P.
@@ -113,6 +115,40 @@ la_status check_dims(const la_dims *d, int32_t dtype, const int32_t *cu, const i
     if (cu_host[P->N] != d->seq_len)
         return fail(LA_ERR_INVALID_ARG, "cu_seqlens[%d] = %d but seq_len = %d", P->N,
                     cu_host[P->N], d->seq_len);
+    P->cu_host.assign(cu_host, cu_host + P->N + 1);
+    return LA_OK;
+}
+
+size_t schedule_bytes(int64_t num_seqs)
+{
+    return num_seqs <= 0 ? 0 : (size_t)((num_seqs * 4 + 255) / 256 * 256);
+}
+
+// Longest-first schedule of packed sequences: sequence indices sorted by
+// length, longest first (ties keep index order), copied into the caller's
+// workspace on `s`.  Returns the device array, or nullptr (index order) when
+// nothing is packed, there is no workspace, or it is too small.
+la_status make_schedule(const Problem &P, void *ws, size_t ws_bytes, cudaStream_t s,
+                        const int32_t **order)
+{
+    *order = nullptr;
+    if (!P.packed || P.N < 2 || !ws || ws_bytes < schedule_bytes(P.N))
+        return LA_OK;
+    if ((reinterpret_cast<uintptr_t>(ws) & 3) != 0)
+        return fail(LA_ERR_INVALID_ARG, "workspace is not 4-byte aligned");
+    std::vector<int32_t> idx((size_t)P.N);
+    for (int n = 0; n < P.N; ++n)
+        idx[(size_t)n] = n;
+    const std::vector<int32_t> &cu = P.cu_host;
+    std::stable_sort(idx.begin(), idx.end(), [&](int32_t x, int32_t y) {
+        return cu[(size_t)x + 1] - cu[(size_t)x] > cu[(size_t)y + 1] - cu[(size_t)y];
+    });
+    // pageable source: the copy is staged before cudaMemcpyAsync returns
+    cudaError_t e = cudaMemcpyAsync(ws, idx.data(), idx.size() * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copying the packed schedule");
+    *order = static_cast<const int32_t *>(ws);
     return LA_OK;
 }
 
@@ -128,7 +164,7 @@ la::Tok tok(const void *p, const int64_t *st) { return la::Tok{p, st[0], st[1], 
 la::TokOut tok_out(void *p, const int64_t *st) { return la::TokOut{p, st[0], st[1], st[2]}; }
 
 la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, const float *g,
-                        float scale, int32_t reverse)
+                        float scale, int32_t reverse, const int32_t *order = nullptr)
 {
     la::SweepArgs a{};
     a.B = P.B;
@@ -136,6 +172,7 @@ la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, cons
     a.H = P.H;
     a.N = P.N;
     a.cu = cu;
+    a.order = order;
     a.g = g;
     a.scale = scale;
     a.reverse = reverse ? 1 : 0;
@@ -166,10 +203,10 @@ la_status run_backward_type(const la::SweepArgs &a, cudaStream_t s)
 
 la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *k, const void *v,
                  const void *d_o, const float *g_gamma, float scale, const float *init,
-                 int32_t reverse, const int32_t *cu, void *dq, cudaStream_t s)
+                 int32_t reverse, const int32_t *cu, const int32_t *order, void *dq, cudaStream_t s)
 {
     // dq = forward-type sweep with (q, k, v) := (do, v, k); the state is S^T (E x D).
-    la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse);
+    la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse, order);
     a.D = P.E;
     a.E = P.D;
     a.q = tok(d_o, d->v_strides);
@@ -184,9 +221,9 @@ la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *
 la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void *q,
                    const void *k, const void *v, const void *d_o, const float *g_gamma,
                    float scale, const float *dfinal, int32_t reverse, const int32_t *cu,
-                   void *dk, void *dv, float *dinit, cudaStream_t s)
+                   const int32_t *order, void *dk, void *dv, float *dinit, cudaStream_t s)
 {
-    la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse);
+    la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse, order);
     // dv: (q, k, w) as given, G = dL/dS (D x E)
     a.D = P.D;
     a.E = P.E;
@@ -218,7 +255,7 @@ extern "C" {
 la_status la_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *k, const void *v,
                  const float *g_gamma, float scale, const float *initial_state, int32_t reverse,
                  const int32_t *cu_seqlens, const int32_t *cu_seqlens_host, void *o,
-                 float *final_state, void *stream)
+                 float *final_state, void *workspace, size_t workspace_bytes, void *stream)
 {
     g_msg.clear();
     cudaStream_t s = (cudaStream_t)stream;
@@ -235,7 +272,10 @@ la_status la_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *
         return LA_OK;
     if ((st = need(g_gamma, "g_gamma")))
         return st;
-    la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
+    const int32_t *order = nullptr;
+    if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
+        return st;
+    la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse, order);
     a.D = P.D;
     a.E = P.E;
     a.q = tok(q, dims->qk_strides);
@@ -250,7 +290,8 @@ la_status la_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *
 la_status la_bwd_dq(const la_dims *dims, int32_t dtype, const void *q, const void *k,
                     const void *v, const void *d_o, const float *g_gamma, float scale,
                     const float *initial_state, int32_t reverse, const int32_t *cu_seqlens,
-                    const int32_t *cu_seqlens_host, void *dq, void *stream)
+                    const int32_t *cu_seqlens_host, void *dq, void *workspace,
+                    size_t workspace_bytes, void *stream)
 {
     (void)q;
     g_msg.clear();
@@ -268,15 +309,19 @@ la_status la_bwd_dq(const la_dims *dims, int32_t dtype, const void *q, const voi
         return LA_OK;
     if ((st = need(g_gamma, "g_gamma")))
         return st;
+    const int32_t *order = nullptr;
+    if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
+        return st;
     return bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens,
-                  dq, s);
+                  order, dq, s);
 }
 
 la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype, const void *q, const void *k,
                       const void *v, const void *d_o, const float *g_gamma, float scale,
                       const float *d_final_state, int32_t reverse, const int32_t *cu_seqlens,
                       const int32_t *cu_seqlens_host, void *dk, void *dv,
-                      float *d_initial_state, void *stream)
+                      float *d_initial_state, void *workspace, size_t workspace_bytes,
+                      void *stream)
 {
     g_msg.clear();
     cudaStream_t s = (cudaStream_t)stream;
@@ -293,15 +338,18 @@ la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype, const void *q, const v
         return LA_OK;
     if ((st = need(g_gamma, "g_gamma")))
         return st;
+    const int32_t *order = nullptr;
+    if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
+        return st;
     return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
-                    cu_seqlens, dk, dv, d_initial_state, s);
+                    cu_seqlens, order, dk, dv, d_initial_state, s);
 }
 
 la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k, const void *v,
                  const void *d_o, const float *g_gamma, float scale, const float *initial_state,
                  const float *d_final_state, int32_t reverse, const int32_t *cu_seqlens,
                  const int32_t *cu_seqlens_host, void *dq, void *dk, void *dv,
-                 float *d_initial_state, void *stream)
+                 float *d_initial_state, void *workspace, size_t workspace_bytes, void *stream)
 {
     g_msg.clear();
     cudaStream_t s = (cudaStream_t)stream;
@@ -319,12 +367,15 @@ la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *
         return LA_OK;
     if ((st = need(g_gamma, "g_gamma")))
         return st;
-    st = bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens, dq,
-                s);
+    const int32_t *order = nullptr;
+    if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
+        return st;
+    st = bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens,
+                order, dq, s);
     if (st != LA_OK)
         return st;
     return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
-                    cu_seqlens, dk, dv, d_initial_state, s);
+                    cu_seqlens, order, dk, dv, d_initial_state, s);
 }
 
 la_status la_get_device_error(void *stream)
@@ -373,6 +424,8 @@ int32_t la_kernel_family(const la_dims *dims, int32_t dtype)
     a.out = tok_out(nullptr, dims->v_strides);
     return la::tc_sweep_supported(a) ? 1 : 0;
 }
+
+size_t la_workspace_size(int32_t num_seqs) { return schedule_bytes(num_seqs); }
 
 uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

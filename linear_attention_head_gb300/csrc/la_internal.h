@@ -49,6 +49,8 @@ struct StateOut {
 struct SweepArgs {
     int B, T, H, D, E, N;     // D: width of q and k; E: width of v (w) and out
     const int32_t *cu;        // device [N+1] or nullptr (dense: N == B rows of T)
+    const int32_t *order;     // device [N]: sequence processed at rank r, longest first;
+                              // nullptr = natural order
     const float *g;           // [H] log-decay
     float scale;
     int reverse;

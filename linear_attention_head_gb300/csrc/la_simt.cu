@@ -108,7 +108,8 @@ __device__ void load_chunk(const SweepArgs &a, const Seq &sq, int h, int64_t t0,
 template <typename T>
 __global__ void __launch_bounds__(SNT) simt_forward_kernel(SweepArgs a)
 {
-    const int n = blockIdx.x, h = blockIdx.y, e0 = blockIdx.z * SET;
+    const int n = a.order ? a.order[blockIdx.x] : (int)blockIdx.x;
+    const int h = blockIdx.y, e0 = blockIdx.z * SET;
     const int D = a.D, DP = D + 1, ew = min(SET, a.E - e0);
     const Seq sq = seq_of(a, n);
     extern __shared__ float sm[];
@@ -192,7 +193,8 @@ __global__ void __launch_bounds__(SNT) simt_forward_kernel(SweepArgs a)
 template <typename T>
 __global__ void __launch_bounds__(SNT) simt_backward_kernel(SweepArgs a)
 {
-    const int n = blockIdx.x, h = blockIdx.y, e0 = blockIdx.z * SET;
+    const int n = a.order ? a.order[blockIdx.x] : (int)blockIdx.x;
+    const int h = blockIdx.y, e0 = blockIdx.z * SET;
     const int D = a.D, DP = D + 1, ew = min(SET, a.E - e0);
     const Seq sq = seq_of(a, n);
     extern __shared__ float sm[];

@@ -202,7 +202,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::ABORTOFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    // work item: the rank-th sequence of the schedule (longest first when an
+    // order is given), one head per CTA
+    const int rank = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    const int n = a.order ? a.order[rank] : rank;
     int64_t row, bos, len;
     if (a.cu) {
         row = 0;

@@ -83,7 +83,7 @@ FAKE = ctypes.c_void_p(0x1000)     # never dereferenced: validation fails first
 
 def _fwd(lib, dims, dtype=0, cu=None, cu_host=None, q=FAKE, g=FAKE, o=FAKE):
     return lib.la_fwd(ctypes.byref(dims) if dims is not None else None, dtype, q, FAKE, FAKE, g,
-                      1.0, None, 0, cu, cu_host, o, None, None)
+                      1.0, None, 0, cu, cu_host, o, None, None, 0, None)
 
 
 def test_validation_errors_return_before_any_launch(lib):
@@ -128,13 +128,13 @@ def test_packed_sequence_table_is_validated_on_the_host(lib):
 def test_backward_entry_points_validate(lib):
     d = _dims()
     st = lib.la_bwd(ctypes.byref(d), 0, FAKE, FAKE, FAKE, None, FAKE, 1.0, None, None, 0, None,
-                    None, FAKE, FAKE, FAKE, None, None)
+                    None, FAKE, FAKE, FAKE, None, None, 0, None)
     assert st == N.LA_ERR_INVALID_ARG and "d_o" in N.last_error()
     st = lib.la_bwd_dq(ctypes.byref(d), 0, None, FAKE, FAKE, FAKE, FAKE, 1.0, None, 0, None,
-                       None, None, None)
+                       None, None, None, 0, None)
     assert st == N.LA_ERR_INVALID_ARG and "dq" in N.last_error()
     st = lib.la_bwd_dkdv(ctypes.byref(d), 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, None, 0, None,
-                         None, FAKE, None, None, None)
+                         None, FAKE, None, None, None, 0, None)
     assert st == N.LA_ERR_INVALID_ARG and "dv" in N.last_error()
 
 
@@ -149,3 +149,10 @@ def test_kernel_family_is_host_only():
     assert la.kernel_family(4, 1024, 32, 128, 128) in (0, 1)
     assert la.kernel_family(1, 256, 2, 32, 32, dtype="f32") == 0
     assert la.kernel_family(1, 256, 2, 0, 32) == -1
+
+
+def test_workspace_size(lib):
+    assert lib.la_workspace_size(0) == 0
+    assert lib.la_workspace_size(1) == 256
+    assert lib.la_workspace_size(64) == 256
+    assert lib.la_workspace_size(65) == 512

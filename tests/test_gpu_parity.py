@@ -207,3 +207,35 @@ def test_repeated_calls_are_deterministic_and_report_no_timeout():
     for n in a:
         assert torch.equal(a[n], b[n]), n
     la.get_device_error()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_longest_first_schedule_is_bit_identical_to_index_order(D):
+    # the packed schedule only changes which CTA runs which sequence
+    import ctypes
+    from linear_attention_head_gb300 import _native as N
+    lens = [5, 300, 0, 129, 64, 1000, 17]
+    w = _custom(1, 0, 2, D, D, torch.bfloat16, seqlens=lens, init=0.1)
+    x = W.make_inputs(w, seed=31)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o_sched, f_sched = la.la_fwd(d["q"], d["k"], d["v"], d["g_gamma"], w.scale,
+                                 d["initial_state"], cu_seqlens=x["cu_seqlens"])
+    o_plain = torch.empty_like(o_sched)
+    f_plain = torch.empty_like(f_sched)
+    dims = N.LaDims()
+    B, T, H, Dq = d["q"].shape
+    dims.batch, dims.seq_len, dims.heads, dims.dim_qk, dims.dim_v = B, T, H, Dq, D
+    dims.num_seqs = len(lens)
+    for i in range(3):
+        dims.qk_strides[i] = d["q"].stride(i)
+        dims.v_strides[i] = d["v"].stride(i)
+    cu_dev = x["cu_seqlens"].cuda()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = N.lib().la_fwd(ctypes.byref(dims), N.LA_DTYPE_BF16, P(d["q"]), P(d["k"]), P(d["v"]),
+                        P(d["g_gamma"]), w.scale, P(d["initial_state"]), 0, P(cu_dev),
+                        P(x["cu_seqlens"]), P(o_plain), P(f_plain), None, 0,
+                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    N.check(st)
+    torch.cuda.synchronize()
+    assert torch.equal(o_sched, o_plain)
+    assert torch.equal(f_sched, f_plain)
