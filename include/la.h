@@ -165,6 +165,29 @@ la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype,
                       void *dk, void *dv, float *d_initial_state,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* The forward pass without any device workspace, for callers that cannot
+ * allocate device memory where they call it (their device memory belongs to
+ * another allocator that hands out no scratch, or a cudaMalloc there would
+ * synchronize the device).  The pages have no counterpart: this is an
+ * interface for such callers.  Arguments, results and validation are those of
+ * la_fwd; the packed-sequence schedule lives in an array compiled into the
+ * library (LA_FWD_NOALLOC_MAX_SEQS int32 per GPU, held until exit) instead of
+ * a caller workspace.  More than LA_FWD_NOALLOC_MAX_SEQS packed sequences is
+ * rejected with LA_ERR_UNSUPPORTED before anything is enqueued.  The first
+ * call on a device looks the array's device address up (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * Every call on a device shares the one array, which keeps the previous
+ * call's schedule; each call overwrites the entries it uses.  Calls whose
+ * work overlaps on the GPU (different streams, or host threads without
+ * ordering between them) race on it and must be serialized by the caller. */
+#define LA_FWD_NOALLOC_MAX_SEQS 16384
+la_status la_fwd_noalloc(const la_dims *dims, int32_t dtype,
+                         const void *q, const void *k, const void *v,
+                         const float *g_gamma, float scale,
+                         const float *initial_state, int32_t reverse,
+                         const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                         void *o, float *final_state, void *stream);
+
 /* Bytes of device workspace for the longest-first schedule of num_seqs packed
  * sequences (0 when num_seqs < 1).  Pure host function. */
 size_t la_workspace_size(int32_t num_seqs);

@@ -19,6 +19,8 @@ LA_ERR_TIMEOUT = 4
 LA_DTYPE_BF16 = 0
 LA_DTYPE_F32 = 1
 
+LA_FWD_NOALLOC_MAX_SEQS = 16384   # include/la.h
+
 
 class LaDims(ctypes.Structure):
     """Mirror of `la_dims` (include/la.h)."""
@@ -66,6 +68,8 @@ PROTOTYPES = {
     "la_bwd_dkdv": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32,
                            _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "la_workspace_size": (_sz, [_i32]),
+    "la_fwd_noalloc": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _vp,
+                              _vp, _vp, _vp]),
     "la_get_device_error": (_i32, [_vp]),
     "la_strerror": (ctypes.c_char_p, [_i32]),
     "la_last_error": (ctypes.c_char_p, []),

@@ -43,6 +43,12 @@ la_status fail(la_status st, const char *fmt, ...)
     return st;
 }
 
+}  // namespace
+
+void la::set_last_error(const char *msg) { g_msg = msg; }
+
+namespace {
+
 la_status cuda_fail(cudaError_t e, const char *where)
 {
     return fail(LA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));

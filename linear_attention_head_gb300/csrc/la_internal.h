@@ -64,6 +64,9 @@ struct SweepArgs {
 // Host-side count of enqueued kernels (la_launch_count).
 void note_launch();
 
+// Sets the message la_last_error returns on this host thread.
+void set_last_error(const char *msg);
+
 // CUDA-core kernels: any D, E in 1..256, bf16 or fp32, every flag.
 cudaError_t simt_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t simt_backward_sweep(const SweepArgs &a, cudaStream_t s);
