@@ -290,6 +290,8 @@ def gpu_bench(args):
         "e2e": e2e,
         "wall_s_timed": t_wall,
     }
+    if not args.no_sweep:
+        line["sweep"] = length_sweep(la, torch, dev, stream, T)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.n, args.cpu_pairs)
     if rank == 0:
@@ -298,6 +300,47 @@ def gpu_bench(args):
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+def length_sweep(la, torch, dev, stream, skip_n):
+    """fwd and bwd times at every length of the Lightning-2 benchmark table (b4 h32
+    d=e=128 bf16), each timed over 5 calls after 3 warm-up calls; inputs of the
+    largest lengths exceed L2, the smaller ones are flushed between calls."""
+    import workloads as W
+    out = {}
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for n in W.SWEEP_LENGTHS:
+        if n == skip_n:
+            continue
+        w = W.sweep_bf16(n)
+        gen = torch.Generator(device=dev).manual_seed(7)
+        q, k, v, do = (torch.randn((w.B, n, w.H, w.d), generator=gen, device=dev).bfloat16()
+                       for _ in range(4))
+        g = w.g_gamma.to(dev)
+        small = 4 * w.B * n * w.H * w.d * 2 < 2 * 129e6
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            tot = 0.0
+            for _ in range(5):
+                if small:
+                    flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+            return tot / 5
+
+        f_ms = timed(lambda: la.la_fwd(q, k, v, g, w.scale))
+        b_ms = timed(lambda: la.la_bwd(q, k, v, do, g, w.scale, want_d_initial_state=False))
+        tps = w.B * n / ((f_ms + b_ms) * 1e-3)
+        out[str(n)] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "tokens_per_s": tps,
+                       "vs_pages": tps / PAGES_TOKENS_PER_S[n], "l2_flushed": small}
+        del q, k, v, do
+    return out
 
 
 def source_sha():
@@ -397,6 +440,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=None)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":

@@ -199,6 +199,14 @@ size_t la_workspace_size(int32_t num_seqs);
  * every stream of the current device. */
 la_status la_get_device_error(void *stream);
 
+/* Diagnostic, for testing error reporting: with on != 0, the next
+ * tensor-core launch made from this host thread withholds one internal
+ * hand-off between its warps, so that a bounded on-device wait runs out
+ * (after about 2 s); the kernel then stops, frees what it holds and returns,
+ * its outputs are undefined, and la_get_device_error reports LA_ERR_TIMEOUT.
+ * The switch resets itself after that launch and is off by default. */
+la_status la_debug_withhold_next_handoff(int32_t on);
+
 /* Static description of a status code (never NULL). */
 const char *la_strerror(int32_t status);
 

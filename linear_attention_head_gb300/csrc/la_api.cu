@@ -31,6 +31,7 @@ void la::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 namespace {
 
 thread_local std::string g_msg;
+thread_local int g_withhold = 0;   // la_debug_withhold_next_handoff
 
 la_status fail(la_status st, const char *fmt, ...)
 {
@@ -189,8 +190,12 @@ la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, cons
 la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    if (la::tc_sweep_supported(a))
-        e = la::tc_forward_sweep(a, s);
+    if (la::tc_sweep_supported(a)) {
+        la::SweepArgs b = a;
+        b.withhold_handoff = g_withhold;
+        g_withhold = 0;
+        e = la::tc_forward_sweep(b, s);
+    }
     // cudaErrorNotSupported: the tensor maps could not be encoded for this layout
     if (e == cudaErrorNotSupported)
         e = la::simt_forward_sweep(a, s);
@@ -200,8 +205,12 @@ la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 la_status run_backward_type(const la::SweepArgs &a, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    if (la::tc_sweep_supported(a))
-        e = la::tc_backward_sweep(a, s);
+    if (la::tc_sweep_supported(a)) {
+        la::SweepArgs b = a;
+        b.withhold_handoff = g_withhold;
+        g_withhold = 0;
+        e = la::tc_backward_sweep(b, s);
+    }
     if (e == cudaErrorNotSupported)
         e = la::simt_backward_sweep(a, s);
     return e == cudaSuccess ? LA_OK : cuda_fail(e, "backward-type sweep launch");
@@ -432,6 +441,12 @@ int32_t la_kernel_family(const la_dims *dims, int32_t dtype)
 }
 
 size_t la_workspace_size(int32_t num_seqs) { return schedule_bytes(num_seqs); }
+
+la_status la_debug_withhold_next_handoff(int32_t on)
+{
+    g_withhold = on ? 1 : 0;
+    return LA_OK;
+}
 
 uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

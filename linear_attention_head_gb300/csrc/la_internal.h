@@ -59,6 +59,7 @@ struct SweepArgs {
     TokOut out;               // forward-type: o (or dq); backward-type: dv (or dk)
     StateIn s_in;             // forward-type: initial state; backward-type: dL/dfinal
     StateOut s_out;           // forward-type: final state; backward-type: dL/dinitial
+    int withhold_handoff;     // diagnostic: tensor-core kernels skip one hand-off
 };
 
 // Host-side count of enqueued kernels (la_launch_count).

@@ -439,7 +439,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(p_ready);
+                if (!(a.withhold_handoff && c == 0))   // diagnostic: let the MMA wait run out
+                    mbar_arrive(p_ready);
             }
         } else if (warp < 14) {
             // ------------------------------------------------------- S group
