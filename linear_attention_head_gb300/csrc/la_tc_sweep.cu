@@ -27,12 +27,17 @@
 //                 each chunk: S -> bf16 copy (B operand of the next X S) and
 //                 S * gamma^Lc(next) back into TMEM, where the next update
 //                 accumulates
-//   warps 14..17  O group: one thread per token row; o = P Z + lrow * X S
+//   warps 14..17  O group: one thread per token row; o = P Z + lrow * X S,
+//                 written as bf16 into the X tile of the finished stage and
+//                 sent out with one TMA store (the last chunk of a packed
+//                 sequence, whose tile would overrun into the next sequence,
+//                 is stored row by row instead)
 // TMEM (512 columns): scores/P [0,128), X S [128,256), P Z [256,384),
 // S [384,512) (value columns: E of them).  MMA order per chunk: scores and
 // X S as soon as the tiles land; then, once P is written, the state update
 // and P Z.  A ring stage is held only from landing to that last MMA, which is
-// what bounds the memory pipeline with two 96 KB stages.
+// what bounds the memory pipeline with two 96 KB stages; it is released when
+// that MMA and the store of the output tile out of its X slot have finished.
 //
 // Every mbarrier wait is bounded (2 s); on expiry the CTA raises a shared
 // abort flag and records LA_ERR_TIMEOUT in a device word, drains its own
@@ -77,14 +82,16 @@ template <int E> struct TcLayout {
     static constexpr int MOFF = SOFF + SB;
     static constexpr int NBAR = 2 * TC_NST + 12;
     static constexpr int PWOFF = MOFF + NBAR * 8;
-    static constexpr int SLOTOFF = PWOFF + (TC_C + 1) * 4;
+    static constexpr int CFOFF = (PWOFF + (TC_C + 1) * 4 + 15) / 16 * 16;   // 32 column factors
+    static constexpr int DTOFF = CFOFF + 32 * 4;                            // 64 diagonal factors
+    static constexpr int SLOTOFF = DTOFF + 64 * 4;
     static constexpr int ABORTOFF = SLOTOFF + 4;
     static constexpr int BYTES = ABORTOFF + 4;
     static constexpr int DYN = BYTES + 1024;           // slack for 1024-byte alignment
 };
 
 struct TcParams {
-    CUtensorMap mx, my, mz;
+    CUtensorMap mx, my, mz, mo;
     SweepArgs a;
 };
 
@@ -167,6 +174,20 @@ __device__ __forceinline__ void store_row_sw128(uint8_t *row_base, int row,
     }
 }
 
+// 32 fp32 (as bits) -> 16-byte chunks 4*half .. 4*half+3 of a 128-byte row of
+// a 128B-swizzled bf16 tile.
+__device__ __forceinline__ void store_half_row_sw128(uint8_t *row_base, int row, int half,
+                                                     const uint32_t (&x)[32])
+{
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4)
+        *reinterpret_cast<uint4 *>(row_base + (((4 * half + k4) ^ (row & 7)) << 4)) = make_uint4(
+            pack_bf16x2(__uint_as_float(x[8 * k4 + 0]), __uint_as_float(x[8 * k4 + 1])),
+            pack_bf16x2(__uint_as_float(x[8 * k4 + 2]), __uint_as_float(x[8 * k4 + 3])),
+            pack_bf16x2(__uint_as_float(x[8 * k4 + 4]), __uint_as_float(x[8 * k4 + 5])),
+            pack_bf16x2(__uint_as_float(x[8 * k4 + 6]), __uint_as_float(x[8 * k4 + 7])));
+}
+
 // 32 fp32 (as bits) -> 32 bf16 at dst (4 x 16-byte stores).
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t (&x)[32])
 {
@@ -177,6 +198,55 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t
             pack_bf16x2(__uint_as_float(x[8 * c16 + 2]), __uint_as_float(x[8 * c16 + 3])),
             pack_bf16x2(__uint_as_float(x[8 * c16 + 4]), __uint_as_float(x[8 * c16 + 5])),
             pack_bf16x2(__uint_as_float(x[8 * c16 + 6]), __uint_as_float(x[8 * c16 + 7])));
+}
+
+// One 32-key block of P for the 32 rows of a warp, on a full chunk.  The
+// decay of the chunk's 128 x 128 mask, cut into 32 x 32 blocks, is per block
+// either zero (the wrong side of the diagonal), a diagonal block, or the
+// product of a row factor and a column factor: gamma^(i-j) =
+// gamma^(32(q-b)+lane-31) gamma^(31-jj) below the diagonal (row quarter q, key
+// block b, jj = j - 32b), and gamma^(32(b-q)-lane) gamma^jj above it, every
+// factor <= 1.  Diagonal blocks take gamma^|lane-jj| (zero on the masked side)
+// from a 63-entry table indexed by jj - lane + 31.  scale is folded into the
+// row factor and the table.  r holds the block's 32 scores; packed pair m of P
+// goes into r[2m].
+__device__ __forceinline__ void p_block_full(uint32_t (&r)[32], int kind, float rf, const float *cf,
+                                             const float *dt, int lane)
+{
+    if (kind == 0) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+            r[2 * m] = 0u;
+    } else if (kind == 1) {
+        const float2 rr = make_float2(rf, rf);
+        const uint32_t cfa = smem_u32(cf);
+#pragma unroll
+        for (int m4 = 0; m4 < 8; ++m4) {
+            float4 c;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(c.x), "=f"(c.y), "=f"(c.z), "=f"(c.w)
+                         : "r"(cfa + 16 * m4));
+            const float2 v0 = mul_f32x2(
+                mul_f32x2(make_float2(__uint_as_float(r[4 * m4]), __uint_as_float(r[4 * m4 + 1])),
+                          make_float2(c.x, c.y)),
+                rr);
+            const float2 v1 = mul_f32x2(
+                mul_f32x2(make_float2(__uint_as_float(r[4 * m4 + 2]), __uint_as_float(r[4 * m4 + 3])),
+                          make_float2(c.z, c.w)),
+                rr);
+            r[4 * m4] = pack_bf16x2(v0.x, v0.y);
+            r[4 * m4 + 2] = pack_bf16x2(v1.x, v1.y);
+        }
+    } else {
+        const float *d = dt + 31 - lane;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float2 v = mul_f32x2(
+                make_float2(__uint_as_float(r[2 * m]), __uint_as_float(r[2 * m + 1])),
+                make_float2(d[2 * m], d[2 * m + 1]));
+            r[2 * m] = pack_bf16x2(v.x, v.y);
+        }
+    }
 }
 
 template <int E, bool BWD>
@@ -197,7 +267,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     uint64_t *ds_full = sc_full + 5;         // state update (and X S) done
     uint64_t *o_full = sc_full + 6;          // P Z (and X S) done
     uint64_t *drain = sc_full + 7;
+    uint64_t *o_tile = sc_full + 8;          // output tile written to shared memory
     float *pw = reinterpret_cast<float *>(sm + L::PWOFF);
+    float *cf = reinterpret_cast<float *>(sm + L::CFOFF);
+    float *dt = reinterpret_cast<float *>(sm + L::DTOFF);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::SLOTOFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::ABORTOFF);
 
@@ -229,7 +302,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     if (threadIdx.x == 0) {
         for (int i = 0; i < TC_NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], 2);   // last MMA of the chunk + output store
         }
         mbar_init(sc_full, 1);
         mbar_init(pv_done, 1);
@@ -239,6 +312,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         mbar_init(ds_full, 1);
         mbar_init(o_full, 1);
         mbar_init(drain, 1);
+        mbar_init(o_tile, TC_OG);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -250,6 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         prefetch_tmap(&P.mx);
         prefetch_tmap(&P.my);
         prefetch_tmap(&P.mz);
+        prefetch_tmap(&P.mo);
     }
     tc_fence_before();
     __syncthreads();
@@ -353,6 +428,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         const float scale = a.scale;
         for (int m = et; m <= TC_C; m += TC_PG + TC_SG + TC_OG)
             pw[m] = m == 0 ? 1.f : expf(g * (float)m);
+        if (et < 32) {   // column factors of the off-diagonal blocks
+            const int m = flip ? et : 31 - et;
+            cf[et] = m == 0 ? 1.f : expf(g * (float)m);
+        } else if (et < 96) {   // diagonal blocks, index jj - lane + 31
+            const int u = et - 32;
+            const int m = flip ? u - 31 : 31 - u;
+            dt[u] = m < 0 || u > 62 ? 0.f : (m == 0 ? scale : scale * expf(g * (float)m));
+        }
         epi_bar_sync();
         const int q = warp & 3;
         const int i = 32 * q + lane;   // TMEM lane = tile row
@@ -362,7 +445,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // ------------------------------------------------------- P group
             const int hh = (warp - 2) >> 2;
             const int j0 = 64 * hh;
-            const float gam = pw[1];
             for (int c = 0; c < nc; ++c) {
                 const int s = c % TC_NST;
                 const int Lc = chunk_len(c);
@@ -374,53 +456,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 tc_fence_after();
                 uint32_t ra[32], rb[32];
                 const uint32_t col = tm + lane_off + TM_SC + j0;
+                // block kinds are warp-uniform: 0 zero, 1 rank one, 2 diagonal
+                const int b0 = 2 * hh, b1 = b0 + 1;
+                const int k0 = b0 == q ? 2 : ((flip ? b0 > q : b0 < q) ? 1 : 0);
+                const int k1 = b1 == q ? 2 : ((flip ? b1 > q : b1 < q) ? 1 : 0);
                 tmem_ld32_issue(col, ra);
                 tmem_ld32_issue(col + 32, rb);
                 tmem_wait_ld(ra, rb);
-                // decay gamma^d, d = |p(i) - p(j)|, walked with a running product
-                // along the row (at most 127 steps) instead of a table load per
-                // element; masked entries are zero.  Each packed pair of P goes
-                // into the even register slot it was read from.
-                if (!flip) {
-                    // keep j <= i (< Lc); d = i - j grows as j falls
-                    int d = i - (j0 + 63);
-                    float w = pw[d > 0 ? d : 0];
-                    const float sc = i < Lc ? scale : 0.f;
+                const float rf0 =
+                    k0 == 1 ? scale * pw[flip ? 32 * (b0 - q) - lane : 32 * (q - b0) + lane - 31] : 0.f;
+                const float rf1 =
+                    k1 == 1 ? scale * pw[flip ? 32 * (b1 - q) - lane : 32 * (q - b1) + lane - 31] : 0.f;
+                p_block_full(ra, k0, rf0, cf, dt, lane);
+                p_block_full(rb, k1, rf1, cf, dt, lane);
+                if (Lc < TC_C) {
+                    // the sequence ends inside this chunk: rows past the end
+                    // (forward order) or keys past it (reverse order) are zero
+                    if (!flip) {
+                        if (i >= Lc) {
 #pragma unroll
-                    for (int jj = 63; jj >= 0; jj -= 2) {
-                        const float x1 = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
-                        const float x0 = __uint_as_float(jj < 32 ? ra[jj - 1] : rb[jj - 33]);
-                        const float v1 = d >= 0 ? sc * x1 * w : 0.f;
-                        w = d >= 0 ? w * gam : w;
-                        ++d;
-                        const float v0 = d >= 0 ? sc * x0 * w : 0.f;
-                        w = d >= 0 ? w * gam : w;
-                        ++d;
-                        const uint32_t pk = pack_bf16x2(v0, v1);
-                        if (jj < 32)
-                            ra[jj - 1] = pk;   // slot just consumed
-                        else
-                            rb[jj - 33] = pk;
-                    }
-                } else {
-                    // keep j >= i, j < Lc; d = j - i grows with j
-                    int d = j0 - i;
-                    float w = pw[d > 0 ? d : 0];
+                            for (int m = 0; m < 16; ++m)
+                                ra[2 * m] = rb[2 * m] = 0u;
+                        }
+                    } else {
 #pragma unroll
-                    for (int jj = 0; jj < 64; jj += 2) {
-                        const float x0 = __uint_as_float(jj < 32 ? ra[jj] : rb[jj - 32]);
-                        const float x1 = __uint_as_float(jj < 32 ? ra[jj + 1] : rb[jj - 31]);
-                        const float v0 = d >= 0 && j0 + jj < Lc ? scale * x0 * w : 0.f;
-                        w = d >= 0 ? w * gam : w;
-                        ++d;
-                        const float v1 = d >= 0 && j0 + jj + 1 < Lc ? scale * x1 * w : 0.f;
-                        w = d >= 0 ? w * gam : w;
-                        ++d;
-                        const uint32_t pk = pack_bf16x2(v0, v1);
-                        if (jj < 32)
-                            ra[jj] = pk;   // slot just consumed
-                        else
-                            rb[jj - 32] = pk;
+                        for (int m = 0; m < 16; ++m) {
+                            const int ja = j0 + 2 * m, jb = j0 + 32 + 2 * m;
+                            ra[2 * m] &= (ja < Lc ? 0xffffu : 0u) | (ja + 1 < Lc ? 0xffff0000u : 0u);
+                            rb[2 * m] &= (jb < Lc ? 0xffffu : 0u) | (jb + 1 < Lc ? 0xffff0000u : 0u);
+                        }
                     }
                 }
                 // P for the keys of this half: 32 packed columns inside the
@@ -525,7 +589,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // ------------------------------------------------------- O group
             __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.out.p) + row * a.out.sb +
                                    (int64_t)h * a.out.sh;
+            const bool o_leader = warp == 14 && lane == 0;
+            int ntile = 0;
             for (int c = 0; c < nc; ++c) {
+                const int s = c % TC_NST;
                 const int Lc = chunk_len(c);
                 if (!warp_all(bwait(o_full, c & 1, abort_flag)))
                     break;
@@ -535,6 +602,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     const int pi = rev ? Lc - 1 - i : i;
                     lr = BWD ? pw[Lc - 1 - pi] : scale * pw[pi + 1];
                 }
+                // a tile store may run past the end of a dense sequence (the
+                // copy clips it) but not into the next packed sequence
+                const bool tile = Lc == TC_C || !a.cu;
+                uint8_t *otile = sm + s * L::STAGE;   // X slot, free once P Z is done
                 __nv_bfloat16 *orow = obase + (bos + chunk_t0(c) + i) * a.out.st;
 #pragma unroll 1
                 for (int part = 0; part < E / 32; ++part) {
@@ -546,11 +617,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     for (int k = 0; k < 32; ++k)
                         ra[k] = __float_as_uint(
                             fmaf(lr, __uint_as_float(ri[k]), __uint_as_float(ra[k])));
-                    if (i < Lc)
+                    if (tile)
+                        store_half_row_sw128(otile + (part >> 1) * (TC_C * 128) + i * 128, i,
+                                             part & 1, ra);
+                    else if (i < Lc)
                         store_bf16x32(orow + 32 * part, ra);
                 }
                 tc_fence_before();
-                mbar_arrive(o_free);
+                mbar_arrive(o_free);   // both accumulators read
+                if (tile) {
+                    fence_proxy_async_smem();   // the tile is visible to the copy engine
+                    mbar_arrive(o_tile);
+                    if (o_leader) {
+                        if (!bwait(o_tile, ntile & 1, abort_flag))
+                            break;
+#pragma unroll
+                        for (int b = 0; b < E / 64; ++b)
+                            tma_store_4d(&P.mo, otile + b * (TC_C * 128), 64 * b, h,
+                                         (int)(bos + chunk_t0(c)), (int)row);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                    }
+                    ++ntile;
+                }
+                if (o_leader)
+                    mbar_arrive(&empty[s]);   // the stage may be refilled
             }
         }
     }
@@ -618,7 +709,8 @@ template <int E, bool BWD> cudaError_t launch_tc(const SweepArgs &a, cudaStream_
     const Tok &x = BWD ? a.k : a.q, &y = BWD ? a.q : a.k;
     if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh) ||
         !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh) ||
-        !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh))
+        !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh) ||
+        !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh))
         return cudaErrorNotSupported;
     p.a = a;
     auto kern = tc_sweep_kernel<E, BWD>;
