@@ -267,7 +267,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     uint64_t *ds_full = sc_full + 5;         // state update (and X S) done
     uint64_t *o_full = sc_full + 6;          // P Z (and X S) done
     uint64_t *drain = sc_full + 7;
-    uint64_t *o_tile = sc_full + 8;          // output tile written to shared memory
     float *pw = reinterpret_cast<float *>(sm + L::PWOFF);
     float *cf = reinterpret_cast<float *>(sm + L::CFOFF);
     float *dt = reinterpret_cast<float *>(sm + L::DTOFF);
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     if (threadIdx.x == 0) {
         for (int i = 0; i < TC_NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 2);   // last MMA of the chunk + output store
+            mbar_init(&empty[i], 1 + TC_OG / 32);   // last MMA of the chunk + each O warp
         }
         mbar_init(sc_full, 1);
         mbar_init(pv_done, 1);
@@ -312,7 +311,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         mbar_init(ds_full, 1);
         mbar_init(o_full, 1);
         mbar_init(drain, 1);
-        mbar_init(o_tile, TC_OG);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -589,8 +587,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // ------------------------------------------------------- O group
             __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.out.p) + row * a.out.sb +
                                    (int64_t)h * a.out.sh;
-            const bool o_leader = warp == 14 && lane == 0;
-            int ntile = 0;
             for (int c = 0; c < nc; ++c) {
                 const int s = c % TC_NST;
                 const int Lc = chunk_len(c);
@@ -626,22 +622,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 tc_fence_before();
                 mbar_arrive(o_free);   // both accumulators read
                 if (tile) {
-                    fence_proxy_async_smem();   // the tile is visible to the copy engine
-                    mbar_arrive(o_tile);
-                    if (o_leader) {
-                        if (!bwait(o_tile, ntile & 1, abort_flag))
-                            break;
+                    // each warp sends its own 32 rows once they are visible to
+                    // the copy engine
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
 #pragma unroll
                         for (int b = 0; b < E / 64; ++b)
-                            tma_store_4d(&P.mo, otile + b * (TC_C * 128), 64 * b, h,
-                                         (int)(bos + chunk_t0(c)), (int)row);
+                            tma_store_4d(&P.mo, otile + b * (TC_C * 128) + q * 32 * 128, 64 * b, h,
+                                         (int)(bos + chunk_t0(c)) + 32 * q, (int)row);
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }
-                    ++ntile;
                 }
-                if (o_leader)
-                    mbar_arrive(&empty[s]);   // the stage may be refilled
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);   // this warp's part of the stage may be refilled
             }
         }
     }
@@ -675,9 +670,9 @@ bool aligned_tok(const void *p, int64_t sb, int64_t st, int64_t sh)
            sh % 8 == 0;
 }
 
-// 4-D map {channel, head, token, batch} with a {64, 1, 128, 1} box, 128-byte swizzle.
+// 4-D map {channel, head, token, batch} with a {64, 1, rows, 1} box, 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t sb, int64_t st,
-              int64_t sh)
+              int64_t sh, int rows = TC_C)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -692,7 +687,7 @@ bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t 
         return false;
     cuuint64_t dims[4] = {(cuuint64_t)X, (cuuint64_t)a.H, (cuuint64_t)a.T, (cuuint64_t)a.B};
     cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)st * 2, (cuuint64_t)sb * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)TC_C, 1};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p), dims, strides,
                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -710,7 +705,7 @@ template <int E, bool BWD> cudaError_t launch_tc(const SweepArgs &a, cudaStream_
     if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh) ||
         !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh) ||
         !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh) ||
-        !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh))
+        !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh, 32))
         return cudaErrorNotSupported;
     p.a = a;
     auto kern = tc_sweep_kernel<E, BWD>;
