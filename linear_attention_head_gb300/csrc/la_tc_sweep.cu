@@ -80,7 +80,7 @@ template <int E> struct TcLayout {
     static constexpr int SOFF = TC_NST * STAGE;       // bf16 copy of S, [E/64][D][64]
     static constexpr int SB = TC_D * E * 2;
     static constexpr int MOFF = SOFF + SB;
-    static constexpr int NBAR = 2 * TC_NST + 12;
+    static constexpr int NBAR = 3 * TC_NST + 12;
     static constexpr int PWOFF = MOFF + NBAR * 8;
     static constexpr int CFOFF = (PWOFF + (TC_C + 1) * 4 + 15) / 16 * 16;   // 32 column factors
     static constexpr int DTOFF = CFOFF + 32 * 4;                            // 64 diagonal factors
@@ -188,16 +188,39 @@ __device__ __forceinline__ void store_half_row_sw128(uint8_t *row_base, int row,
             pack_bf16x2(__uint_as_float(x[8 * k4 + 6]), __uint_as_float(x[8 * k4 + 7])));
 }
 
-// 32 fp32 (as bits) -> 32 bf16 at dst (4 x 16-byte stores).
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t (&x)[32])
+// Initial state row i, 8 columns at a time (once per CTA): fp32 from global
+// (any strides) -> bf16 into the swizzled S copy, and times g0 into TMEM.
+__device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i, int E_,
+                                         uint8_t *sbf, uint32_t tmem_row, float g0)
 {
+#pragma unroll 1
+    for (int p8 = 0; p8 < E_ / 8; ++p8) {
+        float x[8];
+        const float *src = sin.p ? sin.p + base + i * sin.rs + (8 * p8) * sin.cs : nullptr;
 #pragma unroll
-    for (int c16 = 0; c16 < 4; ++c16)
-        *reinterpret_cast<uint4 *>(dst + 8 * c16) = make_uint4(
-            pack_bf16x2(__uint_as_float(x[8 * c16 + 0]), __uint_as_float(x[8 * c16 + 1])),
-            pack_bf16x2(__uint_as_float(x[8 * c16 + 2]), __uint_as_float(x[8 * c16 + 3])),
-            pack_bf16x2(__uint_as_float(x[8 * c16 + 4]), __uint_as_float(x[8 * c16 + 5])),
-            pack_bf16x2(__uint_as_float(x[8 * c16 + 6]), __uint_as_float(x[8 * c16 + 7])));
+        for (int k = 0; k < 8; ++k)
+            x[k] = src ? src[k * sin.cs] : 0.f;
+        *reinterpret_cast<uint4 *>(sbf + (p8 >> 3) * (TC_D * 128) + (((p8 & 7) ^ (i & 7)) << 4)) =
+            make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                       pack_bf16x2(x[6], x[7]));
+        uint32_t r[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            r[k] = __float_as_uint(g0 * x[k]);
+        tmem_st8(tmem_row + 8 * p8, r);
+    }
+}
+
+// Empty sequence: initial state row i (zero when absent) -> final state row i.
+__device__ __forceinline__ void state_copy(const StateIn &sin, const StateOut &sout, int64_t base,
+                                           int i, int E_)
+{
+    if (!sout.p)
+        return;
+#pragma unroll 1
+    for (int k = 0; k < E_; ++k)
+        sout.p[base + i * sout.rs + k * sout.cs] =
+            sin.p ? sin.p[base + i * sin.rs + k * sin.cs] : 0.f;
 }
 
 // One 32-key block of P for the 32 rows of a warp, on a full chunk.  The
@@ -258,8 +281,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                                               ~static_cast<uintptr_t>(1023));
     const SweepArgs &a = P.a;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::MOFF);
-    uint64_t *full = bars, *empty = bars + TC_NST;
-    uint64_t *sc_full = bars + 2 * TC_NST;   // scores of the chunk are in TMEM
+    // full: the stage's three tiles landed; empty: its Y and Z slots are free
+    // (last MMA of the chunk done); xfree: its X slot is free (every O warp
+    // has stored its rows of the output tile out of it)
+    uint64_t *full = bars, *empty = bars + TC_NST, *xfree = bars + 2 * TC_NST;
+    uint64_t *sc_full = bars + 3 * TC_NST;   // scores of the chunk are in TMEM
     uint64_t *pv_done = sc_full + 1;         // P consumed (scores columns free)
     uint64_t *p_ready = sc_full + 2;         // P written, Y scaled
     uint64_t *s_ready = sc_full + 3;         // bf16 S written, TMEM S pre-scaled
@@ -301,7 +327,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     if (threadIdx.x == 0) {
         for (int i = 0; i < TC_NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1 + TC_OG / 32);   // last MMA of the chunk + each O warp
+            mbar_init(&empty[i], 1);
+            mbar_init(&xfree[i], TC_OG / 32);
         }
         mbar_init(sc_full, 1);
         mbar_init(pv_done, 1);
@@ -335,14 +362,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             int issued = 0;
             for (int c = 0; c < nc; ++c) {
                 const int s = c % TC_NST;
-                if (c >= TC_NST && !bwait(&empty[s], ((c / TC_NST) - 1) & 1, abort_flag))
+                const uint32_t ph = ((c / TC_NST) - 1) & 1;
+                if (c >= TC_NST && !bwait(&empty[s], ph, abort_flag))
                     break;
                 const int t0 = (int)(bos + chunk_t0(c));
                 uint8_t *st = sm + s * L::STAGE;
                 mbar_arrive_expect_tx(&full[s], L::STAGE);
-#pragma unroll
-                for (int b = 0; b < TC_D / 64; ++b)
-                    tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, h, t0, (int)row);
+                // Y and Z first: their slots are free once the chunk's MMAs are
+                // done, the X slot only once the output tile has left it
 #pragma unroll
                 for (int b = 0; b < TC_D / 64; ++b)
                     tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, h, t0,
@@ -351,7 +378,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 for (int b = 0; b < E / 64; ++b)
                     tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s], 64 * b, h,
                                 t0, (int)row);
+                // X is copied even when this wait gives up, so that the drain
+                // below sees the stage complete
+                const bool xok = c < TC_NST || bwait(&xfree[s], ph, abort_flag);
+#pragma unroll
+                for (int b = 0; b < TC_D / 64; ++b)
+                    tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, h, t0, (int)row);
                 ++issued;
+                if (!xok)
+                    break;
             }
             // every copy this thread issued has landed before the CTA may exit
             for (int c = issued > TC_NST ? issued - TC_NST : 0; c < issued; ++c)
@@ -508,44 +543,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // ------------------------------------------------------- S group
             const int64_t sb = ((int64_t)n * a.H + h) * (int64_t)a.D * a.E;
             uint8_t *sbf = sm + L::SOFF + i * 128;
-            // initial state: bf16 copy and gamma^L0-scaled fp32 in TMEM
-            {
-                const float g0 = nc > 0 ? pw[chunk_len(0)] : 1.f;
-#pragma unroll 1
-                for (int eb = 0; eb < E / 64; ++eb) {
-                    uint32_t ra[32], rb[32];
-                    const float *src =
-                        a.s_in.p ? a.s_in.p + sb + i * a.s_in.rs + 64 * eb * a.s_in.cs : nullptr;
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        ra[k] = __float_as_uint(src ? src[k * a.s_in.cs] : 0.f);
-                        rb[k] = __float_as_uint(src ? src[(k + 32) * a.s_in.cs] : 0.f);
-                    }
-                    if (nc == 0) {
-                        if (a.s_out.p) {
-                            float *dst = a.s_out.p + sb + i * a.s_out.rs + 64 * eb * a.s_out.cs;
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) {
-                                dst[k * a.s_out.cs] = __uint_as_float(ra[k]);
-                                dst[(k + 32) * a.s_out.cs] = __uint_as_float(rb[k]);
-                            }
-                        }
-                        continue;
-                    }
-                    store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        ra[k] = __float_as_uint(g0 * __uint_as_float(ra[k]));
-                        rb[k] = __float_as_uint(g0 * __uint_as_float(rb[k]));
-                    }
-                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb, ra);
-                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb + 32, rb);
-                    tmem_wait_st();
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(s_ready);
-            }
+            // initial state: bf16 copy and gamma^L0-scaled fp32 in TMEM (an
+            // empty sequence passes it straight to the final state)
+            if (nc == 0)
+                state_copy(a.s_in, a.s_out, sb, i, E);
+            else
+                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, pw[chunk_len(0)]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(s_ready);
             for (int c = 0; c < nc; ++c) {
                 if (!warp_all(bwait(ds_full, c & 1, abort_flag)))
                     break;
@@ -613,11 +619,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     for (int k = 0; k < 32; ++k)
                         ra[k] = __float_as_uint(
                             fmaf(lr, __uint_as_float(ri[k]), __uint_as_float(ra[k])));
-                    if (tile)
-                        store_half_row_sw128(otile + (part >> 1) * (TC_C * 128) + i * 128, i,
-                                             part & 1, ra);
-                    else if (i < Lc)
-                        store_bf16x32(orow + 32 * part, ra);
+                    store_half_row_sw128(otile + (part >> 1) * (TC_C * 128) + i * 128, i, part & 1,
+                                         ra);
                 }
                 tc_fence_before();
                 mbar_arrive(o_free);   // both accumulators read
@@ -634,9 +637,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }
+                } else if (i < Lc) {
+                    // row by row: this thread's own row, back out of the tile
+#pragma unroll 1
+                    for (int c16 = 0; c16 < E / 8; ++c16)
+                        *reinterpret_cast<uint4 *>(orow + 8 * c16) = *reinterpret_cast<const uint4 *>(
+                            otile + (c16 >> 3) * (TC_C * 128) + i * 128 + (((c16 & 7) ^ (i & 7)) << 4));
                 }
+                __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&empty[s]);   // this warp's part of the stage may be refilled
+                    mbar_arrive(&xfree[s]);   // this warp's rows of the X slot may be refilled
             }
         }
     }
