@@ -238,14 +238,32 @@ def gpu_bench(args):
                  torch.empty((B, T, H, E), dtype=torch.bfloat16).pin_memory(),
                  torch.empty((B, H, D, E), dtype=torch.float32).pin_memory()]
 
+        # One batch row at a time on three streams, so that the copies of
+        # neighbouring rows overlap the compute of this one: host-to-device
+        # (q, k, v, do of row b), compute (la_fwd, la_bwd of row b), and
+        # device-to-host (o, dq, dk, dv, final_state of row b).
+        s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
         def e2e_step():
-            dq_, dk_, dv_ = (hq.to(dev, non_blocking=True), hk.to(dev, non_blocking=True),
-                             hv.to(dev, non_blocking=True))
-            ddo = hdo.to(dev, non_blocking=True)
-            o, fin = la.la_fwd(dq_, dk_, dv_, g, scale)
-            gq, gk, gv, _ = la.la_bwd(dq_, dk_, dv_, ddo, g, scale, want_d_initial_state=False)
-            for h, d_ in zip(houts, (o, gq, gk, gv, fin)):
-                h.copy_(d_, non_blocking=True)
+            for b in range(B):
+                with torch.cuda.stream(s_in):
+                    xb = [t[b:b + 1].to(dev, non_blocking=True) for t in (hq, hk, hv, hdo)]
+                    ev_in = torch.cuda.Event()
+                    ev_in.record(s_in)
+                with torch.cuda.stream(s_cmp):
+                    s_cmp.wait_event(ev_in)
+                    for t in xb:
+                        t.record_stream(s_cmp)
+                    o, fin = la.la_fwd(xb[0], xb[1], xb[2], g, scale)
+                    gq, gk, gv, _ = la.la_bwd(xb[0], xb[1], xb[2], xb[3], g, scale,
+                                              want_d_initial_state=False)
+                    ev_cmp = torch.cuda.Event()
+                    ev_cmp.record(s_cmp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_cmp)
+                    for h, d_ in zip(houts, (o, gq, gk, gv, fin)):
+                        d_.record_stream(s_out)
+                        h[b:b + 1].copy_(d_, non_blocking=True)
 
         for _ in range(max(1, min(args.warmup, 2))):
             e2e_step()
@@ -254,15 +272,19 @@ def gpu_bench(args):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
+        s_in.wait_stream(stream)
         for _ in range(ke):
             e2e_step()
+        stream.wait_stream(s_out)
         t1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(t0.elapsed_time(t1), ws, dev)
         bi = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
         bo = sum(t.numel() * t.element_size() for t in houts)
         e2e = {"value": ws * tokens_step * ke / (e_ms * 1e-3), "unit": "tokens/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": ke}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": ke,
+               "schedule": "per batch row: copy in, la_fwd + la_bwd, copy out, on three "
+                           "streams (rows overlap)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
@@ -304,11 +326,14 @@ def gpu_bench(args):
 
 def length_sweep(la, torch, dev, stream, skip_n):
     """fwd and bwd times at every length of the Lightning-2 benchmark table (b4 h32
-    d=e=128 bf16), each timed over 5 calls after 3 warm-up calls; inputs of the
-    largest lengths exceed L2, the smaller ones are flushed between calls."""
+    d=e=128 bf16), each the mean of 5 calls after 3 warm-up calls.  The GPU is first
+    held busy (torch.cuda._sleep) so that all 5 calls are queued before the first
+    runs and host-side call overhead stays out of the events.  Lengths whose four
+    token tensors fit twice in L2 are timed with a 512 MB L2 flush before each call
+    (`fwd_ms`, `bwd_ms`) and also back to back without one (`*_unflushed`)."""
     import workloads as W
     out = {}
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     for n in W.SWEEP_LENGTHS:
         if n == skip_n:
             continue
@@ -319,26 +344,32 @@ def length_sweep(la, torch, dev, stream, skip_n):
         g = w.g_gamma.to(dev)
         small = 4 * w.B * n * w.H * w.d * 2 < 2 * 129e6
 
-        def timed(fn):
+        def timed(fn, flush_first):
             for _ in range(3):
                 fn()
-            tot = 0.0
+            torch.cuda.synchronize()
+            evs = []
+            torch.cuda._sleep(20_000_000)
             for _ in range(5):
-                if small:
+                if flush_first:
                     flush.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 fn()
                 e1.record(stream)
-                torch.cuda.synchronize()
-                tot += e0.elapsed_time(e1)
-            return tot / 5
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            return sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
 
-        f_ms = timed(lambda: la.la_fwd(q, k, v, g, w.scale))
-        b_ms = timed(lambda: la.la_bwd(q, k, v, do, g, w.scale, want_d_initial_state=False))
+        fwd = lambda: la.la_fwd(q, k, v, g, w.scale)
+        bwd = lambda: la.la_bwd(q, k, v, do, g, w.scale, want_d_initial_state=False)
+        f_ms, b_ms = timed(fwd, small), timed(bwd, small)
         tps = w.B * n / ((f_ms + b_ms) * 1e-3)
         out[str(n)] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "tokens_per_s": tps,
                        "vs_pages": tps / PAGES_TOKENS_PER_S[n], "l2_flushed": small}
+        if small:
+            out[str(n)]["fwd_ms_unflushed"] = timed(fwd, False)
+            out[str(n)]["bwd_ms_unflushed"] = timed(bwd, False)
         del q, k, v, do
     return out
 

@@ -33,7 +33,7 @@ def test_small_bf16_fwd_bwd(reverse):
     compare(got, oracle_run(x, reverse), TOL[torch.bfloat16], label=w.name)
 
 
-@pytest.mark.parametrize("n", [512, 2048])
+@pytest.mark.parametrize("n", [512, 1024, 2048, 4096])
 def test_sweep_shape_full_compare(n):
     w = W.sweep_bf16(n)
     x = W.make_inputs(w, seed=0)
@@ -43,7 +43,7 @@ def test_sweep_shape_full_compare(n):
             label=w.name)
 
 
-@pytest.mark.parametrize("n", [8192, 32768])
+@pytest.mark.parametrize("n", [8192, 16384, 32768])
 def test_sweep_shape_sampled(n):
     w = W.sweep_bf16(n)
     x = W.make_inputs(w, seed=0)
