@@ -215,9 +215,12 @@ const char *la_strerror(int32_t status);
 const char *la_last_error(void);
 
 /* Which kernel family la_fwd would launch for these sizes and dtype, assuming
- * 16-byte aligned base pointers: 1 = tensor-core (tcgen05) chunked kernels,
- * 0 = CUDA-core chunked kernels, -1 = invalid or unsupported.  Pure host
- * function; launches nothing. */
+ * 16-byte aligned base pointers: 2 = token-by-token kernels (every sequence
+ * at most 16 tokens long: decoding a few tokens against a carried state),
+ * 1 = tensor-core (tcgen05) chunked kernels, 0 = CUDA-core chunked kernels,
+ * -1 = invalid or unsupported.  The sequence length is dims->seq_len; with
+ * cu_seqlens the longest packed sequence decides, which this function does
+ * not see.  Pure host function; launches nothing. */
 int32_t la_kernel_family(const la_dims *dims, int32_t dtype);
 
 /* Number of kernels this library has enqueued since it was loaded (all

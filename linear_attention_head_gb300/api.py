@@ -253,7 +253,8 @@ def get_device_error(device=None) -> None:
 
 
 def kernel_family(B, T, H, D, E, dtype=torch.bfloat16, layout="bthd") -> int:
-    """1 = tensor-core kernels, 0 = CUDA-core kernels, -1 = unsupported."""
+    """2 = token-by-token kernels (T <= 16), 1 = tensor-core chunked kernels,
+    0 = CUDA-core chunked kernels, -1 = unsupported."""
     d = N.LaDims()
     d.batch, d.seq_len, d.heads, d.dim_qk, d.dim_v, d.num_seqs = B, T, H, D, E, 0
     if layout == "bthd":

@@ -184,13 +184,21 @@ la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, cons
     a.scale = scale;
     a.reverse = reverse ? 1 : 0;
     a.bf16 = dtype == LA_DTYPE_BF16;
+    a.max_len = P.T;
+    if (P.packed) {
+        a.max_len = 0;
+        for (int n = 0; n < P.N; ++n)
+            a.max_len = std::max<int64_t>(a.max_len, P.cu_host[(size_t)n + 1] - P.cu_host[(size_t)n]);
+    }
     return a;
 }
 
 la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    if (la::tc_sweep_supported(a)) {
+    if (a.max_len <= la::SHORT_MAX_T)
+        e = la::short_forward_sweep(a, s);
+    if (e == cudaErrorNotSupported && la::tc_sweep_supported(a)) {
         la::SweepArgs b = a;
         b.withhold_handoff = g_withhold;
         g_withhold = 0;
@@ -205,7 +213,9 @@ la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 la_status run_backward_type(const la::SweepArgs &a, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    if (la::tc_sweep_supported(a)) {
+    if (a.max_len <= la::SHORT_MAX_T)
+        e = la::short_backward_sweep(a, s);
+    if (e == cudaErrorNotSupported && la::tc_sweep_supported(a)) {
         la::SweepArgs b = a;
         b.withhold_handoff = g_withhold;
         g_withhold = 0;
@@ -437,6 +447,8 @@ int32_t la_kernel_family(const la_dims *dims, int32_t dtype)
     a.k = tok(nullptr, dims->qk_strides);
     a.v = tok(nullptr, dims->v_strides);
     a.out = tok_out(nullptr, dims->v_strides);
+    if (a.max_len <= la::SHORT_MAX_T && P.D <= 256)
+        return 2;
     return la::tc_sweep_supported(a) ? 1 : 0;
 }
 
@@ -450,6 +462,6 @@ la_status la_debug_withhold_next_handoff(int32_t on)
 
 uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int32_t la_version(void) { return (0 << 16) | 1; }
+int32_t la_version(void) { return (0 << 16) | 2; }
 
 }  // extern "C"

@@ -60,7 +60,12 @@ struct SweepArgs {
     StateIn s_in;             // forward-type: initial state; backward-type: dL/dfinal
     StateOut s_out;           // forward-type: final state; backward-type: dL/dinitial
     int withhold_handoff;     // diagnostic: tensor-core kernels skip one hand-off
+    int64_t max_len;          // longest sequence (T when dense)
 };
+
+// Calls whose longest sequence has at most this many tokens run the
+// token-by-token kernels (la_short.cu) instead of the chunked ones.
+constexpr int SHORT_MAX_T = 16;
 
 // Host-side count of enqueued kernels (la_launch_count).
 void note_launch();
@@ -71,6 +76,11 @@ void set_last_error(const char *msg);
 // CUDA-core kernels: any D, E in 1..256, bf16 or fp32, every flag.
 cudaError_t simt_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t simt_backward_sweep(const SweepArgs &a, cudaStream_t s);
+
+// Token-by-token kernels for short sequences: any D in 1..256, any E, bf16 or
+// fp32, every flag; cudaErrorNotSupported outside that range.
+cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s);
+cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s);
 
 // Tensor-core (tcgen05) kernels for bf16, both sweep shapes; eligibility
 // (dtype, widths, 16-byte alignment) is the same for both.

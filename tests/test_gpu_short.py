@@ -1,0 +1,85 @@
+"""Short sequences (at most 16 tokens): the token-by-token kernels.
+
+Decoding a few new tokens against a carried state is the serving use of the
+recurrence (the pages' `recurrent` API, an initial state in and the final
+state out).  These calls run la_short.cu instead of the chunked kernels; the
+tests check them against the oracle at every flag, head width and dtype, and
+check that decoding a sequence piece by piece, each call's final state fed to
+the next as its initial state, equals one call over the whole sequence.
+"""
+import math
+
+import pytest
+import torch
+
+import linear_attention_head_gb300 as la
+import workloads as W
+from parity import TOL, compare, gpu_run, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(B, T, H, D, E, dtype, seqlens=None, g=None, init=0.3, dfin=0.3):
+    g = W.alibi_g_gamma(H) if g is None else g
+    return W.Workload("short", B, T if seqlens is None else sum(seqlens), H, D, E, dtype, g,
+                      1.0 / math.sqrt(D), seqlens=seqlens, init_std=init, dfinal_std=dfin)
+
+
+def test_kernel_family_switches_at_16_tokens():
+    assert la.kernel_family(4, 1, 32, 128, 128) == 2
+    assert la.kernel_family(4, 16, 32, 128, 128) == 2
+    assert la.kernel_family(4, 17, 32, 128, 128) == 1
+    assert la.kernel_family(1, 8, 2, 64, 48, dtype=torch.float32) == 2
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 16])
+@pytest.mark.parametrize("dtype,D,E", [(torch.bfloat16, 128, 128), (torch.float32, 64, 64),
+                                       (torch.bfloat16, 192, 192), (torch.bfloat16, 16, 48),
+                                       (torch.float32, 1, 1), (torch.bfloat16, 256, 40)])
+def test_short_matches_oracle(T, dtype, D, E):
+    w = _w(2, T, 3, D, E, dtype, g=torch.tensor([0.0, -0.05, -2.0]))
+    x = W.make_inputs(w, seed=100 + T)
+    for reverse in (False, True):
+        compare(gpu_run(x, reverse), oracle_run(x, reverse), TOL[dtype],
+                label="T=%d D=%d E=%d rev=%d" % (T, D, E, reverse))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_short_packed_with_empty_sequences(dtype):
+    lens = [1, 0, 16, 5, 0, 11, 2]
+    w = _w(1, 0, 4, 128, 128, dtype, seqlens=lens, init=0.1, dfin=0.1)
+    x = W.make_inputs(w, seed=9)
+    for reverse in (False, True):
+        got = gpu_run(x, reverse)
+        compare(got, oracle_run(x, reverse), TOL[dtype], cu=x["cu_seqlens"],
+                label="packed short rev=%d" % reverse)
+        for n in (1, 4):   # zero-length sequences pass their states through
+            assert torch.equal(got["final_state"][n], x["initial_state"][n])
+            assert torch.equal(got["d_initial_state"][n], x["d_final_state"][n])
+
+
+def test_decoding_piece_by_piece_equals_one_call():
+    # a 160-token sequence: one call (chunked kernels), or pieces of 1..16
+    # tokens (token-by-token kernels) chained through the state, and one
+    # longer piece (chunked kernels)
+    B, T, H, D = 2, 160, 4, 128
+    w = _w(B, T, H, D, D, torch.bfloat16, init=0.2, dfin=0.0)
+    x = W.make_inputs(w, seed=21)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o_all, s_all = la.la_fwd(d["q"], d["k"], d["v"], d["g_gamma"], w.scale, d["initial_state"])
+    pieces, t, state, outs = [1, 1, 7, 16, 15, 16, 1, 16, 87], 0, d["initial_state"], []
+    assert sum(pieces) == T
+    for p in pieces:
+        sl = slice(t, t + p)
+        o, state = la.la_fwd(d["q"][:, sl], d["k"][:, sl], d["v"][:, sl], d["g_gamma"], w.scale,
+                             state)
+        outs.append(o)
+        t += p
+    torch.cuda.synchronize()
+    la.get_device_error()
+    o_dec = torch.cat(outs, dim=1)
+    ref = oracle_run(x, backward=False)
+    compare(dict(o=o_dec.cpu(), final_state=state.cpu()), ref, TOL[torch.bfloat16],
+            label="decoded")
+    compare(dict(o=o_all.cpu(), final_state=s_all.cpu()), ref, TOL[torch.bfloat16],
+            label="one call")
