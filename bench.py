@@ -314,6 +314,7 @@ def gpu_bench(args):
     }
     if not args.no_sweep:
         line["sweep"] = length_sweep(la, torch, dev, stream, T)
+        line["decode"] = decode_bench(la, torch, dev, stream, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.n, args.cpu_pairs)
     if rank == 0:
@@ -371,6 +372,46 @@ def length_sweep(la, torch, dev, stream, skip_n):
             out[str(n)]["fwd_ms_unflushed"] = timed(fwd, False)
             out[str(n)]["bwd_ms_unflushed"] = timed(bwd, False)
         del q, k, v, do
+    return out
+
+
+def decode_bench(la, torch, dev, stream, peak):
+    """Decoding against a carried state (the token-by-token kernels): la_fwd on
+    a batch of 64 sequences x 32 heads, d = e = 128 bf16, with a fp32 initial
+    state in and the final state out, for 1 and 16 new tokens per sequence.
+    Each point is the mean of 20 calls queued behind torch.cuda._sleep, so no
+    host gap enters the events.  Bound: HBM; algorithmic bytes per call = the
+    state read and written (2 x B*H*d*e*4) + q, k, v read and o written."""
+    import workloads as W
+    B, H, D, E = 64, 32, 128, 128
+    g = W.alibi_g_gamma(H).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(11)
+    s0 = torch.randn((B, H, D, E), generator=gen, device=dev) * 0.1
+    fin = torch.empty_like(s0)
+    out = {}
+    for T in (1, 16):
+        q, k, v = (torch.randn((B, T, H, D), generator=gen, device=dev).bfloat16()
+                   for _ in range(3))
+        o = torch.empty_like(v)
+        fn = lambda: la.la_fwd(q, k, v, g, D ** -0.5, s0, out=o, final_state=fin)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 20
+        nbytes = 2 * B * H * D * E * 4 + 4 * B * T * H * D * 2
+        out["b%d_h%d_t%d" % (B, H, T)] = {
+            "kernel_family": la.kernel_family(B, T, H, D, E), "us_per_call": ms * 1e3,
+            "tokens_per_s": B * T / (ms * 1e-3), "bytes_per_call": nbytes,
+            "achieved_gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
+        del q, k, v, o
+    la.get_device_error(dev)
     return out
 
 
