@@ -31,13 +31,21 @@
  *   - State tensors (initial_state, final_state, d_final_state,
  *     d_initial_state) are dense fp32 [N, H, D, E], N = B, or num_seqs when
  *     cu_seqlens is given.
- *   - Workspace (optional): with packed sequences the library schedules the
- *     longest sequences first.  It needs la_workspace_size(N) bytes of device
- *     memory for that schedule, passed as (workspace, workspace_bytes); the
- *     schedule is copied there on `stream` and read by the kernels, so the
- *     workspace must not be shared with another call in flight on another
- *     stream.  NULL (or too small a workspace) runs the sequences in index
- *     order; results are identical either way.  Dense batches ignore it.
+ *   - Workspace (optional, 256-byte aligned device memory, passed as
+ *     (workspace, workspace_bytes)); la_workspace_size_for gives the bytes
+ *     that enable everything below.  It holds, when it is large enough:
+ *       * the longest-first schedule of packed sequences (la_workspace_size(N)
+ *         bytes at its start);
+ *       * the sequence split: when the (sequence, head) pairs would occupy at
+ *         most half of the GPU's SMs, long sequences are cut into segments of
+ *         whole 128-token chunks that run in parallel, in two passes around a
+ *         scan of one fp32 state per (segment, head).  This needs every token
+ *         tensor's batch stride to equal T times its token stride (or B = 1).
+ *     Both are copied or computed there on `stream`, so the workspace must
+ *     not be shared with another call in flight on another stream.  NULL (or
+ *     too small a workspace) runs without them.  The schedule never changes
+ *     results; the split changes the summation order of the states (fp32
+ *     rounding only).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) of the current device.  No entry point
  *     allocates device memory or synchronizes, except: when cu_seqlens is given
@@ -113,7 +121,8 @@ typedef struct la_dims {
  *   cu_seqlens_host host copy of cu_seqlens, or NULL (then copied, see above)
  *   o               [B,T,H,E] of `dtype` (output, v_strides)
  *   final_state     [N,H,D,E] fp32 output, or NULL to skip it
- *   workspace       device scratch for the packed schedule, or NULL (above) */
+ *   workspace       device scratch for the schedule and the sequence split,
+ *                   or NULL (above) */
 la_status la_fwd(const la_dims *dims, int32_t dtype,
                  const void *q, const void *k, const void *v,
                  const float *g_gamma, float scale,
@@ -191,6 +200,22 @@ la_status la_fwd_noalloc(const la_dims *dims, int32_t dtype,
 /* Bytes of device workspace for the longest-first schedule of num_seqs packed
  * sequences (0 when num_seqs < 1).  Pure host function. */
 size_t la_workspace_size(int32_t num_seqs);
+
+/* Bytes of device workspace with which la_fwd, la_bwd, la_bwd_dq and
+ * la_bwd_dkdv use the schedule and, when it applies, the sequence split for
+ * these sizes (see Conventions, Workspace).  cu_seqlens_host: host copy of
+ * cu_seqlens (num_seqs + 1 entries) for packed sequences, else NULL.  The
+ * answer depends on the current device's SM count and on
+ * la_set_sequence_split; 0 for invalid sizes.  Host function (reads one
+ * device attribute, once per device). */
+size_t la_workspace_size_for(const la_dims *dims, int32_t dtype, const int32_t *cu_seqlens_host);
+
+/* Sequence split control, process-wide: mode 1 (default) splits when it
+ * applies, 0 never; min_segment_tokens (>= 128, default 2048) is the
+ * shortest segment planned.  The method's pages have no counterpart: the
+ * split is a way of scheduling the same arithmetic.  LA_ERR_INVALID_ARG for
+ * other values. */
+la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens);
 
 /* Reads and clears the device-side error word that bounded on-device waits
  * set when they run out (LA_ERR_TIMEOUT), after synchronizing `stream`.

@@ -51,13 +51,15 @@ def _stream(device) -> ctypes.c_void_p:
 
 class _Packed:
     """cu_seqlens on the device plus a host copy (so the library never syncs), and the
-    device workspace for the library's longest-first schedule of the sequences."""
+    device workspace the library asks for (la_workspace_size_for: the longest-first
+    schedule of packed sequences and the sequence split)."""
 
     def __init__(self, cu_seqlens, device):
         self.dev = None
         self.host = None
         self.n = 0
         self.ws = None
+        self.device = device
         if cu_seqlens is None:
             return
         cu = torch.as_tensor(cu_seqlens)
@@ -69,14 +71,14 @@ class _Packed:
         else:
             self.dev = self.host.to(device)
         self.n = self.host.numel() - 1
-        nbytes = int(N.lib().la_workspace_size(self.n))
-        if nbytes:
-            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
 
-    def ws_args(self):
-        if self.ws is None:
+    def ws_args(self, dims, dtype_code):
+        nbytes = int(N.lib().la_workspace_size_for(ctypes.byref(dims), dtype_code,
+                                                   self.host_ptr()))
+        if nbytes == 0:
             return None, 0
-        return ctypes.c_void_p(self.ws.data_ptr()), self.ws.numel()
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        return ctypes.c_void_p(self.ws.data_ptr()), nbytes
 
     def host_ptr(self):
         return None if self.host is None else ctypes.c_void_p(self.host.data_ptr())
@@ -169,9 +171,10 @@ def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = No
     if final_state is None and want_final_state:
         final_state = torch.empty((Nst, H, D, E), device=dev, dtype=torch.float32)
     dims = _dims(q, v, packed)
+    ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                         scale, _ptr(init), int(bool(reverse)), _ptr(packed.dev),
-                        packed.host_ptr(), _ptr(out), _ptr(final_state), *packed.ws_args(),
+                        packed.host_ptr(), _ptr(out), _ptr(final_state), *ws,
                         _stream(dev))
     N.check(st)
     return out, final_state
@@ -207,10 +210,11 @@ def la_bwd(q: Tensor, k: Tensor, v: Tensor, do: Tensor, g_gamma, scale: Optional
     dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
                          dtype=torch.float32) if want_d_initial_state else None)
     dims = _dims(q, v, packed)
+    ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
                         _ptr(g), scale, _ptr(init), _ptr(dfin), int(bool(reverse)),
                         _ptr(packed.dev), packed.host_ptr(), _ptr(dq), _ptr(dk), _ptr(dv),
-                        _ptr(dinit), *packed.ws_args(), _stream(dev))
+                        _ptr(dinit), *ws, _stream(dev))
     N.check(st)
     return dq, dk, dv, dinit
 
@@ -222,9 +226,10 @@ def la_bwd_dq(q, k, v, do, g_gamma, scale=None, initial_state=None, reverse=Fals
         q, k, v, do, g_gamma, scale, initial_state, None, cu_seqlens)
     dq = _like(q)
     dims = _dims(q, v, packed)
+    ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_bwd_dq(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                            _ptr(do), _ptr(g), scale, _ptr(init), int(bool(reverse)),
-                           _ptr(packed.dev), packed.host_ptr(), _ptr(dq), *packed.ws_args(),
+                           _ptr(packed.dev), packed.host_ptr(), _ptr(dq), *ws,
                            _stream(dev))
     N.check(st)
     return dq
@@ -239,10 +244,11 @@ def la_bwd_dkdv(q, k, v, do, g_gamma, scale=None, d_final_state=None, reverse=Fa
     dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
                          dtype=torch.float32) if want_d_initial_state else None)
     dims = _dims(q, v, packed)
+    ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_bwd_dkdv(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                              _ptr(do), _ptr(g), scale, _ptr(dfin), int(bool(reverse)),
                              _ptr(packed.dev), packed.host_ptr(), _ptr(dk), _ptr(dv),
-                             _ptr(dinit), *packed.ws_args(), _stream(dev))
+                             _ptr(dinit), *ws, _stream(dev))
     N.check(st)
     return dk, dv, dinit
 

@@ -14,8 +14,10 @@
 
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -159,6 +161,168 @@ la_status make_schedule(const Problem &P, void *ws, size_t ws_bytes, cudaStream_
     return LA_OK;
 }
 
+// ---- sequence split -------------------------------------------------------
+// Few (sequence, head) pairs leave most SMs idle while each CTA walks a long
+// sequence.  Then every sequence is cut into segments of seg_len tokens (a
+// multiple of the 128-token chunk) that run as packed sequences, in two
+// passes around a state scan (la_split.cu): pass 1 from zero states gives
+// each segment's own contribution, the scan turns those into each segment's
+// initial state (and the sequence's final state), pass 2 produces the
+// outputs.  Dense batches are viewed as one row of B*T tokens, which needs
+// every token tensor's batch stride to be T times its token stride.
+
+std::atomic<int> g_split_mode{1};            // 0 off, 1 when it pays
+std::atomic<int> g_split_min_seg{2048};      // shortest segment planned
+
+int sm_count()
+{
+    static std::mutex mu;
+    static int cache[256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+struct SplitPlan {
+    int NS = 0;                       // segments; 0 = no split
+    int64_t seg_len = 0;
+    std::vector<int32_t> seg_cu;      // [NS + 1] token offsets of the one-row view
+    std::vector<int32_t> seq_first;   // [N + 1] first segment of each sequence
+    size_t bytes = 0;                 // workspace beyond the schedule
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+bool flat_rows(const Problem &P, const int64_t *st)
+{
+    return P.packed || P.B == 1 || st[0] == (int64_t)P.T * st[1];
+}
+
+// sms = 0: ask the current device.
+SplitPlan plan_split(const Problem &P, const la_dims *d, int sms = 0)
+{
+    SplitPlan S;
+    if (g_split_mode.load() == 0 || !flat_rows(P, d->qk_strides) || !flat_rows(P, d->v_strides))
+        return S;
+    if (sms <= 0)
+        sms = sm_count();
+    const int64_t items = (int64_t)P.N * P.H;
+    const int64_t total = P.packed ? (int64_t)P.T : (int64_t)P.B * P.T;
+    if (sms <= 0 || items == 0 || items * 2 > sms || total >= INT32_MAX)
+        return S;
+    int64_t max_len = 0;
+    for (int n = 0; n < P.N; ++n) {
+        const int64_t len = P.packed ? (int64_t)P.cu_host[(size_t)n + 1] - P.cu_host[(size_t)n]
+                                     : (int64_t)P.T;
+        max_len = std::max(max_len, len);
+    }
+    const int64_t min_seg = std::max(128, g_split_min_seg.load());
+    const int64_t R = std::min<int64_t>(sms / items, max_len / min_seg);
+    if (R < 2)
+        return S;
+    const int64_t seg_len = ((max_len + R - 1) / R + 127) / 128 * 128;
+    S.seq_first.push_back(0);
+    S.seg_cu.push_back(0);
+    for (int n = 0; n < P.N; ++n) {
+        const int64_t start = P.packed ? (int64_t)P.cu_host[(size_t)n] : (int64_t)n * P.T;
+        const int64_t len = P.packed ? (int64_t)P.cu_host[(size_t)n + 1] - start : (int64_t)P.T;
+        for (int64_t t = 0; t < len; t += seg_len) {
+            if (S.seg_cu.back() != start + t)   // a gap (never for these views)
+                return SplitPlan{};
+            S.seg_cu.push_back((int32_t)std::min(start + len, start + t + seg_len));
+        }
+        S.seq_first.push_back((int32_t)S.seg_cu.size() - 1);
+    }
+    S.NS = (int)S.seg_cu.size() - 1;
+    S.seg_len = seg_len;
+    S.bytes = round256(S.seg_cu.size() * 4) + round256(S.seq_first.size() * 4) +
+              (size_t)S.NS * P.H * P.D * P.E * sizeof(float);
+    return S;
+}
+
+// Device copies of the plan and the state buffer, carved from the workspace
+// after the schedule.
+struct SplitBufs {
+    const int32_t *seg_cu, *seq_first;
+    float *W;
+};
+
+la_status split_setup(const Problem &P, const SplitPlan &S, void *ws, cudaStream_t s,
+                      SplitBufs *b)
+{
+    uint8_t *p = static_cast<uint8_t *>(ws) + schedule_bytes(P.N);
+    int32_t *cu = reinterpret_cast<int32_t *>(p);
+    int32_t *first = reinterpret_cast<int32_t *>(p + round256(S.seg_cu.size() * 4));
+    b->W = reinterpret_cast<float *>(p + round256(S.seg_cu.size() * 4) +
+                                     round256(S.seq_first.size() * 4));
+    // pageable sources: each copy is staged before cudaMemcpyAsync returns
+    cudaError_t e = cudaMemcpyAsync(cu, S.seg_cu.data(), S.seg_cu.size() * 4,
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(first, S.seq_first.data(), S.seq_first.size() * 4,
+                            cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "copying the sequence split plan");
+    b->seg_cu = cu;
+    b->seq_first = first;
+    return LA_OK;
+}
+
+// Whether this call runs split: a plan exists and the workspace holds it.
+bool use_split(const Problem &P, const la_dims *d, void *ws, size_t ws_bytes, SplitPlan *S)
+{
+    *S = plan_split(P, d);
+    if (S->NS == 0 || !ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 ||
+        ws_bytes < schedule_bytes(P.N) + S->bytes) {
+        *S = SplitPlan{};
+        return false;
+    }
+    return true;
+}
+
+// Sweep arguments of the segment view: one row of all tokens, the segments
+// as packed sequences.
+void to_segments(la::SweepArgs *a, const Problem &P, const SplitPlan &S, const SplitBufs &b)
+{
+    a->B = 1;
+    a->T = P.packed ? P.T : P.B * P.T;
+    a->N = S.NS;
+    a->cu = b.seg_cu;
+    a->order = nullptr;
+    a->max_len = S.seg_len;
+}
+
+la::SplitScanArgs scan_args(const Problem &P, const SplitBufs &b, const float *g, int D, int E,
+                            la::StateIn start, la::StateOut fin, bool descending)
+{
+    la::SplitScanArgs sc{};
+    sc.N = P.N;
+    sc.H = P.H;
+    sc.D = D;
+    sc.E = E;
+    sc.seg_cu = b.seg_cu;
+    sc.seq_first = b.seq_first;
+    sc.g = g;
+    sc.W = b.W;
+    sc.start = start;
+    sc.fin = fin;
+    sc.descending = descending ? 1 : 0;
+    return sc;
+}
+
+la_status scan(const la::SplitScanArgs &sc, cudaStream_t s)
+{
+    cudaError_t e = la::split_scan(sc, s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "sequence split state scan");
+}
+
 bool has_tokens(const Problem &P) { return (int64_t)P.B * P.T > 0; }
 bool has_states(const Problem &P) { return (int64_t)P.N * P.H > 0; }
 
@@ -187,8 +351,8 @@ la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, cons
     a.max_len = P.T;
     if (P.packed) {
         a.max_len = 0;
-        for (int n = 0; n < P.N; ++n)
-            a.max_len = std::max<int64_t>(a.max_len, P.cu_host[(size_t)n + 1] - P.cu_host[(size_t)n]);
+        for (size_t n = 0; n < (size_t)P.N; ++n)
+            a.max_len = std::max<int64_t>(a.max_len, P.cu_host[n + 1] - P.cu_host[n]);
     }
     return a;
 }
@@ -228,7 +392,8 @@ la_status run_backward_type(const la::SweepArgs &a, cudaStream_t s)
 
 la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *k, const void *v,
                  const void *d_o, const float *g_gamma, float scale, const float *init,
-                 int32_t reverse, const int32_t *cu, const int32_t *order, void *dq, cudaStream_t s)
+                 int32_t reverse, const int32_t *cu, const int32_t *order, void *dq, cudaStream_t s,
+                 const SplitPlan *S = nullptr, const SplitBufs *b = nullptr)
 {
     // dq = forward-type sweep with (q, k, v) := (do, v, k); the state is S^T (E x D).
     la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse, order);
@@ -240,13 +405,29 @@ la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *
     a.out = tok_out(dq, d->qk_strides);
     a.s_in = la::StateIn{init, 1, P.E};
     a.s_out = la::StateOut{nullptr, 0, 0};
+    if (!S)
+        return run_forward_type(a, s);
+    // split: segment states from zero, scan from the initial state, outputs
+    to_segments(&a, P, *S, *b);
+    a.s_in = la::StateIn{nullptr, 0, 0};
+    a.s_out = la::StateOut{b->W, P.D, 1};
+    la_status st = run_forward_type(a, s);
+    if (st == LA_OK)
+        st = scan(scan_args(P, *b, g_gamma, P.E, P.D, la::StateIn{init, 1, P.E},
+                            la::StateOut{nullptr, 0, 0}, reverse != 0),
+                  s);
+    if (st != LA_OK)
+        return st;
+    a.s_in = la::StateIn{b->W, P.D, 1};
+    a.s_out = la::StateOut{nullptr, 0, 0};
     return run_forward_type(a, s);
 }
 
 la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void *q,
                    const void *k, const void *v, const void *d_o, const float *g_gamma,
                    float scale, const float *dfinal, int32_t reverse, const int32_t *cu,
-                   const int32_t *order, void *dk, void *dv, float *dinit, cudaStream_t s)
+                   const int32_t *order, void *dk, void *dv, float *dinit, cudaStream_t s,
+                   const SplitPlan *S = nullptr, const SplitBufs *b = nullptr)
 {
     la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse, order);
     // dv: (q, k, w) as given, G = dL/dS (D x E)
@@ -258,7 +439,28 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
     a.out = tok_out(dv, d->v_strides);
     a.s_in = la::StateIn{dfinal, P.E, 1};
     a.s_out = la::StateOut{dinit, P.E, 1};
-    la_status st = run_backward_type(a, s);
+    la::StateIn g_dk{dfinal, 1, P.E};   // G^T for the dk sweep
+    la_status st;
+    if (!S) {
+        st = run_backward_type(a, s);
+    } else {
+        // split: segment G from zero, scan from d_final (against processing
+        // order), d_initial from the scan, then dv from each segment's G
+        to_segments(&a, P, *S, *b);
+        a.s_in = la::StateIn{nullptr, 0, 0};
+        a.s_out = la::StateOut{b->W, P.E, 1};
+        st = run_backward_type(a, s);
+        if (st == LA_OK)
+            st = scan(scan_args(P, *b, g_gamma, P.D, P.E, la::StateIn{dfinal, P.E, 1},
+                                la::StateOut{dinit, P.E, 1}, reverse == 0),
+                      s);
+        if (st == LA_OK) {
+            a.s_in = la::StateIn{b->W, P.E, 1};
+            a.s_out = la::StateOut{nullptr, 0, 0};
+            st = run_backward_type(a, s);
+        }
+        g_dk = la::StateIn{b->W, 1, P.E};
+    }
     if (st != LA_OK)
         return st;
     // dk: (q, k, w) := (do, v, q), G^T (E x D)
@@ -268,7 +470,7 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
     a.k = tok(v, d->v_strides);
     a.v = tok(q, d->qk_strides);
     a.out = tok_out(dk, d->qk_strides);
-    a.s_in = la::StateIn{dfinal, 1, P.E};
+    a.s_in = g_dk;
     a.s_out = la::StateOut{nullptr, 0, 0};
     return run_backward_type(a, s);
 }
@@ -309,6 +511,25 @@ la_status la_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *
     a.out = tok_out(o, dims->v_strides);
     a.s_in = la::StateIn{initial_state, P.E, 1};
     a.s_out = la::StateOut{final_state, P.E, 1};
+    SplitPlan S;
+    if (!use_split(P, dims, workspace, workspace_bytes, &S))
+        return run_forward_type(a, s);
+    // split: segment states from zero, scan (which also writes the final
+    // state), then every segment from its initial state
+    SplitBufs b;
+    if ((st = split_setup(P, S, workspace, s, &b)))
+        return st;
+    to_segments(&a, P, S, b);
+    a.s_in = la::StateIn{nullptr, 0, 0};
+    a.s_out = la::StateOut{b.W, P.E, 1};
+    if ((st = run_forward_type(a, s)))
+        return st;
+    if ((st = scan(scan_args(P, b, g_gamma, P.D, P.E, la::StateIn{initial_state, P.E, 1},
+                             la::StateOut{final_state, P.E, 1}, reverse != 0),
+                   s)))
+        return st;
+    a.s_in = la::StateIn{b.W, P.E, 1};
+    a.s_out = la::StateOut{nullptr, 0, 0};
     return run_forward_type(a, s);
 }
 
@@ -337,8 +558,13 @@ la_status la_bwd_dq(const la_dims *dims, int32_t dtype, const void *q, const voi
     const int32_t *order = nullptr;
     if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
         return st;
+    SplitPlan S;
+    SplitBufs b;
+    const bool split = use_split(P, dims, workspace, workspace_bytes, &S);
+    if (split && (st = split_setup(P, S, workspace, s, &b)))
+        return st;
     return bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens,
-                  order, dq, s);
+                  order, dq, s, split ? &S : nullptr, split ? &b : nullptr);
 }
 
 la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype, const void *q, const void *k,
@@ -366,8 +592,14 @@ la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype, const void *q, const v
     const int32_t *order = nullptr;
     if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
         return st;
+    SplitPlan S;
+    SplitBufs b;
+    const bool split = use_split(P, dims, workspace, workspace_bytes, &S);
+    if (split && (st = split_setup(P, S, workspace, s, &b)))
+        return st;
     return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
-                    cu_seqlens, order, dk, dv, d_initial_state, s);
+                    cu_seqlens, order, dk, dv, d_initial_state, s, split ? &S : nullptr,
+                    split ? &b : nullptr);
 }
 
 la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k, const void *v,
@@ -395,12 +627,18 @@ la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *
     const int32_t *order = nullptr;
     if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
         return st;
+    SplitPlan S;
+    SplitBufs b;
+    const bool split = use_split(P, dims, workspace, workspace_bytes, &S);
+    if (split && (st = split_setup(P, S, workspace, s, &b)))
+        return st;
     st = bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens,
-                order, dq, s);
+                order, dq, s, split ? &S : nullptr, split ? &b : nullptr);
     if (st != LA_OK)
         return st;
     return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
-                    cu_seqlens, order, dk, dv, d_initial_state, s);
+                    cu_seqlens, order, dk, dv, d_initial_state, s, split ? &S : nullptr,
+                    split ? &b : nullptr);
 }
 
 la_status la_get_device_error(void *stream)
@@ -454,6 +692,31 @@ int32_t la_kernel_family(const la_dims *dims, int32_t dtype)
 
 size_t la_workspace_size(int32_t num_seqs) { return schedule_bytes(num_seqs); }
 
+size_t la_workspace_size_for(const la_dims *dims, int32_t dtype, const int32_t *cu_seqlens_host)
+{
+    Problem P;
+    std::string keep = g_msg;
+    // the host table stands in for the device one: check_dims reads only the host copy
+    la_status st = check_dims(dims, dtype, cu_seqlens_host, cu_seqlens_host, nullptr, &P);
+    g_msg = keep;
+    if (st != LA_OK)
+        return 0;
+    const SplitPlan S = plan_split(P, dims);
+    if (S.NS > 0)
+        return schedule_bytes(P.N) + S.bytes;
+    return P.packed ? schedule_bytes(P.N) : 0;
+}
+
+la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens)
+{
+    if (mode < 0 || mode > 1 || min_segment_tokens < 128)
+        return fail(LA_ERR_INVALID_ARG, "la_set_sequence_split: mode %d, min_segment_tokens %d",
+                    mode, min_segment_tokens);
+    g_split_mode.store(mode);
+    g_split_min_seg.store(min_segment_tokens);
+    return LA_OK;
+}
+
 la_status la_debug_withhold_next_handoff(int32_t on)
 {
     g_withhold = on ? 1 : 0;
@@ -462,6 +725,6 @@ la_status la_debug_withhold_next_handoff(int32_t on)
 
 uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int32_t la_version(void) { return (0 << 16) | 2; }
+int32_t la_version(void) { return (0 << 16) | 3; }
 
 }  // extern "C"

@@ -88,6 +88,25 @@ bool tc_sweep_supported(const SweepArgs &a);
 cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s);
 
+// State scan of the sequence split (la_split.cu).  W holds one D x E fp32
+// state per (segment, head), [NS][H][D][E]; on entry the segments' results
+// from a zero state, on return their initial states.  Sequence n owns the
+// consecutive segments [seq_first[n], seq_first[n+1]), of lengths
+// seg_cu[s+1] - seg_cu[s], visited in token order (or reversed).  start is the
+// sequence's initial state (zero when null) and fin receives its final state
+// (skipped when null), both with the StateIn / StateOut indexing.
+struct SplitScanArgs {
+    int N, H, D, E;
+    const int32_t *seg_cu;      // device [NS + 1]
+    const int32_t *seq_first;   // device [N + 1]
+    const float *g;             // [H]
+    float *W;
+    StateIn start;
+    StateOut fin;
+    int descending;
+};
+cudaError_t split_scan(const SplitScanArgs &a, cudaStream_t s);
+
 // Device error word of the tensor-core kernels (bounded waits that ran out).
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err);
 

@@ -156,3 +156,16 @@ def test_workspace_size(lib):
     assert lib.la_workspace_size(1) == 256
     assert lib.la_workspace_size(64) == 256
     assert lib.la_workspace_size(65) == 512
+
+
+def test_workspace_size_for_and_split_control(lib):
+    # no device here: the split cannot be planned, only the packed schedule is sized
+    d = _dims(B=1, T=16, N_=3)
+    cu, cp = _cu([0, 5, 5, 16])
+    assert lib.la_workspace_size_for(ctypes.byref(d), 0, cp) == lib.la_workspace_size(3)
+    assert lib.la_workspace_size_for(ctypes.byref(_dims()), 0, None) == 0
+    assert lib.la_workspace_size_for(ctypes.byref(_dims(H=0)), 0, None) == 0
+    assert lib.la_set_sequence_split(2, 2048) == N.LA_ERR_INVALID_ARG
+    assert lib.la_set_sequence_split(1, 64) == N.LA_ERR_INVALID_ARG
+    assert lib.la_set_sequence_split(0, 4096) == N.LA_OK
+    assert lib.la_set_sequence_split(1, 2048) == N.LA_OK
