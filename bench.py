@@ -315,6 +315,7 @@ def gpu_bench(args):
     if not args.no_sweep:
         line["sweep"] = length_sweep(la, torch, dev, stream, T)
         line["decode"] = decode_bench(la, torch, dev, stream, peak)
+        line["long_sequence"] = split_bench(la, torch, dev, stream, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.n, args.cpu_pairs)
     if rank == 0:
@@ -415,11 +416,54 @@ def decode_bench(la, torch, dev, stream, peak):
     return out
 
 
+def split_bench(la, torch, dev, stream, peak):
+    """One long sequence with few heads (b1 h8 n262144 d=e=128 bf16): 8
+    (sequence, head) pairs for 152 SMs.  la_fwd + la_bwd with the sequence
+    split (the library's default) and without it (la_set_sequence_split(0)),
+    each the mean of 5 queued steps after 2 warm-up steps.  Algorithmic bytes
+    per step are the unsplit sweeps' compulsory traffic (11 token tensors)."""
+    import workloads as W
+    from linear_attention_head_gb300 import _native
+    B, T, H, D = 1, 262144, 8, 128
+    g = W.alibi_g_gamma(H).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(13)
+    q, k, v, do = (torch.randn((B, T, H, D), generator=gen, device=dev).bfloat16()
+                   for _ in range(4))
+
+    def step():
+        la.la_fwd(q, k, v, g, 1.0)
+        la.la_bwd(q, k, v, do, g, 1.0, want_d_initial_state=False)
+
+    out = {"workload": "fwd+bwd b1 h8 n262144 d=e=128 bf16, ALiBi slopes, scale 1"}
+    nbytes = 11 * B * T * H * D * 2
+    for name, mode in (("split", 1), ("unsplit", 0)):
+        _native.check(_native.lib().la_set_sequence_split(mode, 2048))
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 5
+        out[name] = {"ms_per_step": ms, "tokens_per_s": B * T / (ms * 1e-3),
+                     "compulsory_frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
+    _native.check(_native.lib().la_set_sequence_split(1, 2048))
+    la.get_device_error(dev)
+    del q, k, v, do
+    return out
+
+
 def source_sha():
+    """Hash of the sources the tensor-core sweep kernel is built from (the
+    kernel whose ncu traffic profiles/traffic_tc_sweep_kernel.json records)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_head_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in ("la_internal.h", "la_sm100.cuh", "la_tc_sweep.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
