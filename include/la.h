@@ -24,10 +24,11 @@
  *     never frees, keeps or allocates them.  cu_seqlens_host is a HOST pointer.
  *   - Token tensors are indexed [batch, token, head, channel] through element
  *     strides (batch, token, head); the channel dimension must be contiguous.
- *     q, k, dq, dk share qk_strides; v, o, do, dv share v_strides.  Both the
- *     token-major layout [B,T,H,X] (ejkernel) and the head-major layout
- *     [B,H,T,X] (Lightning-2's (b, h, n, d)) are expressible.  Outputs must
- *     not overlap inputs or each other.
+ *     q, k, dq, dk share qk_strides; v, o, do, dv share v_strides (with
+ *     grouped key/value heads k, dk and v, dv have their own, see la_dims).
+ *     Both the token-major layout [B,T,H,X] (ejkernel) and the head-major
+ *     layout [B,H,T,X] (Lightning-2's (b, h, n, d)) are expressible.  Outputs
+ *     must not overlap inputs or each other.
  *   - State tensors (initial_state, final_state, d_final_state,
  *     d_initial_state) are dense fp32 [N, H, D, E], N = B, or num_seqs when
  *     cu_seqlens is given.
@@ -40,12 +41,14 @@
  *         most half of the GPU's SMs, long sequences are cut into segments of
  *         whole 128-token chunks that run in parallel, in two passes around a
  *         scan of one fp32 state per (segment, head).  This needs every token
- *         tensor's batch stride to equal T times its token stride (or B = 1).
- *     Both are copied or computed there on `stream`, so the workspace must
- *     not be shared with another call in flight on another stream.  NULL (or
- *     too small a workspace) runs without them.  The schedule never changes
- *     results; the split changes the summation order of the states (fp32
- *     rounding only).
+ *         tensor's batch stride to equal T times its token stride (or B = 1);
+ *       * with grouped key/value heads, the backward's per-query-head dk and
+ *         dv contributions (required there, see la_bwd).
+ *     All of it is written there on `stream`, so the workspace must not be
+ *     shared with another call in flight on another stream.  NULL (or too
+ *     small a workspace) runs without the schedule and the split.  The
+ *     schedule never changes results; the split changes the summation order
+ *     of the states (fp32 rounding only).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) of the current device.  No entry point
  *     allocates device memory or synchronizes, except: when cu_seqlens is given
@@ -86,15 +89,25 @@ typedef enum la_dtype {
  *   batch      B  >= 0; must be 1 when cu_seqlens is given (lightning_attn
  *                 docstring, Raises: batch must be 1 with cu_seqlens)
  *   seq_len    T  >= 0 tokens per batch row (total tokens when packed)
- *   heads      H  1..65535; keys and values have the same head count as
- *                 queries (the lightning_attn docstring's "Must have the same
- *                 shape as q")
+ *   heads      H  1..65535 query heads
  *   dim_qk     D  query/key channels, 1..256
  *   dim_v      E  value channels, 1..256
  *   num_seqs   N  number of packed sequences when cu_seqlens is given
  *                 (ignored otherwise; N = B)
- *   qk_strides element strides (batch, token, head) of q, k, dq, dk
- *   v_strides  element strides (batch, token, head) of v, o, do, dv        */
+ *   qk_strides element strides (batch, token, head) of q, dq (and of k, dk
+ *                 when kv_heads is 0)
+ *   v_strides  element strides (batch, token, head) of o, do (and of v, dv
+ *                 when kv_heads is 0)
+ *   kv_heads   0: keys and values have H heads (lightning_attn: "Must have
+ *                 the same shape as q").  Else H_kv, a divisor of H: grouped
+ *                 key/value heads (the num_kv_heads axis of ejkernel
+ *                 `recurrent`'s key and value), query head h reading key and
+ *                 value head h / (H / H_kv).  Decay, states and their
+ *                 gradients stay per query head; dk and dv of a shared head
+ *                 sum its query heads' contributions.
+ *   reserved   must be 0
+ *   k_strides  element strides of k, dk when kv_heads > 0 (k, dk: [B,T,H_kv,D])
+ *   kv_v_strides element strides of v, dv when kv_heads > 0 ([B,T,H_kv,E]) */
 typedef struct la_dims {
     int32_t batch;
     int32_t seq_len;
@@ -104,12 +117,17 @@ typedef struct la_dims {
     int32_t num_seqs;
     int64_t qk_strides[3];
     int64_t v_strides[3];
+    int32_t kv_heads;
+    int32_t reserved;
+    int64_t k_strides[3];
+    int64_t kv_v_strides[3];
 } la_dims;
 
 /* Forward pass (ejkernel `recurrent` / `lightning_attn`: returns the output
  * and the final hidden state).
- *   q, k            [B,T,H,D] of `dtype`
- *   v               [B,T,H,E] of `dtype`
+ *   q               [B,T,H,D] of `dtype`
+ *   k               [B,T,H,D] of `dtype` ([B,T,H_kv,D] with kv_heads)
+ *   v               [B,T,H,E] of `dtype` ([B,T,H_kv,E] with kv_heads)
  *   g_gamma         [H] fp32 log-decay per head (gamma = exp(g_gamma[h]);
  *                   values > 0 are accepted but grow the state)
  *   scale           multiplies q only (the pages' softmax_scale; callers apply
@@ -140,8 +158,14 @@ la_status la_fwd(const la_dims *dims, int32_t dtype,
  *   q, k, v, g_gamma, scale, initial_state, reverse, cu_seqlens: as la_fwd
  *   d_o             [B,T,H,E] of `dtype` (v_strides)
  *   d_final_state   [N,H,D,E] fp32, or NULL for zeros
- *   dq, dk          [B,T,H,D] of `dtype` outputs (qk_strides)
- *   dv              [B,T,H,E] of `dtype` output (v_strides)
+ *   dq              [B,T,H,D] of `dtype` output (qk_strides)
+ *   dk, dv          [B,T,H,D], [B,T,H,E] of `dtype` outputs (qk_strides,
+ *                   v_strides); with kv_heads: [B,T,H_kv,D], [B,T,H_kv,E]
+ *                   (k_strides, kv_v_strides), each the fp32 sum of its
+ *                   group's per-query-head contributions, which pass through
+ *                   the workspace rounded to `dtype`.  Then the workspace is
+ *                   required: la_workspace_size_for gives its size, and too
+ *                   small a workspace is LA_ERR_INVALID_ARG.
  *   d_initial_state [N,H,D,E] fp32 output, or NULL to skip it
  * la_bwd is exactly la_bwd_dq followed by la_bwd_dkdv on the same stream.  */
 la_status la_bwd(const la_dims *dims, int32_t dtype,

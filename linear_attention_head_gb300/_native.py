@@ -33,6 +33,10 @@ class LaDims(ctypes.Structure):
         ("num_seqs", ctypes.c_int32),
         ("qk_strides", ctypes.c_int64 * 3),
         ("v_strides", ctypes.c_int64 * 3),
+        ("kv_heads", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("k_strides", ctypes.c_int64 * 3),
+        ("kv_v_strides", ctypes.c_int64 * 3),
     ]
 
 

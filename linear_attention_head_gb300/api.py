@@ -85,8 +85,14 @@ class _Packed:
 
 
 def _check_tokens(q, k, v, extra=()):
-    if q.ndim != 4 or k.shape != q.shape or v.ndim != 4 or v.shape[:3] != q.shape[:3]:
-        raise ValueError("q, k must be [B, T, H, D] and v [B, T, H, E] (got %s, %s, %s)"
+    """q [B,T,H,D]; k [B,T,H_kv,D] and v [B,T,H_kv,E] with H_kv dividing H (grouped
+    key/value heads, ejkernel `recurrent`'s num_kv_heads)."""
+    ok = (q.ndim == 4 and k.ndim == 4 and v.ndim == 4 and k.shape[:2] == q.shape[:2]
+          and k.shape[3] == q.shape[3] and v.shape[:3] == k.shape[:3] and k.shape[2] >= 1
+          and q.shape[2] % k.shape[2] == 0)
+    if not ok:
+        raise ValueError("q must be [B, T, H, D], k [B, T, H_kv, D] and v [B, T, H_kv, E] "
+                         "with H_kv dividing H (got %s, %s, %s)"
                          % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
     for t in (q, k, v) + tuple(extra):
         if t.device.type != "cuda":
@@ -109,15 +115,22 @@ def _same_strides(group):
     return [t.contiguous() for t in group]
 
 
-def _dims(q, v, packed: _Packed) -> N.LaDims:
+def _dims(q, k, v, o, packed: _Packed) -> N.LaDims:
+    """q (and dq) give qk_strides, o (and do) v_strides; with grouped key/value
+    heads k (dk) and v (dv) have strides of their own."""
     B, T, H, D = q.shape
     E = v.shape[3]
     d = N.LaDims()
     d.batch, d.seq_len, d.heads, d.dim_qk, d.dim_v = B, T, H, D, E
     d.num_seqs = packed.n
+    grouped = k.shape[2] != H
+    d.kv_heads = k.shape[2] if grouped else 0
     for i in range(3):
         d.qk_strides[i] = q.stride(i)
-        d.v_strides[i] = v.stride(i)
+        d.v_strides[i] = o.stride(i)
+        if grouped:
+            d.k_strides[i] = k.stride(i)
+            d.kv_v_strides[i] = v.stride(i)
     return d
 
 
@@ -155,7 +168,9 @@ def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = No
     """Forward pass. q, k: [B,T,H,D]; v: [B,T,H,E]; returns (o [B,T,H,E], final [N,H,D,E])."""
     _check_tokens(q, k, v)
     q, k, v = _channel_contiguous((q, k, v))
-    q, k = _same_strides([q, k])
+    grouped = k.shape[2] != q.shape[2]
+    if not grouped:
+        q, k = _same_strides([q, k])
     dev = q.device
     packed = _Packed(cu_seqlens, dev)
     B, T, H, D = q.shape
@@ -164,13 +179,16 @@ def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = No
     g = _g(g_gamma, H, dev)
     scale = float(D ** -0.5 if scale is None else scale)
     init = _state(initial_state, (Nst, H, D, E), dev, "initial_state")
+    o_shape = q.shape[:3] + v.shape[3:]
     if out is None:
-        out = _like(v)
-    if out.shape != v.shape or out.stride()[:3] != v.stride()[:3] or out.dtype != v.dtype:
-        raise ValueError("out must match v in shape, strides and dtype")
+        out = _like(v) if not grouped else torch.empty(o_shape, dtype=v.dtype, device=dev)
+    if (tuple(out.shape) != tuple(o_shape) or out.dtype != v.dtype or out.stride(-1) != 1
+            or (not grouped and out.stride()[:3] != v.stride()[:3])):
+        raise ValueError("out must be [B, T, H, E] of v's dtype (with v's strides when keys "
+                         "and values have H heads)")
     if final_state is None and want_final_state:
         final_state = torch.empty((Nst, H, D, E), device=dev, dtype=torch.float32)
-    dims = _dims(q, v, packed)
+    dims = _dims(q, k, v, out, packed)
     ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                         scale, _ptr(init), int(bool(reverse)), _ptr(packed.dev),
@@ -182,11 +200,12 @@ def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = No
 
 def _bwd_prep(q, k, v, do, g_gamma, scale, initial_state, d_final_state, cu_seqlens):
     _check_tokens(q, k, v, (do,))
-    if do.shape != v.shape:
-        raise ValueError("do must have v's shape")
+    if tuple(do.shape) != tuple(q.shape[:3] + v.shape[3:]):
+        raise ValueError("do must be [B, T, H, E]")
     q, k, v, do = _channel_contiguous((q, k, v, do))
-    q, k = _same_strides([q, k])
-    v, do = _same_strides([v, do])
+    if k.shape[2] == q.shape[2]:
+        q, k = _same_strides([q, k])
+        v, do = _same_strides([v, do])
     dev = q.device
     packed = _Packed(cu_seqlens, dev)
     B, T, H, D = q.shape
@@ -206,10 +225,10 @@ def la_bwd(q: Tensor, k: Tensor, v: Tensor, do: Tensor, g_gamma, scale: Optional
     sum(o*do) + sum(final_state*d_final_state)."""
     q, k, v, do, dev, packed, g, scale, init, dfin, Nst = _bwd_prep(
         q, k, v, do, g_gamma, scale, initial_state, d_final_state, cu_seqlens)
-    dq, dk, dv = _like(q), _like(q), _like(v)
+    dq, dk, dv = _like(q), _like(k), _like(v)
     dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
                          dtype=torch.float32) if want_d_initial_state else None)
-    dims = _dims(q, v, packed)
+    dims = _dims(q, k, v, do, packed)
     ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
                         _ptr(g), scale, _ptr(init), _ptr(dfin), int(bool(reverse)),
@@ -225,7 +244,7 @@ def la_bwd_dq(q, k, v, do, g_gamma, scale=None, initial_state=None, reverse=Fals
     q, k, v, do, dev, packed, g, scale, init, _, _ = _bwd_prep(
         q, k, v, do, g_gamma, scale, initial_state, None, cu_seqlens)
     dq = _like(q)
-    dims = _dims(q, v, packed)
+    dims = _dims(q, k, v, do, packed)
     ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_bwd_dq(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                            _ptr(do), _ptr(g), scale, _ptr(init), int(bool(reverse)),
@@ -240,10 +259,10 @@ def la_bwd_dkdv(q, k, v, do, g_gamma, scale=None, d_final_state=None, reverse=Fa
     """dk, dv and d_initial_state (one sweep against processing order)."""
     q, k, v, do, dev, packed, g, scale, _, dfin, Nst = _bwd_prep(
         q, k, v, do, g_gamma, scale, None, d_final_state, cu_seqlens)
-    dk, dv = _like(q), _like(v)
+    dk, dv = _like(k), _like(v)
     dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
                          dtype=torch.float32) if want_d_initial_state else None)
-    dims = _dims(q, v, packed)
+    dims = _dims(q, k, v, do, packed)
     ws = packed.ws_args(dims, _dtype_code(q))
     st = N.lib().la_bwd_dkdv(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                              _ptr(do), _ptr(g), scale, _ptr(dfin), int(bool(reverse)),
@@ -287,7 +306,7 @@ class _LinearAttention(torch.autograd.Function):
     def backward(ctx, do, dfin):
         q, k, v, init, g = ctx.saved_tensors
         if do is None:
-            do = torch.zeros_like(v)
+            do = torch.zeros(q.shape[:3] + v.shape[3:], dtype=v.dtype, device=v.device)
         dq, dk, dv, dinit = la_bwd(q, k, v, do.to(v.dtype), g, ctx.scale,
                                    init if ctx.has_init else None, dfin, ctx.reverse, ctx.cu,
                                    want_d_initial_state=ctx.has_init)
@@ -325,7 +344,13 @@ def recurrent(query: Tensor, key: Tensor, value: Tensor, g=None, g_gamma=None, g
 def lightning_attn(query: Tensor, key: Tensor, value: Tensor, layer_idx: int, num_layers: int,
                    softmax_scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
                    reverse: bool = False, cu_seqlens=None):
-    """ejkernel `lightning_attn`: g_gamma from the layer position, then `recurrent`."""
+    """ejkernel `lightning_attn`: g_gamma from the layer position, then `recurrent`.
+    Keys and values have the queries' shape (that page's docstring); grouped
+    key/value heads go through `recurrent` or la_fwd / la_bwd."""
+    if key.shape != query.shape or value.shape[:-1] != query.shape[:-1]:
+        raise ValueError("lightning_attn: key must have the shape of query and value its "
+                         "leading dims (got %s, %s, %s)"
+                         % (tuple(query.shape), tuple(key.shape), tuple(value.shape)))
     if cu_seqlens is not None:
         if query.ndim == 4 and query.shape[0] != 1:
             raise ValueError("The batch size is expected to be 1 rather than %d when using "

@@ -59,6 +59,8 @@ la_status cuda_fail(cudaError_t e, const char *where)
 
 struct Problem {
     int B, T, H, D, E, N;
+    int Hkv, G;                     // key/value heads and query heads per key/value head
+    const int64_t *k_st, *kv_v_st;  // strides of k, dk and of v, dv
     bool packed;
     std::vector<int32_t> cu_host;   // validated host copy of cu_seqlens (packed only)
 };
@@ -83,6 +85,19 @@ la_status check_dims(const la_dims *d, int32_t dtype, const int32_t *cu, const i
     for (int i = 0; i < 3; ++i)
         if (d->qk_strides[i] < 0 || d->v_strides[i] < 0)
             return fail(LA_ERR_INVALID_ARG, "negative stride");
+    if (d->reserved != 0)
+        return fail(LA_ERR_INVALID_ARG, "la_dims.reserved = %d, must be 0", d->reserved);
+    if (d->kv_heads < 0 || d->kv_heads > d->heads || (d->kv_heads && d->heads % d->kv_heads))
+        return fail(LA_ERR_INVALID_ARG, "kv_heads = %d must be 0 or divide heads = %d",
+                    d->kv_heads, d->heads);
+    if (d->kv_heads)
+        for (int i = 0; i < 3; ++i)
+            if (d->k_strides[i] < 0 || d->kv_v_strides[i] < 0)
+                return fail(LA_ERR_INVALID_ARG, "negative key/value stride");
+    P->Hkv = d->kv_heads ? d->kv_heads : d->heads;
+    P->G = d->heads / P->Hkv;
+    P->k_st = d->kv_heads ? d->k_strides : d->qk_strides;
+    P->kv_v_st = d->kv_heads ? d->kv_v_strides : d->v_strides;
     P->B = d->batch;
     P->T = d->seq_len;
     P->H = d->heads;
@@ -209,7 +224,8 @@ bool flat_rows(const Problem &P, const int64_t *st)
 SplitPlan plan_split(const Problem &P, const la_dims *d, int sms = 0)
 {
     SplitPlan S;
-    if (g_split_mode.load() == 0 || !flat_rows(P, d->qk_strides) || !flat_rows(P, d->v_strides))
+    if (g_split_mode.load() == 0 || !flat_rows(P, d->qk_strides) || !flat_rows(P, d->v_strides) ||
+        !flat_rows(P, P.k_st) || !flat_rows(P, P.kv_v_st))
         return S;
     if (sms <= 0)
         sms = sm_count();
@@ -254,10 +270,11 @@ struct SplitBufs {
     float *W;
 };
 
-la_status split_setup(const Problem &P, const SplitPlan &S, void *ws, cudaStream_t s,
-                      SplitBufs *b)
+la_status split_setup(const Problem &P, const SplitPlan &S, void *ws, size_t offset,
+                      cudaStream_t s, SplitBufs *b)
 {
-    uint8_t *p = static_cast<uint8_t *>(ws) + schedule_bytes(P.N);
+    (void)P;
+    uint8_t *p = static_cast<uint8_t *>(ws) + offset;
     int32_t *cu = reinterpret_cast<int32_t *>(p);
     int32_t *first = reinterpret_cast<int32_t *>(p + round256(S.seg_cu.size() * 4));
     b->W = reinterpret_cast<float *>(p + round256(S.seg_cu.size() * 4) +
@@ -275,16 +292,52 @@ la_status split_setup(const Problem &P, const SplitPlan &S, void *ws, cudaStream
     return LA_OK;
 }
 
-// Whether this call runs split: a plan exists and the workspace holds it.
-bool use_split(const Problem &P, const la_dims *d, void *ws, size_t ws_bytes, SplitPlan *S)
+// Whether this call runs split: a plan exists and the workspace holds it
+// from `offset` on.
+bool use_split(const Problem &P, const la_dims *d, void *ws, size_t ws_bytes, size_t offset,
+               SplitPlan *S)
 {
     *S = plan_split(P, d);
     if (S->NS == 0 || !ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 ||
-        ws_bytes < schedule_bytes(P.N) + S->bytes) {
+        ws_bytes < offset + S->bytes) {
         *S = SplitPlan{};
         return false;
     }
     return true;
+}
+
+// ---- grouped key/value heads ---------------------------------------------------
+// The backward sweeps give one dk / dv contribution per query head; they go
+// to two dense [B, T, H, X] buffers of the token dtype in the workspace
+// (after the schedule) and gqa_reduce sums each group into dk / dv.
+struct GqaBufs {
+    la::TokOut ck, cv;
+};
+
+size_t gqa_bytes(const Problem &P, int32_t dtype)
+{
+    if (P.G <= 1)
+        return 0;
+    const size_t elt = dtype == LA_DTYPE_BF16 ? 2 : 4;
+    const size_t tokens = (size_t)(P.packed ? 1 : P.B) * P.T;
+    return round256(tokens * P.H * P.D * elt) + round256(tokens * P.H * P.E * elt);
+}
+
+la_status gqa_setup(const Problem &P, int32_t dtype, void *ws, size_t ws_bytes, GqaBufs *g)
+{
+    const size_t need = schedule_bytes(P.N) + gqa_bytes(P, dtype);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < need)
+        return fail(LA_ERR_INVALID_ARG,
+                    "grouped key/value heads need a 256-byte aligned workspace of at least %zu "
+                    "bytes for the backward (got %zu)",
+                    need, ws ? ws_bytes : (size_t)0);
+    const size_t elt = dtype == LA_DTYPE_BF16 ? 2 : 4;
+    const size_t tokens = (size_t)(P.packed ? 1 : P.B) * P.T;
+    uint8_t *p = static_cast<uint8_t *>(ws) + schedule_bytes(P.N);
+    const int64_t T = P.T, H = P.H;
+    g->ck = la::TokOut{p, T * H * P.D, H * P.D, P.D};
+    g->cv = la::TokOut{p + round256(tokens * P.H * P.D * elt), T * H * P.E, H * P.E, P.E};
+    return LA_OK;
 }
 
 // Sweep arguments of the segment view: one row of all tokens, the segments
@@ -331,7 +384,10 @@ la_status need(const void *p, const char *name)
     return p ? LA_OK : fail(LA_ERR_INVALID_ARG, "%s is NULL", name);
 }
 
-la::Tok tok(const void *p, const int64_t *st) { return la::Tok{p, st[0], st[1], st[2]}; }
+la::Tok tok(const void *p, const int64_t *st, int hdiv = 1)
+{
+    return la::Tok{p, st[0], st[1], st[2], hdiv};
+}
 la::TokOut tok_out(void *p, const int64_t *st) { return la::TokOut{p, st[0], st[1], st[2]}; }
 
 la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, const float *g,
@@ -400,8 +456,8 @@ la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *
     a.D = P.E;
     a.E = P.D;
     a.q = tok(d_o, d->v_strides);
-    a.k = tok(v, d->v_strides);
-    a.v = tok(k, d->qk_strides);
+    a.k = tok(v, P.kv_v_st, P.G);
+    a.v = tok(k, P.k_st, P.G);
     a.out = tok_out(dq, d->qk_strides);
     a.s_in = la::StateIn{init, 1, P.E};
     a.s_out = la::StateOut{nullptr, 0, 0};
@@ -427,16 +483,17 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
                    const void *k, const void *v, const void *d_o, const float *g_gamma,
                    float scale, const float *dfinal, int32_t reverse, const int32_t *cu,
                    const int32_t *order, void *dk, void *dv, float *dinit, cudaStream_t s,
-                   const SplitPlan *S = nullptr, const SplitBufs *b = nullptr)
+                   const SplitPlan *S = nullptr, const SplitBufs *b = nullptr,
+                   const GqaBufs *gqa = nullptr)
 {
     la::SweepArgs a = base_args(P, dtype, cu, g_gamma, scale, reverse, order);
     // dv: (q, k, w) as given, G = dL/dS (D x E)
     a.D = P.D;
     a.E = P.E;
     a.q = tok(q, d->qk_strides);
-    a.k = tok(k, d->qk_strides);
+    a.k = tok(k, P.k_st, P.G);
     a.v = tok(d_o, d->v_strides);
-    a.out = tok_out(dv, d->v_strides);
+    a.out = gqa ? gqa->cv : tok_out(dv, P.kv_v_st);
     a.s_in = la::StateIn{dfinal, P.E, 1};
     a.s_out = la::StateOut{dinit, P.E, 1};
     la::StateIn g_dk{dfinal, 1, P.E};   // G^T for the dk sweep
@@ -467,12 +524,21 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
     a.D = P.E;
     a.E = P.D;
     a.q = tok(d_o, d->v_strides);
-    a.k = tok(v, d->v_strides);
+    a.k = tok(v, P.kv_v_st, P.G);
     a.v = tok(q, d->qk_strides);
-    a.out = tok_out(dk, d->qk_strides);
+    a.out = gqa ? gqa->ck : tok_out(dk, P.k_st);
     a.s_in = g_dk;
     a.s_out = la::StateOut{nullptr, 0, 0};
-    return run_backward_type(a, s);
+    if ((st = run_backward_type(a, s)) != LA_OK || !gqa)
+        return st;
+    // grouped key/value heads: sum each group's per-query-head contributions
+    const int rows = P.packed ? 1 : P.B;
+    cudaError_t e = la::gqa_reduce(gqa->ck.p, tok_out(dk, P.k_st), rows, P.T, P.Hkv, P.G, P.D,
+                                   a.bf16, s);
+    if (e == cudaSuccess)
+        e = la::gqa_reduce(gqa->cv.p, tok_out(dv, P.kv_v_st), rows, P.T, P.Hkv, P.G, P.E, a.bf16,
+                           s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "grouped key/value gradient sum");
 }
 
 }  // namespace
@@ -506,18 +572,19 @@ la_status la_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *
     a.D = P.D;
     a.E = P.E;
     a.q = tok(q, dims->qk_strides);
-    a.k = tok(k, dims->qk_strides);
-    a.v = tok(v, dims->v_strides);
+    a.k = tok(k, P.k_st, P.G);
+    a.v = tok(v, P.kv_v_st, P.G);
     a.out = tok_out(o, dims->v_strides);
     a.s_in = la::StateIn{initial_state, P.E, 1};
     a.s_out = la::StateOut{final_state, P.E, 1};
     SplitPlan S;
-    if (!use_split(P, dims, workspace, workspace_bytes, &S))
+    const size_t off = schedule_bytes(P.N);
+    if (!use_split(P, dims, workspace, workspace_bytes, off, &S))
         return run_forward_type(a, s);
     // split: segment states from zero, scan (which also writes the final
     // state), then every segment from its initial state
     SplitBufs b;
-    if ((st = split_setup(P, S, workspace, s, &b)))
+    if ((st = split_setup(P, S, workspace, off, s, &b)))
         return st;
     to_segments(&a, P, S, b);
     a.s_in = la::StateIn{nullptr, 0, 0};
@@ -560,8 +627,9 @@ la_status la_bwd_dq(const la_dims *dims, int32_t dtype, const void *q, const voi
         return st;
     SplitPlan S;
     SplitBufs b;
-    const bool split = use_split(P, dims, workspace, workspace_bytes, &S);
-    if (split && (st = split_setup(P, S, workspace, s, &b)))
+    const size_t off = schedule_bytes(P.N);
+    const bool split = use_split(P, dims, workspace, workspace_bytes, off, &S);
+    if (split && (st = split_setup(P, S, workspace, off, s, &b)))
         return st;
     return bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens,
                   order, dq, s, split ? &S : nullptr, split ? &b : nullptr);
@@ -592,14 +660,18 @@ la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype, const void *q, const v
     const int32_t *order = nullptr;
     if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
         return st;
+    GqaBufs gb;
+    if (P.G > 1 && (st = gqa_setup(P, dtype, workspace, workspace_bytes, &gb)))
+        return st;
     SplitPlan S;
     SplitBufs b;
-    const bool split = use_split(P, dims, workspace, workspace_bytes, &S);
-    if (split && (st = split_setup(P, S, workspace, s, &b)))
+    const size_t off = schedule_bytes(P.N) + gqa_bytes(P, dtype);
+    const bool split = use_split(P, dims, workspace, workspace_bytes, off, &S);
+    if (split && (st = split_setup(P, S, workspace, off, s, &b)))
         return st;
     return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
                     cu_seqlens, order, dk, dv, d_initial_state, s, split ? &S : nullptr,
-                    split ? &b : nullptr);
+                    split ? &b : nullptr, P.G > 1 ? &gb : nullptr);
 }
 
 la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k, const void *v,
@@ -627,10 +699,14 @@ la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *
     const int32_t *order = nullptr;
     if ((st = make_schedule(P, workspace, workspace_bytes, s, &order)))
         return st;
+    GqaBufs gb;
+    if (P.G > 1 && (st = gqa_setup(P, dtype, workspace, workspace_bytes, &gb)))
+        return st;
     SplitPlan S;
     SplitBufs b;
-    const bool split = use_split(P, dims, workspace, workspace_bytes, &S);
-    if (split && (st = split_setup(P, S, workspace, s, &b)))
+    const size_t off = schedule_bytes(P.N) + gqa_bytes(P, dtype);
+    const bool split = use_split(P, dims, workspace, workspace_bytes, off, &S);
+    if (split && (st = split_setup(P, S, workspace, off, s, &b)))
         return st;
     st = bwd_dq(P, dims, dtype, k, v, d_o, g_gamma, scale, initial_state, reverse, cu_seqlens,
                 order, dq, s, split ? &S : nullptr, split ? &b : nullptr);
@@ -638,7 +714,7 @@ la_status la_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *
         return st;
     return bwd_dkdv(P, dims, dtype, q, k, v, d_o, g_gamma, scale, d_final_state, reverse,
                     cu_seqlens, order, dk, dv, d_initial_state, s, split ? &S : nullptr,
-                    split ? &b : nullptr);
+                    split ? &b : nullptr, P.G > 1 ? &gb : nullptr);
 }
 
 la_status la_get_device_error(void *stream)
@@ -682,8 +758,8 @@ int32_t la_kernel_family(const la_dims *dims, int32_t dtype)
     a.D = P.D;
     a.E = P.E;
     a.q = tok(nullptr, dims->qk_strides);
-    a.k = tok(nullptr, dims->qk_strides);
-    a.v = tok(nullptr, dims->v_strides);
+    a.k = tok(nullptr, P.k_st, P.G);
+    a.v = tok(nullptr, P.kv_v_st, P.G);
     a.out = tok_out(nullptr, dims->v_strides);
     if (a.max_len <= la::SHORT_MAX_T && P.D <= 256)
         return 2;
@@ -702,8 +778,9 @@ size_t la_workspace_size_for(const la_dims *dims, int32_t dtype, const int32_t *
     if (st != LA_OK)
         return 0;
     const SplitPlan S = plan_split(P, dims);
-    if (S.NS > 0)
-        return schedule_bytes(P.N) + S.bytes;
+    const size_t gqa = gqa_bytes(P, dtype);
+    if (S.NS > 0 || gqa > 0)
+        return schedule_bytes(P.N) + gqa + S.bytes;
     return P.packed ? schedule_bytes(P.N) : 0;
 }
 

@@ -1,0 +1,69 @@
+// la_gqa.cu -- gradients of key/value heads shared by a group of query heads.
+//
+// With grouped key/value heads (the num_kv_heads axis of ejkernel
+// `recurrent`'s key and value) a key or value head feeds G query heads, so
+// its gradient is the sum of the G per-query-head gradients (each query head
+// has its own decay and state).  The backward sweeps write those per-query-
+// head contributions, dense [B, T, H, X], and this kernel sums each group in
+// fp32 and writes the result in the token dtype.
+
+#include <cuda_bf16.h>
+
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+template <typename T> __device__ __forceinline__ float ld(const T *p);
+template <> __device__ __forceinline__ float ld<float>(const float *p) { return *p; }
+template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    return __bfloat162float(*p);
+}
+template <typename T> __device__ __forceinline__ void st(T *p, float x);
+template <> __device__ __forceinline__ void st<float>(float *p, float x) { *p = x; }
+template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, float x)
+{
+    *p = __float2bfloat16_rn(x);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) gqa_reduce_kernel(const T *in, TokOut out, int T_, int Hkv,
+                                                         int G, int X, int64_t total)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % X);
+        int64_t r = i / X;
+        const int j = (int)(r % Hkv);
+        r /= Hkv;
+        const int64_t t = r % T_, b = r / T_;
+        const T *src = in + (((b * T_ + t) * Hkv + j) * G) * (int64_t)X + c;
+        float acc = 0.f;
+        for (int g = 0; g < G; ++g)
+            acc += ld(src + (int64_t)g * X);
+        st(reinterpret_cast<T *>(out.p) + b * out.sb + t * out.st + (int64_t)j * out.sh + c, acc);
+    }
+}
+
+}  // namespace
+
+cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv, int G, int X,
+                       int bf16, cudaStream_t s)
+{
+    const int64_t total = (int64_t)B * T * Hkv * X;
+    if (total == 0)
+        return cudaSuccess;
+    const int64_t want = (total + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 4096 ? want : 4096);   // grid-stride loop
+    if (bf16)
+        gqa_reduce_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(in), out, T, Hkv, G, X, total);
+    else
+        gqa_reduce_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(in), out, T,
+                                                        Hkv, G, X, total);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -26,10 +26,12 @@
 namespace la {
 
 // A token tensor: element (row, token, head, c) lives at
-// p + row*sb + token*st + head*sh + c   (elements of the token dtype).
+// p + row*sb + token*st + (head / hdiv)*sh + c   (elements of the token dtype);
+// hdiv > 1 for key/value tensors shared by groups of hdiv query heads.
 struct Tok {
     const void *p;
     int64_t sb, st, sh;
+    int hdiv = 1;
 };
 struct TokOut {
     void *p;
@@ -87,6 +89,12 @@ cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s);
 bool tc_sweep_supported(const SweepArgs &a);
 cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s);
+
+// Sum of grouped contributions (la_gqa.cu): out[b, t, j, c] = sum over
+// i < G of in[b, t, j*G + i, c] in fp32, for j < Hkv and c < X; `in` is dense
+// [B, T, Hkv*G, X] of the token dtype, `out` strided like a TokOut.
+cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv, int G, int X,
+                       int bf16, cudaStream_t s);
 
 // State scan of the sequence split (la_split.cu).  W holds one D x E fp32
 // state per (segment, head), [NS][H][D][E]; on entry the segments' results

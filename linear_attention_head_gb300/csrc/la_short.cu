@@ -118,9 +118,9 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
             if (idx < nqk && k < D) {
                 const int64_t t = token(u);
                 xq[i] = ld_tok(reinterpret_cast<const T *>(a.q.p) + row * a.q.sb + t * a.q.st +
-                               (int64_t)h * a.q.sh + k);
+                               (int64_t)(h / a.q.hdiv) * a.q.sh + k);
                 xk[i] = ld_tok(reinterpret_cast<const T *>(a.k.p) + row * a.k.sb + t * a.k.st +
-                               (int64_t)h * a.k.sh + k);
+                               (int64_t)(h / a.k.hdiv) * a.k.sh + k);
             }
         }
 #pragma unroll
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
             xw[i] = 0.f;
             if (idx < nw && e0 + k < a.E)
                 xw[i] = ld_tok(reinterpret_cast<const T *>(a.v.p) + row * a.v.sb +
-                               token(u) * a.v.st + (int64_t)h * a.v.sh + e0 + k);
+                               token(u) * a.v.st + (int64_t)(h / a.v.hdiv) * a.v.sh + e0 + k);
         }
 #pragma unroll
         for (int i = 0; i < PF; ++i) {

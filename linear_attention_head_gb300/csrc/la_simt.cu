@@ -58,7 +58,8 @@ __device__ __forceinline__ Seq seq_of(const SweepArgs &a, int n)
 template <typename T>
 __device__ __forceinline__ const T *tok(const Tok &t, int64_t row, int64_t tkn, int h)
 {
-    return reinterpret_cast<const T *>(t.p) + row * t.sb + tkn * t.st + (int64_t)h * t.sh;
+    return reinterpret_cast<const T *>(t.p) + row * t.sb + tkn * t.st +
+           (int64_t)(h / t.hdiv) * t.sh;
 }
 template <typename T>
 __device__ __forceinline__ T *tok(const TokOut &t, int64_t row, int64_t tkn, int h)

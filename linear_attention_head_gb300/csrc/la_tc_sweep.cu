@@ -92,6 +92,7 @@ template <int E> struct TcLayout {
 
 struct TcParams {
     CUtensorMap mx, my, mz, mo;
+    int dx, dy, dz;   // head divisors of the X, Y, Z tensors (grouped key/value heads)
     SweepArgs a;
 };
 
@@ -359,6 +360,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            // head coordinate of each tile (key/value heads may be shared)
+            const int hx = h / P.dx, hy = h / P.dy, hz = h / P.dz;
             int issued = 0;
             for (int c = 0; c < nc; ++c) {
                 const int s = c % TC_NST;
@@ -372,18 +375,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 // done, the X slot only once the output tile has left it
 #pragma unroll
                 for (int b = 0; b < TC_D / 64; ++b)
-                    tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, h, t0,
+                    tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, hy, t0,
                                 (int)row);
 #pragma unroll
                 for (int b = 0; b < E / 64; ++b)
-                    tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s], 64 * b, h,
+                    tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s], 64 * b, hz,
                                 t0, (int)row);
                 // X is copied even when this wait gives up, so that the drain
                 // below sees the stage complete
                 const bool xok = c < TC_NST || bwait(&xfree[s], ph, abort_flag);
 #pragma unroll
                 for (int b = 0; b < TC_D / 64; ++b)
-                    tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, h, t0, (int)row);
+                    tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, hx, t0, (int)row);
                 ++issued;
                 if (!xok)
                     break;
@@ -682,20 +685,21 @@ bool aligned_tok(const void *p, int64_t sb, int64_t st, int64_t sh)
 
 // 4-D map {channel, head, token, batch} with a {64, 1, rows, 1} box, 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t sb, int64_t st,
-              int64_t sh, int rows = TC_C)
+              int64_t sh, int rows = TC_C, int hdiv = 1)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     const int64_t lim = (int64_t)1 << 39;
     // a dimension of extent 1 never moves, any legal stride will do
-    if (a.H == 1)
+    const int heads = a.H / hdiv;
+    if (heads == 1)
         sh = X;
     if (a.B == 1)
         sb = st * (int64_t)a.T;
     if (sh <= 0 || st <= 0 || sb <= 0 || sh >= lim || st >= lim || sb >= lim)
         return false;
-    cuuint64_t dims[4] = {(cuuint64_t)X, (cuuint64_t)a.H, (cuuint64_t)a.T, (cuuint64_t)a.B};
+    cuuint64_t dims[4] = {(cuuint64_t)X, (cuuint64_t)heads, (cuuint64_t)a.T, (cuuint64_t)a.B};
     cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)st * 2, (cuuint64_t)sb * 2};
     cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
@@ -712,12 +716,15 @@ template <int E, bool BWD> cudaError_t launch_tc(const SweepArgs &a, cudaStream_
 {
     TcParams p;
     const Tok &x = BWD ? a.k : a.q, &y = BWD ? a.q : a.k;
-    if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh) ||
-        !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh) ||
-        !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh) ||
+    if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh, TC_C, x.hdiv) ||
+        !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh, TC_C, y.hdiv) ||
+        !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh, TC_C, a.v.hdiv) ||
         !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh, 32))
         return cudaErrorNotSupported;
     p.a = a;
+    p.dx = x.hdiv;
+    p.dy = y.hdiv;
+    p.dz = a.v.hdiv;
     auto kern = tc_sweep_kernel<E, BWD>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            TcLayout<E>::DYN);

@@ -55,10 +55,29 @@ def test_prototypes_match_header():
 
 
 def test_dims_struct_layout():
-    # int32 x 6 then two int64[3]: 24 + 48 bytes, no padding
-    assert ctypes.sizeof(N.LaDims) == 72
+    # int32 x 6, two int64[3], int32 x 2, two int64[3]: no padding anywhere
+    assert ctypes.sizeof(N.LaDims) == 128
     assert N.LaDims.qk_strides.offset == 24
     assert N.LaDims.v_strides.offset == 48
+    assert N.LaDims.kv_heads.offset == 72
+    assert N.LaDims.k_strides.offset == 80
+    assert N.LaDims.kv_v_strides.offset == 104
+
+
+def test_grouped_heads_are_validated(lib):
+    d = _dims(H=4)
+    d.kv_heads = 3                                   # does not divide 4
+    assert _fwd(lib, d) == N.LA_ERR_INVALID_ARG
+    assert "kv_heads" in N.last_error()
+    d.kv_heads = 5
+    assert _fwd(lib, d) == N.LA_ERR_INVALID_ARG
+    d = _dims(H=4)
+    d.reserved = 1
+    assert _fwd(lib, d) == N.LA_ERR_INVALID_ARG
+    d = _dims(H=4)
+    d.kv_heads = 2
+    d.k_strides[1] = -1
+    assert _fwd(lib, d) == N.LA_ERR_INVALID_ARG
 
 
 def test_strerror_and_version(lib):
