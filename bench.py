@@ -316,6 +316,7 @@ def gpu_bench(args):
         line["sweep"] = length_sweep(la, torch, dev, stream, T)
         line["decode"] = decode_bench(la, torch, dev, stream, peak)
         line["long_sequence"] = split_bench(la, torch, dev, stream, peak)
+        line["grouped_kv"] = gqa_bench(la, torch, dev, stream, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.n, args.cpu_pairs)
     if rank == 0:
@@ -455,6 +456,43 @@ def split_bench(la, torch, dev, stream, peak):
     la.get_device_error(dev)
     del q, k, v, do
     return out
+
+
+def gqa_bench(la, torch, dev, stream, peak):
+    """Grouped key/value heads: b4 h32 with 8 key/value heads, n32768 d=e=128 bf16.
+    la_fwd and la_bwd timed separately (mean of 5 queued calls after 2 warm-up
+    calls).  Algorithmic bytes: forward reads q and the shared k, v and writes o;
+    backward reads q, k, v, do and writes dq, dk, dv (k, v, dk, dv at 8 heads)."""
+    import workloads as W
+    B, T, H, Hkv, D = 4, 32768, 32, 8, 128
+    g = W.alibi_g_gamma(H).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(17)
+    q, do = (torch.randn((B, T, H, D), generator=gen, device=dev).bfloat16() for _ in range(2))
+    k, v = (torch.randn((B, T, Hkv, D), generator=gen, device=dev).bfloat16() for _ in range(2))
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 5
+
+    f_ms = timed(lambda: la.la_fwd(q, k, v, g, 1.0))
+    b_ms = timed(lambda: la.la_bwd(q, k, v, do, g, 1.0, want_d_initial_state=False))
+    full, kvu = B * T * H * D * 2, B * T * Hkv * D * 2
+    fb, bb = 2 * full + 2 * kvu, 3 * full + 4 * kvu + 2 * kvu
+    la.get_device_error(dev)
+    del q, k, v, do
+    return {"workload": "fwd+bwd b4 h32 kv_heads8 n32768 d=e=128 bf16, ALiBi slopes, scale 1",
+            "fwd_ms": f_ms, "bwd_ms": b_ms, "tokens_per_s": B * T / ((f_ms + b_ms) * 1e-3),
+            "fwd_frac_of_peak": fb / (f_ms * 1e-3) / 1e9 / peak,
+            "bwd_compulsory_frac_of_peak": bb / (b_ms * 1e-3) / 1e9 / peak}
 
 
 def source_sha():

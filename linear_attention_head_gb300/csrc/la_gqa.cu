@@ -7,6 +7,8 @@
 // head contributions, dense [B, T, H, X], and this kernel sums each group in
 // fp32 and writes the result in the token dtype.
 
+#include <cstdint>
+
 #include <cuda_bf16.h>
 
 #include "la_internal.h"
@@ -46,6 +48,43 @@ __global__ void __launch_bounds__(256) gqa_reduce_kernel(const T *in, TokOut out
     }
 }
 
+// Eight channels per thread with 16-byte loads and stores (bf16, X % 8 == 0,
+// 16-byte aligned output rows): one row of the input group is G x X
+// contiguous elements.
+__global__ void __launch_bounds__(256) gqa_reduce_bf16x8(const __nv_bfloat16 *in, TokOut out,
+                                                         int T_, int Hkv, int G, int X,
+                                                         int64_t total8)
+{
+    const int X8 = X / 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total8;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(i % X8);
+        int64_t r = i / X8;
+        const int j = (int)(r % Hkv);
+        r /= Hkv;
+        const int64_t t = r % T_, b = r / T_;
+        const __nv_bfloat16 *src = in + (((b * T_ + t) * Hkv + j) * G) * (int64_t)X + 8 * c8;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int g = 0; g < G; ++g) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(src + (int64_t)g * X);
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __bfloat1622float2(h2[k]);
+                acc[2 * k] += f.x;
+                acc[2 * k + 1] += f.y;
+            }
+        }
+        uint4 o;
+        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            o2[k] = __floats2bfloat162_rn(acc[2 * k], acc[2 * k + 1]);
+        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out.p) + b * out.sb +
+                                   t * out.st + (int64_t)j * out.sh + 8 * c8) = o;
+    }
+}
+
 }  // namespace
 
 cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv, int G, int X,
@@ -54,9 +93,16 @@ cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv,
     const int64_t total = (int64_t)B * T * Hkv * X;
     if (total == 0)
         return cudaSuccess;
-    const int64_t want = (total + 255) / 256;
-    const unsigned blocks = (unsigned)(want < 4096 ? want : 4096);   // grid-stride loop
-    if (bf16)
+    const bool vec = bf16 && X % 8 == 0 && out.sb % 8 == 0 && out.st % 8 == 0 && out.sh % 8 == 0 &&
+                     (reinterpret_cast<uintptr_t>(out.p) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(in) & 15) == 0;
+    const int64_t work = vec ? total / 8 : total;
+    const int64_t want = (work + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 16384 ? want : 16384);   // grid-stride loop
+    if (vec)
+        gqa_reduce_bf16x8<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(in), out, T,
+                                                 Hkv, G, X, work);
+    else if (bf16)
         gqa_reduce_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(in), out, T, Hkv, G, X, total);
     else
