@@ -10,7 +10,10 @@ S_t = exp(g_gamma[h]) * S_{t-1} + outer(k_t, v_t), o_t = scale * q_t^T S_t,
 with initial_state, reverse and packed cu_seqlens, and the gradient of
 sum(o*do) + sum(final*dfinal) with respect to q, k, v and initial_state
 (the `_recurrent_bwd` custom VJP on the same page; g_gamma, scale, reverse and
-cu_seqlens are not differentiated).  This module only marshals numpy arrays.
+cu_seqlens are not differentiated).  gla_forward / gla_backward add the
+per-key gate g [B,T,H,d] (the page's GLA-style gate, read as a log-decay per
+key channel added to g_gamma) and its gradient dg.  This module only marshals
+numpy arrays.
 
 Pins: every function here is checked in tests/test_oracle_*.py against a
 brute-force quadratic form, closed forms, invariants and finite differences.
@@ -41,6 +44,16 @@ def _load():
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, _ip, _dp, _dp, _dp, _dp, ctypes.c_double, _dp,
             ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+        lib.la_oracle_gla_fwd.restype = ctypes.c_int
+        lib.la_oracle_gla_fwd.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, _ip, _dp, _dp, _dp, _dp, _dp, ctypes.c_double, _dp,
+            ctypes.c_int, _dp, _dp, ctypes.c_int]
+        lib.la_oracle_gla_bwd.restype = ctypes.c_int
+        lib.la_oracle_gla_bwd.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, _ip, _dp, _dp, _dp, _dp, _dp, ctypes.c_double, _dp,
+            ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -115,3 +128,44 @@ def backward(q, k, v, g_gamma, scale, dout, initial_state=None, d_final_state=No
     if rc:
         raise RuntimeError("la_oracle_bwd failed (%d)" % rc)
     return dq, dk, dv, dinit
+
+
+def gla_forward(q, k, v, g, g_gamma, scale, initial_state=None, reverse=False,
+                cu_seqlens=None, threads=0):
+    """Gated forward, g [B,T,H,d]: returns (o, final_state) in float64."""
+    q, k, v, gt, gg, init = map(_f64, (q, k, v, g, g_gamma, initial_state))
+    B, T, H, d, e, N, cu = _check(q, k, v, cu_seqlens, init)
+    if gt.shape != q.shape:
+        raise ValueError("g must have the keys' shape")
+    gg = np.ascontiguousarray(np.broadcast_to(gg, (H,)))
+    o = np.zeros((B, T, H, e))
+    fin = np.zeros((N, H, d, e))
+    rc = _load().la_oracle_gla_fwd(B, T, H, d, e, N, _ptr(cu, _ip), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(gg), _ptr(gt), float(scale), _ptr(init),
+                                   int(bool(reverse)), _ptr(o), _ptr(fin), int(threads))
+    if rc:
+        raise RuntimeError("la_oracle_gla_fwd failed (%d)" % rc)
+    return o, fin
+
+
+def gla_backward(q, k, v, g, g_gamma, scale, dout, initial_state=None, d_final_state=None,
+                 reverse=False, cu_seqlens=None, threads=0):
+    """Gated backward: returns (dq, dk, dv, dg, d_initial_state) in float64."""
+    q, k, v, gt, gg, init, do, dfin = map(_f64, (q, k, v, g, g_gamma, initial_state, dout,
+                                                 d_final_state))
+    B, T, H, d, e, N, cu = _check(q, k, v, cu_seqlens, init)
+    if gt.shape != q.shape or do.shape != v.shape:
+        raise ValueError("g must have the keys' shape and dout the values'")
+    if dfin is not None and dfin.shape != (N, H, d, e):
+        raise ValueError("d_final_state must be [N,H,d,e]")
+    gg = np.ascontiguousarray(np.broadcast_to(gg, (H,)))
+    dq, dk, dg = np.zeros((B, T, H, d)), np.zeros((B, T, H, d)), np.zeros((B, T, H, d))
+    dv = np.zeros((B, T, H, e))
+    dinit = np.zeros((N, H, d, e))
+    rc = _load().la_oracle_gla_bwd(B, T, H, d, e, N, _ptr(cu, _ip), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(gg), _ptr(gt), float(scale), _ptr(init),
+                                   int(bool(reverse)), _ptr(do), _ptr(dfin), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), _ptr(dg), _ptr(dinit), int(threads))
+    if rc:
+        raise RuntimeError("la_oracle_gla_bwd failed (%d)" % rc)
+    return dq, dk, dv, dg, dinit

@@ -35,6 +35,19 @@
  *                               d_initial_state = G
  *   (G before the decay is dL/dS_t; the last decay carries it back to S_0.)
  *
+ * Gated form (ejkernel `recurrent` Args: a gate tensor for GLA-style gating
+ * with the keys' shape; the GLA page's `recurrent_gla` passes it on to
+ * `recurrent`).  Read as a log-decay per key channel, added to the head's
+ * g_gamma:
+ *        S_t[a, :] = exp(g_gamma[h] + g_t[a]) * S_{t-1}[a, :] + k_t[a] v_t
+ * (the gate of token t multiplies the state that token t is added to, in
+ * either direction).  Backward as above with the row-wise decay, and
+ *        dg_t[a] = exp(g_gamma[h] + g_t[a]) * sum_b G_t[a, b] S_{t-1}[a, b]
+ * with G_t = dL/dS_t (after token t's term, before its decay) and S_{t-1}
+ * the state token t decays.  Sweep B needs S_{t-1} in reverse order: the
+ * forward states are kept every K = ceil(sqrt(L)) tokens and each block of K
+ * is recomputed from its checkpoint when sweep B reaches it.
+ *
  * Layout: every token tensor is a dense row-major fp64 array [B, T, H, X]
  * (X = d for q, k, dq, dk and e for v, o, do, dv); states are [N, H, d, e].
  * With cu_seqlens (B must be 1) sequence n covers tokens cu[n] .. cu[n+1]-1
@@ -57,6 +70,7 @@ typedef struct {
     int B, T, H, d, e, N;
     const int32_t *cu;          /* [N+1] or NULL */
     const double *q, *k, *v, *g_gamma, *init;
+    const double *gate;         /* [B,T,H,d] per-key log-decay, or NULL */
     double scale;
     int reverse;
     /* forward outputs */
@@ -64,6 +78,7 @@ typedef struct {
     /* backward inputs / outputs */
     const double *dout, *dfinal;
     double *dq, *dk, *dv, *dinit;
+    double *dgate;              /* [B,T,H,d], written when gate is given */
     int mode;                   /* 0 = forward, 1 = backward */
     /* work distribution */
     int next;                   /* next (n, h) task, guarded by lock */
@@ -97,10 +112,29 @@ static inline double *tok_w(double *base, const job_t *J, int64_t row, int64_t t
     return base + (((row * J->T + t) * J->H) + h) * (int64_t)width;
 }
 
+/* decay of row a at token t of batch row `row` */
+static inline double decay(const job_t *J, int64_t row, int64_t t, int h, int a, double gh)
+{
+    return J->gate ? exp(gh + tok(J->gate, J, row, t, h, J->d)[a]) : exp(gh);
+}
+
+/* S <- diag(decay_t) S + outer(k_t, v_t) */
+static void step_state(const job_t *J, int64_t row, int64_t t, int h, double *S)
+{
+    const int d = J->d, e = J->e;
+    const double gh = J->g_gamma[h];
+    const double *kt = tok(J->k, J, row, t, h, d);
+    const double *vt = tok(J->v, J, row, t, h, e);
+    for (int a = 0; a < d; ++a) {
+        const double da = decay(J, row, t, h, a, gh);
+        for (int b = 0; b < e; ++b)
+            S[a * e + b] = da * S[a * e + b] + kt[a] * vt[b];
+    }
+}
+
 static void run_forward(const job_t *J, int n, int h, double *S)
 {
     const int d = J->d, e = J->e;
-    const double gamma = exp(J->g_gamma[h]);
     int64_t bos, len, row;
     seq_range(J, n, &bos, &len, &row);
     const int64_t sidx = ((int64_t)n * J->H + h) * d * e;
@@ -110,12 +144,8 @@ static void run_forward(const job_t *J, int n, int h, double *S)
         memset(S, 0, sizeof(double) * d * e);
     for (int64_t step = 0; step < len; ++step) {
         const int64_t t = bos + (J->reverse ? len - 1 - step : step);
-        const double *kt = tok(J->k, J, row, t, h, d);
-        const double *vt = tok(J->v, J, row, t, h, e);
         const double *qt = tok(J->q, J, row, t, h, d);
-        for (int a = 0; a < d; ++a)
-            for (int b = 0; b < e; ++b)
-                S[a * e + b] = gamma * S[a * e + b] + kt[a] * vt[b];
+        step_state(J, row, t, h, S);
         double *ot = tok_w(J->o, J, row, t, h, e);
         for (int b = 0; b < e; ++b) {
             double acc = 0.0;
@@ -128,27 +158,32 @@ static void run_forward(const job_t *J, int n, int h, double *S)
         memcpy(J->final_state + sidx, S, sizeof(double) * d * e);
 }
 
-static void run_backward(const job_t *J, int n, int h, double *S)
+static void run_backward(const job_t *J, int n, int h, double *S, double *ck)
 {
     const int d = J->d, e = J->e;
-    const double gamma = exp(J->g_gamma[h]);
+    const int64_t de = (int64_t)d * e;
+    const double gh = J->g_gamma[h];
     int64_t bos, len, row;
     seq_range(J, n, &bos, &len, &row);
-    const int64_t sidx = ((int64_t)n * J->H + h) * d * e;
+    const int64_t sidx = ((int64_t)n * J->H + h) * de;
+    /* gated: checkpoint every K tokens; ck holds the block-start states, then
+     * the K + 1 states of the block being replayed */
+    int64_t K = 1;
+    while (K * K < len)
+        ++K;
+    double *blk = ck ? ck + ((len + K - 1) / K) * de : NULL;
 
     /* sweep A: recompute the forward states, dq_t = scale * S_t do_t */
     if (J->init)
-        memcpy(S, J->init + sidx, sizeof(double) * d * e);
+        memcpy(S, J->init + sidx, sizeof(double) * de);
     else
-        memset(S, 0, sizeof(double) * d * e);
+        memset(S, 0, sizeof(double) * de);
     for (int64_t step = 0; step < len; ++step) {
         const int64_t t = bos + (J->reverse ? len - 1 - step : step);
-        const double *kt = tok(J->k, J, row, t, h, d);
-        const double *vt = tok(J->v, J, row, t, h, e);
+        if (J->gate && step % K == 0)
+            memcpy(ck + (step / K) * de, S, sizeof(double) * de);
         const double *dot = tok(J->dout, J, row, t, h, e);
-        for (int a = 0; a < d; ++a)
-            for (int b = 0; b < e; ++b)
-                S[a * e + b] = gamma * S[a * e + b] + kt[a] * vt[b];
+        step_state(J, row, t, h, S);
         double *dqt = tok_w(J->dq, J, row, t, h, d);
         for (int a = 0; a < d; ++a) {
             double acc = 0.0;
@@ -161,11 +196,21 @@ static void run_backward(const job_t *J, int n, int h, double *S)
     /* sweep B: carry G = dL/dS backwards through the processing order */
     double *G = S;
     if (J->dfinal)
-        memcpy(G, J->dfinal + sidx, sizeof(double) * d * e);
+        memcpy(G, J->dfinal + sidx, sizeof(double) * de);
     else
-        memset(G, 0, sizeof(double) * d * e);
+        memset(G, 0, sizeof(double) * de);
     for (int64_t step = len - 1; step >= 0; --step) {
         const int64_t t = bos + (J->reverse ? len - 1 - step : step);
+        if (J->gate && (step == len - 1 || step % K == K - 1)) {
+            /* replay the block holding `step`: blk[i] = state before step b0 + i */
+            const int64_t b0 = (step / K) * K;
+            memcpy(blk, ck + (step / K) * de, sizeof(double) * de);
+            for (int64_t i = 0; b0 + i < step; ++i) {
+                const int64_t ti = bos + (J->reverse ? len - 1 - (b0 + i) : b0 + i);
+                memcpy(blk + (i + 1) * de, blk + i * de, sizeof(double) * de);
+                step_state(J, row, ti, h, blk + (i + 1) * de);
+            }
+        }
         const double *qt = tok(J->q, J, row, t, h, d);
         const double *kt = tok(J->k, J, row, t, h, d);
         const double *vt = tok(J->v, J, row, t, h, e);
@@ -187,19 +232,45 @@ static void run_backward(const job_t *J, int n, int h, double *S)
                 acc += G[a * e + b] * kt[a];
             dvt[b] = acc;
         }
-        for (int a = 0; a < d * e; ++a)
-            G[a] *= gamma;
+        if (J->gate) {
+            const double *prev = blk + (step % K) * de;   /* S_{t-1} */
+            double *dgt = tok_w(J->dgate, J, row, t, h, d);
+            for (int a = 0; a < d; ++a) {
+                double acc = 0.0;
+                for (int b = 0; b < e; ++b)
+                    acc += G[a * e + b] * prev[a * e + b];
+                dgt[a] = decay(J, row, t, h, a, gh) * acc;
+            }
+        }
+        for (int a = 0; a < d; ++a) {
+            const double da = decay(J, row, t, h, a, gh);
+            for (int b = 0; b < e; ++b)
+                G[a * e + b] *= da;
+        }
     }
     if (J->dinit)
-        memcpy(J->dinit + sidx, G, sizeof(double) * d * e);
+        memcpy(J->dinit + sidx, G, sizeof(double) * de);
 }
 
 static void *worker(void *arg)
 {
     job_t *J = (job_t *)arg;
-    double *S = (double *)malloc(sizeof(double) * (size_t)J->d * (size_t)J->e);
-    if (!S)
+    const size_t de = (size_t)J->d * (size_t)J->e;
+    double *S = (double *)malloc(sizeof(double) * de);
+    /* gated backward: checkpoints of the longest sequence plus one block */
+    size_t ck_states = 0;
+    if (J->gate && J->mode == 1) {
+        int64_t K = 1;
+        while (K * K < J->T)
+            ++K;
+        ck_states = (size_t)(2 * K + 2);   /* >= ceil(L/K_L) + K_L for every L <= T */
+    }
+    double *ck = ck_states ? (double *)malloc(sizeof(double) * de * ck_states) : NULL;
+    if (!S || (ck_states && !ck)) {
+        free(S);
+        free(ck);
         return (void *)1;
+    }
     for (;;) {
         pthread_mutex_lock(&J->lock);
         const int task = J->next++;
@@ -210,9 +281,10 @@ static void *worker(void *arg)
         if (J->mode == 0)
             run_forward(J, n, h, S);
         else
-            run_backward(J, n, h, S);
+            run_backward(J, n, h, S, ck);
     }
     free(S);
+    free(ck);
     return NULL;
 }
 
@@ -265,40 +337,68 @@ static int fill_common(job_t *J, int B, int T, int H, int d, int e, int num_seqs
 }
 
 /* Forward: writes o [B,T,H,e] and, if final_state is not NULL, [N,H,d,e].
+ * gate: [B,T,H,d] per-key log-decay added to g_gamma, or NULL.
  * Returns 0 on success, 2 on bad sizes, 1 on a thread/allocation failure. */
-int la_oracle_fwd(int B, int T, int H, int d, int e, int num_seqs, const int32_t *cu_seqlens,
-                  const double *q, const double *k, const double *v,
-                  const double *g_gamma, double scale, const double *initial_state,
-                  int reverse, double *o, double *final_state, int threads)
+int la_oracle_gla_fwd(int B, int T, int H, int d, int e, int num_seqs,
+                      const int32_t *cu_seqlens, const double *q, const double *k,
+                      const double *v, const double *g_gamma, const double *gate, double scale,
+                      const double *initial_state, int reverse, double *o, double *final_state,
+                      int threads)
 {
     job_t J;
     int rc = fill_common(&J, B, T, H, d, e, num_seqs, cu_seqlens, q, k, v, g_gamma,
                          scale, initial_state, reverse);
     if (rc)
         return rc;
+    J.gate = gate;
     J.mode = 0;
     J.o = o;
     J.final_state = final_state;
     return run_job(&J, threads);
 }
 
-/* Backward: writes dq, dk [B,T,H,d], dv [B,T,H,e] and, if d_initial_state is
- * not NULL, [N,H,d,e].  dout is dL/do; d_final_state (or NULL = 0) is
- * dL/dfinal_state. */
-int la_oracle_bwd(int B, int T, int H, int d, int e, int num_seqs, const int32_t *cu_seqlens,
+int la_oracle_fwd(int B, int T, int H, int d, int e, int num_seqs, const int32_t *cu_seqlens,
                   const double *q, const double *k, const double *v,
                   const double *g_gamma, double scale, const double *initial_state,
-                  int reverse, const double *dout, const double *d_final_state,
-                  double *dq, double *dk, double *dv, double *d_initial_state, int threads)
+                  int reverse, double *o, double *final_state, int threads)
+{
+    return la_oracle_gla_fwd(B, T, H, d, e, num_seqs, cu_seqlens, q, k, v, g_gamma, NULL, scale,
+                             initial_state, reverse, o, final_state, threads);
+}
+
+/* Backward: writes dq, dk [B,T,H,d], dv [B,T,H,e], with a gate dgate
+ * [B,T,H,d], and, if d_initial_state is not NULL, [N,H,d,e].  dout is dL/do;
+ * d_final_state (or NULL = 0) is dL/dfinal_state. */
+int la_oracle_gla_bwd(int B, int T, int H, int d, int e, int num_seqs,
+                      const int32_t *cu_seqlens, const double *q, const double *k,
+                      const double *v, const double *g_gamma, const double *gate, double scale,
+                      const double *initial_state, int reverse, const double *dout,
+                      const double *d_final_state, double *dq, double *dk, double *dv,
+                      double *dgate, double *d_initial_state, int threads)
 {
     job_t J;
     int rc = fill_common(&J, B, T, H, d, e, num_seqs, cu_seqlens, q, k, v, g_gamma,
                          scale, initial_state, reverse);
     if (rc)
         return rc;
+    if (gate && !dgate)
+        return 2;
+    J.gate = gate;
+    J.dgate = dgate;
     J.mode = 1;
     J.dout = dout;
     J.dfinal = d_final_state;
     J.dq = dq; J.dk = dk; J.dv = dv; J.dinit = d_initial_state;
     return run_job(&J, threads);
+}
+
+int la_oracle_bwd(int B, int T, int H, int d, int e, int num_seqs, const int32_t *cu_seqlens,
+                  const double *q, const double *k, const double *v,
+                  const double *g_gamma, double scale, const double *initial_state,
+                  int reverse, const double *dout, const double *d_final_state,
+                  double *dq, double *dk, double *dv, double *d_initial_state, int threads)
+{
+    return la_oracle_gla_bwd(B, T, H, d, e, num_seqs, cu_seqlens, q, k, v, g_gamma, NULL, scale,
+                             initial_state, reverse, dout, d_final_state, dq, dk, dv, NULL,
+                             d_initial_state, threads);
 }

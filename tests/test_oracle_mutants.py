@@ -23,19 +23,28 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "la_oracle.c")
 MUTANTS = [
     ("transposed_kv_outer", "kt[a] * vt[b];", "kt[b % d] * vt[a % e];", 0),
     ("dropped_scale", "ot[b] = J->scale * acc;", "ot[b] = acc;", 0),
-    ("wrong_decay_sign", "exp(J->g_gamma[h])", "exp(-J->g_gamma[h])", 0),
+    ("wrong_decay_sign", ": exp(gh);", ": exp(-gh);", 0),
     ("dropped_initial_state", "memcpy(S, J->init + sidx, sizeof(double) * d * e);",
      "memset(S, 0, sizeof(double) * d * e);", 0),
     ("ignored_reverse_fwd", "J->reverse ? len - 1 - step : step", "step", 0),
-    ("read_before_update", "S[a * e + b] = gamma * S[a * e + b] + kt[a] * vt[b];",
-     "S[a * e + b] = S[a * e + b] + kt[a] * vt[b] * gamma;", 0),
+    ("read_before_update", "S[a * e + b] = da * S[a * e + b] + kt[a] * vt[b];",
+     "S[a * e + b] = S[a * e + b] + kt[a] * vt[b] * da;", 0),
     ("dq_missing_scale", "dqt[a] = J->scale * acc;", "dqt[a] = acc;", 0),
-    ("dropped_bwd_decay", "G[a] *= gamma;", "G[a] *= 1.0;", 0),
+    ("dropped_bwd_decay", "G[a * e + b] *= da;", "G[a * e + b] *= 1.0;", 0),
     ("dv_wrong_operand", "acc += G[a * e + b] * kt[a];", "acc += G[a * e + b] * qt[a];", 0),
     ("dk_transposed_state", "acc += G[a * e + b] * vt[b];", "acc += G[b * e + a % e] * vt[b];", 0),
-    ("dropped_dfinal", "memcpy(G, J->dfinal + sidx, sizeof(double) * d * e);",
-     "memset(G, 0, sizeof(double) * d * e);", 0),
+    ("dropped_dfinal", "memcpy(G, J->dfinal + sidx, sizeof(double) * de);",
+     "memset(G, 0, sizeof(double) * de);", 0),
     ("ignored_reverse_bwd", "J->reverse ? len - 1 - step : step", "step", 2),
+]
+
+# Mutants of the gated (per-key decay) form, checked by the gated pins.
+GATED_MUTANTS = [
+    ("dg_missing_decay", "dgt[a] = decay(J, row, t, h, a, gh) * acc;", "dgt[a] = acc;", 0),
+    ("gate_of_first_channel", "const double da = decay(J, row, t, h, a, gh);",
+     "const double da = decay(J, row, t, h, 0, gh);", 0),
+    ("dg_uses_next_state", "const double *prev = blk + (step % K) * de;",
+     "const double *prev = blk + ((step + 1) % K) * de;", 0),
 ]
 
 
@@ -51,7 +60,7 @@ def _compile(tmp_path, name, text):
 def _bind(path, monkeypatch):
     real = oracle._load()
     lib = ctypes.CDLL(path)
-    for fn in ("la_oracle_fwd", "la_oracle_bwd"):
+    for fn in ("la_oracle_fwd", "la_oracle_bwd", "la_oracle_gla_fwd", "la_oracle_gla_bwd"):
         getattr(lib, fn).restype = getattr(real, fn).restype
         getattr(lib, fn).argtypes = getattr(real, fn).argtypes
     monkeypatch.setattr(oracle, "_lib", lib)
@@ -91,3 +100,47 @@ def test_mutant_is_rejected(tmp_path, monkeypatch, name, old, new, occ):
     mutated = old.join(parts[:occ + 1]) + new + old.join(parts[occ + 1:])
     _bind(_compile(tmp_path, name, mutated), monkeypatch)
     assert not _pins_pass(), name + " slipped through the pins"
+
+
+def _gated_pins_pass():
+    """Gated form: forward against the pairwise-decay brute force of
+    test_oracle_gla, and dg against the identity from dq and dk."""
+    from test_oracle_gla import _brute, _problem
+    for seed, reverse in ((0, False), (1, True)):
+        q, k, v, do, g, gg, s0, dfin = _problem(B=2, T=9, H=2, d=4, e=3, seed=seed)
+        o, fin = oracle.gla_forward(q, k, v, g, gg, 0.6, s0, reverse)
+        ob, fb = _brute(q, k, v, g, gg, 0.6, s0, reverse)
+        if not (np.allclose(o, ob, rtol=1e-10, atol=1e-12) and
+                np.allclose(fin, fb, rtol=1e-10, atol=1e-12)):
+            return False
+        dq, dk, dv, dg, ds0 = oracle.gla_backward(q, k, v, g, gg, 0.6, do, s0, dfin, reverse)
+        dG = q * dq - k * dk
+        order = np.arange(9)[::-1] if reverse else np.arange(9)
+        dG[:, order[-1]] += np.einsum("bhde,bhde->bhd", fin, dfin)
+        run = np.zeros((2, 2, 4))
+        ident = np.zeros_like(dG)
+        for t in order[::-1]:
+            run = run + dG[:, t]
+            ident[:, t] = run
+        if not np.allclose(dg, ident, rtol=1e-9, atol=1e-11):
+            return False
+    return True
+
+
+def test_unmodified_copy_passes_gated_pins(tmp_path, monkeypatch):
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    _bind(_compile(tmp_path, "original_g", open(SRC).read()), monkeypatch)
+    assert _gated_pins_pass()
+
+
+@pytest.mark.parametrize("name,old,new,occ", GATED_MUTANTS, ids=[m[0] for m in GATED_MUTANTS])
+def test_gated_mutant_is_rejected(tmp_path, monkeypatch, name, old, new, occ):
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    text = open(SRC).read()
+    parts = text.split(old)
+    assert len(parts) > occ + 1, "mutation site not found: " + old
+    mutated = old.join(parts[:occ + 1]) + new + old.join(parts[occ + 1:])
+    _bind(_compile(tmp_path, name, mutated), monkeypatch)
+    assert not _gated_pins_pass(), name + " slipped through the gated pins"
