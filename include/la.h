@@ -241,6 +241,49 @@ size_t la_workspace_size_for(const la_dims *dims, int32_t dtype, const int32_t *
  * other values. */
 la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens);
 
+/* Gated form (GLA): ejkernel `recurrent` with its gate g (the GLA page's
+ * `recurrent_gla` passes it on), a log-decay per key channel added to the
+ * head's g_gamma:
+ *     S_t[a, :] = exp(g_gamma[h] + g_t[a]) * S_{t-1}[a, :] + k_t[a] v_t,
+ *     o_t = scale * q_t^T S_t
+ * (the reading of the pages' "GLA-style gating"; the gate of token t decays
+ * the state token t is added to, in either direction).
+ *   g          [B,T,H,D] fp32 gate, channel-contiguous, element strides
+ *              g_strides[3] = (batch, token, head)
+ *   g_gamma    [H] fp32, required (zeros for no head decay)
+ *   everything else as la_fwd; kv_heads must be 0 (or H); no workspace.
+ * Runs the token-by-token kernels at any length.  Not differentiated:
+ * g_gamma, scale, reverse, cu_seqlens. */
+la_status la_gla_fwd(const la_dims *dims, int32_t dtype,
+                     const void *q, const void *k, const void *v,
+                     const float *g, const int64_t *g_strides,
+                     const float *g_gamma, float scale,
+                     const float *initial_state, int32_t reverse,
+                     const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                     void *o, float *final_state, void *stream);
+
+/* Backward of la_gla_fwd: dq, dk, dv, d_initial_state as la_bwd, and
+ * dg [B,T,H,D] fp32 (g_strides), the gradient of the gate:
+ *     dg_w = sum over t at or after w (processing order) of
+ *            q_t dq_t - k_t dk_t (+ sum_e F dF at the last token),
+ * F the final state and dF = d_final_state.  Needs a 256-byte aligned device
+ * workspace of la_gla_workspace_size bytes (LA_ERR_INVALID_ARG otherwise). */
+la_status la_gla_bwd(const la_dims *dims, int32_t dtype,
+                     const void *q, const void *k, const void *v, const void *d_o,
+                     const float *g, const int64_t *g_strides,
+                     const float *g_gamma, float scale,
+                     const float *initial_state, const float *d_final_state,
+                     int32_t reverse,
+                     const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                     void *dq, void *dk, void *dv, float *dg, float *d_initial_state,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of la_gla_bwd for these sizes (0 for invalid sizes).
+ * cu_seqlens_host: host copy of cu_seqlens for packed sequences, else NULL.
+ * Pure host function. */
+size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype,
+                             const int32_t *cu_seqlens_host);
+
 /* Reads and clears the device-side error word that bounded on-device waits
  * set when they run out (LA_ERR_TIMEOUT), after synchronizing `stream`.
  * Returns LA_OK when no wait ran out, LA_ERR_TIMEOUT when one did, or

@@ -293,6 +293,97 @@ def kernel_family(B, T, H, D, E, dtype=torch.bfloat16, layout="bthd") -> int:
     return int(N.lib().la_kernel_family(ctypes.byref(d), code))
 
 
+def _gate(g, q):
+    """The per-key gate as fp32 with a contiguous channel dimension."""
+    if tuple(g.shape) != tuple(q.shape):
+        raise ValueError("g must have the queries' shape %s, got %s"
+                         % (tuple(q.shape), tuple(g.shape)))
+    g = g.to(device=q.device, dtype=torch.float32)
+    return g if g.stride(-1) == 1 else g.contiguous()
+
+
+def _strides3(t):
+    return (ctypes.c_int64 * 3)(*t.stride()[:3])
+
+
+def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
+            scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
+            reverse: bool = False, cu_seqlens=None) -> Tuple[Tensor, Tensor]:
+    """Gated forward (GLA): row a of the state decays by exp(g_gamma[h] + g_t[a]) at
+    token t.  q, k, g: [B,T,H,D]; v: [B,T,H,E].  Returns (o, final_state)."""
+    _check_tokens(q, k, v)
+    if k.shape[2] != q.shape[2]:
+        raise ValueError("the gated form needs keys and values with the queries' heads")
+    q, k, v = _channel_contiguous((q, k, v))
+    q, k = _same_strides([q, k])
+    dev = q.device
+    g = _gate(g, q)
+    packed = _Packed(cu_seqlens, dev)
+    B, T, H, D = q.shape
+    E = v.shape[3]
+    Nst = _num_states(q, packed)
+    gg = _g(torch.zeros(H) if g_gamma is None else g_gamma, H, dev)
+    scale = float(D ** -0.5 if scale is None else scale)
+    init = _state(initial_state, (Nst, H, D, E), dev, "initial_state")
+    out = _like(v)
+    fin = torch.empty((Nst, H, D, E), device=dev, dtype=torch.float32)
+    dims = _dims(q, k, v, out, packed)
+    gs = _strides3(g)
+    st = N.lib().la_gla_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
+                            _ptr(g), gs, _ptr(gg), scale, _ptr(init), int(bool(reverse)),
+                            _ptr(packed.dev), packed.host_ptr(), _ptr(out), _ptr(fin),
+                            _stream(dev))
+    N.check(st)
+    return out, fin
+
+
+def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_final_state=None,
+            reverse=False, cu_seqlens=None, want_d_initial_state=True):
+    """Backward of gla_fwd: returns (dq, dk, dv, dg, d_initial_state)."""
+    q, k, v, do, dev, packed, gg, scale, init, dfin, Nst = _bwd_prep(
+        q, k, v, do, torch.zeros(q.shape[2]) if g_gamma is None else g_gamma, scale,
+        initial_state, d_final_state, cu_seqlens)
+    if k.shape[2] != q.shape[2]:
+        raise ValueError("the gated form needs keys and values with the queries' heads")
+    g = _gate(g, q)
+    dq, dk, dv = _like(q), _like(k), _like(v)
+    dg = torch.empty_strided(g.shape, g.stride(), dtype=torch.float32, device=dev)
+    dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
+                         dtype=torch.float32) if want_d_initial_state else None)
+    dims = _dims(q, k, v, do, packed)
+    nbytes = int(N.lib().la_gla_workspace_size(ctypes.byref(dims), _dtype_code(q),
+                                              packed.host_ptr()))
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    st = N.lib().la_gla_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
+                            _ptr(do), _ptr(g), _strides3(g), _ptr(gg), scale, _ptr(init),
+                            _ptr(dfin), int(bool(reverse)), _ptr(packed.dev), packed.host_ptr(),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dinit),
+                            ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(dev))
+    N.check(st)
+    return dq, dk, dv, dg, dinit
+
+
+class _GatedLinearAttention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, init, gg, scale, reverse, cu):
+        o, fin = gla_fwd(q, k, v, g, gg, scale, init, reverse, cu)
+        ctx.save_for_backward(q, k, v, g, init, gg)
+        ctx.scale, ctx.reverse, ctx.cu = scale, reverse, cu
+        ctx.has_init = init is not None
+        return o, fin
+
+    @staticmethod
+    def backward(ctx, do, dfin):
+        q, k, v, g, init, gg = ctx.saved_tensors
+        if do is None:
+            do = torch.zeros(q.shape[:3] + v.shape[3:], dtype=v.dtype, device=v.device)
+        dq, dk, dv, dg, dinit = gla_bwd(q, k, v, do.to(v.dtype), g, gg, ctx.scale,
+                                        init if ctx.has_init else None, dfin, ctx.reverse,
+                                        ctx.cu, want_d_initial_state=ctx.has_init)
+        return (dq, dk, dv, dg.to(g.dtype), (dinit if ctx.has_init else None), None, None,
+                None, None)
+
+
 class _LinearAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, init, g, scale, reverse, cu):
@@ -316,16 +407,18 @@ class _LinearAttention(torch.autograd.Function):
 def recurrent(query: Tensor, key: Tensor, value: Tensor, g=None, g_gamma=None, gk=None, gv=None,
               softmax_scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
               reverse: bool = False, cu_seqlens=None):
-    """ejkernel `recurrent` with the Lightning per-head `g_gamma` gate (the only gate on
-    this path).  Accepts [B,T,H,D] or packed [T_total,H,D] with cu_seqlens.
-    Returns (o, final_state); differentiable in query, key, value, initial_state."""
-    if g is not None or gk is not None or gv is not None:
-        raise NotImplementedError("only the per-head g_gamma decay is implemented")
+    """ejkernel `recurrent` with the per-head `g_gamma` decay and the GLA-style gate `g`
+    (a log-decay per key channel, [B,T,H,D]; gk / gv are not implemented).  Accepts
+    [B,T,H,D] or packed [T_total,H,D] with cu_seqlens.  Returns (o, final_state);
+    differentiable in query, key, value, g and initial_state."""
+    if gk is not None or gv is not None:
+        raise NotImplementedError("the gk / gv gates are not implemented")
     squeeze = False
     if query.ndim == 3:
         if cu_seqlens is None:
             raise ValueError("3-D inputs need cu_seqlens")
         query, key, value = query[None], key[None], value[None]
+        g = None if g is None else g[None]
         squeeze = True
     if cu_seqlens is not None and query.shape[0] != 1:
         raise ValueError("The batch size is expected to be 1 rather than %d when using "
@@ -333,12 +426,37 @@ def recurrent(query: Tensor, key: Tensor, value: Tensor, g=None, g_gamma=None, g
     H = query.shape[2]
     if g_gamma is None:
         g_gamma = torch.zeros(H, dtype=torch.float32)
-    g = _g(g_gamma, H, query.device)
+    gg = _g(g_gamma, H, query.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(query.shape[-1])
-    o, fin = _LinearAttention.apply(query, key, value, initial_state, g, softmax_scale,
-                                    bool(reverse), cu_seqlens)
+    if g is not None:
+        o, fin = _GatedLinearAttention.apply(query, key, value, g, initial_state, gg,
+                                             softmax_scale, bool(reverse), cu_seqlens)
+    else:
+        o, fin = _LinearAttention.apply(query, key, value, initial_state, gg, softmax_scale,
+                                        bool(reverse), cu_seqlens)
     return (o[0] if squeeze else o), fin
+
+
+def recurrent_gla(query: Tensor, key: Tensor, value: Tensor, g: Optional[Tensor] = None,
+                  g_gamma=None, softmax_scale: Optional[float] = None,
+                  initial_state: Optional[Tensor] = None, reverse: bool = False,
+                  cu_seqlens=None):
+    """ejkernel `recurrent_gla` (the GLA page): the batch-1 / initial-state count
+    checks of that page, the default scale from the key width, then `recurrent`."""
+    if cu_seqlens is not None:
+        if query.ndim == 4 and query.shape[0] != 1:
+            raise ValueError("The batch size is expected to be 1 rather than %d when using "
+                             "`cu_seqlens`." % query.shape[0])
+        n = len(cu_seqlens) - 1
+        if initial_state is not None and initial_state.shape[0] != n:
+            raise ValueError("The number of initial states is expected to be equal to the "
+                             "number of input sequences, i.e., %d rather than %d."
+                             % (n, initial_state.shape[0]))
+    if softmax_scale is None:
+        softmax_scale = key.shape[-1] ** -0.5
+    return recurrent(query, key, value, g=g, g_gamma=g_gamma, softmax_scale=softmax_scale,
+                     initial_state=initial_state, reverse=reverse, cu_seqlens=cu_seqlens)
 
 
 def lightning_attn(query: Tensor, key: Tensor, value: Tensor, layer_idx: int, num_layers: int,

@@ -805,3 +805,205 @@ uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxe
 int32_t la_version(void) { return (0 << 16) | 3; }
 
 }  // extern "C"
+
+// ---- gated form (per-key gate, GLA) --------------------------------------------
+namespace {
+
+la_status gla_check(const Problem &P, const la_dims *d, const float *g, const int64_t *gs,
+                    const float *g_gamma)
+{
+    if (d->kv_heads && d->kv_heads != d->heads)
+        return fail(LA_ERR_UNSUPPORTED, "the gated form takes kv_heads = 0 (or = heads)");
+    if (!has_states(P))
+        return LA_OK;
+    la_status st;
+    if ((st = need(g_gamma, "g_gamma")))
+        return st;
+    if (has_tokens(P)) {
+        if ((st = need(g, "g")) || (st = need(gs, "g_strides")))
+            return st;
+        for (int i = 0; i < 3; ++i)
+            if (gs[i] < 0)
+                return fail(LA_ERR_INVALID_ARG, "negative gate stride");
+    }
+    return LA_OK;
+}
+
+la::Gate gate_of(const float *g, const int64_t *gs, bool cols)
+{
+    la::Gate G;
+    G.p = g;
+    if (gs) {
+        G.sb = gs[0];
+        G.st = gs[1];
+        G.sh = gs[2];
+    }
+    G.cols = cols ? 1 : 0;
+    return G;
+}
+
+la_status short_run(const la::SweepArgs &a, bool bwd, cudaStream_t s)
+{
+    cudaError_t e = bwd ? la::short_backward_sweep(a, s) : la::short_forward_sweep(a, s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "gated sweep launch");
+}
+
+int64_t gla_max_len(const Problem &P)
+{
+    int64_t m = P.packed ? 0 : P.T;
+    for (size_t n = 0; P.packed && n < (size_t)P.N; ++n)
+        m = std::max<int64_t>(m, P.cu_host[n + 1] - P.cu_host[n]);
+    return m;
+}
+
+// Workspace of la_gla_bwd: the final state transposed, then the block sums.
+size_t gla_bwd_bytes(const Problem &P)
+{
+    const int64_t nblk = (gla_max_len(P) + la::DG_TB - 1) / la::DG_TB;
+    return round256((size_t)P.N * P.H * P.D * P.E * 4) + round256((size_t)P.N * P.H * nblk * P.D * 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
+                     const void *v, const float *g, const int64_t *g_strides,
+                     const float *g_gamma, float scale, const float *initial_state,
+                     int32_t reverse, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
+                     void *o, float *final_state, void *stream)
+{
+    g_msg.clear();
+    cudaStream_t s = (cudaStream_t)stream;
+    Problem P;
+    la_status st = check_dims(dims, dtype, cu_seqlens, cu_seqlens_host, s, &P);
+    if (st != LA_OK)
+        return st;
+    if (has_tokens(P)) {
+        if ((st = need(q, "q")) || (st = need(k, "k")) || (st = need(v, "v")) ||
+            (st = need(o, "o")))
+            return st;
+    }
+    if ((st = gla_check(P, dims, g, g_strides, g_gamma)) || !has_states(P))
+        return st;
+    la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
+    a.D = P.D;
+    a.E = P.E;
+    a.q = tok(q, dims->qk_strides);
+    a.k = tok(k, dims->qk_strides);
+    a.v = tok(v, dims->v_strides);
+    a.out = tok_out(o, dims->v_strides);
+    a.s_in = la::StateIn{initial_state, P.E, 1};
+    a.s_out = la::StateOut{final_state, P.E, 1};
+    a.gate = gate_of(g, g_strides, false);   // state rows are key channels
+    return short_run(a, false, s);
+}
+
+size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *cu_seqlens_host)
+{
+    Problem P;
+    std::string keep = g_msg;
+    la_status st = check_dims(dims, dtype, cu_seqlens_host, cu_seqlens_host, nullptr, &P);
+    g_msg = keep;
+    return st == LA_OK ? gla_bwd_bytes(P) : 0;
+}
+
+la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
+                     const void *v, const void *d_o, const float *g, const int64_t *g_strides,
+                     const float *g_gamma, float scale, const float *initial_state,
+                     const float *d_final_state, int32_t reverse, const int32_t *cu_seqlens,
+                     const int32_t *cu_seqlens_host, void *dq, void *dk, void *dv, float *dg,
+                     float *d_initial_state, void *workspace, size_t workspace_bytes,
+                     void *stream)
+{
+    g_msg.clear();
+    cudaStream_t s = (cudaStream_t)stream;
+    Problem P;
+    la_status st = check_dims(dims, dtype, cu_seqlens, cu_seqlens_host, s, &P);
+    if (st != LA_OK)
+        return st;
+    if (has_tokens(P)) {
+        if ((st = need(q, "q")) || (st = need(k, "k")) || (st = need(v, "v")) ||
+            (st = need(d_o, "d_o")) || (st = need(dq, "dq")) || (st = need(dk, "dk")) ||
+            (st = need(dv, "dv")) || (st = need(dg, "dg")))
+            return st;
+    }
+    if ((st = gla_check(P, dims, g, g_strides, g_gamma)) || !has_states(P))
+        return st;
+    const size_t need_ws = gla_bwd_bytes(P);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
+        workspace_bytes < need_ws)
+        return fail(LA_ERR_INVALID_ARG,
+                    "la_gla_bwd needs a 256-byte aligned workspace of %zu bytes (got %zu)",
+                    need_ws, workspace ? workspace_bytes : (size_t)0);
+    float *Ft = static_cast<float *>(workspace);
+    float *bsum = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                            round256((size_t)P.N * P.H * P.D * P.E * 4));
+    la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
+    // dq: forward-type with (q, k, v) := (do, v, k), state S^T (E x D): the
+    // gated key channels are its columns; its final state F^T feeds dg
+    a.D = P.E;
+    a.E = P.D;
+    a.q = tok(d_o, dims->v_strides);
+    a.k = tok(v, dims->v_strides);
+    a.v = tok(k, dims->qk_strides);
+    a.out = tok_out(dq, dims->qk_strides);
+    a.s_in = la::StateIn{initial_state, 1, P.E};
+    a.s_out = la::StateOut{Ft, P.D, 1};
+    a.gate = gate_of(g, g_strides, true);
+    if ((st = short_run(a, false, s)))
+        return st;
+    // dv: backward-type (q, k, do), G = dL/dS (D x E): gated rows
+    a.D = P.D;
+    a.E = P.E;
+    a.q = tok(q, dims->qk_strides);
+    a.k = tok(k, dims->qk_strides);
+    a.v = tok(d_o, dims->v_strides);
+    a.out = tok_out(dv, dims->v_strides);
+    a.s_in = la::StateIn{d_final_state, P.E, 1};
+    a.s_out = la::StateOut{d_initial_state, P.E, 1};
+    a.gate = gate_of(g, g_strides, false);
+    if ((st = short_run(a, true, s)))
+        return st;
+    // dk: backward-type (do, v, q), G^T (E x D): gated columns
+    a.D = P.E;
+    a.E = P.D;
+    a.q = tok(d_o, dims->v_strides);
+    a.k = tok(v, dims->v_strides);
+    a.v = tok(q, dims->qk_strides);
+    a.out = tok_out(dk, dims->qk_strides);
+    a.s_in = la::StateIn{d_final_state, 1, P.E};
+    a.s_out = la::StateOut{nullptr, 0, 0};
+    a.gate = gate_of(g, g_strides, true);
+    if ((st = short_run(a, true, s)))
+        return st;
+    // dg from q dq - k dk and the final-state term
+    la::GateGradArgs gg{};
+    gg.N = P.N;
+    gg.H = P.H;
+    gg.D = P.D;
+    gg.E = P.E;
+    gg.T = P.T;
+    gg.nblk = (gla_max_len(P) + la::DG_TB - 1) / la::DG_TB;
+    gg.cu = cu_seqlens;
+    gg.reverse = reverse ? 1 : 0;
+    gg.bf16 = dtype == LA_DTYPE_BF16;
+    gg.q = q;
+    gg.k = k;
+    gg.dq = dq;
+    gg.dk = dk;
+    gg.sb = dims->qk_strides[0];
+    gg.st = dims->qk_strides[1];
+    gg.sh = dims->qk_strides[2];
+    gg.dg = dg;
+    gg.gsb = g_strides[0];
+    gg.gst = g_strides[1];
+    gg.gsh = g_strides[2];
+    gg.Ft = Ft;
+    gg.dF = d_final_state;
+    gg.bsum = bsum;
+    cudaError_t e = la::gate_grad(gg, s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "gate gradient");
+}
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+// la_gla.cu -- gradient of the per-key gate (the GLA form of the recurrence).
+//
+// With a gate g_t (a log-decay per key channel, ejkernel `recurrent`'s
+// GLA-style gate) the state is S_t = diag(exp(g_gamma + g_t)) S_{t-1} + k_t v_t^T.
+// Writing G_t for the cumulative log-decay up to token t (processing order),
+// the output depends on G through q_t exp(G_t) and k_u exp(-G_u) only, and
+// the final state through an extra factor exp(G_L).  Hence, per key channel,
+//     dL/dG_t = q_t dq_t - k_t dk_t   (+ sum_e F dF at the last token),
+// and since g_w enters every G_t with t >= w,
+//     dg_w = sum over t at or after w (processing order) of dL/dG_t.
+// dq and dk are the backward pass's gradients, F the final state and dF its
+// upstream gradient.  Two kernels: per block of DG_TB tokens the sum of
+// q dq - k dk per channel, then the reverse running sum inside each block
+// starting from the later blocks' sums and the final-state term.
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+template <typename T> __device__ __forceinline__ float ldt(const T *p);
+template <> __device__ __forceinline__ float ldt<float>(const float *p) { return *p; }
+template <> __device__ __forceinline__ float ldt<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    return __bfloat162float(*p);
+}
+
+struct Seq {
+    int64_t row, bos, len;
+};
+
+__device__ __forceinline__ Seq seq_of(const GateGradArgs &a, int n)
+{
+    Seq s;
+    if (a.cu) {
+        s.row = 0;
+        s.bos = a.cu[n];
+        s.len = (int64_t)a.cu[n + 1] - a.cu[n];
+    } else {
+        s.row = n;
+        s.bos = 0;
+        s.len = a.T;
+    }
+    return s;
+}
+
+// q dq - k dk at processing position p, channel c
+template <typename T>
+__device__ __forceinline__ float term(const GateGradArgs &a, const Seq &s, int h, int64_t p, int c)
+{
+    const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
+    const int64_t off = s.row * a.sb + t * a.st + (int64_t)h * a.sh + c;
+    const T *q = static_cast<const T *>(a.q), *dq = static_cast<const T *>(a.dq);
+    const T *k = static_cast<const T *>(a.k), *dk = static_cast<const T *>(a.dk);
+    return ldt(q + off) * ldt(dq + off) - ldt(k + off) * ldt(dk + off);
+}
+
+template <typename T> __global__ void __launch_bounds__(256) block_sums(GateGradArgs a)
+{
+    const int j = blockIdx.x, h = blockIdx.y, n = blockIdx.z, c = threadIdx.x;
+    const Seq s = seq_of(a, n);
+    const int64_t p0 = (int64_t)j * DG_TB;
+    if (c >= a.D || p0 >= s.len)
+        return;
+    const int64_t p1 = s.len - p0 < DG_TB ? s.len : p0 + DG_TB;
+    float acc = 0.f;
+    for (int64_t p = p0; p < p1; ++p)
+        acc += term<T>(a, s, h, p, c);
+    a.bsum[(((int64_t)n * a.H + h) * a.nblk + j) * a.D + c] = acc;
+}
+
+template <typename T> __global__ void __launch_bounds__(256) block_scan(GateGradArgs a)
+{
+    const int j = blockIdx.x, h = blockIdx.y, n = blockIdx.z, c = threadIdx.x;
+    const Seq s = seq_of(a, n);
+    const int64_t p0 = (int64_t)j * DG_TB;
+    if (c >= a.D || p0 >= s.len)
+        return;
+    const int64_t p1 = s.len - p0 < DG_TB ? s.len : p0 + DG_TB;
+    // the final-state term: sum_e F[c][e] dF[c][e]; F is stored transposed
+    const int64_t sidx = ((int64_t)n * a.H + h) * (int64_t)a.D * a.E;
+    float acc = 0.f;
+    if (a.dF && a.Ft)
+        for (int e = 0; e < a.E; ++e)
+            acc += a.Ft[sidx + (int64_t)e * a.D + c] * a.dF[sidx + (int64_t)c * a.E + e];
+    const int nb = (int)((s.len + DG_TB - 1) / DG_TB);
+    const float *bs = a.bsum + ((int64_t)n * a.H + h) * a.nblk * a.D + c;
+    for (int jj = j + 1; jj < nb; ++jj)
+        acc += bs[(int64_t)jj * a.D];
+    for (int64_t p = p1 - 1; p >= p0; --p) {
+        acc += term<T>(a, s, h, p, c);
+        const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
+        a.dg[s.row * a.gsb + t * a.gst + (int64_t)h * a.gsh + c] = acc;
+    }
+}
+
+}  // namespace
+
+cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s)
+{
+    if (a.N == 0 || a.H == 0 || a.nblk == 0)
+        return cudaSuccess;
+    if (a.D > 256 || a.N > 65535 || a.H > 65535 || a.nblk > 0x7fffffff)
+        return cudaErrorNotSupported;
+    dim3 grid((unsigned)a.nblk, (unsigned)a.H, (unsigned)a.N);
+    const int threads = (a.D + 31) / 32 * 32;
+    if (a.bf16) {
+        block_sums<__nv_bfloat16><<<grid, threads, 0, s>>>(a);
+        note_launch();
+        block_scan<__nv_bfloat16><<<grid, threads, 0, s>>>(a);
+    } else {
+        block_sums<float><<<grid, threads, 0, s>>>(a);
+        note_launch();
+        block_scan<float><<<grid, threads, 0, s>>>(a);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -48,6 +48,15 @@ struct StateOut {
     int64_t rs, cs;
 };
 
+// A per-key gate (fp32 log-decay added to g[h]): element (row, token, head,
+// channel) at p + row*sb + token*st + head*sh + channel.  The gated channel is
+// the state's row index (cols == 0) or its column index (cols == 1).
+struct Gate {
+    const float *p = nullptr;
+    int64_t sb = 0, st = 0, sh = 0;
+    int cols = 0;
+};
+
 struct SweepArgs {
     int B, T, H, D, E, N;     // D: width of q and k; E: width of v (w) and out
     const int32_t *cu;        // device [N+1] or nullptr (dense: N == B rows of T)
@@ -63,6 +72,7 @@ struct SweepArgs {
     StateOut s_out;           // forward-type: final state; backward-type: dL/dinitial
     int withhold_handoff;     // diagnostic: tensor-core kernels skip one hand-off
     int64_t max_len;          // longest sequence (T when dense)
+    Gate gate;                // per-key log-decay gate, or p == nullptr
 };
 
 // Calls whose longest sequence has at most this many tokens run the
@@ -79,8 +89,11 @@ void set_last_error(const char *msg);
 cudaError_t simt_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t simt_backward_sweep(const SweepArgs &a, cudaStream_t s);
 
-// Token-by-token kernels for short sequences: any D in 1..256, any E, bf16 or
-// fp32, every flag; cudaErrorNotSupported outside that range.
+// Token-by-token kernels: any length (tokens pass through shared memory 16 at
+// a time), any D in 1..256, any E, bf16 or fp32, every flag, and the only
+// kernels that take a gate; cudaErrorNotSupported outside that range.  Used
+// for every gated call and for ungated calls whose longest sequence has at
+// most SHORT_MAX_T tokens.
 cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s);
 
@@ -95,6 +108,26 @@ cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s);
 // [B, T, Hkv*G, X] of the token dtype, `out` strided like a TokOut.
 cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv, int G, int X,
                        int bf16, cudaStream_t s);
+
+// Gradient of the per-key gate (la_gla.cu).  q, k, dq, dk share one layout
+// (token dtype, strides sb, st, sh); dg is fp32 with the gate's strides.
+// Ft: the final state transposed [N][H][E][D] (fp32), dF: its upstream
+// gradient [N][H][D][E] (either may be null: no final-state term).  bsum:
+// scratch [N][H][nblk][D] fp32, nblk = ceil(longest sequence / DG_TB).
+constexpr int DG_TB = 256;
+struct GateGradArgs {
+    int N, H, D, E, T;
+    int64_t nblk;
+    const int32_t *cu;
+    int reverse, bf16;
+    const void *q, *k, *dq, *dk;
+    int64_t sb, st, sh;
+    float *dg;
+    int64_t gsb, gst, gsh;
+    const float *Ft, *dF;
+    float *bsum;
+};
+cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s);
 
 // State scan of the sequence split (la_split.cu).  W holds one D x E fp32
 // state per (segment, head), [NS][H][D][E]; on entry the segments' results

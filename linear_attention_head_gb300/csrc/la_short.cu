@@ -51,16 +51,20 @@ __host__ __device__ inline int short_groups(int D)
     return g;
 }
 
-// Dynamic shared memory (floats): q and k of every token [max_len][20 G]
-// (row group g at offset 20 g: the groups that a quarter warp reads at once
-// fall in different banks; rows past D zero), and the CTA's 32 value columns
-// of every token [max_len][32].
-__host__ __device__ inline size_t short_smem_bytes(int max_len, int D)
+constexpr int TB = 16;   // tokens per shared-memory block
+
+// Dynamic shared memory (floats) for one block of TB tokens: q, k and the
+// row-gate decays [TB][20 G] (row group g at offset 20 g, so that the groups
+// a quarter warp reads at once fall in different banks; rows past D zero),
+// the CTA's 32 value columns [TB][32] and column-gate decays [TB][32].
+__host__ __device__ inline size_t short_smem_bytes(int D)
 {
-    return ((size_t)2 * max_len * 20 * short_groups(D) + (size_t)max_len * KW) * sizeof(float);
+    return ((size_t)3 * TB * 20 * short_groups(D) + (size_t)2 * TB * KW) * sizeof(float);
 }
 
-template <typename T, bool BWD>
+// GATE: 0 the head's decay only, 1 per-row gate (state rows are key
+// channels), 2 per-column gate (state columns are key channels).
+template <typename T, bool BWD, int GATE>
 __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
 {
     const int etiles = (a.E + KW - 1) / KW;
@@ -85,105 +89,135 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
         bos = 0;
         len = a.T;
     }
-    const int L = (int)len;   // <= max_len <= SHORT_MAX_T
     float *qs = sh;
-    float *ks = qs + (size_t)a.max_len * DPP;
-    float *ws = ks + (size_t)a.max_len * DPP;
+    float *ks = qs + TB * DPP;
+    float *as = ks + TB * DPP;   // row-gate decays
+    float *ws = as + TB * DPP;
+    float *acs = ws + TB * KW;   // column-gate decays
     // forward-type visits tokens in processing order, backward-type against it
     const bool flip = (a.reverse != 0) != BWD;
-    auto token = [&](int u) { return bos + (flip ? len - 1 - u : u); };
+    auto token = [&](int64_t u) { return bos + (flip ? len - 1 - u : u); };
 
-    const float gam = expf(a.g[h]);
+    const float gh = a.g[h];
+    const float gam = expf(gh);
     const float scale = a.scale;
     const int64_t sbase = ((int64_t)n * a.H + h) * (int64_t)D * a.E;
+    const T *qb = reinterpret_cast<const T *>(a.q.p) + row * a.q.sb + (int64_t)(h / a.q.hdiv) * a.q.sh;
+    const T *kb = reinterpret_cast<const T *>(a.k.p) + row * a.k.sb + (int64_t)(h / a.k.hdiv) * a.k.sh;
+    const T *vb = reinterpret_cast<const T *>(a.v.p) + row * a.v.sb + (int64_t)(h / a.v.hdiv) * a.v.sh;
+    const float *gb = GATE ? a.gate.p + row * a.gate.sb + (int64_t)h * a.gate.sh : nullptr;
+    T *ob = reinterpret_cast<T *>(a.out.p) + row * a.out.sb + (int64_t)h * a.out.sh;
+
     // S[j] = state(r0 + j, e0 + c); these loads are in flight while the
-    // tokens are copied below
+    // first tokens are copied below
     float S[RP];
 #pragma unroll
     for (int j = 0; j < RP; ++j)
         S[j] = a.s_in.p && col_ok && r0 + j < D
                    ? a.s_in.p[sbase + (int64_t)(r0 + j) * a.s_in.rs + (int64_t)(e0 + c) * a.s_in.cs]
                    : 0.f;
-    // every token of the sequence into shared memory, in visiting order; the
-    // loads of a thread are issued PF at a time before any is used, so the
-    // copy pays a few memory latencies instead of one per element
-    constexpr int PF = 8;
-    const int nqk = L * DP, nthr = blockDim.x;
-    for (int base = threadIdx.x; base < nqk; base += PF * nthr) {
-        float xq[PF], xk[PF];
-#pragma unroll
-        for (int i = 0; i < PF; ++i) {
-            const int idx = base + i * nthr, u = idx / DP, k = idx % DP;
-            xq[i] = xk[i] = 0.f;
-            if (idx < nqk && k < D) {
-                const int64_t t = token(u);
-                xq[i] = ld_tok(reinterpret_cast<const T *>(a.q.p) + row * a.q.sb + t * a.q.st +
-                               (int64_t)(h / a.q.hdiv) * a.q.sh + k);
-                xk[i] = ld_tok(reinterpret_cast<const T *>(a.k.p) + row * a.k.sb + t * a.k.st +
-                               (int64_t)(h / a.k.hdiv) * a.k.sh + k);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < PF; ++i) {
-            const int idx = base + i * nthr, u = idx / DP, k = idx % DP;
-            if (idx < nqk) {
-                qs[u * DPP + k + 4 * (k / RP)] = xq[i];
-                ks[u * DPP + k + 4 * (k / RP)] = xk[i];
-            }
-        }
-    }
-    const int nw = L * KW;
-    for (int base = threadIdx.x; base < nw; base += PF * nthr) {
-        float xw[PF];
-#pragma unroll
-        for (int i = 0; i < PF; ++i) {
-            const int idx = base + i * nthr, u = idx / KW, k = idx % KW;
-            xw[i] = 0.f;
-            if (idx < nw && e0 + k < a.E)
-                xw[i] = ld_tok(reinterpret_cast<const T *>(a.v.p) + row * a.v.sb +
-                               token(u) * a.v.st + (int64_t)(h / a.v.hdiv) * a.v.sh + e0 + k);
-        }
-#pragma unroll
-        for (int i = 0; i < PF; ++i) {
-            const int idx = base + i * nthr;
-            if (idx < nw)
-                ws[idx] = xw[i];
-        }
-    }
 
-    __syncthreads();
-
-    for (int u = 0; u < L; ++u) {
-        const float4 *q4 = reinterpret_cast<const float4 *>(qs + u * DPP + 20 * g);
-        const float4 *k4 = reinterpret_cast<const float4 *>(ks + u * DPP + 20 * g);
-        const float w = ws[u * KW + c];
-        float dot[4] = {0.f, 0.f, 0.f, 0.f};   // four chains, summed at the end
+    constexpr int PF = 4;
+    const int nthr = blockDim.x;
+    for (int64_t b0 = 0; b0 < len; b0 += TB) {
+        const int Lb = (int)(len - b0 < TB ? len - b0 : TB);
+        // the block's tokens into shared memory, in visiting order; each
+        // thread issues PF loads before using any
+        const int nqk = Lb * DP;
+        for (int base = threadIdx.x; base < nqk; base += PF * nthr) {
+            float xq[PF], xk[PF], xa[PF];
 #pragma unroll
-        for (int j4 = 0; j4 < RP / 4; ++j4) {
-            const float4 xq = q4[j4], xk = k4[j4];
-            const float qv[4] = {xq.x, xq.y, xq.z, xq.w};
-            const float kv[4] = {xk.x, xk.y, xk.z, xk.w};
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr, u = idx / DP, k = idx % DP;
+                xq[i] = xk[i] = 0.f;
+                xa[i] = 1.f;
+                if (idx < nqk && k < D) {
+                    const int64_t t = token(b0 + u);
+                    xq[i] = ld_tok(qb + t * a.q.st + k);
+                    xk[i] = ld_tok(kb + t * a.k.st + k);
+                    if (GATE == 1)
+                        xa[i] = gb[t * a.gate.st + k];
+                }
+            }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float &x = S[4 * j4 + i];
-                if (!BWD) {
-                    x = fmaf(kv[i], w, gam * x);
-                    dot[i] = fmaf(qv[i], x, dot[i]);
-                } else {
-                    x = fmaf(scale * qv[i], w, x);
-                    dot[i] = fmaf(kv[i], x, dot[i]);
-                    x *= gam;
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr, u = idx / DP, k = idx % DP;
+                if (idx < nqk) {
+                    const int at = u * DPP + k + 4 * (k / RP);
+                    qs[at] = xq[i];
+                    ks[at] = xk[i];
+                    if (GATE == 1)
+                        as[at] = k < D ? expf(gh + xa[i]) : 1.f;
                 }
             }
         }
-        float dsum = (dot[0] + dot[1]) + (dot[2] + dot[3]);
-        for (int off = 1; off < G; off <<= 1)
-            dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-        if (g == 0 && col_ok) {
-            T *op = reinterpret_cast<T *>(a.out.p) + row * a.out.sb + token(u) * a.out.st +
-                    (int64_t)h * a.out.sh;
-            st_tok(op + e0 + c, BWD ? dsum : scale * dsum);
+        const int nw = Lb * KW;
+        for (int base = threadIdx.x; base < nw; base += PF * nthr) {
+            float xw[PF], xg[PF];
+#pragma unroll
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr, u = idx / KW, k = idx % KW;
+                xw[i] = 0.f;
+                xg[i] = 0.f;
+                if (idx < nw && e0 + k < a.E) {
+                    const int64_t t = token(b0 + u);
+                    xw[i] = ld_tok(vb + t * a.v.st + e0 + k);
+                    if (GATE == 2)
+                        xg[i] = gb[t * a.gate.st + e0 + k];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr;
+                if (idx < nw) {
+                    ws[idx] = xw[i];
+                    if (GATE == 2)
+                        acs[idx] = expf(gh + xg[i]);
+                }
+            }
         }
+        __syncthreads();
+
+        for (int u = 0; u < Lb; ++u) {
+            const float4 *q4 = reinterpret_cast<const float4 *>(qs + u * DPP + 20 * g);
+            const float4 *k4 = reinterpret_cast<const float4 *>(ks + u * DPP + 20 * g);
+            const float4 *a4 = reinterpret_cast<const float4 *>(as + u * DPP + 20 * g);
+            const float w = ws[u * KW + c];
+            const float ac = GATE == 2 ? acs[u * KW + c] : gam;
+            float dot[4] = {0.f, 0.f, 0.f, 0.f};   // four chains, summed at the end
+#pragma unroll
+            for (int j4 = 0; j4 < RP / 4; ++j4) {
+                const float4 xq = q4[j4], xk = k4[j4];
+                const float qv[4] = {xq.x, xq.y, xq.z, xq.w};
+                const float kv[4] = {xk.x, xk.y, xk.z, xk.w};
+                float dv[4] = {ac, ac, ac, ac};
+                if (GATE == 1) {
+                    const float4 xa = a4[j4];
+                    dv[0] = xa.x;
+                    dv[1] = xa.y;
+                    dv[2] = xa.z;
+                    dv[3] = xa.w;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float &x = S[4 * j4 + i];
+                    if (!BWD) {
+                        x = fmaf(kv[i], w, dv[i] * x);
+                        dot[i] = fmaf(qv[i], x, dot[i]);
+                    } else {
+                        x = fmaf(scale * qv[i], w, x);
+                        dot[i] = fmaf(kv[i], x, dot[i]);
+                        x *= dv[i];
+                    }
+                }
+            }
+            float dsum = (dot[0] + dot[1]) + (dot[2] + dot[3]);
+            for (int off = 1; off < G; off <<= 1)
+                dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+            if (g == 0 && col_ok)
+                st_tok(ob + token(b0 + u) * a.out.st + e0 + c, BWD ? dsum : scale * dsum);
+        }
+        __syncthreads();   // the next block overwrites the buffers
     }
 
     if (a.s_out.p && col_ok) {
@@ -197,7 +231,7 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
 
 template <typename K> cudaError_t launch_one(K kernel, const SweepArgs &a, cudaStream_t s)
 {
-    const size_t smem = short_smem_bytes((int)a.max_len, a.D);
+    const size_t smem = short_smem_bytes(a.D);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -211,16 +245,23 @@ template <typename K> cudaError_t launch_one(K kernel, const SweepArgs &a, cudaS
     return cudaGetLastError();
 }
 
+template <typename T, bool BWD> cudaError_t launch_gate(const SweepArgs &a, cudaStream_t s)
+{
+    if (!a.gate.p)
+        return launch_one(short_kernel<T, BWD, 0>, a, s);
+    return a.gate.cols ? launch_one(short_kernel<T, BWD, 2>, a, s)
+                       : launch_one(short_kernel<T, BWD, 1>, a, s);
+}
+
 template <bool BWD> cudaError_t launch_short(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0 || a.H == 0)
         return cudaSuccess;
-    if (a.D < 1 || a.D > RP * MAXG || a.max_len < 0 || a.max_len > SHORT_MAX_T)
+    if (a.D < 1 || a.D > RP * MAXG)
         return cudaErrorNotSupported;
     if ((int64_t)a.N * a.H * ((a.E + KW - 1) / KW) > 0x7fffffff)
         return cudaErrorNotSupported;
-    return a.bf16 ? launch_one(short_kernel<__nv_bfloat16, BWD>, a, s)
-                  : launch_one(short_kernel<float, BWD>, a, s);
+    return a.bf16 ? launch_gate<__nv_bfloat16, BWD>(a, s) : launch_gate<float, BWD>(a, s);
 }
 
 }  // namespace

@@ -1,0 +1,94 @@
+"""Gated form (GLA): a per-key log-decay gate g [B,T,H,D] on top of g_gamma.
+
+Checked against the fp64 oracle's gated recurrence (tests/test_oracle_gla.py
+pins it) for the forward (o, final state) and the backward (dq, dk, dv, dg,
+d_initial_state), bf16 and fp32, both directions, packed sequences with an
+empty one, and through autograd (`recurrent(g=...)`, `recurrent_gla`).
+"""
+import math
+
+import pytest
+import torch
+
+import linear_attention_head_gb300 as la
+import oracle
+import workloads as W
+from parity import TOL, compare
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(B, T, H, D, E, dtype, seqlens=None, seed=0, gate_scale=0.3):
+    w = W.Workload("gla", B, T if seqlens is None else sum(seqlens), H, D, E, dtype,
+                   W.alibi_g_gamma(H), 1.0 / math.sqrt(D), seqlens=seqlens, init_std=0.2,
+                   dfinal_std=0.2)
+    x = W.make_inputs(w, seed=seed)
+    gen = torch.Generator().manual_seed(seed + 1000)
+    x["g"] = -gate_scale * torch.rand(x["q"].shape, generator=gen)
+    return x
+
+
+def _gpu(x, reverse):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o, fin = la.gla_fwd(d["q"], d["k"], d["v"], d["g"], d["g_gamma"], d["scale"],
+                        d["initial_state"], reverse, x["cu_seqlens"])
+    dq, dk, dv, dg, dinit = la.gla_bwd(d["q"], d["k"], d["v"], d["do"], d["g"], d["g_gamma"],
+                                       d["scale"], d["initial_state"], d["d_final_state"],
+                                       reverse, x["cu_seqlens"])
+    torch.cuda.synchronize()
+    la.get_device_error()
+    out = dict(o=o, final_state=fin, dq=dq, dk=dk, dv=dv, dg=dg, d_initial_state=dinit)
+    return {k: v.cpu() for k, v in out.items()}
+
+
+def _oracle(x, reverse):
+    o, fin = oracle.gla_forward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"], x["scale"],
+                                x["initial_state"], reverse, x["cu_seqlens"])
+    dq, dk, dv, dg, dinit = oracle.gla_backward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"],
+                                                x["scale"], x["do"], x["initial_state"],
+                                                x["d_final_state"], reverse, x["cu_seqlens"])
+    return dict(o=o, final_state=fin, dq=dq, dk=dk, dv=dv, dg=dg, d_initial_state=dinit)
+
+
+@pytest.mark.parametrize("T,D,E,dtype", [(300, 128, 128, torch.bfloat16),
+                                         (200, 64, 64, torch.float32),
+                                         (37, 48, 80, torch.bfloat16)])
+def test_gated_matches_oracle(T, D, E, dtype):
+    x = _inputs(2, T, 3, D, E, dtype, seed=T)
+    for reverse in (False, True):
+        compare(_gpu(x, reverse), _oracle(x, reverse), TOL[dtype],
+                label="gla T=%d rev=%d" % (T, reverse))
+
+
+def test_gated_packed_sequences():
+    lens = [70, 0, 133, 5]
+    x = _inputs(1, 0, 2, 64, 64, torch.float32, seqlens=lens, seed=3)
+    for reverse in (False, True):
+        compare(_gpu(x, reverse), _oracle(x, reverse), TOL[torch.float32],
+                cu=x["cu_seqlens"], label="gla packed rev=%d" % reverse)
+
+
+def test_gated_autograd_and_recurrent_gla():
+    x = _inputs(1, 120, 2, 64, 64, torch.float32, seed=5)
+    q, k, v, g = (x[n].cuda().requires_grad_() for n in ("q", "k", "v", "g"))
+    o, fin = la.recurrent_gla(q, k, v, g=g, g_gamma=x["g_gamma"], softmax_scale=x["scale"])
+    (o * x["do"].cuda()).sum().backward()
+    ref_o, _ = oracle.gla_forward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"], x["scale"])
+    rq, rk, rv, rg, _ = oracle.gla_backward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"],
+                                            x["scale"], x["do"])
+    compare(dict(o=o.detach().cpu(), dq=q.grad.cpu(), dk=k.grad.cpu(), dv=v.grad.cpu(),
+                 dg=g.grad.cpu()),
+            dict(o=ref_o, dq=rq, dk=rk, dv=rv, dg=rg), TOL[torch.float32], label="autograd")
+
+
+def test_gate_of_zero_equals_the_ungated_path():
+    x = _inputs(2, 260, 2, 128, 128, torch.bfloat16, seed=7)
+    x["g"] = torch.zeros_like(x["g"])
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o1, f1 = la.gla_fwd(d["q"], d["k"], d["v"], d["g"], d["g_gamma"], d["scale"],
+                        d["initial_state"])
+    o2, f2 = la.la_fwd(d["q"], d["k"], d["v"], d["g_gamma"], d["scale"], d["initial_state"])
+    # the chunked tensor-core path rounds its MMA operands to bf16, the gated
+    # path runs in fp32: both meet the bf16 parity bound against the oracle
+    assert (o1.float() - o2.float()).abs().max() <= 2e-2 * o2.float().abs().max()
+    assert (f1 - f2).abs().max() <= 2e-2 * f2.abs().max()
