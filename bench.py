@@ -317,6 +317,7 @@ def gpu_bench(args):
         line["decode"] = decode_bench(la, torch, dev, stream, peak)
         line["long_sequence"] = split_bench(la, torch, dev, stream, peak)
         line["grouped_kv"] = gqa_bench(la, torch, dev, stream, peak)
+        line["gated"] = gla_bench(la, torch, dev, stream, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.n, args.cpu_pairs)
     if rank == 0:
@@ -493,6 +494,43 @@ def gqa_bench(la, torch, dev, stream, peak):
             "fwd_ms": f_ms, "bwd_ms": b_ms, "tokens_per_s": B * T / ((f_ms + b_ms) * 1e-3),
             "fwd_frac_of_peak": fb / (f_ms * 1e-3) / 1e9 / peak,
             "bwd_compulsory_frac_of_peak": bb / (b_ms * 1e-3) / 1e9 / peak}
+
+
+def gla_bench(la, torch, dev, stream, peak):
+    """Gated form (GLA, per-key gate): b4 h32 n8192 d=e=128 bf16, gate fp32.
+    gla_fwd and gla_bwd timed separately (mean of 3 queued calls after 1 warm-up
+    call).  Algorithmic bytes: forward reads q, k, v, g and writes o; backward
+    reads q, k, v, do, g and writes dq, dk, dv, dg."""
+    import workloads as W
+    B, T, H, D = 4, 8192, 32, 128
+    gg = W.alibi_g_gamma(H).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(19)
+    q, k, v, do = (torch.randn((B, T, H, D), generator=gen, device=dev).bfloat16()
+                   for _ in range(4))
+    g = -0.3 * torch.rand((B, T, H, D), generator=gen, device=dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 3
+
+    f_ms = timed(lambda: la.gla_fwd(q, k, v, g, gg, 1.0))
+    b_ms = timed(lambda: la.gla_bwd(q, k, v, do, g, gg, 1.0, want_d_initial_state=False))
+    unit = B * T * H * D * 2
+    la.get_device_error(dev)
+    del q, k, v, do, g
+    return {"workload": "fwd+bwd b4 h32 n8192 d=e=128 bf16 tokens, fp32 per-key gate",
+            "kernels": "token-by-token (CUDA cores)", "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "tokens_per_s": B * T / ((f_ms + b_ms) * 1e-3),
+            "fwd_frac_of_peak": (4 * unit + 2 * unit) / (f_ms * 1e-3) / 1e9 / peak,
+            "bwd_frac_of_peak": (7 * unit + 4 * unit) / (b_ms * 1e-3) / 1e9 / peak}
 
 
 def source_sha():
