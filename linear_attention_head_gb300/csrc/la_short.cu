@@ -57,14 +57,22 @@ constexpr int TB = 16;   // tokens per shared-memory block
 // row-gate decays [TB][20 G] (row group g at offset 20 g, so that the groups
 // a quarter warp reads at once fall in different banks; rows past D zero),
 // the CTA's 32 value columns [TB][32] and column-gate decays [TB][32].
-__host__ __device__ inline size_t short_smem_bytes(int D)
+// gate < 0: the synchronous path (no raw buffers).
+__host__ __device__ inline size_t short_smem_bytes(int D, int esz, int gate)
 {
-    return ((size_t)3 * TB * 20 * short_groups(D) + (size_t)2 * TB * KW) * sizeof(float);
+    const size_t layout = ((size_t)3 * TB * 20 * short_groups(D) + (size_t)2 * TB * KW) * 4;
+    if (gate < 0)
+        return layout;
+    // double-buffered raw rows of the asynchronous path: q, k, v tile, gate
+    const size_t raw = (size_t)2 * TB * ((size_t)2 * D * esz + (size_t)KW * esz +
+                                         (gate == 1 ? (size_t)D * 4 : 0) +
+                                         (gate == 2 ? (size_t)KW * 4 : 0));
+    return layout + raw;
 }
 
 // GATE: 0 the head's decay only, 1 per-row gate (state rows are key
 // channels), 2 per-column gate (state columns are key channels).
-template <typename T, bool BWD, int GATE>
+template <typename T, bool BWD, int GATE, bool ASYNC>
 __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
 {
     const int etiles = (a.E + KW - 1) / KW;
@@ -102,9 +110,13 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
     const float gam = expf(gh);
     const float scale = a.scale;
     const int64_t sbase = ((int64_t)n * a.H + h) * (int64_t)D * a.E;
-    const T *qb = reinterpret_cast<const T *>(a.q.p) + row * a.q.sb + (int64_t)(h / a.q.hdiv) * a.q.sh;
-    const T *kb = reinterpret_cast<const T *>(a.k.p) + row * a.k.sb + (int64_t)(h / a.k.hdiv) * a.k.sh;
-    const T *vb = reinterpret_cast<const T *>(a.v.p) + row * a.v.sb + (int64_t)(h / a.v.hdiv) * a.v.sh;
+    // token rows of this (sequence, head): key/value heads may be shared
+    const T *qb = reinterpret_cast<const T *>(a.q.p) + row * a.q.sb +
+                  (int64_t)(h / a.q.hdiv) * a.q.sh;
+    const T *kb = reinterpret_cast<const T *>(a.k.p) + row * a.k.sb +
+                  (int64_t)(h / a.k.hdiv) * a.k.sh;
+    const T *vb = reinterpret_cast<const T *>(a.v.p) + row * a.v.sb +
+                  (int64_t)(h / a.v.hdiv) * a.v.sh;
     const float *gb = GATE ? a.gate.p + row * a.gate.sb + (int64_t)h * a.gate.sh : nullptr;
     T *ob = reinterpret_cast<T *>(a.out.p) + row * a.out.sb + (int64_t)h * a.out.sh;
 
@@ -119,10 +131,10 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
 
     constexpr int PF = 4;
     const int nthr = blockDim.x;
-    for (int64_t b0 = 0; b0 < len; b0 += TB) {
-        const int Lb = (int)(len - b0 < TB ? len - b0 : TB);
-        // the block's tokens into shared memory, in visiting order; each
-        // thread issues PF loads before using any
+
+    // one block of Lb tokens from b0 on, copied synchronously into the
+    // compute layout; each thread issues PF loads before using any
+    auto load_sync = [&](int64_t b0, int Lb) {
         const int nqk = Lb * DP;
         for (int base = threadIdx.x; base < nqk; base += PF * nthr) {
             float xq[PF], xk[PF], xa[PF];
@@ -176,48 +188,155 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
                 }
             }
         }
-        __syncthreads();
-
-        for (int u = 0; u < Lb; ++u) {
-            const float4 *q4 = reinterpret_cast<const float4 *>(qs + u * DPP + 20 * g);
-            const float4 *k4 = reinterpret_cast<const float4 *>(ks + u * DPP + 20 * g);
-            const float4 *a4 = reinterpret_cast<const float4 *>(as + u * DPP + 20 * g);
-            const float w = ws[u * KW + c];
-            const float ac = GATE == 2 ? acs[u * KW + c] : gam;
-            float dot[4] = {0.f, 0.f, 0.f, 0.f};   // four chains, summed at the end
+    };
+    // the per-token recurrence over one block in the compute layout; the
+    // partial dot products of four tokens are summed over the row groups
+    // together, so that their shuffles overlap
+    auto compute = [&](int64_t b0, int Lb) {
+        for (int u0 = 0; u0 < Lb; u0 += 4) {
+            float pend[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j4 = 0; j4 < RP / 4; ++j4) {
-                const float4 xq = q4[j4], xk = k4[j4];
-                const float qv[4] = {xq.x, xq.y, xq.z, xq.w};
-                const float kv[4] = {xk.x, xk.y, xk.z, xk.w};
-                float dv[4] = {ac, ac, ac, ac};
-                if (GATE == 1) {
-                    const float4 xa = a4[j4];
-                    dv[0] = xa.x;
-                    dv[1] = xa.y;
-                    dv[2] = xa.z;
-                    dv[3] = xa.w;
-                }
+            for (int i = 0; i < 4; ++i) {
+                const int u = u0 + i;
+                if (u >= Lb)
+                    break;
+                const float4 *q4 = reinterpret_cast<const float4 *>(qs + u * DPP + 20 * g);
+                const float4 *k4 = reinterpret_cast<const float4 *>(ks + u * DPP + 20 * g);
+                const float4 *a4 = reinterpret_cast<const float4 *>(as + u * DPP + 20 * g);
+                const float w = ws[u * KW + c];
+                const float ac = GATE == 2 ? acs[u * KW + c] : gam;
+                float dot[4] = {0.f, 0.f, 0.f, 0.f};   // four chains, summed at the end
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float &x = S[4 * j4 + i];
-                    if (!BWD) {
-                        x = fmaf(kv[i], w, dv[i] * x);
-                        dot[i] = fmaf(qv[i], x, dot[i]);
-                    } else {
-                        x = fmaf(scale * qv[i], w, x);
-                        dot[i] = fmaf(kv[i], x, dot[i]);
-                        x *= dv[i];
+                for (int j4 = 0; j4 < RP / 4; ++j4) {
+                    const float4 xq = q4[j4], xk = k4[j4];
+                    const float qv[4] = {xq.x, xq.y, xq.z, xq.w};
+                    const float kv[4] = {xk.x, xk.y, xk.z, xk.w};
+                    float dv[4] = {ac, ac, ac, ac};
+                    if (GATE == 1) {
+                        const float4 xa = a4[j4];
+                        dv[0] = xa.x;
+                        dv[1] = xa.y;
+                        dv[2] = xa.z;
+                        dv[3] = xa.w;
+                    }
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        float &x = S[4 * j4 + m];
+                        if (!BWD) {
+                            x = fmaf(kv[m], w, dv[m] * x);
+                            dot[m] = fmaf(qv[m], x, dot[m]);
+                        } else {
+                            x = fmaf(scale * qv[m], w, x);
+                            dot[m] = fmaf(kv[m], x, dot[m]);
+                            x *= dv[m];
+                        }
                     }
                 }
+                pend[i] = (dot[0] + dot[1]) + (dot[2] + dot[3]);
             }
-            float dsum = (dot[0] + dot[1]) + (dot[2] + dot[3]);
-            for (int off = 1; off < G; off <<= 1)
-                dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-            if (g == 0 && col_ok)
-                st_tok(ob + token(b0 + u) * a.out.st + e0 + c, BWD ? dsum : scale * dsum);
+            for (int off = 1; off < G; off <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    pend[i] += __shfl_xor_sync(0xffffffffu, pend[i], off);
+            }
+            if (g == 0 && col_ok) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (u0 + i < Lb)
+                        st_tok(ob + token(b0 + u0 + i) * a.out.st + e0 + c,
+                               BWD ? pend[i] : scale * pend[i]);
+            }
         }
-        __syncthreads();   // the next block overwrites the buffers
+    };
+
+    // ASYNC (chosen on the host when every row is 16-byte aligned and the
+    // sequences span more than one block): double-buffered asynchronous
+    // copies (16-byte cp.async) of the raw rows, the next block's loads in
+    // flight while this block is converted and computed.
+    const int esz = (int)sizeof(T);
+    if (!ASYNC) {
+        for (int64_t b0 = 0; b0 < len; b0 += TB) {
+            const int Lb = (int)(len - b0 < TB ? len - b0 : TB);
+            load_sync(b0, Lb);
+            __syncthreads();
+            compute(b0, Lb);
+            __syncthreads();   // the next block overwrites the buffers
+        }
+    } else {
+        // raw double buffers after the compute layout
+        T *rq = reinterpret_cast<T *>(acs + TB * KW);
+        T *rk = rq + 2 * TB * D;
+        T *rv = rk + 2 * TB * D;
+        float *rg = reinterpret_cast<float *>(rv + 2 * TB * KW);   // row gate [2][TB][D]
+        float *rgc = rg + (GATE == 1 ? 2 * TB * D : 0);            // column gate [2][TB][KW]
+        const int cq = D * esz / 16, cv = KW * esz / 16, cgr = D / 4, cgc = KW / 4;
+        auto issue = [&](int64_t b0, int Lb, int buf) {
+            const int per = cq * 2 + cv + (GATE == 1 ? cgr : 0) + (GATE == 2 ? cgc : 0);
+            for (int idx = threadIdx.x; idx < Lb * per; idx += nthr) {
+                const int u = idx / per;
+                int r = idx % per;
+                const int64_t t = token(b0 + u);
+                const void *src;
+                void *dst;
+                if (r < cq) {
+                    src = qb + t * a.q.st + r * (16 / esz);
+                    dst = rq + ((size_t)buf * TB + u) * D + r * (16 / esz);
+                } else if ((r -= cq) < cq) {
+                    src = kb + t * a.k.st + r * (16 / esz);
+                    dst = rk + ((size_t)buf * TB + u) * D + r * (16 / esz);
+                } else if ((r -= cq) < cv) {
+                    src = vb + t * a.v.st + e0 + r * (16 / esz);
+                    dst = rv + ((size_t)buf * TB + u) * KW + r * (16 / esz);
+                } else if (GATE == 1) {
+                    r -= cv;
+                    src = gb + t * a.gate.st + 4 * r;
+                    dst = rg + ((size_t)buf * TB + u) * D + 4 * r;
+                } else {
+                    r -= cv;
+                    src = gb + t * a.gate.st + e0 + 4 * r;
+                    dst = rgc + ((size_t)buf * TB + u) * KW + 4 * r;
+                }
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                 static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                             "l"(src)
+                             : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        auto convert = [&](int Lb, int buf) {
+            for (int idx = threadIdx.x; idx < Lb * DP; idx += nthr) {
+                const int u = idx / DP, k = idx % DP;
+                const int at = u * DPP + k + 4 * (k / RP);
+                const size_t rr = ((size_t)buf * TB + u) * D + k;
+                qs[at] = k < D ? ld_tok(rq + rr) : 0.f;
+                ks[at] = k < D ? ld_tok(rk + rr) : 0.f;
+                if (GATE == 1)
+                    as[at] = k < D ? expf(gh + rg[rr]) : 1.f;
+            }
+            for (int idx = threadIdx.x; idx < Lb * KW; idx += nthr) {
+                const size_t rr = (size_t)buf * TB * KW + idx;
+                ws[idx] = ld_tok(rv + rr);
+                if (GATE == 2)
+                    acs[idx] = expf(gh + rgc[rr]);
+            }
+        };
+        int it = 0;
+        if (len > 0)
+            issue(0, (int)(len < TB ? len : TB), 0);
+        for (int64_t b0 = 0; b0 < len; b0 += TB, ++it) {
+            const int Lb = (int)(len - b0 < TB ? len - b0 : TB);
+            if (b0 + TB < len) {
+                issue(b0 + TB, (int)(len - b0 - TB < TB ? len - b0 - TB : TB), (it + 1) & 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+            __syncthreads();   // every thread's copies of this block landed
+            convert(Lb, it & 1);
+            __syncthreads();
+            compute(b0, Lb);
+        }
+        __syncthreads();
     }
 
     if (a.s_out.p && col_ok) {
@@ -229,9 +348,10 @@ __global__ void __launch_bounds__(KW * MAXG) short_kernel(SweepArgs a)
     }
 }
 
-template <typename K> cudaError_t launch_one(K kernel, const SweepArgs &a, cudaStream_t s)
+template <typename K>
+cudaError_t launch_one(K kernel, const SweepArgs &a, cudaStream_t s, int gate, bool async)
 {
-    const size_t smem = short_smem_bytes(a.D);
+    const size_t smem = short_smem_bytes(a.D, a.bf16 ? 2 : 4, async ? gate : -1);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -245,12 +365,35 @@ template <typename K> cudaError_t launch_one(K kernel, const SweepArgs &a, cudaS
     return cudaGetLastError();
 }
 
-template <typename T, bool BWD> cudaError_t launch_gate(const SweepArgs &a, cudaStream_t s)
+// Rows of every tensor 16-byte aligned (base, strides, widths) and value tiles
+// full: the copies can be 16-byte cp.async.
+bool rows_aligned(const SweepArgs &a, int esz)
+{
+    auto ok = [&](const void *p, int64_t sb, int64_t st, int64_t sh, int64_t es) {
+        return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && (sb * es) % 16 == 0 &&
+               (st * es) % 16 == 0 && (sh * es) % 16 == 0;
+    };
+    bool r = ok(a.q.p, a.q.sb, a.q.st, a.q.sh, esz) && ok(a.k.p, a.k.sb, a.k.st, a.k.sh, esz) &&
+             ok(a.v.p, a.v.sb, a.v.st, a.v.sh, esz) && (a.D * esz) % 16 == 0 && a.E % KW == 0;
+    if (a.gate.p)
+        r = r && ok(a.gate.p, a.gate.sb, a.gate.st, a.gate.sh, 4) && a.D % 4 == 0;
+    return r;
+}
+
+template <typename T, bool BWD, bool ASYNC>
+cudaError_t launch_async(const SweepArgs &a, cudaStream_t s)
 {
     if (!a.gate.p)
-        return launch_one(short_kernel<T, BWD, 0>, a, s);
-    return a.gate.cols ? launch_one(short_kernel<T, BWD, 2>, a, s)
-                       : launch_one(short_kernel<T, BWD, 1>, a, s);
+        return launch_one(short_kernel<T, BWD, 0, ASYNC>, a, s, 0, ASYNC);
+    return a.gate.cols ? launch_one(short_kernel<T, BWD, 2, ASYNC>, a, s, 2, ASYNC)
+                       : launch_one(short_kernel<T, BWD, 1, ASYNC>, a, s, 1, ASYNC);
+}
+
+template <typename T, bool BWD> cudaError_t launch_gate(const SweepArgs &a, cudaStream_t s)
+{
+    if (a.max_len > TB && rows_aligned(a, (int)sizeof(T)))
+        return launch_async<T, BWD, true>(a, s);
+    return launch_async<T, BWD, false>(a, s);
 }
 
 template <bool BWD> cudaError_t launch_short(const SweepArgs &a, cudaStream_t s)
