@@ -28,16 +28,18 @@
 //                 S * gamma^Lc(next) back into TMEM, where the next update
 //                 accumulates
 //   warps 14..17  O group: one thread per token row; o = P Z + lrow * X S,
-//                 written as bf16 into the X tile of the finished stage and
-//                 sent out with one TMA store (the last chunk of a packed
-//                 sequence, whose tile would overrun into the next sequence,
-//                 is stored row by row instead)
+//                 written as bf16 into the Z tile of the finished stage and
+//                 sent out with TMA stores, one per warp and 64-column block
+//                 (the last chunk of a packed sequence, whose tile would
+//                 overrun into the next sequence, is stored row by row)
 // TMEM (512 columns): scores/P [0,128), X S [128,256), P Z [256,384),
 // S [384,512) (value columns: E of them).  MMA order per chunk: scores and
 // X S as soon as the tiles land; then, once P is written, the state update
 // and P Z.  A ring stage is held only from landing to that last MMA, which is
-// what bounds the memory pipeline with two 96 KB stages; it is released when
-// that MMA and the store of the output tile out of its X slot have finished.
+// what bounds the memory pipeline with two 96 KB stages.  The X and Y slots of
+// a stage are released by the state update (the last MMA reading them), the
+// Z slot once the output tile staged in it has been stored; the next chunk's
+// scores need only X and Y.
 //
 // Every mbarrier wait is bounded (2 s); on expiry the CTA raises a shared
 // abort flag and records LA_ERR_TIMEOUT in a device word, drains its own
@@ -80,7 +82,7 @@ template <int E> struct TcLayout {
     static constexpr int SOFF = TC_NST * STAGE;       // bf16 copy of S, [E/64][D][64]
     static constexpr int SB = TC_D * E * 2;
     static constexpr int MOFF = SOFF + SB;
-    static constexpr int NBAR = 3 * TC_NST + 12;
+    static constexpr int NBAR = 4 * TC_NST + 12;
     static constexpr int PWOFF = MOFF + NBAR * 8;
     static constexpr int CFOFF = (PWOFF + (TC_C + 1) * 4 + 15) / 16 * 16;   // 32 column factors
     static constexpr int DTOFF = CFOFF + 32 * 4;                            // 64 diagonal factors
@@ -282,11 +284,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                                               ~static_cast<uintptr_t>(1023));
     const SweepArgs &a = P.a;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::MOFF);
-    // full: the stage's three tiles landed; empty: its Y and Z slots are free
-    // (last MMA of the chunk done); xfree: its X slot is free (every O warp
-    // has stored its rows of the output tile out of it)
-    uint64_t *full = bars, *empty = bars + TC_NST, *xfree = bars + 2 * TC_NST;
-    uint64_t *sc_full = bars + 3 * TC_NST;   // scores of the chunk are in TMEM
+    // full: the stage's X and Y tiles landed; zfull: its Z tile landed;
+    // empty: its X and Y slots are free (the state update, the chunk's last
+    // MMA reading them, is done); zfree: its Z slot is free (every O warp has
+    // stored its rows of the output tile, staged there, out of it)
+    uint64_t *full = bars, *empty = bars + TC_NST, *zfull = bars + 2 * TC_NST,
+             *zfree = bars + 3 * TC_NST;
+    uint64_t *sc_full = bars + 4 * TC_NST;   // scores of the chunk are in TMEM
     uint64_t *pv_done = sc_full + 1;         // P consumed (scores columns free)
     uint64_t *p_ready = sc_full + 2;         // P written, Y scaled
     uint64_t *s_ready = sc_full + 3;         // bf16 S written, TMEM S pre-scaled
@@ -329,7 +333,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         for (int i = 0; i < TC_NST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
-            mbar_init(&xfree[i], TC_OG / 32);
+            mbar_init(&zfull[i], 1);
+            mbar_init(&zfree[i], TC_OG / 32);
         }
         mbar_init(sc_full, 1);
         mbar_init(pv_done, 1);
@@ -370,30 +375,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     break;
                 const int t0 = (int)(bos + chunk_t0(c));
                 uint8_t *st = sm + s * L::STAGE;
-                mbar_arrive_expect_tx(&full[s], L::STAGE);
-                // Y and Z first: their slots are free once the chunk's MMAs are
-                // done, the X slot only once the output tile has left it
+                // X and Y first: their slots are free once the chunk's state
+                // update is done and the next scores need them; the Z slot
+                // only once the output tile staged in it has left
+                mbar_arrive_expect_tx(&full[s], L::XB + L::YB);
+#pragma unroll
+                for (int b = 0; b < TC_D / 64; ++b)
+                    tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, hx, t0, (int)row);
 #pragma unroll
                 for (int b = 0; b < TC_D / 64; ++b)
                     tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, hy, t0,
                                 (int)row);
+                // Z is copied even when this wait gives up, so that the drain
+                // below sees the stage complete
+                const bool zok = c < TC_NST || bwait(&zfree[s], ph, abort_flag);
+                mbar_arrive_expect_tx(&zfull[s], L::ZB);
 #pragma unroll
                 for (int b = 0; b < E / 64; ++b)
-                    tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s], 64 * b, hz,
+                    tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &zfull[s], 64 * b, hz,
                                 t0, (int)row);
-                // X is copied even when this wait gives up, so that the drain
-                // below sees the stage complete
-                const bool xok = c < TC_NST || bwait(&xfree[s], ph, abort_flag);
-#pragma unroll
-                for (int b = 0; b < TC_D / 64; ++b)
-                    tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, hx, t0, (int)row);
                 ++issued;
-                if (!xok)
+                if (!zok)
                     break;
             }
             // every copy this thread issued has landed before the CTA may exit
-            for (int c = issued > TC_NST ? issued - TC_NST : 0; c < issued; ++c)
+            for (int c = issued > TC_NST ? issued - TC_NST : 0; c < issued; ++c) {
                 drain_wait(&full[c % TC_NST], (c / TC_NST) & 1);
+                drain_wait(&zfull[c % TC_NST], (c / TC_NST) & 1);
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -436,6 +445,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 }
                 if (!bwait(p_ready, c & 1, abort_flag))
                     break;
+                if (!bwait(&zfull[s], (c / TC_NST) & 1, abort_flag))
+                    break;
                 tc_fence_after();
                 // S += (lcol Y)^T Z  (both MN-major, M = D, K = C tokens): the recurrence
 #pragma unroll
@@ -443,6 +454,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     mma_ss(tm + TM_S, sdesc_sw128(ya + kk * 2048, TC_C * 128, 1024),
                            sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_yz, 1);
                 mma_commit(ds_full);
+                mma_commit(&empty[s]);   // X and Y have been read for the last time
                 // P Z  (P from TMEM, Z: MN-major, K = C tokens)
 #pragma unroll
                 for (int kk = 0; kk < TC_C / 16; ++kk)
@@ -450,7 +462,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                            sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_xz, kk > 0);
                 mma_commit(o_full);
                 mma_commit(pv_done);
-                mma_commit(&empty[s]);
             }
             if (any) {   // every MMA has finished before TMEM is released
                 mma_commit(drain);
@@ -610,7 +621,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 // a tile store may run past the end of a dense sequence (the
                 // copy clips it) but not into the next packed sequence
                 const bool tile = Lc == TC_C || !a.cu;
-                uint8_t *otile = sm + s * L::STAGE;   // X slot, free once P Z is done
+                uint8_t *otile = sm + s * L::STAGE + L::XB + L::YB;   // Z slot, free once P Z is done
                 __nv_bfloat16 *orow = obase + (bos + chunk_t0(c) + i) * a.out.st;
 #pragma unroll 1
                 for (int part = 0; part < E / 32; ++part) {
@@ -649,7 +660,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 }
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&xfree[s]);   // this warp's rows of the X slot may be refilled
+                    mbar_arrive(&zfree[s]);   // this warp's rows of the Z slot may be refilled
             }
         }
     }
