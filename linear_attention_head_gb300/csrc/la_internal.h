@@ -73,10 +73,11 @@ struct SweepArgs {
     int withhold_handoff;     // diagnostic: tensor-core kernels skip one hand-off
     int64_t max_len;          // longest sequence (T when dense)
     Gate gate;                // per-key log-decay gate, or p == nullptr
+    int64_t prefetch_ctas = 0;  // token-by-token kernels: L2 prefetch distance in CTAs
 };
 
 // Calls whose longest sequence has at most this many tokens run the
-// token-by-token kernels (la_short.cu) instead of the chunked ones.
+// token-by-token kernels (la_token.cu) instead of the chunked ones.
 constexpr int SHORT_MAX_T = 16;
 
 // Host-side count of enqueued kernels (la_launch_count).

@@ -1,0 +1,672 @@
+// la_token.cu -- token-by-token kernels: decoding a few new tokens against a
+// carried state, any call whose longest sequence has at most SHORT_MAX_T
+// tokens, and every call with a per-key gate (any length).
+//
+// They run the recurrence itself (ejkernel `recurrent` docstring, "The core
+// update") one token at a time instead of the chunked form:
+//   forward-type:  S <- A_t S + k_t v_t^T,   out_t = s q_t^T S
+//   backward-type: G <- G + s q_t w_t^T,     out_t = G^T k_t,   G <- A_t G
+// (the two sweep shapes of la_internal.h, visited in the same token order as
+// the chunked kernels), where A_t is the decay exp(g[h]) -- times exp(gate)
+// per state row or per state column when a gate is given.
+//
+// Thread layout.  A thread carries a 16-row x 4-column block of the fp32
+// state in registers for the whole sequence: rows 16 rg .. 16 rg + 15 and
+// the four adjacent columns of its column quad.  A warp holds RGN row groups
+// x QW quads (RGN x QW = 32, RGN the smallest power of two with 16 RGN >= D),
+// i.e. every row of 4 QW columns, so
+//   * the state is read and written once, in 16-byte pieces, and the QW lanes
+//     of a row group cover 16 QW contiguous bytes of a state row;
+//   * a column's dot product over the rows is summed inside the warp: a
+//     reduce-scatter over the row-group lanes (halves of the quad first).
+// Each row is updated with packed f32x2 arithmetic on the column pairs.  The
+// per-row factors (q, k, row decay) come from shared-memory tables that hold
+// every value twice, so that one 16-byte load yields the pairs of two rows.
+// Tokens pass through shared memory TB at a time (16-byte cp.async copies,
+// double-buffered, when every row is 16-byte aligned); warps share nothing
+// else, and the token loop has no barrier inside a block.
+
+#include <cstdint>
+#include <type_traits>
+
+#include <cuda_bf16.h>
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int TB = 16;    // tokens per shared-memory block
+constexpr int MAXW = 8;   // warps per CTA
+// floats per (token, row group) in the paired row tables for RP rows per
+// thread: the 2 RP values and a pad that puts the row groups a quarter warp
+// reads at once in different banks
+__host__ __device__ constexpr int pair_stride(int rp) { return 2 * rp + (rp == 16 ? 8 : 4); }
+
+template <typename T> __device__ __forceinline__ float ld_tok(const T *p);
+template <> __device__ __forceinline__ float ld_tok<float>(const float *p) { return *p; }
+template <> __device__ __forceinline__ float ld_tok<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    return __bfloat162float(*p);
+}
+template <typename T> __device__ __forceinline__ void st_tok(T *p, float x);
+template <> __device__ __forceinline__ void st_tok<float>(float *p, float x) { *p = x; }
+template <> __device__ __forceinline__ void st_tok<__nv_bfloat16>(__nv_bfloat16 *p, float x)
+{
+    *p = __float2bfloat16_rn(x);
+}
+
+// Packed two-lane fp32 arithmetic (round to nearest) on 64-bit register
+// pairs: a pair of floats is carried as one 64-bit value, so that the
+// operands of the packed instructions are always aligned register pairs.
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
+{
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b)
+{
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b)
+{
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2 pack2(float lo, float hi)
+{
+    f2 d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ float2 unpack2(f2 x)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x));
+    return r;
+}
+
+__device__ __forceinline__ float &comp(float4 &v, int c)
+{
+    return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
+// CTA shape for widths D (state rows) and E (state columns).
+struct Shape {
+    int rgn;     // row groups per warp (power of two, 16 rgn >= D)
+    int qw;      // column quads per warp (32 / rgn)
+    int wc;      // columns per warp (4 qw)
+    int wpc;     // warps per CTA
+    int cw;      // columns per CTA (wpc wc)
+    int tiles;   // CTAs per (sequence, head)
+};
+
+__host__ __device__ inline Shape token_shape(int D, int E, int rp)
+{
+    Shape s;
+    s.rgn = 1;
+    while (rp * s.rgn < D)
+        s.rgn *= 2;
+    s.qw = 32 / s.rgn;
+    s.wc = 4 * s.qw;
+    const int need = (E + s.wc - 1) / s.wc;
+    s.wpc = need < MAXW ? need : MAXW;
+    s.cw = s.wpc * s.wc;
+    s.tiles = (E + s.cw - 1) / s.cw;
+    return s;
+}
+
+// tokens per shared-memory block for a call whose longest sequence is max_len
+__host__ __device__ inline int token_block(int64_t max_len)
+{
+    return max_len >= TB ? TB : (max_len < 1 ? 1 : (int)max_len);
+}
+
+// Dynamic shared memory of one CTA: the paired row tables q, k (and the row
+// decays for a row gate) [tbe][rgn][SK], the value columns (and column
+// decays for a column gate) [tbe][cw]; for the asynchronous path two raw
+// buffers of tbe token rows: q, k [D], the value tile [cw] (token dtype) and
+// the gate's row [D] or tile [cw] (fp32).
+__host__ __device__ inline size_t token_smem_bytes(const Shape &s, int rp, int D, int tbe,
+                                                   int esz, int gate, bool async)
+{
+    const size_t tab = (size_t)tbe * s.rgn * pair_stride(rp);
+    size_t f = tab * (gate == 1 ? 3 : 2) + (size_t)tbe * s.cw * (gate == 2 ? 2 : 1);
+    size_t b = f * 4;
+    if (async)
+        b += (size_t)2 * tbe * ((size_t)2 * D * esz + (size_t)s.cw * esz +
+                                (gate == 1 ? (size_t)D * 4 : 0) + (gate == 2 ? (size_t)s.cw * 4 : 0));
+    return b;
+}
+
+// GATE: 0 the head's decay only, 1 per-row gate, 2 per-column gate.
+// SHORTC (calls of at most SHORT_MAX_T tokens): one token at a time, so
+// that the kernel fits two CTAs per SM and keeps twice the state loads in
+// flight; otherwise tokens go in batches of four, whose row-group sums
+// overlap, at one CTA per SM.
+template <typename T, bool BWD, int GATE, bool ASYNC, bool SHORTC>
+__global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepArgs a)
+{
+    constexpr int RP = 16;
+    constexpr int SK = pair_stride(RP);
+    const int D = a.D, E = a.E;
+    const Shape sp = token_shape(D, E, RP);
+    const int tile = (int)(blockIdx.x % sp.tiles);
+    const int h = (int)((blockIdx.x / sp.tiles) % a.H);
+    const int n = (int)(blockIdx.x / ((unsigned)sp.tiles * a.H));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qd = lane & (sp.qw - 1), rg = lane / sp.qw;
+    const int cb = tile * sp.cw;                 // the CTA's first column
+    const int cl = warp * sp.wc + 4 * qd;        // the thread's quad within the CTA's columns
+    const int c0 = cb + cl;                      // ... and in the state
+    const int r0 = RP * rg;
+    const int tbe = token_block(a.max_len);
+    const int nthr = blockDim.x;
+    extern __shared__ __align__(16) float sh[];
+
+    int64_t row, bos, len;
+    if (a.cu) {
+        row = 0;
+        bos = a.cu[n];
+        len = (int64_t)a.cu[n + 1] - a.cu[n];
+    } else {
+        row = n;
+        bos = 0;
+        len = a.T;
+    }
+    const int tab = tbe * sp.rgn * SK;
+    float *qs = sh;
+    float *ks = qs + tab;
+    float *as = ks + tab;                               // row decays (GATE 1)
+    float *vs = as + (GATE == 1 ? tab : 0);
+    float *acs = vs + tbe * sp.cw;                      // column decays (GATE 2)
+    // forward-type visits tokens in processing order, backward-type against it
+    const bool flip = (a.reverse != 0) != BWD;
+    auto token = [&](int64_t u) { return bos + (flip ? len - 1 - u : u); };
+
+    const float gh = a.g[h];
+    const float gam = expf(gh);
+    const float scale = a.scale;
+    const int64_t sbase = ((int64_t)n * a.H + h) * (int64_t)D * E;
+    // token rows of this (sequence, head): key/value heads may be shared
+    const T *qb = reinterpret_cast<const T *>(a.q.p) + row * a.q.sb +
+                  (int64_t)(h / a.q.hdiv) * a.q.sh;
+    const T *kb = reinterpret_cast<const T *>(a.k.p) + row * a.k.sb +
+                  (int64_t)(h / a.k.hdiv) * a.k.sh;
+    const T *vb = reinterpret_cast<const T *>(a.v.p) + row * a.v.sb +
+                  (int64_t)(h / a.v.hdiv) * a.v.sh;
+    const float *gb = GATE ? a.gate.p + row * a.gate.sb + (int64_t)h * a.gate.sh : nullptr;
+    T *ob = reinterpret_cast<T *>(a.out.p) + row * a.out.sb + (int64_t)h * a.out.sh;
+
+    // ---- the state block: S[j] = state(r0 + j, c0 .. c0 + 3) ----------------
+    // Loaded as 16-byte pieces along whichever state axis is contiguous,
+    // element by element otherwise; these loads are in flight while the first
+    // tokens are copied below.
+    float4 S[RP];
+    {
+        const float *p = a.s_in.p;
+        // bulk prefetches of whole (sequence, head) state blocks into L2 when
+        // they are contiguous: this CTA's own, and the one of the CTA that
+        // starts a resident wave later, so that its loads find the state in
+        // L2 instead of each waiting a full trip to HBM
+        if (threadIdx.x == 0 && p && (reinterpret_cast<uintptr_t>(p) & 15) == 0 &&
+            ((a.s_in.cs == 1 && a.s_in.rs == E) || (a.s_in.rs == 1 && a.s_in.cs == D)) &&
+            ((int64_t)D * E) % 4 == 0) {
+            const uint32_t bytes = (uint32_t)((int64_t)D * E * 4);
+            if (tile == 0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + sbase),
+                             "r"(bytes)
+                             : "memory");
+            const int64_t ahead = (int64_t)blockIdx.x + a.prefetch_ctas;
+            if (a.prefetch_ctas > 0 && ahead < (int64_t)gridDim.x && ahead % sp.tiles == 0) {
+                const int64_t hn = ahead / sp.tiles;   // (sequence, head) of that CTA
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                 p + hn * (int64_t)D * E),
+                             "r"(bytes)
+                             : "memory");
+            }
+        }
+        const int64_t rs = a.s_in.rs, cs = a.s_in.cs;
+        const bool al = p && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+        if (p && al && cs == 1 && rs % 4 == 0 && E % 4 == 0) {
+#pragma unroll
+            for (int j = 0; j < RP; ++j)
+                S[j] = c0 < E && r0 + j < D
+                           ? *reinterpret_cast<const float4 *>(p + sbase + (int64_t)(r0 + j) * rs + c0)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (p && al && rs == 1 && cs % 4 == 0 && D % 4 == 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int j4 = 0; j4 < RP / 4; ++j4) {
+                    const float4 x = c0 + c < E && r0 + 4 * j4 < D
+                                         ? *reinterpret_cast<const float4 *>(
+                                               p + sbase + (int64_t)(c0 + c) * cs + r0 + 4 * j4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    comp(S[4 * j4 + 0], c) = x.x;
+                    comp(S[4 * j4 + 1], c) = x.y;
+                    comp(S[4 * j4 + 2], c) = x.z;
+                    comp(S[4 * j4 + 3], c) = x.w;
+                }
+        } else {
+#pragma unroll
+            for (int j = 0; j < RP; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    comp(S[j], c) = p && c0 + c < E && r0 + j < D
+                                        ? p[sbase + (int64_t)(r0 + j) * rs + (int64_t)(c0 + c) * cs]
+                                        : 0.f;
+        }
+    }
+
+    // the state as column pairs: S01[j] = columns c0, c0 + 1 of row r0 + j,
+    // S23[j] = columns c0 + 2, c0 + 3
+    f2 S01[RP], S23[RP];
+#pragma unroll
+    for (int j = 0; j < RP; ++j) {
+        S01[j] = pack2(S[j].x, S[j].y);
+        S23[j] = pack2(S[j].z, S[j].w);
+    }
+
+    // ---- staging: one block of Lb tokens into the compute layout -------------
+    // paired row tables: (token u, row r) at (u rgn + r / 16) SK + 2 (r % 16),
+    // twice; rows past D hold zero (decay one)
+    const int RR = RP * sp.rgn;
+    auto put_row = [&](int u, int r, float xq, float xk, float xa) {
+        const int at = (u * sp.rgn + r / RP) * SK + 2 * (r % RP);
+        if (BWD)
+            xq *= scale;
+        *reinterpret_cast<float2 *>(qs + at) = make_float2(xq, xq);
+        *reinterpret_cast<float2 *>(ks + at) = make_float2(xk, xk);
+        if (GATE == 1)
+            *reinterpret_cast<float2 *>(as + at) = make_float2(xa, xa);
+    };
+    constexpr int PF = 8;
+    auto load_sync = [&](int64_t b0, int Lb) {
+        const int nr = Lb * RR;
+        for (int base = threadIdx.x; base < nr; base += PF * nthr) {
+            float xq[PF], xk[PF], xa[PF];
+#pragma unroll
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr, u = idx / RR, r = idx % RR;
+                xq[i] = xk[i] = 0.f;
+                xa[i] = 0.f;
+                if (idx < nr && r < D) {
+                    const int64_t t = token(b0 + u);
+                    xq[i] = ld_tok(qb + t * a.q.st + r);
+                    xk[i] = ld_tok(kb + t * a.k.st + r);
+                    if (GATE == 1)
+                        xa[i] = gb[t * a.gate.st + r];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr, u = idx / RR, r = idx % RR;
+                if (idx < nr)
+                    put_row(u, r, xq[i], xk[i], GATE == 1 && r < D ? expf(gh + xa[i]) : 1.f);
+            }
+        }
+        const int nv = Lb * sp.cw;
+        for (int base = threadIdx.x; base < nv; base += PF * nthr) {
+            float xv[PF], xg[PF];
+#pragma unroll
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr, u = idx / sp.cw, c = idx % sp.cw;
+                xv[i] = 0.f;
+                xg[i] = 0.f;
+                if (idx < nv && cb + c < E) {
+                    const int64_t t = token(b0 + u);
+                    xv[i] = ld_tok(vb + t * a.v.st + cb + c);
+                    if (GATE == 2)
+                        xg[i] = gb[t * a.gate.st + cb + c];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < PF; ++i) {
+                const int idx = base + i * nthr;
+                if (idx < nv) {
+                    vs[idx] = xv[i];
+                    if (GATE == 2)
+                        acs[idx] = expf(gh + xg[i]);
+                }
+            }
+        }
+    };
+
+    // ---- the recurrence over one staged block --------------------------------
+    // Per token a thread forms the partial dot products of its four columns
+    // over its 16 rows; those of four tokens are then summed over the warp's
+    // row groups together, so that their shuffles overlap.
+    const bool bA = (rg & 1) != 0, bB = (rg & 2) != 0;
+    const f2 gg = pack2(gam, gam);
+    const float sc = BWD ? 1.f : scale;
+    // NT tokens from u0 on (NT = 4: a full batch, 1: the tail of a block)
+    auto process = [&](auto ntc, int64_t b0, int u0) {
+        constexpr int NT = decltype(ntc)::value;
+        // after the exchange over the first row-group bit each lane keeps two
+        // columns of the quad: 2 bA, 2 bA + 1 (hv; all four, hv and hw, when
+        // rgn = 1)
+        float2 hv[NT], hw[NT];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            const int u = u0 + i;
+            // (row 2p, row 2p + 1) pairs of q, k and the row decays
+            const int at = (u * sp.rgn + rg) * SK;
+            const ulonglong2 *q2 = reinterpret_cast<const ulonglong2 *>(qs + at);
+            const ulonglong2 *k2 = reinterpret_cast<const ulonglong2 *>(ks + at);
+            const ulonglong2 *a2 = reinterpret_cast<const ulonglong2 *>(as + at);
+            const ulonglong2 w = *reinterpret_cast<const ulonglong2 *>(vs + u * sp.cw + cl);
+            f2 c01 = gg, c23 = gg;   // column decays
+            if (GATE == 2) {
+                const ulonglong2 ac = *reinterpret_cast<const ulonglong2 *>(acs + u * sp.cw + cl);
+                c01 = ac.x;
+                c23 = ac.y;
+            }
+            f2 e01 = 0ull, e23 = 0ull, o01 = 0ull, o23 = 0ull;
+#pragma unroll
+            for (int p = 0; p < RP / 2; ++p) {
+                const ulonglong2 qq = q2[p], kk = k2[p];
+                ulonglong2 aa;
+                if (GATE == 1)
+                    aa = a2[p];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int j = 2 * p + half;
+                    const f2 qp = half ? qq.y : qq.x, kp = half ? kk.y : kk.x;
+                    f2 d01 = c01, d23 = c23;
+                    if (GATE == 1)
+                        d01 = d23 = half ? aa.y : aa.x;
+                    f2 &x01 = half ? o01 : e01, &x23 = half ? o23 : e23;
+                    if (!BWD) {
+                        S01[j] = fma2(S01[j], d01, mul2(kp, w.x));
+                        S23[j] = fma2(S23[j], d23, mul2(kp, w.y));
+                        x01 = fma2(qp, S01[j], x01);
+                        x23 = fma2(qp, S23[j], x23);
+                    } else {
+                        S01[j] = fma2(qp, w.x, S01[j]);
+                        S23[j] = fma2(qp, w.y, S23[j]);
+                        x01 = fma2(kp, S01[j], x01);
+                        x23 = fma2(kp, S23[j], x23);
+                        S01[j] = mul2(S01[j], d01);
+                        S23[j] = mul2(S23[j], d23);
+                    }
+                }
+            }
+            const float2 p01 = unpack2(add2(e01, o01)), p23 = unpack2(add2(e23, o23));
+            if (sp.rgn == 1) {
+                hv[i] = p01;
+                hw[i] = p23;
+            } else {
+                const float2 keep = bA ? p23 : p01, send = bA ? p01 : p23;
+                hv[i].x = keep.x + __shfl_xor_sync(0xffffffffu, send.x, sp.qw);
+                hv[i].y = keep.y + __shfl_xor_sync(0xffffffffu, send.y, sp.qw);
+            }
+        }
+        if (sp.rgn == 1) {
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                T *op = ob + token(b0 + u0 + i) * a.out.st + c0;
+                const float x[4] = {hv[i].x, hv[i].y, hw[i].x, hw[i].y};
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (c0 + c < E)
+                        st_tok(op + c, sc * x[c]);
+            }
+            return;
+        }
+        if (sp.rgn == 2) {
+            const int c = c0 + (bA ? 2 : 0);
+#pragma unroll
+            for (int i = 0; i < NT; ++i) {
+                T *op = ob + token(b0 + u0 + i) * a.out.st;
+                if (c < E)
+                    st_tok(op + c, sc * hv[i].x);
+                if (c + 1 < E)
+                    st_tok(op + c + 1, sc * hv[i].y);
+            }
+            return;
+        }
+        // one column per lane over the second bit, then plain sums
+        float val[NT];
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            const float keep = bB ? hv[i].y : hv[i].x;
+            const float send = bB ? hv[i].x : hv[i].y;
+            val[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * sp.qw);
+        }
+        for (int off = 4 * sp.qw; off < 32; off <<= 1) {
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+                val[i] += __shfl_xor_sync(0xffffffffu, val[i], off);
+        }
+        const int c = c0 + (bA ? 2 : 0) + (bB ? 1 : 0);
+        if (rg < 4 && c < E) {
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+                st_tok(ob + token(b0 + u0 + i) * a.out.st + c, sc * val[i]);
+        }
+    };
+    auto compute = [&](int64_t b0, int Lb) {
+        int u0 = 0;
+        for (; !SHORTC && u0 + 4 <= Lb; u0 += 4)
+            process(std::integral_constant<int, 4>(), b0, u0);
+        for (; u0 < Lb; ++u0)
+            process(std::integral_constant<int, 1>(), b0, u0);
+    };
+
+    // ASYNC (chosen on the host when every row is 16-byte aligned):
+    // double-buffered 16-byte cp.async copies of the raw rows, the next
+    // block's copies in flight while this block is converted and computed.
+    if (!ASYNC) {
+        for (int64_t b0 = 0; b0 < len; b0 += tbe) {
+            const int Lb = (int)(len - b0 < tbe ? len - b0 : tbe);
+            load_sync(b0, Lb);
+            __syncthreads();
+            compute(b0, Lb);
+            __syncthreads();   // the next block overwrites the tables
+        }
+    } else {
+        const int esz = (int)sizeof(T);
+        T *rq = reinterpret_cast<T *>(acs + (GATE == 2 ? tbe * sp.cw : 0));
+        T *rk = rq + 2 * tbe * D;
+        T *rv = rk + 2 * tbe * D;
+        float *rgt = reinterpret_cast<float *>(rv + 2 * tbe * sp.cw);   // gate rows or tiles
+        const int gw = GATE == 1 ? D : sp.cw;                            // gate floats per token
+        const int ecols = E - cb < sp.cw ? E - cb : sp.cw;               // valid columns here
+        const int cq = D * esz / 16, cv = ecols * esz / 16;
+        const int cg = GATE == 1 ? D / 4 : (GATE == 2 ? ecols / 4 : 0);
+        auto issue = [&](int64_t b0, int Lb, int buf) {
+            const int per = 2 * cq + cv + cg;
+            for (int idx = threadIdx.x; idx < Lb * per; idx += nthr) {
+                const int u = idx / per;
+                int r = idx % per;
+                const int64_t t = token(b0 + u);
+                const void *src;
+                void *dst;
+                if (r < cq) {
+                    src = qb + t * a.q.st + r * (16 / esz);
+                    dst = rq + ((size_t)buf * tbe + u) * D + r * (16 / esz);
+                } else if ((r -= cq) < cq) {
+                    src = kb + t * a.k.st + r * (16 / esz);
+                    dst = rk + ((size_t)buf * tbe + u) * D + r * (16 / esz);
+                } else if ((r -= cq) < cv) {
+                    src = vb + t * a.v.st + cb + r * (16 / esz);
+                    dst = rv + ((size_t)buf * tbe + u) * sp.cw + r * (16 / esz);
+                } else {
+                    r -= cv;
+                    src = gb + t * a.gate.st + (GATE == 2 ? cb : 0) + 4 * r;
+                    dst = rgt + ((size_t)buf * tbe + u) * gw + 4 * r;
+                }
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                 static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                             "l"(src)
+                             : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        auto convert = [&](int Lb, int buf) {
+            for (int idx = threadIdx.x; idx < Lb * RR; idx += nthr) {
+                const int u = idx / RR, r = idx % RR;
+                const size_t rr = ((size_t)buf * tbe + u) * D + r;
+                const bool ok = r < D;
+                put_row(u, r, ok ? ld_tok(rq + rr) : 0.f, ok ? ld_tok(rk + rr) : 0.f,
+                        GATE == 1 && ok ? expf(gh + rgt[((size_t)buf * tbe + u) * gw + r]) : 1.f);
+            }
+            for (int idx = threadIdx.x; idx < Lb * sp.cw; idx += nthr) {
+                const int u = idx / sp.cw, c = idx % sp.cw;
+                const bool ok = c < ecols;
+                vs[idx] = ok ? ld_tok(rv + ((size_t)buf * tbe + u) * sp.cw + c) : 0.f;
+                if (GATE == 2)
+                    acs[idx] = ok ? expf(gh + rgt[((size_t)buf * tbe + u) * gw + c]) : 1.f;
+            }
+        };
+        int it = 0;
+        if (len > 0)
+            issue(0, (int)(len < tbe ? len : tbe), 0);
+        for (int64_t b0 = 0; b0 < len; b0 += tbe, ++it) {
+            const int Lb = (int)(len - b0 < tbe ? len - b0 : tbe);
+            if (b0 + tbe < len) {
+                issue(b0 + tbe, (int)(len - b0 - tbe < tbe ? len - b0 - tbe : tbe), (it + 1) & 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+            __syncthreads();   // every thread's copies of this block landed
+            convert(Lb, it & 1);
+            __syncthreads();
+            compute(b0, Lb);
+            __syncthreads();   // the tables and this raw buffer are free again
+        }
+    }
+
+    // ---- the state block out --------------------------------------------------
+#pragma unroll
+    for (int j = 0; j < RP; ++j) {
+        const float2 lo = unpack2(S01[j]), hi = unpack2(S23[j]);
+        S[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    float *p = a.s_out.p;
+    if (p) {
+        const int64_t rs = a.s_out.rs, cs = a.s_out.cs;
+        const bool al = (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+        if (al && cs == 1 && rs % 4 == 0 && E % 4 == 0) {
+            if (c0 < E) {
+#pragma unroll
+                for (int j = 0; j < RP; ++j)
+                    if (r0 + j < D)
+                        *reinterpret_cast<float4 *>(p + sbase + (int64_t)(r0 + j) * rs + c0) = S[j];
+            }
+        } else if (al && rs == 1 && cs % 4 == 0 && D % 4 == 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int j4 = 0; j4 < RP / 4; ++j4)
+                    if (c0 + c < E && r0 + 4 * j4 < D)
+                        *reinterpret_cast<float4 *>(p + sbase + (int64_t)(c0 + c) * cs + r0 +
+                                                    4 * j4) =
+                            make_float4(comp(S[4 * j4 + 0], c), comp(S[4 * j4 + 1], c),
+                                        comp(S[4 * j4 + 2], c), comp(S[4 * j4 + 3], c));
+        } else {
+#pragma unroll
+            for (int j = 0; j < RP; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (c0 + c < E && r0 + j < D)
+                        p[sbase + (int64_t)(r0 + j) * rs + (int64_t)(c0 + c) * cs] = comp(S[j], c);
+        }
+    }
+}
+
+// Rows of every tensor 16-byte aligned (base, strides, widths): the copies
+// can be 16-byte cp.async.
+bool rows_aligned(const SweepArgs &a, int esz)
+{
+    auto ok = [&](const void *p, int64_t sb, int64_t st, int64_t sh, int64_t es) {
+        return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && (sb * es) % 16 == 0 &&
+               (st * es) % 16 == 0 && (sh * es) % 16 == 0;
+    };
+    bool r = ok(a.q.p, a.q.sb, a.q.st, a.q.sh, esz) && ok(a.k.p, a.k.sb, a.k.st, a.k.sh, esz) &&
+             ok(a.v.p, a.v.sb, a.v.st, a.v.sh, esz) && (a.D * esz) % 16 == 0 &&
+             (a.E * esz) % 16 == 0;
+    if (a.gate.p)
+        r = r && ok(a.gate.p, a.gate.sb, a.gate.st, a.gate.sh, 4) && a.D % 4 == 0 && a.E % 4 == 0;
+    return r;
+}
+
+template <typename K>
+cudaError_t launch_one(K kernel, const SweepArgs &a0, cudaStream_t s, int gate, bool async)
+{
+    SweepArgs a = a0;
+    const Shape sp = token_shape(a.D, a.E, 16);
+    const size_t smem =
+        token_smem_bytes(sp, 16, a.D, token_block(a.max_len), a.bf16 ? 2 : 4, gate, async);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    // CTAs resident at once: the distance of the L2 prefetch ahead
+    int per_sm = 0, dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, sp.wpc * 32, smem);
+    if (e != cudaSuccess)
+        return e;
+    a.prefetch_ctas = (int64_t)per_sm * sms;
+    const int64_t blocks = (int64_t)a.N * a.H * sp.tiles;
+    kernel<<<(unsigned)blocks, sp.wpc * 32, smem, s>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <typename T, bool BWD, bool ASYNC, bool SHORTC>
+cudaError_t launch_gate(const SweepArgs &a, cudaStream_t s)
+{
+    if (!a.gate.p)
+        return launch_one(token_kernel<T, BWD, 0, ASYNC, SHORTC>, a, s, 0, ASYNC);
+    return a.gate.cols ? launch_one(token_kernel<T, BWD, 2, ASYNC, SHORTC>, a, s, 2, ASYNC)
+                       : launch_one(token_kernel<T, BWD, 1, ASYNC, SHORTC>, a, s, 1, ASYNC);
+}
+
+template <typename T, bool BWD, bool SHORTC>
+cudaError_t launch_rows(const SweepArgs &a, cudaStream_t s)
+{
+    return rows_aligned(a, (int)sizeof(T)) ? launch_gate<T, BWD, true, SHORTC>(a, s)
+                                           : launch_gate<T, BWD, false, SHORTC>(a, s);
+}
+
+template <bool BWD> cudaError_t launch_token(const SweepArgs &a, cudaStream_t s)
+{
+    if (a.N == 0 || a.H == 0)
+        return cudaSuccess;
+    if (a.D < 1 || a.D > 256 || a.E < 1)
+        return cudaErrorNotSupported;
+    if ((int64_t)a.N * a.H * token_shape(a.D, a.E, 16).tiles > 0x7fffffff)
+        return cudaErrorNotSupported;
+    const bool shortc = a.max_len <= SHORT_MAX_T;
+    if (a.bf16)
+        return shortc ? launch_rows<__nv_bfloat16, BWD, true>(a, s)
+                      : launch_rows<__nv_bfloat16, BWD, false>(a, s);
+    return shortc ? launch_rows<float, BWD, true>(a, s) : launch_rows<float, BWD, false>(a, s);
+}
+
+}  // namespace
+
+cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s)
+{
+    return launch_token<false>(a, s);
+}
+
+cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s)
+{
+    return launch_token<true>(a, s);
+}
+
+}  // namespace la

@@ -2,7 +2,7 @@
 
 Decoding a few new tokens against a carried state is the serving use of the
 recurrence (the pages' `recurrent` API, an initial state in and the final
-state out).  These calls run la_short.cu instead of the chunked kernels; the
+state out).  These calls run la_token.cu instead of the chunked kernels; the
 tests check them against the oracle at every flag, head width and dtype, and
 check that decoding a sequence piece by piece, each call's final state fed to
 the next as its initial state, equals one call over the whole sequence.
