@@ -28,7 +28,9 @@
  *     grouped key/value heads k, dk and v, dv have their own, see la_dims).
  *     Both the token-major layout [B,T,H,X] (ejkernel) and the head-major
  *     layout [B,H,T,X] (Lightning-2's (b, h, n, d)) are expressible.  Outputs
- *     must not overlap inputs or each other.
+ *     must not overlap inputs or each other, with one exception: the forward
+ *     calls' final_state may be the very buffer passed as initial_state (an
+ *     in-place state update, as in decoding).
  *   - State tensors (initial_state, final_state, d_final_state,
  *     d_initial_state) are dense fp32 [N, H, D, E], N = B, or num_seqs when
  *     cu_seqlens is given.

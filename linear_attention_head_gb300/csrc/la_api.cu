@@ -724,8 +724,13 @@ la_status la_get_device_error(void *stream)
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e == cudaSuccess)
         e = la::tc_read_and_clear_error((cudaStream_t)stream, &err);
+    int err2 = 0;
+    if (e == cudaSuccess)
+        e = la::token_read_and_clear_error((cudaStream_t)stream, &err2);
     if (e != cudaSuccess)
         return cuda_fail(e, "la_get_device_error");
+    if (!err)
+        err = err2;
     if (err)
         return fail(LA_ERR_TIMEOUT, "an on-device wait ran out (code %d)", err);
     return LA_OK;

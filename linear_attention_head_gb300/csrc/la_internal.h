@@ -97,6 +97,9 @@ cudaError_t simt_backward_sweep(const SweepArgs &a, cudaStream_t s);
 // most SHORT_MAX_T tokens.
 cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s);
+// Reads (after synchronizing s) and clears the token kernels' device error
+// word (LA_ERR_TIMEOUT when a wait of the streamed decode kernel ran out).
+cudaError_t token_read_and_clear_error(cudaStream_t s, int *err);
 
 // Tensor-core (tcgen05) kernels for bf16, both sweep shapes; eligibility
 // (dtype, widths, 16-byte alignment) is the same for both.

@@ -31,10 +31,12 @@
 
 #include <cuda_bf16.h>
 #include "la_internal.h"
+#include "la_sm100.cuh"
 
 namespace la {
 namespace {
 
+constexpr int RP = 16;    // state rows per thread
 constexpr int TB = 16;    // tokens per shared-memory block
 constexpr int MAXW = 8;   // warps per CTA
 // floats per (token, row group) in the paired row tables for RP rows per
@@ -144,29 +146,43 @@ __host__ __device__ inline size_t token_smem_bytes(const Shape &s, int rp, int D
 }
 
 // GATE: 0 the head's decay only, 1 per-row gate, 2 per-column gate.
-// SHORTC (calls of at most SHORT_MAX_T tokens): one token at a time, so
-// that the kernel fits two CTAs per SM and keeps twice the state loads in
-// flight; otherwise tokens go in batches of four, whose row-group sums
-// overlap, at one CTA per SM.
-template <typename T, bool BWD, int GATE, bool ASYNC, bool SHORTC>
-__global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepArgs a)
+struct CtaSync {
+    __device__ void operator()() const { __syncthreads(); }
+};
+// barrier 1 over the first `count` threads of the CTA
+struct NamedSync {
+    int count;
+    __device__ void operator()() const { asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory"); }
+};
+
+// The tokens of (sequence n, head h) for the state block of thread tid (of
+// nthr, column tile `tile`), carried in S01 / S23: staging through `sh` and
+// the recurrence.  Sync is a barrier over the nthr threads.  SHORTC (calls
+// of at most SHORT_MAX_T tokens): one token at a time; otherwise batches of
+// four tokens whose row-group sums overlap.
+// Raw token rows of one short sequence already in shared memory, in
+// processing order: q, k [u][D], the value tile [u][cw] (token dtype) and the
+// row gate [u][D] (fp32); q == nullptr when the rows are to be fetched.
+struct RawRows {
+    const void *q = nullptr, *k = nullptr, *v = nullptr;
+    const float *g = nullptr;
+};
+
+template <typename T, bool BWD, int GATE, bool ASYNC, bool SHORTC, typename Sync>
+__device__ __forceinline__ void token_loop(const SweepArgs &a, const Shape &sp, int n, int h,
+                                           int tile, int tid, int nthr, float *sh,
+                                           f2 (&S01)[RP], f2 (&S23)[RP], Sync sync,
+                                           RawRows pre = RawRows())
 {
-    constexpr int RP = 16;
     constexpr int SK = pair_stride(RP);
     const int D = a.D, E = a.E;
-    const Shape sp = token_shape(D, E, RP);
-    const int tile = (int)(blockIdx.x % sp.tiles);
-    const int h = (int)((blockIdx.x / sp.tiles) % a.H);
-    const int n = (int)(blockIdx.x / ((unsigned)sp.tiles * a.H));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = tid >> 5, lane = tid & 31;
     const int qd = lane & (sp.qw - 1), rg = lane / sp.qw;
     const int cb = tile * sp.cw;                 // the CTA's first column
     const int cl = warp * sp.wc + 4 * qd;        // the thread's quad within the CTA's columns
     const int c0 = cb + cl;                      // ... and in the state
     const int r0 = RP * rg;
     const int tbe = token_block(a.max_len);
-    const int nthr = blockDim.x;
-    extern __shared__ __align__(16) float sh[];
 
     int64_t row, bos, len;
     if (a.cu) {
@@ -191,7 +207,6 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
     const float gh = a.g[h];
     const float gam = expf(gh);
     const float scale = a.scale;
-    const int64_t sbase = ((int64_t)n * a.H + h) * (int64_t)D * E;
     // token rows of this (sequence, head): key/value heads may be shared
     const T *qb = reinterpret_cast<const T *>(a.q.p) + row * a.q.sb +
                   (int64_t)(h / a.q.hdiv) * a.q.sh;
@@ -201,76 +216,6 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
                   (int64_t)(h / a.v.hdiv) * a.v.sh;
     const float *gb = GATE ? a.gate.p + row * a.gate.sb + (int64_t)h * a.gate.sh : nullptr;
     T *ob = reinterpret_cast<T *>(a.out.p) + row * a.out.sb + (int64_t)h * a.out.sh;
-
-    // ---- the state block: S[j] = state(r0 + j, c0 .. c0 + 3) ----------------
-    // Loaded as 16-byte pieces along whichever state axis is contiguous,
-    // element by element otherwise; these loads are in flight while the first
-    // tokens are copied below.
-    float4 S[RP];
-    {
-        const float *p = a.s_in.p;
-        // bulk prefetches of whole (sequence, head) state blocks into L2 when
-        // they are contiguous: this CTA's own, and the one of the CTA that
-        // starts a resident wave later, so that its loads find the state in
-        // L2 instead of each waiting a full trip to HBM
-        if (threadIdx.x == 0 && p && (reinterpret_cast<uintptr_t>(p) & 15) == 0 &&
-            ((a.s_in.cs == 1 && a.s_in.rs == E) || (a.s_in.rs == 1 && a.s_in.cs == D)) &&
-            ((int64_t)D * E) % 4 == 0) {
-            const uint32_t bytes = (uint32_t)((int64_t)D * E * 4);
-            if (tile == 0)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + sbase),
-                             "r"(bytes)
-                             : "memory");
-            const int64_t ahead = (int64_t)blockIdx.x + a.prefetch_ctas;
-            if (a.prefetch_ctas > 0 && ahead < (int64_t)gridDim.x && ahead % sp.tiles == 0) {
-                const int64_t hn = ahead / sp.tiles;   // (sequence, head) of that CTA
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                                 p + hn * (int64_t)D * E),
-                             "r"(bytes)
-                             : "memory");
-            }
-        }
-        const int64_t rs = a.s_in.rs, cs = a.s_in.cs;
-        const bool al = p && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
-        if (p && al && cs == 1 && rs % 4 == 0 && E % 4 == 0) {
-#pragma unroll
-            for (int j = 0; j < RP; ++j)
-                S[j] = c0 < E && r0 + j < D
-                           ? *reinterpret_cast<const float4 *>(p + sbase + (int64_t)(r0 + j) * rs + c0)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-        } else if (p && al && rs == 1 && cs % 4 == 0 && D % 4 == 0) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int j4 = 0; j4 < RP / 4; ++j4) {
-                    const float4 x = c0 + c < E && r0 + 4 * j4 < D
-                                         ? *reinterpret_cast<const float4 *>(
-                                               p + sbase + (int64_t)(c0 + c) * cs + r0 + 4 * j4)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                    comp(S[4 * j4 + 0], c) = x.x;
-                    comp(S[4 * j4 + 1], c) = x.y;
-                    comp(S[4 * j4 + 2], c) = x.z;
-                    comp(S[4 * j4 + 3], c) = x.w;
-                }
-        } else {
-#pragma unroll
-            for (int j = 0; j < RP; ++j)
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    comp(S[j], c) = p && c0 + c < E && r0 + j < D
-                                        ? p[sbase + (int64_t)(r0 + j) * rs + (int64_t)(c0 + c) * cs]
-                                        : 0.f;
-        }
-    }
-
-    // the state as column pairs: S01[j] = columns c0, c0 + 1 of row r0 + j,
-    // S23[j] = columns c0 + 2, c0 + 3
-    f2 S01[RP], S23[RP];
-#pragma unroll
-    for (int j = 0; j < RP; ++j) {
-        S01[j] = pack2(S[j].x, S[j].y);
-        S23[j] = pack2(S[j].z, S[j].w);
-    }
 
     // ---- staging: one block of Lb tokens into the compute layout -------------
     // paired row tables: (token u, row r) at (u rgn + r / 16) SK + 2 (r % 16),
@@ -288,7 +233,7 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
     constexpr int PF = 8;
     auto load_sync = [&](int64_t b0, int Lb) {
         const int nr = Lb * RR;
-        for (int base = threadIdx.x; base < nr; base += PF * nthr) {
+        for (int base = tid; base < nr; base += PF * nthr) {
             float xq[PF], xk[PF], xa[PF];
 #pragma unroll
             for (int i = 0; i < PF; ++i) {
@@ -311,7 +256,7 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
             }
         }
         const int nv = Lb * sp.cw;
-        for (int base = threadIdx.x; base < nv; base += PF * nthr) {
+        for (int base = tid; base < nv; base += PF * nthr) {
             float xv[PF], xg[PF];
 #pragma unroll
             for (int i = 0; i < PF; ++i) {
@@ -458,6 +403,26 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
             process(std::integral_constant<int, 1>(), b0, u0);
     };
 
+    if (pre.q) {
+        // the whole (short) sequence is in shared memory already
+        const T *pq = static_cast<const T *>(pre.q), *pk = static_cast<const T *>(pre.k);
+        const T *pv = static_cast<const T *>(pre.v);
+        const int Lb = (int)len;
+        for (int idx = tid; idx < Lb * RR; idx += nthr) {
+            const int u = idx / RR, r = idx % RR;
+            const bool ok = r < D;
+            put_row(u, r, ok ? ld_tok(pq + u * D + r) : 0.f, ok ? ld_tok(pk + u * D + r) : 0.f,
+                    GATE == 1 && ok ? expf(gh + pre.g[u * D + r]) : 1.f);
+        }
+        for (int idx = tid; idx < Lb * sp.cw; idx += nthr) {
+            const int u = idx / sp.cw, c = idx % sp.cw;
+            vs[idx] = cb + c < E ? ld_tok(pv + u * sp.cw + c) : 0.f;
+        }
+        sync();
+        compute(0, Lb);
+        sync();   // the tables are free again
+        return;
+    }
     // ASYNC (chosen on the host when every row is 16-byte aligned):
     // double-buffered 16-byte cp.async copies of the raw rows, the next
     // block's copies in flight while this block is converted and computed.
@@ -465,9 +430,9 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
         for (int64_t b0 = 0; b0 < len; b0 += tbe) {
             const int Lb = (int)(len - b0 < tbe ? len - b0 : tbe);
             load_sync(b0, Lb);
-            __syncthreads();
+            sync();
             compute(b0, Lb);
-            __syncthreads();   // the next block overwrites the tables
+            sync();   // the next block overwrites the tables
         }
     } else {
         const int esz = (int)sizeof(T);
@@ -481,7 +446,7 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
         const int cg = GATE == 1 ? D / 4 : (GATE == 2 ? ecols / 4 : 0);
         auto issue = [&](int64_t b0, int Lb, int buf) {
             const int per = 2 * cq + cv + cg;
-            for (int idx = threadIdx.x; idx < Lb * per; idx += nthr) {
+            for (int idx = tid; idx < Lb * per; idx += nthr) {
                 const int u = idx / per;
                 int r = idx % per;
                 const int64_t t = token(b0 + u);
@@ -509,14 +474,14 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
         auto convert = [&](int Lb, int buf) {
-            for (int idx = threadIdx.x; idx < Lb * RR; idx += nthr) {
+            for (int idx = tid; idx < Lb * RR; idx += nthr) {
                 const int u = idx / RR, r = idx % RR;
                 const size_t rr = ((size_t)buf * tbe + u) * D + r;
                 const bool ok = r < D;
                 put_row(u, r, ok ? ld_tok(rq + rr) : 0.f, ok ? ld_tok(rk + rr) : 0.f,
                         GATE == 1 && ok ? expf(gh + rgt[((size_t)buf * tbe + u) * gw + r]) : 1.f);
             }
-            for (int idx = threadIdx.x; idx < Lb * sp.cw; idx += nthr) {
+            for (int idx = tid; idx < Lb * sp.cw; idx += nthr) {
                 const int u = idx / sp.cw, c = idx % sp.cw;
                 const bool ok = c < ecols;
                 vs[idx] = ok ? ld_tok(rv + ((size_t)buf * tbe + u) * sp.cw + c) : 0.f;
@@ -535,15 +500,115 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
             } else {
                 asm volatile("cp.async.wait_group 0;" ::: "memory");
             }
-            __syncthreads();   // every thread's copies of this block landed
+            sync();   // every thread's copies of this block landed
             convert(Lb, it & 1);
-            __syncthreads();
+            sync();
             compute(b0, Lb);
-            __syncthreads();   // the tables and this raw buffer are free again
+            sync();   // the tables and this raw buffer are free again
         }
     }
 
+}
+
+// One CTA per (sequence, head, column tile).  SHORTC: fits two CTAs per SM
+// (128 registers), twice the state loads in flight; otherwise one CTA per SM.
+template <typename T, bool BWD, int GATE, bool ASYNC, bool SHORTC>
+__global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepArgs a)
+{
+    const int D = a.D, E = a.E;
+    const Shape sp = token_shape(D, E, RP);
+    const int tile = (int)(blockIdx.x % sp.tiles);
+    const int h = (int)((blockIdx.x / sp.tiles) % a.H);
+    const int n = (int)(blockIdx.x / ((unsigned)sp.tiles * a.H));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qd = lane & (sp.qw - 1), rg = lane / sp.qw;
+    const int c0 = tile * sp.cw + warp * sp.wc + 4 * qd;
+    const int r0 = RP * rg;
+    const int64_t sbase = ((int64_t)n * a.H + h) * (int64_t)D * E;
+    extern __shared__ __align__(16) float sh[];
+
+    // ---- the state block: S[j] = state(r0 + j, c0 .. c0 + 3) ----------------
+    // Loaded as 16-byte pieces along whichever state axis is contiguous,
+    // element by element otherwise; these loads are in flight while the first
+    // tokens are copied below.
+    // the state as column pairs: S01[j] = columns c0, c0 + 1 of row r0 + j,
+    // S23[j] = columns c0 + 2, c0 + 3
+    f2 S01[RP], S23[RP];
+    {
+        const float *p = a.s_in.p;
+        // bulk prefetches of whole (sequence, head) state blocks into L2 when
+        // they are contiguous: this CTA's own, and the one of the CTA that
+        // starts a resident wave later, so that its loads find the state in
+        // L2 instead of each waiting a full trip to HBM
+        if (threadIdx.x == 0 && p && (reinterpret_cast<uintptr_t>(p) & 15) == 0 &&
+            ((a.s_in.cs == 1 && a.s_in.rs == E) || (a.s_in.rs == 1 && a.s_in.cs == D)) &&
+            ((int64_t)D * E) % 4 == 0) {
+            const uint32_t bytes = (uint32_t)((int64_t)D * E * 4);
+            if (tile == 0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + sbase),
+                             "r"(bytes)
+                             : "memory");
+            const int64_t ahead = (int64_t)blockIdx.x + a.prefetch_ctas;
+            if (a.prefetch_ctas > 0 && ahead < (int64_t)gridDim.x && ahead % sp.tiles == 0) {
+                const int64_t hn = ahead / sp.tiles;   // (sequence, head) of that CTA
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                 p + hn * (int64_t)D * E),
+                             "r"(bytes)
+                             : "memory");
+            }
+        }
+        const int64_t rs = a.s_in.rs, cs = a.s_in.cs;
+        const bool al = p && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+        if (p && al && cs == 1 && rs % 4 == 0 && E % 4 == 0) {
+            // straight into the column pairs: nothing waits on these loads
+            // before the first token needs the state
+#pragma unroll
+            for (int j = 0; j < RP; ++j) {
+                ulonglong2 x = make_ulonglong2(0ull, 0ull);
+                if (c0 < E && r0 + j < D)
+                    x = *reinterpret_cast<const ulonglong2 *>(p + sbase + (int64_t)(r0 + j) * rs + c0);
+                S01[j] = x.x;
+                S23[j] = x.y;
+            }
+        } else {
+            float4 S[RP];
+            if (p && al && rs == 1 && cs % 4 == 0 && D % 4 == 0) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int j4 = 0; j4 < RP / 4; ++j4) {
+                        const float4 x = c0 + c < E && r0 + 4 * j4 < D
+                                             ? *reinterpret_cast<const float4 *>(
+                                                   p + sbase + (int64_t)(c0 + c) * cs + r0 + 4 * j4)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                        comp(S[4 * j4 + 0], c) = x.x;
+                        comp(S[4 * j4 + 1], c) = x.y;
+                        comp(S[4 * j4 + 2], c) = x.z;
+                        comp(S[4 * j4 + 3], c) = x.w;
+                    }
+            } else {
+#pragma unroll
+                for (int j = 0; j < RP; ++j)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        comp(S[j], c) = p && c0 + c < E && r0 + j < D
+                                            ? p[sbase + (int64_t)(r0 + j) * rs +
+                                                (int64_t)(c0 + c) * cs]
+                                            : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < RP; ++j) {
+                S01[j] = pack2(S[j].x, S[j].y);
+                S23[j] = pack2(S[j].z, S[j].w);
+            }
+        }
+    }
+
+    token_loop<T, BWD, GATE, ASYNC, SHORTC>(a, sp, n, h, tile, threadIdx.x, blockDim.x, sh, S01,
+                                            S23, CtaSync());
+
     // ---- the state block out --------------------------------------------------
+    float4 S[RP];
 #pragma unroll
     for (int j = 0; j < RP; ++j) {
         const float2 lo = unpack2(S01[j]), hi = unpack2(S23[j]);
@@ -578,6 +643,282 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
                     if (c0 + c < E && r0 + j < D)
                         p[sbase + (int64_t)(r0 + j) * rs + (int64_t)(c0 + c) * cs] = comp(S[j], c);
         }
+    }
+}
+
+// ---- streamed decode ----------------------------------------------------------
+// Forward-type calls of at most SHORT_MAX_T tokens with whole (sequence,
+// head) state blocks contiguous ([D][E] rows, E a multiple of 4) and one
+// column tile: one
+// persistent CTA per SM walks the (sequence, head) blocks.  A copy warp moves
+// each fp32 state block (D E 4 bytes) into a ring of NS shared-memory buffers
+// by one 1-D bulk copy and back out by one bulk store, so that NS - 1 blocks
+// are in flight while the compute warps, which hold only the block they work
+// on, run the tokens.  Waits on the ring are bounded (2 s); on expiry the CTA
+// records LA_ERR_TIMEOUT, drains its copies and returns.
+
+// Longest call that takes the streamed kernel: beyond it one CTA per SM is
+// compute-bound on the token loop and the per-CTA kernel is faster.
+constexpr int STREAM_MAX_T = 4;
+
+__device__ int g_token_error;
+constexpr uint64_t TOK_WAIT_NS = 2000000000ull;
+constexpr int TOK_ERR_TIMEOUT = 4;
+
+__device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes,
+                                             uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1], %2, [%3];" ::"r"(sm100::smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(sm100::smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_store_1d(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(sm100::smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+// every committed bulk store of this thread complete (written)
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Bounded wait: false when the CTA is aborting or this wait ran out.
+__device__ __forceinline__ bool tok_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (sm100::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = sm100::globaltimer_ns();
+    for (;;) {
+        if (sm100::mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (sm100::globaltimer_ns() - t0 > TOK_WAIT_NS) {
+            *abort_flag = 1;
+            atomicExch(&g_token_error, TOK_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// Bounded wait that ignores the abort flag (draining this CTA's own copies).
+__device__ __forceinline__ void tok_drain(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = sm100::globaltimer_ns();
+    while (!sm100::mbar_try_wait(bar, parity))
+        if (sm100::globaltimer_ns() - t0 > TOK_WAIT_NS) {
+            atomicExch(&g_token_error, TOK_ERR_TIMEOUT);
+            return;
+        }
+}
+// AND of `ok` over the first `count` threads (barrier 2)
+__device__ __forceinline__ bool named_and(bool ok, int count)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.u32 q, %1, 0;\n\t"
+                 "bar.red.and.pred p, 2, %2, q;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r)
+                 : "r"(ok ? 1u : 0u), "r"(count)
+                 : "memory");
+    return r != 0;
+}
+
+// Bytes of one raw token slot of the streamed kernel: q, k rows [tbe][D] and
+// value rows [tbe][cw] of the token dtype, row gates [tbe][D] fp32.
+__host__ __device__ inline size_t stream_slot_bytes(const Shape &sp, int D, int tbe, int esz,
+                                                    int gate)
+{
+    return ((size_t)tbe * ((size_t)2 * D * esz + (size_t)sp.cw * esz +
+                           (gate == 1 ? (size_t)D * 4 : 0)) + 15) / 16 * 16;
+}
+// Shared memory of the streamed kernel: NS state buffers, NS raw token slots,
+// 2 NS barriers, the abort word (16 bytes), then the token tables.
+__host__ __device__ inline size_t stream_smem_bytes(const Shape &sp, int D, int E, int tbe,
+                                                    int esz, int gate, int ns)
+{
+    return (size_t)ns * D * E * 4 + (size_t)ns * stream_slot_bytes(sp, D, tbe, esz, gate) +
+           (size_t)2 * ns * 8 + 16 + token_smem_bytes(sp, RP, D, tbe, 4, gate, false);
+}
+
+template <typename T, int GATE>
+__global__ void __launch_bounds__(MAXW * 32 + 32, 1) stream_kernel(SweepArgs a, int ns)
+{
+    const int D = a.D, E = a.E;
+    const Shape sp = token_shape(D, E, RP);   // one column tile
+    const int ncomp = sp.wpc * 32;            // compute threads; the copy warp follows
+    const int heads = a.N * a.H;
+    const int64_t SE = (int64_t)D * E;
+    const uint32_t sbytes = (uint32_t)(SE * 4);
+    const int tbe = token_block(a.max_len);
+    const int esz = (int)sizeof(T);
+    const size_t slot = stream_slot_bytes(sp, D, tbe, esz, GATE);
+    extern __shared__ __align__(128) float sh[];
+    float *sbuf = sh;
+    uint8_t *raw = reinterpret_cast<uint8_t *>(sbuf + ns * SE);
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw + ns * slot);
+    uint64_t *done = full + ns;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(done + ns);
+    float *tok = reinterpret_cast<float *>(done + ns) + 4;
+    const int tid = threadIdx.x;
+    const bool has_in = a.s_in.p != nullptr, has_out = a.s_out.p != nullptr;
+    // raw rows of slot b: q, k [tbe][D], v [tbe][cw], gate [tbe][D]
+    auto slot_q = [&](int b) { return reinterpret_cast<T *>(raw + b * slot); };
+    auto slot_k = [&](int b) { return slot_q(b) + tbe * D; };
+    auto slot_v = [&](int b) { return slot_k(b) + tbe * D; };
+    auto slot_g = [&](int b) { return reinterpret_cast<float *>(slot_v(b) + tbe * sp.cw); };
+    auto seq = [&](int hn, int64_t &row, int64_t &bos, int64_t &len) {
+        const int n = hn / a.H;
+        if (a.cu) {
+            row = 0;
+            bos = a.cu[n];
+            len = (int64_t)a.cu[n + 1] - a.cu[n];
+        } else {
+            row = n;
+            bos = 0;
+            len = a.T;
+        }
+    };
+    if (tid == 0) {
+        for (int i = 0; i < ns; ++i) {
+            sm100::mbar_init(&full[i], 1);
+            sm100::mbar_init(&done[i], 1);
+        }
+        *abort_flag = 0;
+        sm100::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (tid >= ncomp) {
+        // ---- copy warp ----
+        const int lane = tid - ncomp;
+        int li = 0;
+        bool ok = true;
+        for (int hn = blockIdx.x; hn < heads; hn += gridDim.x, ++li) {
+            const int buf = li % ns;
+            if (lane == 0 && li >= ns) {
+                // the block ns heads back has left this buffer: store it
+                ok = tok_wait(&done[buf], ((li - ns) / ns) & 1, abort_flag);
+                if (ok && has_out) {
+                    bulk_store_1d(a.s_out.p + (int64_t)(hn - ns * (int)gridDim.x) * SE,
+                                  sbuf + buf * SE, sbytes);
+                    sm100::bulk_commit_group();
+                    sm100::bulk_wait_read_all();   // before the buffer is refilled
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            int64_t row, bos, len;
+            seq(hn, row, bos, len);
+            const int h = hn % a.H;
+            const uint32_t rowb = (uint32_t)(2 * D * esz + E * esz + (GATE == 1 ? D * 4 : 0));
+            const uint32_t tx = (has_in ? sbytes : 0u) + (uint32_t)len * rowb;
+            if (lane == 0) {
+                if (tx)
+                    sm100::mbar_arrive_expect_tx(&full[buf], tx);
+                else
+                    sm100::mbar_arrive(&full[buf]);
+                if (has_in)
+                    bulk_load_1d(sbuf + buf * SE, a.s_in.p + (int64_t)hn * SE, sbytes, &full[buf]);
+            }
+            __syncwarp();
+            // token rows in processing order (forward-type: reversed when reverse)
+            const int nrow = (int)len * (GATE == 1 ? 4 : 3);
+            for (int i = lane; i < nrow; i += 32) {
+                const int u = i / (GATE == 1 ? 4 : 3), kind = i % (GATE == 1 ? 4 : 3);
+                const int64_t t = bos + (a.reverse ? len - 1 - u : u);
+                if (kind == 0)
+                    bulk_load_1d(slot_q(buf) + u * D,
+                                 reinterpret_cast<const T *>(a.q.p) + row * a.q.sb + t * a.q.st +
+                                     (int64_t)(h / a.q.hdiv) * a.q.sh,
+                                 (uint32_t)(D * esz), &full[buf]);
+                else if (kind == 1)
+                    bulk_load_1d(slot_k(buf) + u * D,
+                                 reinterpret_cast<const T *>(a.k.p) + row * a.k.sb + t * a.k.st +
+                                     (int64_t)(h / a.k.hdiv) * a.k.sh,
+                                 (uint32_t)(D * esz), &full[buf]);
+                else if (kind == 2)
+                    bulk_load_1d(slot_v(buf) + u * sp.cw,
+                                 reinterpret_cast<const T *>(a.v.p) + row * a.v.sb + t * a.v.st +
+                                     (int64_t)(h / a.v.hdiv) * a.v.sh,
+                                 (uint32_t)(E * esz), &full[buf]);
+                else
+                    bulk_load_1d(slot_g(buf) + u * D,
+                                 a.gate.p + row * a.gate.sb + t * a.gate.st +
+                                     (int64_t)h * a.gate.sh,
+                                 (uint32_t)(D * 4), &full[buf]);
+            }
+            __syncwarp();
+        }
+        if (lane != 0)
+            return;
+        const int issued = li;
+        if (ok) {
+            // the last blocks
+            for (int lj = issued > ns ? issued - ns : 0; lj < issued; ++lj) {
+                const int buf = lj % ns;
+                if (!tok_wait(&done[buf], (lj / ns) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (has_out)
+                    bulk_store_1d(a.s_out.p + (int64_t)(blockIdx.x + lj * (int)gridDim.x) * SE,
+                                  sbuf + buf * SE, sbytes);
+            }
+            if (has_out)
+                sm100::bulk_commit_group();
+        }
+        if (!ok) {
+            // no copy into this CTA's shared memory may outlive it
+            for (int lj = issued > ns ? issued - ns : 0; lj < issued; ++lj)
+                tok_drain(&full[lj % ns], (lj / ns) & 1);
+        }
+        bulk_wait_all();
+        return;
+    }
+
+    // ---- compute warps ----
+    const int warp = tid >> 5, lane = tid & 31;
+    const int qd = lane & (sp.qw - 1), rg = lane / sp.qw;
+    const int c0 = warp * sp.wc + 4 * qd;
+    const int r0 = RP * rg;
+    int li = 0;
+    for (int hn = blockIdx.x; hn < heads; hn += gridDim.x, ++li) {
+        const int buf = li % ns;
+        float *sb = sbuf + buf * SE;
+        if (!named_and(tok_wait(&full[buf], (li / ns) & 1, abort_flag), ncomp))
+            break;
+        f2 S01[RP], S23[RP];
+#pragma unroll
+        for (int j = 0; j < RP; ++j) {
+            ulonglong2 x = make_ulonglong2(0ull, 0ull);
+            if (has_in && c0 < E && r0 + j < D)
+                x = *reinterpret_cast<const ulonglong2 *>(sb + (int64_t)(r0 + j) * E + c0);
+            S01[j] = x.x;
+            S23[j] = x.y;
+        }
+        RawRows pre;
+        pre.q = slot_q(buf);
+        pre.k = slot_k(buf);
+        pre.v = slot_v(buf);
+        pre.g = slot_g(buf);
+        token_loop<T, false, GATE, false, true>(a, sp, hn / a.H, hn % a.H, 0, tid, ncomp, tok, S01,
+                                               S23, NamedSync{ncomp}, pre);
+        if (has_out && c0 < E) {
+#pragma unroll
+            for (int j = 0; j < RP; ++j)
+                if (r0 + j < D)
+                    *reinterpret_cast<ulonglong2 *>(sb + (int64_t)(r0 + j) * E + c0) =
+                        make_ulonglong2(S01[j], S23[j]);
+        }
+        sm100::fence_proxy_async_smem();   // the writes, visible to the bulk store
+        NamedSync{ncomp}();
+        if (tid == 0)
+            sm100::mbar_arrive(&done[buf]);
     }
 }
 
@@ -642,10 +983,57 @@ cudaError_t launch_rows(const SweepArgs &a, cudaStream_t s)
                                            : launch_gate<T, BWD, false, SHORTC>(a, s);
 }
 
+// The streamed decode kernel when the call qualifies (forward-type, short,
+// no gate or a row gate, contiguous 16-byte aligned state blocks, one column
+// tile, at least two ring buffers in shared memory, more blocks than SMs);
+// cudaErrorNotSupported otherwise.
+template <typename T> cudaError_t try_stream(const SweepArgs &a, cudaStream_t s)
+{
+    const Shape sp = token_shape(a.D, a.E, RP);
+    auto state_ok = [&](const float *p, int64_t rs, int64_t cs) {
+        return !p || ((reinterpret_cast<uintptr_t>(p) & 15) == 0 && rs == a.E && cs == 1);
+    };
+    const int esz = (int)sizeof(T);
+    if (a.max_len > STREAM_MAX_T || a.gate.cols || sp.tiles != 1 || a.E % 4 ||
+        !state_ok(a.s_in.p, a.s_in.rs, a.s_in.cs) || !state_ok(a.s_out.p, a.s_out.rs, a.s_out.cs) ||
+        !rows_aligned(a, esz))
+        return cudaErrorNotSupported;
+    int dev = 0, sms = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t heads = (int64_t)a.N * a.H;
+    if (heads < 2 * (int64_t)sms || heads > 0x7fffffff)
+        return cudaErrorNotSupported;
+    const int gate = a.gate.p ? 1 : 0, tbe = token_block(a.max_len);
+    int ns = 3;
+    while (ns >= 2 && stream_smem_bytes(sp, a.D, a.E, tbe, esz, gate, ns) > (size_t)optin)
+        --ns;
+    if (ns < 2)
+        return cudaErrorNotSupported;
+    const size_t smem = stream_smem_bytes(sp, a.D, a.E, tbe, esz, gate, ns);
+    auto kernel = gate ? stream_kernel<T, 1> : stream_kernel<T, 0>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    kernel<<<(unsigned)sms, sp.wpc * 32 + 32, smem, s>>>(a, ns);
+    note_launch();
+    return cudaGetLastError();
+}
+
 template <bool BWD> cudaError_t launch_token(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0 || a.H == 0)
         return cudaSuccess;
+    if (!BWD && a.D >= 1 && a.D <= 256 && a.E >= 1) {
+        const cudaError_t e = a.bf16 ? try_stream<__nv_bfloat16>(a, s) : try_stream<float>(a, s);
+        if (e != cudaErrorNotSupported)
+            return e;
+    }
     if (a.D < 1 || a.D > 256 || a.E < 1)
         return cudaErrorNotSupported;
     if ((int64_t)a.N * a.H * token_shape(a.D, a.E, 16).tiles > 0x7fffffff)
@@ -667,6 +1055,19 @@ cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s)
 cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s)
 {
     return launch_token<true>(a, s);
+}
+
+cudaError_t token_read_and_clear_error(cudaStream_t s, int *err)
+{
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(err, g_token_error, sizeof(int), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_token_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                    s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    return e;
 }
 
 }  // namespace la

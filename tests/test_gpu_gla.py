@@ -92,3 +92,21 @@ def test_gate_of_zero_equals_the_ungated_path():
     # path runs in fp32: both meet the bf16 parity bound against the oracle
     assert (o1.float() - o2.float()).abs().max() <= 2e-2 * o2.float().abs().max()
     assert (f1 - f2).abs().max() <= 2e-2 * f2.abs().max()
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_gated_decode_streamed(T):
+    # 20 x 16 = 320 (sequence, head) blocks of at most 4 tokens: the gated
+    # forward takes the streamed decode kernel (row gate)
+    assert torch.cuda.get_device_properties(0).multi_processor_count <= 160
+    x = _inputs(20, T, 16, 128, 128, torch.bfloat16, seed=40 + T)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    for reverse in (False, True):
+        o, fin = la.gla_fwd(d["q"], d["k"], d["v"], d["g"], d["g_gamma"], d["scale"],
+                            d["initial_state"], reverse)
+        torch.cuda.synchronize()
+        la.get_device_error()
+        ro, rf = oracle.gla_forward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"], x["scale"],
+                                    x["initial_state"], reverse)
+        compare(dict(o=o.cpu(), final_state=fin.cpu()), dict(o=ro, final_state=rf),
+                TOL[torch.bfloat16], label="gated streamed T=%d rev=%d" % (T, reverse))

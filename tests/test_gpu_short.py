@@ -83,3 +83,40 @@ def test_decoding_piece_by_piece_equals_one_call():
             label="decoded")
     compare(dict(o=o_all.cpu(), final_state=s_all.cpu()), ref, TOL[torch.bfloat16],
             label="one call")
+
+
+# At least twice as many (sequence, head) blocks as the GPU has SMs: calls of
+# at most 4 tokens take the streamed decode kernel (state blocks moved through
+# shared memory by bulk copies), 16 tokens the per-CTA kernel.  20 x 16 = 320
+# blocks covers GPUs of up to 160 SMs.
+@pytest.mark.parametrize("T", [1, 4, 16])
+@pytest.mark.parametrize("dtype,D,E", [(torch.bfloat16, 128, 128), (torch.float32, 64, 64),
+                                       (torch.bfloat16, 32, 96), (torch.bfloat16, 48, 80)])
+@pytest.mark.parametrize("init", [0.3, 0.0])
+def test_streamed_decode_matches_oracle(T, dtype, D, E, init):
+    assert torch.cuda.get_device_properties(0).multi_processor_count <= 160
+    w = _w(20, T, 16, D, E, dtype, init=init, dfin=0.0)
+    x = W.make_inputs(w, seed=300 + T + D)
+    for reverse in (False, True):
+        compare(gpu_run(x, reverse, backward=False), oracle_run(x, reverse, backward=False),
+                TOL[dtype], label="streamed T=%d D=%d E=%d init=%g rev=%d" % (T, D, E, init,
+                                                                                 reverse))
+
+
+def test_streamed_decode_packed_and_in_place():
+    # 330 packed sequences of 0..4 tokens (the streamed kernel); the state
+    # updated in place (initial and final state the same buffer)
+    gen = torch.Generator().manual_seed(5)
+    lens = torch.randint(0, 5, (330,), generator=gen).tolist()
+    w = _w(1, 0, 2, 128, 128, torch.bfloat16, seqlens=lens, init=0.2, dfin=0.0)
+    x = W.make_inputs(w, seed=12)
+    ref = oracle_run(x, backward=False)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    state = d["initial_state"].clone()
+    o, fin = la.la_fwd(d["q"], d["k"], d["v"], d["g_gamma"], w.scale, state,
+                       cu_seqlens=x["cu_seqlens"], final_state=state)
+    torch.cuda.synchronize()
+    la.get_device_error()
+    assert fin.data_ptr() == state.data_ptr()
+    compare(dict(o=o.cpu(), final_state=fin.cpu()), ref, TOL[torch.bfloat16],
+            cu=x["cu_seqlens"], label="streamed packed in place")
