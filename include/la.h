@@ -253,16 +253,35 @@ la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens);
  *   g          [B,T,H,D] fp32 gate, channel-contiguous, element strides
  *              g_strides[3] = (batch, token, head)
  *   g_gamma    [H] fp32, required (zeros for no head decay)
- *   everything else as la_fwd; kv_heads must be 0 (or H); no workspace.
- * Runs the token-by-token kernels at any length.  Not differentiated:
- * g_gamma, scale, reverse, cu_seqlens. */
+ *   workspace  256-byte aligned device scratch of at least
+ *              la_gla_fwd_workspace_size bytes, or NULL
+ *   everything else as la_fwd; kv_heads must be 0 (or H).
+ * With the workspace, bf16 calls with D = 128, E in {64, 128} and sequences
+ * longer than 16 tokens run the chunked form on the tensor cores: per chunk
+ * of 128 tokens the gate's running sums b are split around a reference r
+ * (the middle of their range, raised to -72 if lower), q and k are rescaled
+ * by exp(b - r) and exp(r - b) into the workspace, and the chunked sweep runs
+ * on them.  Every (sequence, head) with a chunk where some |b - r| or r
+ * exceeds 72 (gates stronger than the factors' bf16 range allows: a chunk's
+ * total log-decay below about -144) runs the token-by-token kernels instead,
+ * decided on the device.  All other calls, and calls without the
+ * workspace, run the token-by-token kernels.  Not differentiated: g_gamma,
+ * scale, reverse, cu_seqlens. */
 la_status la_gla_fwd(const la_dims *dims, int32_t dtype,
                      const void *q, const void *k, const void *v,
                      const float *g, const int64_t *g_strides,
                      const float *g_gamma, float scale,
                      const float *initial_state, int32_t reverse,
                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                     void *o, float *final_state, void *stream);
+                     void *o, float *final_state, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace with which la_gla_fwd runs the chunked form for these
+ * sizes (q~, k~ as bf16 [rows][T][H][D] each, two fp32 vectors per chunk and
+ * (sequence, head), one flag per (sequence, head)); 0 when the chunked form
+ * does not apply.  cu_seqlens_host as la_workspace_size_for.  Host only. */
+size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
+                                 const int32_t *cu_seqlens_host);
 
 /* Backward of la_gla_fwd: dq, dk, dv, d_initial_state as la_bwd, and
  * dg [B,T,H,D] fp32 (g_strides), the gradient of the gate:

@@ -308,9 +308,13 @@ def _strides3(t):
 
 def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
             scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
-            reverse: bool = False, cu_seqlens=None) -> Tuple[Tensor, Tensor]:
+            reverse: bool = False, cu_seqlens=None, chunked: bool = True
+            ) -> Tuple[Tensor, Tensor]:
     """Gated forward (GLA): row a of the state decays by exp(g_gamma[h] + g_t[a]) at
-    token t.  q, k, g: [B,T,H,D]; v: [B,T,H,E].  Returns (o, final_state)."""
+    token t.  q, k, g: [B,T,H,D]; v: [B,T,H,E].  Returns (o, final_state).
+    chunked=False withholds the workspace, so that every (sequence, head) runs
+    token by token (otherwise the chunked tensor-core form runs where it
+    applies)."""
     _check_tokens(q, k, v)
     if k.shape[2] != q.shape[2]:
         raise ValueError("the gated form needs keys and values with the queries' heads")
@@ -329,10 +333,13 @@ def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
     fin = torch.empty((Nst, H, D, E), device=dev, dtype=torch.float32)
     dims = _dims(q, k, v, out, packed)
     gs = _strides3(g)
+    nbytes = (int(N.lib().la_gla_fwd_workspace_size(ctypes.byref(dims), _dtype_code(q),
+                                                    packed.host_ptr())) if chunked else 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
     st = N.lib().la_gla_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                             _ptr(g), gs, _ptr(gg), scale, _ptr(init), int(bool(reverse)),
                             _ptr(packed.dev), packed.host_ptr(), _ptr(out), _ptr(fin),
-                            _stream(dev))
+                            _ptr(ws), nbytes, _stream(dev))
     N.check(st)
     return out, fin
 

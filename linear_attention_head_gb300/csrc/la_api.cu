@@ -861,6 +861,33 @@ int64_t gla_max_len(const Problem &P)
     return m;
 }
 
+// Workspace of the chunked gated forward: q~, k~ (bf16, dense [rows][T][H][D]),
+// exp(r) and exp(B - r) per chunk ([N][H][ncmax][D] fp32), one flag per
+// (sequence, head).  0 when the chunked form does not apply to these sizes.
+struct GlaFwdWs {
+    size_t xq, yk, er, u, flags, total;
+    int64_t ncmax;
+};
+GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype)
+{
+    GlaFwdWs w{};
+    const int64_t maxlen = gla_max_len(P);
+    if (dtype != LA_DTYPE_BF16 || P.D != 128 || (P.E != 64 && P.E != 128) ||
+        maxlen <= la::SHORT_MAX_T || P.N > 65535 || P.H > 65535)
+        return w;
+    w.ncmax = (maxlen + 127) / 128;
+    const int64_t rows = P.packed ? 1 : P.B;
+    const size_t tok = round256((size_t)rows * P.T * P.H * P.D * 2);
+    const size_t vec = round256((size_t)P.N * P.H * w.ncmax * P.D * 4);
+    w.xq = 0;
+    w.yk = tok;
+    w.er = 2 * tok;
+    w.u = 2 * tok + vec;
+    w.flags = 2 * tok + 2 * vec;
+    w.total = w.flags + round256((size_t)P.N * P.H * 4);
+    return w;
+}
+
 // Workspace of la_gla_bwd: the final state transposed, then the block sums.
 size_t gla_bwd_bytes(const Problem &P)
 {
@@ -872,11 +899,22 @@ size_t gla_bwd_bytes(const Problem &P)
 
 extern "C" {
 
+size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
+                                 const int32_t *cu_seqlens_host)
+{
+    Problem P;
+    std::string keep = g_msg;
+    la_status st = check_dims(dims, dtype, cu_seqlens_host, cu_seqlens_host, nullptr, &P);
+    g_msg = keep;
+    return st == LA_OK ? gla_fwd_layout(P, dtype).total : 0;
+}
+
 la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
                      const void *v, const float *g, const int64_t *g_strides,
                      const float *g_gamma, float scale, const float *initial_state,
                      int32_t reverse, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
-                     void *o, float *final_state, void *stream)
+                     void *o, float *final_state, void *workspace, size_t workspace_bytes,
+                     void *stream)
 {
     g_msg.clear();
     cudaStream_t s = (cudaStream_t)stream;
@@ -901,6 +939,61 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.s_in = la::StateIn{initial_state, P.E, 1};
     a.s_out = la::StateOut{final_state, P.E, 1};
     a.gate = gate_of(g, g_strides, false);   // state rows are key channels
+    const GlaFwdWs w = gla_fwd_layout(P, dtype);
+    // the operands are prepared two channels at a time: 8-byte gate pairs
+    const bool gate_pairs = (reinterpret_cast<uintptr_t>(g) & 7) == 0 && g_strides[0] % 2 == 0 &&
+                            g_strides[1] % 2 == 0 && g_strides[2] % 2 == 0;
+    if (w.total && workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) == 0 &&
+        workspace_bytes >= w.total && gate_pairs && la::tc_sweep_supported(a)) {
+        // the chunked form on the tensor cores, for every (sequence, head)
+        // whose gates stay in its range; the others token by token
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        int *flags = reinterpret_cast<int *>(ws + w.flags);
+        cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)P.N * P.H * 4, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "gated forward flags");
+        la::GlaPrepArgs pa{};
+        pa.N = P.N;
+        pa.H = P.H;
+        pa.D = P.D;
+        pa.T = P.T;
+        pa.ncmax = w.ncmax;
+        pa.cu = cu_seqlens;
+        pa.reverse = reverse ? 1 : 0;
+        pa.bf16 = 1;
+        pa.q = q;
+        pa.k = k;
+        pa.sb = dims->qk_strides[0];
+        pa.st = dims->qk_strides[1];
+        pa.sh = dims->qk_strides[2];
+        pa.g = g;
+        pa.gsb = g_strides[0];
+        pa.gst = g_strides[1];
+        pa.gsh = g_strides[2];
+        pa.g_gamma = g_gamma;
+        pa.xq = ws + w.xq;
+        pa.yk = ws + w.yk;
+        pa.er = reinterpret_cast<float *>(ws + w.er);
+        pa.u = reinterpret_cast<float *>(ws + w.u);
+        pa.flags = flags;
+        pa.lim = 72.f;
+        if ((e = la::gla_prepare(pa, s)) != cudaSuccess)
+            return cuda_fail(e, "gated forward operands");
+        la::SweepArgs t = a;
+        t.gate = la::Gate{};
+        t.gla_er = pa.er;
+        t.gla_u = pa.u;
+        t.gla_ncmax = w.ncmax;
+        t.gla_flags = flags;
+        t.gla_flag_run = 0;
+        e = la::tc_gla_forward_sweep(t, pa.xq, pa.yk, s);
+        if (e == cudaSuccess) {
+            a.gla_flags = flags;
+            a.gla_flag_run = 1;
+        } else if (e != cudaErrorNotSupported) {
+            return cuda_fail(e, "gated tensor-core sweep launch");
+        }
+    }
     return short_run(a, false, s);
 }
 

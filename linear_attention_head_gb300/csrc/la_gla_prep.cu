@@ -1,0 +1,208 @@
+// la_gla_prep.cu -- operands of the chunked tensor-core form of the gated
+// recurrence (the per-key gate of ejkernel `recurrent`, GLA-style).
+//
+// With a gate, token t decays state row a by exp(l_t[a]), l_t = g_gamma[h] +
+// g_t[a].  Inside a chunk of up to 128 tokens, in processing order, let b_t be
+// the running sum of l over the chunk's tokens up to and including t, B the
+// sum over the whole chunk, and S the state entering the chunk.  Then
+//     o_t  = s [ (q_t exp(b_t)) . S  +  sum_{u <= t} (q_t exp(b_t - b_u) . k_u) v_u ]
+//     S'   = diag(exp(B)) S + sum_u (k_u exp(B - b_u))^T v_u
+// (products per key channel).  With a reference r (the middle of the range of
+// b over the chunk, raised to -LIM if lower), every factor splits into two
+// that stay within exp(+-LIM) when all |b_t - r| <= LIM and |r| <= LIM:
+//     q~_t = q_t exp(b_t - r),   k~_u = k_u exp(r - b_u),
+//     o_t  = s [ q~_t . (diag(exp(r)) S) + sum_{u <= t} (q~_t . k~_u) v_u ]
+//     S'   = diag(exp(B - r)) [ diag(exp(r)) S + sum_u k~_u^T v_u ]
+// so the tensor-core sweep runs on q~, k~ with a plain causal mask and scales
+// state rows by exp(r) and exp(B - r).  This kernel writes q~, k~ (bf16, dense
+// [rows][T][H][D]), exp(r) and exp(B - r) per chunk, and flags every
+// (sequence, head) with a chunk outside the range; those run the token-by-
+// token kernels instead.  Chunks are cut from the start of each sequence, as
+// the sweep cuts them, in either direction.
+
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int PC = 128;   // tokens per chunk (the tensor-core sweep's chunk)
+
+template <typename T> __device__ __forceinline__ float ldt(const T *p);
+template <> __device__ __forceinline__ float ldt<float>(const float *p) { return *p; }
+template <> __device__ __forceinline__ float ldt<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    return __bfloat162float(*p);
+}
+
+template <typename T> struct Pair;
+template <> struct Pair<float> {
+    static __device__ __forceinline__ float2 load(const float *p)
+    {
+        return *reinterpret_cast<const float2 *>(p);
+    }
+};
+template <> struct Pair<__nv_bfloat16> {
+    static __device__ __forceinline__ float2 load(const __nv_bfloat16 *p)
+    {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    }
+};
+
+// One CTA per (chunk position, head, sequence); thread (channel pair cp,
+// group grp) takes channels 2 cp, 2 cp + 1 over the chunk's processing
+// indices PT grp .. PT grp + PT - 1.  Its gates are read once, all in flight
+// together, and their running sums stay in registers; the groups' totals are
+// combined through shared memory.  The factors exp(b - r), exp(r - b) use the
+// fast exponential: they are rounded to bf16 with their operands anyway.
+constexpr int PG = 4, PT = PC / PG;   // token groups per chunk, tokens per group
+template <typename T> __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
+{
+    const int pc = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int cp = threadIdx.x & 63, grp = threadIdx.x >> 6, c = 2 * cp;
+    int64_t row, bos, len;
+    if (a.cu) {
+        row = 0;
+        bos = a.cu[n];
+        len = (int64_t)a.cu[n + 1] - a.cu[n];
+    } else {
+        row = n;
+        bos = 0;
+        len = a.T;
+    }
+    const int64_t t0 = (int64_t)pc * PC;
+    if (t0 >= len)
+        return;
+    const int Lc = (int)(len - t0 < PC ? len - t0 : PC);
+    const int p0 = PT * grp;
+    const int np = Lc - p0 < 0 ? 0 : (Lc - p0 < PT ? Lc - p0 : PT);   // this group's tokens
+    const float gh = a.g_gamma[h];
+    // token of processing index p0 + j: tb + j ts
+    const int64_t tb = bos + t0 + (np == 0 ? 0 : (a.reverse ? Lc - 1 - p0 : p0));
+    const int64_t ts = a.reverse ? -1 : 1;
+
+    // pass 1: this group's gates and their running sums (constant past its end)
+    float2 b[PT];
+    {
+        const float *gp = a.g + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
+        const int64_t gstep = ts * a.gst;
+#pragma unroll
+        for (int j = 0; j < PT; ++j) {
+            b[j] = make_float2(0.f, 0.f);
+            if (j < np) {
+                const float2 x = *reinterpret_cast<const float2 *>(gp + j * gstep);
+                b[j] = make_float2(gh + x.x, gh + x.y);
+            }
+        }
+    }
+    float2 lo = make_float2(INFINITY, INFINITY), hi = make_float2(-INFINITY, -INFINITY);
+#pragma unroll
+    for (int j = 0; j < PT; ++j) {
+        if (j > 0) {
+            b[j].x += b[j - 1].x;
+            b[j].y += b[j - 1].y;
+        }
+        if (j < np) {
+            lo = make_float2(fminf(lo.x, b[j].x), fminf(lo.y, b[j].y));
+            hi = make_float2(fmaxf(hi.x, b[j].x), fmaxf(hi.y, b[j].y));
+        }
+    }
+    __shared__ float2 tot[PG][64], los[PG][64], his[PG][64];
+    tot[grp][cp] = b[PT - 1];
+    __syncthreads();
+    float2 off = make_float2(0.f, 0.f), B = off;   // the sums entering this group; the totals
+#pragma unroll
+    for (int k = 0; k < PG; ++k) {
+        const float2 x = tot[k][cp];
+        if (k < grp) {
+            off.x += x.x;
+            off.y += x.y;
+        }
+        B.x += x.x;
+        B.y += x.y;
+    }
+    los[grp][cp] = make_float2(lo.x + off.x, lo.y + off.y);
+    his[grp][cp] = make_float2(hi.x + off.x, hi.y + off.y);
+    __syncthreads();
+    float2 LO = los[0][cp], HI = his[0][cp];
+#pragma unroll
+    for (int k = 1; k < PG; ++k) {
+        LO = make_float2(fminf(LO.x, los[k][cp].x), fminf(LO.y, los[k][cp].y));
+        HI = make_float2(fmaxf(HI.x, his[k][cp].x), fmaxf(HI.y, his[k][cp].y));
+    }
+    const float2 r = make_float2(fmaxf(0.5f * (LO.x + HI.x), -a.lim),
+                                 fmaxf(0.5f * (LO.y + HI.y), -a.lim));
+    const bool okx = HI.x - r.x <= a.lim && r.x - LO.x <= a.lim && r.x <= a.lim;
+    const bool oky = HI.y - r.y <= a.lim && r.y - LO.y <= a.lim && r.y <= a.lim;
+    if (grp == 0) {
+        if (!(okx && oky))
+            atomicOr(a.flags + (int64_t)n * a.H + h, 1);
+        const int64_t vi = (((int64_t)n * a.H + h) * a.ncmax + pc) * a.D + c;
+        *reinterpret_cast<float2 *>(a.er + vi) =
+            make_float2(okx ? expf(r.x) : 0.f, oky ? expf(r.y) : 0.f);
+        *reinterpret_cast<float2 *>(a.u + vi) =
+            make_float2(okx ? expf(B.x - r.x) : 0.f, oky ? expf(B.y - r.y) : 0.f);
+    }
+
+    // pass 2: q~ = q exp(b - r), k~ = k exp(r - b); zeros when out of range
+    const T *qp = static_cast<const T *>(a.q) + row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
+    const T *kp = static_cast<const T *>(a.k) + row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
+    const int64_t dst = (int64_t)a.H * a.D;   // token stride of the dense outputs
+    __nv_bfloat162 *xq = reinterpret_cast<__nv_bfloat162 *>(
+        static_cast<__nv_bfloat16 *>(a.xq) + ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst);
+    __nv_bfloat162 *yk = reinterpret_cast<__nv_bfloat162 *>(
+        static_cast<__nv_bfloat16 *>(a.yk) + ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst);
+    const int64_t istep = ts * a.st, ostep = ts * dst / 2;
+    const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
+    // eight tokens' q, k pairs loaded together (indices clamped into the
+    // group), then scaled and stored
+    constexpr int PB = 8;
+#pragma unroll
+    for (int j0 = 0; j0 < PT; j0 += PB) {
+        float2 qv[PB], kv[PB];
+#pragma unroll
+        for (int jj = 0; jj < PB; ++jj) {
+            const int j = j0 + jj;
+            const int jl = j < np ? j : (np > 0 ? np - 1 : 0);
+            qv[jj] = Pair<T>::load(qp + jl * istep);
+            kv[jj] = Pair<T>::load(kp + jl * istep);
+        }
+#pragma unroll
+        for (int jj = 0; jj < PB; ++jj) {
+            const int j = j0 + jj;
+            if (j < np) {
+                const float ex = b[j].x + sh0.x, ey = b[j].y + sh0.y;   // b - r
+                const float2 x = make_float2(okx ? qv[jj].x * __expf(ex) : 0.f,
+                                             oky ? qv[jj].y * __expf(ey) : 0.f);
+                const float2 y = make_float2(okx ? kv[jj].x * __expf(-ex) : 0.f,
+                                             oky ? kv[jj].y * __expf(-ey) : 0.f);
+                xq[j * ostep] = __float22bfloat162_rn(x);
+                yk[j * ostep] = __float22bfloat162_rn(y);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s)
+{
+    if (a.N == 0 || a.H == 0 || a.ncmax == 0)
+        return cudaSuccess;
+    if (a.D != 128 || a.N > 65535 || a.H > 65535 || a.ncmax > 0x7fffffff)
+        return cudaErrorNotSupported;
+    dim3 grid((unsigned)a.ncmax, (unsigned)a.H, (unsigned)a.N);
+    const int threads = PG * 64;
+    if (a.bf16)
+        gla_prep_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(a);
+    else
+        gla_prep_kernel<float><<<grid, threads, 0, s>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -74,7 +74,39 @@ struct SweepArgs {
     int64_t max_len;          // longest sequence (T when dense)
     Gate gate;                // per-key log-decay gate, or p == nullptr
     int64_t prefetch_ctas = 0;  // token-by-token kernels: L2 prefetch distance in CTAs
+    // gated form on the tensor cores (la_gla_prep.cu): per chunk position and
+    // state row, exp(r) and exp(B - r), [N][H][gla_ncmax][D]
+    const float *gla_er = nullptr, *gla_u = nullptr;
+    int64_t gla_ncmax = 0;
+    // a CTA of (sequence n, head h) runs only if gla_flags is null or
+    // gla_flags[n H + h] == gla_flag_run (1: gates out of the chunked form's
+    // range, run token by token)
+    const int *gla_flags = nullptr;
+    int gla_flag_run = 0;
 };
+
+// Operands of the chunked gated forward (la_gla_prep.cu).
+struct GlaPrepArgs {
+    int N, H, D, T;
+    int64_t ncmax;            // chunks of the longest sequence
+    const int32_t *cu;        // packed sequences, or nullptr
+    int reverse, bf16;
+    const void *q, *k;        // token dtype, element strides sb, st, sh (shared)
+    int64_t sb, st, sh;
+    const float *g;           // gate, strides gsb, gst, gsh
+    int64_t gsb, gst, gsh;
+    const float *g_gamma;
+    void *xq, *yk;            // bf16 [rows][T][H][D]: q~ and k~
+    float *er, *u;            // [N][H][ncmax][D]
+    int *flags;               // [N H], zeroed beforehand
+    float lim;                // largest |b - r| (and |r|) the chunked form takes
+};
+cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s);
+// Tensor-core forward of the gated form on the operands gla_prepare wrote
+// (xq, yk dense [rows][T][H][D] bf16); a.gla_* set.  cudaErrorNotSupported
+// when the tensor maps cannot be built.
+cudaError_t tc_gla_forward_sweep(const SweepArgs &a, const void *xq, const void *yk,
+                                 cudaStream_t s);
 
 // Calls whose longest sequence has at most this many tokens run the
 // token-by-token kernels (la_token.cu) instead of the chunked ones.

@@ -192,9 +192,10 @@ __device__ __forceinline__ void store_half_row_sw128(uint8_t *row_base, int row,
 }
 
 // Initial state row i, 8 columns at a time (once per CTA): fp32 from global
-// (any strides) -> bf16 into the swizzled S copy, and times g0 into TMEM.
+// (any strides) -> times c0 as bf16 into the swizzled S copy, and times g0
+// into TMEM.
 __device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i, int E_,
-                                         uint8_t *sbf, uint32_t tmem_row, float g0)
+                                         uint8_t *sbf, uint32_t tmem_row, float g0, float c0)
 {
 #pragma unroll 1
     for (int p8 = 0; p8 < E_ / 8; ++p8) {
@@ -204,8 +205,8 @@ __device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i
         for (int k = 0; k < 8; ++k)
             x[k] = src ? src[k * sin.cs] : 0.f;
         *reinterpret_cast<uint4 *>(sbf + (p8 >> 3) * (TC_D * 128) + (((p8 & 7) ^ (i & 7)) << 4)) =
-            make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                       pack_bf16x2(x[6], x[7]));
+            make_uint4(pack_bf16x2(c0 * x[0], c0 * x[1]), pack_bf16x2(c0 * x[2], c0 * x[3]),
+                       pack_bf16x2(c0 * x[4], c0 * x[5]), pack_bf16x2(c0 * x[6], c0 * x[7]));
         uint32_t r[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -275,7 +276,47 @@ __device__ __forceinline__ void p_block_full(uint32_t (&r)[32], int kind, float 
     }
 }
 
-template <int E, bool BWD>
+// The gated form's P block: the decay is inside the operands, so P is the
+// scaled scores under the causal mask alone.  Masked scores may be infinite
+// (the operands' factors are only bounded on the causal side), so they are
+// replaced, never multiplied.  kind: 0 masked block, 1 visible, 2 diagonal.
+__device__ __forceinline__ void p_block_gated(uint32_t (&r)[32], int kind, float scale, bool flip,
+                                              int lane)
+{
+    if (kind == 0) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+            r[2 * m] = 0u;
+    } else {
+        const float2 ss = make_float2(scale, scale);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            float2 v = mul_f32x2(
+                make_float2(__uint_as_float(r[2 * m]), __uint_as_float(r[2 * m + 1])), ss);
+            if (kind == 2) {
+                const int j0 = 2 * m, j1 = 2 * m + 1;
+                if (flip ? j0 < lane : j0 > lane)
+                    v.x = 0.f;
+                if (flip ? j1 < lane : j1 > lane)
+                    v.y = 0.f;
+            }
+            r[2 * m] = pack_bf16x2(v.x, v.y);
+        }
+    }
+}
+
+// One 128-byte row of a tile set to zero.
+__device__ __forceinline__ void zero_row(uint8_t *row_base)
+{
+#pragma unroll
+    for (int c16 = 0; c16 < 8; ++c16)
+        *reinterpret_cast<uint4 *>(row_base + (c16 << 4)) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// GLA: the gated forward on the operands of la_gla_prep.cu (X = q~, Y = k~):
+// plain causal P, no column factor on Y, state rows scaled per chunk by
+// exp(B - r) and the next chunk's exp(r), the inter term scaled by s alone.
+template <int E, bool BWD, bool GLA>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_constant__ TcParams P)
 {
     using L = TcLayout<E>;
@@ -319,6 +360,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         bos = 0;
         len = a.T;
     }
+    // gated form: (sequence, head) pairs whose gates are out of range run
+    // token by token instead
+    if (GLA && a.gla_flags && a.gla_flags[(int64_t)n * a.H + h] != a.gla_flag_run)
+        return;
     const int nc = (int)((len + TC_C - 1) / TC_C);
     const bool rev = a.reverse != 0;
     const bool flip = rev != BWD;   // chunk order and mask direction
@@ -510,12 +555,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 tmem_ld32_issue(col, ra);
                 tmem_ld32_issue(col + 32, rb);
                 tmem_wait_ld(ra, rb);
-                const float rf0 =
-                    k0 == 1 ? scale * pw[flip ? 32 * (b0 - q) - lane : 32 * (q - b0) + lane - 31] : 0.f;
-                const float rf1 =
-                    k1 == 1 ? scale * pw[flip ? 32 * (b1 - q) - lane : 32 * (q - b1) + lane - 31] : 0.f;
-                p_block_full(ra, k0, rf0, cf, dt, lane);
-                p_block_full(rb, k1, rf1, cf, dt, lane);
+                if (GLA) {
+                    p_block_gated(ra, k0, scale, flip, lane);
+                    p_block_gated(rb, k1, scale, flip, lane);
+                } else {
+                    const float rf0 =
+                        k0 == 1 ? scale * pw[flip ? 32 * (b0 - q) - lane : 32 * (q - b0) + lane - 31]
+                                : 0.f;
+                    const float rf1 =
+                        k1 == 1 ? scale * pw[flip ? 32 * (b1 - q) - lane : 32 * (q - b1) + lane - 31]
+                                : 0.f;
+                    p_block_full(ra, k0, rf0, cf, dt, lane);
+                    p_block_full(rb, k1, rf1, cf, dt, lane);
+                }
                 if (Lc < TC_C) {
                     // the sequence ends inside this chunk: rows past the end
                     // (forward order) or keys past it (reverse order) are zero
@@ -539,7 +591,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 tmem_st16_even_issue(col, ra);
                 tmem_st16_even_issue(col + 16, rb);
                 tmem_wait_st();
-                {
+                if (GLA) {
+                    // Y carries its factors already; rows past the sequence's
+                    // end (the next packed sequence's, or zero fill) are cleared
+                    if (i >= Lc)
+                        zero_row(sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128);
+                } else {
                     // column factor for the state update, applied to row i of Y
                     float lc = 0.f;
                     if (i < Lc) {
@@ -559,19 +616,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             uint8_t *sbf = sm + L::SOFF + i * 128;
             // initial state: bf16 copy and gamma^L0-scaled fp32 in TMEM (an
             // empty sequence passes it straight to the final state)
-            if (nc == 0)
+            // gated form: row factors of chunk position pc, [N][H][ncmax][D]
+            const int64_t vrow = ((int64_t)n * a.H + h) * a.gla_ncmax;
+            auto vidx = [&](int pc) { return (vrow + pc) * TC_D + i; };
+            if (nc == 0) {
                 state_copy(a.s_in, a.s_out, sb, i, E);
-            else
-                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, pw[chunk_len(0)]);
+            } else if (GLA) {
+                const float e0 = a.gla_er[vidx(flip ? nc - 1 : 0)];
+                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, e0, e0);
+            } else {
+                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, pw[chunk_len(0)], 1.f);
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(s_ready);
             for (int c = 0; c < nc; ++c) {
+                const bool last = c + 1 == nc;
+                // out = fo x (last chunk); else the copy and TMEM get ft x
+                // (gated form) or x and gn x
+                float fo = 1.f, ft = last ? 1.f : pw[chunk_len(c + 1)];
+                if (GLA) {
+                    fo = a.gla_u[vidx(flip ? nc - 1 - c : c)];
+                    if (!last)
+                        ft = fo * a.gla_er[vidx(flip ? nc - 2 - c : c + 1)];
+                }
                 if (!warp_all(bwait(ds_full, c & 1, abort_flag)))
                     break;
                 tc_fence_after();
-                const bool last = c + 1 == nc;
-                const float gn = last ? 1.f : pw[chunk_len(c + 1)];
+                const float gn = ft;
 #pragma unroll 1
                 for (int eb = 0; eb < E / 64; ++eb) {
                     uint32_t ra[32], rb[32];
@@ -583,18 +655,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                             float *dst = a.s_out.p + sb + i * a.s_out.rs + 64 * eb * a.s_out.cs;
 #pragma unroll
                             for (int k = 0; k < 32; ++k) {
-                                dst[k * a.s_out.cs] = __uint_as_float(ra[k]);
-                                dst[(k + 32) * a.s_out.cs] = __uint_as_float(rb[k]);
+                                dst[k * a.s_out.cs] = fo * __uint_as_float(ra[k]);
+                                dst[(k + 32) * a.s_out.cs] = fo * __uint_as_float(rb[k]);
                             }
                         }
                         continue;
                     }
-                    store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
+                    if (!GLA)
+                        store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         ra[k] = __float_as_uint(gn * __uint_as_float(ra[k]));
                         rb[k] = __float_as_uint(gn * __uint_as_float(rb[k]));
                     }
+                    if (GLA)
+                        store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
                     tmem_st32_issue(tm + lane_off + TM_S + 64 * eb, ra);
                     tmem_st32_issue(tm + lane_off + TM_S + 64 * eb + 32, rb);
                     tmem_wait_st();
@@ -616,7 +691,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 float lr = 0.f;
                 if (i < Lc) {
                     const int pi = rev ? Lc - 1 - i : i;
-                    lr = BWD ? pw[Lc - 1 - pi] : scale * pw[pi + 1];
+                    lr = GLA ? scale : (BWD ? pw[Lc - 1 - pi] : scale * pw[pi + 1]);
                 }
                 // a tile store may run past the end of a dense sequence (the
                 // copy clips it) but not into the next packed sequence
@@ -723,10 +798,18 @@ bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t 
 // Tile roles: X rows (scores = X Y^T, inter term X S), Y columns (scaled in
 // place for the state update), Z values.  Forward: (X, Y, Z) = (q, k, v);
 // backward: (k, q, w).
-template <int E, bool BWD> cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s)
+template <int E, bool BWD, bool GLA>
+cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const void *xq = nullptr,
+                      const void *yk = nullptr)
 {
     TcParams p;
-    const Tok &x = BWD ? a.k : a.q, &y = BWD ? a.q : a.k;
+    Tok x = BWD ? a.k : a.q, y = BWD ? a.q : a.k;
+    if (GLA) {
+        // the prepared operands: dense [rows][T][H][D]
+        const int64_t sh = TC_D, st = (int64_t)a.H * TC_D, sb = st * a.T;
+        x = Tok{xq, sb, st, sh, 1};
+        y = Tok{yk, sb, st, sh, 1};
+    }
     if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh, TC_C, x.hdiv) ||
         !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh, TC_C, y.hdiv) ||
         !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh, TC_C, a.v.hdiv) ||
@@ -736,7 +819,7 @@ template <int E, bool BWD> cudaError_t launch_tc(const SweepArgs &a, cudaStream_
     p.dx = x.hdiv;
     p.dy = y.hdiv;
     p.dz = a.v.hdiv;
-    auto kern = tc_sweep_kernel<E, BWD>;
+    auto kern = tc_sweep_kernel<E, BWD, GLA>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            TcLayout<E>::DYN);
     if (err != cudaSuccess)
@@ -764,14 +847,23 @@ cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
-    return a.E == 128 ? launch_tc<128, false>(a, s) : launch_tc<64, false>(a, s);
+    return a.E == 128 ? launch_tc<128, false, false>(a, s) : launch_tc<64, false, false>(a, s);
 }
 
 cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
-    return a.E == 128 ? launch_tc<128, true>(a, s) : launch_tc<64, true>(a, s);
+    return a.E == 128 ? launch_tc<128, true, false>(a, s) : launch_tc<64, true, false>(a, s);
+}
+
+cudaError_t tc_gla_forward_sweep(const SweepArgs &a, const void *xq, const void *yk,
+                                 cudaStream_t s)
+{
+    if (a.N == 0)
+        return cudaSuccess;
+    return a.E == 128 ? launch_tc<128, false, true>(a, s, xq, yk)
+                      : launch_tc<64, false, true>(a, s, xq, yk);
 }
 
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err)

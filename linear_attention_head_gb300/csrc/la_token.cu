@@ -520,6 +520,9 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
     const int tile = (int)(blockIdx.x % sp.tiles);
     const int h = (int)((blockIdx.x / sp.tiles) % a.H);
     const int n = (int)(blockIdx.x / ((unsigned)sp.tiles * a.H));
+    // gated form: only the (sequence, head) pairs the chunked form left over
+    if (a.gla_flags && a.gla_flags[(int64_t)n * a.H + h] != a.gla_flag_run)
+        return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qd = lane & (sp.qw - 1), rg = lane / sp.qw;
     const int c0 = tile * sp.cw + warp * sp.wc + 4 * qd;
@@ -994,7 +997,7 @@ template <typename T> cudaError_t try_stream(const SweepArgs &a, cudaStream_t s)
         return !p || ((reinterpret_cast<uintptr_t>(p) & 15) == 0 && rs == a.E && cs == 1);
     };
     const int esz = (int)sizeof(T);
-    if (a.max_len > STREAM_MAX_T || a.gate.cols || sp.tiles != 1 || a.E % 4 ||
+    if (a.max_len > STREAM_MAX_T || a.gate.cols || a.gla_flags || sp.tiles != 1 || a.E % 4 ||
         !state_ok(a.s_in.p, a.s_in.rs, a.s_in.cs) || !state_ok(a.s_out.p, a.s_out.rs, a.s_out.cs) ||
         !rows_aligned(a, esz))
         return cudaErrorNotSupported;

@@ -188,3 +188,18 @@ def test_workspace_size_for_and_split_control(lib):
     assert lib.la_set_sequence_split(1, 64) == N.LA_ERR_INVALID_ARG
     assert lib.la_set_sequence_split(0, 4096) == N.LA_OK
     assert lib.la_set_sequence_split(1, 2048) == N.LA_OK
+
+
+def test_gated_forward_workspace_size(lib):
+    # the chunked gated forward applies to bf16, D = 128, E in {64, 128} and
+    # sequences longer than 16 tokens: q~ and k~ (bf16), two fp32 vectors per
+    # 128-token chunk and (sequence, head), one flag per (sequence, head)
+    big = _dims(B=2, T=300, H=3, D=128, E=128)
+    r = lambda x: (x + 255) // 256 * 256
+    tok, vec = 2 * 300 * 3 * 128 * 2, 2 * 3 * 3 * 128 * 4
+    assert lib.la_gla_fwd_workspace_size(ctypes.byref(big), 0, None) == \
+        2 * r(tok) + 2 * r(vec) + r(2 * 3 * 4)
+    assert lib.la_gla_fwd_workspace_size(ctypes.byref(big), 1, None) == 0
+    assert lib.la_gla_fwd_workspace_size(ctypes.byref(_dims(T=16, D=128, E=128)), 0, None) == 0
+    assert lib.la_gla_fwd_workspace_size(ctypes.byref(_dims(T=300, D=64)), 0, None) == 0
+    assert lib.la_gla_fwd_workspace_size(ctypes.byref(_dims(T=300, D=128, E=64)), 0, None) > 0
