@@ -498,9 +498,10 @@ def gqa_bench(la, torch, dev, stream, peak):
 
 def gla_bench(la, torch, dev, stream, peak):
     """Gated form (GLA, per-key gate): b4 h32 n8192 d=e=128 bf16, gate fp32.
-    gla_fwd (the chunked tensor-core form: operand pre-pass + tcgen05 sweep)
-    and gla_bwd (token-by-token kernels) timed separately (mean of 3 queued
-    calls after 1 warm-up call).  Algorithmic bytes: forward reads q, k, v, g
+    gla_fwd and gla_bwd (the chunked tensor-core form: operand pre-pass,
+    tcgen05 sweeps, and for the backward the in-place rescaling of dq, dk and
+    dg's block scan) timed separately (mean of 3 queued calls after 1 warm-up
+    call).  Algorithmic bytes: forward reads q, k, v, g
     and writes o; backward reads q, k, v, do, g and writes dq, dk, dv, dg."""
     import workloads as W
     B, T, H, D = 4, 8192, 32, 128
@@ -528,7 +529,7 @@ def gla_bench(la, torch, dev, stream, peak):
     la.get_device_error(dev)
     del q, k, v, do, g
     return {"workload": "fwd+bwd b4 h32 n8192 d=e=128 bf16 tokens, fp32 per-key gate",
-            "kernels": "fwd: chunked tensor-core form; bwd: token-by-token (CUDA cores)",
+            "kernels": "chunked tensor-core form (operand pre-pass + tcgen05 sweeps)",
             "fwd_ms": f_ms, "bwd_ms": b_ms,
             "tokens_per_s": B * T / ((f_ms + b_ms) * 1e-3),
             "fwd_frac_of_peak": (4 * unit + 2 * unit) / (f_ms * 1e-3) / 1e9 / peak,

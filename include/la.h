@@ -288,7 +288,15 @@ size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
  *     dg_w = sum over t at or after w (processing order) of
  *            q_t dq_t - k_t dk_t (+ sum_e F dF at the last token),
  * F the final state and dF = d_final_state.  Needs a 256-byte aligned device
- * workspace of la_gla_workspace_size bytes (LA_ERR_INVALID_ARG otherwise). */
+ * workspace (LA_ERR_INVALID_ARG otherwise); la_gla_workspace_size gives the
+ * bytes with which bf16 calls with D = E = 128, sequences longer than 16
+ * tokens and 16-byte aligned token rows run the chunked form on the tensor
+ * cores: the forward's rescaled q~, k~ (see la_gla_fwd), three sweeps on
+ * them -- forward-type (do, v, k~) giving dq exp(r - b), backward-type
+ * (k~, q~, do) giving dv, backward-type (v, do, q~) giving dk exp(b - r) --
+ * and a pass that rescales dq and dk in place.  Pairs out of range, smaller
+ * workspaces (down to the token-by-token part, the final state and dg's
+ * block sums) and other shapes run the token-by-token kernels. */
 la_status la_gla_bwd(const la_dims *dims, int32_t dtype,
                      const void *q, const void *k, const void *v, const void *d_o,
                      const float *g, const int64_t *g_strides,

@@ -868,11 +868,12 @@ struct GlaFwdWs {
     size_t xq, yk, er, u, flags, total;
     int64_t ncmax;
 };
-GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype)
+GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype, bool bwd = false)
 {
     GlaFwdWs w{};
     const int64_t maxlen = gla_max_len(P);
-    if (dtype != LA_DTYPE_BF16 || P.D != 128 || (P.E != 64 && P.E != 128) ||
+    // the backward's dq and dk sweeps put the 128 value channels on TMEM lanes
+    if (dtype != LA_DTYPE_BF16 || P.D != 128 || (P.E != 64 && P.E != 128) || (bwd && P.E != 128) ||
         maxlen <= la::SHORT_MAX_T || P.N > 65535 || P.H > 65535)
         return w;
     w.ncmax = (maxlen + 127) / 128;
@@ -986,7 +987,10 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
         t.gla_ncmax = w.ncmax;
         t.gla_flags = flags;
         t.gla_flag_run = 0;
-        e = la::tc_gla_forward_sweep(t, pa.xq, pa.yk, s);
+        // X = q~, Y = k~ (dense [rows][T][H][D]), Z = v; state rows gated
+        const int64_t dsh = P.D, dst = (int64_t)P.H * P.D, dsb = dst * P.T;
+        e = la::tc_gla_sweep(t, false, false, la::Tok{pa.xq, dsb, dst, dsh, 1},
+                             la::Tok{pa.yk, dsb, dst, dsh, 1}, t.v, s);
         if (e == cudaSuccess) {
             a.gla_flags = flags;
             a.gla_flag_run = 1;
@@ -1003,7 +1007,7 @@ size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *
     std::string keep = g_msg;
     la_status st = check_dims(dims, dtype, cu_seqlens_host, cu_seqlens_host, nullptr, &P);
     g_msg = keep;
-    return st == LA_OK ? gla_bwd_bytes(P) : 0;
+    return st == LA_OK ? gla_bwd_bytes(P) + gla_fwd_layout(P, dtype, true).total : 0;
 }
 
 la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
@@ -1038,6 +1042,102 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     float *bsum = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                             round256((size_t)P.N * P.H * P.D * P.E * 4));
     la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
+    // The chunked form on the tensor cores, when it applies and the workspace
+    // also holds its operands: the three sweeps on q~, k~ for the (sequence,
+    // head) pairs in range, then dq~, dk~ rescaled in place; the token-by-
+    // token sweeps below run only the flagged pairs.
+    const int *flags = nullptr;
+    la::GlaPrepArgs pa{};
+    {
+        const GlaFwdWs w = gla_fwd_layout(P, dtype, true);
+        auto al = [](const void *p, const int64_t *st) {
+            return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && st[0] % 8 == 0 && st[1] % 8 == 0 &&
+                   st[2] % 8 == 0;
+        };
+        const bool aligned = al(q, dims->qk_strides) && al(k, dims->qk_strides) &&
+                             al(dq, dims->qk_strides) && al(dk, dims->qk_strides) &&
+                             al(v, dims->v_strides) && al(d_o, dims->v_strides) &&
+                             al(dv, dims->v_strides);
+        const bool gate_pairs = (reinterpret_cast<uintptr_t>(g) & 7) == 0 &&
+                                (reinterpret_cast<uintptr_t>(dg) & 7) == 0 &&
+                                g_strides[0] % 2 == 0 && g_strides[1] % 2 == 0 &&
+                                g_strides[2] % 2 == 0;
+        if (w.total && workspace_bytes >= need_ws + w.total && aligned && gate_pairs) {
+            uint8_t *ws = static_cast<uint8_t *>(workspace) + need_ws;
+            int *fl = reinterpret_cast<int *>(ws + w.flags);
+            cudaError_t e = cudaMemsetAsync(fl, 0, (size_t)P.N * P.H * 4, s);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "gated backward flags");
+            pa.N = P.N;
+            pa.H = P.H;
+            pa.D = P.D;
+            pa.T = P.T;
+            pa.ncmax = w.ncmax;
+            pa.cu = cu_seqlens;
+            pa.reverse = reverse ? 1 : 0;
+            pa.bf16 = 1;
+            pa.q = q;
+            pa.k = k;
+            pa.sb = dims->qk_strides[0];
+            pa.st = dims->qk_strides[1];
+            pa.sh = dims->qk_strides[2];
+            pa.g = g;
+            pa.gsb = g_strides[0];
+            pa.gst = g_strides[1];
+            pa.gsh = g_strides[2];
+            pa.g_gamma = g_gamma;
+            pa.xq = ws + w.xq;
+            pa.yk = ws + w.yk;
+            pa.er = reinterpret_cast<float *>(ws + w.er);
+            pa.u = reinterpret_cast<float *>(ws + w.u);
+            pa.flags = fl;
+            pa.lim = 72.f;
+            pa.dq = dq;
+            pa.dk = dk;
+            pa.dg = dg;
+            if ((e = la::gla_prepare(pa, s)) != cudaSuccess)
+                return cuda_fail(e, "gated backward operands");
+            const int64_t dsh = P.D, dst = (int64_t)P.H * P.D, dsb = dst * P.T;
+            const la::Tok tq{pa.xq, dsb, dst, dsh, 1}, tk{pa.yk, dsb, dst, dsh, 1};
+            const la::Tok tdo = tok(d_o, dims->v_strides), tv = tok(v, dims->v_strides);
+            la::SweepArgs t = a;
+            t.gla_er = pa.er;
+            t.gla_u = pa.u;
+            t.gla_ncmax = w.ncmax;
+            t.gla_flags = fl;
+            t.gla_flag_run = 0;
+            // dq~: forward-type (do, v, k~), state S^T with gated columns
+            t.D = P.E;
+            t.E = P.D;
+            t.out = tok_out(dq, dims->qk_strides);
+            t.s_in = la::StateIn{initial_state, 1, P.E};
+            t.s_out = la::StateOut{Ft, P.D, 1};
+            e = la::tc_gla_sweep(t, false, true, tdo, tv, tk, s);
+            if (e == cudaSuccess) {
+                // dv: backward-type (k~, q~, do), G with gated rows
+                t.D = P.D;
+                t.E = P.E;
+                t.out = tok_out(dv, dims->v_strides);
+                t.s_in = la::StateIn{d_final_state, P.E, 1};
+                t.s_out = la::StateOut{d_initial_state, P.E, 1};
+                e = la::tc_gla_sweep(t, true, false, tk, tq, tdo, s);
+            }
+            if (e == cudaSuccess) {
+                // dk~: backward-type (v, do, q~), G^T with gated columns
+                t.D = P.E;
+                t.E = P.D;
+                t.out = tok_out(dk, dims->qk_strides);
+                t.s_in = la::StateIn{d_final_state, 1, P.E};
+                t.s_out = la::StateOut{nullptr, 0, 0};
+                e = la::tc_gla_sweep(t, true, true, tv, tdo, tq, s);
+            }
+            if (e != cudaSuccess)
+                return cuda_fail(e, "gated tensor-core sweep launch");
+            flags = fl;
+            a.gla_flags = fl;
+            a.gla_flag_run = 1;
+        }
+    }
     // dq: forward-type with (q, k, v) := (do, v, k), state S^T (E x D): the
     // gated key channels are its columns; its final state F^T feeds dg
     a.D = P.E;
@@ -1075,6 +1175,11 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.gate = gate_of(g, g_strides, true);
     if ((st = short_run(a, true, s)))
         return st;
+    if (flags) {
+        cudaError_t e = la::gla_undo(pa, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "gated backward rescale");
+    }
     // dg from q dq - k dk and the final-state term
     la::GateGradArgs gg{};
     gg.N = P.N;
@@ -1100,6 +1205,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     gg.Ft = Ft;
     gg.dF = d_final_state;
     gg.bsum = bsum;
+    gg.flags = flags;
     cudaError_t e = la::gate_grad(gg, s);
     return e == cudaSuccess ? LA_OK : cuda_fail(e, "gate gradient");
 }

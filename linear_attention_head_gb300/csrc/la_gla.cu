@@ -48,11 +48,15 @@ __device__ __forceinline__ Seq seq_of(const GateGradArgs &a, int n)
     return s;
 }
 
-// q dq - k dk at processing position p, channel c
+// q dq - k dk at processing position p, channel c; pre: the value is already
+// in dg (written in fp32 by the chunked backward's rescaling pass)
 template <typename T>
-__device__ __forceinline__ float term(const GateGradArgs &a, const Seq &s, int h, int64_t p, int c)
+__device__ __forceinline__ float term(const GateGradArgs &a, const Seq &s, int h, int64_t p, int c,
+                                      bool pre)
 {
     const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
+    if (pre)
+        return a.dg[s.row * a.gsb + t * a.gst + (int64_t)h * a.gsh + c];
     const int64_t off = s.row * a.sb + t * a.st + (int64_t)h * a.sh + c;
     const T *q = static_cast<const T *>(a.q), *dq = static_cast<const T *>(a.dq);
     const T *k = static_cast<const T *>(a.k), *dk = static_cast<const T *>(a.dk);
@@ -67,9 +71,10 @@ template <typename T> __global__ void __launch_bounds__(256) block_sums(GateGrad
     if (c >= a.D || p0 >= s.len)
         return;
     const int64_t p1 = s.len - p0 < DG_TB ? s.len : p0 + DG_TB;
+    const bool pre = a.flags && !a.flags[(int64_t)n * a.H + h];
     float acc = 0.f;
     for (int64_t p = p0; p < p1; ++p)
-        acc += term<T>(a, s, h, p, c);
+        acc += term<T>(a, s, h, p, c, pre);
     a.bsum[(((int64_t)n * a.H + h) * a.nblk + j) * a.D + c] = acc;
 }
 
@@ -91,8 +96,9 @@ template <typename T> __global__ void __launch_bounds__(256) block_scan(GateGrad
     const float *bs = a.bsum + ((int64_t)n * a.H + h) * a.nblk * a.D + c;
     for (int jj = j + 1; jj < nb; ++jj)
         acc += bs[(int64_t)jj * a.D];
+    const bool pre = a.flags && !a.flags[(int64_t)n * a.H + h];
     for (int64_t p = p1 - 1; p >= p0; --p) {
-        acc += term<T>(a, s, h, p, c);
+        acc += term<T>(a, s, h, p, c, pre);
         const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
         a.dg[s.row * a.gsb + t * a.gst + (int64_t)h * a.gsh + c] = acc;
     }

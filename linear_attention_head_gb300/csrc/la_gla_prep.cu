@@ -19,6 +19,11 @@
 // (sequence, head) with a chunk outside the range; those run the token-by-
 // token kernels instead.  Chunks are cut from the start of each sequence, as
 // the sweep cuts them, in either direction.
+//
+// The backward runs its three sweeps on the same operands and yields
+// dq~ = dq exp(r - b) and dk~ = dk exp(b - r); the second mode of this kernel
+// recomputes b and r (the same arithmetic, so the same values) and turns them
+// into dq and dk in place, for every (sequence, head) not flagged.
 
 #include <cmath>
 #include <cstdint>
@@ -45,11 +50,19 @@ template <> struct Pair<float> {
     {
         return *reinterpret_cast<const float2 *>(p);
     }
+    static __device__ __forceinline__ void store(float *p, float2 v)
+    {
+        *reinterpret_cast<float2 *>(p) = v;
+    }
 };
 template <> struct Pair<__nv_bfloat16> {
     static __device__ __forceinline__ float2 load(const __nv_bfloat16 *p)
     {
         return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float2 v)
+    {
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __float22bfloat162_rn(v);
     }
 };
 
@@ -60,7 +73,10 @@ template <> struct Pair<__nv_bfloat16> {
 // combined through shared memory.  The factors exp(b - r), exp(r - b) use the
 // fast exponential: they are rounded to bf16 with their operands anyway.
 constexpr int PG = 4, PT = PC / PG;   // token groups per chunk, tokens per group
-template <typename T> __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
+// UNDO: instead of writing the operands, rescale dq~, dk~ (token dtype, the
+// strides of q and k) in place into dq, dk.
+template <typename T, bool UNDO>
+__global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
 {
     const int pc = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int cp = threadIdx.x & 63, grp = threadIdx.x >> 6, c = 2 * cp;
@@ -138,6 +154,48 @@ template <typename T> __global__ void __launch_bounds__(PG * 64, 2) gla_prep_ker
                                  fmaxf(0.5f * (LO.y + HI.y), -a.lim));
     const bool okx = HI.x - r.x <= a.lim && r.x - LO.x <= a.lim && r.x <= a.lim;
     const bool oky = HI.y - r.y <= a.lim && r.y - LO.y <= a.lim && r.y <= a.lim;
+    if (UNDO) {
+        if (a.flags[(int64_t)n * a.H + h])
+            return;   // computed token by token
+        const int64_t qo = row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
+        T *dqp = static_cast<T *>(a.dq) + qo;
+        T *dkp = static_cast<T *>(a.dk) + qo;
+        const T *qp = static_cast<const T *>(a.q) + qo;
+        const T *kp = static_cast<const T *>(a.k) + qo;
+        float *dgp = a.dg + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
+        const int64_t step = ts * a.st, gstep = ts * a.gst;
+        const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
+        constexpr int PB = 4;
+#pragma unroll
+        for (int j0 = 0; j0 < PT; j0 += PB) {
+            float2 dqv[PB], dkv[PB], qv[PB], kv[PB];
+#pragma unroll
+            for (int jj = 0; jj < PB; ++jj) {
+                const int j = j0 + jj;
+                const int64_t jl = j < np ? j : (np > 0 ? np - 1 : 0);
+                dqv[jj] = Pair<T>::load(dqp + jl * step);
+                dkv[jj] = Pair<T>::load(dkp + jl * step);
+                qv[jj] = Pair<T>::load(qp + jl * step);
+                kv[jj] = Pair<T>::load(kp + jl * step);
+            }
+#pragma unroll
+            for (int jj = 0; jj < PB; ++jj) {
+                const int j = j0 + jj;
+                if (j < np) {
+                    const float ex = b[j].x + sh0.x, ey = b[j].y + sh0.y;   // b - r
+                    const float2 dq2 = make_float2(dqv[jj].x * __expf(ex), dqv[jj].y * __expf(ey));
+                    const float2 dk2 =
+                        make_float2(dkv[jj].x * __expf(-ex), dkv[jj].y * __expf(-ey));
+                    Pair<T>::store(dqp + j * step, dq2);
+                    Pair<T>::store(dkp + j * step, dk2);
+                    *reinterpret_cast<float2 *>(dgp + j * gstep) =
+                        make_float2(qv[jj].x * dq2.x - kv[jj].x * dk2.x,
+                                    qv[jj].y * dq2.y - kv[jj].y * dk2.y);
+                }
+            }
+        }
+        return;
+    }
     if (grp == 0) {
         if (!(okx && oky))
             atomicOr(a.flags + (int64_t)n * a.H + h, 1);
@@ -198,9 +256,24 @@ cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s)
     dim3 grid((unsigned)a.ncmax, (unsigned)a.H, (unsigned)a.N);
     const int threads = PG * 64;
     if (a.bf16)
-        gla_prep_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(a);
+        gla_prep_kernel<__nv_bfloat16, false><<<grid, threads, 0, s>>>(a);
     else
-        gla_prep_kernel<float><<<grid, threads, 0, s>>>(a);
+        gla_prep_kernel<float, false><<<grid, threads, 0, s>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s)
+{
+    if (a.N == 0 || a.H == 0 || a.ncmax == 0)
+        return cudaSuccess;
+    if (a.D != 128 || a.N > 65535 || a.H > 65535 || a.ncmax > 0x7fffffff)
+        return cudaErrorNotSupported;
+    dim3 grid((unsigned)a.ncmax, (unsigned)a.H, (unsigned)a.N);
+    if (a.bf16)
+        gla_prep_kernel<__nv_bfloat16, true><<<grid, PG * 64, 0, s>>>(a);
+    else
+        gla_prep_kernel<float, true><<<grid, PG * 64, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }

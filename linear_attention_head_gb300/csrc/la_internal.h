@@ -100,13 +100,21 @@ struct GlaPrepArgs {
     float *er, *u;            // [N][H][ncmax][D]
     int *flags;               // [N H], zeroed beforehand
     float lim;                // largest |b - r| (and |r|) the chunked form takes
+    void *dq, *dk;            // gla_undo: dq~, dk~ in, dq, dk out (q's strides)
+    float *dg;                // gla_undo: q dq - k dk (fp32, before dq and dk are
+                              // rounded) per element, the gate's strides
 };
 cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s);
-// Tensor-core forward of the gated form on the operands gla_prepare wrote
-// (xq, yk dense [rows][T][H][D] bf16); a.gla_* set.  cudaErrorNotSupported
-// when the tensor maps cannot be built.
-cudaError_t tc_gla_forward_sweep(const SweepArgs &a, const void *xq, const void *yk,
-                                 cudaStream_t s);
+// dq~ -> dq, dk~ -> dk in place, and dg's terms q dq - k dk into dg, for the
+// (sequence, head) pairs not flagged.
+cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s);
+// A tensor-core sweep of the gated form on rescaled operands (la_gla_prep.cu)
+// with tile roles X, Y, Z given (bf16, D = 128 X and Y width): forward-type or
+// backward-type (bwd), the gated key channels being the state's rows or its
+// columns (cols, needs E = 128); a.gla_* set, a.out the output.
+// cudaErrorNotSupported when the tensor maps cannot be built.
+cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, const Tok &y,
+                         const Tok &z, cudaStream_t s);
 
 // Calls whose longest sequence has at most this many tokens run the
 // token-by-token kernels (la_token.cu) instead of the chunked ones.
@@ -162,6 +170,9 @@ struct GateGradArgs {
     int64_t gsb, gst, gsh;
     const float *Ft, *dF;
     float *bsum;
+    // when set, the (sequence, head) pairs whose flag is 0 find their terms
+    // q dq - k dk already in dg (written by gla_undo in fp32)
+    const int *flags = nullptr;
 };
 cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s);
 

@@ -192,10 +192,11 @@ __device__ __forceinline__ void store_half_row_sw128(uint8_t *row_base, int row,
 }
 
 // Initial state row i, 8 columns at a time (once per CTA): fp32 from global
-// (any strides) -> times c0 as bf16 into the swizzled S copy, and times g0
-// into TMEM.
+// (any strides), times colf[column] when colf is given, -> times c0 as bf16
+// into the swizzled S copy, and times g0 into TMEM.
 __device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i, int E_,
-                                         uint8_t *sbf, uint32_t tmem_row, float g0, float c0)
+                                         uint8_t *sbf, uint32_t tmem_row, float g0, float c0,
+                                         const float *colf = nullptr)
 {
 #pragma unroll 1
     for (int p8 = 0; p8 < E_ / 8; ++p8) {
@@ -203,7 +204,7 @@ __device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i
         const float *src = sin.p ? sin.p + base + i * sin.rs + (8 * p8) * sin.cs : nullptr;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            x[k] = src ? src[k * sin.cs] : 0.f;
+            x[k] = (src ? src[k * sin.cs] : 0.f) * (colf ? colf[8 * p8 + k] : 1.f);
         *reinterpret_cast<uint4 *>(sbf + (p8 >> 3) * (TC_D * 128) + (((p8 & 7) ^ (i & 7)) << 4)) =
             make_uint4(pack_bf16x2(c0 * x[0], c0 * x[1]), pack_bf16x2(c0 * x[2], c0 * x[3]),
                        pack_bf16x2(c0 * x[4], c0 * x[5]), pack_bf16x2(c0 * x[6], c0 * x[7]));
@@ -313,10 +314,13 @@ __device__ __forceinline__ void zero_row(uint8_t *row_base)
         *reinterpret_cast<uint4 *>(row_base + (c16 << 4)) = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// GLA: the gated forward on the operands of la_gla_prep.cu (X = q~, Y = k~):
-// plain causal P, no column factor on Y, state rows scaled per chunk by
-// exp(B - r) and the next chunk's exp(r), the inter term scaled by s alone.
-template <int E, bool BWD, bool GLA>
+// GLA (gated form, on operands rescaled by la_gla_prep.cu): plain causal P,
+// no decay factor on Y (backward-type: Y times s), the inter term scaled by
+// s (forward-type) or 1; the state scaled after each chunk's update by the
+// chunk's factor and the next chunk's -- exp(B - r) then exp(r) going
+// forward, exp(r) then exp(B - r) going backward -- on its rows (GLA 1: the
+// gated key channels are the state's rows) or columns (GLA 2).
+template <int E, bool BWD, int GLA>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_constant__ TcParams P)
 {
     using L = TcLayout<E>;
@@ -592,10 +596,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 tmem_st16_even_issue(col + 16, rb);
                 tmem_wait_st();
                 if (GLA) {
-                    // Y carries its factors already; rows past the sequence's
-                    // end (the next packed sequence's, or zero fill) are cleared
+                    // Y carries its factors already (backward-type: times s);
+                    // rows past the sequence's end (the next packed
+                    // sequence's, or zero fill) are cleared
+                    uint8_t *yrow = sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128;
                     if (i >= Lc)
-                        zero_row(sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128);
+                        zero_row(yrow);
+                    else if (BWD)
+                        scale_row_sw128(yrow, i, scale);
                 } else {
                     // column factor for the state update, applied to row i of Y
                     float lc = 0.f;
@@ -616,14 +624,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             uint8_t *sbf = sm + L::SOFF + i * 128;
             // initial state: bf16 copy and gamma^L0-scaled fp32 in TMEM (an
             // empty sequence passes it straight to the final state)
-            // gated form: row factors of chunk position pc, [N][H][ncmax][D]
+            // gated form: factors of chunk position pc for key channel i (the
+            // state's row i, or column i), [N][H][ncmax][128]; vo the chunk's
+            // own factor, vn the next chunk's (also the initial state's)
             const int64_t vrow = ((int64_t)n * a.H + h) * a.gla_ncmax;
             auto vidx = [&](int pc) { return (vrow + pc) * TC_D + i; };
+            const float *vo = BWD ? a.gla_er : a.gla_u, *vn = BWD ? a.gla_u : a.gla_er;
+            // GLA 2: this step's per-column factors, shared by the S group
+            float *colf = pw;
+            auto sg_sync = [] { asm volatile("bar.sync 2, %0;" ::"n"(TC_SG) : "memory"); };
             if (nc == 0) {
                 state_copy(a.s_in, a.s_out, sb, i, E);
-            } else if (GLA) {
-                const float e0 = a.gla_er[vidx(flip ? nc - 1 : 0)];
+            } else if (GLA == 1) {
+                const float e0 = vn[vidx(flip ? nc - 1 : 0)];
                 state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, e0, e0);
+            } else if (GLA == 2) {
+                if (i < E)
+                    colf[i] = vn[vidx(flip ? nc - 1 : 0)];
+                sg_sync();
+                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, 1.f, 1.f, colf);
             } else {
                 state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, pw[chunk_len(0)], 1.f);
             }
@@ -636,12 +655,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 // (gated form) or x and gn x
                 float fo = 1.f, ft = last ? 1.f : pw[chunk_len(c + 1)];
                 if (GLA) {
-                    fo = a.gla_u[vidx(flip ? nc - 1 - c : c)];
+                    fo = GLA == 1 || i < E ? vo[vidx(flip ? nc - 1 - c : c)] : 1.f;
                     if (!last)
-                        ft = fo * a.gla_er[vidx(flip ? nc - 2 - c : c + 1)];
+                        ft = fo * (GLA == 1 || i < E ? vn[vidx(flip ? nc - 2 - c : c + 1)] : 1.f);
                 }
-                if (!warp_all(bwait(ds_full, c & 1, abort_flag)))
+                if (GLA == 2) {
+                    // one decision for the whole S group: its barriers below
+                    // must not be left by some warps only
+                    uint32_t all;
+                    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                                 "setp.ne.u32 q, %1, 0;\n\t"
+                                 "bar.red.and.pred p, 3, %2, q;\n\t"
+                                 "selp.u32 %0, 1, 0, p;\n\t}"
+                                 : "=r"(all)
+                                 : "r"(bwait(ds_full, c & 1, abort_flag) ? 1u : 0u), "n"(TC_SG)
+                                 : "memory");
+                    if (!all)
+                        break;
+                    if (i < E)
+                        colf[i] = last ? fo : ft;
+                    sg_sync();
+                } else if (!warp_all(bwait(ds_full, c & 1, abort_flag))) {
                     break;
+                }
                 tc_fence_after();
                 const float gn = ft;
 #pragma unroll 1
@@ -655,8 +691,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                             float *dst = a.s_out.p + sb + i * a.s_out.rs + 64 * eb * a.s_out.cs;
 #pragma unroll
                             for (int k = 0; k < 32; ++k) {
-                                dst[k * a.s_out.cs] = fo * __uint_as_float(ra[k]);
-                                dst[(k + 32) * a.s_out.cs] = fo * __uint_as_float(rb[k]);
+                                const float f0 = GLA == 2 ? colf[64 * eb + k] : fo;
+                                const float f1 = GLA == 2 ? colf[64 * eb + 32 + k] : fo;
+                                dst[k * a.s_out.cs] = f0 * __uint_as_float(ra[k]);
+                                dst[(k + 32) * a.s_out.cs] = f1 * __uint_as_float(rb[k]);
                             }
                         }
                         continue;
@@ -665,8 +703,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        ra[k] = __float_as_uint(gn * __uint_as_float(ra[k]));
-                        rb[k] = __float_as_uint(gn * __uint_as_float(rb[k]));
+                        const float f0 = GLA == 2 ? colf[64 * eb + k] : gn;
+                        const float f1 = GLA == 2 ? colf[64 * eb + 32 + k] : gn;
+                        ra[k] = __float_as_uint(f0 * __uint_as_float(ra[k]));
+                        rb[k] = __float_as_uint(f1 * __uint_as_float(rb[k]));
                     }
                     if (GLA)
                         store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
@@ -691,7 +731,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 float lr = 0.f;
                 if (i < Lc) {
                     const int pi = rev ? Lc - 1 - i : i;
-                    lr = GLA ? scale : (BWD ? pw[Lc - 1 - pi] : scale * pw[pi + 1]);
+                    lr = GLA ? (BWD ? 1.f : scale) : (BWD ? pw[Lc - 1 - pi] : scale * pw[pi + 1]);
                 }
                 // a tile store may run past the end of a dense sequence (the
                 // copy clips it) but not into the next packed sequence
@@ -798,27 +838,22 @@ bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t 
 // Tile roles: X rows (scores = X Y^T, inter term X S), Y columns (scaled in
 // place for the state update), Z values.  Forward: (X, Y, Z) = (q, k, v);
 // backward: (k, q, w).
-template <int E, bool BWD, bool GLA>
-cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const void *xq = nullptr,
-                      const void *yk = nullptr)
+template <int E, bool BWD, int GLA>
+cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullptr)
 {
     TcParams p;
-    Tok x = BWD ? a.k : a.q, y = BWD ? a.q : a.k;
-    if (GLA) {
-        // the prepared operands: dense [rows][T][H][D]
-        const int64_t sh = TC_D, st = (int64_t)a.H * TC_D, sb = st * a.T;
-        x = Tok{xq, sb, st, sh, 1};
-        y = Tok{yk, sb, st, sh, 1};
-    }
+    // tile roles; the gated form names its three operands itself
+    const Tok x = xyz ? xyz[0] : (BWD ? a.k : a.q), y = xyz ? xyz[1] : (BWD ? a.q : a.k);
+    const Tok z = xyz ? xyz[2] : a.v;
     if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh, TC_C, x.hdiv) ||
         !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh, TC_C, y.hdiv) ||
-        !make_map(&p.mz, a.v.p, E, a, a.v.sb, a.v.st, a.v.sh, TC_C, a.v.hdiv) ||
+        !make_map(&p.mz, z.p, E, a, z.sb, z.st, z.sh, TC_C, z.hdiv) ||
         !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh, 32))
         return cudaErrorNotSupported;
     p.a = a;
     p.dx = x.hdiv;
     p.dy = y.hdiv;
-    p.dz = a.v.hdiv;
+    p.dz = z.hdiv;
     auto kern = tc_sweep_kernel<E, BWD, GLA>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            TcLayout<E>::DYN);
@@ -847,23 +882,31 @@ cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
-    return a.E == 128 ? launch_tc<128, false, false>(a, s) : launch_tc<64, false, false>(a, s);
+    return a.E == 128 ? launch_tc<128, false, 0>(a, s) : launch_tc<64, false, 0>(a, s);
 }
 
 cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
-    return a.E == 128 ? launch_tc<128, true, false>(a, s) : launch_tc<64, true, false>(a, s);
+    return a.E == 128 ? launch_tc<128, true, 0>(a, s) : launch_tc<64, true, 0>(a, s);
 }
 
-cudaError_t tc_gla_forward_sweep(const SweepArgs &a, const void *xq, const void *yk,
-                                 cudaStream_t s)
+cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, const Tok &y,
+                         const Tok &z, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
-    return a.E == 128 ? launch_tc<128, false, true>(a, s, xq, yk)
-                      : launch_tc<64, false, true>(a, s, xq, yk);
+    const Tok xyz[3] = {x, y, z};
+    if (cols && a.E != 128)
+        return cudaErrorNotSupported;   // column factors: 128 key channels as columns
+    if (bwd)
+        return cols ? launch_tc<128, true, 2>(a, s, xyz)
+                    : (a.E == 128 ? launch_tc<128, true, 1>(a, s, xyz)
+                                  : launch_tc<64, true, 1>(a, s, xyz));
+    return cols ? launch_tc<128, false, 2>(a, s, xyz)
+                : (a.E == 128 ? launch_tc<128, false, 1>(a, s, xyz)
+                              : launch_tc<64, false, 1>(a, s, xyz));
 }
 
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err)
