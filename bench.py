@@ -637,13 +637,35 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=None)
+    ap.add_argument("--only", default=None,
+                    choices=["sweep", "decode", "long_sequence", "grouped_kv", "gated"],
+                    help="run one of the secondary measurements alone (one GPU) and print "
+                         "its JSON object")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.only:
+        section_only(args)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         gpu_bench(args)
+
+
+def section_only(args):
+    """One secondary measurement of the bench line on cuda:0, e.g. for a profiler."""
+    import torch
+    import linear_attention_head_gb300 as la
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, _ = peaks()
+    fn = {"sweep": lambda: length_sweep(la, torch, dev, stream, args.n),
+          "decode": lambda: decode_bench(la, torch, dev, stream, peak),
+          "long_sequence": lambda: split_bench(la, torch, dev, stream, peak),
+          "grouped_kv": lambda: gqa_bench(la, torch, dev, stream, peak),
+          "gated": lambda: gla_bench(la, torch, dev, stream, peak)}[args.only]
+    print(json.dumps({args.only: fn()}), flush=True)
 
 
 if __name__ == "__main__":
