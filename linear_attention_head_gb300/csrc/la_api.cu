@@ -1095,6 +1095,9 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             pa.dq = dq;
             pa.dk = dk;
             pa.dg = dg;
+            pa.Ft = Ft;
+            pa.dF = d_final_state;
+            pa.E = P.E;
             if ((e = la::gla_prepare(pa, s)) != cudaSuccess)
                 return cuda_fail(e, "gated backward operands");
             const int64_t dsh = P.D, dst = (int64_t)P.H * P.D, dsb = dst * P.T;

@@ -48,15 +48,11 @@ __device__ __forceinline__ Seq seq_of(const GateGradArgs &a, int n)
     return s;
 }
 
-// q dq - k dk at processing position p, channel c; pre: the value is already
-// in dg (written in fp32 by the chunked backward's rescaling pass)
+// q dq - k dk at processing position p, channel c
 template <typename T>
-__device__ __forceinline__ float term(const GateGradArgs &a, const Seq &s, int h, int64_t p, int c,
-                                      bool pre)
+__device__ __forceinline__ float term(const GateGradArgs &a, const Seq &s, int h, int64_t p, int c)
 {
     const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
-    if (pre)
-        return a.dg[s.row * a.gsb + t * a.gst + (int64_t)h * a.gsh + c];
     const int64_t off = s.row * a.sb + t * a.st + (int64_t)h * a.sh + c;
     const T *q = static_cast<const T *>(a.q), *dq = static_cast<const T *>(a.dq);
     const T *k = static_cast<const T *>(a.k), *dk = static_cast<const T *>(a.dk);
@@ -71,10 +67,11 @@ template <typename T> __global__ void __launch_bounds__(256) block_sums(GateGrad
     if (c >= a.D || p0 >= s.len)
         return;
     const int64_t p1 = s.len - p0 < DG_TB ? s.len : p0 + DG_TB;
-    const bool pre = a.flags && !a.flags[(int64_t)n * a.H + h];
+    if (a.flags && !a.flags[(int64_t)n * a.H + h])
+        return;   // done by the chunked form
     float acc = 0.f;
     for (int64_t p = p0; p < p1; ++p)
-        acc += term<T>(a, s, h, p, c, pre);
+        acc += term<T>(a, s, h, p, c);
     a.bsum[(((int64_t)n * a.H + h) * a.nblk + j) * a.D + c] = acc;
 }
 
@@ -86,6 +83,8 @@ template <typename T> __global__ void __launch_bounds__(256) block_scan(GateGrad
     if (c >= a.D || p0 >= s.len)
         return;
     const int64_t p1 = s.len - p0 < DG_TB ? s.len : p0 + DG_TB;
+    if (a.flags && !a.flags[(int64_t)n * a.H + h])
+        return;   // done by the chunked form
     // the final-state term: sum_e F[c][e] dF[c][e]; F is stored transposed
     const int64_t sidx = ((int64_t)n * a.H + h) * (int64_t)a.D * a.E;
     float acc = 0.f;
@@ -96,9 +95,8 @@ template <typename T> __global__ void __launch_bounds__(256) block_scan(GateGrad
     const float *bs = a.bsum + ((int64_t)n * a.H + h) * a.nblk * a.D + c;
     for (int jj = j + 1; jj < nb; ++jj)
         acc += bs[(int64_t)jj * a.D];
-    const bool pre = a.flags && !a.flags[(int64_t)n * a.H + h];
     for (int64_t p = p1 - 1; p >= p0; --p) {
-        acc += term<T>(a, s, h, p, c, pre);
+        acc += term<T>(a, s, h, p, c);
         const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
         a.dg[s.row * a.gsb + t * a.gst + (int64_t)h * a.gsh + c] = acc;
     }

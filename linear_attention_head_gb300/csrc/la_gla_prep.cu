@@ -22,8 +22,13 @@
 //
 // The backward runs its three sweeps on the same operands and yields
 // dq~ = dq exp(r - b) and dk~ = dk exp(b - r); the second mode of this kernel
-// recomputes b and r (the same arithmetic, so the same values) and turns them
-// into dq and dk in place, for every (sequence, head) not flagged.
+// recomputes b and r (the same arithmetic, so the same values), turns them
+// into dq and dk in place and forms the gate's gradient, for every (sequence,
+// head) not flagged:
+//     dg_w = sum over t at or after w (processing order) of q_t dq_t - k_t dk_t
+//            + sum_e F dF,
+// the terms in fp32 from the unrounded products, summed within the chunk
+// there and completed by gla_dg_finish with the later chunks' totals.
 
 #include <cmath>
 #include <cstdint>
@@ -165,6 +170,9 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
         float *dgp = a.dg + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
         const int64_t step = ts * a.st, gstep = ts * a.gst;
         const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
+        // dq, dk, and dg's terms q dq - k dk (fp32, from the unrounded
+        // products) into b[], which the factors no longer need
+        float2 gt = make_float2(0.f, 0.f);   // this group's sum of terms
         constexpr int PB = 4;
 #pragma unroll
         for (int j0 = 0; j0 < PT; j0 += PB) {
@@ -181,6 +189,7 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
 #pragma unroll
             for (int jj = 0; jj < PB; ++jj) {
                 const int j = j0 + jj;
+                float2 tm = make_float2(0.f, 0.f);
                 if (j < np) {
                     const float ex = b[j].x + sh0.x, ey = b[j].y + sh0.y;   // b - r
                     const float2 dq2 = make_float2(dqv[jj].x * __expf(ex), dqv[jj].y * __expf(ey));
@@ -188,11 +197,53 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
                         make_float2(dkv[jj].x * __expf(-ex), dkv[jj].y * __expf(-ey));
                     Pair<T>::store(dqp + j * step, dq2);
                     Pair<T>::store(dkp + j * step, dk2);
-                    *reinterpret_cast<float2 *>(dgp + j * gstep) =
-                        make_float2(qv[jj].x * dq2.x - kv[jj].x * dk2.x,
-                                    qv[jj].y * dq2.y - kv[jj].y * dk2.y);
+                    tm = make_float2(qv[jj].x * dq2.x - kv[jj].x * dk2.x,
+                                     qv[jj].y * dq2.y - kv[jj].y * dk2.y);
+                }
+                b[j] = tm;
+                gt.x += tm.x;
+                gt.y += tm.y;
+            }
+        }
+        // dg within the chunk: the sum of the terms at or after each token in
+        // processing order; the later groups' totals come through shared
+        // memory, the later chunks' (and the final state's) from gla_dg_finish
+        __shared__ float2 gts[PG][64];
+        gts[grp][cp] = gt;
+        __syncthreads();
+        float2 acc = make_float2(0.f, 0.f), tot = acc;
+#pragma unroll
+        for (int k = 0; k < PG; ++k) {
+            const float2 x = gts[k][cp];
+            if (k > grp) {
+                acc.x += x.x;
+                acc.y += x.y;
+            }
+            tot.x += x.x;
+            tot.y += x.y;
+        }
+#pragma unroll
+        for (int j = PT - 1; j >= 0; --j) {
+            acc.x += b[j].x;
+            acc.y += b[j].y;
+            if (j < np)
+                *reinterpret_cast<float2 *>(dgp + j * gstep) = acc;
+        }
+        const int64_t hv = (int64_t)n * a.H + h;
+        if (grp == 0)   // the chunk's total per channel
+            *reinterpret_cast<float2 *>(a.er + (hv * a.ncmax + pc) * a.D + c) = tot;
+        if (grp == 1 && pc == 0) {
+            // sum_e F[c][e] dF[c][e] (F stored transposed), once per (sequence, head)
+            float2 f = make_float2(0.f, 0.f);
+            if (a.dF) {
+                const float *Ft = a.Ft + hv * a.D * a.E, *dF = a.dF + hv * a.D * a.E;
+                for (int e = 0; e < a.E; ++e) {
+                    const float2 fe = *reinterpret_cast<const float2 *>(Ft + (int64_t)e * a.D + c);
+                    f.x += fe.x * dF[(int64_t)c * a.E + e];
+                    f.y += fe.y * dF[(int64_t)(c + 1) * a.E + e];
                 }
             }
+            *reinterpret_cast<float2 *>(a.u + hv * a.D + c) = f;
         }
         return;
     }
@@ -245,6 +296,44 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
     }
 }
 
+// The rest of dg for a chunk run in the chunked form: the totals of the
+// chunks after it in processing order (a.er, per channel) and the final
+// state's term (a.u), added to every token of the chunk.
+__global__ void __launch_bounds__(PG * 64) gla_dg_finish(GlaPrepArgs a)
+{
+    const int pc = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int cp = threadIdx.x & 63, grp = threadIdx.x >> 6, c = 2 * cp;
+    int64_t row, bos, len;
+    if (a.cu) {
+        row = 0;
+        bos = a.cu[n];
+        len = (int64_t)a.cu[n + 1] - a.cu[n];
+    } else {
+        row = n;
+        bos = 0;
+        len = a.T;
+    }
+    const int64_t hv = (int64_t)n * a.H + h;
+    const int64_t t0 = (int64_t)pc * PC;
+    if (t0 >= len || a.flags[hv])
+        return;
+    const int nc = (int)((len + PC - 1) / PC);
+    float2 add = *reinterpret_cast<const float2 *>(a.u + hv * a.D + c);
+    for (int p = a.reverse ? 0 : pc + 1; p < (a.reverse ? pc : nc); ++p) {
+        const float2 x = *reinterpret_cast<const float2 *>(a.er + (hv * a.ncmax + p) * a.D + c);
+        add.x += x.x;
+        add.y += x.y;
+    }
+    const int Lc = (int)(len - t0 < PC ? len - t0 : PC);
+    float *dgp = a.dg + row * a.gsb + (int64_t)h * a.gsh + c + (bos + t0) * a.gst;
+#pragma unroll 4
+    for (int i = grp; i < Lc; i += PG) {
+        float2 *p = reinterpret_cast<float2 *>(dgp + i * a.gst);
+        const float2 x = *p;
+        *p = make_float2(x.x + add.x, x.y + add.y);
+    }
+}
+
 }  // namespace
 
 cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s)
@@ -274,6 +363,11 @@ cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s)
         gla_prep_kernel<__nv_bfloat16, true><<<grid, PG * 64, 0, s>>>(a);
     else
         gla_prep_kernel<float, true><<<grid, PG * 64, 0, s>>>(a);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    gla_dg_finish<<<grid, PG * 64, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }

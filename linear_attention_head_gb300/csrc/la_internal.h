@@ -101,12 +101,14 @@ struct GlaPrepArgs {
     int *flags;               // [N H], zeroed beforehand
     float lim;                // largest |b - r| (and |r|) the chunked form takes
     void *dq, *dk;            // gla_undo: dq~, dk~ in, dq, dk out (q's strides)
-    float *dg;                // gla_undo: q dq - k dk (fp32, before dq and dk are
-                              // rounded) per element, the gate's strides
+    float *dg;                // gla_undo: the gate's gradient (the gate's strides)
+    const float *Ft, *dF;     // gla_undo: final state (transposed, [E][D] per
+                              // pair) and its gradient ([D][E]), or dF null
+    int E;
 };
 cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s);
-// dq~ -> dq, dk~ -> dk in place, and dg's terms q dq - k dk into dg, for the
-// (sequence, head) pairs not flagged.
+// dq~ -> dq, dk~ -> dk in place, and the gate's gradient dg, for the
+// (sequence, head) pairs not flagged (a.er and a.u are reused as scratch).
 cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s);
 // A tensor-core sweep of the gated form on rescaled operands (la_gla_prep.cu)
 // with tile roles X, Y, Z given (bf16, D = 128 X and Y width): forward-type or
@@ -170,8 +172,8 @@ struct GateGradArgs {
     int64_t gsb, gst, gsh;
     const float *Ft, *dF;
     float *bsum;
-    // when set, the (sequence, head) pairs whose flag is 0 find their terms
-    // q dq - k dk already in dg (written by gla_undo in fp32)
+    // when set, only the (sequence, head) pairs whose flag is set are done
+    // (gla_undo did the others)
     const int *flags = nullptr;
 };
 cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s);
