@@ -498,10 +498,11 @@ def gqa_bench(la, torch, dev, stream, peak):
 
 def gla_bench(la, torch, dev, stream, peak):
     """Gated form (GLA, per-key gate): b4 h32 n8192 d=e=128 bf16, gate fp32.
-    gla_fwd and gla_bwd (the chunked tensor-core form: operand pre-pass,
-    tcgen05 sweeps, and for the backward the in-place rescaling of dq, dk and
-    dg's block scan) timed separately (mean of 3 queued calls after 1 warm-up
-    call).  Algorithmic bytes: forward reads q, k, v, g
+    gla_fwd alone, then a step (gla_fwd keeping its rescaled operands, gla_bwd
+    reusing them); bwd_ms = step - fwd.  The chunked tensor-core form: operand
+    pre-pass, tcgen05 sweeps, and for the backward the in-place rescaling of
+    dq, dk with dg.  Each figure is the mean of 3 queued calls after 1 warm-up
+    call; bwd_alone_ms is gla_bwd computing the operands itself.  Algorithmic bytes: forward reads q, k, v, g
     and writes o; backward reads q, k, v, do, g and writes dq, dk, dv, dg."""
     import workloads as W
     B, T, H, D = 4, 8192, 32, 128
@@ -523,15 +524,22 @@ def gla_bench(la, torch, dev, stream, peak):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 3
 
+    def step():
+        # a training step: the backward reuses the forward's rescaled q, k
+        o, fin, ops = la.gla_fwd(q, k, v, g, gg, 1.0, keep_operands=True)
+        la.gla_bwd(q, k, v, do, g, gg, 1.0, want_d_initial_state=False, operands=ops)
+
     f_ms = timed(lambda: la.gla_fwd(q, k, v, g, gg, 1.0))
-    b_ms = timed(lambda: la.gla_bwd(q, k, v, do, g, gg, 1.0, want_d_initial_state=False))
+    b_alone_ms = timed(lambda: la.gla_bwd(q, k, v, do, g, gg, 1.0, want_d_initial_state=False))
+    s_ms = timed(step)
+    b_ms = s_ms - f_ms
     unit = B * T * H * D * 2
     la.get_device_error(dev)
     del q, k, v, do, g
     return {"workload": "fwd+bwd b4 h32 n8192 d=e=128 bf16 tokens, fp32 per-key gate",
             "kernels": "chunked tensor-core form (operand pre-pass + tcgen05 sweeps)",
-            "fwd_ms": f_ms, "bwd_ms": b_ms,
-            "tokens_per_s": B * T / ((f_ms + b_ms) * 1e-3),
+            "fwd_ms": f_ms, "bwd_ms": b_ms, "step_ms": s_ms, "bwd_alone_ms": b_alone_ms,
+            "tokens_per_s": B * T / (s_ms * 1e-3),
             "fwd_frac_of_peak": (4 * unit + 2 * unit) / (f_ms * 1e-3) / 1e9 / peak,
             "bwd_frac_of_peak": (7 * unit + 4 * unit) / (b_ms * 1e-3) / 1e9 / peak}
 

@@ -255,6 +255,9 @@ la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens);
  *   g_gamma    [H] fp32, required (zeros for no head decay)
  *   workspace  256-byte aligned device scratch of at least
  *              la_gla_fwd_workspace_size bytes, or NULL
+ *   operands_written  host int32, or NULL: set to 1 when the call ran the
+ *              chunked form, leaving its operands in the workspace (which
+ *              la_gla_bwd can then reuse), else 0
  *   everything else as la_fwd; kv_heads must be 0 (or H).
  * With the workspace, bf16 calls with D = 128, E in {64, 128} and sequences
  * longer than 16 tokens run the chunked form on the tensor cores: per chunk
@@ -274,7 +277,8 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype,
                      const float *initial_state, int32_t reverse,
                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                      void *o, float *final_state, void *workspace,
-                     size_t workspace_bytes, void *stream);
+                     size_t workspace_bytes, int32_t *operands_written,
+                     void *stream);
 
 /* Bytes of workspace with which la_gla_fwd runs the chunked form for these
  * sizes (q~, k~ as bf16 [rows][T][H][D] each, two fp32 vectors per chunk and
@@ -296,7 +300,13 @@ size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
  * (k~, q~, do) giving dv, backward-type (v, do, q~) giving dk exp(b - r) --
  * and a pass that rescales dq and dk in place.  Pairs out of range, smaller
  * workspaces (down to the token-by-token part, the final state and dg's
- * block sums) and other shapes run the token-by-token kernels. */
+ * block sums) and other shapes run the token-by-token kernels.
+ *   fwd_workspace  the workspace of a la_gla_fwd call on the same q, k, g,
+ *              g_gamma, reverse and cu_seqlens that reported operands_written
+ *              = 1, untouched since; or NULL.  The backward then uses the
+ *              operands in it instead of computing them again (the main
+ *              workspace needs only the token-by-token part) and uses the
+ *              rest of it as scratch: it serves one backward. */
 la_status la_gla_bwd(const la_dims *dims, int32_t dtype,
                      const void *q, const void *k, const void *v, const void *d_o,
                      const float *g, const int64_t *g_strides,
@@ -305,13 +315,16 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype,
                      int32_t reverse,
                      const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                      void *dq, void *dk, void *dv, float *dg, float *d_initial_state,
-                     void *workspace, size_t workspace_bytes, void *stream);
+                     void *workspace, size_t workspace_bytes,
+                     void *fwd_workspace, size_t fwd_workspace_bytes, void *stream);
 
-/* Workspace bytes of la_gla_bwd for these sizes (0 for invalid sizes).
- * cu_seqlens_host: host copy of cu_seqlens for packed sequences, else NULL.
- * Pure host function. */
+/* Workspace bytes of la_gla_bwd for these sizes (0 for invalid sizes): with
+ * with_forward_operands = 0, enough to run the chunked form on its own where
+ * it applies; nonzero, the part needed when the forward's operands are passed
+ * as fwd_workspace.  cu_seqlens_host: host copy of cu_seqlens for packed
+ * sequences, else NULL.  Pure host function. */
 size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype,
-                             const int32_t *cu_seqlens_host);
+                             const int32_t *cu_seqlens_host, int32_t with_forward_operands);
 
 /* Reads and clears the device-side error word that bounded on-device waits
  * set when they run out (LA_ERR_TIMEOUT), after synchronizing `stream`.

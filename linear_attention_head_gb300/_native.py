@@ -75,11 +75,11 @@ PROTOTYPES = {
     "la_workspace_size_for": (_sz, [_dims_p, _i32, _vp]),
     "la_set_sequence_split": (_i32, [_i32, _i32]),
     "la_gla_fwd": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _vp,
-                          _vp, _vp, _vp, _vp, _sz, _vp]),
+                          _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "la_gla_fwd_workspace_size": (_sz, [_dims_p, _i32, _vp]),
     "la_gla_bwd": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp,
-                          _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "la_gla_workspace_size": (_sz, [_dims_p, _i32, _vp]),
+                          _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp]),
+    "la_gla_workspace_size": (_sz, [_dims_p, _i32, _vp, _i32]),
     "la_debug_withhold_next_handoff": (_i32, [_i32]),
     "la_fwd_noalloc": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _vp,
                               _vp, _vp, _vp]),

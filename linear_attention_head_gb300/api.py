@@ -308,13 +308,15 @@ def _strides3(t):
 
 def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
             scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
-            reverse: bool = False, cu_seqlens=None, chunked: bool = True
-            ) -> Tuple[Tensor, Tensor]:
+            reverse: bool = False, cu_seqlens=None, chunked: bool = True,
+            keep_operands: bool = False):
     """Gated forward (GLA): row a of the state decays by exp(g_gamma[h] + g_t[a]) at
-    token t.  q, k, g: [B,T,H,D]; v: [B,T,H,E].  Returns (o, final_state).
-    chunked=False withholds the workspace, so that every (sequence, head) runs
-    token by token (otherwise the chunked tensor-core form runs where it
-    applies)."""
+    token t.  q, k, g: [B,T,H,D]; v: [B,T,H,E].  Returns (o, final_state), and with
+    keep_operands=True (o, final_state, operands): operands is the workspace holding
+    the chunked form's rescaled q, k when the call ran that form (else None), to be
+    passed once to gla_bwd on the same inputs.  chunked=False withholds the
+    workspace, so that every (sequence, head) runs token by token (otherwise the
+    chunked tensor-core form runs where it applies)."""
     _check_tokens(q, k, v)
     if k.shape[2] != q.shape[2]:
         raise ValueError("the gated form needs keys and values with the queries' heads")
@@ -336,17 +338,22 @@ def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
     nbytes = (int(N.lib().la_gla_fwd_workspace_size(ctypes.byref(dims), _dtype_code(q),
                                                     packed.host_ptr())) if chunked else 0)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+    written = ctypes.c_int32(0)
     st = N.lib().la_gla_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                             _ptr(g), gs, _ptr(gg), scale, _ptr(init), int(bool(reverse)),
                             _ptr(packed.dev), packed.host_ptr(), _ptr(out), _ptr(fin),
-                            _ptr(ws), nbytes, _stream(dev))
+                            _ptr(ws), nbytes, ctypes.byref(written), _stream(dev))
     N.check(st)
+    if keep_operands:
+        return out, fin, (ws if written.value else None)
     return out, fin
 
 
 def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_final_state=None,
-            reverse=False, cu_seqlens=None, want_d_initial_state=True):
-    """Backward of gla_fwd: returns (dq, dk, dv, dg, d_initial_state)."""
+            reverse=False, cu_seqlens=None, want_d_initial_state=True, operands=None):
+    """Backward of gla_fwd: returns (dq, dk, dv, dg, d_initial_state).  operands: what
+    gla_fwd(..., keep_operands=True) returned for the same inputs, or None; it is
+    consumed (used as scratch)."""
     q, k, v, do, dev, packed, gg, scale, init, dfin, Nst = _bwd_prep(
         q, k, v, do, torch.zeros(q.shape[2]) if g_gamma is None else g_gamma, scale,
         initial_state, d_final_state, cu_seqlens)
@@ -358,14 +365,17 @@ def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_fina
     dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
                          dtype=torch.float32) if want_d_initial_state else None)
     dims = _dims(q, k, v, do, packed)
+    # with the forward's operands the workspace needs only the token-by-token part
     nbytes = int(N.lib().la_gla_workspace_size(ctypes.byref(dims), _dtype_code(q),
-                                              packed.host_ptr()))
+                                              packed.host_ptr(), int(operands is not None)))
+    fwd_bytes = operands.numel() if operands is not None else 0
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     st = N.lib().la_gla_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                             _ptr(do), _ptr(g), _strides3(g), _ptr(gg), scale, _ptr(init),
                             _ptr(dfin), int(bool(reverse)), _ptr(packed.dev), packed.host_ptr(),
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dinit),
-                            ctypes.c_void_p(ws.data_ptr()), nbytes, _stream(dev))
+                            ctypes.c_void_p(ws.data_ptr()), nbytes, _ptr(operands), fwd_bytes,
+                            _stream(dev))
     N.check(st)
     return dq, dk, dv, dg, dinit
 
@@ -373,10 +383,11 @@ def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_fina
 class _GatedLinearAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, init, gg, scale, reverse, cu):
-        o, fin = gla_fwd(q, k, v, g, gg, scale, init, reverse, cu)
+        o, fin, ops = gla_fwd(q, k, v, g, gg, scale, init, reverse, cu, keep_operands=True)
         ctx.save_for_backward(q, k, v, g, init, gg)
         ctx.scale, ctx.reverse, ctx.cu = scale, reverse, cu
         ctx.has_init = init is not None
+        ctx.ops = ops   # the chunked form's operands, reused once by the backward
         return o, fin
 
     @staticmethod
@@ -384,9 +395,11 @@ class _GatedLinearAttention(torch.autograd.Function):
         q, k, v, g, init, gg = ctx.saved_tensors
         if do is None:
             do = torch.zeros(q.shape[:3] + v.shape[3:], dtype=v.dtype, device=v.device)
+        ops, ctx.ops = ctx.ops, None
         dq, dk, dv, dg, dinit = gla_bwd(q, k, v, do.to(v.dtype), g, gg, ctx.scale,
                                         init if ctx.has_init else None, dfin, ctx.reverse,
-                                        ctx.cu, want_d_initial_state=ctx.has_init)
+                                        ctx.cu, want_d_initial_state=ctx.has_init,
+                                        operands=ops)
         return (dq, dk, dv, dg.to(g.dtype), (dinit if ctx.has_init else None), None, None,
                 None, None)
 

@@ -915,8 +915,10 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
                      const float *g_gamma, float scale, const float *initial_state,
                      int32_t reverse, const int32_t *cu_seqlens, const int32_t *cu_seqlens_host,
                      void *o, float *final_state, void *workspace, size_t workspace_bytes,
-                     void *stream)
+                     int32_t *operands_written, void *stream)
 {
+    if (operands_written)
+        *operands_written = 0;
     g_msg.clear();
     cudaStream_t s = (cudaStream_t)stream;
     Problem P;
@@ -994,6 +996,8 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
         if (e == cudaSuccess) {
             a.gla_flags = flags;
             a.gla_flag_run = 1;
+            if (operands_written)
+                *operands_written = 1;
         } else if (e != cudaErrorNotSupported) {
             return cuda_fail(e, "gated tensor-core sweep launch");
         }
@@ -1001,13 +1005,16 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     return short_run(a, false, s);
 }
 
-size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *cu_seqlens_host)
+size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *cu_seqlens_host,
+                             int32_t with_forward_operands)
 {
     Problem P;
     std::string keep = g_msg;
     la_status st = check_dims(dims, dtype, cu_seqlens_host, cu_seqlens_host, nullptr, &P);
     g_msg = keep;
-    return st == LA_OK ? gla_bwd_bytes(P) + gla_fwd_layout(P, dtype, true).total : 0;
+    if (st != LA_OK)
+        return 0;
+    return gla_bwd_bytes(P) + (with_forward_operands ? 0 : gla_fwd_layout(P, dtype, true).total);
 }
 
 la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
@@ -1016,7 +1023,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
                      const float *d_final_state, int32_t reverse, const int32_t *cu_seqlens,
                      const int32_t *cu_seqlens_host, void *dq, void *dk, void *dv, float *dg,
                      float *d_initial_state, void *workspace, size_t workspace_bytes,
-                     void *stream)
+                     void *fwd_workspace, size_t fwd_workspace_bytes, void *stream)
 {
     g_msg.clear();
     cudaStream_t s = (cudaStream_t)stream;
@@ -1062,10 +1069,15 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
                                 (reinterpret_cast<uintptr_t>(dg) & 7) == 0 &&
                                 g_strides[0] % 2 == 0 && g_strides[1] % 2 == 0 &&
                                 g_strides[2] % 2 == 0;
-        if (w.total && workspace_bytes >= need_ws + w.total && aligned && gate_pairs) {
-            uint8_t *ws = static_cast<uint8_t *>(workspace) + need_ws;
+        // the forward's operands, when the caller kept them
+        const bool ready = w.total && fwd_workspace &&
+                           (reinterpret_cast<uintptr_t>(fwd_workspace) & 255) == 0 &&
+                           fwd_workspace_bytes >= w.total;
+        if (w.total && (ready || workspace_bytes >= need_ws + w.total) && aligned && gate_pairs) {
+            uint8_t *ws = ready ? static_cast<uint8_t *>(fwd_workspace)
+                                : static_cast<uint8_t *>(workspace) + need_ws;
             int *fl = reinterpret_cast<int *>(ws + w.flags);
-            cudaError_t e = cudaMemsetAsync(fl, 0, (size_t)P.N * P.H * 4, s);
+            cudaError_t e = ready ? cudaSuccess : cudaMemsetAsync(fl, 0, (size_t)P.N * P.H * 4, s);
             if (e != cudaSuccess)
                 return cuda_fail(e, "gated backward flags");
             pa.N = P.N;
@@ -1098,7 +1110,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             pa.Ft = Ft;
             pa.dF = d_final_state;
             pa.E = P.E;
-            if ((e = la::gla_prepare(pa, s)) != cudaSuccess)
+            if (!ready && (e = la::gla_prepare(pa, s)) != cudaSuccess)
                 return cuda_fail(e, "gated backward operands");
             const int64_t dsh = P.D, dst = (int64_t)P.H * P.D, dsb = dst * P.T;
             const la::Tok tq{pa.xq, dsb, dst, dsh, 1}, tk{pa.yk, dsb, dst, dsh, 1};

@@ -203,3 +203,16 @@ def test_gated_forward_workspace_size(lib):
     assert lib.la_gla_fwd_workspace_size(ctypes.byref(_dims(T=16, D=128, E=128)), 0, None) == 0
     assert lib.la_gla_fwd_workspace_size(ctypes.byref(_dims(T=300, D=64)), 0, None) == 0
     assert lib.la_gla_fwd_workspace_size(ctypes.byref(_dims(T=300, D=128, E=64)), 0, None) > 0
+
+
+def test_gated_backward_workspace_with_forward_operands(lib):
+    # with the forward's operands the backward needs only its token-by-token
+    # part; the difference is the forward's workspace where the chunked
+    # backward applies (D = E = 128), nothing otherwise
+    d = _dims(B=2, T=300, H=3, D=128, E=128)
+    full = lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 0)
+    part = lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 1)
+    assert full - part == lib.la_gla_fwd_workspace_size(ctypes.byref(d), 0, None) > 0
+    d64 = _dims(B=2, T=300, H=3, D=128, E=64)
+    assert lib.la_gla_workspace_size(ctypes.byref(d64), 0, None, 0) == \
+        lib.la_gla_workspace_size(ctypes.byref(d64), 0, None, 1) > 0

@@ -47,7 +47,7 @@ def _dg_condition(x, ref, reverse):
 def _compare_gla(got, ref, x, reverse, tol, label):
     """dg against the oracle relative to _dg_condition; every other output by
     the usual per-slice maximum relative error."""
-    rest = {k: v for k, v in ref.items() if k != "dg"}
+    rest = {k: v for k, v in ref.items() if k != "dg" and k in got}
     compare({k: got[k] for k in rest}, rest, tol, cu=x["cu_seqlens"], label=label)
     if "dg" not in ref:
         return
@@ -215,3 +215,45 @@ def test_gated_chunked_strong_gates_run_token_by_token():
         got, ref = _fwd_only(x, reverse)
         tok, _ = _fwd_only(x, reverse, chunked=False)
         compare(tok, ref, TOL[torch.bfloat16], label="token rev=%d" % reverse)
+
+
+def test_gated_backward_reuses_forward_operands():
+    # gla_fwd(keep_operands=True) hands its rescaled q, k to gla_bwd, which
+    # skips computing them; out-of-range pairs (head 1) keep their flags
+    x = _inputs(2, 400, 3, 128, 128, torch.bfloat16, seed=12)
+    x["g"][:, :, 1] = -3.0
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    for reverse in (False, True):
+        o, fin, ops = la.gla_fwd(d["q"], d["k"], d["v"], d["g"], d["g_gamma"], d["scale"],
+                                 d["initial_state"], reverse, keep_operands=True)
+        assert ops is not None
+        dq, dk, dv, dg, dinit = la.gla_bwd(d["q"], d["k"], d["v"], d["do"], d["g"],
+                                           d["g_gamma"], d["scale"], d["initial_state"],
+                                           d["d_final_state"], reverse, operands=ops)
+        torch.cuda.synchronize()
+        la.get_device_error()
+        got = dict(o=o, final_state=fin, dq=dq, dk=dk, dv=dv, dg=dg, d_initial_state=dinit)
+        _compare_gla({k: v.cpu() for k, v in got.items()}, _oracle(x, reverse), x, reverse,
+                     TOL[torch.bfloat16], "reused operands rev=%d" % reverse)
+    # the token-by-token forward leaves no operands to reuse
+    _, _, none = la.gla_fwd(d["q"], d["k"], d["v"], d["g"], d["g_gamma"], d["scale"],
+                            keep_operands=True, chunked=False)
+    assert none is None
+
+
+def test_gated_autograd_chunked_bf16():
+    # recurrent_gla's autograd path at the chunked form's sizes (the backward
+    # reuses the forward's operands)
+    x = _inputs(1, 300, 2, 128, 128, torch.bfloat16, seed=13)
+    q, k, v, g = (x[n].cuda().requires_grad_() for n in ("q", "k", "v", "g"))
+    o, fin = la.recurrent_gla(q, k, v, g=g, g_gamma=x["g_gamma"], softmax_scale=x["scale"])
+    ((o.float() * x["do"].cuda().float()).sum()).backward()
+    torch.cuda.synchronize()
+    ref_o, ref_f = oracle.gla_forward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"], x["scale"])
+    rq, rk, rv, rg, _ = oracle.gla_backward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"],
+                                            x["scale"], x["do"])
+    y = dict(x, initial_state=None, d_final_state=None)
+    _compare_gla(dict(o=o.detach().cpu(), dq=q.grad.cpu(), dk=k.grad.cpu(), dv=v.grad.cpu(),
+                      dg=g.grad.cpu()),
+                 dict(o=ref_o, final_state=ref_f, dq=rq, dk=rk, dv=rv, dg=rg), y, False,
+                 TOL[torch.bfloat16], "autograd chunked")
