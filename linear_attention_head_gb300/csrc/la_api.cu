@@ -446,6 +446,19 @@ la_status run_backward_type(const la::SweepArgs &a, cudaStream_t s)
     return e == cudaSuccess ? LA_OK : cuda_fail(e, "backward-type sweep launch");
 }
 
+// The sweep's final states only (the sequence split's first pass): the
+// tensor-core state-only mode where it applies, else the full sweep (whose
+// outputs the second pass overwrites).
+la_status run_states(const la::SweepArgs &a, bool bwd, cudaStream_t s)
+{
+    cudaError_t e = cudaErrorNotSupported;
+    if (a.max_len > la::SHORT_MAX_T && la::tc_sweep_supported(a))
+        e = la::tc_state_sweep(a, bwd, s);
+    if (e == cudaErrorNotSupported)
+        return bwd ? run_backward_type(a, s) : run_forward_type(a, s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "state sweep launch");
+}
+
 la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *k, const void *v,
                  const void *d_o, const float *g_gamma, float scale, const float *init,
                  int32_t reverse, const int32_t *cu, const int32_t *order, void *dq, cudaStream_t s,
@@ -467,7 +480,7 @@ la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *
     to_segments(&a, P, *S, *b);
     a.s_in = la::StateIn{nullptr, 0, 0};
     a.s_out = la::StateOut{b->W, P.D, 1};
-    la_status st = run_forward_type(a, s);
+    la_status st = run_states(a, false, s);
     if (st == LA_OK)
         st = scan(scan_args(P, *b, g_gamma, P.E, P.D, la::StateIn{init, 1, P.E},
                             la::StateOut{nullptr, 0, 0}, reverse != 0),
@@ -506,7 +519,7 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
         to_segments(&a, P, *S, *b);
         a.s_in = la::StateIn{nullptr, 0, 0};
         a.s_out = la::StateOut{b->W, P.E, 1};
-        st = run_backward_type(a, s);
+        st = run_states(a, true, s);
         if (st == LA_OK)
             st = scan(scan_args(P, *b, g_gamma, P.D, P.E, la::StateIn{dfinal, P.E, 1},
                                 la::StateOut{dinit, P.E, 1}, reverse == 0),
@@ -589,7 +602,7 @@ la_status la_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *
     to_segments(&a, P, S, b);
     a.s_in = la::StateIn{nullptr, 0, 0};
     a.s_out = la::StateOut{b.W, P.E, 1};
-    if ((st = run_forward_type(a, s)))
+    if ((st = run_states(a, false, s)))
         return st;
     if ((st = scan(scan_args(P, b, g_gamma, P.D, P.E, la::StateIn{initial_state, P.E, 1},
                              la::StateOut{final_state, P.E, 1}, reverse != 0),

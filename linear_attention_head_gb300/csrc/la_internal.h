@@ -117,6 +117,10 @@ cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s);
 // cudaErrorNotSupported when the tensor maps cannot be built.
 cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, const Tok &y,
                          const Tok &z, cudaStream_t s);
+// The final states of a sweep alone (its outputs are not written; X is not
+// read): the tensor-core kernel's state-only mode, for the sequence split's
+// first pass.  Eligibility as tc_sweep_supported.
+cudaError_t tc_state_sweep(const SweepArgs &a, bool bwd, cudaStream_t s);
 
 // Calls whose longest sequence has at most this many tokens run the
 // token-by-token kernels (la_token.cu) instead of the chunked ones.

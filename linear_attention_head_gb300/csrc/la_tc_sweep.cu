@@ -320,7 +320,10 @@ __device__ __forceinline__ void zero_row(uint8_t *row_base)
 // chunk's factor and the next chunk's -- exp(B - r) then exp(r) going
 // forward, exp(r) then exp(B - r) going backward -- on its rows (GLA 1: the
 // gated key channels are the state's rows) or columns (GLA 2).
-template <int E, bool BWD, int GLA>
+// SO (state only): the sweep's final states alone (the sequence split's first
+// pass): Y and Z are loaded, the state update runs, X, the scores, P Z, the
+// inter term and the output are skipped.
+template <int E, bool BWD, int GLA, bool SO = false>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_constant__ TcParams P)
 {
     using L = TcLayout<E>;
@@ -424,6 +427,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     break;
                 const int t0 = (int)(bos + chunk_t0(c));
                 uint8_t *st = sm + s * L::STAGE;
+                if (SO) {
+                    // Y and Z, both free once the chunk's state update is done
+                    mbar_arrive_expect_tx(&full[s], L::YB + L::ZB);
+#pragma unroll
+                    for (int b = 0; b < TC_D / 64; ++b)
+                        tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, hy, t0,
+                                    (int)row);
+#pragma unroll
+                    for (int b = 0; b < E / 64; ++b)
+                        tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s], 64 * b,
+                                    hz, t0, (int)row);
+                    ++issued;
+                    continue;
+                }
                 // X and Y first: their slots are free once the chunk's state
                 // update is done and the next scores need them; the Z slot
                 // only once the output tile staged in it has left
@@ -450,7 +467,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // every copy this thread issued has landed before the CTA may exit
             for (int c = issued > TC_NST ? issued - TC_NST : 0; c < issued; ++c) {
                 drain_wait(&full[c % TC_NST], (c / TC_NST) & 1);
-                drain_wait(&zfull[c % TC_NST], (c / TC_NST) & 1);
+                if (!SO)
+                    drain_wait(&zfull[c % TC_NST], (c / TC_NST) & 1);
             }
         }
     } else if (warp == 1) {
@@ -467,6 +485,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 const uint32_t xa = sbase + s * L::STAGE, ya = xa + L::XB, za = ya + L::YB;
                 if (!bwait(&full[s], (c / TC_NST) & 1, abort_flag))
                     break;
+                if (SO) {
+                    // the state update alone, once the state is pre-scaled
+                    // and Y scaled
+                    if (!bwait(s_ready, c & 1, abort_flag) || !bwait(p_ready, c & 1, abort_flag))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < TC_C / 16; ++kk)
+                        mma_ss(tm + TM_S, sdesc_sw128(ya + kk * 2048, TC_C * 128, 1024),
+                               sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_yz, 1);
+                    mma_commit(ds_full);
+                    mma_commit(&empty[s]);
+                    any = true;
+                    continue;
+                }
                 if (c > 0 && !bwait(pv_done, (c - 1) & 1, abort_flag))
                     break;
                 tc_fence_after();
@@ -545,11 +578,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 const int s = c % TC_NST;
                 const int Lc = chunk_len(c);
                 bool ok = warp_all(bwait(&full[s], (c / TC_NST) & 1, abort_flag));
-                if (ok)
+                if (ok && !SO)
                     ok = warp_all(bwait(sc_full, c & 1, abort_flag));
+                // state only: no scores hold this group in step with the MMA
+                // issuer, so it waits for the previous state update, else it
+                // could complete p_ready twice before the issuer's wait on it
+                // and the parity of that wait would read the wrong phase
+                if (ok && SO && c > 0)
+                    ok = warp_all(bwait(ds_full, (c - 1) & 1, abort_flag));
                 if (!ok)
                     break;
                 tc_fence_after();
+                if (SO) {
+                    // column factor for the state update, applied to row i of Y
+                    float lc = 0.f;
+                    if (i < Lc) {
+                        const int pi = rev ? Lc - 1 - i : i;
+                        lc = BWD ? scale * pw[pi + 1] : pw[Lc - 1 - pi];
+                    }
+                    scale_row_sw128(sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128, i, lc);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(p_ready);
+                    continue;
+                }
                 uint32_t ra[32], rb[32];
                 const uint32_t col = tm + lane_off + TM_SC + j0;
                 // block kinds are warp-uniform: 0 zero, 1 rank one, 2 diagonal
@@ -699,7 +751,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         }
                         continue;
                     }
-                    if (!GLA)
+                    if (!GLA && !SO)
                         store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
@@ -722,7 +774,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // ------------------------------------------------------- O group
             __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.out.p) + row * a.out.sb +
                                    (int64_t)h * a.out.sh;
-            for (int c = 0; c < nc; ++c) {
+            for (int c = 0; c < (SO ? 0 : nc); ++c) {
                 const int s = c % TC_NST;
                 const int Lc = chunk_len(c);
                 if (!warp_all(bwait(o_full, c & 1, abort_flag)))
@@ -838,23 +890,26 @@ bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t 
 // Tile roles: X rows (scores = X Y^T, inter term X S), Y columns (scaled in
 // place for the state update), Z values.  Forward: (X, Y, Z) = (q, k, v);
 // backward: (k, q, w).
-template <int E, bool BWD, int GLA>
+template <int E, bool BWD, int GLA, bool SO = false>
 cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullptr)
 {
     TcParams p;
     // tile roles; the gated form names its three operands itself
     const Tok x = xyz ? xyz[0] : (BWD ? a.k : a.q), y = xyz ? xyz[1] : (BWD ? a.q : a.k);
     const Tok z = xyz ? xyz[2] : a.v;
-    if (!make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh, TC_C, x.hdiv) ||
+    // state only: no X, no output (their maps are not used)
+    if ((!SO && !make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh, TC_C, x.hdiv)) ||
         !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh, TC_C, y.hdiv) ||
         !make_map(&p.mz, z.p, E, a, z.sb, z.st, z.sh, TC_C, z.hdiv) ||
-        !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh, 32))
+        (!SO && !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh, 32)))
         return cudaErrorNotSupported;
+    if (SO)
+        p.mx = p.mo = p.my;
     p.a = a;
     p.dx = x.hdiv;
     p.dy = y.hdiv;
     p.dz = z.hdiv;
-    auto kern = tc_sweep_kernel<E, BWD, GLA>;
+    auto kern = tc_sweep_kernel<E, BWD, GLA, SO>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            TcLayout<E>::DYN);
     if (err != cudaSuccess)
@@ -907,6 +962,15 @@ cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, 
     return cols ? launch_tc<128, false, 2>(a, s, xyz)
                 : (a.E == 128 ? launch_tc<128, false, 1>(a, s, xyz)
                               : launch_tc<64, false, 1>(a, s, xyz));
+}
+
+cudaError_t tc_state_sweep(const SweepArgs &a, bool bwd, cudaStream_t s)
+{
+    if (a.N == 0)
+        return cudaSuccess;
+    if (bwd)
+        return a.E == 128 ? launch_tc<128, true, 0, true>(a, s) : launch_tc<64, true, 0, true>(a, s);
+    return a.E == 128 ? launch_tc<128, false, 0, true>(a, s) : launch_tc<64, false, 0, true>(a, s);
 }
 
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err)
