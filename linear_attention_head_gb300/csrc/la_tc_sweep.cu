@@ -86,7 +86,8 @@ template <int E> struct TcLayout {
     static constexpr int PWOFF = MOFF + NBAR * 8;
     static constexpr int CFOFF = (PWOFF + (TC_C + 1) * 4 + 15) / 16 * 16;   // 32 column factors
     static constexpr int DTOFF = CFOFF + 32 * 4;                            // 64 diagonal factors
-    static constexpr int SLOTOFF = DTOFF + 64 * 4;
+    static constexpr int COLNOFF = DTOFF + 64 * 4;                        // 128 column factors (gated)
+    static constexpr int SLOTOFF = COLNOFF + 128 * 4;
     static constexpr int ABORTOFF = SLOTOFF + 4;
     static constexpr int BYTES = ABORTOFF + 4;
     static constexpr int DYN = BYTES + 1024;           // slack for 1024-byte alignment
@@ -682,8 +683,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             const int64_t vrow = ((int64_t)n * a.H + h) * a.gla_ncmax;
             auto vidx = [&](int pc) { return (vrow + pc) * TC_D + i; };
             const float *vo = BWD ? a.gla_er : a.gla_u, *vn = BWD ? a.gla_u : a.gla_er;
-            // GLA 2: this step's per-column factors, shared by the S group
+            // GLA 2: this step's per-column factors, shared by the S group:
+            // the chunk's own (colf) and the next chunk's (coln)
             float *colf = pw;
+            float *coln = reinterpret_cast<float *>(sm + L::COLNOFF);
             auto sg_sync = [] { asm volatile("bar.sync 2, %0;" ::"n"(TC_SG) : "memory"); };
             if (nc == 0) {
                 state_copy(a.s_in, a.s_out, sb, i, E);
@@ -705,11 +708,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 const bool last = c + 1 == nc;
                 // out = fo x (last chunk); else the copy and TMEM get ft x
                 // (gated form) or x and gn x
-                float fo = 1.f, ft = last ? 1.f : pw[chunk_len(c + 1)];
+                // gated form: the chunk's factor fo, then the next chunk's fn,
+                // applied one after the other (their product can underflow
+                // where each step stays in range)
+                float fo = 1.f, fn = 1.f, ft = last ? 1.f : pw[chunk_len(c + 1)];
                 if (GLA) {
                     fo = GLA == 1 || i < E ? vo[vidx(flip ? nc - 1 - c : c)] : 1.f;
                     if (!last)
-                        ft = fo * (GLA == 1 || i < E ? vn[vidx(flip ? nc - 2 - c : c + 1)] : 1.f);
+                        fn = GLA == 1 || i < E ? vn[vidx(flip ? nc - 2 - c : c + 1)] : 1.f;
                 }
                 if (GLA == 2) {
                     // one decision for the whole S group: its barriers below
@@ -724,8 +730,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                                  : "memory");
                     if (!all)
                         break;
-                    if (i < E)
-                        colf[i] = last ? fo : ft;
+                    if (i < E) {
+                        colf[i] = fo;
+                        coln[i] = fn;
+                    }
                     sg_sync();
                 } else if (!warp_all(bwait(ds_full, c & 1, abort_flag))) {
                     break;
@@ -755,10 +763,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
-                        const float f0 = GLA == 2 ? colf[64 * eb + k] : gn;
-                        const float f1 = GLA == 2 ? colf[64 * eb + 32 + k] : gn;
-                        ra[k] = __float_as_uint(f0 * __uint_as_float(ra[k]));
-                        rb[k] = __float_as_uint(f1 * __uint_as_float(rb[k]));
+                        if (GLA) {
+                            const float o0 = GLA == 2 ? colf[64 * eb + k] : fo;
+                            const float o1 = GLA == 2 ? colf[64 * eb + 32 + k] : fo;
+                            const float n0 = GLA == 2 ? coln[64 * eb + k] : fn;
+                            const float n1 = GLA == 2 ? coln[64 * eb + 32 + k] : fn;
+                            ra[k] = __float_as_uint(n0 * (o0 * __uint_as_float(ra[k])));
+                            rb[k] = __float_as_uint(n1 * (o1 * __uint_as_float(rb[k])));
+                        } else {
+                            ra[k] = __float_as_uint(gn * __uint_as_float(ra[k]));
+                            rb[k] = __float_as_uint(gn * __uint_as_float(rb[k]));
+                        }
                     }
                     if (GLA)
                         store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);

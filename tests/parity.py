@@ -119,3 +119,51 @@ def take_out(got, heads, rows=None):
             s = s[list(rows)]
         y[n] = s
     return y
+
+
+def dg_condition(x, ref, reverse):
+    """Per (sequence, head): the largest running sum, in the order dg sums them
+    (from the last processed token back), of |q dq| + |k dk| per channel, plus
+    sum_e |F dF| -- the scale of dg's rounding error, whatever dg's own size
+    (dg is a sum of differences of rounded products, so cancellation can make
+    it small while its error is not)."""
+    q, k = (np.asarray(x[n].float().numpy(), dtype=np.float64) for n in ("q", "k"))
+    dq, dk = np.asarray(ref["dq"], dtype=np.float64), np.asarray(ref["dk"], dtype=np.float64)
+    term = np.abs(q * dq) + np.abs(k * dk)                     # [B, T, H, D]
+    fin = np.asarray(ref["final_state"], dtype=np.float64)
+    dfin = x.get("d_final_state")
+    fdf = (np.abs(fin * np.asarray(dfin.numpy(), dtype=np.float64)).sum(-1)
+           if dfin is not None else np.zeros(fin.shape[:3]))  # [N, H, D]
+    cu = x["cu_seqlens"]
+    spans = ([(0, b, 0, q.shape[1]) for b in range(q.shape[0])] if cu is None else
+             [(n, 0, int(cu[n]), int(cu[n + 1])) for n in range(len(cu) - 1)])
+    cond = {}
+    for n, row, a, b in spans:
+        seg = term[row, a:b]                                   # [L, H, D]
+        order = seg if reverse else seg[::-1]                  # dg sums from the last processed
+        run = np.cumsum(order, axis=0) + fdf[n if cu is not None else row][None]
+        cond[(n if cu is not None else row)] = run.max(axis=(0, 2)) if b > a else fdf[n].max(-1)
+    return cond
+
+
+def compare_gated(got, ref, x, reverse, tol, label):
+    """dg against the oracle relative to dg_condition; every other output by
+    the usual per-slice maximum relative error."""
+    rest = {k: v for k, v in ref.items() if k != "dg" and k in got}
+    compare({k: got[k] for k in rest}, rest, tol, cu=x["cu_seqlens"], label=label)
+    if "dg" not in ref:
+        return
+    cond = dg_condition(x, ref, reverse)
+    d = np.abs(np.asarray(got["dg"].double().numpy()) - np.asarray(ref["dg"], dtype=np.float64))
+    cu = x["cu_seqlens"]
+    worst = 0.0
+    for key, c in cond.items():
+        if cu is None:
+            e = d[key].max(axis=(0, 2))
+        else:
+            a, b = int(cu[key]), int(cu[key + 1])
+            if b == a:
+                continue
+            e = d[0, a:b].max(axis=(0, 2))
+        worst = max(worst, float((e / np.maximum(c, 1e-30)).max()))
+    assert worst <= tol, "%s: dg error %.3e of its condition above %.1e" % (label, worst, tol)
