@@ -203,9 +203,20 @@ __device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i
     for (int p8 = 0; p8 < E_ / 8; ++p8) {
         float x[8];
         const float *src = sin.p ? sin.p + base + i * sin.rs + (8 * p8) * sin.cs : nullptr;
+        if (src && sin.cs == 1 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+            // contiguous row: two 16-byte loads
+            const float4 lo = *reinterpret_cast<const float4 *>(src);
+            const float4 hi = *reinterpret_cast<const float4 *>(src + 4);
+            x[0] = lo.x, x[1] = lo.y, x[2] = lo.z, x[3] = lo.w;
+            x[4] = hi.x, x[5] = hi.y, x[6] = hi.z, x[7] = hi.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                x[k] = src ? src[k * sin.cs] : 0.f;
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            x[k] = (src ? src[k * sin.cs] : 0.f) * (colf ? colf[8 * p8 + k] : 1.f);
+            x[k] *= colf ? colf[8 * p8 + k] : 1.f;
         *reinterpret_cast<uint4 *>(sbf + (p8 >> 3) * (TC_D * 128) + (((p8 & 7) ^ (i & 7)) << 4)) =
             make_uint4(pack_bf16x2(c0 * x[0], c0 * x[1]), pack_bf16x2(c0 * x[2], c0 * x[3]),
                        pack_bf16x2(c0 * x[4], c0 * x[5]), pack_bf16x2(c0 * x[6], c0 * x[7]));
@@ -753,8 +764,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                             for (int k = 0; k < 32; ++k) {
                                 const float f0 = GLA == 2 ? colf[64 * eb + k] : fo;
                                 const float f1 = GLA == 2 ? colf[64 * eb + 32 + k] : fo;
-                                dst[k * a.s_out.cs] = f0 * __uint_as_float(ra[k]);
-                                dst[(k + 32) * a.s_out.cs] = f1 * __uint_as_float(rb[k]);
+                                ra[k] = __float_as_uint(f0 * __uint_as_float(ra[k]));
+                                rb[k] = __float_as_uint(f1 * __uint_as_float(rb[k]));
+                            }
+                            if (a.s_out.cs == 1 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                                // contiguous row: 16-byte stores
+#pragma unroll
+                                for (int k4 = 0; k4 < 8; ++k4) {
+                                    *reinterpret_cast<uint4 *>(dst + 4 * k4) =
+                                        make_uint4(ra[4 * k4], ra[4 * k4 + 1], ra[4 * k4 + 2],
+                                                   ra[4 * k4 + 3]);
+                                    *reinterpret_cast<uint4 *>(dst + 32 + 4 * k4) =
+                                        make_uint4(rb[4 * k4], rb[4 * k4 + 1], rb[4 * k4 + 2],
+                                                   rb[4 * k4 + 3]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) {
+                                    dst[k * a.s_out.cs] = __uint_as_float(ra[k]);
+                                    dst[(k + 32) * a.s_out.cs] = __uint_as_float(rb[k]);
+                                }
                             }
                         }
                         continue;
