@@ -106,6 +106,23 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
     const int64_t tb = bos + t0 + (np == 0 ? 0 : (a.reverse ? Lc - 1 - p0 : p0));
     const int64_t ts = a.reverse ? -1 : 1;
 
+    // The operands' q, k rows into L2 while the gates are summed: the lane
+    // that starts each 128-byte line of a warp's channels asks for it.  (The
+    // rescaling mode reads four tensors; prefetching them there was slower.)
+    if (!UNDO) {
+        const int esz = (int)sizeof(T);
+        if ((c * esz) % 128 == 0) {
+            const int64_t qo = row * a.sb + (int64_t)h * a.sh + c;
+            const char *qr = reinterpret_cast<const char *>(static_cast<const T *>(a.q) + qo);
+            const char *kr = reinterpret_cast<const char *>(static_cast<const T *>(a.k) + qo);
+            for (int j = 0; j < np; ++j) {
+                const int64_t off = (tb + j * ts) * a.st * esz;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + off));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + off));
+            }
+        }
+    }
+
     // pass 1: this group's gates and their running sums (constant past its end)
     float2 b[PT];
     {
