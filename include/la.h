@@ -333,9 +333,11 @@ size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype,
  * every stream of the current device. */
 la_status la_get_device_error(void *stream);
 
-/* Diagnostic, for testing error reporting: with on != 0, the next
- * tensor-core launch made from this host thread withholds one internal
- * hand-off between its warps, so that a bounded on-device wait runs out
+/* Diagnostic, for testing error reporting: with on != 0, the next launch of
+ * a kernel with internal hand-offs (the tensor-core sweeps, the streamed
+ * decode kernel) made from this host thread withholds one of them -- between
+ * its warps, or the copy of a state block -- so that a bounded on-device wait
+ * runs out
  * (after about 2 s); the kernel then stops, frees what it holds and returns,
  * its outputs are undefined, and la_get_device_error reports LA_ERR_TIMEOUT.
  * The switch resets itself after that launch and is off by default. */

@@ -416,8 +416,14 @@ la::SweepArgs base_args(const Problem &P, int32_t dtype, const int32_t *cu, cons
 la_status run_forward_type(const la::SweepArgs &a, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    if (a.max_len <= la::SHORT_MAX_T)
-        e = la::short_forward_sweep(a, s);
+    if (a.max_len <= la::SHORT_MAX_T) {
+        la::SweepArgs b = a;
+        b.withhold_handoff = g_withhold;
+        bool streamed = false;
+        e = la::short_forward_sweep(b, s, &streamed);
+        if (streamed)   // the only token-by-token kernel with hand-offs to withhold
+            g_withhold = 0;
+    }
     if (e == cudaErrorNotSupported && la::tc_sweep_supported(a)) {
         la::SweepArgs b = a;
         b.withhold_handoff = g_withhold;

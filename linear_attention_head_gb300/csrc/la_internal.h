@@ -70,7 +70,7 @@ struct SweepArgs {
     TokOut out;               // forward-type: o (or dq); backward-type: dv (or dk)
     StateIn s_in;             // forward-type: initial state; backward-type: dL/dfinal
     StateOut s_out;           // forward-type: final state; backward-type: dL/dinitial
-    int withhold_handoff;     // diagnostic: tensor-core kernels skip one hand-off
+    int withhold_handoff;     // diagnostic: the tensor-core and streamed decode kernels skip one hand-off
     int64_t max_len;          // longest sequence (T when dense)
     Gate gate;                // per-key log-decay gate, or p == nullptr
     int64_t prefetch_ctas = 0;  // token-by-token kernels: L2 prefetch distance in CTAs
@@ -141,7 +141,8 @@ cudaError_t simt_backward_sweep(const SweepArgs &a, cudaStream_t s);
 // kernels that take a gate; cudaErrorNotSupported outside that range.  Used
 // for every gated call and for ungated calls whose longest sequence has at
 // most SHORT_MAX_T tokens.
-cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s);
+// (*streamed, when given: whether the streamed decode kernel ran.)
+cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s, bool *streamed = nullptr);
 cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s);
 // Reads (after synchronizing s) and clears the token kernels' device error
 // word (LA_ERR_TIMEOUT when a wait of the streamed decode kernel ran out).

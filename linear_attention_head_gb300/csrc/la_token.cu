@@ -798,10 +798,15 @@ __global__ void __launch_bounds__(MAXW * 32 + 32, 1) stream_kernel(SweepArgs a, 
     if (tid >= ncomp) {
         // ---- copy warp ----
         const int lane = tid - ncomp;
+        // diagnostic (la_debug_withhold_next_handoff): the first block is
+        // never copied, so the compute warps' bounded wait on it runs out
+        const int skip = a.withhold_handoff ? 1 : 0;
         int li = 0;
         bool ok = true;
         for (int hn = blockIdx.x; hn < heads; hn += gridDim.x, ++li) {
             const int buf = li % ns;
+            if (li < skip)
+                continue;
             if (lane == 0 && li >= ns) {
                 // the block ns heads back has left this buffer: store it
                 ok = tok_wait(&done[buf], ((li - ns) / ns) & 1, abort_flag);
@@ -877,7 +882,7 @@ __global__ void __launch_bounds__(MAXW * 32 + 32, 1) stream_kernel(SweepArgs a, 
         }
         if (!ok) {
             // no copy into this CTA's shared memory may outlive it
-            for (int lj = issued > ns ? issued - ns : 0; lj < issued; ++lj)
+            for (int lj = issued - ns > skip ? issued - ns : skip; lj < issued; ++lj)
                 tok_drain(&full[lj % ns], (lj / ns) & 1);
         }
         bulk_wait_all();
@@ -1032,11 +1037,7 @@ template <bool BWD> cudaError_t launch_token(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0 || a.H == 0)
         return cudaSuccess;
-    if (!BWD && a.D >= 1 && a.D <= 256 && a.E >= 1) {
-        const cudaError_t e = a.bf16 ? try_stream<__nv_bfloat16>(a, s) : try_stream<float>(a, s);
-        if (e != cudaErrorNotSupported)
-            return e;
-    }
+
     if (a.D < 1 || a.D > 256 || a.E < 1)
         return cudaErrorNotSupported;
     if ((int64_t)a.N * a.H * token_shape(a.D, a.E, 16).tiles > 0x7fffffff)
@@ -1050,8 +1051,18 @@ template <bool BWD> cudaError_t launch_token(const SweepArgs &a, cudaStream_t s)
 
 }  // namespace
 
-cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s)
+cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s, bool *streamed)
 {
+    if (streamed)
+        *streamed = false;
+    if (a.N != 0 && a.H != 0 && a.D >= 1 && a.D <= 256 && a.E >= 1) {
+        const cudaError_t e = a.bf16 ? try_stream<__nv_bfloat16>(a, s) : try_stream<float>(a, s);
+        if (e != cudaErrorNotSupported) {
+            if (streamed)
+                *streamed = e == cudaSuccess;
+            return e;
+        }
+    }
     return launch_token<false>(a, s);
 }
 
