@@ -16,9 +16,7 @@ the same workload.  Under torchrun (N > 1) every rank runs its own batch
 (weak scaling, no collective on the data path); rank 0 prints one JSON line.
 """
 import argparse
-import ctypes
 import json
-import math
 import os
 import statistics
 import subprocess

@@ -11,7 +11,6 @@ oracle then computes sampled (batch row, head) slices, which must match:
 - the gated form: gla_fwd + gla_bwd on b4 h32 n8192 d=e=128 bf16 with the
   bench's gate recipe (the chunked tensor-core form).
 """
-import math
 
 import pytest
 import torch
