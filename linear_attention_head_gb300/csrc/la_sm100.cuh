@@ -55,6 +55,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Block until every grid this launch depends on in its stream has completed
+// and its memory writes are visible (a no-op for a launch without the
+// programmatic-serialization attribute).
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the stream's next grid, when launched as a programmatic dependent, be
+// scheduled once every CTA of this grid has made this call or exited.
+__device__ __forceinline__ void grid_dep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- async proxy fences ---------------------------------------------------
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem()

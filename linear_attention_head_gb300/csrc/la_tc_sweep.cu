@@ -365,33 +365,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::ABORTOFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // work item: the rank-th sequence of the schedule (longest first when an
-    // order is given), one head per CTA
-    const int rank = blockIdx.x / a.H, h = blockIdx.x % a.H;
-    const int n = a.order ? a.order[rank] : rank;
-    int64_t row, bos, len;
-    if (a.cu) {
-        row = 0;
-        bos = a.cu[n];
-        len = (int64_t)a.cu[n + 1] - a.cu[n];
-    } else {
-        row = n;
-        bos = 0;
-        len = a.T;
-    }
-    // gated form: (sequence, head) pairs whose gates are out of range run
-    // token by token instead
-    if (GLA && a.gla_flags && a.gla_flags[(int64_t)n * a.H + h] != a.gla_flag_run)
-        return;
-    const int nc = (int)((len + TC_C - 1) / TC_C);
-    const bool rev = a.reverse != 0;
-    const bool flip = rev != BWD;   // chunk order and mask direction
-    // first token and valid length of the chunk processed c-th
-    auto chunk_t0 = [&](int c) { return (int64_t)(flip ? nc - 1 - c : c) * TC_C; };
-    auto chunk_len = [&](int c) {
-        const int64_t t0 = chunk_t0(c);
-        return (int)(len - t0 < TC_C ? len - t0 : TC_C);
-    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < TC_NST; ++i) {
@@ -425,6 +398,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tslot;
+    // The set-up above touches only this CTA's shared memory, its TMEM and the
+    // kernel parameters, so it overlaps the end of the stream's previous
+    // kernel; global memory is read and written only after that kernel is done.
+    grid_dep_wait();
+    grid_dep_launch_dependents();
+
+    // work item: the rank-th sequence of the schedule (longest first when an
+    // order is given), one head per CTA
+    const int rank = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    const int n = a.order ? a.order[rank] : rank;
+    int64_t row, bos, len;
+    if (a.cu) {
+        row = 0;
+        bos = a.cu[n];
+        len = (int64_t)a.cu[n + 1] - a.cu[n];
+    } else {
+        row = n;
+        bos = 0;
+        len = a.T;
+    }
+    // gated form: (sequence, head) pairs whose gates are out of range run
+    // token by token instead
+    if (GLA && a.gla_flags && a.gla_flags[(int64_t)n * a.H + h] != a.gla_flag_run) {
+        if (warp == 1)
+            tmem_dealloc(tm, TM_COLS);
+        return;
+    }
+    const int nc = (int)((len + TC_C - 1) / TC_C);
+    const bool rev = a.reverse != 0;
+    const bool flip = rev != BWD;   // chunk order and mask direction
+    // first token and valid length of the chunk processed c-th
+    auto chunk_t0 = [&](int c) { return (int64_t)(flip ? nc - 1 - c : c) * TC_C; };
+    auto chunk_len = [&](int c) {
+        const int64_t t0 = chunk_t0(c);
+        return (int)(len - t0 < TC_C ? len - t0 : TC_C);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -958,8 +967,23 @@ cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullp
                                            TcLayout<E>::DYN);
     if (err != cudaSuccess)
         return err;
-    kern<<<(unsigned)((int64_t)a.N * a.H), TC_THREADS, TcLayout<E>::DYN, s>>>(p);
+    // programmatic dependent launch: the CTAs may be scheduled, and run their
+    // set-up, while the stream's previous kernel drains (the kernel waits for
+    // it before touching global memory)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)a.N * a.H));
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = TcLayout<E>::DYN;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kern, p);
     note_launch();
+    if (err != cudaSuccess)
+        return err;
     return cudaGetLastError();
 }
 
