@@ -16,7 +16,7 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests are skipped when no GPU is visible; on a GPU machine the CUDA path
+    # GPU tests are skipped when no GPU is visible; on a machine with one the CUDA path
     # must load (a missing extension is a failure, never a fallback).
     try:
         import torch
