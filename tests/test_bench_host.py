@@ -1,5 +1,6 @@
 """Host-side logic of bench.py without a GPU: the max-over-ranks timing
-reduction on two gloo ranks, and the CPU reference arm on a tiny sample."""
+reduction on two gloo ranks, and the CPU reference arm on a tiny sample, alone
+and under a two-rank torchrun launch."""
 import json
 import os
 import subprocess
@@ -49,3 +50,18 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_under_torchrun_prints_from_rank_0_only():
+    # the launch a multi-GPU run uses; ranks other than 0 exit 0 without work
+    port = 29000 + os.getpid() % 1000
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(port), "bench.py", "--impl", "reference",
+                          "--gpus", "2", "--steps", "1", "--warmup", "1", "--cpu-pairs", "2"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT, check=True)
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["config"]["parallelism"] == "dp2"
