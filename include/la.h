@@ -4,7 +4,7 @@
  * `g_gamma` path of ejkernel's `recurrent`).
  *
  * The operation (ejkernel docs, kernels/_xla/recurrent/_interface, `recurrent`
- * docstring, "The core update", with the per-head `g_gamma` decay of its Args
+ * docstring, its state-update formula, with the per-head `g_gamma` decay of its Args
  * and of the kernels/_triton/lightning_attn/_interface page), per sequence n
  * and head h, with gamma = exp(g_gamma[h]) and tokens t in processing order:
  *
@@ -100,8 +100,8 @@ typedef enum la_dtype {
  *                 when kv_heads is 0)
  *   v_strides  element strides (batch, token, head) of o, do (and of v, dv
  *                 when kv_heads is 0)
- *   kv_heads   0: keys and values have H heads (lightning_attn: "Must have
- *                 the same shape as q").  Else H_kv, a divisor of H: grouped
+ *   kv_heads   0: keys and values have H heads (lightning_attn's Args give
+ *                 them the queries' shape).  Else H_kv, a divisor of H: grouped
  *                 key/value heads (the num_kv_heads axis of ejkernel
  *                 `recurrent`'s key and value), query head h reading key and
  *                 value head h / (H / H_kv).  Decay, states and their

@@ -27,8 +27,8 @@ Tensor = torch.Tensor
 
 
 def lightning_g_gamma(num_heads: int, layer_idx: int, num_layers: int) -> Tensor:
-    """ejkernel lightning_attn, "Key innovation":
-    g_gamma = -(8 / num_heads) * (1 - layer_idx / num_layers) * arange(num_heads)."""
+    """The layer-dependent decay of the ejkernel lightning_attn page (module
+    docstring): head h of layer l out of L gets g_gamma[h] = -(8/H)(1 - l/L) h."""
     return -(8.0 / num_heads * (1.0 - layer_idx / num_layers)) * torch.arange(
         num_heads, dtype=torch.float32)
 
@@ -424,6 +424,29 @@ class _LinearAttention(torch.autograd.Function):
         return dq, dk, dv, (dinit if ctx.has_init else None), None, None, None, None
 
 
+def _packed_batch_msg(batch):
+    return ("with cu_seqlens every sequence is packed into one batch row, so the batch "
+            "dimension must be 1 (got %d)" % batch)
+
+
+def _check_packing(query, cu_seqlens, initial_state):
+    """A packed call (cu_seqlens given) holds every sequence in one batch row and,
+    with an initial state, one state per sequence."""
+    if cu_seqlens is None:
+        return
+    if query.ndim == 4 and query.shape[0] != 1:
+        raise ValueError(_packed_batch_msg(query.shape[0]))
+    n_seqs = len(cu_seqlens) - 1
+    if initial_state is not None and initial_state.shape[0] != n_seqs:
+        raise ValueError("initial_state needs one state per packed sequence: %d sequences, "
+                         "%d states" % (n_seqs, initial_state.shape[0]))
+
+
+def _scale_for(softmax_scale, head_dim):
+    """The query scale: the caller's, else 1/sqrt(head width)."""
+    return 1.0 / math.sqrt(head_dim) if softmax_scale is None else softmax_scale
+
+
 def recurrent(query: Tensor, key: Tensor, value: Tensor, g=None, g_gamma=None, gk=None, gv=None,
               softmax_scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
               reverse: bool = False, cu_seqlens=None):
@@ -441,14 +464,12 @@ def recurrent(query: Tensor, key: Tensor, value: Tensor, g=None, g_gamma=None, g
         g = None if g is None else g[None]
         squeeze = True
     if cu_seqlens is not None and query.shape[0] != 1:
-        raise ValueError("The batch size is expected to be 1 rather than %d when using "
-                         "`cu_seqlens`." % query.shape[0])
+        raise ValueError(_packed_batch_msg(query.shape[0]))
     H = query.shape[2]
     if g_gamma is None:
         g_gamma = torch.zeros(H, dtype=torch.float32)
     gg = _g(g_gamma, H, query.device)
-    if softmax_scale is None:
-        softmax_scale = 1.0 / math.sqrt(query.shape[-1])
+    softmax_scale = _scale_for(softmax_scale, query.shape[-1])
     if g is not None:
         o, fin = _GatedLinearAttention.apply(query, key, value, g, initial_state, gg,
                                              softmax_scale, bool(reverse), cu_seqlens)
@@ -464,18 +485,9 @@ def recurrent_gla(query: Tensor, key: Tensor, value: Tensor, g: Optional[Tensor]
                   cu_seqlens=None):
     """ejkernel `recurrent_gla` (the GLA page): the batch-1 / initial-state count
     checks of that page, the default scale from the key width, then `recurrent`."""
-    if cu_seqlens is not None:
-        if query.ndim == 4 and query.shape[0] != 1:
-            raise ValueError("The batch size is expected to be 1 rather than %d when using "
-                             "`cu_seqlens`." % query.shape[0])
-        n = len(cu_seqlens) - 1
-        if initial_state is not None and initial_state.shape[0] != n:
-            raise ValueError("The number of initial states is expected to be equal to the "
-                             "number of input sequences, i.e., %d rather than %d."
-                             % (n, initial_state.shape[0]))
-    if softmax_scale is None:
-        softmax_scale = key.shape[-1] ** -0.5
-    return recurrent(query, key, value, g=g, g_gamma=g_gamma, softmax_scale=softmax_scale,
+    _check_packing(query, cu_seqlens, initial_state)
+    return recurrent(query, key, value, g=g, g_gamma=g_gamma,
+                     softmax_scale=_scale_for(softmax_scale, key.shape[-1]),
                      initial_state=initial_state, reverse=reverse, cu_seqlens=cu_seqlens)
 
 
@@ -489,21 +501,11 @@ def lightning_attn(query: Tensor, key: Tensor, value: Tensor, layer_idx: int, nu
         raise ValueError("lightning_attn: key must have the shape of query and value its "
                          "leading dims (got %s, %s, %s)"
                          % (tuple(query.shape), tuple(key.shape), tuple(value.shape)))
-    if cu_seqlens is not None:
-        if query.ndim == 4 and query.shape[0] != 1:
-            raise ValueError("The batch size is expected to be 1 rather than %d when using "
-                             "`cu_seqlens`." % query.shape[0])
-        n = len(cu_seqlens) - 1
-        if initial_state is not None and initial_state.shape[0] != n:
-            raise ValueError("The number of initial states is expected to be equal to the "
-                             "number of input sequences, i.e., %d rather than %d."
-                             % (n, initial_state.shape[0]))
-    if softmax_scale is None:
-        softmax_scale = key.shape[-1] ** -0.5
+    _check_packing(query, cu_seqlens, initial_state)
     H = query.shape[-2]
     return recurrent(query, key, value, g_gamma=lightning_g_gamma(H, layer_idx, num_layers),
-                     softmax_scale=softmax_scale, initial_state=initial_state, reverse=reverse,
-                     cu_seqlens=cu_seqlens)
+                     softmax_scale=_scale_for(softmax_scale, key.shape[-1]),
+                     initial_state=initial_state, reverse=reverse, cu_seqlens=cu_seqlens)
 
 
 def lightning_attn_func(q: Tensor, k: Tensor, v: Tensor, s: Tensor) -> Tensor:

@@ -114,7 +114,8 @@ la_status check_dims(const la_dims *d, int32_t dtype, const int32_t *cu, const i
     }
     if (d->batch != 1)
         return fail(LA_ERR_INVALID_ARG,
-                    "the batch size is expected to be 1 rather than %d when using cu_seqlens",
+                    "with cu_seqlens the sequences are packed in one batch row: "
+                    "batch must be 1, got %d",
                     d->batch);
     if (d->num_seqs < 0 || d->num_seqs > (1 << 30))
         return fail(LA_ERR_INVALID_ARG, "num_seqs = %d", d->num_seqs);

@@ -5,8 +5,8 @@
 // dims the tensor-core kernels do not take, and unaligned layouts.  They
 // evaluate the chunked (Lightning Attention-2) form in fp32 FFMA: per chunk of
 // SC tokens an intra-chunk decay-masked score block and an inter-chunk carried
-// state (ejkernel `recurrent` docstring, "The core update", unrolled over a
-// chunk).
+// state (the state-update formula of the ejkernel `recurrent` docstring,
+// unrolled over a chunk).
 //
 // One CTA owns one (sequence, head, value-tile); the state tile (D x SET fp32)
 // stays in shared memory for the whole sequence.  The score block is

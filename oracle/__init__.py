@@ -5,7 +5,7 @@ cpu_baseline / reference legs may import this package; the product package
 (linear_attention_head_gb300) never does, and this package never imports it.
 
 The arithmetic lives in la_oracle.c (plain C, fp64, token by token): the
-recurrence of the ejkernel `recurrent` docstring ("The core update"),
+recurrence of the ejkernel `recurrent` docstring (its state-update formula),
 S_t = exp(g_gamma[h]) * S_{t-1} + outer(k_t, v_t), o_t = scale * q_t^T S_t,
 with initial_state, reverse and packed cu_seqlens, and the gradient of
 sum(o*do) + sum(final*dfinal) with respect to q, k, v and initial_state

@@ -10,16 +10,16 @@
  * What it computes (token by token, no chunking, no reordering):
  *
  *   ejkernel docs, kernels/_xla/recurrent/_interface, `recurrent` docstring,
- *   "The core update":   h_t = decay_t * h_{t-1} + k_t^T (x) v_t ,
- *                        o_t = h_t @ q_t
- *   read as (see the readings below)
+ *   its state-update formula: the state h decays by decay_t and gains the
+ *   outer product of k_t and v_t; the output reads the state with q_t.
+ *   Read as (see the readings below)
  *        S_t = gamma * S_{t-1} + outer(k_t, v_t)          S is d x e
  *        o_t = scale * (q_t^T S_t)                        an e-vector
- *   with gamma = exp(g_gamma[h])   (g_gamma: "per-head decay factor [num_heads]
- *   for Lightning attention", same docstring, Args; Lightning's layer-dependent
- *   g_gamma formula in the ejkernel lightning_attn page, module docstring, is
- *   negative, so the decay is exp of it),
- *   scale multiplying the query only ("Query scaling factor", same Args),
+ *   with gamma = exp(g_gamma[h])   (g_gamma holds one log-decay per head, same
+ *   docstring, Args; Lightning's layer-dependent g_gamma formula in the
+ *   ejkernel lightning_attn page, module docstring, is negative, so the decay
+ *   is exp of it),
+ *   scale multiplying the query only (softmax_scale, same Args),
  *   S_0 = initial_state or zeros, final_state = S after the last processed
  *   token, `reverse` = the same recurrence over t = L-1 .. 0 of each sequence,
  *   and packed sequences delimited by cu_seqlens = [0, len1, len1+len2, ...]

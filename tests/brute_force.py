@@ -2,7 +2,7 @@
 attention, used only to pin the recurrent fp64 oracle.
 
 Unrolling the recurrence S_t = gamma S_{t-1} + outer(k_t, v_t) (ejkernel
-`recurrent` docstring, "The core update") from S_0 gives, for the token at
+`recurrent` docstring, its state-update formula) from S_0 gives, for the token at
 processing position p(t) (p(t) = t, or L-1-t when reversed):
 
   o_t   = s * sum_{u: p(u) <= p(t)} gamma^(p(t)-p(u)) (q_t . k_u) v_u

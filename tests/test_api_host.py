@@ -1,0 +1,55 @@
+"""Argument checks of the Python entry points that run before any device work
+(CPU tensors, no GPU): packed calls need one batch row and one initial state
+per sequence; 3-D inputs need cu_seqlens; the gk / gv gates are refused."""
+import pytest
+import torch
+
+import linear_attention_head_gb300 as la
+
+
+def _qkv(B, T, H=2, D=8):
+    x = torch.zeros(B, T, H, D)
+    return x, x.clone(), x.clone()
+
+
+def test_packed_calls_need_one_batch_row():
+    q, k, v = _qkv(2, 6)
+    cu = torch.tensor([0, 3, 6], dtype=torch.int32)
+    for fn in (la.recurrent, la.recurrent_gla):
+        with pytest.raises(ValueError, match="batch dimension must be 1"):
+            fn(q, k, v, cu_seqlens=cu)
+    with pytest.raises(ValueError, match="batch dimension must be 1"):
+        la.lightning_attn(q, k, v, 0, 4, cu_seqlens=cu)
+
+
+def test_packed_calls_need_one_state_per_sequence():
+    q, k, v = _qkv(1, 6)
+    cu = torch.tensor([0, 3, 6], dtype=torch.int32)
+    s0 = torch.zeros(3, 2, 8, 8)
+    with pytest.raises(ValueError, match="2 sequences, 3 states"):
+        la.recurrent_gla(q, k, v, cu_seqlens=cu, initial_state=s0)
+    with pytest.raises(ValueError, match="2 sequences, 3 states"):
+        la.lightning_attn(q, k, v, 1, 4, cu_seqlens=cu, initial_state=s0)
+
+
+def test_three_dim_inputs_need_cu_seqlens_and_extra_gates_are_refused():
+    q, k, v = _qkv(1, 6)
+    with pytest.raises(ValueError, match="cu_seqlens"):
+        la.recurrent(q[0], k[0], v[0])
+    with pytest.raises(NotImplementedError):
+        la.recurrent(q, k, v, gk=torch.zeros(1))
+
+
+def test_lightning_keys_take_the_queries_shape():
+    q, k, v = _qkv(1, 6)
+    with pytest.raises(ValueError, match="shape of query"):
+        la.lightning_attn(q, k[:, :, :1], v, 0, 4)
+
+
+def test_layer_dependent_decay():
+    # g_gamma[h] = -(8/H)(1 - l/L) h: zero for head 0, steepest in the first layer
+    g = la.lightning_g_gamma(8, 0, 4)
+    assert g.dtype == torch.float32 and g.shape == (8,)
+    assert g[0] == 0 and torch.allclose(g[1:] / g[1], torch.arange(1, 8, dtype=torch.float32))
+    assert torch.isclose(g[1], torch.tensor(-1.0))
+    assert torch.isclose(la.lightning_g_gamma(8, 2, 4)[1], torch.tensor(-0.5))

@@ -122,9 +122,9 @@ def test_head_major_layout_and_lightning2_call():
     # OpenNLPLab README: q, k, v as (b, h, n, d), slopes s, o = lightning_attn_func(q, k, v, s)
     b, h, n, d, e = 2, 4, 300, 64, 64
     gen = torch.Generator().manual_seed(3)
-    q = torch.randn((b, h, n, d), generator=gen).bfloat16()
-    k = torch.randn((b, h, n, d), generator=gen).bfloat16()
-    v = torch.randn((b, h, n, e), generator=gen).bfloat16()
+    qk_shape, v_shape = (b, h, n, d), (b, h, n, e)
+    q, k, v = (torch.randn(shape, generator=gen).bfloat16()
+               for shape in (qk_shape, qk_shape, v_shape))
     s = -W.alibi_g_gamma(h)
     o = la.lightning_attn_func(q.cuda(), k.cuda(), v.cuda(), s.cuda())
     ref, _ = oracle_run(dict(q=q.transpose(1, 2), k=k.transpose(1, 2), v=v.transpose(1, 2),

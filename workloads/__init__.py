@@ -11,9 +11,9 @@ identical numbers.
 
 Decay recipes, as the pages give them:
   * Lightning layer-dependent decay (ejkernel lightning_attn, module
-    docstring "Key innovation"):
+    docstring, the decay formula):
         g_gamma[h] = -(8 / H) * (1 - layer_idx / num_layers) * h
-  * ALiBi-style slopes (Lightning-Attention README "How to use":
+  * ALiBi-style slopes (Lightning-Attention README, usage section:
     `_build_slope_tensor(h)`, decay = exp(-slope)); the slope list itself is
     not printed, the workload uses s_i = 2^(-8 i / H), i = 1..H.
 """
