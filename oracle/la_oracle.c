@@ -35,8 +35,8 @@
  *                               d_initial_state = G
  *   (G before the decay is dL/dS_t; the last decay carries it back to S_0.)
  *
- * Gated form (ejkernel `recurrent` Args: a gate tensor for GLA-style gating
- * with the keys' shape; the GLA page's `recurrent_gla` passes it on to
+ * Gated form (ejkernel `recurrent` Args: the optional gate `g`, shaped like
+ * the keys; the GLA page's `recurrent_gla` passes it on to
  * `recurrent`).  Read as a log-decay per key channel, added to the head's
  * g_gamma:
  *        S_t[a, :] = exp(g_gamma[h] + g_t[a]) * S_{t-1}[a, :] + k_t[a] v_t
