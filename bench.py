@@ -38,6 +38,7 @@ PAGES_TOKENS_PER_S = {512: 4 * 512 / ((0.351540 + 1.169621) * 1e-3),
                       16384: 4 * 16384 / ((8.832678 + 37.212578) * 1e-3),
                       32768: 4 * 32768 / ((17.661427 + 74.594788) * 1e-3)}
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def dist_env():
@@ -67,6 +68,52 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s: the measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# The method's own roofline.  Per (token, head) of B*T*H token-heads:
+#   bytes   fwd 2(2d + 2e) (q, k, v read, o written, bf16) + the fp32 final states;
+#           bwd 2(4d + 3e) (q, k, v, do read; dq, dk, dv written)
+#   FLOPs   chunked accounting with 64-token chunks and full 64 x 64 tiles:
+#           fwd 2C(d + e) + 4de, bwd 6C(d + e) + 10de
+# Roofline time = max(FLOPs / tensor peak, bytes / HBM peak); the fraction is
+# roofline time / measured time.  (The kernels run 128-token chunks, so they
+# execute more than these FLOPs; the count is the fixed convention.)
+ACCOUNT_CHUNK = 64
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def method_work(B, T, H, d, e, token_bytes=2):
+    th = B * T * H
+    C = ACCOUNT_CHUNK
+    return {"fwd_bytes": th * token_bytes * (2 * d + 2 * e) + B * H * d * e * 4,
+            "bwd_bytes": th * token_bytes * (4 * d + 3 * e),
+            "fwd_flops": th * (2 * C * (d + e) + 4 * d * e),
+            "bwd_flops": th * (6 * C * (d + e) + 10 * d * e)}
+
+
+def method_roofline(work, fwd_ms, bwd_ms, hbm_gbs, tflops):
+    """TFLOP/s, GB/s and the roofline fraction of the forward and the backward."""
+    out = {}
+    for name, ms in (("fwd", fwd_ms), ("bwd", bwd_ms)):
+        t_mem = work[name + "_bytes"] / (hbm_gbs * 1e9)
+        t_math = work[name + "_flops"] / (tflops * 1e12)
+        roof = max(t_mem, t_math)
+        out[name] = {"tflops": work[name + "_flops"] / (ms * 1e-3) / 1e12,
+                     "gbs": work[name + "_bytes"] / (ms * 1e-3) / 1e9,
+                     "roofline_ms": roof * 1e3,
+                     "bound": "hbm" if t_mem >= t_math else "tensor",
+                     "frac": roof / (ms * 1e-3)}
+    return out
 
 
 class ClockSampler:
@@ -208,6 +255,22 @@ def gpu_bench(args):
     dom = max(groups, key=lambda n: groups[n]["ms"])
     gd = groups[dom]
     peak, peak_src = peaks()
+    tpeak, tpeak_src = tensor_peak()
+    work = method_work(B, T, H, D, E)
+    method = {
+        "definition": "per (token, head): bytes fwd 2(2d+2e) + final states, bwd 2(4d+3e); "
+                      "FLOPs with 64-token chunks fwd 2C(d+e)+4de, bwd 6C(d+e)+10de; frac = "
+                      "max(FLOPs / tensor peak, bytes / HBM peak) / measured; fwd = la_fwd, "
+                      "bwd = la_bwd_dq + la_bwd_dkdv",
+        "work": work,
+        "step_tflops": (work["fwd_flops"] + work["bwd_flops"]) / (ms / args.steps * 1e-3) / 1e12,
+        "measured_peaks": dict(method_roofline(work, fwd_ms, dq_ms + dkdv_ms, peak, tpeak),
+                               hbm_gbs=peak, bf16_tflops=tpeak,
+                               source=peak_src + "/" + tpeak_src),
+        "nominal_peaks": dict(method_roofline(work, fwd_ms, dq_ms + dkdv_ms, NOMINAL_HBM_GBS,
+                                              NOMINAL_BF16_TFLOPS),
+                              hbm_gbs=NOMINAL_HBM_GBS, bf16_tflops=NOMINAL_BF16_TFLOPS),
+    }
     achieved = (gd["bytes"] / gd["launches"]) / (gd["ms"] / gd["launches"] * 1e-3) / 1e9
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic_tc_sweep_kernel.json")
@@ -301,6 +364,7 @@ def gpu_bench(args):
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else peak_src,
                      "step_compulsory_frac": roof_ms / (ms / args.steps)},
+        "method_roofline": method,
         "calls_ms": {"la_fwd": fwd_ms, "la_bwd_dq": dq_ms, "la_bwd_dkdv": dkdv_ms},
         "bytes_per_call": {"la_fwd": bytes_fwd, "la_bwd_dq": bytes_dq,
                            "la_bwd_dkdv": bytes_dkdv},
@@ -335,6 +399,7 @@ def length_sweep(la, torch, dev, stream, skip_n):
     (`fwd_ms`, `bwd_ms`) and also back to back without one (`*_unflushed`)."""
     import workloads as W
     out = {}
+    hbm, tfl = peaks()[0], tensor_peak()[0]
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     for n in W.SWEEP_LENGTHS:
         if n == skip_n:
@@ -367,8 +432,12 @@ def length_sweep(la, torch, dev, stream, skip_n):
         bwd = lambda: la.la_bwd(q, k, v, do, g, w.scale, want_d_initial_state=False)
         f_ms, b_ms = timed(fwd, small), timed(bwd, small)
         tps = w.B * n / ((f_ms + b_ms) * 1e-3)
+        rf = method_roofline(method_work(w.B, n, w.H, w.d, w.e), f_ms, b_ms, hbm, tfl)
         out[str(n)] = {"fwd_ms": f_ms, "bwd_ms": b_ms, "tokens_per_s": tps,
-                       "vs_pages": tps / PAGES_TOKENS_PER_S[n], "l2_flushed": small}
+                       "vs_pages": tps / PAGES_TOKENS_PER_S[n], "l2_flushed": small,
+                       "tflops_fwd": rf["fwd"]["tflops"], "tflops_bwd": rf["bwd"]["tflops"],
+                       "roofline_frac_fwd": rf["fwd"]["frac"],
+                       "roofline_frac_bwd": rf["bwd"]["frac"]}
         if small:
             out[str(n)]["fwd_ms_unflushed"] = timed(fwd, False)
             out[str(n)]["bwd_ms_unflushed"] = timed(bwd, False)

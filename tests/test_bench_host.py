@@ -65,3 +65,26 @@ def test_reference_arm_under_torchrun_prints_from_rank_0_only():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["config"]["parallelism"] == "dp2"
+
+
+def test_method_roofline_counts_and_fractions():
+    sys.path.insert(0, ROOT)
+    import bench
+    # b4 h32 n32768 d=e=128 bf16: 4.29 GB of tokens + 8.4 MB of final states forward,
+    # 7.52 GB backward; 0.412 / 1.10 TFLOP in the 64-token chunk accounting
+    w = bench.method_work(4, 32768, 32, 128, 128)
+    th = 4 * 32768 * 32
+    assert w["fwd_bytes"] == th * 2 * 512 + 4 * 32 * 128 * 128 * 4
+    assert w["bwd_bytes"] == th * 2 * 896
+    assert abs(w["fwd_flops"] / 1e12 - 0.4123) < 1e-3
+    assert abs(w["bwd_flops"] / 1e12 - 1.0995) < 1e-3
+    # at 1 TB/s and 1000 TFLOP/s the bytes bound both; a run at exactly the
+    # roofline time has fraction 1
+    r = bench.method_roofline(w, w["fwd_bytes"] / 1e9, w["bwd_bytes"] / 1e9, 1000.0, 1000.0)
+    for k in ("fwd", "bwd"):
+        assert r[k]["bound"] == "hbm" and abs(r[k]["frac"] - 1.0) < 1e-12
+        assert abs(r[k]["gbs"] - 1000.0) < 1e-9
+    # with a tiny tensor peak the FLOPs bound instead
+    r = bench.method_roofline(w, 1.0, 1.0, 1e6, 1.0)
+    assert r["fwd"]["bound"] == "tensor"
+    assert abs(r["fwd"]["frac"] - w["fwd_flops"] / 1e12 / 1e-3) < 1e-6
