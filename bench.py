@@ -646,6 +646,27 @@ def _oracle_step(w, q, k, v, do, g, cores):
     oracle.backward(q, k, v, g, w.scale, do, threads=cores)
 
 
+def cpu_model():
+    """The host CPU's name from /proc/cpuinfo (x86 `model name`; Arm implementer and
+    part numbers), else the machine type."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                fields.setdefault(key.strip().lower(), val.strip())
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    if fields.get("cpu part"):
+        return "%s implementer %s part %s" % (platform.machine(),
+                                              fields.get("cpu implementer", "?"),
+                                              fields["cpu part"])
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(n, pairs=None, n_sample=32768):
     """The fp64 oracle as it stands, fwd+bwd, timed on the host cores on a bounded sample;
     reported as the full workload's tokens/s."""
@@ -660,6 +681,7 @@ def cpu_baseline(n, pairs=None, n_sample=32768):
     ns = q.shape[1]
     value = pairs * ns / dt / w.H          # tokens of one (all-heads) sequence per second
     return {"value": value, "unit": "tokens/s", "cores": min(cores, pairs), "kind": "oracle",
+            "host_cpus": cores, "cpu_model": cpu_model(),
             "sample": "fwd+bwd of %d (batch, head) streams x %d tokens of the %d x %d-token "
                       "workload in %.2f s on %d threads; tokens/s = streams*tokens/time/H"
                       % (pairs, ns, w.B * w.H, n, dt, min(cores, pairs))}
@@ -694,7 +716,8 @@ def reference_arm(args):
                        % (w.B, w.H, args.n, w.d), "B": w.B, "H": w.H, "n": args.n,
                        "d": w.d, "e": w.e, "parallelism": "dp%d" % ws},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, pairs),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "host_cpus": cores, "cpu_model": cpu_model(),
+                             "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}

@@ -49,6 +49,7 @@ def test_reference_arm_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
     assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cpu_model"] and d["cpu_baseline"]["host_cpus"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
 
 
