@@ -7,13 +7,13 @@ streams only.
 """
 from ._native import (LaDims, LaError, LaInvalidArgument, LaUnsupported, LA_DTYPE_BF16,
                       LA_DTYPE_F32, lib)
-from .api import (get_device_error, gla_bwd, gla_fwd, kernel_family, la_bwd, la_bwd_dkdv,
-                  la_bwd_dq, la_fwd, lightning_attn, lightning_attn_func, lightning_g_gamma,
-                  recurrent, recurrent_gla)
+from .api import (alibi_g_gamma, get_device_error, gla_bwd, gla_fwd, kernel_family, la_bwd,
+                  la_bwd_dkdv, la_bwd_dq, la_fwd, lightning_attn, lightning_attn_func,
+                  lightning_g_gamma, recurrent, recurrent_gla)
 
 __all__ = [
     "LaDims", "LaError", "LaInvalidArgument", "LaUnsupported", "LA_DTYPE_BF16", "LA_DTYPE_F32",
-    "lib", "get_device_error", "gla_bwd", "gla_fwd", "kernel_family", "la_bwd", "la_bwd_dkdv",
-    "la_bwd_dq", "la_fwd", "lightning_attn", "lightning_attn_func", "lightning_g_gamma",
-    "recurrent", "recurrent_gla",
+    "lib", "alibi_g_gamma", "get_device_error", "gla_bwd", "gla_fwd", "kernel_family", "la_bwd",
+    "la_bwd_dkdv", "la_bwd_dq", "la_fwd", "lightning_attn", "lightning_attn_func",
+    "lightning_g_gamma", "recurrent", "recurrent_gla",
 ]

@@ -33,6 +33,15 @@ def lightning_g_gamma(num_heads: int, layer_idx: int, num_layers: int) -> Tensor
         num_heads, dtype=torch.float32)
 
 
+def alibi_g_gamma(num_heads: int) -> Tensor:
+    """Per-head log-decay from ALiBi-style slopes: g_gamma[i-1] = -2^(-8 i / H),
+    i = 1..H, so head i decays by exp(-slope_i) per token.  The Lightning-Attention
+    README's usage section builds such a slope tensor for its decay; the list is
+    not printed there, and this is the geometric ALiBi recipe."""
+    i = torch.arange(1, num_heads + 1, dtype=torch.float64)
+    return (-(2.0 ** (-8.0 * i / num_heads))).to(torch.float32)
+
+
 def _dtype_code(t: Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return N.LA_DTYPE_BF16

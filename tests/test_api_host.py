@@ -53,3 +53,12 @@ def test_layer_dependent_decay():
     assert g[0] == 0 and torch.allclose(g[1:] / g[1], torch.arange(1, 8, dtype=torch.float32))
     assert torch.isclose(g[1], torch.tensor(-1.0))
     assert torch.isclose(la.lightning_g_gamma(8, 2, 4)[1], torch.tensor(-0.5))
+
+
+def test_alibi_decay():
+    # head i of H decays by exp(-2^(-8 i / H)) per token: slopes halve every H/8 heads
+    g = la.alibi_g_gamma(32)
+    assert g.dtype == torch.float32 and g.shape == (32,)
+    assert torch.all(g < 0) and torch.all(g[1:] > g[:-1])
+    assert g[-1] == -2.0 ** -8 and g[3] == -0.5
+    assert torch.allclose(g[4:] / g[:-4], torch.full((28,), 0.5))
