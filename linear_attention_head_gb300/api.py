@@ -16,7 +16,9 @@ Entry points mirror the pages:
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
+import os
 from typing import Optional, Tuple
 
 import torch
@@ -24,6 +26,25 @@ import torch
 from . import _native as N
 
 Tensor = torch.Tensor
+
+# LA_NVTX=1 in the environment when the package is imported: every C-ABI entry
+# point below runs inside an NVTX range named after it (for Nsight Systems or
+# `ncu --nvtx`).  Otherwise the functions are left as they are.
+_NVTX = os.environ.get("LA_NVTX", "0") not in ("", "0")
+
+
+def _traced(fn):
+    if not _NVTX:
+        return fn
+
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        torch.cuda.nvtx.range_push(fn.__name__)
+        try:
+            return fn(*args, **kwargs)
+        finally:
+            torch.cuda.nvtx.range_pop()
+    return wrapper
 
 
 def lightning_g_gamma(num_heads: int, layer_idx: int, num_layers: int) -> Tensor:
@@ -169,6 +190,7 @@ def _like(t: Tensor) -> Tensor:
     return torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
 
 
+@_traced
 def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = None,
            initial_state: Optional[Tensor] = None, reverse: bool = False,
            cu_seqlens=None, out: Optional[Tensor] = None,
@@ -227,6 +249,7 @@ def _bwd_prep(q, k, v, do, g_gamma, scale, initial_state, d_final_state, cu_seql
     return q, k, v, do, dev, packed, g, scale, init, dfin, Nst
 
 
+@_traced
 def la_bwd(q: Tensor, k: Tensor, v: Tensor, do: Tensor, g_gamma, scale: Optional[float] = None,
            initial_state: Optional[Tensor] = None, d_final_state: Optional[Tensor] = None,
            reverse: bool = False, cu_seqlens=None, want_d_initial_state: bool = True):
@@ -247,6 +270,7 @@ def la_bwd(q: Tensor, k: Tensor, v: Tensor, do: Tensor, g_gamma, scale: Optional
     return dq, dk, dv, dinit
 
 
+@_traced
 def la_bwd_dq(q, k, v, do, g_gamma, scale=None, initial_state=None, reverse=False,
               cu_seqlens=None):
     """dq only (one sweep in processing order)."""
@@ -263,6 +287,7 @@ def la_bwd_dq(q, k, v, do, g_gamma, scale=None, initial_state=None, reverse=Fals
     return dq
 
 
+@_traced
 def la_bwd_dkdv(q, k, v, do, g_gamma, scale=None, d_final_state=None, reverse=False,
                 cu_seqlens=None, want_d_initial_state=True):
     """dk, dv and d_initial_state (one sweep against processing order)."""
@@ -315,6 +340,7 @@ def _strides3(t):
     return (ctypes.c_int64 * 3)(*t.stride()[:3])
 
 
+@_traced
 def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
             scale: Optional[float] = None, initial_state: Optional[Tensor] = None,
             reverse: bool = False, cu_seqlens=None, chunked: bool = True,
@@ -358,6 +384,7 @@ def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
     return out, fin
 
 
+@_traced
 def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_final_state=None,
             reverse=False, cu_seqlens=None, want_d_initial_state=True, operands=None):
     """Backward of gla_fwd: returns (dq, dk, dv, dg, d_initial_state).  operands: what

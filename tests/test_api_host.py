@@ -62,3 +62,24 @@ def test_alibi_decay():
     assert torch.all(g < 0) and torch.all(g[1:] > g[:-1])
     assert g[-1] == -2.0 ** -8 and g[3] == -0.5
     assert torch.allclose(g[4:] / g[:-4], torch.full((28,), 0.5))
+
+
+def test_nvtx_ranges_are_opt_in():
+    # without LA_NVTX the entry points are the plain functions; with LA_NVTX=1 they
+    # are wrapped, and a call that fails validation still closes its range
+    import os
+    import subprocess
+    import sys
+    assert not hasattr(la.la_fwd, "__wrapped__")
+    code = ("import torch, linear_attention_head_gb300 as la\n"
+            "assert hasattr(la.la_fwd, '__wrapped__') and la.la_fwd.__name__ == 'la_fwd'\n"
+            "try:\n"
+            "    la.la_fwd(torch.zeros(1, 2, 1, 4), torch.zeros(1, 2, 1, 4),\n"
+            "              torch.zeros(1, 2, 1, 4), torch.zeros(1))\n"
+            "except ValueError:\n"
+            "    print('raised')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    run = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         cwd=root, env=dict(os.environ, LA_NVTX="1"), timeout=300)
+    assert run.returncode == 0, run.stderr
+    assert "raised" in run.stdout
