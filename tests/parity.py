@@ -19,8 +19,16 @@ def _np(t):
     return t.detach().float().cpu().double().numpy() if isinstance(t, torch.Tensor) else t
 
 
+def _worse(worst, e):
+    """Running maximum in which a NaN error (a NaN or inf anywhere in the slice)
+    wins: Python's max() would silently keep the previous value."""
+    e = float(e)
+    return float("inf") if e != e else max(worst, e)
+
+
 def slice_err(x, ref, cu=None, state=False):
-    """Max over (sequence, head) slices of max|x-ref| / max|ref|."""
+    """Max over (sequence, head) slices of max|x-ref| / max|ref|; inf when any
+    slice holds a NaN."""
     x, ref = _np(x), _np(ref)
     assert x.shape == ref.shape, (x.shape, ref.shape)
     worst = 0.0
@@ -28,7 +36,7 @@ def slice_err(x, ref, cu=None, state=False):
         for n in range(ref.shape[0]):
             for h in range(ref.shape[1]):
                 a, b = x[n, h], ref[n, h]
-                worst = max(worst, np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+                worst = _worse(worst, np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
         return worst
     H = ref.shape[2]
     if cu is None:
@@ -41,7 +49,7 @@ def slice_err(x, ref, cu=None, state=False):
             continue
         for h in range(H):
             a, b = x[row, s:e, h], ref[row, s:e, h]
-            worst = max(worst, np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+            worst = _worse(worst, np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
     return worst
 
 
@@ -77,12 +85,21 @@ def oracle_run(x, reverse=False, backward=True, threads=0):
     return out
 
 
+def rms_rel(x, ref):
+    """Whole-tensor RMS-relative error, reported beside the gated metric."""
+    x, ref = _np(x), _np(ref)
+    return float(np.sqrt(np.mean((x - ref) ** 2)) / max(np.sqrt(np.mean(ref ** 2)), 1e-30))
+
+
 def compare(got, ref, tol, cu=None, label=""):
     errs = {}
     for name, r in ref.items():
         errs[name] = slice_err(got[name], r, cu, state=name in ("final_state", "d_initial_state"))
     bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, "%s: errors above %.1e: %s (all: %s)" % (label, tol, bad, errs)
+    if bad:
+        rms = {k: rms_rel(got[k], ref[k]) for k in ref}
+        raise AssertionError("%s: errors above %.1e: %s (all: %s; RMS-relative: %s)"
+                             % (label, tol, bad, errs, rms))
     return errs
 
 
@@ -165,5 +182,5 @@ def compare_gated(got, ref, x, reverse, tol, label):
             if b == a:
                 continue
             e = d[0, a:b].max(axis=(0, 2))
-        worst = max(worst, float((e / np.maximum(c, 1e-30)).max()))
+        worst = _worse(worst, (e / np.maximum(c, 1e-30)).max())
     assert worst <= tol, "%s: dg error %.3e of its condition above %.1e" % (label, worst, tol)
