@@ -4,8 +4,9 @@
  * `g_gamma` path of ejkernel's `recurrent`).
  *
  * The operation (ejkernel docs, kernels/_xla/recurrent/_interface, `recurrent`
- * docstring, its state-update formula, with the per-head `g_gamma` decay of its Args
- * and of the kernels/_triton/lightning_attn/_interface page), per sequence n
+ * docstring, its state-update formula, with the per-head `g_gamma` decay of
+ * its Args and of the kernels/_triton/lightning_attn/_interface page), per
+ * sequence n
  * and head h, with gamma = exp(g_gamma[h]) and tokens t in processing order:
  *
  *     S_t = gamma * S_{t-1} + k_t^T v_t          (S: d x e, fp32)
@@ -56,6 +57,10 @@
  *     allocates device memory or synchronizes, except: when cu_seqlens is given
  *     without cu_seqlens_host the library copies cu_seqlens to the host and
  *     waits for that copy; and la_get_device_error synchronizes `stream`.
+ *     The tensor-core kernels are launched as programmatic dependents of
+ *     the stream's previous kernel: they may start their set-up while it
+ *     drains, but read and write global memory only after it has completed,
+ *     so stream order holds as for any launch.
  *   - Every argument is validated before anything is enqueued.  A failed
  *     validation returns LA_ERR_INVALID_ARG or LA_ERR_UNSUPPORTED, launches
  *     nothing and leaves every output untouched; la_last_error() describes it.
