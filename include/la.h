@@ -6,8 +6,8 @@
  * The operation (ejkernel docs, kernels/_xla/recurrent/_interface, `recurrent`
  * docstring, its state-update formula, with the per-head `g_gamma` decay of
  * its Args and of the kernels/_triton/lightning_attn/_interface page), per
- * sequence n
- * and head h, with gamma = exp(g_gamma[h]) and tokens t in processing order:
+ * sequence n and head h, with gamma = exp(g_gamma[h]) and tokens t in
+ * processing order:
  *
  *     S_t = gamma * S_{t-1} + k_t^T v_t          (S: d x e, fp32)
  *     o_t = (scale * q_t) S_t                    (an e-vector)
