@@ -117,26 +117,29 @@ def method_roofline(work, fwd_ms, bwd_ms, hbm_gbs, tflops):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling around the timed region.  Each sample
+    carries nvidia-smi's timestamp; the summary uses the samples that fall inside
+    the timed region (wall clock) and falls back to all of them when none does."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """t0, t1: the timed region in time.time() seconds."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -145,24 +148,41 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        return self.summarize(out, t0, t1)
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    @classmethod
+    def summarize(cls, out, t0=None, t1=None):
+        rows = []
+        for line in (out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for name, flag in zip(names, parts[4:8]):
-                if flag.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+            flags = {name for name, flag in zip(cls.REASONS, parts[5:9])
+                     if flag.lower().startswith("active")}
+            rows.append((cls._stamp(parts[0]), sm, mx, flags))
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows
+                  if t0 is not None and r[0] is not None and t0 <= r[0] <= t1]
+        use = inside or rows
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(set().union(*(r[3] for r in use))),
+                "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
 def gpu_bench(args):
@@ -219,14 +239,16 @@ def gpu_bench(args):
     time.sleep(0.3)
     launches0 = _native.lib().la_launch_count()
     t_wall0 = time.perf_counter()
+    t_region0 = time.time()
     start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     end.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
+    t_region1 = time.time()
     launches = _native.lib().la_launch_count() - launches0
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_region0, t_region1)
     la.get_device_error(dev)
     ms = start.elapsed_time(end)
     ms = max_over_ranks(ms, ws, dev)
@@ -727,7 +749,7 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--n", type=int, default=32768)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])

@@ -89,3 +89,31 @@ def test_method_roofline_counts_and_fractions():
     r = bench.method_roofline(w, 1.0, 1.0, 1e6, 1.0)
     assert r["fwd"]["bound"] == "tensor"
     assert abs(r["fwd"]["frac"] - w["fwd_flops"] / 1e12 / 1e-3) < 1e-6
+
+
+def test_clock_summary_keeps_the_timed_region():
+    sys.path.insert(0, ROOT)
+    import datetime
+    import bench
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+
+    def line(dt_s, sm, power_cap="Not Active", thermal="Not Active"):
+        ts = (base + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return ", ".join([ts, str(sm), "2070", "900.0", "0x0", "Not Active", "Not Active",
+                          thermal, power_cap])
+
+    out = "\n".join([line(0.0, 2070), line(0.05, 2070), line(0.40, 1900, "Active"),
+                     line(0.45, 1950), line(0.50, 1800, "Active"), line(0.90, 2070,
+                                                                        thermal="Active")])
+    t0 = base.timestamp() + 0.30
+    t1 = base.timestamp() + 0.60
+    c = bench.ClockSampler.summarize(out, t0, t1)
+    assert c["samples_in_timed_region"] == 3 and c["samples"] == 3
+    assert c["sm_mhz"] == 1900 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]          # the thermal flag came after the region
+    # no sample inside the region: every sample is summarised, and the count says so
+    c = bench.ClockSampler.summarize(out, t1 + 10, t1 + 11)
+    assert c["samples_in_timed_region"] == 0 and c["samples"] == 6
+    assert "sw_thermal_slowdown" in c["reasons"]
+    assert bench.ClockSampler.summarize("", t0, t1) is None
+    assert bench.ClockSampler.summarize("garbage\n1,2,3", t0, t1) is None
