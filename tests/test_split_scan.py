@@ -1,0 +1,83 @@
+"""The sequence split's algebra on the CPU, with the fp64 oracle as the
+per-segment runner: every sequence is cut into segments; a first pass from
+zero states gives each segment's own contribution F; a scan in visiting order
+(carry <- gamma^L carry + F, starting from the initial state) gives each
+segment's entering state and the final state; a second pass from those
+states gives the outputs.  The backward scans its G = dL/dS the same way
+against the visiting order, starting from d_final_state.  Both must reproduce
+the unsplit run, because each segment maps its entering state affinely."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+
+def _seg_bounds(L, seg):
+    return [(a, min(L, a + seg)) for a in range(0, L, seg)]
+
+
+def _split_run(x, seg, reverse):
+    q, k, v, do = (x[n] for n in ("q", "k", "v", "do"))
+    g, s = x["g_gamma"], x["scale"]
+    S0, dF = x["initial_state"], x["d_final_state"]
+    B, T, H, d = q.shape
+    e = v.shape[3]
+    gamma = torch.exp(g.double())[None, :, None, None]
+    segs = _seg_bounds(T, seg)
+    visit = segs[::-1] if reverse else segs
+    part = lambda t, a, b: t[:, a:b].contiguous()
+    zero = torch.zeros((B, H, d, e), dtype=torch.float64)
+    # pass 1: each segment from zero states (forward state, backward gradient)
+    F = {}
+    Gc = {}
+    for a, b in segs:
+        _, F[a] = oracle.forward(part(q, a, b), part(k, a, b), part(v, a, b), g, s, None,
+                                 reverse)
+        *_, Gc[a] = oracle.backward(part(q, a, b), part(k, a, b), part(v, a, b), g, s,
+                                    part(do, a, b), zero, zero, reverse)
+    # scans
+    Win, carry = {}, S0.double()
+    for a, b in visit:
+        Win[a] = carry
+        carry = gamma ** (b - a) * carry + torch.as_tensor(F[a])
+    final = carry
+    Wout, carry = {}, dF.double()
+    for a, b in visit[::-1]:
+        Wout[a] = carry
+        carry = gamma ** (b - a) * carry + torch.as_tensor(Gc[a])
+    dinit = carry
+    # pass 2
+    o = np.zeros((B, T, H, e))
+    dq, dk, dv = np.zeros((B, T, H, d)), np.zeros((B, T, H, d)), np.zeros((B, T, H, e))
+    for a, b in segs:
+        o[:, a:b], _ = oracle.forward(part(q, a, b), part(k, a, b), part(v, a, b), g, s,
+                                      Win[a], reverse)
+        dq[:, a:b], dk[:, a:b], dv[:, a:b], _ = oracle.backward(
+            part(q, a, b), part(k, a, b), part(v, a, b), g, s, part(do, a, b), Win[a],
+            Wout[a], reverse)
+    return dict(o=o, final_state=final.numpy(), dq=dq, dk=dk, dv=dv,
+                d_initial_state=dinit.numpy())
+
+
+@pytest.mark.parametrize("seg", [1, 7, 16])
+@pytest.mark.parametrize("reverse", [False, True])
+def test_split_passes_around_a_state_scan_equal_the_unsplit_run(seg, reverse):
+    x = W.random_small(11, 2, 45, 3, 4, 5, g_lo=-0.8, g_hi=0.0)
+    x["g_gamma"][1] = 0.0
+    gen = torch.Generator().manual_seed(12)
+    x["initial_state"] = torch.randn((2, 3, 4, 5), generator=gen, dtype=torch.float64)
+    x["d_final_state"] = torch.randn((2, 3, 4, 5), generator=gen, dtype=torch.float64)
+    x["scale"] = 0.9
+    got = _split_run(x, seg, reverse)
+    o, fin = oracle.forward(x["q"], x["k"], x["v"], x["g_gamma"], x["scale"],
+                            x["initial_state"], reverse)
+    dq, dk, dv, dinit = oracle.backward(x["q"], x["k"], x["v"], x["g_gamma"], x["scale"],
+                                        x["do"], x["initial_state"], x["d_final_state"],
+                                        reverse)
+    ref = dict(o=o, final_state=fin, dq=dq, dk=dk, dv=dv, d_initial_state=dinit)
+    for name, r in ref.items():
+        r = np.asarray(r)
+        err = np.max(np.abs(got[name] - r)) / np.max(np.abs(r))
+        assert err <= 1e-12, (name, err)
