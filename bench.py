@@ -388,6 +388,10 @@ def gpu_bench(args):
                      "step_compulsory_frac": roof_ms / (ms / args.steps)},
         "method_roofline": method,
         "calls_ms": {"la_fwd": fwd_ms, "la_bwd_dq": dq_ms, "la_bwd_dkdv": dkdv_ms},
+        "calls_ms_median": {
+            "la_fwd": statistics.median(e[0].elapsed_time(e[1]) for e in evs),
+            "la_bwd_dq": statistics.median(e[1].elapsed_time(e[2]) for e in evs),
+            "la_bwd_dkdv": statistics.median(e[2].elapsed_time(e[3]) for e in evs)},
         "bytes_per_call": {"la_fwd": bytes_fwd, "la_bwd_dq": bytes_dq,
                            "la_bwd_dkdv": bytes_dkdv},
         "kernel_family": la.kernel_family(B, T, H, D, E),
