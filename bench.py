@@ -41,6 +41,16 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
+def bench_config(B, H, n, d, e, ws):
+    """The `config` object of the bench line, shared by both arms."""
+    unit = B * n * H * d * 2
+    l2 = ("inputs larger than L2 (%.2f GB per token tensor), no flush" % (unit / 1e9)
+          if unit > 2 * 129e6 else "inputs within twice the L2 (%.3f GB per token tensor)"
+          % (unit / 1e9))
+    return {"workload": "fwd+bwd b%d h%d n%d d=e=%d bf16, ALiBi slopes, scale 1" % (B, H, n, d),
+            "B": B, "H": H, "n": n, "d": d, "e": e, "l2": l2, "parallelism": "dp%d" % ws}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -259,26 +269,41 @@ def gpu_bench(args):
     tokens_step = B * T
     value = ws * tokens_step * args.steps / (ms * 1e-3)
 
-    # Algorithmic bytes per launch (bf16 tokens, fp32 states); one unit = one token tensor.
-    # Every call is one launch of the tcgen05 sweep kernel except la_bwd_dkdv (two: dv, dk).
-    #   forward-type  (la_fwd, la_bwd_dq): read 3 units, write 1 (+ the fp32 final state for la_fwd)
-    #   backward-type (dv and dk launches): read 3 units, write 1
+    # Algorithmic bytes of each call, by the method's steps (bf16 tokens, fp32
+    # states; one unit = one token tensor of B*T*H*128 bf16):
+    #   la_fwd      (a1-a8)  q, k, v read, o written: 4 units + the fp32 final state
+    #   la_bwd_dq   (b1)     k, v, do read, dq written: 4 units
+    #   la_bwd_dkdv (b2)     q, k, v, do read, dk, dv written: 6 units
+    # and the bytes its launches stream (what each kernel moves): a sweep
+    # launch reads 3 token tensors and writes 1, so la_bwd_dkdv streams 4 units
+    # per launch (2 launches when dv and dk run as separate sweeps).
     unit = B * T * H * D * 2
     state_bytes = B * H * D * E * 4
-    bytes_fwd = 4 * unit + state_bytes
-    bytes_dq = 4 * unit
-    bytes_dkdv = 8 * unit
-    groups = {
-        "tc_sweep_kernel forward-type (la_fwd, la_bwd_dq)":
-            dict(launches=2, ms=fwd_ms + dq_ms, bytes=bytes_fwd + bytes_dq),
-        "tc_sweep_kernel backward-type (la_bwd_dkdv: dv, dk)":
-            dict(launches=2, ms=dkdv_ms, bytes=bytes_dkdv),
+    n_launch = call_launches(la, q, k, v, do, g, scale)
+    calls = {
+        "la_fwd": dict(ms=fwd_ms, launches=n_launch["la_fwd"],
+                       method=4 * unit + state_bytes,
+                       stream=4 * unit * n_launch["la_fwd"] + state_bytes),
+        "la_bwd_dq": dict(ms=dq_ms, launches=n_launch["la_bwd_dq"], method=4 * unit,
+                          stream=4 * unit * n_launch["la_bwd_dq"]),
+        "la_bwd_dkdv": dict(ms=dkdv_ms, launches=n_launch["la_bwd_dkdv"], method=6 * unit,
+                            stream=4 * unit * n_launch["la_bwd_dkdv"]),
     }
-    dom = max(groups, key=lambda n: groups[n]["ms"])
-    gd = groups[dom]
+    fused = n_launch["la_bwd_dkdv"] == 1
+    groups = {
+        "tc_sweep_kernel forward-type (la_fwd, la_bwd_dq)": ("la_fwd", "la_bwd_dq"),
+        ("tc_dkdv_kernel (la_bwd_dkdv: dk and dv in one sweep)" if fused else
+         "tc_sweep_kernel backward-type (la_bwd_dkdv: dv, dk)"): ("la_bwd_dkdv",),
+    }
+    gsum = {name: {f: sum(calls[c][f] for c in members)
+                   for f in ("ms", "launches", "method", "stream")}
+            for name, members in groups.items()}
+    dom = max(gsum, key=lambda n: gsum[n]["ms"])
+    gd = gsum[dom]
     peak, peak_src = peaks()
     tpeak, tpeak_src = tensor_peak()
     work = method_work(B, T, H, D, E)
+    measured_rf = method_roofline(work, fwd_ms, dq_ms + dkdv_ms, peak, tpeak)
     method = {
         "definition": "per (token, head): bytes fwd 2(2d+2e) + final states, bwd 2(4d+3e); "
                       "FLOPs with 64-token chunks fwd 2C(d+e)+4de, bwd 6C(d+e)+10de; frac = "
@@ -286,21 +311,23 @@ def gpu_bench(args):
                       "bwd = la_bwd_dq + la_bwd_dkdv",
         "work": work,
         "step_tflops": (work["fwd_flops"] + work["bwd_flops"]) / (ms / args.steps * 1e-3) / 1e12,
-        "measured_peaks": dict(method_roofline(work, fwd_ms, dq_ms + dkdv_ms, peak, tpeak),
-                               hbm_gbs=peak, bf16_tflops=tpeak,
+        "measured_peaks": dict(measured_rf, hbm_gbs=peak, bf16_tflops=tpeak,
                                source=peak_src + "/" + tpeak_src),
         "nominal_peaks": dict(method_roofline(work, fwd_ms, dq_ms + dkdv_ms, NOMINAL_HBM_GBS,
                                               NOMINAL_BF16_TFLOPS),
                               hbm_gbs=NOMINAL_HBM_GBS, bf16_tflops=NOMINAL_BF16_TFLOPS),
     }
-    achieved = (gd["bytes"] / gd["launches"]) / (gd["ms"] / gd["launches"] * 1e-3) / 1e9
+    ms_launch = gd["ms"] / gd["launches"]
+    achieved = (gd["method"] / gd["launches"]) / (ms_launch * 1e-3) / 1e9
+    streamed = (gd["stream"] / gd["launches"]) / (ms_launch * 1e-3) / 1e9
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic_tc_sweep_kernel.json")
     if os.path.exists(tr_path):
         try:
             with open(tr_path) as f:
                 tr = json.load(f)
-            key = "forward-type" if "forward-type" in dom else "backward-type"
+            key = ("forward-type" if "forward-type" in dom else
+                   "dkdv" if fused else "backward-type")
             entry = tr.get(key)
             if entry and entry.get("source_sha") == source_sha():
                 traffic = entry["bytes_per_launch_scaled"] * T / entry["n_full"]
@@ -375,14 +402,19 @@ def gpu_bench(args):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / PAGES_TOKENS_PER_S[T] if T in PAGES_TOKENS_PER_S else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "fwd+bwd b%d h%d n%d d=e=%d bf16, ALiBi slopes, scale 1"
-                   % (B, H, T, D), "B": B, "H": H, "n": T, "d": D, "e": E,
-                   "l2": "inputs larger than L2 (%.2f GB per token tensor), no flush" %
-                   (unit / 1e9), "parallelism": "dp%d" % ws},
+        "config": bench_config(B, H, T, D, E, ws),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "bytes_per_launch": gd["bytes"] / gd["launches"],
-                     "ms_per_launch": gd["ms"] / gd["launches"],
+                     "bytes_per_launch": gd["method"] / gd["launches"],
+                     "bytes_definition": "the method's algorithmic bytes of the kernel's "
+                                         "calls (la_fwd 4 units + final state, la_bwd_dq 4, "
+                                         "la_bwd_dkdv 6; unit = one bf16 token tensor) per "
+                                         "launch",
+                     "ms_per_launch": ms_launch,
+                     "stream_bytes_per_launch": gd["stream"] / gd["launches"],
+                     "stream_frac": streamed / peak,
+                     "method_fwd_frac": measured_rf["fwd"]["frac"],
+                     "method_bwd_frac": measured_rf["bwd"]["frac"],
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else peak_src,
                      "step_compulsory_frac": roof_ms / (ms / args.steps)},
@@ -392,8 +424,8 @@ def gpu_bench(args):
             "la_fwd": statistics.median(e[0].elapsed_time(e[1]) for e in evs),
             "la_bwd_dq": statistics.median(e[1].elapsed_time(e[2]) for e in evs),
             "la_bwd_dkdv": statistics.median(e[2].elapsed_time(e[3]) for e in evs)},
-        "bytes_per_call": {"la_fwd": bytes_fwd, "la_bwd_dq": bytes_dq,
-                           "la_bwd_dkdv": bytes_dkdv},
+        "bytes_per_call": {c: calls[c]["method"] for c in calls},
+        "launches_per_call": {c: calls[c]["launches"] for c in calls},
         "kernel_family": la.kernel_family(B, T, H, D, E),
         "gpu_launches": int(launches),
         "clocks": clocks,
@@ -414,6 +446,22 @@ def gpu_bench(args):
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+def call_launches(la, q, k, v, do, g, scale):
+    """Kernel launches of one call of each entry point of the step, by the
+    library's own launch counter."""
+    from linear_attention_head_gb300 import _native
+    lib = _native.lib()
+    out = {}
+    for name, fn in (("la_fwd", lambda: la.la_fwd(q, k, v, g, scale)),
+                     ("la_bwd_dq", lambda: la.la_bwd_dq(q, k, v, do, g, scale)),
+                     ("la_bwd_dkdv", lambda: la.la_bwd_dkdv(q, k, v, do, g, scale,
+                                                            want_d_initial_state=False))):
+        n0 = lib.la_launch_count()
+        fn()
+        out[name] = max(1, int(lib.la_launch_count() - n0))
+    return out
 
 
 def length_sweep(la, torch, dev, stream, skip_n):
@@ -734,13 +782,15 @@ def reference_arm(args):
     sample = ("per step: fwd+bwd of %d (batch, head) streams x %d tokens of the %d x %d-token "
               "workload on %d host threads; tokens/s = streams*tokens/time/H"
               % (pairs, ns, w.B * w.H, args.n, min(cores, pairs)))
+    # ms_per_step is the time of one timed step as run (the bounded sample);
+    # the full workload's step time at the same rate is reported beside it
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": w.B * args.n / value * 1e3, "higher_is_better": True,
+            "ms_per_step": dt / args.steps * 1e3,
+            "projected_full_workload_ms_per_step": w.B * args.n / value * 1e3,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "fwd+bwd b%d h%d n%d d=e=%d bf16, ALiBi slopes, scale 1"
-                       % (w.B, w.H, args.n, w.d), "B": w.B, "H": w.H, "n": args.n,
-                       "d": w.d, "e": w.e, "parallelism": "dp%d" % ws},
+            "config": bench_config(w.B, w.H, args.n, w.d, w.e, ws),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, pairs),
                              "kind": "oracle", "host_cpus": cores, "cpu_model": cpu_model(),
                              "sample": sample},

@@ -57,6 +57,10 @@
  *     allocates device memory or synchronizes, except: when cu_seqlens is given
  *     without cu_seqlens_host the library copies cu_seqlens to the host and
  *     waits for that copy; and la_get_device_error synchronizes `stream`.
+ *     Packed calls that use a workspace (or la_fwd_noalloc's array) also
+ *     copy host data into it during the call: the longest-first schedule
+ *     and the sequence split's segment table are built on the host and sent
+ *     with cudaMemcpyAsync from pageable memory.
  *     The tensor-core kernels are launched as programmatic dependents of
  *     the stream's previous kernel: they may start their set-up while it
  *     drains, but read and write global memory only after it has completed,
@@ -213,10 +217,14 @@ la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype,
  * la_fwd; the packed-sequence schedule lives in an array compiled into the
  * library (LA_FWD_NOALLOC_MAX_SEQS int32 per GPU, held until exit) instead of
  * a caller workspace.  More than LA_FWD_NOALLOC_MAX_SEQS packed sequences is
- * rejected with LA_ERR_UNSUPPORTED before anything is enqueued.  The first
- * call on a device looks the array's device address up (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.
- * Every call on a device shares the one array, which keeps the previous
+ * rejected with LA_ERR_UNSUPPORTED before anything is enqueued.  The array
+ * only ever holds the schedule (never the sequence split's states, so packed
+ * calls here always run unsplit).  The first packed call on a device looks the
+ * array's device address up (cudaGetSymbolAddress) with that device current
+ * and keeps it for the rest of the process; make that first call before any
+ * stream capture begins.  The kept address does not survive a
+ * cudaDeviceReset: do not use this entry point on a device after resetting
+ * it.  Every call on a device shares the one array, which keeps the previous
  * call's schedule; each call overwrites the entries it uses.  Calls whose
  * work overlaps on the GPU (different streams, or host threads without
  * ordering between them) race on it and must be serialized by the caller. */

@@ -13,7 +13,11 @@
 // library holds it (LA_FWD_NOALLOC_MAX_SEQS int32) until the process exits.
 // In host code its name is only a host-side stand-in, so its device address
 // is looked up with cudaGetSymbolAddress once per device, with that device
-// current, on the first call made on that device.
+// current, on the first packed call made on that device, and kept for the
+// rest of the process (a cudaDeviceReset would make it stale, so the header
+// tells callers not to use this entry point after one).  Only the schedule
+// goes into the array: the workspace size passed on is the schedule's own,
+// so la_fwd never places the sequence split's states there.
 
 #include <cstdio>
 #include <mutex>
@@ -79,7 +83,7 @@ extern "C" la_status la_fwd_noalloc(const la_dims *dims, int32_t dtype, const vo
         la_status st = schedule_address(&ws);
         if (st != LA_OK)
             return st;
-        ws_bytes = sizeof(g_noalloc_schedule);
+        ws_bytes = la_workspace_size(dims ? dims->num_seqs : 0);
     }
     // The schedule overwrites the first num_seqs entries on every call and the
     // kernels read only those, so nothing has to be cleared beforehand.
