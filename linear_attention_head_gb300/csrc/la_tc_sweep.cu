@@ -64,25 +64,36 @@ using namespace sm100;
 __device__ int g_tc_error;
 
 constexpr int TC_C = 128;        // tokens per chunk (MMA M and the P Z K-extent)
-constexpr int TC_D = 128;        // key width
-constexpr int TC_NST = 2;        // TMA ring stages
 constexpr int TC_THREADS = 576;  // 18 warps
 constexpr int TC_PG = 256;       // P group threads (warps 2..9)
 constexpr int TC_SG = 128;       // S group threads (warps 10..13)
 constexpr int TC_OG = 128;       // O group threads (warps 14..17)
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;
 constexpr int TC_ERR_TIMEOUT = 4;
-constexpr uint32_t TM_SC = 0, TM_OI = 128, TM_OA = 256, TM_S = 384, TM_COLS = 512;
+constexpr uint32_t TM_SC = 0, TM_COLS = 512;
 
-template <int E> struct TcLayout {
-    static constexpr int XB = TC_C * TC_D * 2;
-    static constexpr int YB = TC_C * TC_D * 2;
+// Shared memory and TMEM of one CTA with key width D and a tile of E value
+// columns.  Tiles are [channel block of 64][C rows][128 bytes], 128-byte
+// swizzled.  The Y slot is padded to a multiple of 128 channels with zero
+// blocks (written once, never loaded), so the state update is always M = 128
+// MMAs: state rows past D only ever receive zeros and are never read.  The
+// state occupies NP = YPAD / 128 TMEM pieces of E columns.
+template <int D, int E> struct TcLayout {
+    static constexpr int YPAD = (D + 127) / 128 * 128;
+    static constexpr int NP = YPAD / 128;              // 128-row state pieces
+    static constexpr int NST = D <= 128 ? 2 : 1;       // TMA ring stages
+    static constexpr int XB = TC_C * D * 2;
+    static constexpr int YB = TC_C * YPAD * 2;
+    static constexpr int YLB = TC_C * D * 2;           // bytes of Y loaded per chunk
     static constexpr int ZB = TC_C * E * 2;
     static constexpr int STAGE = XB + YB + ZB;
-    static constexpr int SOFF = TC_NST * STAGE;       // bf16 copy of S, [E/64][D][64]
-    static constexpr int SB = TC_D * E * 2;
+    static constexpr int SOFF = NST * STAGE;           // bf16 copy of S, [E/64][D][64]
+    static constexpr int SB = D * E * 2;
     static constexpr int MOFF = SOFF + SB;
-    static constexpr int NBAR = 4 * TC_NST + 12;
+    static constexpr int NBAR = 4 * NST + 12;
+    // TMEM columns: scores [0,128), X S, P Z, then the state pieces
+    static constexpr uint32_t TM_OI = 128, TM_OA = 128 + E, TM_S = 128 + 2 * E;
+    static_assert(TM_S + NP * E <= TM_COLS, "TMEM columns");
     static constexpr int PWOFF = MOFF + NBAR * 8;
     static constexpr int CFOFF = (PWOFF + (TC_C + 1) * 4 + 15) / 16 * 16;   // 32 column factors
     static constexpr int DTOFF = CFOFF + 32 * 4;                            // 64 diagonal factors
@@ -91,6 +102,7 @@ template <int E> struct TcLayout {
     static constexpr int ABORTOFF = SLOTOFF + 4;
     static constexpr int BYTES = ABORTOFF + 4;
     static constexpr int DYN = BYTES + 1024;           // slack for 1024-byte alignment
+    static_assert(DYN <= 232448, "shared memory per CTA");
 };
 
 struct TcParams {
@@ -193,16 +205,18 @@ __device__ __forceinline__ void store_half_row_sw128(uint8_t *row_base, int row,
 }
 
 // Initial state row i, 8 columns at a time (once per CTA): fp32 from global
-// (any strides), times colf[column] when colf is given, -> times c0 as bf16
-// into the swizzled S copy, and times g0 into TMEM.
-__device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i, int E_,
-                                         uint8_t *sbf, uint32_t tmem_row, float g0, float c0,
-                                         const float *colf = nullptr)
+// (any strides; this CTA's value columns start at e0), times colf[column]
+// when colf is given, -> times c0 as bf16 into the swizzled S copy (row i at
+// sbf, blocks of 64 columns dstride bytes apart), and times g0 into TMEM.
+__device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i, int e0, int E_,
+                                         uint8_t *sbf, int dstride, uint32_t tmem_row, float g0,
+                                         float c0, const float *colf = nullptr)
 {
 #pragma unroll 1
     for (int p8 = 0; p8 < E_ / 8; ++p8) {
         float x[8];
-        const float *src = sin.p ? sin.p + base + i * sin.rs + (8 * p8) * sin.cs : nullptr;
+        const float *src =
+            sin.p ? sin.p + base + i * sin.rs + (int64_t)(e0 + 8 * p8) * sin.cs : nullptr;
         if (src && sin.cs == 1 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
             // contiguous row: two 16-byte loads
             const float4 lo = *reinterpret_cast<const float4 *>(src);
@@ -217,7 +231,7 @@ __device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             x[k] *= colf ? colf[8 * p8 + k] : 1.f;
-        *reinterpret_cast<uint4 *>(sbf + (p8 >> 3) * (TC_D * 128) + (((p8 & 7) ^ (i & 7)) << 4)) =
+        *reinterpret_cast<uint4 *>(sbf + (p8 >> 3) * dstride + (((p8 & 7) ^ (i & 7)) << 4)) =
             make_uint4(pack_bf16x2(c0 * x[0], c0 * x[1]), pack_bf16x2(c0 * x[2], c0 * x[3]),
                        pack_bf16x2(c0 * x[4], c0 * x[5]), pack_bf16x2(c0 * x[6], c0 * x[7]));
         uint32_t r[8];
@@ -228,14 +242,15 @@ __device__ __forceinline__ void state_in(const StateIn &sin, int64_t base, int i
     }
 }
 
-// Empty sequence: initial state row i (zero when absent) -> final state row i.
+// Empty sequence: initial state row i (zero when absent) -> final state row i,
+// value columns e0 .. e0 + E_ - 1.
 __device__ __forceinline__ void state_copy(const StateIn &sin, const StateOut &sout, int64_t base,
-                                           int i, int E_)
+                                           int i, int e0, int E_)
 {
     if (!sout.p)
         return;
 #pragma unroll 1
-    for (int k = 0; k < E_; ++k)
+    for (int k = e0; k < e0 + E_; ++k)
         sout.p[base + i * sout.rs + k * sout.cs] =
             sin.p ? sin.p[base + i * sin.rs + k * sin.cs] : 0.f;
 }
@@ -335,10 +350,17 @@ __device__ __forceinline__ void zero_row(uint8_t *row_base)
 // SO (state only): the sweep's final states alone (the sequence split's first
 // pass): Y and Z are loaded, the state update runs, X, the scores, P Z, the
 // inter term and the output are skipped.
-template <int E, bool BWD, int GLA, bool SO = false>
+// D: key width (X and Y channels); E: the value columns of one CTA, a tile of
+// the a.E columns (a.E / E CTAs per (sequence, head), adjacent in the grid so
+// that their X and Y reads meet in L2).
+template <int D, int E, bool BWD, int GLA, bool SO = false>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_constant__ TcParams P)
 {
-    using L = TcLayout<E>;
+    static_assert(D % 64 == 0 && D <= 256 && (E == 64 || E == 128), "tile shape");
+    static_assert(!GLA || D == 128, "the gated form has 128 key channels");
+    using L = TcLayout<D, E>;
+    constexpr int NST = L::NST;
+    constexpr uint32_t TM_OI = L::TM_OI, TM_OA = L::TM_OA, TM_S = L::TM_S;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -348,9 +370,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     // empty: its X and Y slots are free (the state update, the chunk's last
     // MMA reading them, is done); zfree: its Z slot is free (every O warp has
     // stored its rows of the output tile, staged there, out of it)
-    uint64_t *full = bars, *empty = bars + TC_NST, *zfull = bars + 2 * TC_NST,
-             *zfree = bars + 3 * TC_NST;
-    uint64_t *sc_full = bars + 4 * TC_NST;   // scores of the chunk are in TMEM
+    uint64_t *full = bars, *empty = bars + NST, *zfull = bars + 2 * NST,
+             *zfree = bars + 3 * NST;
+    uint64_t *sc_full = bars + 4 * NST;      // scores of the chunk are in TMEM
     uint64_t *pv_done = sc_full + 1;         // P consumed (scores columns free)
     uint64_t *p_ready = sc_full + 2;         // P written, Y scaled
     uint64_t *s_ready = sc_full + 3;         // bf16 S written, TMEM S pre-scaled
@@ -367,7 +389,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < TC_NST; ++i) {
+        for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
             mbar_init(&zfull[i], 1);
@@ -394,6 +416,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         prefetch_tmap(&P.mz);
         prefetch_tmap(&P.mo);
     }
+    if (L::YPAD > D) {
+        // zero blocks padding each stage's Y slot to whole 128-channel pieces
+        // (never loaded; the MMAs read them through the async proxy)
+        constexpr int PADB = (L::YPAD - D) * TC_C * 2;
+        for (int st = 0; st < NST; ++st)
+            for (int o = 16 * threadIdx.x; o < PADB; o += 16 * TC_THREADS)
+                *reinterpret_cast<uint4 *>(sm + st * L::STAGE + L::XB + L::YLB + o) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -405,8 +437,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
     grid_dep_launch_dependents();
 
     // work item: the rank-th sequence of the schedule (longest first when an
-    // order is given), one head per CTA
-    const int rank = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    // order is given), one head and one tile of E value columns per CTA
+    const int net = a.E / E;
+    const int et = (int)(blockIdx.x % (unsigned)net);
+    const int pair = (int)(blockIdx.x / (unsigned)net);
+    const int rank = pair / a.H, h = pair % a.H;
+    const int e0 = et * E;   // first value column of this CTA
     const int n = a.order ? a.order[rank] : rank;
     int64_t row, bos, len;
     if (a.cu) {
@@ -442,54 +478,54 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             const int hx = h / P.dx, hy = h / P.dy, hz = h / P.dz;
             int issued = 0;
             for (int c = 0; c < nc; ++c) {
-                const int s = c % TC_NST;
-                const uint32_t ph = ((c / TC_NST) - 1) & 1;
-                if (c >= TC_NST && !bwait(&empty[s], ph, abort_flag))
+                const int s = c % NST;
+                const uint32_t ph = ((c / NST) - 1) & 1;
+                if (c >= NST && !bwait(&empty[s], ph, abort_flag))
                     break;
                 const int t0 = (int)(bos + chunk_t0(c));
                 uint8_t *st = sm + s * L::STAGE;
                 if (SO) {
                     // Y and Z, both free once the chunk's state update is done
-                    mbar_arrive_expect_tx(&full[s], L::YB + L::ZB);
+                    mbar_arrive_expect_tx(&full[s], L::YLB + L::ZB);
 #pragma unroll
-                    for (int b = 0; b < TC_D / 64; ++b)
+                    for (int b = 0; b < D / 64; ++b)
                         tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, hy, t0,
                                     (int)row);
 #pragma unroll
                     for (int b = 0; b < E / 64; ++b)
-                        tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s], 64 * b,
-                                    hz, t0, (int)row);
+                        tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &full[s],
+                                    64 * b + e0, hz, t0, (int)row);
                     ++issued;
                     continue;
                 }
                 // X and Y first: their slots are free once the chunk's state
                 // update is done and the next scores need them; the Z slot
                 // only once the output tile staged in it has left
-                mbar_arrive_expect_tx(&full[s], L::XB + L::YB);
+                mbar_arrive_expect_tx(&full[s], L::XB + L::YLB);
 #pragma unroll
-                for (int b = 0; b < TC_D / 64; ++b)
+                for (int b = 0; b < D / 64; ++b)
                     tma_load_4d(st + b * (TC_C * 128), &P.mx, &full[s], 64 * b, hx, t0, (int)row);
 #pragma unroll
-                for (int b = 0; b < TC_D / 64; ++b)
+                for (int b = 0; b < D / 64; ++b)
                     tma_load_4d(st + L::XB + b * (TC_C * 128), &P.my, &full[s], 64 * b, hy, t0,
                                 (int)row);
                 // Z is copied even when this wait gives up, so that the drain
                 // below sees the stage complete
-                const bool zok = c < TC_NST || bwait(&zfree[s], ph, abort_flag);
+                const bool zok = c < NST || bwait(&zfree[s], ph, abort_flag);
                 mbar_arrive_expect_tx(&zfull[s], L::ZB);
 #pragma unroll
                 for (int b = 0; b < E / 64; ++b)
-                    tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &zfull[s], 64 * b, hz,
-                                t0, (int)row);
+                    tma_load_4d(st + L::XB + L::YB + b * (TC_C * 128), &P.mz, &zfull[s],
+                                64 * b + e0, hz, t0, (int)row);
                 ++issued;
                 if (!zok)
                     break;
             }
             // every copy this thread issued has landed before the CTA may exit
-            for (int c = issued > TC_NST ? issued - TC_NST : 0; c < issued; ++c) {
-                drain_wait(&full[c % TC_NST], (c / TC_NST) & 1);
+            for (int c = issued > NST ? issued - NST : 0; c < issued; ++c) {
+                drain_wait(&full[c % NST], (c / NST) & 1);
                 if (!SO)
-                    drain_wait(&zfull[c % TC_NST], (c / TC_NST) & 1);
+                    drain_wait(&zfull[c % NST], (c / NST) & 1);
             }
         }
     } else if (warp == 1) {
@@ -501,10 +537,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             const uint32_t sbase = smem_u32(sm);
             const uint32_t sa = sbase + L::SOFF;
             bool any = false;
+            // S (piece pc: state rows 128 pc ..) += (lcol Y)^T Z  (both MN-major,
+            // M = 128 channels of Y, K = C tokens): the recurrence
+            auto state_update = [&](uint32_t ya, uint32_t za) {
+#pragma unroll
+                for (int pc = 0; pc < L::NP; ++pc)
+#pragma unroll
+                    for (int kk = 0; kk < TC_C / 16; ++kk)
+                        mma_ss(tm + TM_S + pc * E,
+                               sdesc_sw128(ya + pc * 2 * (TC_C * 128) + kk * 2048, TC_C * 128,
+                                           1024),
+                               sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_yz, 1);
+            };
             for (int c = 0; c < nc; ++c) {
-                const int s = c % TC_NST;
+                const int s = c % NST;
                 const uint32_t xa = sbase + s * L::STAGE, ya = xa + L::XB, za = ya + L::YB;
-                if (!bwait(&full[s], (c / TC_NST) & 1, abort_flag))
+                if (!bwait(&full[s], (c / NST) & 1, abort_flag))
                     break;
                 if (SO) {
                     // the state update alone, once the state is pre-scaled
@@ -512,10 +560,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     if (!bwait(s_ready, c & 1, abort_flag) || !bwait(p_ready, c & 1, abort_flag))
                         break;
                     tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < TC_C / 16; ++kk)
-                        mma_ss(tm + TM_S, sdesc_sw128(ya + kk * 2048, TC_C * 128, 1024),
-                               sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_yz, 1);
+                    state_update(ya, za);
                     mma_commit(ds_full);
                     mma_commit(&empty[s]);
                     any = true;
@@ -526,7 +571,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 tc_fence_after();
                 // scores = X Y^T  (both K-major, K = D)
 #pragma unroll
-                for (int kk = 0; kk < TC_D / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (TC_C * 128) + (kk & 3) * 32;
                     mma_ss(tm + TM_SC, sdesc_sw128(xa + off, 16, 1024),
                            sdesc_sw128(ya + off, 16, 1024), id_xy, kk > 0);
@@ -541,21 +586,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < TC_D / 16; ++kk) {
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (TC_C * 128) + (kk & 3) * 32;
                     mma_ss(tm + TM_OI, sdesc_sw128(xa + off, 16, 1024),
-                           sdesc_sw128(sa + kk * 2048, TC_D * 128, 1024), id_xz, kk > 0);
+                           sdesc_sw128(sa + kk * 2048, D * 128, 1024), id_xz, kk > 0);
                 }
                 if (!bwait(p_ready, c & 1, abort_flag))
                     break;
-                if (!bwait(&zfull[s], (c / TC_NST) & 1, abort_flag))
+                if (!bwait(&zfull[s], (c / NST) & 1, abort_flag))
                     break;
                 tc_fence_after();
-                // S += (lcol Y)^T Z  (both MN-major, M = D, K = C tokens): the recurrence
-#pragma unroll
-                for (int kk = 0; kk < TC_C / 16; ++kk)
-                    mma_ss(tm + TM_S, sdesc_sw128(ya + kk * 2048, TC_C * 128, 1024),
-                           sdesc_sw128(za + kk * 2048, TC_C * 128, 1024), id_yz, 1);
+                state_update(ya, za);
                 mma_commit(ds_full);
                 mma_commit(&empty[s]);   // X and Y have been read for the last time
                 // P Z  (P from TMEM, Z: MN-major, K = C tokens)
@@ -595,10 +636,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // ------------------------------------------------------- P group
             const int hh = (warp - 2) >> 2;
             const int j0 = 64 * hh;
+            // row i of every loaded 64-channel block of Y scaled in place
+            // (the two halves of the group take alternate blocks)
+            auto scale_y = [&](int s, float f) {
+#pragma unroll
+                for (int b = hh; b < D / 64; b += 2)
+                    scale_row_sw128(sm + s * L::STAGE + L::XB + b * (TC_C * 128) + i * 128, i, f);
+            };
             for (int c = 0; c < nc; ++c) {
-                const int s = c % TC_NST;
+                const int s = c % NST;
                 const int Lc = chunk_len(c);
-                bool ok = warp_all(bwait(&full[s], (c / TC_NST) & 1, abort_flag));
+                bool ok = warp_all(bwait(&full[s], (c / NST) & 1, abort_flag));
                 if (ok && !SO)
                     ok = warp_all(bwait(sc_full, c & 1, abort_flag));
                 // state only: no scores hold this group in step with the MMA
@@ -617,7 +665,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         const int pi = rev ? Lc - 1 - i : i;
                         lc = BWD ? scale * pw[pi + 1] : pw[Lc - 1 - pi];
                     }
-                    scale_row_sw128(sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128, i, lc);
+                    scale_y(s, lc);
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(p_ready);
@@ -684,7 +732,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         const int pi = rev ? Lc - 1 - i : i;
                         lc = BWD ? scale * pw[pi + 1] : pw[Lc - 1 - pi];
                     }
-                    scale_row_sw128(sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128, i, lc);
+                    scale_y(s, lc);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -694,14 +742,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         } else if (warp < 14) {
             // ------------------------------------------------------- S group
             const int64_t sb = ((int64_t)n * a.H + h) * (int64_t)a.D * a.E;
-            uint8_t *sbf = sm + L::SOFF + i * 128;
+            // thread i holds row r = 128 pc + i of state piece pc (TMEM lane i,
+            // columns TM_S + pc E ..) for every r < D; rows past D are padding
+            // that only ever receives zeros and is never read.  Whether a row
+            // exists is warp-uniform (D is a multiple of 64).
+            auto srow = [&](int pc) { return 128 * pc + i; };
+            auto sbf = [&](int pc) { return sm + L::SOFF + srow(pc) * 128; };
+            auto stm = [&](int pc) { return tm + lane_off + TM_S + pc * E; };
             // initial state: bf16 copy and gamma^L0-scaled fp32 in TMEM (an
             // empty sequence passes it straight to the final state)
             // gated form: factors of chunk position pc for key channel i (the
             // state's row i, or column i), [N][H][ncmax][128]; vo the chunk's
             // own factor, vn the next chunk's (also the initial state's)
             const int64_t vrow = ((int64_t)n * a.H + h) * a.gla_ncmax;
-            auto vidx = [&](int pc) { return (vrow + pc) * TC_D + i; };
+            auto vidx = [&](int cpos) { return (vrow + cpos) * D + i; };
             const float *vo = BWD ? a.gla_er : a.gla_u, *vn = BWD ? a.gla_u : a.gla_er;
             // GLA 2: this step's per-column factors, shared by the S group:
             // the chunk's own (colf) and the next chunk's (coln)
@@ -709,17 +763,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             float *coln = reinterpret_cast<float *>(sm + L::COLNOFF);
             auto sg_sync = [] { asm volatile("bar.sync 2, %0;" ::"n"(TC_SG) : "memory"); };
             if (nc == 0) {
-                state_copy(a.s_in, a.s_out, sb, i, E);
+#pragma unroll 1
+                for (int pc = 0; pc < L::NP; ++pc)
+                    if (srow(pc) < D)
+                        state_copy(a.s_in, a.s_out, sb, srow(pc), e0, E);
             } else if (GLA == 1) {
-                const float e0 = vn[vidx(flip ? nc - 1 : 0)];
-                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, e0, e0);
+                const float f0 = vn[vidx(flip ? nc - 1 : 0)];
+                state_in(a.s_in, sb, i, e0, E, sbf(0), D * 128, stm(0), f0, f0);
             } else if (GLA == 2) {
                 if (i < E)
                     colf[i] = vn[vidx(flip ? nc - 1 : 0)];
                 sg_sync();
-                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, 1.f, 1.f, colf);
+                state_in(a.s_in, sb, i, e0, E, sbf(0), D * 128, stm(0), 1.f, 1.f, colf);
             } else {
-                state_in(a.s_in, sb, i, E, sbf, tm + lane_off + TM_S, pw[chunk_len(0)], 1.f);
+#pragma unroll 1
+                for (int pc = 0; pc < L::NP; ++pc)
+                    if (srow(pc) < D)
+                        state_in(a.s_in, sb, srow(pc), e0, E, sbf(pc), D * 128, stm(pc),
+                                 pw[chunk_len(0)], 1.f);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -761,63 +822,71 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 tc_fence_after();
                 const float gn = ft;
 #pragma unroll 1
-                for (int eb = 0; eb < E / 64; ++eb) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32_issue(tm + lane_off + TM_S + 64 * eb, ra);
-                    tmem_ld32_issue(tm + lane_off + TM_S + 64 * eb + 32, rb);
-                    tmem_wait_ld(ra, rb);
-                    if (last) {
-                        if (a.s_out.p && !*abort_flag) {
-                            float *dst = a.s_out.p + sb + i * a.s_out.rs + 64 * eb * a.s_out.cs;
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) {
-                                const float f0 = GLA == 2 ? colf[64 * eb + k] : fo;
-                                const float f1 = GLA == 2 ? colf[64 * eb + 32 + k] : fo;
-                                ra[k] = __float_as_uint(f0 * __uint_as_float(ra[k]));
-                                rb[k] = __float_as_uint(f1 * __uint_as_float(rb[k]));
-                            }
-                            if (a.s_out.cs == 1 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                                // contiguous row: 16-byte stores
-#pragma unroll
-                                for (int k4 = 0; k4 < 8; ++k4) {
-                                    *reinterpret_cast<uint4 *>(dst + 4 * k4) =
-                                        make_uint4(ra[4 * k4], ra[4 * k4 + 1], ra[4 * k4 + 2],
-                                                   ra[4 * k4 + 3]);
-                                    *reinterpret_cast<uint4 *>(dst + 32 + 4 * k4) =
-                                        make_uint4(rb[4 * k4], rb[4 * k4 + 1], rb[4 * k4 + 2],
-                                                   rb[4 * k4 + 3]);
-                                }
-                            } else {
+                for (int pc = 0; pc < L::NP; ++pc) {
+                    if (srow(pc) >= D)
+                        continue;
+                    const int r = srow(pc);
+#pragma unroll 1
+                    for (int eb = 0; eb < E / 64; ++eb) {
+                        uint32_t ra[32], rb[32];
+                        tmem_ld32_issue(stm(pc) + 64 * eb, ra);
+                        tmem_ld32_issue(stm(pc) + 64 * eb + 32, rb);
+                        tmem_wait_ld(ra, rb);
+                        if (last) {
+                            if (a.s_out.p && !*abort_flag) {
+                                float *dst = a.s_out.p + sb + r * a.s_out.rs +
+                                             (int64_t)(e0 + 64 * eb) * a.s_out.cs;
 #pragma unroll
                                 for (int k = 0; k < 32; ++k) {
-                                    dst[k * a.s_out.cs] = __uint_as_float(ra[k]);
-                                    dst[(k + 32) * a.s_out.cs] = __uint_as_float(rb[k]);
+                                    const float f0 = GLA == 2 ? colf[64 * eb + k] : fo;
+                                    const float f1 = GLA == 2 ? colf[64 * eb + 32 + k] : fo;
+                                    ra[k] = __float_as_uint(f0 * __uint_as_float(ra[k]));
+                                    rb[k] = __float_as_uint(f1 * __uint_as_float(rb[k]));
+                                }
+                                if (a.s_out.cs == 1 &&
+                                    (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                                    // contiguous row: 16-byte stores
+#pragma unroll
+                                    for (int k4 = 0; k4 < 8; ++k4) {
+                                        *reinterpret_cast<uint4 *>(dst + 4 * k4) =
+                                            make_uint4(ra[4 * k4], ra[4 * k4 + 1], ra[4 * k4 + 2],
+                                                       ra[4 * k4 + 3]);
+                                        *reinterpret_cast<uint4 *>(dst + 32 + 4 * k4) =
+                                            make_uint4(rb[4 * k4], rb[4 * k4 + 1], rb[4 * k4 + 2],
+                                                       rb[4 * k4 + 3]);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int k = 0; k < 32; ++k) {
+                                        dst[k * a.s_out.cs] = __uint_as_float(ra[k]);
+                                        dst[(k + 32) * a.s_out.cs] = __uint_as_float(rb[k]);
+                                    }
                                 }
                             }
+                            continue;
                         }
-                        continue;
-                    }
-                    if (!GLA && !SO)
-                        store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
+                        if (!GLA && !SO)
+                            store_row_sw128(sbf(pc) + eb * (D * 128), r, ra, rb);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        if (GLA) {
-                            const float o0 = GLA == 2 ? colf[64 * eb + k] : fo;
-                            const float o1 = GLA == 2 ? colf[64 * eb + 32 + k] : fo;
-                            const float n0 = GLA == 2 ? coln[64 * eb + k] : fn;
-                            const float n1 = GLA == 2 ? coln[64 * eb + 32 + k] : fn;
-                            ra[k] = __float_as_uint(n0 * (o0 * __uint_as_float(ra[k])));
-                            rb[k] = __float_as_uint(n1 * (o1 * __uint_as_float(rb[k])));
-                        } else {
-                            ra[k] = __float_as_uint(gn * __uint_as_float(ra[k]));
-                            rb[k] = __float_as_uint(gn * __uint_as_float(rb[k]));
+                        for (int k = 0; k < 32; ++k) {
+                            if (GLA) {
+                                const float o0 = GLA == 2 ? colf[64 * eb + k] : fo;
+                                const float o1 = GLA == 2 ? colf[64 * eb + 32 + k] : fo;
+                                const float n0 = GLA == 2 ? coln[64 * eb + k] : fn;
+                                const float n1 = GLA == 2 ? coln[64 * eb + 32 + k] : fn;
+                                ra[k] = __float_as_uint(n0 * (o0 * __uint_as_float(ra[k])));
+                                rb[k] = __float_as_uint(n1 * (o1 * __uint_as_float(rb[k])));
+                            } else {
+                                ra[k] = __float_as_uint(gn * __uint_as_float(ra[k]));
+                                rb[k] = __float_as_uint(gn * __uint_as_float(rb[k]));
+                            }
                         }
+                        if (GLA)
+                            store_row_sw128(sbf(pc) + eb * (D * 128), r, ra, rb);
+                        tmem_st32_issue(stm(pc) + 64 * eb, ra);
+                        tmem_st32_issue(stm(pc) + 64 * eb + 32, rb);
+                        tmem_wait_st();
                     }
-                    if (GLA)
-                        store_row_sw128(sbf + eb * (TC_D * 128), i, ra, rb);
-                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb, ra);
-                    tmem_st32_issue(tm + lane_off + TM_S + 64 * eb + 32, rb);
-                    tmem_wait_st();
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -826,9 +895,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         } else {
             // ------------------------------------------------------- O group
             __nv_bfloat16 *obase = reinterpret_cast<__nv_bfloat16 *>(a.out.p) + row * a.out.sb +
-                                   (int64_t)h * a.out.sh;
+                                   (int64_t)h * a.out.sh + e0;
             for (int c = 0; c < (SO ? 0 : nc); ++c) {
-                const int s = c % TC_NST;
+                const int s = c % NST;
                 const int Lc = chunk_len(c);
                 if (!warp_all(bwait(o_full, c & 1, abort_flag)))
                     break;
@@ -866,8 +935,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     if (lane == 0) {
 #pragma unroll
                         for (int b = 0; b < E / 64; ++b)
-                            tma_store_4d(&P.mo, otile + b * (TC_C * 128) + q * 32 * 128, 64 * b, h,
-                                         (int)(bos + chunk_t0(c)) + 32 * q, (int)row);
+                            tma_store_4d(&P.mo, otile + b * (TC_C * 128) + q * 32 * 128, 64 * b + e0,
+                                         h, (int)(bos + chunk_t0(c)) + 32 * q, (int)row);
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }
@@ -942,19 +1011,22 @@ bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t 
 
 // Tile roles: X rows (scores = X Y^T, inter term X S), Y columns (scaled in
 // place for the state update), Z values.  Forward: (X, Y, Z) = (q, k, v);
-// backward: (k, q, w).
-template <int E, bool BWD, int GLA, bool SO = false>
+// backward: (k, q, w).  D = a.D; E is the value tile of one CTA (a.E / E
+// CTAs per (sequence, head)).
+template <int D, int E, bool BWD, int GLA, bool SO = false>
 cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullptr)
 {
+    if (a.D != D || a.E % E != 0)
+        return cudaErrorNotSupported;
     TcParams p;
     // tile roles; the gated form names its three operands itself
     const Tok x = xyz ? xyz[0] : (BWD ? a.k : a.q), y = xyz ? xyz[1] : (BWD ? a.q : a.k);
     const Tok z = xyz ? xyz[2] : a.v;
     // state only: no X, no output (their maps are not used)
-    if ((!SO && !make_map(&p.mx, x.p, TC_D, a, x.sb, x.st, x.sh, TC_C, x.hdiv)) ||
-        !make_map(&p.my, y.p, TC_D, a, y.sb, y.st, y.sh, TC_C, y.hdiv) ||
-        !make_map(&p.mz, z.p, E, a, z.sb, z.st, z.sh, TC_C, z.hdiv) ||
-        (!SO && !make_map(&p.mo, a.out.p, E, a, a.out.sb, a.out.st, a.out.sh, 32)))
+    if ((!SO && !make_map(&p.mx, x.p, D, a, x.sb, x.st, x.sh, TC_C, x.hdiv)) ||
+        !make_map(&p.my, y.p, D, a, y.sb, y.st, y.sh, TC_C, y.hdiv) ||
+        !make_map(&p.mz, z.p, a.E, a, z.sb, z.st, z.sh, TC_C, z.hdiv) ||
+        (!SO && !make_map(&p.mo, a.out.p, a.E, a, a.out.sb, a.out.st, a.out.sh, 32)))
         return cudaErrorNotSupported;
     if (SO)
         p.mx = p.mo = p.my;
@@ -962,9 +1034,9 @@ cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullp
     p.dx = x.hdiv;
     p.dy = y.hdiv;
     p.dz = z.hdiv;
-    auto kern = tc_sweep_kernel<E, BWD, GLA, SO>;
+    auto kern = tc_sweep_kernel<D, E, BWD, GLA, SO>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           TcLayout<E>::DYN);
+                                           TcLayout<D, E>::DYN);
     if (err != cudaSuccess)
         return err;
     // programmatic dependent launch: the CTAs may be scheduled, and run their
@@ -974,9 +1046,9 @@ cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullp
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)a.N * a.H));
+    cfg.gridDim = dim3((unsigned)((int64_t)a.N * a.H * (a.E / E)));
     cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = TcLayout<E>::DYN;
+    cfg.dynamicSmemBytes = TcLayout<D, E>::DYN;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -989,11 +1061,18 @@ cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullp
 
 }  // namespace
 
+// Value columns per CTA for key width D and a.E value columns: 128 where the
+// state (D <= 128 rows) leaves TMEM room for it, else 64.
+int tc_value_tile(int D, int E) { return D <= 128 && E % 128 == 0 ? 128 : 64; }
+
 bool tc_sweep_supported(const SweepArgs &a)
 {
-    if (!a.bf16 || a.D != TC_D || (a.E != 64 && a.E != 128) || a.T < 1 || a.B < 1)
+    if (!a.bf16 || a.T < 1 || a.B < 1)
         return false;
-    if ((int64_t)a.N * a.H > INT_MAX)
+    if ((a.D != 64 && a.D != 128 && a.D != 192 && a.D != 256) || a.E % 64 != 0 || a.E < 64 ||
+        a.E > 256)
+        return false;
+    if ((int64_t)a.N * a.H * (a.E / tc_value_tile(a.D, a.E)) > INT_MAX)
         return false;
     return aligned_tok(a.q.p, a.q.sb, a.q.st, a.q.sh) &&
            aligned_tok(a.k.p, a.k.sb, a.k.st, a.k.sh) &&
@@ -1001,19 +1080,30 @@ bool tc_sweep_supported(const SweepArgs &a)
            aligned_tok(a.out.p, a.out.sb, a.out.st, a.out.sh);
 }
 
-cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s)
+namespace {
+template <bool BWD> cudaError_t tc_sweep(const SweepArgs &a, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
-    return a.E == 128 ? launch_tc<128, false, 0>(a, s) : launch_tc<64, false, 0>(a, s);
+    const bool wide = tc_value_tile(a.D, a.E) == 128;
+    switch (a.D) {
+    case 64:
+        return wide ? launch_tc<64, 128, BWD, 0>(a, s) : launch_tc<64, 64, BWD, 0>(a, s);
+    case 128:
+        return wide ? launch_tc<128, 128, BWD, 0>(a, s) : launch_tc<128, 64, BWD, 0>(a, s);
+    case 192:
+        return launch_tc<192, 64, BWD, 0>(a, s);
+    case 256:
+        return launch_tc<256, 64, BWD, 0>(a, s);
+    default:
+        return cudaErrorNotSupported;
+    }
 }
+}  // namespace
 
-cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s)
-{
-    if (a.N == 0)
-        return cudaSuccess;
-    return a.E == 128 ? launch_tc<128, true, 0>(a, s) : launch_tc<64, true, 0>(a, s);
-}
+cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s) { return tc_sweep<false>(a, s); }
+
+cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s) { return tc_sweep<true>(a, s); }
 
 cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, const Tok &y,
                          const Tok &z, cudaStream_t s)
@@ -1021,24 +1111,32 @@ cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, 
     if (a.N == 0)
         return cudaSuccess;
     const Tok xyz[3] = {x, y, z};
+    if (a.D != 128 || (a.E != 64 && a.E != 128))
+        return cudaErrorNotSupported;   // one CTA per (sequence, head), 128 key channels
     if (cols && a.E != 128)
         return cudaErrorNotSupported;   // column factors: 128 key channels as columns
     if (bwd)
-        return cols ? launch_tc<128, true, 2>(a, s, xyz)
-                    : (a.E == 128 ? launch_tc<128, true, 1>(a, s, xyz)
-                                  : launch_tc<64, true, 1>(a, s, xyz));
-    return cols ? launch_tc<128, false, 2>(a, s, xyz)
-                : (a.E == 128 ? launch_tc<128, false, 1>(a, s, xyz)
-                              : launch_tc<64, false, 1>(a, s, xyz));
+        return cols ? launch_tc<128, 128, true, 2>(a, s, xyz)
+                    : (a.E == 128 ? launch_tc<128, 128, true, 1>(a, s, xyz)
+                                  : launch_tc<128, 64, true, 1>(a, s, xyz));
+    return cols ? launch_tc<128, 128, false, 2>(a, s, xyz)
+                : (a.E == 128 ? launch_tc<128, 128, false, 1>(a, s, xyz)
+                              : launch_tc<128, 64, false, 1>(a, s, xyz));
 }
 
 cudaError_t tc_state_sweep(const SweepArgs &a, bool bwd, cudaStream_t s)
 {
     if (a.N == 0)
         return cudaSuccess;
+    // the state-only mode is built for 128 key channels and one value tile;
+    // other shapes run the full sweep instead (the caller's fallback)
+    if (a.D != 128 || (a.E != 64 && a.E != 128))
+        return cudaErrorNotSupported;
     if (bwd)
-        return a.E == 128 ? launch_tc<128, true, 0, true>(a, s) : launch_tc<64, true, 0, true>(a, s);
-    return a.E == 128 ? launch_tc<128, false, 0, true>(a, s) : launch_tc<64, false, 0, true>(a, s);
+        return a.E == 128 ? launch_tc<128, 128, true, 0, true>(a, s)
+                          : launch_tc<128, 64, true, 0, true>(a, s);
+    return a.E == 128 ? launch_tc<128, 128, false, 0, true>(a, s)
+                      : launch_tc<128, 64, false, 0, true>(a, s);
 }
 
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err)

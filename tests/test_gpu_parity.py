@@ -94,7 +94,8 @@ def test_ragged_lengths(T, dtype, D):
 
 
 @pytest.mark.parametrize("D,E", [(32, 32), (64, 128), (128, 64), (128, 128), (192, 192),
-                                 (256, 256), (16, 48), (80, 96), (1, 1)])
+                                 (256, 256), (16, 48), (80, 96), (1, 1), (64, 64), (192, 128),
+                                 (128, 192), (256, 64)])
 def test_head_dims(D, E):
     w = _custom(1, 200, 2, D, E, torch.bfloat16, init=0.2, dfin=0.2)
     x = W.make_inputs(w, seed=D * 1000 + E)
@@ -177,6 +178,36 @@ def test_tensor_core_path_is_selected_for_the_benchmark_shape():
     assert la.kernel_family(4, 32768, 32, 128, 128) == 1
     assert la.kernel_family(1, 4096, 16, 128, 64) == 1
     assert la.kernel_family(1, 256, 2, 32, 32, dtype=torch.float32) == 0
+
+
+def test_tensor_core_path_is_selected_for_the_other_head_dims():
+    # the small bf16 shape (d = e = 64) and the non-power-of-two one (d = e = 192,
+    # the OpenNLPLab README's usage example) run on the tensor cores too
+    assert la.kernel_family(2, 2048, 8, 64, 64) == 1
+    assert la.kernel_family(2, 2048, 12, 192, 192) == 1
+    assert la.kernel_family(1, 300, 2, 256, 64) == 1
+    assert la.kernel_family(1, 300, 2, 64, 256) == 1
+    # widths that are not multiples of 64 stay on the CUDA-core kernels
+    assert la.kernel_family(1, 300, 2, 96, 96) == 0
+    assert la.kernel_family(1, 300, 2, 128, 80) == 0
+
+
+@pytest.mark.parametrize("D,E", [(64, 64), (64, 192), (192, 64), (192, 192), (256, 128),
+                                 (128, 256)])
+def test_tensor_core_head_dims_packed_states_both_directions(D, E):
+    # packed sequences with an empty one and ragged tails, initial state and
+    # final-state gradient, forward and reverse: every value tile of every
+    # (sequence, head) and every 128-row piece of the state
+    lens = [0, 300, 1, 129, 517, 64]
+    w = _custom(1, 0, 2, D, E, torch.bfloat16, seqlens=lens, init=0.1, dfin=0.1,
+                g=torch.tensor([-0.01, -0.4]))
+    x = W.make_inputs(w, seed=D + 7 * E)
+    for reverse in (False, True):
+        got = gpu_run(x, reverse)
+        compare(got, oracle_run(x, reverse), TOL[torch.bfloat16], cu=x["cu_seqlens"],
+                label="D=%d E=%d rev=%d" % (D, E, reverse))
+        assert torch.equal(got["final_state"][0], x["initial_state"][0])
+        assert torch.equal(got["d_initial_state"][0], x["d_final_state"][0])
 
 
 def test_unaligned_layout_falls_back_and_matches():
