@@ -434,6 +434,7 @@ def gpu_bench(args):
     }
     if not args.no_sweep:
         line["sweep"] = length_sweep(la, torch, dev, stream, T)
+        line["configs"] = configs_bench(la, torch, dev, stream, peak, tpeak)
         line["decode"] = decode_bench(la, torch, dev, stream, peak)
         line["long_sequence"] = split_bench(la, torch, dev, stream, peak)
         line["grouped_kv"] = gqa_bench(la, torch, dev, stream, peak)
@@ -516,6 +517,105 @@ def length_sweep(la, torch, dev, stream, skip_n):
             out[str(n)]["fwd_ms_unflushed"] = timed(fwd, False)
             out[str(n)]["bwd_ms_unflushed"] = timed(bwd, False)
         del q, k, v, do
+    return out
+
+
+def _timed_calls(torch, stream, fn, flush=None, calls=5, warm=3):
+    """Mean event time of `calls` calls of fn queued behind torch.cuda._sleep (no host
+    gap enters the events), after `warm` untimed calls; with `flush`, that buffer is
+    overwritten before each call (an L2 flush, inside the stream but outside the events)."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    torch.cuda._sleep(20_000_000)
+    for _ in range(calls):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
+
+
+def packed_work(T, H, d, e, n_seqs, token_bytes=2):
+    """The method's work for packed sequences with states in and out (same accounting as
+    method_work): forward adds the initial state read and the final state written,
+    backward the initial state (dq sweep) and d_final_state read and d_initial_state
+    written."""
+    w = method_work(1, T, H, d, e, token_bytes)
+    st = n_seqs * H * d * e * 4
+    w["fwd_bytes"] = T * H * token_bytes * (2 * d + 2 * e) + 2 * st
+    w["bwd_bytes"] = T * H * token_bytes * (4 * d + 3 * e) + 3 * st
+    return w
+
+
+def configs_bench(la, torch, dev, stream, hbm, tfl):
+    """The other workload shapes, fwd and bwd timed separately (mean of 5 queued
+    calls after 3 warm-up calls):
+      * b2 h8 n2048 d=e=64 and b2 h12 n2048 d=e=192 (bf16): their token tensors fit
+        in L2, so each call follows a 512 MB L2 flush (`*_ms`); back to back without
+        one in `*_ms_unflushed`;
+      * 16 packed sequences of U[64, 8192] tokens (seed 0), h16 d=e=128 bf16, initial
+        state and d_final_state in, final state and d_initial_state out, reverse off
+        and on; each with the longest-first schedule (the library's workspace) and
+        without it (no workspace: index order).  Its tensors exceed L2; no flush.
+    Fractions are the method's roofline against the measured peaks."""
+    import workloads as W
+    out = {}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for w in (W.small_bf16(), W.d192_bf16()):
+        gen = torch.Generator(device=dev).manual_seed(23)
+        q, k = (torch.randn((w.B, w.T, w.H, w.d), generator=gen, device=dev).bfloat16()
+                for _ in range(2))
+        v, do = (torch.randn((w.B, w.T, w.H, w.e), generator=gen, device=dev).bfloat16()
+                 for _ in range(2))
+        g = w.g_gamma.to(dev)
+        fwd = lambda: la.la_fwd(q, k, v, g, w.scale)
+        bwd = lambda: la.la_bwd(q, k, v, do, g, w.scale, want_d_initial_state=False)
+        f_ms, b_ms = _timed_calls(torch, stream, fwd, flush), _timed_calls(torch, stream, bwd, flush)
+        rf = method_roofline(method_work(w.B, w.T, w.H, w.d, w.e), f_ms, b_ms, hbm, tfl)
+        out[w.name] = {
+            "kernel_family": la.kernel_family(w.B, w.T, w.H, w.d, w.e),
+            "fwd_ms": f_ms, "bwd_ms": b_ms, "tokens_per_s": w.B * w.T / ((f_ms + b_ms) * 1e-3),
+            "roofline_frac_fwd": rf["fwd"]["frac"], "roofline_frac_bwd": rf["bwd"]["frac"],
+            "tflops_fwd": rf["fwd"]["tflops"], "tflops_bwd": rf["bwd"]["tflops"],
+            "fwd_ms_unflushed": _timed_calls(torch, stream, fwd),
+            "bwd_ms_unflushed": _timed_calls(torch, stream, bwd),
+            "l2": "flushed before each call (512 MB write)"}
+        del q, k, v, do
+    w = W.varlen_bf16(seed=0)
+    gen = torch.Generator(device=dev).manual_seed(29)
+    q, k = (torch.randn((1, w.T, w.H, w.d), generator=gen, device=dev).bfloat16()
+            for _ in range(2))
+    v, do = (torch.randn((1, w.T, w.H, w.e), generator=gen, device=dev).bfloat16()
+             for _ in range(2))
+    S = (w.num_seqs, w.H, w.d, w.e)
+    init = torch.randn(S, generator=gen, device=dev) * 0.02
+    dfin = torch.randn(S, generator=gen, device=dev) * 0.02
+    g = w.g_gamma.to(dev)
+    cu = w.cu_seqlens
+    work = packed_work(w.T, w.H, w.d, w.e, w.num_seqs)
+    pk = {"workload": "16 packed sequences, lengths U[64, 8192] (seed 0, %d tokens, longest %d),"
+                      " h16 d=e=128 bf16, states in and out" % (w.T, max(w.seqlens)),
+          "tokens": w.T}
+    for rev in (False, True):
+        for sched in (True, False):
+            fwd = lambda: la.la_fwd(q, k, v, g, w.scale, init, rev, cu, workspace=sched)
+            bwd = lambda: la.la_bwd(q, k, v, do, g, w.scale, init, dfin, rev, cu,
+                                    workspace=sched)
+            f_ms, b_ms = _timed_calls(torch, stream, fwd), _timed_calls(torch, stream, bwd)
+            rf = method_roofline(work, f_ms, b_ms, hbm, tfl)
+            pk["%s_%s" % ("reverse" if rev else "forward",
+                          "longest_first" if sched else "index_order")] = {
+                "fwd_ms": f_ms, "bwd_ms": b_ms, "tokens_per_s": w.T / ((f_ms + b_ms) * 1e-3),
+                "roofline_frac_fwd": rf["fwd"]["frac"], "roofline_frac_bwd": rf["bwd"]["frac"]}
+    out["varlen16_h16_d128_bf16"] = pk
+    la.get_device_error(dev)
+    del q, k, v, do, flush
     return out
 
 
@@ -812,7 +912,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=None)
     ap.add_argument("--only", default=None,
-                    choices=["sweep", "decode", "long_sequence", "grouped_kv", "gated"],
+                    choices=["sweep", "configs", "decode", "long_sequence", "grouped_kv",
+                             "gated"],
                     help="run one of the secondary measurements alone (one GPU) and print "
                          "its JSON object")
     args = ap.parse_args()
@@ -834,7 +935,9 @@ def section_only(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     peak, _ = peaks()
+    tpeak, _ = tensor_peak()
     fn = {"sweep": lambda: length_sweep(la, torch, dev, stream, args.n),
+          "configs": lambda: configs_bench(la, torch, dev, stream, peak, tpeak),
           "decode": lambda: decode_bench(la, torch, dev, stream, peak),
           "long_sequence": lambda: split_bench(la, torch, dev, stream, peak),
           "grouped_kv": lambda: gqa_bench(la, torch, dev, stream, peak),

@@ -194,9 +194,11 @@ def _like(t: Tensor) -> Tensor:
 def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = None,
            initial_state: Optional[Tensor] = None, reverse: bool = False,
            cu_seqlens=None, out: Optional[Tensor] = None,
-           final_state: Optional[Tensor] = None, want_final_state: bool = True
-           ) -> Tuple[Tensor, Optional[Tensor]]:
-    """Forward pass. q, k: [B,T,H,D]; v: [B,T,H,E]; returns (o [B,T,H,E], final [N,H,D,E])."""
+           final_state: Optional[Tensor] = None, want_final_state: bool = True,
+           workspace: bool = True) -> Tuple[Tensor, Optional[Tensor]]:
+    """Forward pass. q, k: [B,T,H,D]; v: [B,T,H,E]; returns (o [B,T,H,E], final [N,H,D,E]).
+    workspace=False passes no device workspace: packed sequences then run in index
+    order (no longest-first schedule) and never split."""
     _check_tokens(q, k, v)
     q, k, v = _channel_contiguous((q, k, v))
     grouped = k.shape[2] != q.shape[2]
@@ -220,7 +222,7 @@ def la_fwd(q: Tensor, k: Tensor, v: Tensor, g_gamma, scale: Optional[float] = No
     if final_state is None and want_final_state:
         final_state = torch.empty((Nst, H, D, E), device=dev, dtype=torch.float32)
     dims = _dims(q, k, v, out, packed)
-    ws = packed.ws_args(dims, _dtype_code(q))
+    ws = packed.ws_args(dims, _dtype_code(q)) if workspace else (None, 0)
     st = N.lib().la_fwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                         scale, _ptr(init), int(bool(reverse)), _ptr(packed.dev),
                         packed.host_ptr(), _ptr(out), _ptr(final_state), *ws,
@@ -252,16 +254,18 @@ def _bwd_prep(q, k, v, do, g_gamma, scale, initial_state, d_final_state, cu_seql
 @_traced
 def la_bwd(q: Tensor, k: Tensor, v: Tensor, do: Tensor, g_gamma, scale: Optional[float] = None,
            initial_state: Optional[Tensor] = None, d_final_state: Optional[Tensor] = None,
-           reverse: bool = False, cu_seqlens=None, want_d_initial_state: bool = True):
+           reverse: bool = False, cu_seqlens=None, want_d_initial_state: bool = True,
+           workspace: bool = True):
     """Backward pass: returns (dq, dk, dv, d_initial_state) of
-    sum(o*do) + sum(final_state*d_final_state)."""
+    sum(o*do) + sum(final_state*d_final_state).  workspace=False as in la_fwd (not
+    with grouped key/value heads, which need it)."""
     q, k, v, do, dev, packed, g, scale, init, dfin, Nst = _bwd_prep(
         q, k, v, do, g_gamma, scale, initial_state, d_final_state, cu_seqlens)
     dq, dk, dv = _like(q), _like(k), _like(v)
     dinit = (torch.empty((Nst, q.shape[2], q.shape[3], v.shape[3]), device=dev,
                          dtype=torch.float32) if want_d_initial_state else None)
     dims = _dims(q, k, v, do, packed)
-    ws = packed.ws_args(dims, _dtype_code(q))
+    ws = packed.ws_args(dims, _dtype_code(q)) if workspace else (None, 0)
     st = N.lib().la_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(do),
                         _ptr(g), scale, _ptr(init), _ptr(dfin), int(bool(reverse)),
                         _ptr(packed.dev), packed.host_ptr(), _ptr(dq), _ptr(dk), _ptr(dv),

@@ -499,6 +499,40 @@ la_status bwd_dq(const Problem &P, const la_dims *d, int32_t dtype, const void *
     return run_forward_type(a, s);
 }
 
+// dk and dv of grouped key/value heads: each group's per-query-head
+// contributions (in the workspace) summed into dk and dv.
+la_status gqa_sum(const Problem &P, const GqaBufs *gqa, void *dk, void *dv, int bf16,
+                  cudaStream_t s)
+{
+    const int rows = P.packed ? 1 : P.B;
+    cudaError_t e = la::gqa_reduce(gqa->ck.p, tok_out(dk, P.k_st), rows, P.T, P.Hkv, P.G, P.D,
+                                   bf16, s);
+    if (e == cudaSuccess)
+        e = la::gqa_reduce(gqa->cv.p, tok_out(dv, P.kv_v_st), rows, P.T, P.Hkv, P.G, P.E, bf16,
+                           s);
+    return e == cudaSuccess ? LA_OK : cuda_fail(e, "grouped key/value gradient sum");
+}
+
+// The dv half of the backward: the fused dk/dv sweep (the tensor-core kernel
+// of la_tc_dkdv.cu) when `fused` and its tensor maps can be built (*ran set),
+// else the dv sweep alone (the dk sweep follows).
+la_status run_dv(const la::SweepArgs &a, bool fused, const la::Tok &v, const la::TokOut &dk,
+                 cudaStream_t s, bool *ran)
+{
+    *ran = false;
+    if (fused) {
+        la::SweepArgs b = a;
+        b.withhold_handoff = g_withhold;
+        cudaError_t e = la::tc_dkdv_sweep(b, v, dk, s);
+        if (e != cudaErrorNotSupported) {
+            g_withhold = 0;
+            *ran = e == cudaSuccess;
+            return e == cudaSuccess ? LA_OK : cuda_fail(e, "dk/dv sweep launch");
+        }
+    }
+    return run_backward_type(a, s);
+}
+
 la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void *q,
                    const void *k, const void *v, const void *d_o, const float *g_gamma,
                    float scale, const float *dfinal, int32_t reverse, const int32_t *cu,
@@ -517,9 +551,14 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
     a.s_in = la::StateIn{dfinal, P.E, 1};
     a.s_out = la::StateOut{dinit, P.E, 1};
     la::StateIn g_dk{dfinal, 1, P.E};   // G^T for the dk sweep
+    const la::Tok vt = tok(v, P.kv_v_st, P.G);
+    const la::TokOut dkt = gqa ? gqa->ck : tok_out(dk, P.k_st);
+    // dk and dv in one sweep where the fused tensor-core kernel applies
+    const bool fused = a.max_len > la::SHORT_MAX_T && la::tc_dkdv_supported(a, vt, dkt);
     la_status st;
+    bool fused_ran = false;
     if (!S) {
-        st = run_backward_type(a, s);
+        st = run_dv(a, fused, vt, dkt, s, &fused_ran);
     } else {
         // split: segment G from zero, scan from d_final (against processing
         // order), d_initial from the scan, then dv from each segment's G
@@ -534,12 +573,14 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
         if (st == LA_OK) {
             a.s_in = la::StateIn{b->W, P.E, 1};
             a.s_out = la::StateOut{nullptr, 0, 0};
-            st = run_backward_type(a, s);
+            st = run_dv(a, fused, vt, dkt, s, &fused_ran);
         }
         g_dk = la::StateIn{b->W, 1, P.E};
     }
     if (st != LA_OK)
         return st;
+    if (fused_ran)
+        return gqa ? gqa_sum(P, gqa, dk, dv, a.bf16, s) : LA_OK;
     // dk: (q, k, w) := (do, v, q), G^T (E x D)
     a.D = P.E;
     a.E = P.D;
@@ -551,14 +592,7 @@ la_status bwd_dkdv(const Problem &P, const la_dims *d, int32_t dtype, const void
     a.s_out = la::StateOut{nullptr, 0, 0};
     if ((st = run_backward_type(a, s)) != LA_OK || !gqa)
         return st;
-    // grouped key/value heads: sum each group's per-query-head contributions
-    const int rows = P.packed ? 1 : P.B;
-    cudaError_t e = la::gqa_reduce(gqa->ck.p, tok_out(dk, P.k_st), rows, P.T, P.Hkv, P.G, P.D,
-                                   a.bf16, s);
-    if (e == cudaSuccess)
-        e = la::gqa_reduce(gqa->cv.p, tok_out(dv, P.kv_v_st), rows, P.T, P.Hkv, P.G, P.E, a.bf16,
-                           s);
-    return e == cudaSuccess ? LA_OK : cuda_fail(e, "grouped key/value gradient sum");
+    return gqa_sum(P, gqa, dk, dv, a.bf16, s);
 }
 
 }  // namespace
@@ -744,13 +778,15 @@ la_status la_get_device_error(void *stream)
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e == cudaSuccess)
         e = la::tc_read_and_clear_error((cudaStream_t)stream, &err);
-    int err2 = 0;
+    int err2 = 0, err3 = 0;
     if (e == cudaSuccess)
         e = la::token_read_and_clear_error((cudaStream_t)stream, &err2);
+    if (e == cudaSuccess)
+        e = la::tc_dkdv_read_and_clear_error((cudaStream_t)stream, &err3);
     if (e != cudaSuccess)
         return cuda_fail(e, "la_get_device_error");
     if (!err)
-        err = err2;
+        err = err2 ? err2 : err3;
     if (err)
         return fail(LA_ERR_TIMEOUT, "an on-device wait ran out (code %d)", err);
     return LA_OK;

@@ -205,4 +205,13 @@ cudaError_t split_scan(const SplitScanArgs &a, cudaStream_t s);
 // Device error word of the tensor-core kernels (bounded waits that ran out).
 cudaError_t tc_read_and_clear_error(cudaStream_t s, int *err);
 
+// The backward's dk and dv in one tensor-core sweep (la_tc_dkdv.cu): bf16,
+// D = E = 128, layouts TMA can describe.  Arguments as the dv sweep (a.q = q,
+// a.k = k, a.v = do, a.out = dv, a.s_in = dL/dfinal as D x E, a.s_out =
+// dL/dinitial) plus v and dk.  cudaErrorNotSupported when the tensor maps
+// cannot be built.
+bool tc_dkdv_supported(const SweepArgs &a, const Tok &v, const TokOut &dk);
+cudaError_t tc_dkdv_sweep(const SweepArgs &a, const Tok &v, const TokOut &dk, cudaStream_t s);
+cudaError_t tc_dkdv_read_and_clear_error(cudaStream_t s, int *err);
+
 }  // namespace la
