@@ -112,23 +112,33 @@ __device__ __forceinline__ bool pg_all(bool ok)
     return all != 0;
 }
 
+// Two bf16 products in one instruction (round to nearest even).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Row i of both 64-channel blocks of the 128B-swizzled tile at t, times f, in
-// place, four 16-byte chunks at a time (all four loaded before any is stored).
+// place: the factor is rounded to bf16 once and each product to bf16 (as an
+// in-place scaling of a bf16 tile must be); each block's eight 16-byte chunks
+// are all loaded before any is stored.
 __device__ __forceinline__ void scale_tile_row(uint8_t *t, int i, float f)
 {
+    const uint32_t f2 = pack_bf16x2(f, f);
 #pragma unroll 1
     for (int b = 0; b < 2; ++b) {
         uint8_t *rowp = t + b * (TC_C * 128) + i * 128;
-#pragma unroll 1
-        for (int h4 = 0; h4 < 2; ++h4) {
-            uint4 v[4];
+        uint4 v[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                v[k] = *reinterpret_cast<const uint4 *>(rowp + (((4 * h4 + k) ^ (i & 7)) << 4));
+        for (int k = 0; k < 8; ++k)
+            v[k] = *reinterpret_cast<const uint4 *>(rowp + ((k ^ (i & 7)) << 4));
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(rowp + (((4 * h4 + k) ^ (i & 7)) << 4)) = scale8(v[k], f);
-        }
+        for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4 *>(rowp + ((k ^ (i & 7)) << 4)) =
+                make_uint4(mul_bf16x2(v[k].x, f2), mul_bf16x2(v[k].y, f2), mul_bf16x2(v[k].z, f2),
+                           mul_bf16x2(v[k].w, f2));
     }
 }
 
