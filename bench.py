@@ -469,9 +469,10 @@ def length_sweep(la, torch, dev, stream, skip_n):
     """fwd and bwd times at every length of the Lightning-2 benchmark table (b4 h32
     d=e=128 bf16), each the mean of 5 calls after 3 warm-up calls.  The GPU is first
     held busy (torch.cuda._sleep) so that all 5 calls are queued before the first
-    runs and host-side call overhead stays out of the events.  Lengths whose four
-    token tensors fit twice in L2 are timed with a 512 MB L2 flush before each call
-    (`fwd_ms`, `bwd_ms`) and also back to back without one (`*_unflushed`)."""
+    runs and host-side call overhead stays out of the events.  Lengths up to 4096
+    tokens are timed with a 512 MB L2 flush before each call (`fwd_ms`, `bwd_ms`)
+    and also back to back without one (`*_unflushed`); longer ones stream more
+    than the 129 MB L2 holds per call and are timed back to back."""
     import workloads as W
     out = {}
     hbm, tfl = peaks()[0], tensor_peak()[0]
@@ -484,7 +485,7 @@ def length_sweep(la, torch, dev, stream, skip_n):
         q, k, v, do = (torch.randn((w.B, n, w.H, w.d), generator=gen, device=dev).bfloat16()
                        for _ in range(4))
         g = w.g_gamma.to(dev)
-        small = 4 * w.B * n * w.H * w.d * 2 < 2 * 129e6
+        small = n <= 4096
 
         def timed(fn, flush_first):
             for _ in range(3):
@@ -786,12 +787,14 @@ def gla_bench(la, torch, dev, stream, peak):
 
 
 def source_sha():
-    """Hash of the sources the tensor-core sweep kernel is built from (the
-    kernel whose ncu traffic profiles/traffic_tc_sweep_kernel.json records)."""
+    """Hash of the sources the tensor-core kernels of the step are built from
+    (the sweep kernel and the fused dk/dv kernel, whose ncu traffic
+    profiles/traffic_tc_sweep_kernel.json records)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_head_gb300", "csrc")
-    for f in ("la_internal.h", "la_sm100.cuh", "la_tc_sweep.cu"):
+    for f in ("la_internal.h", "la_sm100.cuh", "la_tc_common.cuh", "la_tc_sweep.cu",
+              "la_tc_dkdv.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
