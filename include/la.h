@@ -86,7 +86,9 @@ typedef enum la_status {
     LA_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride or cu_seqlens        */
     LA_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels handle  */
     LA_ERR_CUDA = 3,          /* a CUDA runtime call or a launch failed         */
-    LA_ERR_TIMEOUT = 4        /* a bounded on-device wait ran out (device word) */
+    LA_ERR_TIMEOUT = 4,       /* a bounded on-device wait ran out (device word) */
+    LA_ERR_BOUNDS = 5         /* an index check of the bounds-checking build
+                                 failed (device word; never in the normal build) */
 } la_status;
 
 /* Element type of the token tensors q, k, v, o, do, dq, dk, dv.  g_gamma and
@@ -339,11 +341,16 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype,
 size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype,
                              const int32_t *cu_seqlens_host, int32_t with_forward_operands);
 
-/* Reads and clears the device-side error word that bounded on-device waits
+/* Reads and clears the device-side error words that bounded on-device waits
  * set when they run out (LA_ERR_TIMEOUT), after synchronizing `stream`.
  * Returns LA_OK when no wait ran out, LA_ERR_TIMEOUT when one did, or
- * LA_ERR_CUDA when the synchronization itself failed.  The word is shared by
- * every stream of the current device. */
+ * LA_ERR_CUDA when the synchronization itself failed.  The words are shared
+ * by every stream of the current device.
+ * A library built with LA_CHECK_BOUNDS defined (build.py --checked) also
+ * checks the tensor-core kernels' shared-memory, TMEM, descriptor, table and
+ * global indices; a failed check skips the access and records the first
+ * failing site here, reported as LA_ERR_BOUNDS with the site number in
+ * la_last_error(). */
 la_status la_get_device_error(void *stream);
 
 /* Diagnostic, for testing error reporting: with on != 0, the next launch of
@@ -355,6 +362,12 @@ la_status la_get_device_error(void *stream);
  * its outputs are undefined, and la_get_device_error reports LA_ERR_TIMEOUT.
  * The switch resets itself after that launch and is off by default. */
 la_status la_debug_withhold_next_handoff(int32_t on);
+
+/* How this copy of the library was built: LA_BUILD_BOUNDS_CHECKED set when
+ * the tensor-core kernels' index checks are compiled in (build.py --checked,
+ * liblagb300_checked.so; see la_get_device_error).  Pure host function. */
+#define LA_BUILD_BOUNDS_CHECKED 1
+int32_t la_build_flags(void);
 
 /* Static description of a status code (never NULL). */
 const char *la_strerror(int32_t status);

@@ -8,18 +8,22 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "liblagb300.so")
+# LA_LIBRARY in the environment names another build of the same library (the
+# bounds-checking one, liblagb300_checked.so) to load instead
+LIB_PATH = os.environ.get("LA_LIBRARY") or os.path.join(HERE, "liblagb300.so")
 
 LA_OK = 0
 LA_ERR_INVALID_ARG = 1
 LA_ERR_UNSUPPORTED = 2
 LA_ERR_CUDA = 3
 LA_ERR_TIMEOUT = 4
+LA_ERR_BOUNDS = 5
 
 LA_DTYPE_BF16 = 0
 LA_DTYPE_F32 = 1
 
 LA_FWD_NOALLOC_MAX_SEQS = 16384   # include/la.h
+LA_BUILD_BOUNDS_CHECKED = 1       # include/la.h
 
 
 class LaDims(ctypes.Structure):
@@ -89,6 +93,7 @@ PROTOTYPES = {
     "la_kernel_family": (_i32, [_dims_p, _i32]),
     "la_launch_count": (ctypes.c_uint64, []),
     "la_version": (_i32, []),
+    "la_build_flags": (_i32, []),
 }
 
 _lib = None
@@ -99,8 +104,8 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise ImportError("liblagb300.so is not built (run linear_attention_head_gb300/"
-                              "build.py); this package has no fallback path")
+            raise ImportError("%s is not built (run linear_attention_head_gb300/build.py); "
+                              "this package has no fallback path" % os.path.basename(LIB_PATH))
         handle = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in PROTOTYPES.items():
             fn = getattr(handle, name)

@@ -16,6 +16,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "liblagb300.so")
 OBJDIR = os.path.join(HERE, "_build")
+# the bounds-checking build (LA_CHECK_BOUNDS): index checks in the tensor-core
+# kernels record failures in the device error word instead of accessing
+CHECKED_LIB = os.path.join(HERE, "liblagb300_checked.so")
+CHECKED_OBJDIR = os.path.join(HERE, "_build_checked")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -40,14 +44,19 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = False) -> str:
+    """Build liblagb300.so, or with checked=True liblagb300_checked.so (the
+    same sources with LA_CHECK_BOUNDS defined); returns the library's path."""
+    lib, objdir = (CHECKED_LIB, CHECKED_OBJDIR) if checked else (LIB, OBJDIR)
+    if checked:
+        extra = (*extra, "-DLA_CHECK_BOUNDS")
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps():
+        return lib
     nvcc = _nvcc()
-    os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -58,16 +67,17 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = lib + ".tmp.%d" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     extra = [a for a in sys.argv[1:] if a.startswith("-X") or a.startswith("--")]
-    extra = [a for a in extra if a != "--force"]
-    print(build(force="--force" in sys.argv, verbose=True, extra=extra))
+    extra = [a for a in extra if a not in ("--force", "--checked")]
+    print(build(force="--force" in sys.argv, verbose=True, extra=extra,
+                checked="--checked" in sys.argv))

@@ -787,6 +787,10 @@ la_status la_get_device_error(void *stream)
         return cuda_fail(e, "la_get_device_error");
     if (!err)
         err = err2 ? err2 : err3;
+    else if ((err & 0xff) != LA_ERR_BOUNDS && (err3 & 0xff) == LA_ERR_BOUNDS)
+        err = err3;
+    if ((err & 0xff) == LA_ERR_BOUNDS)
+        return fail(LA_ERR_BOUNDS, "an index check failed at site %d", err >> 8);
     if (err)
         return fail(LA_ERR_TIMEOUT, "an on-device wait ran out (code %d)", err);
     return LA_OK;
@@ -800,6 +804,7 @@ const char *la_strerror(int32_t status)
     case LA_ERR_UNSUPPORTED: return "unsupported configuration";
     case LA_ERR_CUDA: return "CUDA error";
     case LA_ERR_TIMEOUT: return "on-device wait timed out";
+    case LA_ERR_BOUNDS: return "on-device index check failed";
     default: return "unknown status";
     }
 }
@@ -863,7 +868,16 @@ la_status la_debug_withhold_next_handoff(int32_t on)
 
 uint64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int32_t la_version(void) { return (0 << 16) | 3; }
+int32_t la_version(void) { return (0 << 16) | 4; }
+
+int32_t la_build_flags(void)
+{
+#ifdef LA_CHECK_BOUNDS
+    return LA_BUILD_BOUNDS_CHECKED;
+#else
+    return 0;
+#endif
+}
 
 }  // extern "C"
 

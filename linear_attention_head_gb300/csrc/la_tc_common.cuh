@@ -29,6 +29,24 @@ __device__ int g_tc_error;
 constexpr int TC_C = 128;        // tokens per chunk (MMA M and the P Z K-extent)
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;
 constexpr int TC_ERR_TIMEOUT = 4;
+constexpr int TC_ERR_BOUNDS = 5;   // bounds-checking build: a failed index check
+
+// Index checks of the bounds-checking build (LA_CHECK_BOUNDS defined): LA_OK_AT
+// (cond, site) is the condition, and records a failure as TC_ERR_BOUNDS with
+// the site number above the low byte of the error word (the first failure
+// wins); the caller skips the access it guards.  In the normal build it is
+// true without evaluating the condition, and the checks compile away.
+#ifdef LA_CHECK_BOUNDS
+__device__ __noinline__ bool la_ok_at(bool ok, int site)
+{
+    if (!ok)
+        atomicCAS(&g_tc_error, 0, TC_ERR_BOUNDS | (site << 8));
+    return ok;
+}
+#define LA_OK_AT(cond, site) la_ok_at((cond), (site))
+#else
+#define LA_OK_AT(cond, site) (true || (cond))
+#endif
 
 // Bounded wait: false when the CTA is aborting or this wait ran out.
 __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)

@@ -126,6 +126,8 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
 // are all loaded before any is stored.
 __device__ __forceinline__ void scale_tile_row(uint8_t *t, int i, float f)
 {
+    if (!LA_OK_AT(i >= 0 && i < TC_C, 101))
+        return;
     const uint32_t f2 = pack_bf16x2(f, f);
 #pragma unroll 1
     for (int b = 0; b < 2; ++b) {
@@ -256,6 +258,8 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
                 const CUtensorMap *m = r == 0 ? &P.mk : r == 1 ? &P.mq : r == 2 ? &P.mv : &P.mdo;
                 const int hh = r == 0 ? hk : r == 2 ? hv : h;
                 const int t0 = (int)(bos + chunk_t0(c));
+                if (!LA_OK_AT(t0 >= 0 && t0 < a.T && s >= 0 && s < DK_NSLOT, 114))
+                    break;
                 if (r == 0) {
                     // the v and do tiles of this chunk wait for slots the
                     // chunk before frees late: have them in L2 by then
@@ -287,6 +291,10 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
             for (int c = 0; c < nc; ++c) {
                 const int tk = 4 * c, tq = tk + 1, tv = tk + 2, to = tk + 3;
                 const uint32_t ka = addr(tk), qa = addr(tq), va = addr(tv), oa = addr(to);
+                if (!LA_OK_AT(ka + DK_TILE <= ga && qa + DK_TILE <= ga && va + DK_TILE <= ga &&
+                                  oa + DK_TILE <= ga && ga + DK_D * DK_D * 2 <= sbase + L::MOFF,
+                              107))
+                    break;
                 // K Q^T goes to [0,128): free once the previous chunk's dK
                 // MMAs, the last to read P1 and P2 there, are done
                 if (c > 0 && !bwait(dk_full, (c - 1) & 1, abort_flag))
@@ -404,13 +412,17 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
             // block kinds are warp-uniform: 0 zero, 1 rank one, 2 diagonal
             const int k0 = b0 == q ? 2 : ((flip ? b0 > q : b0 < q) ? 1 : 0);
             const int k1 = b1 == q ? 2 : ((flip ? b1 > q : b1 < q) ? 1 : 0);
+            const int ix0 = flip ? 32 * (b0 - q) - lane : 32 * (q - b0) + lane - 31;
+            const int ix1 = flip ? 32 * (b1 - q) - lane : 32 * (q - b1) + lane - 31;
             const float rf0 =
-                k0 == 1 ? scale * pw[flip ? 32 * (b0 - q) - lane : 32 * (q - b0) + lane - 31] : 0.f;
+                k0 == 1 && LA_OK_AT(ix0 >= 0 && ix0 <= TC_C, 104) ? scale * pw[ix0] : 0.f;
             const float rf1 =
-                k1 == 1 ? scale * pw[flip ? 32 * (b1 - q) - lane : 32 * (q - b1) + lane - 31] : 0.f;
+                k1 == 1 && LA_OK_AT(ix1 >= 0 && ix1 <= TC_C, 104) ? scale * pw[ix1] : 0.f;
             bool run = true;
             for (int c = 0; c < nc && run; ++c) {
                 const int Lc = chunk_len(c);
+                if (!LA_OK_AT(Lc >= 1 && Lc <= TC_C, 105))
+                    break;
 #pragma unroll 1
                 for (int pass = 0; pass < 2; ++pass) {
                     // pass 0: P1 from K Q^T, pass 1: P2 from V dO^T
@@ -469,7 +481,17 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
             const int64_t sb = ((int64_t)n * a.H + h) * (int64_t)DK_D * DK_D;
             uint8_t *grow = sm + L::GOFF + i * 128;
             const uint32_t gtm = tm + lane_off + TG;
-            if (nc == 0)
+            // the state tensors' extent: both ends of row i fall inside it
+            const int64_t s_total = (int64_t)a.N * a.H * DK_D * DK_D;
+            auto s_ok = [&](int64_t rs, int64_t cs) {
+                const int64_t lo = sb + i * rs, hi = lo + (int64_t)(DK_D - 1) * cs;
+                return lo >= 0 && hi < s_total;
+            };
+            const bool in_ok = !a.s_in.p || LA_OK_AT(s_ok(a.s_in.rs, a.s_in.cs), 109);
+            const bool out_ok = !a.s_out.p || LA_OK_AT(s_ok(a.s_out.rs, a.s_out.cs), 110);
+            if (!in_ok || !out_ok) {
+                // leave the state alone: the MMA issuer's s_ready wait runs out
+            } else if (nc == 0)
                 state_copy(a.s_in, a.s_out, sb, i, 0, DK_D);
             else
                 state_in(a.s_in, sb, i, 0, DK_D, grow, DK_D * 128, gtm, pw[chunk_len(0)], 1.f);
@@ -511,7 +533,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
                     tmem_ld32_issue(gtm + 64 * eb + 32, rb);
                     tmem_wait_ld(ra, rb);
                     if (last) {
-                        if (a.s_out.p && !*abort_flag) {
+                        if (a.s_out.p && out_ok && !*abort_flag) {
                             float *dst = a.s_out.p + sb + i * a.s_out.rs + 64 * eb * a.s_out.cs;
                             if (a.s_out.cs == 1 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
@@ -531,7 +553,8 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
                         }
                         continue;
                     }
-                    store_row_sw128(grow + eb * (DK_D * 128), i, ra, rb);
+                    if (LA_OK_AT(i * 128 + eb * (DK_D * 128) + 128 <= DK_D * DK_D * 2, 103))
+                        store_row_sw128(grow + eb * (DK_D * 128), i, ra, rb);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         ra[k] = __float_as_uint(gn * __uint_as_float(ra[k]));
@@ -583,7 +606,8 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
                             tc_fence_before();
                             mbar_arrive(which ? dk_drained : dv_drained);
                         }
-                        store_half_row_sw128(stage + (part >> 1) * (TC_C * 128) + i * 128, i,
+                        if (LA_OK_AT((part >> 1) * (TC_C * 128) + i * 128 + 128 <= DK_TILE, 102))
+                            store_half_row_sw128(stage + (part >> 1) * (TC_C * 128) + i * 128, i,
                                              part & 1, ra);
                     }
                     const TokOut &dst = which ? P.dk : a.out;
@@ -592,7 +616,9 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
                         // visible to the copy engine
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) {
+                        // a store may start past a dense sequence's end (the
+                        // copy clips it), never before the tensor's start
+                        if (lane == 0 && LA_OK_AT(t0 + 32 * q >= 0 && t0 < a.T, 113)) {
                             const CUtensorMap *m = which ? &P.mdk : &P.mdv;
 #pragma unroll
                             for (int b = 0; b < DK_D / 64; ++b)
@@ -601,7 +627,7 @@ __global__ void __launch_bounds__(DK_THREADS, 1) tc_dkdv_kernel(const __grid_con
                             bulk_commit_group();
                             bulk_wait_read_all();
                         }
-                    } else if (i < Lc) {
+                    } else if (i < Lc && LA_OK_AT(t0 + i < a.T, 112)) {
                         // row by row: this thread's own row, back out of the tile
                         __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(dst.p) +
                                               row * dst.sb + (t0 + i) * dst.st + (int64_t)h * dst.sh;

@@ -228,8 +228,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
         constexpr int PADB = (L::YPAD - D) * TC_C * 2;
         for (int st = 0; st < NST; ++st)
             for (int o = 16 * threadIdx.x; o < PADB; o += 16 * TC_THREADS)
-                *reinterpret_cast<uint4 *>(sm + st * L::STAGE + L::XB + L::YLB + o) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                if (LA_OK_AT(L::YLB + o + 16 <= L::YB, 1))
+                    *reinterpret_cast<uint4 *>(sm + st * L::STAGE + L::XB + L::YLB + o) =
+                        make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -290,6 +291,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     break;
                 const int t0 = (int)(bos + chunk_t0(c));
                 uint8_t *st = sm + s * L::STAGE;
+                if (!LA_OK_AT(t0 >= 0 && t0 < a.T && e0 + E <= a.E, 21))
+                    break;
                 if (SO) {
                     // Y and Z, both free once the chunk's state update is done
                     mbar_arrive_expect_tx(&full[s], L::YLB + L::ZB);
@@ -358,6 +361,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             for (int c = 0; c < nc; ++c) {
                 const int s = c % NST;
                 const uint32_t xa = sbase + s * L::STAGE, ya = xa + L::XB, za = ya + L::YB;
+                if (!LA_OK_AT(za + L::ZB <= sbase + (uint32_t)L::SOFF &&
+                                  sa + (uint32_t)L::SB <= sbase + (uint32_t)L::MOFF,
+                              12))
+                    break;
                 if (!bwait(&full[s], (c / NST) & 1, abort_flag))
                     break;
                 if (SO) {
@@ -447,11 +454,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             auto scale_y = [&](int s, float f) {
 #pragma unroll
                 for (int b = hh; b < D / 64; b += 2)
-                    scale_row_sw128(sm + s * L::STAGE + L::XB + b * (TC_C * 128) + i * 128, i, f);
+                    if (LA_OK_AT(b * (TC_C * 128) + i * 128 + 128 <= L::YLB && s < NST, 7))
+                        scale_row_sw128(sm + s * L::STAGE + L::XB + b * (TC_C * 128) + i * 128, i,
+                                        f);
             };
             for (int c = 0; c < nc; ++c) {
                 const int s = c % NST;
                 const int Lc = chunk_len(c);
+                if (!LA_OK_AT(Lc >= 1 && Lc <= TC_C, 5))
+                    break;
                 bool ok = warp_all(bwait(&full[s], (c / NST) & 1, abort_flag));
                 if (ok && !SO)
                     ok = warp_all(bwait(sc_full, c & 1, abort_flag));
@@ -490,12 +501,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     p_block_gated(ra, k0, scale, flip, lane);
                     p_block_gated(rb, k1, scale, flip, lane);
                 } else {
+                    const int ix0 = flip ? 32 * (b0 - q) - lane : 32 * (q - b0) + lane - 31;
+                    const int ix1 = flip ? 32 * (b1 - q) - lane : 32 * (q - b1) + lane - 31;
                     const float rf0 =
-                        k0 == 1 ? scale * pw[flip ? 32 * (b0 - q) - lane : 32 * (q - b0) + lane - 31]
-                                : 0.f;
+                        k0 == 1 && LA_OK_AT(ix0 >= 0 && ix0 <= TC_C, 3) ? scale * pw[ix0] : 0.f;
                     const float rf1 =
-                        k1 == 1 ? scale * pw[flip ? 32 * (b1 - q) - lane : 32 * (q - b1) + lane - 31]
-                                : 0.f;
+                        k1 == 1 && LA_OK_AT(ix1 >= 0 && ix1 <= TC_C, 3) ? scale * pw[ix1] : 0.f;
                     p_block_full(ra, k0, rf0, cf, dt, lane);
                     p_block_full(rb, k1, rf1, cf, dt, lane);
                 }
@@ -568,7 +579,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             float *colf = pw;
             float *coln = reinterpret_cast<float *>(sm + L::COLNOFF);
             auto sg_sync = [] { asm volatile("bar.sync 2, %0;" ::"n"(TC_SG) : "memory"); };
-            if (nc == 0) {
+            // the state tensors' extent (element offsets of both corners of
+            // this CTA's rows and columns must fall inside it)
+            const int64_t s_total = (int64_t)a.N * a.H * a.D * a.E;
+            auto s_ok = [&](int64_t rs, int64_t cs, int r) {
+                const int64_t lo = sb + r * rs + (int64_t)e0 * cs;
+                const int64_t hi = lo + (int64_t)(E - 1) * cs;
+                return lo >= 0 && hi < s_total;
+            };
+            const bool in_ok = !a.s_in.p || LA_OK_AT(s_ok(a.s_in.rs, a.s_in.cs, D - 1), 15);
+            const bool out_ok = !a.s_out.p || LA_OK_AT(s_ok(a.s_out.rs, a.s_out.cs, D - 1), 16);
+            if (!LA_OK_AT((L::NP - 1) * 128 + 127 < L::YPAD &&
+                              (D - 1) * 128 + (E / 64 - 1) * (D * 128) + 128 <= L::SB,
+                          9) ||
+                !in_ok || !out_ok) {
+                // nothing below is safe: leave the state alone (the MMA
+                // issuer's s_ready wait runs out and the kernel stops)
+            } else if (nc == 0) {
 #pragma unroll 1
                 for (int pc = 0; pc < L::NP; ++pc)
                     if (srow(pc) < D)
@@ -639,7 +666,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         tmem_ld32_issue(stm(pc) + 64 * eb + 32, rb);
                         tmem_wait_ld(ra, rb);
                         if (last) {
-                            if (a.s_out.p && !*abort_flag) {
+                            if (a.s_out.p && out_ok && !*abort_flag) {
                                 float *dst = a.s_out.p + sb + r * a.s_out.rs +
                                              (int64_t)(e0 + 64 * eb) * a.s_out.cs;
 #pragma unroll
@@ -671,7 +698,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                             }
                             continue;
                         }
-                        if (!GLA && !SO)
+                        if (!GLA && !SO &&
+                            LA_OK_AT(r * 128 + eb * (D * 128) + 128 <= L::SB, 8))
                             store_row_sw128(sbf(pc) + eb * (D * 128), r, ra, rb);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) {
@@ -687,7 +715,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                                 rb[k] = __float_as_uint(gn * __uint_as_float(rb[k]));
                             }
                         }
-                        if (GLA)
+                        if (GLA && LA_OK_AT(r * 128 + eb * (D * 128) + 128 <= L::SB, 8))
                             store_row_sw128(sbf(pc) + eb * (D * 128), r, ra, rb);
                         tmem_st32_issue(stm(pc) + 64 * eb, ra);
                         tmem_st32_issue(stm(pc) + 64 * eb + 32, rb);
@@ -728,8 +756,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     for (int k = 0; k < 32; ++k)
                         ra[k] = __float_as_uint(
                             fmaf(lr, __uint_as_float(ri[k]), __uint_as_float(ra[k])));
-                    store_half_row_sw128(otile + (part >> 1) * (TC_C * 128) + i * 128, i, part & 1,
-                                         ra);
+                    if (LA_OK_AT((part >> 1) * (TC_C * 128) + i * 128 + 128 <= L::ZB, 11))
+                        store_half_row_sw128(otile + (part >> 1) * (TC_C * 128) + i * 128, i,
+                                             part & 1, ra);
                 }
                 tc_fence_before();
                 mbar_arrive(o_free);   // both accumulators read
@@ -738,7 +767,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     // the copy engine
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
+                    // a store may start past a dense sequence's end (the copy
+                    // clips it), never before the tensor's start
+                    if (lane == 0 && LA_OK_AT(bos + chunk_t0(c) + 32 * q >= 0 &&
+                                                  bos + chunk_t0(c) < a.T && e0 + E <= a.E,
+                                              19)) {
 #pragma unroll
                         for (int b = 0; b < E / 64; ++b)
                             tma_store_4d(&P.mo, otile + b * (TC_C * 128) + q * 32 * 128, 64 * b + e0,
@@ -746,7 +779,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                         bulk_commit_group();
                         bulk_wait_read_all();
                     }
-                } else if (i < Lc) {
+                } else if (i < Lc && LA_OK_AT(bos + chunk_t0(c) + i < a.T, 18)) {
                     // row by row: this thread's own row, back out of the tile
 #pragma unroll 1
                     for (int c16 = 0; c16 < E / 8; ++c16)
