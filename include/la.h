@@ -311,11 +311,15 @@ size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
  * bytes with which bf16 calls with D = E = 128, sequences longer than 16
  * tokens and 16-byte aligned token rows run the chunked form on the tensor
  * cores: the forward's rescaled q~, k~ (see la_gla_fwd), three sweeps on
- * them -- forward-type (do, v, k~) giving dq exp(r - b), backward-type
- * (k~, q~, do) giving dv, backward-type (v, do, q~) giving dk exp(b - r) --
- * and a pass that rescales dq and dk in place.  Pairs out of range, smaller
- * workspaces (down to the token-by-token part, the final state and dg's
- * block sums) and other shapes run the token-by-token kernels.
+ * them -- forward-type (do, v, k~) giving dq~ = dq exp(r - b), backward-
+ * type (k~, q~, do) giving dv, backward-type (v, do, q~) giving dk~ =
+ * dk exp(b - r), dq~ and dk~ in fp32 -- and a pass that rescales dq~, dk~
+ * into dq, dk and forms dg, each term as q~ dq~ - k~ dk~ from the rounded
+ * operands and their own gradients.  Pairs out of range, smaller workspaces
+ * (down to the token-by-token part: the final state, dg's block sums and,
+ * for bf16, dq and dk in fp32) and other shapes run the token-by-token
+ * kernels.  dg never takes bf16-rounded gradients: rounding each of its T
+ * terms would add errors that grow with T while dg does not.
  *   fwd_workspace  the workspace of a la_gla_fwd call on the same q, k, g,
  *              g_gamma, reverse and cu_seqlens that reported operands_written
  *              = 1, untouched since; or NULL.  The backward then uses the

@@ -390,10 +390,15 @@ def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
 
 @_traced
 def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_final_state=None,
-            reverse=False, cu_seqlens=None, want_d_initial_state=True, operands=None):
+            reverse=False, cu_seqlens=None, want_d_initial_state=True, operands=None,
+            chunked: bool = True):
     """Backward of gla_fwd: returns (dq, dk, dv, dg, d_initial_state).  operands: what
     gla_fwd(..., keep_operands=True) returned for the same inputs, or None; it is
-    consumed (used as scratch)."""
+    consumed (used as scratch).  chunked=False (with operands None) gives only the
+    token-by-token part of the workspace, so that every (sequence, head) runs token
+    by token."""
+    if not chunked and operands is not None:
+        raise ValueError("chunked=False takes no operands")
     q, k, v, do, dev, packed, gg, scale, init, dfin, Nst = _bwd_prep(
         q, k, v, do, torch.zeros(q.shape[2]) if g_gamma is None else g_gamma, scale,
         initial_state, d_final_state, cu_seqlens)
@@ -407,7 +412,8 @@ def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_fina
     dims = _dims(q, k, v, do, packed)
     # with the forward's operands the workspace needs only the token-by-token part
     nbytes = int(N.lib().la_gla_workspace_size(ctypes.byref(dims), _dtype_code(q),
-                                              packed.host_ptr(), int(operands is not None)))
+                                              packed.host_ptr(),
+                                              int(operands is not None or not chunked)))
     fwd_bytes = operands.numel() if operands is not None else 0
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     st = N.lib().la_gla_bwd(ctypes.byref(dims), _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),

@@ -959,11 +959,25 @@ GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype, bool bwd = false)
     return w;
 }
 
-// Workspace of la_gla_bwd: the final state transposed, then the block sums.
-size_t gla_bwd_bytes(const Problem &P)
+// Workspace of la_gla_bwd: the final state transposed, the block sums and,
+// for bf16 tokens, dq and dk in fp32 (dense [rows][T][H][D]): the sweeps
+// write them there and the gate's gradient reads them unrounded before the
+// bf16 copies are written.
+struct GlaBwdWs {
+    size_t bsum, dqf, dkf, total;
+};
+GlaBwdWs gla_bwd_layout(const Problem &P, int32_t dtype)
 {
+    GlaBwdWs w{};
     const int64_t nblk = (gla_max_len(P) + la::DG_TB - 1) / la::DG_TB;
-    return round256((size_t)P.N * P.H * P.D * P.E * 4) + round256((size_t)P.N * P.H * nblk * P.D * 4);
+    const int64_t rows = P.packed ? 1 : P.B;
+    const size_t tokf =
+        dtype == LA_DTYPE_BF16 ? round256((size_t)rows * P.T * P.H * P.D * 4) : 0;
+    w.bsum = round256((size_t)P.N * P.H * P.D * P.E * 4);
+    w.dqf = w.bsum + round256((size_t)P.N * P.H * nblk * P.D * 4);
+    w.dkf = w.dqf + tokf;
+    w.total = w.dkf + tokf;
+    return w;
 }
 
 }  // namespace
@@ -1084,7 +1098,8 @@ size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *
     g_msg = keep;
     if (st != LA_OK)
         return 0;
-    return gla_bwd_bytes(P) + (with_forward_operands ? 0 : gla_fwd_layout(P, dtype, true).total);
+    return gla_bwd_layout(P, dtype).total +
+           (with_forward_operands ? 0 : gla_fwd_layout(P, dtype, true).total);
 }
 
 la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
@@ -1109,20 +1124,27 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     }
     if ((st = gla_check(P, dims, g, g_strides, g_gamma)) || !has_states(P))
         return st;
-    const size_t need_ws = gla_bwd_bytes(P);
+    const GlaBwdWs bw = gla_bwd_layout(P, dtype);
+    const size_t need_ws = bw.total;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
         workspace_bytes < need_ws)
         return fail(LA_ERR_INVALID_ARG,
                     "la_gla_bwd needs a 256-byte aligned workspace of %zu bytes (got %zu)",
                     need_ws, workspace ? workspace_bytes : (size_t)0);
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
     float *Ft = static_cast<float *>(workspace);
-    float *bsum = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                            round256((size_t)P.N * P.H * P.D * P.E * 4));
+    float *bsum = reinterpret_cast<float *>(wsb + bw.bsum);
+    // bf16 tokens: dq and dk in fp32, dense (token stride H D)
+    const bool f32g = dtype == LA_DTYPE_BF16;
+    float *dqf = f32g ? reinterpret_cast<float *>(wsb + bw.dqf) : nullptr;
+    float *dkf = f32g ? reinterpret_cast<float *>(wsb + bw.dkf) : nullptr;
+    const int64_t fsh = P.D, fst = (int64_t)P.H * P.D, fsb = fst * P.T;
     la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
     // The chunked form on the tensor cores, when it applies and the workspace
     // also holds its operands: the three sweeps on q~, k~ for the (sequence,
-    // head) pairs in range, then dq~, dk~ rescaled in place; the token-by-
-    // token sweeps below run only the flagged pairs.
+    // head) pairs in range (dq~, dk~ in fp32 into the workspace), then dq~,
+    // dk~ rescaled into dq, dk with dg; the token-by-token sweeps below run
+    // only the flagged pairs.
     const int *flags = nullptr;
     la::GlaPrepArgs pa{};
     {
@@ -1176,6 +1198,8 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             pa.lim = 72.f;
             pa.dq = dq;
             pa.dk = dk;
+            pa.dqf = dqf;
+            pa.dkf = dkf;
             pa.dg = dg;
             pa.Ft = Ft;
             pa.dF = d_final_state;
@@ -1191,10 +1215,10 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             t.gla_ncmax = w.ncmax;
             t.gla_flags = fl;
             t.gla_flag_run = 0;
-            // dq~: forward-type (do, v, k~), state S^T with gated columns
+            // dq~ (fp32): forward-type (do, v, k~), state S^T with gated columns
             t.D = P.E;
             t.E = P.D;
-            t.out = tok_out(dq, dims->qk_strides);
+            t.out = la::TokOut{dqf, fsb, fst, fsh};
             t.s_in = la::StateIn{initial_state, 1, P.E};
             t.s_out = la::StateOut{Ft, P.D, 1};
             e = la::tc_gla_sweep(t, false, true, tdo, tv, tk, s);
@@ -1208,10 +1232,10 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
                 e = la::tc_gla_sweep(t, true, false, tk, tq, tdo, s);
             }
             if (e == cudaSuccess) {
-                // dk~: backward-type (v, do, q~), G^T with gated columns
+                // dk~ (fp32): backward-type (v, do, q~), G^T with gated columns
                 t.D = P.E;
                 t.E = P.D;
-                t.out = tok_out(dk, dims->qk_strides);
+                t.out = la::TokOut{dkf, fsb, fst, fsh};
                 t.s_in = la::StateIn{d_final_state, 1, P.E};
                 t.s_out = la::StateOut{nullptr, 0, 0};
                 e = la::tc_gla_sweep(t, true, true, tv, tdo, tq, s);
@@ -1230,7 +1254,8 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.q = tok(d_o, dims->v_strides);
     a.k = tok(v, dims->v_strides);
     a.v = tok(k, dims->qk_strides);
-    a.out = tok_out(dq, dims->qk_strides);
+    a.out = f32g ? la::TokOut{dqf, fsb, fst, fsh} : tok_out(dq, dims->qk_strides);
+    a.out_f32 = f32g ? 1 : 0;
     a.s_in = la::StateIn{initial_state, 1, P.E};
     a.s_out = la::StateOut{Ft, P.D, 1};
     a.gate = gate_of(g, g_strides, true);
@@ -1243,6 +1268,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.k = tok(k, dims->qk_strides);
     a.v = tok(d_o, dims->v_strides);
     a.out = tok_out(dv, dims->v_strides);
+    a.out_f32 = 0;
     a.s_in = la::StateIn{d_final_state, P.E, 1};
     a.s_out = la::StateOut{d_initial_state, P.E, 1};
     a.gate = gate_of(g, g_strides, false);
@@ -1254,7 +1280,8 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.q = tok(d_o, dims->v_strides);
     a.k = tok(v, dims->v_strides);
     a.v = tok(q, dims->qk_strides);
-    a.out = tok_out(dk, dims->qk_strides);
+    a.out = f32g ? la::TokOut{dkf, fsb, fst, fsh} : tok_out(dk, dims->qk_strides);
+    a.out_f32 = f32g ? 1 : 0;
     a.s_in = la::StateIn{d_final_state, 1, P.E};
     a.s_out = la::StateOut{nullptr, 0, 0};
     a.gate = gate_of(g, g_strides, true);
@@ -1278,11 +1305,25 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     gg.bf16 = dtype == LA_DTYPE_BF16;
     gg.q = q;
     gg.k = k;
-    gg.dq = dq;
-    gg.dk = dk;
     gg.sb = dims->qk_strides[0];
     gg.st = dims->qk_strides[1];
     gg.sh = dims->qk_strides[2];
+    if (f32g) {
+        // fp32 gradients from the workspace; the kernels write the bf16 ones
+        gg.dqf = dqf;
+        gg.dkf = dkf;
+        gg.fsb = fsb;
+        gg.fst = fst;
+        gg.fsh = fsh;
+        gg.dq = dq;
+        gg.dk = dk;
+    } else {
+        gg.dqf = static_cast<const float *>(dq);
+        gg.dkf = static_cast<const float *>(dk);
+        gg.fsb = gg.sb;
+        gg.fst = gg.st;
+        gg.fsh = gg.sh;
+    }
     gg.dg = dg;
     gg.gsb = g_strides[0];
     gg.gst = g_strides[1];

@@ -21,14 +21,15 @@
 // the sweep cuts them, in either direction.
 //
 // The backward runs its three sweeps on the same operands and yields
-// dq~ = dq exp(r - b) and dk~ = dk exp(b - r); the second mode of this kernel
-// recomputes b and r (the same arithmetic, so the same values), turns them
-// into dq and dk in place and forms the gate's gradient, for every (sequence,
-// head) not flagged:
+// dq~ = dq exp(r - b) and dk~ = dk exp(b - r) in fp32; the second mode of this
+// kernel recomputes b and r (the same arithmetic, so the same values), turns
+// them into dq and dk (token dtype) and forms the gate's gradient, for every
+// (sequence, head) not flagged:
 //     dg_w = sum over t at or after w (processing order) of q_t dq_t - k_t dk_t
 //            + sum_e F dF,
-// the terms in fp32 from the unrounded products, summed within the chunk
-// there and completed by gla_dg_finish with the later chunks' totals.
+// each term as q~ dq~ - k~ dk~ in fp32 (the bf16 operands and their own
+// gradients), summed within the chunk there and completed by gla_dg_finish
+// with the later chunks' totals.
 
 #include <cmath>
 #include <cstdint>
@@ -41,13 +42,6 @@ namespace la {
 namespace {
 
 constexpr int PC = 128;   // tokens per chunk (the tensor-core sweep's chunk)
-
-template <typename T> __device__ __forceinline__ float ldt(const T *p);
-template <> __device__ __forceinline__ float ldt<float>(const float *p) { return *p; }
-template <> __device__ __forceinline__ float ldt<__nv_bfloat16>(const __nv_bfloat16 *p)
-{
-    return __bfloat162float(*p);
-}
 
 template <typename T> struct Pair;
 template <> struct Pair<float> {
@@ -78,8 +72,8 @@ template <> struct Pair<__nv_bfloat16> {
 // combined through shared memory.  The factors exp(b - r), exp(r - b) use the
 // fast exponential: they are rounded to bf16 with their operands anyway.
 constexpr int PG = 4, PT = PC / PG;   // token groups per chunk, tokens per group
-// UNDO: instead of writing the operands, rescale dq~, dk~ (token dtype, the
-// strides of q and k) in place into dq, dk.
+// UNDO: instead of writing the operands, rescale dq~, dk~ (fp32, dense) into
+// dq, dk (token dtype, the strides of q and k).
 template <typename T, bool UNDO>
 __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
 {
@@ -182,13 +176,20 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
         const int64_t qo = row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
         T *dqp = static_cast<T *>(a.dq) + qo;
         T *dkp = static_cast<T *>(a.dk) + qo;
-        const T *qp = static_cast<const T *>(a.q) + qo;
-        const T *kp = static_cast<const T *>(a.k) + qo;
+        // dq~, dk~ (fp32) and the operands q~, k~ (bf16), all dense
+        const int64_t fo = ((int64_t)row * a.T * a.H + h) * a.D + c + tb * (int64_t)a.H * a.D;
+        const float *dqf = a.dqf + fo, *dkf = a.dkf + fo;
+        const __nv_bfloat16 *xq = static_cast<const __nv_bfloat16 *>(a.xq) + fo;
+        const __nv_bfloat16 *yk = static_cast<const __nv_bfloat16 *>(a.yk) + fo;
         float *dgp = a.dg + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
-        const int64_t step = ts * a.st, gstep = ts * a.gst;
+        const int64_t step = ts * a.st, fstep = ts * (int64_t)a.H * a.D, gstep = ts * a.gst;
         const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
-        // dq, dk, and dg's terms q dq - k dk (fp32, from the unrounded
-        // products) into b[], which the factors no longer need
+        // dq, dk, and dg's terms into b[], which the factors no longer need.
+        // A term is q dq - k dk = q~ dq~ - k~ dk~; it is taken from the
+        // rounded operands the sweeps multiplied and their own (fp32)
+        // gradients, which makes dg the exact gradient of what the sweeps
+        // computed.  With q, k instead, each term would carry the operands'
+        // rounding (about 2^-9 of it), a random walk over the T terms.
         float2 gt = make_float2(0.f, 0.f);   // this group's sum of terms
         constexpr int PB = 4;
 #pragma unroll
@@ -198,10 +199,10 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
             for (int jj = 0; jj < PB; ++jj) {
                 const int j = j0 + jj;
                 const int64_t jl = j < np ? j : (np > 0 ? np - 1 : 0);
-                dqv[jj] = Pair<T>::load(dqp + jl * step);
-                dkv[jj] = Pair<T>::load(dkp + jl * step);
-                qv[jj] = Pair<T>::load(qp + jl * step);
-                kv[jj] = Pair<T>::load(kp + jl * step);
+                dqv[jj] = Pair<float>::load(dqf + jl * fstep);
+                dkv[jj] = Pair<float>::load(dkf + jl * fstep);
+                qv[jj] = Pair<__nv_bfloat16>::load(xq + jl * fstep);
+                kv[jj] = Pair<__nv_bfloat16>::load(yk + jl * fstep);
             }
 #pragma unroll
             for (int jj = 0; jj < PB; ++jj) {
@@ -214,8 +215,8 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
                         make_float2(dkv[jj].x * __expf(-ex), dkv[jj].y * __expf(-ey));
                     Pair<T>::store(dqp + j * step, dq2);
                     Pair<T>::store(dkp + j * step, dk2);
-                    tm = make_float2(qv[jj].x * dq2.x - kv[jj].x * dk2.x,
-                                     qv[jj].y * dq2.y - kv[jj].y * dk2.y);
+                    tm = make_float2(qv[jj].x * dqv[jj].x - kv[jj].x * dkv[jj].x,
+                                     qv[jj].y * dqv[jj].y - kv[jj].y * dkv[jj].y);
                 }
                 b[j] = tm;
                 gt.x += tm.x;

@@ -83,6 +83,8 @@ struct SweepArgs {
     // range, run token by token)
     const int *gla_flags = nullptr;
     int gla_flag_run = 0;
+    // token-by-token kernels with bf16 tokens: out is fp32 (strides in floats)
+    int out_f32 = 0;
 };
 
 // Operands of the chunked gated forward (la_gla_prep.cu).
@@ -100,20 +102,23 @@ struct GlaPrepArgs {
     float *er, *u;            // [N][H][ncmax][D]
     int *flags;               // [N H], zeroed beforehand
     float lim;                // largest |b - r| (and |r|) the chunked form takes
-    void *dq, *dk;            // gla_undo: dq~, dk~ in, dq, dk out (q's strides)
+    void *dq, *dk;            // gla_undo: dq, dk out (token dtype, q's strides)
+    const float *dqf, *dkf;   // gla_undo: dq~, dk~ in (fp32, dense [rows][T][H][D])
     float *dg;                // gla_undo: the gate's gradient (the gate's strides)
     const float *Ft, *dF;     // gla_undo: final state (transposed, [E][D] per
                               // pair) and its gradient ([D][E]), or dF null
     int E;
 };
 cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s);
-// dq~ -> dq, dk~ -> dk in place, and the gate's gradient dg, for the
-// (sequence, head) pairs not flagged (a.er and a.u are reused as scratch).
+// dq~ -> dq, dk~ -> dk (fp32 in, token dtype out), and the gate's gradient
+// dg from the rounded operands q~, k~ and their own gradients dq~, dk~, for
+// the (sequence, head) pairs not flagged (a.er and a.u are reused as scratch).
 cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s);
 // A tensor-core sweep of the gated form on rescaled operands (la_gla_prep.cu)
 // with tile roles X, Y, Z given (bf16, D = 128 X and Y width): forward-type or
 // backward-type (bwd), the gated key channels being the state's rows or its
-// columns (cols, needs E = 128); a.gla_* set, a.out the output.
+// columns (cols, needs E = 128); a.gla_* set, a.out the output: bf16 rows,
+// or with cols (the sweeps giving dq~ and dk~) fp32 rows, 16-byte aligned.
 // cudaErrorNotSupported when the tensor maps cannot be built.
 cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, const Tok &y,
                          const Tok &z, cudaStream_t s);
@@ -160,8 +165,9 @@ cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s);
 cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv, int G, int X,
                        int bf16, cudaStream_t s);
 
-// Gradient of the per-key gate (la_gla.cu).  q, k, dq, dk share one layout
-// (token dtype, strides sb, st, sh); dg is fp32 with the gate's strides.
+// Gradient of the per-key gate (la_gla.cu) from q, k (token dtype) and the
+// fp32 gradients dqf, dkf; dg is fp32 with the gate's strides.  With dq, dk
+// set, the kernels also write dqf, dkf there in the token dtype.
 // Ft: the final state transposed [N][H][E][D] (fp32), dF: its upstream
 // gradient [N][H][D][E] (either may be null: no final-state term).  bsum:
 // scratch [N][H][nblk][D] fp32, nblk = ceil(longest sequence / DG_TB).
@@ -171,8 +177,11 @@ struct GateGradArgs {
     int64_t nblk;
     const int32_t *cu;
     int reverse, bf16;
-    const void *q, *k, *dq, *dk;
+    const void *q, *k;        // token dtype, strides sb, st, sh
     int64_t sb, st, sh;
+    const float *dqf, *dkf;   // fp32 dq, dk, strides fsb, fst, fsh
+    int64_t fsb, fst, fsh;
+    void *dq, *dk;            // or null: token-dtype copies of dqf, dkf (q's strides)
     float *dg;
     int64_t gsb, gst, gsh;
     const float *Ft, *dF;

@@ -136,6 +136,16 @@ __device__ __forceinline__ void store_half_row_sw128(uint8_t *row_base, int row,
             pack_bf16x2(__uint_as_float(x[8 * k4 + 6]), __uint_as_float(x[8 * k4 + 7])));
 }
 
+// 32 fp32 values as one 128-byte row of a 128B-swizzled tile.
+__device__ __forceinline__ void store_row_f32_sw128(uint8_t *row_base, int row,
+                                                    const uint32_t (&x)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4 *>(row_base + ((j ^ (row & 7)) << 4)) =
+            make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+}
+
 // Initial state row i, 8 columns at a time (once per CTA): fp32 from global
 // (any strides; this CTA's value columns start at e0), times colf[column]
 // when colf is given, -> times c0 as bf16 into the swizzled S copy (row i at
@@ -259,8 +269,9 @@ bool aligned_tok(const void *p, int64_t sb, int64_t st, int64_t sh)
 
 // 4-D map {channel, head, token, batch} with a {64, 1, rows, 1} box, 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t sb, int64_t st,
-              int64_t sh, int rows = TC_C, int hdiv = 1)
+              int64_t sh, int rows = TC_C, int hdiv = 1, bool f32 = false)
 {
+    const int esz = f32 ? 4 : 2;
     auto fn = encode_fn();
     if (!fn)
         return false;
@@ -274,12 +285,15 @@ bool make_map(CUtensorMap *m, const void *p, int X, const SweepArgs &a, int64_t 
     if (sh <= 0 || st <= 0 || sb <= 0 || sh >= lim || st >= lim || sb >= lim)
         return false;
     cuuint64_t dims[4] = {(cuuint64_t)X, (cuuint64_t)heads, (cuuint64_t)a.T, (cuuint64_t)a.B};
-    cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)st * 2, (cuuint64_t)sb * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+    cuuint64_t strides[3] = {(cuuint64_t)(sh * esz), (cuuint64_t)(st * esz),
+                             (cuuint64_t)(sb * esz)};
+    // the inner box is one 128-byte swizzle row: 64 bf16 or 32 fp32 values
+    cuuint32_t box[4] = {(cuuint32_t)(128 / esz), 1, (cuuint32_t)rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p), dims, strides,
-                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                    const_cast<void *>(p), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -152,7 +152,8 @@ __device__ __forceinline__ void zero_row(uint8_t *row_base)
 // s (forward-type) or 1; the state scaled after each chunk's update by the
 // chunk's factor and the next chunk's -- exp(B - r) then exp(r) going
 // forward, exp(r) then exp(B - r) going backward -- on its rows (GLA 1: the
-// gated key channels are the state's rows) or columns (GLA 2).
+// gated key channels are the state's rows) or columns (GLA 2).  GLA 2 gives
+// dq~ or dk~, which the gate's gradient needs unrounded: its output is fp32.
 // SO (state only): the sweep's final states alone (the sequence split's first
 // pass): Y and Z are loaded, the state update runs, X, the scores, P Z, the
 // inter term and the output are skipped.
@@ -744,6 +745,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 // a tile store may run past the end of a dense sequence (the
                 // copy clips it) but not into the next packed sequence
                 const bool tile = Lc == TC_C || !a.cu;
+                // GLA 2 (dq~ or dk~, which the gate's gradient takes
+                // unrounded): fp32 tiles, two 32-column parts at a time
+                // through the Z slot; a packed sequence's last chunk row by
+                // row from the registers
+                const bool f32tile = GLA == 2 && tile;
                 uint8_t *otile = sm + s * L::STAGE + L::XB + L::YB;   // Z slot, free once P Z is done
                 __nv_bfloat16 *orow = obase + (bos + chunk_t0(c) + i) * a.out.st;
 #pragma unroll 1
@@ -756,13 +762,58 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     for (int k = 0; k < 32; ++k)
                         ra[k] = __float_as_uint(
                             fmaf(lr, __uint_as_float(ri[k]), __uint_as_float(ra[k])));
-                    if (LA_OK_AT((part >> 1) * (TC_C * 128) + i * 128 + 128 <= L::ZB, 11))
+                    if (f32tile && part == E / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(o_free);   // both accumulators read
+                    }
+                    if (f32tile) {
+                        if (LA_OK_AT((part & 1) * (TC_C * 128) + i * 128 + 128 <= L::ZB, 23))
+                            store_row_f32_sw128(otile + (part & 1) * (TC_C * 128) + i * 128, i,
+                                                ra);
+                        if (part & 1) {
+                            // this warp's 32 rows of both parts, once the
+                            // copy engine can see them; the slot is written
+                            // again only after the copy has read it
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0 && LA_OK_AT(bos + chunk_t0(c) + 32 * q >= 0 &&
+                                                          bos + chunk_t0(c) < a.T &&
+                                                          e0 + E <= a.E,
+                                                      24)) {
+#pragma unroll
+                                for (int pp = 0; pp < 2; ++pp)
+                                    tma_store_4d(&P.mo, otile + pp * (TC_C * 128) + q * 32 * 128,
+                                                 32 * (part - 1 + pp) + e0, h,
+                                                 (int)(bos + chunk_t0(c)) + 32 * q, (int)row);
+                                bulk_commit_group();
+                                bulk_wait_read_all();
+                            }
+                            __syncwarp();
+                        }
+                    } else if (GLA == 2) {
+                        if (i < Lc && LA_OK_AT(bos + chunk_t0(c) + i < a.T, 22)) {
+                            float4 *frow = reinterpret_cast<float4 *>(
+                                static_cast<float *>(a.out.p) + row * a.out.sb +
+                                (int64_t)h * a.out.sh + (bos + chunk_t0(c) + i) * a.out.st + e0 +
+                                32 * part);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                frow[k] = make_float4(
+                                    __uint_as_float(ra[4 * k]), __uint_as_float(ra[4 * k + 1]),
+                                    __uint_as_float(ra[4 * k + 2]), __uint_as_float(ra[4 * k + 3]));
+                        }
+                    } else if (LA_OK_AT((part >> 1) * (TC_C * 128) + i * 128 + 128 <= L::ZB, 11)) {
                         store_half_row_sw128(otile + (part >> 1) * (TC_C * 128) + i * 128, i,
                                              part & 1, ra);
+                    }
                 }
-                tc_fence_before();
-                mbar_arrive(o_free);   // both accumulators read
-                if (tile) {
+                if (!f32tile) {
+                    tc_fence_before();
+                    mbar_arrive(o_free);   // both accumulators read
+                }
+                if (GLA == 2) {
+                    // written above
+                } else if (tile) {
                     // each warp sends its own 32 rows once they are visible to
                     // the copy engine
                     fence_proxy_async_smem();
@@ -818,10 +869,17 @@ cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullp
     if ((!SO && !make_map(&p.mx, x.p, D, a, x.sb, x.st, x.sh, TC_C, x.hdiv)) ||
         !make_map(&p.my, y.p, D, a, y.sb, y.st, y.sh, TC_C, y.hdiv) ||
         !make_map(&p.mz, z.p, a.E, a, z.sb, z.st, z.sh, TC_C, z.hdiv) ||
-        (!SO && !make_map(&p.mo, a.out.p, a.E, a, a.out.sb, a.out.st, a.out.sh, 32)))
+        (!SO && GLA != 2 && !make_map(&p.mo, a.out.p, a.E, a, a.out.sb, a.out.st, a.out.sh, 32)))
         return cudaErrorNotSupported;
     if (SO)
         p.mx = p.mo = p.my;
+    if (GLA == 2) {
+        // fp32 output: 32-column tiles, or 16-byte row writes
+        if ((reinterpret_cast<uintptr_t>(a.out.p) & 15) || a.out.sb % 4 || a.out.st % 4 ||
+            a.out.sh % 4 ||
+            !make_map(&p.mo, a.out.p, a.E, a, a.out.sb, a.out.st, a.out.sh, 32, 1, true))
+            return cudaErrorNotSupported;
+    }
     p.a = a;
     p.dx = x.hdiv;
     p.dy = y.hdiv;

@@ -181,7 +181,6 @@ __device__ __forceinline__ void token_loop(const SweepArgs &a, const Shape &sp, 
     const int cb = tile * sp.cw;                 // the CTA's first column
     const int cl = warp * sp.wc + 4 * qd;        // the thread's quad within the CTA's columns
     const int c0 = cb + cl;                      // ... and in the state
-    const int r0 = RP * rg;
     const int tbe = token_block(a.max_len);
 
     int64_t row, bos, len;
@@ -215,7 +214,14 @@ __device__ __forceinline__ void token_loop(const SweepArgs &a, const Shape &sp, 
     const T *vb = reinterpret_cast<const T *>(a.v.p) + row * a.v.sb +
                   (int64_t)(h / a.v.hdiv) * a.v.sh;
     const float *gb = GATE ? a.gate.p + row * a.gate.sb + (int64_t)h * a.gate.sh : nullptr;
-    T *ob = reinterpret_cast<T *>(a.out.p) + row * a.out.sb + (int64_t)h * a.out.sh;
+    // output rows: the token dtype, or fp32 when a bf16 call asks for it
+    const int64_t ob = row * a.out.sb + (int64_t)h * a.out.sh;
+    auto put = [&](int64_t off, float x) {
+        if (sizeof(T) == 2 && a.out_f32)
+            static_cast<float *>(a.out.p)[ob + off] = x;
+        else
+            st_tok(static_cast<T *>(a.out.p) + ob + off, x);
+    };
 
     // ---- staging: one block of Lb tokens into the compute layout -------------
     // paired row tables: (token u, row r) at (u rgn + r / 16) SK + 2 (r % 16),
@@ -354,12 +360,12 @@ __device__ __forceinline__ void token_loop(const SweepArgs &a, const Shape &sp, 
         if (sp.rgn == 1) {
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
-                T *op = ob + token(b0 + u0 + i) * a.out.st + c0;
+                const int64_t op = token(b0 + u0 + i) * a.out.st + c0;
                 const float x[4] = {hv[i].x, hv[i].y, hw[i].x, hw[i].y};
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     if (c0 + c < E)
-                        st_tok(op + c, sc * x[c]);
+                        put(op + c, sc * x[c]);
             }
             return;
         }
@@ -367,11 +373,11 @@ __device__ __forceinline__ void token_loop(const SweepArgs &a, const Shape &sp, 
             const int c = c0 + (bA ? 2 : 0);
 #pragma unroll
             for (int i = 0; i < NT; ++i) {
-                T *op = ob + token(b0 + u0 + i) * a.out.st;
+                const int64_t op = token(b0 + u0 + i) * a.out.st;
                 if (c < E)
-                    st_tok(op + c, sc * hv[i].x);
+                    put(op + c, sc * hv[i].x);
                 if (c + 1 < E)
-                    st_tok(op + c + 1, sc * hv[i].y);
+                    put(op + c + 1, sc * hv[i].y);
             }
             return;
         }
@@ -392,7 +398,7 @@ __device__ __forceinline__ void token_loop(const SweepArgs &a, const Shape &sp, 
         if (rg < 4 && c < E) {
 #pragma unroll
             for (int i = 0; i < NT; ++i)
-                st_tok(ob + token(b0 + u0 + i) * a.out.st + c, sc * val[i]);
+                put(token(b0 + u0 + i) * a.out.st + c, sc * val[i]);
         }
     };
     auto compute = [&](int64_t b0, int Lb) {
@@ -1002,7 +1008,8 @@ template <typename T> cudaError_t try_stream(const SweepArgs &a, cudaStream_t s)
         return !p || ((reinterpret_cast<uintptr_t>(p) & 15) == 0 && rs == a.E && cs == 1);
     };
     const int esz = (int)sizeof(T);
-    if (a.max_len > STREAM_MAX_T || a.gate.cols || a.gla_flags || sp.tiles != 1 || a.E % 4 ||
+    if (a.max_len > STREAM_MAX_T || a.gate.cols || a.gla_flags || a.out_f32 || sp.tiles != 1 ||
+        a.E % 4 ||
         !state_ok(a.s_in.p, a.s_in.rs, a.s_in.cs) || !state_ok(a.s_out.p, a.s_out.rs, a.s_out.cs) ||
         !rows_aligned(a, esz))
         return cudaErrorNotSupported;

@@ -164,12 +164,13 @@ def dg_condition(x, ref, reverse):
 
 
 def compare_gated(got, ref, x, reverse, tol, label):
-    """dg against the oracle relative to dg_condition; every other output by
-    the usual per-slice maximum relative error."""
-    rest = {k: v for k, v in ref.items() if k != "dg" and k in got}
-    compare({k: got[k] for k in rest}, rest, tol, cu=x["cu_seqlens"], label=label)
+    """Every output by the usual per-slice maximum relative error, dg
+    included; dg also relative to dg_condition (its error against the scale of
+    the sums it is made of).  Returns (plain, conditioned) for dg, or None."""
+    rest = {k: v for k, v in ref.items() if k in got}
+    errs = compare({k: got[k] for k in rest}, rest, tol, cu=x["cu_seqlens"], label=label)
     if "dg" not in ref:
-        return
+        return None
     cond = dg_condition(x, ref, reverse)
     d = np.abs(np.asarray(got["dg"].double().numpy()) - np.asarray(ref["dg"], dtype=np.float64))
     cu = x["cu_seqlens"]
@@ -184,3 +185,4 @@ def compare_gated(got, ref, x, reverse, tol, label):
             e = d[0, a:b].max(axis=(0, 2))
         worst = _worse(worst, (e / np.maximum(c, 1e-30)).max())
     assert worst <= tol, "%s: dg error %.3e of its condition above %.1e" % (label, worst, tol)
+    return errs["dg"], worst

@@ -216,3 +216,15 @@ def test_gated_backward_workspace_with_forward_operands(lib):
     d64 = _dims(B=2, T=300, H=3, D=128, E=64)
     assert lib.la_gla_workspace_size(ctypes.byref(d64), 0, None, 0) == \
         lib.la_gla_workspace_size(ctypes.byref(d64), 0, None, 1) > 0
+
+
+def test_gated_backward_workspace_holds_fp32_gradients(lib):
+    # the token-by-token part: the final state (fp32, transposed), dg's block
+    # sums (fp32, one per 256 tokens, channel and (sequence, head)) and, for
+    # bf16 tokens, dq and dk in fp32 ([B][T][H][D]), which dg takes unrounded
+    r = lambda x: (x + 255) // 256 * 256
+    d = _dims(B=2, T=300, H=3, D=128, E=96)
+    state, bsum, tokf = 2 * 3 * 128 * 96 * 4, 2 * 3 * 2 * 128 * 4, 2 * 300 * 3 * 128 * 4
+    assert lib.la_gla_workspace_size(ctypes.byref(d), 1, None, 1) == r(state) + r(bsum)
+    assert lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 1) == \
+        r(state) + r(bsum) + 2 * r(tokf)
