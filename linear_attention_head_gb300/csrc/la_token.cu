@@ -664,10 +664,12 @@ __global__ void __launch_bounds__(MAXW * 32, SHORTC ? 2 : 1) token_kernel(SweepA
 // by one 1-D bulk copy and back out by one bulk store, so that NS - 1 blocks
 // are in flight while the compute warps, which hold only the block they work
 // on, run the tokens.  Waits on the ring are bounded (2 s); on expiry the CTA
-// records LA_ERR_TIMEOUT, drains its copies and returns.
+// records LA_ERR_TIMEOUT, drains its copies and returns.  Blocks of up to
+// STREAM_MAX_T tokens run token by token, longer ones (up to TB tokens, no
+// gate) as one chunk of the chunked form (chunk_decode).
 
-// Longest call that takes the streamed kernel: beyond it one CTA per SM is
-// compute-bound on the token loop and the per-CTA kernel is faster.
+// Longest call that the streamed kernel runs token by token: beyond it one CTA
+// per SM is compute-bound on the token loop.
 constexpr int STREAM_MAX_T = 4;
 
 __device__ int g_token_error;
@@ -736,6 +738,13 @@ __device__ __forceinline__ bool named_and(bool ok, int count)
     return r != 0;
 }
 
+// Shared memory (floats) of the chunk form's tables: q and k rows as paired
+// row tables [TB][rgn][SK], the scores [TB][TB].
+__host__ __device__ inline size_t chunk_table_floats(int rgn)
+{
+    return (size_t)2 * TB * rgn * pair_stride(RP) + TB * TB;
+}
+
 // Bytes of one raw token slot of the streamed kernel: q, k rows [tbe][D] and
 // value rows [tbe][cw] of the token dtype, row gates [tbe][D] fp32.
 __host__ __device__ inline size_t stream_slot_bytes(const Shape &sp, int D, int tbe, int esz,
@@ -745,15 +754,221 @@ __host__ __device__ inline size_t stream_slot_bytes(const Shape &sp, int D, int 
                            (gate == 1 ? (size_t)D * 4 : 0)) + 15) / 16 * 16;
 }
 // Shared memory of the streamed kernel: NS state buffers, NS raw token slots,
-// 2 NS barriers, the abort word (16 bytes), then the token tables.
+// 2 NS barriers, the abort word (16 bytes), then the token tables (of the
+// token loop, or of the chunk form).
 __host__ __device__ inline size_t stream_smem_bytes(const Shape &sp, int D, int E, int tbe,
-                                                    int esz, int gate, int ns)
+                                                    int esz, int gate, int ns, bool chunk)
 {
     return (size_t)ns * D * E * 4 + (size_t)ns * stream_slot_bytes(sp, D, tbe, esz, gate) +
-           (size_t)2 * ns * 8 + 16 + token_smem_bytes(sp, RP, D, tbe, 4, gate, false);
+           (size_t)2 * ns * 8 + 16 +
+           (chunk ? chunk_table_floats(sp.rgn) * 4
+                  : token_smem_bytes(sp, RP, D, tbe, 4, gate, false));
 }
 
-template <typename T, int GATE>
+__device__ __forceinline__ f2 shfl_xor2(f2 x, int m)
+{
+    const float2 v = unpack2(x);
+    return pack2(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m));
+}
+// eight consecutive token values (16-byte aligned) as fp32
+template <typename T> __device__ __forceinline__ void ld8(const T *p, float (&x)[8]);
+template <> __device__ __forceinline__ void ld8<float>(const float *p, float (&x)[8])
+{
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+template <> __device__ __forceinline__ void ld8<__nv_bfloat16>(const __nv_bfloat16 *p, float (&x)[8])
+{
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+// four consecutive token values (8-byte aligned for bf16, 16 for fp32)
+template <typename T> __device__ __forceinline__ float4 ld4(const T *p);
+template <> __device__ __forceinline__ float4 ld4<float>(const float *p)
+{
+    return *reinterpret_cast<const float4 *>(p);
+}
+template <> __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    const uint2 r = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// One (sequence, head) block of L <= TB tokens as one chunk of the chunked
+// form (forward-type, the head's decay gamma = exp(g[h]) only), for the
+// streamed kernel: with the entering state S0 and processing index t,
+//   o_t = s gamma^(t+1) q_t S0 + s sum_{u <= t} gamma^(t-u) (q_t . k_u) v_u,
+//   S   = gamma^L S0 + sum_u gamma^(L-1-u) k_u^T v_u,
+// the recurrence summed in closed form (ejkernel `recurrent` docstring, "The
+// core update"; the Lightning Attention-2 paper's intra/inter split for one
+// block).  Each thread keeps its 16-row x 4-column state block in registers
+// (the layout of token_loop): the inter term for all L tokens is one pass
+// over its rows (fp32 pairs from the paired q table, 2 L FMA2 per row), then
+// a reduce-scatter over the RGN row-group lanes leaves each lane the sums of
+// its share of the tokens; the update is one more pass (paired k table).  The
+// token loop's reduction and state pass per token become one reduction per
+// group of 8 (or 16) tokens and one state pass per block.  All arithmetic fp32.  Raw rows (processing
+// order): q, k [L][D], v [L][cw] of the token dtype, 16-byte aligned.
+template <typename T, int RGN>
+__device__ __forceinline__ void chunk_decode(const SweepArgs &a, const Shape &sp, int n, int h,
+                                             int tid, int ncomp, float *tab, f2 (&S01)[RP],
+                                             f2 (&S23)[RP], const T *rq, const T *rk,
+                                             const T *rv)
+{
+    constexpr int QW = 32 / RGN, SK = pair_stride(RP);
+    const int D = a.D, E = a.E;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int qd = lane & (QW - 1), rg = lane / QW;
+    const int c0 = warp * sp.wc + 4 * qd;
+    int64_t row, bos, len;
+    if (a.cu) {
+        row = 0;
+        bos = a.cu[n];
+        len = (int64_t)a.cu[n + 1] - a.cu[n];
+    } else {
+        row = n;
+        bos = 0;
+        len = a.T;
+    }
+    const int L = (int)len;
+    const float g = a.g[h], scale = a.scale;
+    float *QQ = tab;                      // s gamma^(t+1) q_t, paired rows
+    float *KK = QQ + TB * RGN * SK;       // gamma^(L-1-u) k_u, paired rows
+    float *P = KK + TB * RGN * SK;        // [t][u]: s gamma^(t-u) q_t . k_u, u <= t
+    for (int i = tid; i < L * RGN * RP; i += ncomp) {
+        const int t = i / (RGN * RP), r = i % (RGN * RP);
+        float qv = 0.f, kv = 0.f;
+        if (r < D) {
+            qv = ld_tok(rq + t * D + r) * scale * expf(g * (float)(t + 1));
+            kv = ld_tok(rk + t * D + r) * expf(g * (float)(L - 1 - t));
+        }
+        const int at = (t * RGN + r / RP) * SK + 2 * (r % RP);
+        *reinterpret_cast<float2 *>(QQ + at) = make_float2(qv, qv);
+        *reinterpret_cast<float2 *>(KK + at) = make_float2(kv, kv);
+    }
+    for (int i = tid; i < TB * TB; i += ncomp) {
+        const int t = i / TB, u = i % TB;
+        float sc = 0.f;
+        if (u <= t && t < L) {
+            // pieces of 8 channels, started at piece u: the 16 lanes of a
+            // half warp read 16 different k rows in different banks
+            const int np = D / 8;
+            float acc = 0.f;
+            for (int p = 0, pc = u % np; p < np; ++p, pc = pc + 1 == np ? 0 : pc + 1) {
+                float xq[8], xk[8];
+                ld8(rq + t * D + 8 * pc, xq);
+                ld8(rk + u * D + 8 * pc, xk);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    acc = fmaf(xq[e], xk[e], acc);
+            }
+            sc = acc * scale * expf(g * (float)(t - u));
+        }
+        P[i] = sc;
+    }
+    NamedSync{ncomp}();
+
+    // Tokens in groups of TG (8, or 16 for 16 row groups: the live sums stay
+    // at 4 TG registers).  Inter term: A[t] = (s gamma^(t+1) q_t) . S0 over
+    // this thread's rows; then a reduce-scatter over the row-group lanes
+    // (lane bits of rg, highest first) leaves the lane of row group rg the
+    // tokens t0 + rg TPG .. t0 + rg TPG + TPG - 1, summed over all rows, in
+    // A[0 .. TPG - 1]; then the intra term and the output.
+    constexpr int TG = RGN > 8 ? TB : 8, TPG = TG / RGN;
+    constexpr int LEVELS = RGN >= 16 ? 4 : RGN >= 8 ? 3 : RGN >= 4 ? 2 : RGN >= 2 ? 1 : 0;
+    T *ob = static_cast<T *>(a.out.p) + row * a.out.sb + (int64_t)h * a.out.sh + c0;
+#pragma unroll 1
+    for (int t0 = 0; t0 < L; t0 += TG) {
+        f2 A01[TG], A23[TG];
+#pragma unroll
+        for (int k = 0; k < TG; ++k) {
+            A01[k] = 0ull;
+            A23[k] = 0ull;
+            if (t0 + k < L) {
+                const float *qp = QQ + ((t0 + k) * RGN + rg) * SK;
+#pragma unroll
+                for (int j = 0; j < RP; j += 2) {
+                    const ulonglong2 w = *reinterpret_cast<const ulonglong2 *>(qp + 2 * j);
+                    A01[k] = fma2(w.x, S01[j], A01[k]);
+                    A23[k] = fma2(w.x, S23[j], A23[k]);
+                    A01[k] = fma2(w.y, S01[j + 1], A01[k]);
+                    A23[k] = fma2(w.y, S23[j + 1], A23[k]);
+                }
+            }
+        }
+#pragma unroll
+        for (int l = 0; l < LEVELS; ++l) {
+            const int lv = RGN >> (l + 1), half = TG >> (l + 1);
+            const bool hi = (rg & lv) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const f2 k01 = hi ? A01[i + half] : A01[i], s01 = hi ? A01[i] : A01[i + half];
+                const f2 k23 = hi ? A23[i + half] : A23[i], s23 = hi ? A23[i] : A23[i + half];
+                A01[i] = add2(k01, shfl_xor2(s01, lv * QW));
+                A23[i] = add2(k23, shfl_xor2(s23, lv * QW));
+            }
+        }
+        if (c0 < E) {
+#pragma unroll
+            for (int k = 0; k < TPG; ++k) {
+                const int t = t0 + rg * TPG + k;
+                if (t >= L)
+                    break;
+                const float2 i01 = unpack2(A01[k]), i23 = unpack2(A23[k]);
+                float o0 = i01.x, o1 = i01.y, o2 = i23.x, o3 = i23.y;
+                for (int u = 0; u <= t; ++u) {
+                    const float pr = P[t * TB + u];
+                    const float4 v4 = ld4(rv + u * sp.cw + c0);
+                    o0 = fmaf(pr, v4.x, o0);
+                    o1 = fmaf(pr, v4.y, o1);
+                    o2 = fmaf(pr, v4.z, o2);
+                    o3 = fmaf(pr, v4.w, o3);
+                }
+                T *op = ob + (bos + (a.reverse ? L - 1 - t : t)) * a.out.st;
+                st_tok(op, o0);
+                st_tok(op + 1, o1);
+                st_tok(op + 2, o2);
+                st_tok(op + 3, o3);
+            }
+        }
+    }
+    // the state: gamma^L S0 + sum_u (gamma^(L-1-u) k_u)^T v_u
+    const float gl = expf(g * (float)L);
+    const f2 gl2 = pack2(gl, gl);
+#pragma unroll
+    for (int j = 0; j < RP; ++j) {
+        S01[j] = mul2(S01[j], gl2);
+        S23[j] = mul2(S23[j], gl2);
+    }
+    if (c0 < E) {
+#pragma unroll 2
+        for (int u = 0; u < L; ++u) {
+            const float4 v4 = ld4(rv + u * sp.cw + c0);
+            const f2 v01 = pack2(v4.x, v4.y), v23 = pack2(v4.z, v4.w);
+            const float *kp = KK + (u * RGN + rg) * SK;
+#pragma unroll
+            for (int j = 0; j < RP; j += 2) {
+                const ulonglong2 w = *reinterpret_cast<const ulonglong2 *>(kp + 2 * j);
+                S01[j] = fma2(w.x, v01, S01[j]);
+                S23[j] = fma2(w.x, v23, S23[j]);
+                S01[j + 1] = fma2(w.y, v01, S01[j + 1]);
+                S23[j + 1] = fma2(w.y, v23, S23[j + 1]);
+            }
+        }
+    }
+}
+
+// CRGN > 0: the blocks run as one chunk each (chunk_decode, CRGN row groups)
+// instead of token by token.
+template <typename T, int GATE, int CRGN = 0>
 __global__ void __launch_bounds__(MAXW * 32 + 32, 1) stream_kernel(SweepArgs a, int ns)
 {
     const int D = a.D, E = a.E;
@@ -915,13 +1130,18 @@ __global__ void __launch_bounds__(MAXW * 32 + 32, 1) stream_kernel(SweepArgs a, 
             S01[j] = x.x;
             S23[j] = x.y;
         }
-        RawRows pre;
-        pre.q = slot_q(buf);
-        pre.k = slot_k(buf);
-        pre.v = slot_v(buf);
-        pre.g = slot_g(buf);
-        token_loop<T, false, GATE, false, true>(a, sp, hn / a.H, hn % a.H, 0, tid, ncomp, tok, S01,
-                                               S23, NamedSync{ncomp}, pre);
+        if constexpr (CRGN > 0) {
+            chunk_decode<T, CRGN>(a, sp, hn / a.H, hn % a.H, tid, ncomp, tok, S01, S23,
+                                  slot_q(buf), slot_k(buf), slot_v(buf));
+        } else {
+            RawRows pre;
+            pre.q = slot_q(buf);
+            pre.k = slot_k(buf);
+            pre.v = slot_v(buf);
+            pre.g = slot_g(buf);
+            token_loop<T, false, GATE, false, true>(a, sp, hn / a.H, hn % a.H, 0, tid, ncomp, tok,
+                                                   S01, S23, NamedSync{ncomp}, pre);
+        }
         if (has_out && c0 < E) {
 #pragma unroll
             for (int j = 0; j < RP; ++j)
@@ -1008,10 +1228,12 @@ template <typename T> cudaError_t try_stream(const SweepArgs &a, cudaStream_t s)
         return !p || ((reinterpret_cast<uintptr_t>(p) & 15) == 0 && rs == a.E && cs == 1);
     };
     const int esz = (int)sizeof(T);
-    if (a.max_len > STREAM_MAX_T || a.gate.cols || a.gla_flags || a.out_f32 || sp.tiles != 1 ||
-        a.E % 4 ||
-        !state_ok(a.s_in.p, a.s_in.rs, a.s_in.cs) || !state_ok(a.s_out.p, a.s_out.rs, a.s_out.cs) ||
-        !rows_aligned(a, esz))
+    // up to STREAM_MAX_T tokens token by token; up to TB tokens (no gate, key
+    // width a multiple of 8) as one chunk
+    const bool chunk = a.max_len > STREAM_MAX_T;
+    if (a.max_len > TB || (chunk && (a.gate.p || a.D % 8)) || a.gate.cols || a.gla_flags ||
+        a.out_f32 || sp.tiles != 1 || a.E % 4 || !state_ok(a.s_in.p, a.s_in.rs, a.s_in.cs) ||
+        !state_ok(a.s_out.p, a.s_out.rs, a.s_out.cs) || !rows_aligned(a, esz))
         return cudaErrorNotSupported;
     int dev = 0, sms = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1026,12 +1248,22 @@ template <typename T> cudaError_t try_stream(const SweepArgs &a, cudaStream_t s)
         return cudaErrorNotSupported;
     const int gate = a.gate.p ? 1 : 0, tbe = token_block(a.max_len);
     int ns = 3;
-    while (ns >= 2 && stream_smem_bytes(sp, a.D, a.E, tbe, esz, gate, ns) > (size_t)optin)
+    while (ns >= 2 && stream_smem_bytes(sp, a.D, a.E, tbe, esz, gate, ns, chunk) > (size_t)optin)
         --ns;
     if (ns < 2)
         return cudaErrorNotSupported;
-    const size_t smem = stream_smem_bytes(sp, a.D, a.E, tbe, esz, gate, ns);
+    const size_t smem = stream_smem_bytes(sp, a.D, a.E, tbe, esz, gate, ns, chunk);
     auto kernel = gate ? stream_kernel<T, 1> : stream_kernel<T, 0>;
+    if (chunk) {
+        switch (sp.rgn) {
+        case 1: kernel = stream_kernel<T, 0, 1>; break;
+        case 2: kernel = stream_kernel<T, 0, 2>; break;
+        case 4: kernel = stream_kernel<T, 0, 4>; break;
+        case 8: kernel = stream_kernel<T, 0, 8>; break;
+        case 16: kernel = stream_kernel<T, 0, 16>; break;
+        default: return cudaErrorNotSupported;
+        }
+    }
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
@@ -1062,6 +1294,13 @@ cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s, bool *stream
 {
     if (streamed)
         *streamed = false;
+    // more than STREAM_MAX_T tokens: one chunk on the tensor cores where it
+    // applies
+    if (a.max_len > STREAM_MAX_T) {
+        const cudaError_t e = decode_chunk_sweep(a, s);
+        if (e != cudaErrorNotSupported)
+            return e;
+    }
     if (a.N != 0 && a.H != 0 && a.D >= 1 && a.D <= 256 && a.E >= 1) {
         const cudaError_t e = a.bf16 ? try_stream<__nv_bfloat16>(a, s) : try_stream<float>(a, s);
         if (e != cudaErrorNotSupported) {

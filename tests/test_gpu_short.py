@@ -33,7 +33,8 @@ def test_kernel_family_switches_at_16_tokens():
 
 
 @pytest.mark.parametrize("T", [1, 2, 7, 16])
-@pytest.mark.parametrize("dtype,D,E", [(torch.bfloat16, 128, 128), (torch.float32, 64, 64),
+@pytest.mark.parametrize("dtype,D,E", [(torch.bfloat16, 128, 128), (torch.bfloat16, 128, 16),
+                                       (torch.float32, 64, 64),
                                        (torch.bfloat16, 192, 192), (torch.bfloat16, 16, 48),
                                        (torch.float32, 1, 1), (torch.bfloat16, 256, 40)])
 def test_short_matches_oracle(T, dtype, D, E):
@@ -85,13 +86,20 @@ def test_decoding_piece_by_piece_equals_one_call():
             label="one call")
 
 
-# At least twice as many (sequence, head) blocks as the GPU has SMs: calls of
-# at most 4 tokens take the streamed decode kernel (state blocks moved through
-# shared memory by bulk copies), 16 tokens the per-CTA kernel.  20 x 16 = 320
-# blocks covers GPUs of up to 160 SMs.
-@pytest.mark.parametrize("T", [1, 4, 16])
+# At least twice as many (sequence, head) blocks as the GPU has SMs: the
+# streamed decode kernel (state blocks moved through shared memory by bulk
+# copies) runs calls of at most 4 tokens token by token, and of 5 to 16
+# tokens (key width a multiple of 8) as one chunk of the chunked form: one
+# group of 8 tokens or two, every row-group count (D = 8..256); D = 12 takes
+# the per-CTA kernel.  bf16 with D = 128 and E a multiple of 16 runs 5 to 16
+# tokens on the tensor cores instead (la_decode.cu), E = 40 not.  20 x 16 =
+# 320 blocks covers GPUs of up to 160 SMs.
+@pytest.mark.parametrize("T", [1, 4, 5, 9, 16])
 @pytest.mark.parametrize("dtype,D,E", [(torch.bfloat16, 128, 128), (torch.float32, 64, 64),
-                                       (torch.bfloat16, 32, 96), (torch.bfloat16, 48, 80)])
+                                       (torch.bfloat16, 32, 96), (torch.bfloat16, 48, 80),
+                                       (torch.bfloat16, 256, 64), (torch.float32, 16, 128),
+                                       (torch.bfloat16, 8, 32), (torch.float32, 12, 20),
+                                       (torch.bfloat16, 128, 48), (torch.bfloat16, 128, 40)])
 @pytest.mark.parametrize("init", [0.3, 0.0])
 def test_streamed_decode_matches_oracle(T, dtype, D, E, init):
     assert torch.cuda.get_device_properties(0).multi_processor_count <= 160
@@ -103,11 +111,13 @@ def test_streamed_decode_matches_oracle(T, dtype, D, E, init):
                                                                                  reverse))
 
 
-def test_streamed_decode_packed_and_in_place():
-    # 330 packed sequences of 0..4 tokens (the streamed kernel); the state
-    # updated in place (initial and final state the same buffer)
+@pytest.mark.parametrize("longest", [4, 16])
+def test_streamed_decode_packed_and_in_place(longest):
+    # 330 packed sequences of 0..4 tokens (the streamed kernel, token by
+    # token) or 0..16 (as chunks); the state updated in place (initial and
+    # final state the same buffer)
     gen = torch.Generator().manual_seed(5)
-    lens = torch.randint(0, 5, (330,), generator=gen).tolist()
+    lens = torch.randint(0, longest + 1, (330,), generator=gen).tolist()
     w = _w(1, 0, 2, 128, 128, torch.bfloat16, seqlens=lens, init=0.2, dfin=0.0)
     x = W.make_inputs(w, seed=12)
     ref = oracle_run(x, backward=False)
