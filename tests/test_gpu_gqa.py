@@ -4,8 +4,9 @@ The reference result is the oracle run with every key/value head repeated
 for its G = H / H_kv query heads (the definition of sharing), with the
 gradient of a shared head the sum of its copies' gradients (the chain rule
 through the repetition).  Checked for the chunked tensor-core path (bf16,
-D = 128), the CUDA-core path (fp32), the token-by-token path (short
-sequences), packed sequences, both directions, and with the sequence split.
+D = 128, groups of 2, 3, 4 and 8), the CUDA-core path (fp32), the
+token-by-token path (short sequences), packed sequences, both directions,
+and with the sequence split.
 """
 import math
 
@@ -41,8 +42,10 @@ def _reference(rep, G, reverse):
 
 
 @pytest.mark.parametrize("T,H,Hkv,D,dtype", [
-    (300, 4, 2, 128, torch.bfloat16),     # tensor-core chunked kernels
+    (300, 4, 2, 128, torch.bfloat16),     # tensor-core chunked kernels, groups of 2
+    (300, 8, 2, 128, torch.bfloat16),     # groups of 4
     (300, 8, 1, 128, torch.bfloat16),     # one key/value head for all queries
+    (300, 6, 2, 128, torch.bfloat16),     # groups of 3
     (200, 4, 2, 64, torch.float32),       # CUDA-core chunked kernels
     (7, 6, 3, 128, torch.bfloat16),       # token-by-token kernels
 ])
