@@ -778,15 +778,17 @@ la_status la_get_device_error(void *stream)
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e == cudaSuccess)
         e = la::tc_read_and_clear_error((cudaStream_t)stream, &err);
-    int err2 = 0, err3 = 0;
+    int err2 = 0, err3 = 0, err4 = 0;
     if (e == cudaSuccess)
         e = la::token_read_and_clear_error((cudaStream_t)stream, &err2);
     if (e == cudaSuccess)
         e = la::tc_dkdv_read_and_clear_error((cudaStream_t)stream, &err3);
+    if (e == cudaSuccess)
+        e = la::decode_read_and_clear_error((cudaStream_t)stream, &err4);
     if (e != cudaSuccess)
         return cuda_fail(e, "la_get_device_error");
     if (!err)
-        err = err2 ? err2 : err3;
+        err = err2 ? err2 : err3 ? err3 : err4;
     else if ((err & 0xff) != LA_ERR_BOUNDS && (err3 & 0xff) == LA_ERR_BOUNDS)
         err = err3;
     if ((err & 0xff) == LA_ERR_BOUNDS)

@@ -151,8 +151,12 @@ cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s, bool *stream
 // Decoding up to 16 tokens as one chunk on the tensor cores (la_decode.cu):
 // bf16, D = 128, E a multiple of 16 up to 128, forward-type, no gate,
 // contiguous 16-byte aligned states, 16-byte aligned token rows;
-// cudaErrorNotSupported otherwise.
-cudaError_t decode_chunk_sweep(const SweepArgs &a, cudaStream_t s);
+// cudaErrorNotSupported otherwise.  (*streamed, when given: whether the
+// streamed form, the one with ring hand-offs, ran.)
+cudaError_t decode_chunk_sweep(const SweepArgs &a, cudaStream_t s, bool *streamed = nullptr);
+// Reads (after synchronizing s) and clears the decode kernels' device error
+// word (LA_ERR_TIMEOUT when a wait of the streamed form ran out).
+cudaError_t decode_read_and_clear_error(cudaStream_t s, int *err);
 cudaError_t short_backward_sweep(const SweepArgs &a, cudaStream_t s);
 // Reads (after synchronizing s) and clears the token kernels' device error
 // word (LA_ERR_TIMEOUT when a wait of the streamed decode kernel ran out).

@@ -1297,7 +1297,7 @@ cudaError_t short_forward_sweep(const SweepArgs &a, cudaStream_t s, bool *stream
     // more than STREAM_MAX_T tokens: one chunk on the tensor cores where it
     // applies
     if (a.max_len > STREAM_MAX_T) {
-        const cudaError_t e = decode_chunk_sweep(a, s);
+        const cudaError_t e = decode_chunk_sweep(a, s, streamed);
         if (e != cudaErrorNotSupported)
             return e;
     }

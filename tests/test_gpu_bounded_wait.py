@@ -37,12 +37,14 @@ def test_withheld_handoff_reports_timeout_and_context_survives():
     compare(got, oracle_run(x, backward=False), TOL[torch.bfloat16], label="after timeout")
 
 
-def test_withheld_copy_in_streamed_decode_reports_timeout():
-    # 20 x 16 = 320 (sequence, head) blocks of one token: the streamed decode
-    # kernel, whose copy warp then skips each CTA's first state block, so the
-    # compute warps' bounded wait on it runs out
+@pytest.mark.parametrize("T", [1, 16])
+def test_withheld_copy_in_streamed_decode_reports_timeout(T):
+    # 20 x 16 = 320 (sequence, head) blocks of one token (the streamed decode
+    # kernel, token by token) or 16 (its tensor-core form): the copy warp
+    # then skips each CTA's first state block, so the compute warps' bounded
+    # wait on it runs out
     assert torch.cuda.get_device_properties(0).multi_processor_count <= 160
-    w = W.Workload("decode", 20, 1, 16, 128, 128, torch.bfloat16, W.alibi_g_gamma(16), 0.1,
+    w = W.Workload("decode", 20, T, 16, 128, 128, torch.bfloat16, W.alibi_g_gamma(16), 0.1,
                    init_std=0.1, backward=False)
     x = W.make_inputs(w, seed=52)
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}

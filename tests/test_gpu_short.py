@@ -92,8 +92,9 @@ def test_decoding_piece_by_piece_equals_one_call():
 # tokens (key width a multiple of 8) as one chunk of the chunked form: one
 # group of 8 tokens or two, every row-group count (D = 8..256); D = 12 takes
 # the per-CTA kernel.  bf16 with D = 128 and E a multiple of 16 runs 5 to 16
-# tokens on the tensor cores instead (la_decode.cu), E = 40 not.  20 x 16 =
-# 320 blocks covers GPUs of up to 160 SMs.
+# tokens on the tensor cores instead (la_decode.cu: its streamed form at
+# E = 128, its per-CTA form at E = 48), E = 40 not.  20 x 16 = 320 blocks
+# covers GPUs of up to 160 SMs.
 @pytest.mark.parametrize("T", [1, 4, 5, 9, 16])
 @pytest.mark.parametrize("dtype,D,E", [(torch.bfloat16, 128, 128), (torch.float32, 64, 64),
                                        (torch.bfloat16, 32, 96), (torch.bfloat16, 48, 80),
