@@ -467,7 +467,7 @@ def call_launches(la, q, k, v, do, g, scale):
 
 def length_sweep(la, torch, dev, stream, skip_n):
     """fwd and bwd times at every length of the Lightning-2 benchmark table (b4 h32
-    d=e=128 bf16), each the mean of 5 calls after 3 warm-up calls.  The GPU is first
+    d=e=128 bf16), each the median of 20 calls after 5 warm-up calls.  The GPU is first
     held busy (torch.cuda._sleep) so that all 5 calls are queued before the first
     runs and host-side call overhead stays out of the events.  Lengths up to 4096
     tokens are timed with a 512 MB L2 flush before each call (`fwd_ms`, `bwd_ms`)
@@ -488,21 +488,7 @@ def length_sweep(la, torch, dev, stream, skip_n):
         small = n <= 4096
 
         def timed(fn, flush_first):
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            evs = []
-            torch.cuda._sleep(20_000_000)
-            for _ in range(5):
-                if flush_first:
-                    flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                evs.append((e0, e1))
-            torch.cuda.synchronize()
-            return sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
+            return _timed_calls(torch, stream, fn, flush if flush_first else None)
 
         fwd = lambda: la.la_fwd(q, k, v, g, w.scale)
         bwd = lambda: la.la_bwd(q, k, v, do, g, w.scale, want_d_initial_state=False)
@@ -521,10 +507,11 @@ def length_sweep(la, torch, dev, stream, skip_n):
     return out
 
 
-def _timed_calls(torch, stream, fn, flush=None, calls=5, warm=3):
-    """Mean event time of `calls` calls of fn queued behind torch.cuda._sleep (no host
+def _timed_calls(torch, stream, fn, flush=None, calls=20, warm=5):
+    """Median event time of `calls` calls of fn queued behind torch.cuda._sleep (no host
     gap enters the events), after `warm` untimed calls; with `flush`, that buffer is
     overwritten before each call (an L2 flush, inside the stream but outside the events)."""
+    import statistics
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
@@ -539,7 +526,7 @@ def _timed_calls(torch, stream, fn, flush=None, calls=5, warm=3):
         e1.record(stream)
         evs.append((e0, e1))
     torch.cuda.synchronize()
-    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
 
 def packed_work(T, H, d, e, n_seqs, token_bytes=2):
@@ -555,8 +542,8 @@ def packed_work(T, H, d, e, n_seqs, token_bytes=2):
 
 
 def configs_bench(la, torch, dev, stream, hbm, tfl):
-    """The other workload shapes, fwd and bwd timed separately (mean of 5 queued
-    calls after 3 warm-up calls):
+    """The other workload shapes, fwd and bwd timed separately (median of 20 queued
+    calls after 5 warm-up calls):
       * b2 h8 n2048 d=e=64 and b2 h12 n2048 d=e=192 (bf16): their token tensors fit
         in L2, so each call follows a 512 MB L2 flush (`*_ms`); back to back without
         one in `*_ms_unflushed`;
