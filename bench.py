@@ -668,7 +668,7 @@ def split_bench(la, torch, dev, stream, peak):
     out = {"workload": "fwd+bwd b1 h8 n262144 d=e=128 bf16, ALiBi slopes, scale 1"}
     nbytes = 11 * B * T * H * D * 2
     for name, mode in (("split", 1), ("unsplit", 0)):
-        _native.check(_native.lib().la_set_sequence_split(mode, 2048))
+        _native.check(_native.lib().la_set_sequence_split(mode, 0))
         for _ in range(2):
             step()
         torch.cuda.synchronize()
@@ -682,7 +682,7 @@ def split_bench(la, torch, dev, stream, peak):
         ms = e0.elapsed_time(e1) / 5
         out[name] = {"ms_per_step": ms, "tokens_per_s": B * T / (ms * 1e-3),
                      "compulsory_frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
-    _native.check(_native.lib().la_set_sequence_split(1, 2048))
+    _native.check(_native.lib().la_set_sequence_split(1, 0))
     la.get_device_error(dev)
     del q, k, v, do
     return out

@@ -252,10 +252,12 @@ size_t la_workspace_size(int32_t num_seqs);
 size_t la_workspace_size_for(const la_dims *dims, int32_t dtype, const int32_t *cu_seqlens_host);
 
 /* Sequence split control, process-wide: mode 1 (default) splits when it
- * applies, 0 never; min_segment_tokens (>= 128, default 2048) is the
- * shortest segment planned.  The method's pages have no counterpart: the
- * split is a way of scheduling the same arithmetic.  LA_ERR_INVALID_ARG for
- * other values. */
+ * applies, 0 never.  min_segment_tokens 0 (default) chooses by head width:
+ * segments of at least 256 tokens at D <= 64, at least 4 segments of at
+ * least 1024 tokens at D <= 128, no split above; a value >= 128 is the
+ * shortest segment planned, at any width.  The method's pages have no
+ * counterpart: the split is a way of scheduling the same arithmetic.
+ * LA_ERR_INVALID_ARG for other values. */
 la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens);
 
 /* Gated form (GLA): ejkernel `recurrent` with its gate g (the GLA page's

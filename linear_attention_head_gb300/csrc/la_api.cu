@@ -188,7 +188,7 @@ la_status make_schedule(const Problem &P, void *ws, size_t ws_bytes, cudaStream_
 // every token tensor's batch stride to be T times its token stride.
 
 std::atomic<int> g_split_mode{1};            // 0 off, 1 when it pays
-std::atomic<int> g_split_min_seg{2048};      // shortest segment planned
+std::atomic<int> g_split_min_seg{0};         // shortest segment planned; 0 automatic
 
 int sm_count()
 {
@@ -240,9 +240,22 @@ SplitPlan plan_split(const Problem &P, const la_dims *d, int sms = 0)
                                      : (int64_t)P.T;
         max_len = std::max(max_len, len);
     }
-    const int64_t min_seg = std::max(128, g_split_min_seg.load());
+    // Automatic segments, from measured calls (b2.h8.n2048 d=64, b2.h16.n4096
+    // and b1.h16.n8192 d=128, b2.h12.n2048 d=192, fwd + bwd): at d <= 64
+    // segments of 256 tokens already pay (154.7 -> 117.9 us); at d = 128 a
+    // split pays from 4 segments of at least 1024 tokens (324 -> 288 us,
+    // 623 -> 299 us) but not with 2 (348 us) or with 256-token segments; at
+    // d > 128 the state pass has no state-only form and the split costs
+    // (278 -> 399 us at 1024-token segments).
+    int64_t min_seg = g_split_min_seg.load(), min_r = 2;
+    if (min_seg == 0) {
+        if (P.D > 128)
+            return S;
+        min_seg = P.D <= 64 ? 256 : 1024;
+        min_r = P.D <= 64 ? 2 : 4;
+    }
     const int64_t R = std::min<int64_t>(sms / items, max_len / min_seg);
-    if (R < 2)
+    if (R < min_r)
         return S;
     const int64_t seg_len = ((max_len + R - 1) / R + 127) / 128 * 128;
     S.seq_first.push_back(0);
@@ -854,7 +867,7 @@ size_t la_workspace_size_for(const la_dims *dims, int32_t dtype, const int32_t *
 
 la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens)
 {
-    if (mode < 0 || mode > 1 || min_segment_tokens < 128)
+    if (mode < 0 || mode > 1 || (min_segment_tokens != 0 && min_segment_tokens < 128))
         return fail(LA_ERR_INVALID_ARG, "la_set_sequence_split: mode %d, min_segment_tokens %d",
                     mode, min_segment_tokens);
     g_split_mode.store(mode);

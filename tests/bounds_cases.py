@@ -50,7 +50,7 @@ def main():
     try:
         parity_case("split d128", custom(1, 1100, 1, 128, 128), 3)
     finally:
-        N.check(N.lib().la_set_sequence_split(1, 2048))
+        N.check(N.lib().la_set_sequence_split(1, 0))
     # grouped key/value heads (per-query-head contributions) and the gated
     # form on the tensor cores: run only, the index checks are what is read
     dev = "cuda"

@@ -188,6 +188,8 @@ def test_workspace_size_for_and_split_control(lib):
     assert lib.la_set_sequence_split(1, 64) == N.LA_ERR_INVALID_ARG
     assert lib.la_set_sequence_split(0, 4096) == N.LA_OK
     assert lib.la_set_sequence_split(1, 2048) == N.LA_OK
+    assert lib.la_set_sequence_split(1, 127) == N.LA_ERR_INVALID_ARG
+    assert lib.la_set_sequence_split(1, 0) == N.LA_OK   # automatic, the default
 
 
 def test_gated_forward_workspace_size(lib):

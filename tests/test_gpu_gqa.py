@@ -70,7 +70,7 @@ def test_grouped_heads_with_sequence_split():
         kv, rep, G = _grouped(1, 3000, 4, 2, 128, torch.bfloat16, seed=11)
         compare(gpu_run(kv), _reference(rep, G, False), TOL[torch.bfloat16], label="split")
     finally:
-        N.check(N.lib().la_set_sequence_split(1, 2048))
+        N.check(N.lib().la_set_sequence_split(1, 0))
 
 
 def test_grouped_heads_autograd_and_shape_checks():

@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 def short_segments():
     N.check(N.lib().la_set_sequence_split(1, 256))
     yield
-    N.check(N.lib().la_set_sequence_split(1, 2048))
+    N.check(N.lib().la_set_sequence_split(1, 0))
 
 
 def _w(B, T, H, D, dtype, seqlens=None):
