@@ -56,6 +56,16 @@ def test_grouped_heads_match_oracle(T, H, Hkv, D, dtype):
                 label="T=%d H=%d Hkv=%d rev=%d" % (T, H, Hkv, reverse))
 
 
+def test_grouped_heads_streamed_decode():
+    # 20 x 16 = 320 (sequence, head) blocks of 9 tokens, 4 query heads per
+    # key/value head: the streamed tensor-core decode reads the shared rows
+    assert torch.cuda.get_device_properties(0).multi_processor_count <= 160
+    kv, rep, G = _grouped(20, 9, 16, 4, 128, torch.bfloat16, seed=19)
+    for reverse in (False, True):
+        compare(gpu_run(kv, reverse), _reference(rep, G, reverse), TOL[torch.bfloat16],
+                label="streamed decode rev=%d" % reverse)
+
+
 def test_grouped_heads_packed():
     lens = [130, 0, 257, 5]
     kv, rep, G = _grouped(1, 0, 4, 2, 128, torch.bfloat16, seqlens=lens, seed=9)

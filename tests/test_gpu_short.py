@@ -100,7 +100,8 @@ def test_decoding_piece_by_piece_equals_one_call():
                                        (torch.bfloat16, 32, 96), (torch.bfloat16, 48, 80),
                                        (torch.bfloat16, 256, 64), (torch.float32, 16, 128),
                                        (torch.bfloat16, 8, 32), (torch.float32, 12, 20),
-                                       (torch.bfloat16, 128, 48), (torch.bfloat16, 128, 40)])
+                                       (torch.bfloat16, 128, 48), (torch.bfloat16, 128, 40),
+                                       (torch.bfloat16, 128, 64)])
 @pytest.mark.parametrize("init", [0.3, 0.0])
 def test_streamed_decode_matches_oracle(T, dtype, D, E, init):
     assert torch.cuda.get_device_properties(0).multi_processor_count <= 160
