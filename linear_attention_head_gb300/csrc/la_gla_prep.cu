@@ -21,15 +21,14 @@
 // the sweep cuts them, in either direction.
 //
 // The backward runs its three sweeps on the same operands and yields
-// dq~ = dq exp(r - b) and dk~ = dk exp(b - r) in fp32; the second mode of this
-// kernel recomputes b and r (the same arithmetic, so the same values), turns
-// them into dq and dk (token dtype) and forms the gate's gradient, for every
-// (sequence, head) not flagged:
+// dq~ = dq exp(r - b) and dk~ = dk exp(b - r) in fp32; a second kernel
+// recomputes b and r, turns them into dq and dk (token dtype) and forms the
+// gate's gradient, for every (sequence, head) not flagged:
 //     dg_w = sum over t at or after w (processing order) of q_t dq_t - k_t dk_t
 //            + sum_e F dF,
 // each term as q~ dq~ - k~ dk~ in fp32 (the bf16 operands and their own
-// gradients), summed within the chunk there and completed by gla_dg_finish
-// with the later chunks' totals.
+// gradients): gla_undo_kernel walks each sequence's chunks against the
+// processing order, carrying the later chunks' sum.
 
 #include <cmath>
 #include <cstdint>
@@ -72,9 +71,7 @@ template <> struct Pair<__nv_bfloat16> {
 // combined through shared memory.  The factors exp(b - r), exp(r - b) use the
 // fast exponential: they are rounded to bf16 with their operands anyway.
 constexpr int PG = 4, PT = PC / PG;   // token groups per chunk, tokens per group
-// UNDO: instead of writing the operands, rescale dq~, dk~ (fp32, dense) into
-// dq, dk (token dtype, the strides of q and k).
-template <typename T, bool UNDO>
+template <typename T>
 __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
 {
     const int pc = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
@@ -101,9 +98,8 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
     const int64_t ts = a.reverse ? -1 : 1;
 
     // The operands' q, k rows into L2 while the gates are summed: the lane
-    // that starts each 128-byte line of a warp's channels asks for it.  (The
-    // rescaling mode reads four tensors; prefetching them there was slower.)
-    if (!UNDO) {
+    // that starts each 128-byte line of a warp's channels asks for it.
+    {
         const int esz = (int)sizeof(T);
         if ((c * esz) % 128 == 0) {
             const int64_t qo = row * a.sb + (int64_t)h * a.sh + c;
@@ -170,101 +166,6 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
                                  fmaxf(0.5f * (LO.y + HI.y), -a.lim));
     const bool okx = HI.x - r.x <= a.lim && r.x - LO.x <= a.lim && r.x <= a.lim;
     const bool oky = HI.y - r.y <= a.lim && r.y - LO.y <= a.lim && r.y <= a.lim;
-    if (UNDO) {
-        if (a.flags[(int64_t)n * a.H + h])
-            return;   // computed token by token
-        const int64_t qo = row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
-        T *dqp = static_cast<T *>(a.dq) + qo;
-        T *dkp = static_cast<T *>(a.dk) + qo;
-        // dq~, dk~ (fp32) and the operands q~, k~ (bf16), all dense
-        const int64_t fo = ((int64_t)row * a.T * a.H + h) * a.D + c + tb * (int64_t)a.H * a.D;
-        const float *dqf = a.dqf + fo, *dkf = a.dkf + fo;
-        const __nv_bfloat16 *xq = static_cast<const __nv_bfloat16 *>(a.xq) + fo;
-        const __nv_bfloat16 *yk = static_cast<const __nv_bfloat16 *>(a.yk) + fo;
-        float *dgp = a.dg + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
-        const int64_t step = ts * a.st, fstep = ts * (int64_t)a.H * a.D, gstep = ts * a.gst;
-        const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
-        // dq, dk, and dg's terms into b[], which the factors no longer need.
-        // A term is q dq - k dk = q~ dq~ - k~ dk~; it is taken from the
-        // rounded operands the sweeps multiplied and their own (fp32)
-        // gradients, which makes dg the exact gradient of what the sweeps
-        // computed.  With q, k instead, each term would carry the operands'
-        // rounding (about 2^-9 of it), a random walk over the T terms.
-        float2 gt = make_float2(0.f, 0.f);   // this group's sum of terms
-        constexpr int PB = 4;
-#pragma unroll
-        for (int j0 = 0; j0 < PT; j0 += PB) {
-            float2 dqv[PB], dkv[PB], qv[PB], kv[PB];
-#pragma unroll
-            for (int jj = 0; jj < PB; ++jj) {
-                const int j = j0 + jj;
-                const int64_t jl = j < np ? j : (np > 0 ? np - 1 : 0);
-                dqv[jj] = Pair<float>::load(dqf + jl * fstep);
-                dkv[jj] = Pair<float>::load(dkf + jl * fstep);
-                qv[jj] = Pair<__nv_bfloat16>::load(xq + jl * fstep);
-                kv[jj] = Pair<__nv_bfloat16>::load(yk + jl * fstep);
-            }
-#pragma unroll
-            for (int jj = 0; jj < PB; ++jj) {
-                const int j = j0 + jj;
-                float2 tm = make_float2(0.f, 0.f);
-                if (j < np) {
-                    const float ex = b[j].x + sh0.x, ey = b[j].y + sh0.y;   // b - r
-                    const float2 dq2 = make_float2(dqv[jj].x * __expf(ex), dqv[jj].y * __expf(ey));
-                    const float2 dk2 =
-                        make_float2(dkv[jj].x * __expf(-ex), dkv[jj].y * __expf(-ey));
-                    Pair<T>::store(dqp + j * step, dq2);
-                    Pair<T>::store(dkp + j * step, dk2);
-                    tm = make_float2(qv[jj].x * dqv[jj].x - kv[jj].x * dkv[jj].x,
-                                     qv[jj].y * dqv[jj].y - kv[jj].y * dkv[jj].y);
-                }
-                b[j] = tm;
-                gt.x += tm.x;
-                gt.y += tm.y;
-            }
-        }
-        // dg within the chunk: the sum of the terms at or after each token in
-        // processing order; the later groups' totals come through shared
-        // memory, the later chunks' (and the final state's) from gla_dg_finish
-        __shared__ float2 gts[PG][64];
-        gts[grp][cp] = gt;
-        __syncthreads();
-        float2 acc = make_float2(0.f, 0.f), tot = acc;
-#pragma unroll
-        for (int k = 0; k < PG; ++k) {
-            const float2 x = gts[k][cp];
-            if (k > grp) {
-                acc.x += x.x;
-                acc.y += x.y;
-            }
-            tot.x += x.x;
-            tot.y += x.y;
-        }
-#pragma unroll
-        for (int j = PT - 1; j >= 0; --j) {
-            acc.x += b[j].x;
-            acc.y += b[j].y;
-            if (j < np)
-                *reinterpret_cast<float2 *>(dgp + j * gstep) = acc;
-        }
-        const int64_t hv = (int64_t)n * a.H + h;
-        if (grp == 0)   // the chunk's total per channel
-            *reinterpret_cast<float2 *>(a.er + (hv * a.ncmax + pc) * a.D + c) = tot;
-        if (grp == 1 && pc == 0) {
-            // sum_e F[c][e] dF[c][e] (F stored transposed), once per (sequence, head)
-            float2 f = make_float2(0.f, 0.f);
-            if (a.dF) {
-                const float *Ft = a.Ft + hv * a.D * a.E, *dF = a.dF + hv * a.D * a.E;
-                for (int e = 0; e < a.E; ++e) {
-                    const float2 fe = *reinterpret_cast<const float2 *>(Ft + (int64_t)e * a.D + c);
-                    f.x += fe.x * dF[(int64_t)c * a.E + e];
-                    f.y += fe.y * dF[(int64_t)(c + 1) * a.E + e];
-                }
-            }
-            *reinterpret_cast<float2 *>(a.u + hv * a.D + c) = f;
-        }
-        return;
-    }
     if (grp == 0) {
         if (!(okx && oky))
             atomicOr(a.flags + (int64_t)n * a.H + h, 1);
@@ -314,13 +215,22 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
     }
 }
 
-// The rest of dg for a chunk run in the chunked form: the totals of the
-// chunks after it in processing order (a.er, per channel) and the final
-// state's term (a.u), added to every token of the chunk.
-__global__ void __launch_bounds__(PG * 64) gla_dg_finish(GlaPrepArgs a)
+// dq~, dk~ -> dq, dk and the gate's gradient, one CTA per (group of 16
+// channels, head, sequence) walking the sequence's chunks against the
+// processing order, so that the sum of the terms of every later chunk (and
+// the final state's term) is carried in registers and dg is written once.
+// Thread (channel pair cp, token group grp) takes processing indices
+// 8 grp .. 8 grp + 7 of each chunk.  b and r are recomputed from the gates
+// as the pre-pass formed them (the same definitions; the sums grouped
+// differently, so they may differ in the last bits: dq and dk take their
+// factor exp(b - r) from them, dg does not).
+constexpr int UG = 16, UT = PC / UG, UCP = 8;   // token groups, tokens per group, channel pairs
+template <typename T>
+__global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
 {
-    const int pc = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-    const int cp = threadIdx.x & 63, grp = threadIdx.x >> 6, c = 2 * cp;
+    const int cg = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int cp = threadIdx.x % UCP, grp = threadIdx.x / UCP;
+    const int c = 2 * (UCP * cg + cp);
     int64_t row, bos, len;
     if (a.cu) {
         row = 0;
@@ -332,23 +242,138 @@ __global__ void __launch_bounds__(PG * 64) gla_dg_finish(GlaPrepArgs a)
         len = a.T;
     }
     const int64_t hv = (int64_t)n * a.H + h;
-    const int64_t t0 = (int64_t)pc * PC;
-    if (t0 >= len || a.flags[hv])
-        return;
+    if (a.flags[hv] || c >= a.D)
+        return;   // computed token by token
+    const bool rev = a.reverse != 0;
+    const float gh = a.g_gamma[h];
     const int nc = (int)((len + PC - 1) / PC);
-    float2 add = *reinterpret_cast<const float2 *>(a.u + hv * a.D + c);
-    for (int p = a.reverse ? 0 : pc + 1; p < (a.reverse ? pc : nc); ++p) {
-        const float2 x = *reinterpret_cast<const float2 *>(a.er + (hv * a.ncmax + p) * a.D + c);
-        add.x += x.x;
-        add.y += x.y;
+    __shared__ float2 s_tot[UG][UCP], s_lo[UG][UCP], s_hi[UG][UCP], s_tm[UG][UCP];
+    __shared__ float2 s_fdf[UCP];
+    // the final state's term, sum_e F[c][e] dF[c][e] (F stored transposed)
+    if (grp == 0) {
+        float2 f = make_float2(0.f, 0.f);
+        if (a.dF) {
+            const float *Ft = a.Ft + hv * a.D * a.E, *dF = a.dF + hv * a.D * a.E;
+            for (int e = 0; e < a.E; ++e) {
+                const float2 fe = *reinterpret_cast<const float2 *>(Ft + (int64_t)e * a.D + c);
+                f.x += fe.x * dF[(int64_t)c * a.E + e];
+                f.y += fe.y * dF[(int64_t)(c + 1) * a.E + e];
+            }
+        }
+        s_fdf[cp] = f;
     }
-    const int Lc = (int)(len - t0 < PC ? len - t0 : PC);
-    float *dgp = a.dg + row * a.gsb + (int64_t)h * a.gsh + c + (bos + t0) * a.gst;
-#pragma unroll 4
-    for (int i = grp; i < Lc; i += PG) {
-        float2 *p = reinterpret_cast<float2 *>(dgp + i * a.gst);
-        const float2 x = *p;
-        *p = make_float2(x.x + add.x, x.y + add.y);
+    __syncthreads();
+    float2 carry = s_fdf[cp];   // the terms after the current chunk, plus F dF
+    const int64_t dst = (int64_t)a.H * a.D;   // token stride of the dense tensors
+    for (int k = 0; k < nc; ++k) {
+        // chunks cut from the sequence's start; visited against the
+        // processing order (forward: last chunk first)
+        const int pc = rev ? k : nc - 1 - k;
+        const int64_t t0 = (int64_t)pc * PC;
+        const int Lc = (int)(len - t0 < PC ? len - t0 : PC);
+        const int p0 = UT * grp;
+        const int np = Lc - p0 < 0 ? 0 : (Lc - p0 < UT ? Lc - p0 : UT);
+        // token of processing index p0 + j: tb + j ts
+        const int64_t tb = bos + t0 + (np == 0 ? 0 : (rev ? Lc - 1 - p0 : p0));
+        const int64_t ts = rev ? -1 : 1;
+        const float *gp = a.g + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
+        const int64_t qo = row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
+        const int64_t fo = ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst;
+        float2 b[UT], dqv[UT], dkv[UT], qv[UT], kv[UT];
+#pragma unroll
+        for (int j = 0; j < UT; ++j) {
+            const int jl = j < np ? j : (np > 0 ? np - 1 : 0);
+            const float2 x = *reinterpret_cast<const float2 *>(gp + jl * ts * a.gst);
+            b[j] = j < np ? make_float2(gh + x.x, gh + x.y) : make_float2(0.f, 0.f);
+            dqv[j] = *reinterpret_cast<const float2 *>(a.dqf + fo + jl * ts * dst);
+            dkv[j] = *reinterpret_cast<const float2 *>(a.dkf + fo + jl * ts * dst);
+            qv[j] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(
+                static_cast<const __nv_bfloat16 *>(a.xq) + fo + jl * ts * dst));
+            kv[j] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(
+                static_cast<const __nv_bfloat16 *>(a.yk) + fo + jl * ts * dst));
+        }
+        // running sums of the log-decays from the chunk's first processed token
+        float2 lo = make_float2(INFINITY, INFINITY), hi = make_float2(-INFINITY, -INFINITY);
+#pragma unroll
+        for (int j = 0; j < UT; ++j) {
+            if (j > 0) {
+                b[j].x += b[j - 1].x;
+                b[j].y += b[j - 1].y;
+            }
+            if (j < np) {
+                lo = make_float2(fminf(lo.x, b[j].x), fminf(lo.y, b[j].y));
+                hi = make_float2(fmaxf(hi.x, b[j].x), fmaxf(hi.y, b[j].y));
+            }
+        }
+        s_tot[grp][cp] = b[UT - 1];
+        __syncthreads();
+        float2 off = make_float2(0.f, 0.f);   // the sums entering this group
+#pragma unroll
+        for (int q = 0; q < UG; ++q)
+            if (q < grp) {
+                off.x += s_tot[q][cp].x;
+                off.y += s_tot[q][cp].y;
+            }
+        s_lo[grp][cp] = make_float2(lo.x + off.x, lo.y + off.y);
+        s_hi[grp][cp] = make_float2(hi.x + off.x, hi.y + off.y);
+        __syncthreads();
+        float2 LO = s_lo[0][cp], HI = s_hi[0][cp];
+#pragma unroll
+        for (int q = 1; q < UG; ++q) {
+            LO = make_float2(fminf(LO.x, s_lo[q][cp].x), fminf(LO.y, s_lo[q][cp].y));
+            HI = make_float2(fmaxf(HI.x, s_hi[q][cp].x), fmaxf(HI.y, s_hi[q][cp].y));
+        }
+        const float2 r = make_float2(fmaxf(0.5f * (LO.x + HI.x), -a.lim),
+                                     fmaxf(0.5f * (LO.y + HI.y), -a.lim));
+        const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
+        // dq, dk, and the terms q~ dq~ - k~ dk~ (the rounded operands and
+        // their own gradients) into b[]
+        T *dqp = static_cast<T *>(a.dq) + qo;
+        T *dkp = static_cast<T *>(a.dk) + qo;
+        float2 gt = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < UT; ++j) {
+            float2 tm = make_float2(0.f, 0.f);
+            if (j < np) {
+                const float ex = b[j].x + sh0.x, ey = b[j].y + sh0.y;   // b - r
+                Pair<T>::store(dqp + j * ts * a.st,
+                               make_float2(dqv[j].x * __expf(ex), dqv[j].y * __expf(ey)));
+                Pair<T>::store(dkp + j * ts * a.st,
+                               make_float2(dkv[j].x * __expf(-ex), dkv[j].y * __expf(-ey)));
+                tm = make_float2(qv[j].x * dqv[j].x - kv[j].x * dkv[j].x,
+                                 qv[j].y * dqv[j].y - kv[j].y * dkv[j].y);
+            }
+            b[j] = tm;
+            gt.x += tm.x;
+            gt.y += tm.y;
+        }
+        __syncthreads();   // every thread is done with s_tot, s_lo, s_hi
+        s_tm[grp][cp] = gt;
+        __syncthreads();
+        // dg = carry + the later groups' totals + this group's terms at or
+        // after each token
+        float2 acc = carry, tot = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < UG; ++q) {
+            const float2 x = s_tm[q][cp];
+            if (q > grp) {
+                acc.x += x.x;
+                acc.y += x.y;
+            }
+            tot.x += x.x;
+            tot.y += x.y;
+        }
+        float *dgp = a.dg + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
+#pragma unroll
+        for (int j = UT - 1; j >= 0; --j) {
+            acc.x += b[j].x;
+            acc.y += b[j].y;
+            if (j < np)
+                *reinterpret_cast<float2 *>(dgp + j * ts * a.gst) = acc;
+        }
+        carry.x += tot.x;
+        carry.y += tot.y;
+        __syncthreads();   // s_tm read by all before the next chunk writes it
     }
 }
 
@@ -363,9 +388,9 @@ cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s)
     dim3 grid((unsigned)a.ncmax, (unsigned)a.H, (unsigned)a.N);
     const int threads = PG * 64;
     if (a.bf16)
-        gla_prep_kernel<__nv_bfloat16, false><<<grid, threads, 0, s>>>(a);
+        gla_prep_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(a);
     else
-        gla_prep_kernel<float, false><<<grid, threads, 0, s>>>(a);
+        gla_prep_kernel<float><<<grid, threads, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }
@@ -374,18 +399,13 @@ cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s)
 {
     if (a.N == 0 || a.H == 0 || a.ncmax == 0)
         return cudaSuccess;
-    if (a.D != 128 || a.N > 65535 || a.H > 65535 || a.ncmax > 0x7fffffff)
+    if (a.D != 128 || a.N > 65535 || a.H > 65535)
         return cudaErrorNotSupported;
-    dim3 grid((unsigned)a.ncmax, (unsigned)a.H, (unsigned)a.N);
+    dim3 grid((unsigned)(a.D / (2 * UCP)), (unsigned)a.H, (unsigned)a.N);
     if (a.bf16)
-        gla_prep_kernel<__nv_bfloat16, true><<<grid, PG * 64, 0, s>>>(a);
+        gla_undo_kernel<__nv_bfloat16><<<grid, UG * UCP, 0, s>>>(a);
     else
-        gla_prep_kernel<float, true><<<grid, PG * 64, 0, s>>>(a);
-    note_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return e;
-    gla_dg_finish<<<grid, PG * 64, 0, s>>>(a);
+        gla_undo_kernel<float><<<grid, UG * UCP, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }

@@ -112,7 +112,8 @@ struct GlaPrepArgs {
 cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s);
 // dq~ -> dq, dk~ -> dk (fp32 in, token dtype out), and the gate's gradient
 // dg from the rounded operands q~, k~ and their own gradients dq~, dk~, for
-// the (sequence, head) pairs not flagged (a.er and a.u are reused as scratch).
+// the (sequence, head) pairs not flagged: one pass over each sequence against
+// the processing order, the later chunks' terms carried in registers.
 cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s);
 // A tensor-core sweep of the gated form on rescaled operands (la_gla_prep.cu)
 // with tile roles X, Y, Z given (bf16, D = 128 X and Y width): forward-type or
