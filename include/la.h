@@ -369,6 +369,14 @@ la_status la_get_device_error(void *stream);
  * The switch resets itself after that launch and is off by default. */
 la_status la_debug_withhold_next_handoff(int32_t on);
 
+/* Diagnostic, for testing the sequence split's planning without a device:
+ * the number of segments la_fwd / la_bwd would cut these sizes into on a GPU
+ * with `sms` multiprocessors under the current la_set_sequence_split
+ * settings; 0 when they would run unsplit, -1 for invalid sizes.
+ * cu_seqlens_host as la_workspace_size_for.  Pure host function. */
+int32_t la_debug_split_segments(const la_dims *dims, int32_t dtype,
+                                const int32_t *cu_seqlens_host, int32_t sms);
+
 /* How this copy of the library was built: LA_BUILD_BOUNDS_CHECKED set when
  * the tensor-core kernels' index checks are compiled in (build.py --checked,
  * liblagb300_checked.so; see la_get_device_error).  Pure host function. */

@@ -85,6 +85,7 @@ PROTOTYPES = {
                           _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _sz, _vp]),
     "la_gla_workspace_size": (_sz, [_dims_p, _i32, _vp, _i32]),
     "la_debug_withhold_next_handoff": (_i32, [_i32]),
+    "la_debug_split_segments": (_i32, [_dims_p, _i32, _vp, _i32]),
     "la_fwd_noalloc": (_i32, [_dims_p, _i32, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _vp,
                               _vp, _vp, _vp]),
     "la_get_device_error": (_i32, [_vp]),

@@ -875,6 +875,18 @@ la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens)
     return LA_OK;
 }
 
+int32_t la_debug_split_segments(const la_dims *dims, int32_t dtype,
+                                const int32_t *cu_seqlens_host, int32_t sms)
+{
+    Problem P;
+    std::string keep = g_msg;
+    la_status st = check_dims(dims, dtype, cu_seqlens_host, cu_seqlens_host, nullptr, &P);
+    g_msg = keep;
+    if (st != LA_OK || sms < 1)
+        return -1;
+    return plan_split(P, dims, sms).NS;
+}
+
 la_status la_debug_withhold_next_handoff(int32_t on)
 {
     g_withhold = on ? 1 : 0;

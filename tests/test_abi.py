@@ -177,6 +177,34 @@ def test_workspace_size(lib):
     assert lib.la_workspace_size(65) == 512
 
 
+def test_split_planning_by_head_width(lib):
+    # la_debug_split_segments plans for a given SM count without a device.
+    # Automatic segments: >= 256 tokens at d <= 64, >= 4 segments of >= 1024
+    # tokens at d <= 128, none above; only when the pairs fill at most half
+    # of the SMs.
+    seg = lambda d, sms=152: lib.la_debug_split_segments(ctypes.byref(d), 0, None, sms)
+    assert lib.la_set_sequence_split(1, 0) == N.LA_OK
+    assert seg(_dims(B=2, T=2048, H=8, D=64, E=64)) == 2 * 8        # 256-token segments
+    assert seg(_dims(B=2, T=4096, H=16, D=128, E=128)) == 2 * 4     # 4 x 1024
+    assert seg(_dims(B=2, T=2048, H=8, D=128, E=128)) == 0          # only 2 of 1024
+    assert seg(_dims(B=2, T=2048, H=12, D=192, E=192)) == 0         # wide heads: never
+    assert seg(_dims(B=1, T=262144, H=8, D=128, E=128)) == 19       # 152 / 8 pairs
+    assert seg(_dims(B=4, T=32768, H=32, D=128, E=128)) == 0        # 128 pairs > 76
+    assert seg(_dims(B=2, T=4096, H=16, D=128, E=128), sms=0) == -1
+    # an explicit minimum applies at any width, from 2 segments
+    assert lib.la_set_sequence_split(1, 256) == N.LA_OK
+    try:
+        assert seg(_dims(B=2, T=2048, H=8, D=128, E=128)) == 2 * 8
+        d = _dims(B=1, T=5817, H=2, D=128, E=128, N_=5)
+        _, cp = _cu([0, 3000, 3017, 3017, 5117, 5817])
+        # R = min(152 / 10, 3000 / 256) = 11 -> 384-token segments: 8 + 1 + 0 + 6 + 2
+        assert lib.la_debug_split_segments(ctypes.byref(d), 0, cp, 152) == 17
+        assert lib.la_set_sequence_split(0, 0) == N.LA_OK
+        assert seg(_dims(B=1, T=262144, H=8, D=128, E=128)) == 0
+    finally:
+        assert lib.la_set_sequence_split(1, 0) == N.LA_OK
+
+
 def test_workspace_size_for_and_split_control(lib):
     # no device here: the split cannot be planned, only the packed schedule is sized
     d = _dims(B=1, T=16, N_=3)
