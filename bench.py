@@ -774,14 +774,14 @@ def gla_bench(la, torch, dev, stream, peak):
 
 
 def source_sha():
-    """Hash of the sources the tensor-core kernels of the step are built from
-    (the sweep kernel and the fused dk/dv kernel, whose ncu traffic
-    profiles/traffic_tc_sweep_kernel.json records)."""
+    """Hash of the device code the tensor-core kernels of the step are built
+    from (the sweep kernel and the fused dk/dv kernel, whose ncu traffic
+    profiles/traffic_tc_sweep_kernel.json records; the shared declarations of
+    la_internal.h, which every kernel file includes, are left out)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_head_gb300", "csrc")
-    for f in ("la_internal.h", "la_sm100.cuh", "la_tc_common.cuh", "la_tc_sweep.cu",
-              "la_tc_dkdv.cu"):
+    for f in ("la_sm100.cuh", "la_tc_common.cuh", "la_tc_sweep.cu", "la_tc_dkdv.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
