@@ -544,6 +544,7 @@ def packed_work(T, H, d, e, n_seqs, token_bytes=2):
 def configs_bench(la, torch, dev, stream, hbm, tfl):
     """The other workload shapes, fwd and bwd timed separately (median of 20 queued
     calls after 5 warm-up calls):
+      * b1 h2 n256 d=e=32 fp32, forward only (L2 flushed before each call);
       * b2 h8 n2048 d=e=64 and b2 h12 n2048 d=e=192 (bf16): their token tensors fit
         in L2, so each call follows a 512 MB L2 flush (`*_ms`); back to back without
         one in `*_ms_unflushed`;
@@ -575,6 +576,22 @@ def configs_bench(la, torch, dev, stream, hbm, tfl):
             "bwd_ms_unflushed": _timed_calls(torch, stream, bwd),
             "l2": "flushed before each call (512 MB write)"}
         del q, k, v, do
+    # config 1: b1 h2 n256 d=e=32 fp32, forward only (the CUDA-core chunked
+    # kernels; fp32 tokens, 4-byte method bytes)
+    w = W.tiny_fp32()
+    gen = torch.Generator(device=dev).manual_seed(31)
+    q, k, v = (torch.randn((w.B, w.T, w.H, w.d), generator=gen, device=dev) for _ in range(3))
+    g = w.g_gamma.to(dev)
+    fwd = lambda: la.la_fwd(q, k, v, g, w.scale)
+    f_ms = _timed_calls(torch, stream, fwd, flush)
+    rf = method_roofline(method_work(w.B, w.T, w.H, w.d, w.e, token_bytes=4), f_ms, f_ms, hbm,
+                         tfl)
+    out[w.name] = {"kernel_family": la.kernel_family(w.B, w.T, w.H, w.d, w.e, dtype=torch.float32),
+                   "fwd_ms": f_ms, "tokens_per_s": w.B * w.T / (f_ms * 1e-3),
+                   "roofline_frac_fwd": rf["fwd"]["frac"],
+                   "fwd_ms_unflushed": _timed_calls(torch, stream, fwd),
+                   "l2": "flushed before each call (512 MB write)"}
+    del q, k, v
     w = W.varlen_bf16(seed=0)
     gen = torch.Generator(device=dev).manual_seed(29)
     q, k = (torch.randn((1, w.T, w.H, w.d), generator=gen, device=dev).bfloat16()

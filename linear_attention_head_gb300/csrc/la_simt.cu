@@ -11,7 +11,11 @@
 // One CTA owns one (sequence, head, value-tile); the state tile (D x SET fp32)
 // stays in shared memory for the whole sequence.  The score block is
 // recomputed by each value tile (cheap next to the state work for these
-// fallback sizes).
+// fallback sizes).  The chunk's three loops are register-blocked: thread t
+// takes row t / 8 of a 32-row block and the 8 columns t % 8 + 8 m (m < 8) of
+// the 64-column value tile (scores: 4 adjacent keys), so each shared-memory
+// row value it loads feeds 4 or 8 independent accumulators; one accumulator
+// per thread left every loop waiting on the previous load and FMA.
 
 #include <cuda_bf16.h>
 #include "la_internal.h"
@@ -82,27 +86,49 @@ __device__ __forceinline__ int chunk_len(int64_t len, int64_t t0)
 
 // Loads the chunk rows [t0, t0+Lc) of q, k (all D) and of the third tensor's
 // value tile [e0, e0+ew) into shared memory as fp32; rows >= Lc are zeroed.
+// Each thread issues its loads in batches of 8 before storing any, so that a
+// chunk waits for a few global-memory round trips instead of one per element.
 template <typename T>
 __device__ void load_chunk(const SweepArgs &a, const Seq &sq, int h, int64_t t0, int Lc,
                            int e0, int ew, float *Qs, float *Ks, float *Vs, int DP)
 {
     const int D = a.D;
-    for (int idx = threadIdx.x; idx < SC * D; idx += SNT) {
-        const int i = idx / D, c = idx % D;
-        float qv = 0.f, kv = 0.f;
-        if (i < Lc) {
-            qv = ldf(tok<T>(a.q, sq.row, sq.bos + t0 + i, h) + c);
-            kv = ldf(tok<T>(a.k, sq.row, sq.bos + t0 + i, h) + c);
+    constexpr int LB = 8;
+    for (int base = threadIdx.x; base < SC * D; base += LB * SNT) {
+        float qv[LB], kv[LB];
+#pragma unroll
+        for (int u = 0; u < LB; ++u) {
+            const int idx = base + u * SNT, i = idx / D, c = idx % D;
+            qv[u] = kv[u] = 0.f;
+            if (idx < SC * D && i < Lc) {
+                qv[u] = ldf(tok<T>(a.q, sq.row, sq.bos + t0 + i, h) + c);
+                kv[u] = ldf(tok<T>(a.k, sq.row, sq.bos + t0 + i, h) + c);
+            }
         }
-        Qs[i * DP + c] = qv;
-        Ks[i * DP + c] = kv;
+#pragma unroll
+        for (int u = 0; u < LB; ++u) {
+            const int idx = base + u * SNT, i = idx / D, c = idx % D;
+            if (idx < SC * D) {
+                Qs[i * DP + c] = qv[u];
+                Ks[i * DP + c] = kv[u];
+            }
+        }
     }
-    for (int idx = threadIdx.x; idx < SC * SET; idx += SNT) {
-        const int i = idx / SET, c = idx % SET;
-        float vv = 0.f;
-        if (i < Lc && c < ew)
-            vv = ldf(tok<T>(a.v, sq.row, sq.bos + t0 + i, h) + e0 + c);
-        Vs[i * (SET + 1) + c] = vv;
+    for (int base = threadIdx.x; base < SC * SET; base += LB * SNT) {
+        float vv[LB];
+#pragma unroll
+        for (int u = 0; u < LB; ++u) {
+            const int idx = base + u * SNT, i = idx / SET, c = idx % SET;
+            vv[u] = 0.f;
+            if (idx < SC * SET && i < Lc && c < ew)
+                vv[u] = ldf(tok<T>(a.v, sq.row, sq.bos + t0 + i, h) + e0 + c);
+        }
+#pragma unroll
+        for (int u = 0; u < LB; ++u) {
+            const int idx = base + u * SNT, i = idx / SET, c = idx % SET;
+            if (idx < SC * SET)
+                Vs[i * (SET + 1) + c] = vv[u];
+        }
     }
 }
 
@@ -141,44 +167,77 @@ __global__ void __launch_bounds__(SNT) simt_forward_kernel(SweepArgs a)
         __syncthreads();
         load_chunk<T>(a, sq, h, t0, Lc, e0, ew, Qs, Ks, Vs, DP);
         __syncthreads();
-        // decay-masked scores P[i][j] = s (q_i . k_j) gamma^(p(i)-p(j)), p(j) <= p(i)
-        for (int idx = threadIdx.x; idx < SC * SC; idx += SNT) {
-            const int i = idx / SC, j = idx % SC;
-            const int pi = a.reverse ? Lc - 1 - i : i, pj = a.reverse ? Lc - 1 - j : j;
-            float val = 0.f;
-            if (i < Lc && j < Lc && pj <= pi) {
-                float acc = 0.f;
-                for (int c2 = 0; c2 < D; ++c2)
-                    acc = fmaf(Qs[i * DP + c2], Ks[j * DP + c2], acc);
-                val = a.scale * acc * pw[pi - pj];
+        // decay-masked scores P[i][j] = s (q_i . k_j) gamma^(p(i)-p(j)), p(j) <= p(i):
+        // row i = t / 8, keys 4 (t % 8) .. + 3
+        {
+            const int i = threadIdx.x >> 3, j0 = 4 * (threadIdx.x & 7);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c2 = 0; c2 < D; ++c2) {
+                const float qv = Qs[i * DP + c2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    acc[u] = fmaf(qv, Ks[(j0 + u) * DP + c2], acc[u]);
             }
-            Ps[i * (SC + 1) + j] = val;
-        }
-        __syncthreads();
-        // out_i = sum_j P[i][j] v_j + s gamma^(p(i)+1) q_i^T S
-        for (int idx = threadIdx.x; idx < SC * SET; idx += SNT) {
-            const int i = idx / SET, b = idx % SET;
-            if (i >= Lc || b >= ew)
-                continue;
-            float intra = 0.f, inter = 0.f;
-            for (int j = 0; j < SC; ++j)
-                intra = fmaf(Ps[i * (SC + 1) + j], Vs[j * (SET + 1) + b], intra);
-            for (int r = 0; r < D; ++r)
-                inter = fmaf(Qs[i * DP + r], Ss[r * SET + b], inter);
             const int pi = a.reverse ? Lc - 1 - i : i;
-            stf(tok<T>(a.out, sq.row, sq.bos + t0 + i, h) + e0 + b,
-                intra + a.scale * pw[pi + 1] * inter);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u, pj = a.reverse ? Lc - 1 - j : j;
+                Ps[i * (SC + 1) + j] =
+                    i < Lc && j < Lc && pj <= pi ? a.scale * acc[u] * pw[pi - pj] : 0.f;
+            }
         }
         __syncthreads();
-        // S = gamma^Lc S + sum_j gamma^(Lc-1-p(j)) k_j v_j^T
-        for (int idx = threadIdx.x; idx < D * SET; idx += SNT) {
-            const int r = idx / SET, b = idx % SET;
-            float acc = 0.f;
+        // out_i = sum_j P[i][j] v_j + s gamma^(p(i)+1) q_i^T S: row i = t / 8,
+        // columns t % 8 + 8 m
+        {
+            const int i = threadIdx.x >> 3, b0 = threadIdx.x & 7;
+            float intra[8], inter[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                intra[m] = inter[m] = 0.f;
+            for (int j = 0; j < SC; ++j) {
+                const float pv = Ps[i * (SC + 1) + j];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    intra[m] = fmaf(pv, Vs[j * (SET + 1) + b0 + 8 * m], intra[m]);
+            }
+            for (int r = 0; r < D; ++r) {
+                const float qv = Qs[i * DP + r];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    inter[m] = fmaf(qv, Ss[r * SET + b0 + 8 * m], inter[m]);
+            }
+            if (i < Lc) {
+                const int pi = a.reverse ? Lc - 1 - i : i;
+                const float f = a.scale * pw[pi + 1];
+                T *orow = tok<T>(a.out, sq.row, sq.bos + t0 + i, h) + e0;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    if (b0 + 8 * m < ew)
+                        stf(orow + b0 + 8 * m, intra[m] + f * inter[m]);
+            }
+        }
+        __syncthreads();
+        // S = gamma^Lc S + sum_j gamma^(Lc-1-p(j)) k_j v_j^T: rows t / 8 + 32 rr,
+        // columns t % 8 + 8 m
+        for (int r = threadIdx.x >> 3; r < D; r += SNT / 8) {
+            const int b0 = threadIdx.x & 7;
+            float acc[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                acc[m] = 0.f;
             for (int j = 0; j < Lc; ++j) {
                 const int pj = a.reverse ? Lc - 1 - j : j;
-                acc = fmaf(pw[Lc - 1 - pj] * Ks[j * DP + r], Vs[j * (SET + 1) + b], acc);
+                const float kv = pw[Lc - 1 - pj] * Ks[j * DP + r];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    acc[m] = fmaf(kv, Vs[j * (SET + 1) + b0 + 8 * m], acc[m]);
             }
-            Ss[idx] = fmaf(pw[Lc], Ss[idx], acc);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float *sp = Ss + r * SET + b0 + 8 * m;
+                *sp = fmaf(pw[Lc], *sp, acc[m]);
+            }
         }
     }
     __syncthreads();
@@ -227,43 +286,77 @@ __global__ void __launch_bounds__(SNT) simt_backward_kernel(SweepArgs a)
         __syncthreads();
         load_chunk<T>(a, sq, h, t0, Lc, e0, ew, Qs, Ks, Ws, DP);
         __syncthreads();
-        for (int idx = threadIdx.x; idx < SC * SC; idx += SNT) {
-            const int j = idx / SC, i = idx % SC;
-            const int pi = a.reverse ? Lc - 1 - i : i, pj = a.reverse ? Lc - 1 - j : j;
-            float val = 0.f;
-            if (i < Lc && j < Lc && pj <= pi) {
-                float acc = 0.f;
-                for (int c2 = 0; c2 < D; ++c2)
-                    acc = fmaf(Qs[i * DP + c2], Ks[j * DP + c2], acc);
-                val = a.scale * acc * pw[pi - pj];
+        // Ps[j][i] = s (q_i . k_j) gamma^(p(i)-p(j)), p(j) <= p(i): key row
+        // j = t / 8, queries 4 (t % 8) .. + 3
+        {
+            const int j = threadIdx.x >> 3, i0 = 4 * (threadIdx.x & 7);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int c2 = 0; c2 < D; ++c2) {
+                const float kv = Ks[j * DP + c2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    acc[u] = fmaf(Qs[(i0 + u) * DP + c2], kv, acc[u]);
             }
-            Ps[j * (SC + 1) + i] = val;
-        }
-        __syncthreads();
-        // out_j = sum_i P[j][i] w_i + gamma^(Lc-1-p(j)) G^T k_j
-        for (int idx = threadIdx.x; idx < SC * SET; idx += SNT) {
-            const int j = idx / SET, b = idx % SET;
-            if (j >= Lc || b >= ew)
-                continue;
-            float intra = 0.f, inter = 0.f;
-            for (int i = 0; i < SC; ++i)
-                intra = fmaf(Ps[j * (SC + 1) + i], Ws[i * (SET + 1) + b], intra);
-            for (int r = 0; r < D; ++r)
-                inter = fmaf(Ks[j * DP + r], Gs[r * SET + b], inter);
             const int pj = a.reverse ? Lc - 1 - j : j;
-            stf(tok<T>(a.out, sq.row, sq.bos + t0 + j, h) + e0 + b,
-                intra + pw[Lc - 1 - pj] * inter);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u, pi = a.reverse ? Lc - 1 - i : i;
+                Ps[j * (SC + 1) + i] =
+                    i < Lc && j < Lc && pj <= pi ? a.scale * acc[u] * pw[pi - pj] : 0.f;
+            }
         }
         __syncthreads();
-        // G = gamma^Lc G + s sum_i gamma^(p(i)+1) q_i w_i^T
-        for (int idx = threadIdx.x; idx < D * SET; idx += SNT) {
-            const int r = idx / SET, b = idx % SET;
-            float acc = 0.f;
+        // out_j = sum_i P[j][i] w_i + gamma^(Lc-1-p(j)) G^T k_j: row j = t / 8,
+        // columns t % 8 + 8 m
+        {
+            const int j = threadIdx.x >> 3, b0 = threadIdx.x & 7;
+            float intra[8], inter[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                intra[m] = inter[m] = 0.f;
+            for (int i = 0; i < SC; ++i) {
+                const float pv = Ps[j * (SC + 1) + i];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    intra[m] = fmaf(pv, Ws[i * (SET + 1) + b0 + 8 * m], intra[m]);
+            }
+            for (int r = 0; r < D; ++r) {
+                const float kv = Ks[j * DP + r];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    inter[m] = fmaf(kv, Gs[r * SET + b0 + 8 * m], inter[m]);
+            }
+            if (j < Lc) {
+                const int pj = a.reverse ? Lc - 1 - j : j;
+                const float f = pw[Lc - 1 - pj];
+                T *orow = tok<T>(a.out, sq.row, sq.bos + t0 + j, h) + e0;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    if (b0 + 8 * m < ew)
+                        stf(orow + b0 + 8 * m, intra[m] + f * inter[m]);
+            }
+        }
+        __syncthreads();
+        // G = gamma^Lc G + s sum_i gamma^(p(i)+1) q_i w_i^T: rows t / 8 + 32 rr,
+        // columns t % 8 + 8 m
+        for (int r = threadIdx.x >> 3; r < D; r += SNT / 8) {
+            const int b0 = threadIdx.x & 7;
+            float acc[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+                acc[m] = 0.f;
             for (int i = 0; i < Lc; ++i) {
                 const int pi = a.reverse ? Lc - 1 - i : i;
-                acc = fmaf(pw[pi + 1] * Qs[i * DP + r], Ws[i * (SET + 1) + b], acc);
+                const float qv = pw[pi + 1] * Qs[i * DP + r];
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    acc[m] = fmaf(qv, Ws[i * (SET + 1) + b0 + 8 * m], acc[m]);
             }
-            Gs[idx] = fmaf(pw[Lc], Gs[idx], a.scale * acc);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float *gp = Gs + r * SET + b0 + 8 * m;
+                *gp = fmaf(pw[Lc], *gp, a.scale * acc[m]);
+            }
         }
     }
     __syncthreads();
