@@ -391,8 +391,10 @@ const char *la_strerror(int32_t status);
 const char *la_last_error(void);
 
 /* Which kernel family la_fwd would launch for these sizes and dtype, assuming
- * 16-byte aligned base pointers: 2 = token-by-token kernels (every sequence
- * at most 16 tokens long: decoding a few tokens against a carried state),
+ * 16-byte aligned base pointers: 2 = the short-call kernels (every sequence
+ * at most 16 tokens long: decoding a few tokens against a carried state;
+ * token by token, or for 5 to 16 tokens as one chunk -- on the tensor cores
+ * for bf16 with D = 128 and E a multiple of 16),
  * 1 = tensor-core (tcgen05) chunked kernels, 0 = CUDA-core chunked kernels,
  * -1 = invalid or unsupported.  The sequence length is dims->seq_len; with
  * cu_seqlens the longest packed sequence decides, which this function does
