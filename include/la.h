@@ -275,7 +275,11 @@ la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens);
  *   operands_written  host int32, or NULL: set to 1 when the call ran the
  *              chunked form, leaving its operands in the workspace (which
  *              la_gla_bwd can then reuse), else 0
- *   everything else as la_fwd; kv_heads must be 0 (or H).
+ *   everything else as la_fwd, grouped key/value heads included: k and v
+ *              with kv_heads heads (k_strides, kv_v_strides), query head h
+ *              reading key/value head h / (H / kv_heads); the gate, the
+ *              state and o are the query head's (ejkernel `recurrent`: key
+ *              and value with num_kv_heads heads, g with num_heads).
  * With the workspace, bf16 calls with D = 128, E in {64, 128} and sequences
  * longer than 16 tokens run the chunked form on the tensor cores: per chunk
  * of 128 tokens the gate's running sums b are split around a reference r
@@ -322,6 +326,10 @@ size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
  * for bf16, dq and dk in fp32) and other shapes run the token-by-token
  * kernels.  dg never takes bf16-rounded gradients: rounding each of its T
  * terms would add errors that grow with T while dg does not.
+ * Grouped key/value heads: dq and dg are per query head as without
+ * grouping; dk and dv are the sums over each group's query heads, formed
+ * from every query head's part (dk's in fp32, dv's in the token dtype, both
+ * in the workspace) in fp32 and written in the token dtype.
  *   fwd_workspace  the workspace of a la_gla_fwd call on the same q, k, g,
  *              g_gamma, reverse and cu_seqlens that reported operands_written
  *              = 1, untouched since; or NULL.  The backward then uses the
@@ -342,7 +350,10 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype,
 /* Workspace bytes of la_gla_bwd for these sizes (0 for invalid sizes): with
  * with_forward_operands = 0, enough to run the chunked form on its own where
  * it applies; nonzero, the part needed when the forward's operands are passed
- * as fwd_workspace.  cu_seqlens_host: host copy of cu_seqlens for packed
+ * as fwd_workspace.  That part: the final state, dg's block sums, dq and dk
+ * in fp32 ([rows][T][H][D] each; for bf16 tokens, and for fp32 tokens when
+ * kv_heads is set) and, with kv_heads < H, the query heads' parts of dv
+ * ([rows][T][H][E], token dtype).  cu_seqlens_host: host copy of cu_seqlens for packed
  * sequences, else NULL.  Pure host function. */
 size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype,
                              const int32_t *cu_seqlens_host, int32_t with_forward_operands);

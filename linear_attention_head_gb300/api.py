@@ -350,17 +350,18 @@ def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
             reverse: bool = False, cu_seqlens=None, chunked: bool = True,
             keep_operands: bool = False):
     """Gated forward (GLA): row a of the state decays by exp(g_gamma[h] + g_t[a]) at
-    token t.  q, k, g: [B,T,H,D]; v: [B,T,H,E].  Returns (o, final_state), and with
+    token t.  q, g: [B,T,H,D]; k: [B,T,H_kv,D], v: [B,T,H_kv,E] with H_kv dividing H
+    (query head h reads key/value head h // (H / H_kv); the gate and the state are
+    the query head's).  Returns (o, final_state), and with
     keep_operands=True (o, final_state, operands): operands is the workspace holding
     the chunked form's rescaled q, k when the call ran that form (else None), to be
     passed once to gla_bwd on the same inputs.  chunked=False withholds the
     workspace, so that every (sequence, head) runs token by token (otherwise the
     chunked tensor-core form runs where it applies)."""
     _check_tokens(q, k, v)
-    if k.shape[2] != q.shape[2]:
-        raise ValueError("the gated form needs keys and values with the queries' heads")
     q, k, v = _channel_contiguous((q, k, v))
-    q, k = _same_strides([q, k])
+    if k.shape[2] == q.shape[2]:
+        q, k = _same_strides([q, k])
     dev = q.device
     g = _gate(g, q)
     packed = _Packed(cu_seqlens, dev)
@@ -370,7 +371,9 @@ def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
     gg = _g(torch.zeros(H) if g_gamma is None else g_gamma, H, dev)
     scale = float(D ** -0.5 if scale is None else scale)
     init = _state(initial_state, (Nst, H, D, E), dev, "initial_state")
-    out = _like(v)
+    # o has the queries' heads; with H heads for keys and values too, v's strides
+    out = (_like(v) if k.shape[2] == H
+           else torch.empty(q.shape[:3] + v.shape[3:], dtype=v.dtype, device=dev))
     fin = torch.empty((Nst, H, D, E), device=dev, dtype=torch.float32)
     dims = _dims(q, k, v, out, packed)
     gs = _strides3(g)
@@ -392,7 +395,8 @@ def gla_fwd(q: Tensor, k: Tensor, v: Tensor, g: Tensor, g_gamma=None,
 def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_final_state=None,
             reverse=False, cu_seqlens=None, want_d_initial_state=True, operands=None,
             chunked: bool = True):
-    """Backward of gla_fwd: returns (dq, dk, dv, dg, d_initial_state).  operands: what
+    """Backward of gla_fwd: returns (dq, dk, dv, dg, d_initial_state); with grouped
+    key/value heads dk and dv are the sums over each group's query heads.  operands: what
     gla_fwd(..., keep_operands=True) returned for the same inputs, or None; it is
     consumed (used as scratch).  chunked=False (with operands None) gives only the
     token-by-token part of the workspace, so that every (sequence, head) runs token
@@ -402,8 +406,6 @@ def gla_bwd(q, k, v, do, g, g_gamma=None, scale=None, initial_state=None, d_fina
     q, k, v, do, dev, packed, gg, scale, init, dfin, Nst = _bwd_prep(
         q, k, v, do, torch.zeros(q.shape[2]) if g_gamma is None else g_gamma, scale,
         initial_state, d_final_state, cu_seqlens)
-    if k.shape[2] != q.shape[2]:
-        raise ValueError("the gated form needs keys and values with the queries' heads")
     g = _gate(g, q)
     dq, dk, dv = _like(q), _like(k), _like(v)
     dg = torch.empty_strided(g.shape, g.stride(), dtype=torch.float32, device=dev)

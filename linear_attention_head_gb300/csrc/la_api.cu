@@ -914,8 +914,7 @@ namespace {
 la_status gla_check(const Problem &P, const la_dims *d, const float *g, const int64_t *gs,
                     const float *g_gamma)
 {
-    if (d->kv_heads && d->kv_heads != d->heads)
-        return fail(LA_ERR_UNSUPPORTED, "the gated form takes kv_heads = 0 (or = heads)");
+    (void)d;
     if (!has_states(P))
         return LA_OK;
     la_status st;
@@ -986,24 +985,38 @@ GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype, bool bwd = false)
     return w;
 }
 
-// Workspace of la_gla_bwd: the final state transposed, the block sums and,
-// for bf16 tokens, dq and dk in fp32 (dense [rows][T][H][D]): the sweeps
-// write them there and the gate's gradient reads them unrounded before the
-// bf16 copies are written.
+// dq and dk of the gated backward go through fp32 workspace rows (dense
+// [rows][T][H][D], one row per query head) for bf16 tokens (the gate's
+// gradient reads them unrounded before the bf16 copies are written) and
+// whenever k has strides of its own (grouped key/value heads: the rows hold
+// each query head's part of dk until the group is summed).
+bool gla_f32_grads(const Problem &P, const la_dims *d, int32_t dtype)
+{
+    return dtype == LA_DTYPE_BF16 || P.G > 1 || P.k_st[0] != d->qk_strides[0] ||
+           P.k_st[1] != d->qk_strides[1] || P.k_st[2] != d->qk_strides[2];
+}
+
+// Workspace of la_gla_bwd: the final state transposed, the block sums, the
+// fp32 dq and dk rows (gla_f32_grads) and, with grouped key/value heads, each
+// query head's part of dv (dense [rows][T][H][E], token dtype).
 struct GlaBwdWs {
-    size_t bsum, dqf, dkf, total;
+    size_t bsum, dqf, dkf, cv, total;
 };
-GlaBwdWs gla_bwd_layout(const Problem &P, int32_t dtype)
+GlaBwdWs gla_bwd_layout(const Problem &P, const la_dims *d, int32_t dtype)
 {
     GlaBwdWs w{};
     const int64_t nblk = (gla_max_len(P) + la::DG_TB - 1) / la::DG_TB;
     const int64_t rows = P.packed ? 1 : P.B;
     const size_t tokf =
-        dtype == LA_DTYPE_BF16 ? round256((size_t)rows * P.T * P.H * P.D * 4) : 0;
+        gla_f32_grads(P, d, dtype) ? round256((size_t)rows * P.T * P.H * P.D * 4) : 0;
+    const size_t tokv =
+        P.G > 1 ? round256((size_t)rows * P.T * P.H * P.E * (dtype == LA_DTYPE_BF16 ? 2 : 4))
+                : 0;
     w.bsum = round256((size_t)P.N * P.H * P.D * P.E * 4);
     w.dqf = w.bsum + round256((size_t)P.N * P.H * nblk * P.D * 4);
     w.dkf = w.dqf + tokf;
-    w.total = w.dkf + tokf;
+    w.cv = w.dkf + tokf;
+    w.total = w.cv + tokv;
     return w;
 }
 
@@ -1047,8 +1060,8 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.D = P.D;
     a.E = P.E;
     a.q = tok(q, dims->qk_strides);
-    a.k = tok(k, dims->qk_strides);
-    a.v = tok(v, dims->v_strides);
+    a.k = tok(k, P.k_st, P.G);
+    a.v = tok(v, P.kv_v_st, P.G);
     a.out = tok_out(o, dims->v_strides);
     a.s_in = la::StateIn{initial_state, P.E, 1};
     a.s_out = la::StateOut{final_state, P.E, 1};
@@ -1080,6 +1093,10 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
         pa.sb = dims->qk_strides[0];
         pa.st = dims->qk_strides[1];
         pa.sh = dims->qk_strides[2];
+        pa.ksb = P.k_st[0];
+        pa.kst = P.k_st[1];
+        pa.ksh = P.k_st[2];
+        pa.khd = P.G;
         pa.g = g;
         pa.gsb = g_strides[0];
         pa.gst = g_strides[1];
@@ -1125,7 +1142,7 @@ size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *
     g_msg = keep;
     if (st != LA_OK)
         return 0;
-    return gla_bwd_layout(P, dtype).total +
+    return gla_bwd_layout(P, dims, dtype).total +
            (with_forward_operands ? 0 : gla_fwd_layout(P, dtype, true).total);
 }
 
@@ -1151,7 +1168,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     }
     if ((st = gla_check(P, dims, g, g_strides, g_gamma)) || !has_states(P))
         return st;
-    const GlaBwdWs bw = gla_bwd_layout(P, dtype);
+    const GlaBwdWs bw = gla_bwd_layout(P, dims, dtype);
     const size_t need_ws = bw.total;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
         workspace_bytes < need_ws)
@@ -1161,11 +1178,17 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     uint8_t *wsb = static_cast<uint8_t *>(workspace);
     float *Ft = static_cast<float *>(workspace);
     float *bsum = reinterpret_cast<float *>(wsb + bw.bsum);
-    // bf16 tokens: dq and dk in fp32, dense (token stride H D)
-    const bool f32g = dtype == LA_DTYPE_BF16;
+    // dq and dk in fp32 rows of the workspace, dense (token stride H D)
+    const bool f32g = gla_f32_grads(P, dims, dtype);
     float *dqf = f32g ? reinterpret_cast<float *>(wsb + bw.dqf) : nullptr;
     float *dkf = f32g ? reinterpret_cast<float *>(wsb + bw.dkf) : nullptr;
     const int64_t fsh = P.D, fst = (int64_t)P.H * P.D, fsb = fst * P.T;
+    // grouped key/value heads: every query head's part of dk (in dkf) and of
+    // dv (below) first, each group summed at the end
+    const bool grouped = P.G > 1;
+    const int64_t vsh = P.E, vst = (int64_t)P.H * P.E, vsb = vst * P.T;
+    const la::TokOut dvo =
+        grouped ? la::TokOut{wsb + bw.cv, vsb, vst, vsh} : tok_out(dv, P.kv_v_st);
     la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
     // The chunked form on the tensor cores, when it applies and the workspace
     // also holds its operands: the three sweeps on q~, k~ for the (sequence,
@@ -1180,10 +1203,10 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && st[0] % 8 == 0 && st[1] % 8 == 0 &&
                    st[2] % 8 == 0;
         };
-        const bool aligned = al(q, dims->qk_strides) && al(k, dims->qk_strides) &&
-                             al(dq, dims->qk_strides) && al(dk, dims->qk_strides) &&
-                             al(v, dims->v_strides) && al(d_o, dims->v_strides) &&
-                             al(dv, dims->v_strides);
+        const bool aligned = al(q, dims->qk_strides) && al(k, P.k_st) &&
+                             al(dq, dims->qk_strides) && al(dk, P.k_st) &&
+                             al(v, P.kv_v_st) && al(d_o, dims->v_strides) &&
+                             al(dv, P.kv_v_st);
         const bool gate_pairs = (reinterpret_cast<uintptr_t>(g) & 7) == 0 &&
                                 (reinterpret_cast<uintptr_t>(dg) & 7) == 0 &&
                                 g_strides[0] % 2 == 0 && g_strides[1] % 2 == 0 &&
@@ -1212,6 +1235,10 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             pa.sb = dims->qk_strides[0];
             pa.st = dims->qk_strides[1];
             pa.sh = dims->qk_strides[2];
+            pa.ksb = P.k_st[0];
+            pa.kst = P.k_st[1];
+            pa.ksh = P.k_st[2];
+            pa.khd = P.G;
             pa.g = g;
             pa.gsb = g_strides[0];
             pa.gst = g_strides[1];
@@ -1225,6 +1252,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             pa.lim = 72.f;
             pa.dq = dq;
             pa.dk = dk;
+            pa.dk32 = grouped ? dkf : nullptr;
             pa.dqf = dqf;
             pa.dkf = dkf;
             pa.dg = dg;
@@ -1235,7 +1263,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
                 return cuda_fail(e, "gated backward operands");
             const int64_t dsh = P.D, dst = (int64_t)P.H * P.D, dsb = dst * P.T;
             const la::Tok tq{pa.xq, dsb, dst, dsh, 1}, tk{pa.yk, dsb, dst, dsh, 1};
-            const la::Tok tdo = tok(d_o, dims->v_strides), tv = tok(v, dims->v_strides);
+            const la::Tok tdo = tok(d_o, dims->v_strides), tv = tok(v, P.kv_v_st, P.G);
             la::SweepArgs t = a;
             t.gla_er = pa.er;
             t.gla_u = pa.u;
@@ -1253,7 +1281,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
                 // dv: backward-type (k~, q~, do), G with gated rows
                 t.D = P.D;
                 t.E = P.E;
-                t.out = tok_out(dv, dims->v_strides);
+                t.out = dvo;
                 t.s_in = la::StateIn{d_final_state, P.E, 1};
                 t.s_out = la::StateOut{d_initial_state, P.E, 1};
                 e = la::tc_gla_sweep(t, true, false, tk, tq, tdo, s);
@@ -1279,8 +1307,8 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.D = P.E;
     a.E = P.D;
     a.q = tok(d_o, dims->v_strides);
-    a.k = tok(v, dims->v_strides);
-    a.v = tok(k, dims->qk_strides);
+    a.k = tok(v, P.kv_v_st, P.G);
+    a.v = tok(k, P.k_st, P.G);
     a.out = f32g ? la::TokOut{dqf, fsb, fst, fsh} : tok_out(dq, dims->qk_strides);
     a.out_f32 = f32g ? 1 : 0;
     a.s_in = la::StateIn{initial_state, 1, P.E};
@@ -1292,9 +1320,9 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.D = P.D;
     a.E = P.E;
     a.q = tok(q, dims->qk_strides);
-    a.k = tok(k, dims->qk_strides);
+    a.k = tok(k, P.k_st, P.G);
     a.v = tok(d_o, dims->v_strides);
-    a.out = tok_out(dv, dims->v_strides);
+    a.out = dvo;
     a.out_f32 = 0;
     a.s_in = la::StateIn{d_final_state, P.E, 1};
     a.s_out = la::StateOut{d_initial_state, P.E, 1};
@@ -1305,9 +1333,9 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.D = P.E;
     a.E = P.D;
     a.q = tok(d_o, dims->v_strides);
-    a.k = tok(v, dims->v_strides);
+    a.k = tok(v, P.kv_v_st, P.G);
     a.v = tok(q, dims->qk_strides);
-    a.out = f32g ? la::TokOut{dkf, fsb, fst, fsh} : tok_out(dk, dims->qk_strides);
+    a.out = f32g ? la::TokOut{dkf, fsb, fst, fsh} : tok_out(dk, P.k_st);
     a.out_f32 = f32g ? 1 : 0;
     a.s_in = la::StateIn{d_final_state, 1, P.E};
     a.s_out = la::StateOut{nullptr, 0, 0};
@@ -1335,15 +1363,20 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     gg.sb = dims->qk_strides[0];
     gg.st = dims->qk_strides[1];
     gg.sh = dims->qk_strides[2];
+    gg.ksb = P.k_st[0];
+    gg.kst = P.k_st[1];
+    gg.ksh = P.k_st[2];
+    gg.khd = P.G;
     if (f32g) {
-        // fp32 gradients from the workspace; the kernels write the bf16 ones
+        // fp32 gradients from the workspace; the kernels write the token-dtype
+        // copies (dk: the group sums below, when grouped)
         gg.dqf = dqf;
         gg.dkf = dkf;
         gg.fsb = fsb;
         gg.fst = fst;
         gg.fsh = fsh;
         gg.dq = dq;
-        gg.dk = dk;
+        gg.dk = grouped ? nullptr : dk;
     } else {
         gg.dqf = static_cast<const float *>(dq);
         gg.dkf = static_cast<const float *>(dk);
@@ -1360,7 +1393,19 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     gg.bsum = bsum;
     gg.flags = flags;
     cudaError_t e = la::gate_grad(gg, s);
-    return e == cudaSuccess ? LA_OK : cuda_fail(e, "gate gradient");
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gate gradient");
+    if (grouped) {
+        const int rows = P.packed ? 1 : P.B;
+        const int bf16 = dtype == LA_DTYPE_BF16;
+        e = la::gqa_reduce(dkf, tok_out(dk, P.k_st), rows, P.T, P.Hkv, P.G, P.D, bf16, s, true);
+        if (e == cudaSuccess)
+            e = la::gqa_reduce(dvo.p, tok_out(dv, P.kv_v_st), rows, P.T, P.Hkv, P.G, P.E, bf16,
+                               s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "grouped key/value gradient sum");
+    }
+    return LA_OK;
 }
 
 }  // extern "C"

@@ -60,21 +60,25 @@ __device__ __forceinline__ Seq seq_of(const GateGradArgs &a, int n)
     return s;
 }
 
-// q dq - k dk at processing position p, channel c; COPY: also writes the
-// token-dtype dq, dk there
+// q dq - k dk at processing position p, channel c of query head h (k of
+// its key head h / khd, dk this query head's part); COPY: also writes the
+// token-dtype dq, dk there (each when its pointer is set)
 template <typename T, bool COPY>
 __device__ __forceinline__ float term(const GateGradArgs &a, const Seq &s, int h, int64_t p, int c)
 {
     const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
     const int64_t off = s.row * a.sb + t * a.st + (int64_t)h * a.sh + c;
+    const int64_t ko = s.row * a.ksb + t * a.kst + c;
     const int64_t fo = s.row * a.fsb + t * a.fst + (int64_t)h * a.fsh + c;
     const T *q = static_cast<const T *>(a.q), *k = static_cast<const T *>(a.k);
     const float dq = a.dqf[fo], dk = a.dkf[fo];
     if (COPY) {
-        stt(static_cast<T *>(a.dq) + off, dq);
-        stt(static_cast<T *>(a.dk) + off, dk);
+        if (a.dq)
+            stt(static_cast<T *>(a.dq) + off, dq);
+        if (a.dk)
+            stt(static_cast<T *>(a.dk) + ko + (int64_t)h * a.ksh, dk);
     }
-    return ldt(q + off) * dq - ldt(k + off) * dk;
+    return ldt(q + off) * dq - ldt(k + ko + (int64_t)(h / a.khd) * a.ksh) * dk;
 }
 
 template <typename T> __global__ void __launch_bounds__(256) block_sums(GateGradArgs a)
@@ -114,7 +118,7 @@ template <typename T> __global__ void __launch_bounds__(256) block_scan(GateGrad
     for (int jj = j + 1; jj < nb; ++jj)
         acc += bs[(int64_t)jj * a.D];
     for (int64_t p = p1 - 1; p >= p0; --p) {
-        acc += a.dq ? term<T, true>(a, s, h, p, c) : term<T, false>(a, s, h, p, c);
+        acc += (a.dq || a.dk) ? term<T, true>(a, s, h, p, c) : term<T, false>(a, s, h, p, c);
         const int64_t t = s.bos + (a.reverse ? s.len - 1 - p : p);
         a.dg[s.row * a.gsb + t * a.gst + (int64_t)h * a.gsh + c] = acc;
     }
@@ -126,7 +130,7 @@ cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s)
 {
     if (a.N == 0 || a.H == 0 || a.nblk == 0)
         return cudaSuccess;
-    if (a.D > 256 || a.N > 65535 || a.H > 65535 || a.nblk > 0x7fffffff)
+    if (a.D > 256 || a.N > 65535 || a.H > 65535 || a.nblk > 0x7fffffff || a.khd < 1)
         return cudaErrorNotSupported;
     dim3 grid((unsigned)a.nblk, (unsigned)a.H, (unsigned)a.N);
     const int threads = (a.D + 31) / 32 * 32;

@@ -102,13 +102,13 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
     {
         const int esz = (int)sizeof(T);
         if ((c * esz) % 128 == 0) {
-            const int64_t qo = row * a.sb + (int64_t)h * a.sh + c;
-            const char *qr = reinterpret_cast<const char *>(static_cast<const T *>(a.q) + qo);
-            const char *kr = reinterpret_cast<const char *>(static_cast<const T *>(a.k) + qo);
+            const char *qr = reinterpret_cast<const char *>(
+                static_cast<const T *>(a.q) + row * a.sb + (int64_t)h * a.sh + c);
+            const char *kr = reinterpret_cast<const char *>(
+                static_cast<const T *>(a.k) + row * a.ksb + (int64_t)(h / a.khd) * a.ksh + c);
             for (int j = 0; j < np; ++j) {
-                const int64_t off = (tb + j * ts) * a.st * esz;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + off));
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + off));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + (tb + j * ts) * a.st * esz));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + (tb + j * ts) * a.kst * esz));
             }
         }
     }
@@ -178,13 +178,14 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
 
     // pass 2: q~ = q exp(b - r), k~ = k exp(r - b); zeros when out of range
     const T *qp = static_cast<const T *>(a.q) + row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
-    const T *kp = static_cast<const T *>(a.k) + row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
+    const T *kp = static_cast<const T *>(a.k) + row * a.ksb + (int64_t)(h / a.khd) * a.ksh + c +
+                  tb * a.kst;
     const int64_t dst = (int64_t)a.H * a.D;   // token stride of the dense outputs
     __nv_bfloat162 *xq = reinterpret_cast<__nv_bfloat162 *>(
         static_cast<__nv_bfloat16 *>(a.xq) + ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst);
     __nv_bfloat162 *yk = reinterpret_cast<__nv_bfloat162 *>(
         static_cast<__nv_bfloat16 *>(a.yk) + ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst);
-    const int64_t istep = ts * a.st, ostep = ts * dst / 2;
+    const int64_t istep = ts * a.st, kstep = ts * a.kst, ostep = ts * dst / 2;
     const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
     // eight tokens' q, k pairs loaded together (indices clamped into the
     // group), then scaled and stored
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
             const int j = j0 + jj;
             const int jl = j < np ? j : (np > 0 ? np - 1 : 0);
             qv[jj] = Pair<T>::load(qp + jl * istep);
-            kv[jj] = Pair<T>::load(kp + jl * istep);
+            kv[jj] = Pair<T>::load(kp + jl * kstep);
         }
 #pragma unroll
         for (int jj = 0; jj < PB; ++jj) {
@@ -278,6 +279,7 @@ __global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
         const int64_t ts = rev ? -1 : 1;
         const float *gp = a.g + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
         const int64_t qo = row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
+        const int64_t ko = row * a.ksb + (int64_t)h * a.ksh + c + tb * a.kst;
         const int64_t fo = ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst;
         float2 b[UT], dqv[UT], dkv[UT], qv[UT], kv[UT];
 #pragma unroll
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
         // dq, dk, and the terms q~ dq~ - k~ dk~ (the rounded operands and
         // their own gradients) into b[]
         T *dqp = static_cast<T *>(a.dq) + qo;
-        T *dkp = static_cast<T *>(a.dk) + qo;
+        T *dkp = a.dk32 ? nullptr : static_cast<T *>(a.dk) + ko;
         float2 gt = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < UT; ++j) {
@@ -338,8 +340,11 @@ __global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
                 const float ex = b[j].x + sh0.x, ey = b[j].y + sh0.y;   // b - r
                 Pair<T>::store(dqp + j * ts * a.st,
                                make_float2(dqv[j].x * __expf(ex), dqv[j].y * __expf(ey)));
-                Pair<T>::store(dkp + j * ts * a.st,
-                               make_float2(dkv[j].x * __expf(-ex), dkv[j].y * __expf(-ey)));
+                const float2 dkj = make_float2(dkv[j].x * __expf(-ex), dkv[j].y * __expf(-ey));
+                if (dkp)
+                    Pair<T>::store(dkp + j * ts * a.kst, dkj);
+                else   // this thread read dk~ here above: overwritten in place
+                    *reinterpret_cast<float2 *>(a.dk32 + fo + j * ts * dst) = dkj;
                 tm = make_float2(qv[j].x * dqv[j].x - kv[j].x * dkv[j].x,
                                  qv[j].y * dqv[j].y - kv[j].y * dkv[j].y);
             }
@@ -383,7 +388,7 @@ cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s)
 {
     if (a.N == 0 || a.H == 0 || a.ncmax == 0)
         return cudaSuccess;
-    if (a.D != 128 || a.N > 65535 || a.H > 65535 || a.ncmax > 0x7fffffff)
+    if (a.D != 128 || a.N > 65535 || a.H > 65535 || a.ncmax > 0x7fffffff || a.khd < 1)
         return cudaErrorNotSupported;
     dim3 grid((unsigned)a.ncmax, (unsigned)a.H, (unsigned)a.N);
     const int threads = PG * 64;

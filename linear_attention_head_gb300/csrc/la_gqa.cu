@@ -29,8 +29,8 @@ template <> __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, 
     *p = __float2bfloat16_rn(x);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256) gqa_reduce_kernel(const T *in, TokOut out, int T_, int Hkv,
+template <typename TI, typename T>
+__global__ void __launch_bounds__(256) gqa_reduce_kernel(const TI *in, TokOut out, int T_, int Hkv,
                                                          int G, int X, int64_t total)
 {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(256) gqa_reduce_kernel(const T *in, TokOut out
         const int j = (int)(r % Hkv);
         r /= Hkv;
         const int64_t t = r % T_, b = r / T_;
-        const T *src = in + (((b * T_ + t) * Hkv + j) * G) * (int64_t)X + c;
+        const TI *src = in + (((b * T_ + t) * Hkv + j) * G) * (int64_t)X + c;
         float acc = 0.f;
         for (int g = 0; g < G; ++g)
             acc += ld(src + (int64_t)g * X);
@@ -88,12 +88,12 @@ __global__ void __launch_bounds__(256) gqa_reduce_bf16x8(const __nv_bfloat16 *in
 }  // namespace
 
 cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv, int G, int X,
-                       int bf16, cudaStream_t s)
+                       int bf16, cudaStream_t s, bool in_f32)
 {
     const int64_t total = (int64_t)B * T * Hkv * X;
     if (total == 0)
         return cudaSuccess;
-    const bool vec = bf16 && X % 8 == 0 && out.sb % 8 == 0 && out.st % 8 == 0 && out.sh % 8 == 0 &&
+    const bool vec = bf16 && !in_f32 && X % 8 == 0 && out.sb % 8 == 0 && out.st % 8 == 0 && out.sh % 8 == 0 &&
                      (reinterpret_cast<uintptr_t>(out.p) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(in) & 15) == 0;
     const int64_t work = vec ? total / 8 : total;
@@ -102,12 +102,15 @@ cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv,
     if (vec)
         gqa_reduce_bf16x8<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(in), out, T,
                                                  Hkv, G, X, work);
+    else if (bf16 && in_f32)
+        gqa_reduce_kernel<float, __nv_bfloat16><<<blocks, 256, 0, s>>>(
+            static_cast<const float *>(in), out, T, Hkv, G, X, total);
     else if (bf16)
-        gqa_reduce_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        gqa_reduce_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, 256, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(in), out, T, Hkv, G, X, total);
     else
-        gqa_reduce_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float *>(in), out, T,
-                                                        Hkv, G, X, total);
+        gqa_reduce_kernel<float, float><<<blocks, 256, 0, s>>>(static_cast<const float *>(in),
+                                                               out, T, Hkv, G, X, total);
     note_launch();
     return cudaGetLastError();
 }

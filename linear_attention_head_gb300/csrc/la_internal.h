@@ -93,8 +93,10 @@ struct GlaPrepArgs {
     int64_t ncmax;            // chunks of the longest sequence
     const int32_t *cu;        // packed sequences, or nullptr
     int reverse, bf16;
-    const void *q, *k;        // token dtype, element strides sb, st, sh (shared)
-    int64_t sb, st, sh;
+    const void *q, *k;        // token dtype: q (and dq) at strides sb, st, sh; k
+    int64_t sb, st, sh;       // (and dk) at ksb, kst, ksh, head h reading key
+    int64_t ksb, kst, ksh;    // head h / khd (grouped key/value heads)
+    int khd;
     const float *g;           // gate, strides gsb, gst, gsh
     int64_t gsb, gst, gsh;
     const float *g_gamma;
@@ -102,8 +104,10 @@ struct GlaPrepArgs {
     float *er, *u;            // [N][H][ncmax][D]
     int *flags;               // [N H], zeroed beforehand
     float lim;                // largest |b - r| (and |r|) the chunked form takes
-    void *dq, *dk;            // gla_undo: dq, dk out (token dtype, q's strides)
+    void *dq, *dk;            // gla_undo: dq, dk out (token dtype, their strides)
     const float *dqf, *dkf;   // gla_undo: dq~, dk~ in (fp32, dense [rows][T][H][D])
+    float *dk32;              // gla_undo: when set, dk goes there in fp32, in
+                              // place of dk~ (per query head), not to dk
     float *dg;                // gla_undo: the gate's gradient (the gate's strides)
     const float *Ft, *dF;     // gla_undo: final state (transposed, [E][D] per
                               // pair) and its gradient ([D][E]), or dF null
@@ -171,13 +175,14 @@ cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s);
 
 // Sum of grouped contributions (la_gqa.cu): out[b, t, j, c] = sum over
 // i < G of in[b, t, j*G + i, c] in fp32, for j < Hkv and c < X; `in` is dense
-// [B, T, Hkv*G, X] of the token dtype, `out` strided like a TokOut.
+// [B, T, Hkv*G, X] of the token dtype (fp32 when in_f32), `out` strided like a
+// TokOut, of the token dtype.
 cudaError_t gqa_reduce(const void *in, const TokOut &out, int B, int T, int Hkv, int G, int X,
-                       int bf16, cudaStream_t s);
+                       int bf16, cudaStream_t s, bool in_f32 = false);
 
 // Gradient of the per-key gate (la_gla.cu) from q, k (token dtype) and the
-// fp32 gradients dqf, dkf; dg is fp32 with the gate's strides.  With dq, dk
-// set, the kernels also write dqf, dkf there in the token dtype.
+// fp32 gradients dqf, dkf; dg is fp32 with the gate's strides.  With dq (dk)
+// set, the kernels also write dqf (dkf) there in the token dtype.
 // Ft: the final state transposed [N][H][E][D] (fp32), dF: its upstream
 // gradient [N][H][D][E] (either may be null: no final-state term).  bsum:
 // scratch [N][H][nblk][D] fp32, nblk = ceil(longest sequence / DG_TB).
@@ -187,11 +192,13 @@ struct GateGradArgs {
     int64_t nblk;
     const int32_t *cu;
     int reverse, bf16;
-    const void *q, *k;        // token dtype, strides sb, st, sh
-    int64_t sb, st, sh;
-    const float *dqf, *dkf;   // fp32 dq, dk, strides fsb, fst, fsh
+    const void *q, *k;        // token dtype: q (and dq) at strides sb, st, sh; k
+    int64_t sb, st, sh;       // (and dk) at ksb, kst, ksh, head h reading key
+    int64_t ksb, kst, ksh;    // head h / khd
+    int khd;
+    const float *dqf, *dkf;   // fp32 dq, dk (per query head), strides fsb, fst, fsh
     int64_t fsb, fst, fsh;
-    void *dq, *dk;            // or null: token-dtype copies of dqf, dkf (q's strides)
+    void *dq, *dk;            // or null: token-dtype copies of dqf, dkf
     float *dg;
     int64_t gsb, gst, gsh;
     const float *Ft, *dF;

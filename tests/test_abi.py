@@ -258,3 +258,29 @@ def test_gated_backward_workspace_holds_fp32_gradients(lib):
     assert lib.la_gla_workspace_size(ctypes.byref(d), 1, None, 1) == r(state) + r(bsum)
     assert lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 1) == \
         r(state) + r(bsum) + 2 * r(tokf)
+
+
+def test_gated_backward_workspace_with_grouped_heads(lib):
+    # grouped key/value heads: every query head's part of dk in the fp32 rows
+    # (also for fp32 tokens, where dq and dk otherwise go straight to the
+    # caller) and of dv ([B][T][H][E], token dtype), summed per group at the end
+    r = lambda x: (x + 255) // 256 * 256
+    B, T, H, Hkv, D, E = 2, 300, 6, 2, 128, 96
+    d = _dims(B=B, T=T, H=H, D=D, E=E)
+    d.kv_heads = Hkv
+    for i, (ks, vs) in enumerate(zip((T * Hkv * D, Hkv * D, D), (T * Hkv * E, Hkv * E, E))):
+        d.k_strides[i], d.kv_v_strides[i] = ks, vs
+    state, bsum, tokf = B * H * D * E * 4, B * H * 2 * D * 4, B * T * H * D * 4
+    for dtype, esz in ((0, 2), (1, 4)):
+        assert lib.la_gla_workspace_size(ctypes.byref(d), dtype, None, 1) == \
+            r(state) + r(bsum) + 2 * r(tokf) + r(B * T * H * E * esz)
+    # the same sizes with kv_heads = heads: k's own strides, no group sums
+    d1 = _dims(B=B, T=T, H=H, D=D, E=E)
+    d1.kv_heads = H
+    for i, (ks, vs) in enumerate(zip((T * H * D, H * D, D), (T * H * E, H * E, E))):
+        d1.k_strides[i], d1.kv_v_strides[i] = ks, vs
+    assert lib.la_gla_workspace_size(ctypes.byref(d1), 1, None, 1) == r(state) + r(bsum)
+    d1.k_strides[1] = H * D + 8     # k strided unlike q: the fp32 rows again
+    d1.k_strides[0] = T * (H * D + 8)
+    assert lib.la_gla_workspace_size(ctypes.byref(d1), 1, None, 1) == \
+        r(state) + r(bsum) + 2 * r(tokf)
