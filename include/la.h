@@ -57,10 +57,17 @@
  *     allocates device memory or synchronizes, except: when cu_seqlens is given
  *     without cu_seqlens_host the library copies cu_seqlens to the host and
  *     waits for that copy; and la_get_device_error synchronizes `stream`.
- *     Packed calls that use a workspace (or la_fwd_noalloc's array) also
- *     copy host data into it during the call: the longest-first schedule
- *     and the sequence split's segment table are built on the host and sent
- *     with cudaMemcpyAsync from pageable memory.
+ *     Calls that use a workspace (or la_fwd_noalloc's array) for the
+ *     schedule or the split -- packed calls, and sequences the split cuts --
+ *     also copy host data into it during the call: the longest-first
+ *     schedule and the sequence split's segment table are built on the host
+ *     and sent with cudaMemcpyAsync from pageable memory.
+ *   - CUDA graphs: those calls (and packed calls without cu_seqlens_host)
+ *     cannot be captured.  Every other call -- no cu_seqlens, and no split
+ *     (la_set_sequence_split(0, 0), or sizes it leaves whole) -- enqueues
+ *     only kernels and memsets on `stream` (tensor maps travel as kernel
+ *     parameters) and can be captured once and replayed with new contents
+ *     in the same buffers; replays equal eager calls bit for bit.
  *     The tensor-core kernels are launched as programmatic dependents of
  *     the stream's previous kernel: they may start their set-up while it
  *     drains, but read and write global memory only after it has completed,
@@ -223,8 +230,10 @@ la_status la_bwd_dkdv(const la_dims *dims, int32_t dtype,
  * only ever holds the schedule (never the sequence split's states, so packed
  * calls here always run unsplit).  The first packed call on a device looks the
  * array's device address up (cudaGetSymbolAddress) with that device current
- * and keeps it for the rest of the process; make that first call before any
- * stream capture begins.  The kept address does not survive a
+ * and keeps it for the rest of the process.  Packed calls copy the schedule
+ * from pageable host memory into the array, so they cannot be captured in a
+ * CUDA graph (dense calls never touch the array and capture as la_fwd
+ * does).  The kept address does not survive a
  * cudaDeviceReset: do not use this entry point on a device after resetting
  * it.  Every call on a device shares the one array, which keeps the previous
  * call's schedule; each call overwrites the entries it uses.  Calls whose
