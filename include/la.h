@@ -323,8 +323,8 @@ size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
  *            q_t dq_t - k_t dk_t (+ sum_e F dF at the last token),
  * F the final state and dF = d_final_state.  Needs a 256-byte aligned device
  * workspace (LA_ERR_INVALID_ARG otherwise); la_gla_workspace_size gives the
- * bytes with which bf16 calls with D = E = 128, sequences longer than 16
- * tokens and 16-byte aligned token rows run the chunked form on the tensor
+ * bytes with which bf16 calls with D = 128, E in {64, 128}, sequences
+ * longer than 16 tokens and 16-byte aligned token rows run the chunked form on the tensor
  * cores: the forward's rescaled q~, k~ (see la_gla_fwd), three sweeps on
  * them -- forward-type (do, v, k~) giving dq~ = dq exp(r - b), backward-
  * type (k~, q~, do) giving dv, backward-type (v, do, q~) giving dk~ =

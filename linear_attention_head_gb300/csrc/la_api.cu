@@ -964,12 +964,13 @@ struct GlaFwdWs {
     size_t xq, yk, er, u, flags, total;
     int64_t ncmax;
 };
-GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype, bool bwd = false)
+GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype)
 {
     GlaFwdWs w{};
     const int64_t maxlen = gla_max_len(P);
-    // the backward's dq and dk sweeps put the 128 value channels on TMEM lanes
-    if (dtype != LA_DTYPE_BF16 || P.D != 128 || (P.E != 64 && P.E != 128) || (bwd && P.E != 128) ||
+    // 128 key channels; the backward's dq~ and dk~ sweeps put the 64 or 128
+    // value channels on TMEM lanes
+    if (dtype != LA_DTYPE_BF16 || P.D != 128 || (P.E != 64 && P.E != 128) ||
         maxlen <= la::SHORT_MAX_T || P.N > 65535 || P.H > 65535)
         return w;
     w.ncmax = (maxlen + 127) / 128;
@@ -1143,7 +1144,7 @@ size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *
     if (st != LA_OK)
         return 0;
     return gla_bwd_layout(P, dims, dtype).total +
-           (with_forward_operands ? 0 : gla_fwd_layout(P, dtype, true).total);
+           (with_forward_operands ? 0 : gla_fwd_layout(P, dtype).total);
 }
 
 la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
@@ -1198,7 +1199,7 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     const int *flags = nullptr;
     la::GlaPrepArgs pa{};
     {
-        const GlaFwdWs w = gla_fwd_layout(P, dtype, true);
+        const GlaFwdWs w = gla_fwd_layout(P, dtype);
         auto al = [](const void *p, const int64_t *st) {
             return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && st[0] % 8 == 0 && st[1] % 8 == 0 &&
                    st[2] % 8 == 0;

@@ -164,7 +164,9 @@ template <int D, int E, bool BWD, int GLA, bool SO = false>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_constant__ TcParams P)
 {
     static_assert(D % 64 == 0 && D <= 256 && (E == 64 || E == 128), "tile shape");
-    static_assert(!GLA || D == 128, "the gated form has 128 key channels");
+    // the gated form has 128 key channels: the state's rows (GLA 1) or its
+    // columns (GLA 2, whose rows are the 64 or 128 value channels)
+    static_assert(GLA == 0 || (GLA == 1 ? D == 128 : E == 128), "gated key channels");
     using L = TcLayout<D, E>;
     constexpr int NST = L::NST;
     constexpr uint32_t TM_OI = L::TM_OI, TM_OA = L::TM_OA, TM_S = L::TM_S;
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
             // state's row i, or column i), [N][H][ncmax][128]; vo the chunk's
             // own factor, vn the next chunk's (also the initial state's)
             const int64_t vrow = ((int64_t)n * a.H + h) * a.gla_ncmax;
-            auto vidx = [&](int cpos) { return (vrow + cpos) * D + i; };
+            auto vidx = [&](int cpos) { return (vrow + cpos) * 128 + i; };
             const float *vo = BWD ? a.gla_er : a.gla_u, *vn = BWD ? a.gla_u : a.gla_er;
             // GLA 2: this step's per-column factors, shared by the S group:
             // the chunk's own (colf) and the next chunk's (coln)
@@ -608,7 +610,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                 if (i < E)
                     colf[i] = vn[vidx(flip ? nc - 1 : 0)];
                 sg_sync();
-                state_in(a.s_in, sb, i, e0, E, sbf(0), D * 128, stm(0), 1.f, 1.f, colf);
+                if (i < D)   // rows past D (64 value channels) are padding
+                    state_in(a.s_in, sb, i, e0, E, sbf(0), D * 128, stm(0), 1.f, 1.f, colf);
             } else {
 #pragma unroll 1
                 for (int pc = 0; pc < L::NP; ++pc)
@@ -961,17 +964,24 @@ cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, 
     if (a.N == 0)
         return cudaSuccess;
     const Tok xyz[3] = {x, y, z};
+    // one CTA per (sequence, head) with the 128 key channels as the state's
+    // rows (D = 128, E in {64, 128}) or columns (E = 128, D in {64, 128})
+    if (cols) {
+        if (a.E != 128 || (a.D != 64 && a.D != 128))
+            return cudaErrorNotSupported;
+        if (bwd)
+            return a.D == 128 ? launch_tc<128, 128, true, 2>(a, s, xyz)
+                              : launch_tc<64, 128, true, 2>(a, s, xyz);
+        return a.D == 128 ? launch_tc<128, 128, false, 2>(a, s, xyz)
+                          : launch_tc<64, 128, false, 2>(a, s, xyz);
+    }
     if (a.D != 128 || (a.E != 64 && a.E != 128))
-        return cudaErrorNotSupported;   // one CTA per (sequence, head), 128 key channels
-    if (cols && a.E != 128)
-        return cudaErrorNotSupported;   // column factors: 128 key channels as columns
+        return cudaErrorNotSupported;
     if (bwd)
-        return cols ? launch_tc<128, 128, true, 2>(a, s, xyz)
-                    : (a.E == 128 ? launch_tc<128, 128, true, 1>(a, s, xyz)
-                                  : launch_tc<128, 64, true, 1>(a, s, xyz));
-    return cols ? launch_tc<128, 128, false, 2>(a, s, xyz)
-                : (a.E == 128 ? launch_tc<128, 128, false, 1>(a, s, xyz)
-                              : launch_tc<128, 64, false, 1>(a, s, xyz));
+        return a.E == 128 ? launch_tc<128, 128, true, 1>(a, s, xyz)
+                          : launch_tc<128, 64, true, 1>(a, s, xyz);
+    return a.E == 128 ? launch_tc<128, 128, false, 1>(a, s, xyz)
+                      : launch_tc<128, 64, false, 1>(a, s, xyz);
 }
 
 cudaError_t tc_state_sweep(const SweepArgs &a, bool bwd, cudaStream_t s)

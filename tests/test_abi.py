@@ -238,14 +238,15 @@ def test_gated_forward_workspace_size(lib):
 def test_gated_backward_workspace_with_forward_operands(lib):
     # with the forward's operands the backward needs only its token-by-token
     # part; the difference is the forward's workspace where the chunked
-    # backward applies (D = E = 128), nothing otherwise
-    d = _dims(B=2, T=300, H=3, D=128, E=128)
-    full = lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 0)
-    part = lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 1)
-    assert full - part == lib.la_gla_fwd_workspace_size(ctypes.byref(d), 0, None) > 0
-    d64 = _dims(B=2, T=300, H=3, D=128, E=64)
-    assert lib.la_gla_workspace_size(ctypes.byref(d64), 0, None, 0) == \
-        lib.la_gla_workspace_size(ctypes.byref(d64), 0, None, 1) > 0
+    # backward applies (bf16, D = 128, E in {64, 128}), nothing otherwise
+    for E in (128, 64):
+        d = _dims(B=2, T=300, H=3, D=128, E=E)
+        full = lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 0)
+        part = lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 1)
+        assert full - part == lib.la_gla_fwd_workspace_size(ctypes.byref(d), 0, None) > 0
+    for d in (_dims(B=2, T=300, H=3, D=64, E=64), _dims(B=2, T=300, H=3, D=128, E=96)):
+        assert lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 0) == \
+            lib.la_gla_workspace_size(ctypes.byref(d), 0, None, 1) > 0
 
 
 def test_gated_backward_workspace_holds_fp32_gradients(lib):

@@ -13,6 +13,7 @@ import torch
 import linear_attention_head_gb300 as la
 import oracle
 import workloads as W
+from linear_attention_head_gb300 import _native as N
 from parity import TOL, compare, compare_gated as _compare_gla
 
 pytestmark = pytest.mark.gpu
@@ -146,10 +147,10 @@ def _fwd_only(x, reverse, chunked=True):
 
 # The chunked tensor-core form (bf16, D = 128, E in {64, 128}, > 16 tokens):
 # several chunks and a ragged tail, both directions, with and without an
-# initial state.
-# (The backward takes the chunked form at D = E = 128; E = 64 checks the
-# forward alone.)
-@pytest.mark.parametrize("T,E", [(300, 128), (1000, 128), (517, 64)])
+# initial state.  At E = 64 the backward's dq~ and dk~ sweeps hold the 64
+# value channels on TMEM lanes (the state's rows) and the 128 gated key
+# channels as columns.
+@pytest.mark.parametrize("T,E", [(300, 128), (1000, 128), (517, 64), (300, 64)])
 @pytest.mark.parametrize("init", [0.2, 0.0])
 def test_gated_chunked_matches_oracle(T, E, init):
     x = _inputs(2, T, 3, 128, E, torch.bfloat16, seed=T + E)
@@ -157,12 +158,28 @@ def test_gated_chunked_matches_oracle(T, E, init):
         x["initial_state"] = None
     for reverse in (False, True):
         label = "chunked T=%d E=%d rev=%d" % (T, E, reverse)
-        if E == 128:
-            _compare_gla(_gpu(x, reverse), _oracle(x, reverse), x, reverse, TOL[torch.bfloat16],
-                         label)
-        else:
-            got, ref = _fwd_only(x, reverse)
-            compare(got, ref, TOL[torch.bfloat16], label=label)
+        _compare_gla(_gpu(x, reverse), _oracle(x, reverse), x, reverse, TOL[torch.bfloat16],
+                     label)
+
+
+def test_gated_backward_at_e64_runs_the_chunked_form():
+    # the chunked backward launches the pre-pass, three tensor-core sweeps and
+    # the rescaling pass on top of the token-by-token launches (which find
+    # every pair done and return): at least five more launches than the
+    # token-by-token backward, and different rounding
+    lib = N.lib()
+    x = _inputs(1, 400, 2, 128, 64, torch.bfloat16, seed=64)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    got, counts = {}, {}
+    for chunked in (True, False):
+        n0 = lib.la_launch_count()
+        got[chunked] = la.gla_bwd(d["q"], d["k"], d["v"], d["do"], d["g"], d["g_gamma"],
+                                  d["scale"], d["initial_state"], d["d_final_state"],
+                                  chunked=chunked)
+        torch.cuda.synchronize()
+        counts[chunked] = lib.la_launch_count() - n0
+    assert counts[True] >= counts[False] + 5, counts
+    assert not torch.equal(got[True][0], got[False][0])
 
 
 def test_gated_chunked_packed_sequences():
