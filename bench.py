@@ -782,12 +782,40 @@ def gla_bench(la, torch, dev, stream, peak):
     unit = B * T * H * D * 2
     la.get_device_error(dev)
     del q, k, v, do, g
-    return {"workload": "fwd+bwd b4 h32 n8192 d=e=128 bf16 tokens, fp32 per-key gate",
-            "kernels": "chunked tensor-core form (operand pre-pass + tcgen05 sweeps)",
-            "fwd_ms": f_ms, "bwd_ms": b_ms, "step_ms": s_ms, "bwd_alone_ms": b_alone_ms,
-            "tokens_per_s": B * T / (s_ms * 1e-3),
-            "fwd_frac_of_peak": (4 * unit + 2 * unit) / (f_ms * 1e-3) / 1e9 / peak,
-            "bwd_frac_of_peak": (7 * unit + 4 * unit) / (b_ms * 1e-3) / 1e9 / peak}
+    out = {"workload": "fwd+bwd b4 h32 n8192 d=e=128 bf16 tokens, fp32 per-key gate",
+           "kernels": "chunked tensor-core form (operand pre-pass + tcgen05 sweeps)",
+           "fwd_ms": f_ms, "bwd_ms": b_ms, "step_ms": s_ms, "bwd_alone_ms": b_alone_ms,
+           "tokens_per_s": B * T / (s_ms * 1e-3),
+           "fwd_frac_of_peak": (4 * unit + 2 * unit) / (f_ms * 1e-3) / 1e9 / peak,
+           "bwd_frac_of_peak": (7 * unit + 4 * unit) / (b_ms * 1e-3) / 1e9 / peak}
+    out["long_sequence_fwd"] = gla_long_bench(la, torch, dev, timed, peak)
+    return out
+
+
+def gla_long_bench(la, torch, dev, timed, peak):
+    """The gated forward on one long sequence with few heads (b1 h8 n262144
+    d=e=128 bf16, fp32 gate): 8 (sequence, head) pairs for 152 SMs, with the
+    sequence split (segment decays, pre-pass, two passes around the scan with
+    per-channel decays) and without it.  Algorithmic bytes: q, k, v, g read
+    (the gate fp32), o written."""
+    import workloads as W
+    from linear_attention_head_gb300 import _native
+    B, T, H, D = 1, 262144, 8, 128
+    gg = W.alibi_g_gamma(H).to(dev)
+    gen = torch.Generator(device=dev).manual_seed(23)
+    q, k, v = (torch.randn((B, T, H, D), generator=gen, device=dev).bfloat16() for _ in range(3))
+    g = -0.3 * torch.rand((B, T, H, D), generator=gen, device=dev)
+    out = {"workload": "gla_fwd b1 h8 n262144 d=e=128 bf16 tokens, fp32 per-key gate"}
+    nbytes = 6 * B * T * H * D * 2
+    for name, mode in (("split", 1), ("unsplit", 0)):
+        _native.check(_native.lib().la_set_sequence_split(mode, 0))
+        ms = timed(lambda: la.gla_fwd(q, k, v, g, gg, 1.0))
+        out[name] = {"ms": ms, "tokens_per_s": B * T / (ms * 1e-3),
+                     "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
+    _native.check(_native.lib().la_set_sequence_split(1, 0))
+    la.get_device_error(dev)
+    del q, k, v, g
+    return out
 
 
 def source_sha():

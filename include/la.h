@@ -299,7 +299,14 @@ la_status la_set_sequence_split(int32_t mode, int32_t min_segment_tokens);
  * total log-decay below about -144) runs the token-by-token kernels instead,
  * decided on the device.  All other calls, and calls without the
  * workspace, run the token-by-token kernels.  Not differentiated: g_gamma,
- * scale, reverse, cu_seqlens. */
+ * scale, reverse, cu_seqlens.
+ * Sequence split (as la_fwd's, la_set_sequence_split): with few (sequence,
+ * head) pairs and a gate whose strides allow the one-row token view, the
+ * chunked form runs on segments of whole chunks in two passes around a
+ * scan whose decay is per key channel, exp of the segment's summed
+ * log-decays (len * g_gamma[h] + the gates), formed from the pre-pass's
+ * chunk totals.  la_gla_fwd_workspace_size covers it.  Its operands are
+ * laid out per segment: operands_written stays 0. */
 la_status la_gla_fwd(const la_dims *dims, int32_t dtype,
                      const void *q, const void *k, const void *v,
                      const float *g, const int64_t *g_strides,

@@ -964,26 +964,186 @@ struct GlaFwdWs {
     size_t xq, yk, er, u, flags, total;
     int64_t ncmax;
 };
-GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype)
+// N sequences of at most maxlen tokens (the call's own, or the segments of
+// the sequence split, whose tokens are the same).
+GlaFwdWs gla_layout(const Problem &P, int32_t dtype, int64_t N, int64_t maxlen)
 {
     GlaFwdWs w{};
-    const int64_t maxlen = gla_max_len(P);
     // 128 key channels; the backward's dq~ and dk~ sweeps put the 64 or 128
     // value channels on TMEM lanes
     if (dtype != LA_DTYPE_BF16 || P.D != 128 || (P.E != 64 && P.E != 128) ||
-        maxlen <= la::SHORT_MAX_T || P.N > 65535 || P.H > 65535)
+        maxlen <= la::SHORT_MAX_T || N > 65535 || P.H > 65535)
         return w;
     w.ncmax = (maxlen + 127) / 128;
     const int64_t rows = P.packed ? 1 : P.B;
     const size_t tok = round256((size_t)rows * P.T * P.H * P.D * 2);
-    const size_t vec = round256((size_t)P.N * P.H * w.ncmax * P.D * 4);
+    const size_t vec = round256((size_t)N * P.H * w.ncmax * P.D * 4);
     w.xq = 0;
     w.yk = tok;
     w.er = 2 * tok;
     w.u = 2 * tok + vec;
     w.flags = 2 * tok + 2 * vec;
-    w.total = w.flags + round256((size_t)P.N * P.H * 4);
+    w.total = w.flags + round256((size_t)N * P.H * 4);
     return w;
+}
+GlaFwdWs gla_fwd_layout(const Problem &P, int32_t dtype)
+{
+    return gla_layout(P, dtype, P.N, gla_max_len(P));
+}
+
+// The gated forward's sequence split: the plan, its tables and per-segment
+// states (split_setup, at offset 0), each segment's log-decays per key
+// channel (lam, [NS][H][D] fp32), its chunks' totals (btot, [NS][H][ncmax][D]
+// fp32, from the pre-pass) and the chunked form's buffers for the segments
+// (prep).  total 0: no split.  gs: the gate's strides, which must allow the
+// one-row token view (NULL: assume they do, for sizing).
+struct GlaSplitWs {
+    SplitPlan S;
+    GlaFwdWs w;
+    size_t lam = 0, btot = 0, prep = 0, total = 0;
+};
+GlaSplitWs gla_split_layout(const Problem &P, const la_dims *d, int32_t dtype, const int64_t *gs)
+{
+    GlaSplitWs x;
+    if (gs && !(P.packed || P.B == 1 || gs[0] == (int64_t)P.T * gs[1]))
+        return x;
+    x.S = plan_split(P, d);
+    if (x.S.NS == 0)
+        return x;
+    x.w = gla_layout(P, dtype, x.S.NS, x.S.seg_len);
+    if (!x.w.total) {
+        x.S = SplitPlan{};
+        return x;
+    }
+    x.lam = round256(x.S.bytes);
+    x.btot = x.lam + round256((size_t)x.S.NS * P.H * P.D * 4);
+    x.prep = x.btot + round256((size_t)x.S.NS * P.H * x.w.ncmax * P.D * 4);
+    x.total = x.prep + x.w.total;
+    return x;
+}
+
+// The pre-pass's arguments for N sequences (or segments, cu their table) of
+// the T-token rows; its buffers from the layout w at ws.
+la::GlaPrepArgs gla_prep_args(const Problem &P, const la_dims *d, const void *q, const void *k,
+                              const float *g, const int64_t *gs, const float *g_gamma,
+                              int32_t reverse, uint8_t *ws, const GlaFwdWs &w, int N, int T,
+                              const int32_t *cu)
+{
+    la::GlaPrepArgs pa{};
+    pa.N = N;
+    pa.H = P.H;
+    pa.D = P.D;
+    pa.T = T;
+    pa.ncmax = w.ncmax;
+    pa.cu = cu;
+    pa.reverse = reverse ? 1 : 0;
+    pa.bf16 = 1;
+    pa.q = q;
+    pa.k = k;
+    pa.sb = d->qk_strides[0];
+    pa.st = d->qk_strides[1];
+    pa.sh = d->qk_strides[2];
+    pa.ksb = P.k_st[0];
+    pa.kst = P.k_st[1];
+    pa.ksh = P.k_st[2];
+    pa.khd = P.G;
+    pa.g = g;
+    pa.gsb = gs[0];
+    pa.gst = gs[1];
+    pa.gsh = gs[2];
+    pa.g_gamma = g_gamma;
+    pa.xq = ws + w.xq;
+    pa.yk = ws + w.yk;
+    pa.er = reinterpret_cast<float *>(ws + w.er);
+    pa.u = reinterpret_cast<float *>(ws + w.u);
+    pa.flags = reinterpret_cast<int *>(ws + w.flags);
+    pa.lim = 72.f;
+    return pa;
+}
+
+// The chunked form's forward sweep on the pre-pass's operands: X = q~,
+// Y = k~ (dense [rows][T][H][D]), Z = v, the state's rows gated; pairs the
+// pre-pass flagged are left to the token-by-token kernels.
+cudaError_t gla_chunked_sweep(const la::SweepArgs &a, const la::GlaPrepArgs &pa, int64_t ncmax,
+                              cudaStream_t s)
+{
+    la::SweepArgs t = a;
+    t.gate = la::Gate{};
+    t.gla_er = pa.er;
+    t.gla_u = pa.u;
+    t.gla_ncmax = ncmax;
+    t.gla_flags = pa.flags;
+    t.gla_flag_run = 0;
+    const int64_t dsh = a.D, dst = (int64_t)a.H * a.D, dsb = dst * a.T;
+    return la::tc_gla_sweep(t, false, false, la::Tok{pa.xq, dsb, dst, dsh, 1},
+                            la::Tok{pa.yk, dsb, dst, dsh, 1}, t.v, s);
+}
+
+// The gated forward split into segments (few long sequences): the pre-pass
+// over the segments (also giving each chunk's total log-decay), the
+// segments' log-decays from those, the sweep from zero states
+// (chunked, flagged segments token by token) into the per-segment states,
+// the scan with per-channel decays (which writes the final state), and the
+// sweep again from the scanned states for the outputs.  The operands are
+// laid out per segment, so they are not offered to the backward.
+la_status gla_fwd_split(const Problem &P, const la_dims *d, const GlaSplitWs &sw, la::SweepArgs a,
+                        const void *q, const void *k, const float *g, const int64_t *gs,
+                        const float *g_gamma, const float *initial_state, float *final_state,
+                        int32_t reverse, void *workspace, cudaStream_t s)
+{
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    SplitBufs b;
+    la_status st = split_setup(P, sw.S, workspace, 0, s, &b);
+    if (st != LA_OK)
+        return st;
+    float *lam = reinterpret_cast<float *>(ws + sw.lam);
+    uint8_t *pw = ws + sw.prep;
+    cudaError_t e = cudaMemsetAsync(pw + sw.w.flags, 0, (size_t)sw.S.NS * P.H * 4, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gated forward flags");
+    to_segments(&a, P, sw.S, b);
+    la::GlaPrepArgs pa = gla_prep_args(P, d, q, k, g, gs, g_gamma, reverse, pw, sw.w, sw.S.NS,
+                                       a.T, b.seg_cu);
+    pa.btot = reinterpret_cast<float *>(ws + sw.btot);
+    if ((e = la::gla_prepare(pa, s)) != cudaSuccess)
+        return cuda_fail(e, "gated forward operands");
+    la::SegDecayArgs sd{};
+    sd.NS = sw.S.NS;
+    sd.H = P.H;
+    sd.D = P.D;
+    sd.seg_cu = b.seg_cu;
+    sd.btot = pa.btot;
+    sd.ncmax = sw.w.ncmax;
+    sd.lam = lam;
+    if ((e = la::gla_segment_decay(sd, s)) != cudaSuccess)
+        return cuda_fail(e, "gated segment decays");
+    // two passes: from zero states into W, then from the scanned W
+    bool tc = true;
+    for (int pass = 0; pass < 2; ++pass) {
+        la::SweepArgs t = a;
+        t.s_in = pass ? la::StateIn{b.W, P.E, 1} : la::StateIn{nullptr, 0, 0};
+        t.s_out = pass ? la::StateOut{nullptr, 0, 0} : la::StateOut{b.W, P.E, 1};
+        if (tc) {
+            e = gla_chunked_sweep(t, pa, sw.w.ncmax, s);
+            if (e == cudaErrorNotSupported && pass == 0)
+                tc = false;   // every segment token by token, in both passes
+            else if (e != cudaSuccess)
+                return cuda_fail(e, "gated tensor-core sweep launch");
+        }
+        t.gla_flags = tc ? pa.flags : nullptr;
+        t.gla_flag_run = 1;
+        if ((st = short_run(t, false, s)))
+            return st;
+        if (pass == 0) {
+            la::SplitScanArgs sc =
+                scan_args(P, b, g_gamma, P.D, P.E, la::StateIn{initial_state, P.E, 1},
+                          la::StateOut{final_state, P.E, 1}, reverse != 0);
+            sc.lam = lam;   // the key channels are the state's rows
+            if ((st = scan(sc, s)))
+                return st;
+        }
+    }
+    return LA_OK;
 }
 
 // dq and dk of the gated backward go through fp32 workspace rows (dense
@@ -1032,7 +1192,10 @@ size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
     std::string keep = g_msg;
     la_status st = check_dims(dims, dtype, cu_seqlens_host, cu_seqlens_host, nullptr, &P);
     g_msg = keep;
-    return st == LA_OK ? gla_fwd_layout(P, dtype).total : 0;
+    if (st != LA_OK)
+        return 0;
+    return std::max(gla_fwd_layout(P, dtype).total,
+                    gla_split_layout(P, dims, dtype, nullptr).total);
 }
 
 la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
@@ -1067,63 +1230,30 @@ la_status la_gla_fwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     a.s_in = la::StateIn{initial_state, P.E, 1};
     a.s_out = la::StateOut{final_state, P.E, 1};
     a.gate = gate_of(g, g_strides, false);   // state rows are key channels
-    const GlaFwdWs w = gla_fwd_layout(P, dtype);
     // the operands are prepared two channels at a time: 8-byte gate pairs
     const bool gate_pairs = (reinterpret_cast<uintptr_t>(g) & 7) == 0 && g_strides[0] % 2 == 0 &&
                             g_strides[1] % 2 == 0 && g_strides[2] % 2 == 0;
-    if (w.total && workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) == 0 &&
-        workspace_bytes >= w.total && gate_pairs && la::tc_sweep_supported(a)) {
+    const bool ws_ok = workspace && (reinterpret_cast<uintptr_t>(workspace) & 255) == 0;
+    const bool chunked = ws_ok && gate_pairs && la::tc_sweep_supported(a);
+    const GlaSplitWs sw = gla_split_layout(P, dims, dtype, g_strides);
+    if (chunked && sw.total && workspace_bytes >= sw.total)
+        return gla_fwd_split(P, dims, sw, a, q, k, g, g_strides, g_gamma, initial_state,
+                             final_state, reverse, workspace, s);
+    const GlaFwdWs w = gla_fwd_layout(P, dtype);
+    if (chunked && w.total && workspace_bytes >= w.total) {
         // the chunked form on the tensor cores, for every (sequence, head)
         // whose gates stay in its range; the others token by token
         uint8_t *ws = static_cast<uint8_t *>(workspace);
-        int *flags = reinterpret_cast<int *>(ws + w.flags);
-        cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)P.N * P.H * 4, s);
+        cudaError_t e = cudaMemsetAsync(ws + w.flags, 0, (size_t)P.N * P.H * 4, s);
         if (e != cudaSuccess)
             return cuda_fail(e, "gated forward flags");
-        la::GlaPrepArgs pa{};
-        pa.N = P.N;
-        pa.H = P.H;
-        pa.D = P.D;
-        pa.T = P.T;
-        pa.ncmax = w.ncmax;
-        pa.cu = cu_seqlens;
-        pa.reverse = reverse ? 1 : 0;
-        pa.bf16 = 1;
-        pa.q = q;
-        pa.k = k;
-        pa.sb = dims->qk_strides[0];
-        pa.st = dims->qk_strides[1];
-        pa.sh = dims->qk_strides[2];
-        pa.ksb = P.k_st[0];
-        pa.kst = P.k_st[1];
-        pa.ksh = P.k_st[2];
-        pa.khd = P.G;
-        pa.g = g;
-        pa.gsb = g_strides[0];
-        pa.gst = g_strides[1];
-        pa.gsh = g_strides[2];
-        pa.g_gamma = g_gamma;
-        pa.xq = ws + w.xq;
-        pa.yk = ws + w.yk;
-        pa.er = reinterpret_cast<float *>(ws + w.er);
-        pa.u = reinterpret_cast<float *>(ws + w.u);
-        pa.flags = flags;
-        pa.lim = 72.f;
+        const la::GlaPrepArgs pa = gla_prep_args(P, dims, q, k, g, g_strides, g_gamma, reverse,
+                                                 ws, w, P.N, P.T, cu_seqlens);
         if ((e = la::gla_prepare(pa, s)) != cudaSuccess)
             return cuda_fail(e, "gated forward operands");
-        la::SweepArgs t = a;
-        t.gate = la::Gate{};
-        t.gla_er = pa.er;
-        t.gla_u = pa.u;
-        t.gla_ncmax = w.ncmax;
-        t.gla_flags = flags;
-        t.gla_flag_run = 0;
-        // X = q~, Y = k~ (dense [rows][T][H][D]), Z = v; state rows gated
-        const int64_t dsh = P.D, dst = (int64_t)P.H * P.D, dsb = dst * P.T;
-        e = la::tc_gla_sweep(t, false, false, la::Tok{pa.xq, dsb, dst, dsh, 1},
-                             la::Tok{pa.yk, dsb, dst, dsh, 1}, t.v, s);
+        e = gla_chunked_sweep(a, pa, w.ncmax, s);
         if (e == cudaSuccess) {
-            a.gla_flags = flags;
+            a.gla_flags = pa.flags;
             a.gla_flag_run = 1;
             if (operands_written)
                 *operands_written = 1;
@@ -1223,34 +1353,8 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
             cudaError_t e = ready ? cudaSuccess : cudaMemsetAsync(fl, 0, (size_t)P.N * P.H * 4, s);
             if (e != cudaSuccess)
                 return cuda_fail(e, "gated backward flags");
-            pa.N = P.N;
-            pa.H = P.H;
-            pa.D = P.D;
-            pa.T = P.T;
-            pa.ncmax = w.ncmax;
-            pa.cu = cu_seqlens;
-            pa.reverse = reverse ? 1 : 0;
-            pa.bf16 = 1;
-            pa.q = q;
-            pa.k = k;
-            pa.sb = dims->qk_strides[0];
-            pa.st = dims->qk_strides[1];
-            pa.sh = dims->qk_strides[2];
-            pa.ksb = P.k_st[0];
-            pa.kst = P.k_st[1];
-            pa.ksh = P.k_st[2];
-            pa.khd = P.G;
-            pa.g = g;
-            pa.gsb = g_strides[0];
-            pa.gst = g_strides[1];
-            pa.gsh = g_strides[2];
-            pa.g_gamma = g_gamma;
-            pa.xq = ws + w.xq;
-            pa.yk = ws + w.yk;
-            pa.er = reinterpret_cast<float *>(ws + w.er);
-            pa.u = reinterpret_cast<float *>(ws + w.u);
-            pa.flags = fl;
-            pa.lim = 72.f;
+            pa = gla_prep_args(P, dims, q, k, g, g_strides, g_gamma, reverse, ws, w, P.N, P.T,
+                               cu_seqlens);
             pa.dq = dq;
             pa.dk = dk;
             pa.dk32 = grouped ? dkf : nullptr;

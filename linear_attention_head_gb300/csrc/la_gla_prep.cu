@@ -70,8 +70,10 @@ template <> struct Pair<__nv_bfloat16> {
 // together, and their running sums stay in registers; the groups' totals are
 // combined through shared memory.  The factors exp(b - r), exp(r - b) use the
 // fast exponential: they are rounded to bf16 with their operands anyway.
+// KSEP: k has strides (or a head divisor) of its own; otherwise k is read at
+// q's offsets.
 constexpr int PG = 4, PT = PC / PG;   // token groups per chunk, tokens per group
-template <typename T>
+template <typename T, bool KSEP>
 __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
 {
     const int pc = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
@@ -102,13 +104,22 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
     {
         const int esz = (int)sizeof(T);
         if ((c * esz) % 128 == 0) {
-            const char *qr = reinterpret_cast<const char *>(
-                static_cast<const T *>(a.q) + row * a.sb + (int64_t)h * a.sh + c);
-            const char *kr = reinterpret_cast<const char *>(
-                static_cast<const T *>(a.k) + row * a.ksb + (int64_t)(h / a.khd) * a.ksh + c);
-            for (int j = 0; j < np; ++j) {
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + (tb + j * ts) * a.st * esz));
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + (tb + j * ts) * a.kst * esz));
+            const int64_t qo = row * a.sb + (int64_t)h * a.sh + c;
+            const char *qr = reinterpret_cast<const char *>(static_cast<const T *>(a.q) + qo);
+            if (KSEP) {
+                const char *kr = reinterpret_cast<const char *>(
+                    static_cast<const T *>(a.k) + row * a.ksb + (int64_t)(h / a.khd) * a.ksh + c);
+                for (int j = 0; j < np; ++j) {
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + (tb + j * ts) * a.st * esz));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + (tb + j * ts) * a.kst * esz));
+                }
+            } else {
+                const char *kr = reinterpret_cast<const char *>(static_cast<const T *>(a.k) + qo);
+                for (int j = 0; j < np; ++j) {
+                    const int64_t off = (tb + j * ts) * a.st * esz;
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + off));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + off));
+                }
             }
         }
     }
@@ -174,18 +185,22 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
             make_float2(okx ? expf(r.x) : 0.f, oky ? expf(r.y) : 0.f);
         *reinterpret_cast<float2 *>(a.u + vi) =
             make_float2(okx ? expf(B.x - r.x) : 0.f, oky ? expf(B.y - r.y) : 0.f);
+        if (a.btot)
+            *reinterpret_cast<float2 *>(a.btot + vi) = B;
     }
 
     // pass 2: q~ = q exp(b - r), k~ = k exp(r - b); zeros when out of range
     const T *qp = static_cast<const T *>(a.q) + row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
-    const T *kp = static_cast<const T *>(a.k) + row * a.ksb + (int64_t)(h / a.khd) * a.ksh + c +
-                  tb * a.kst;
+    const T *kp = KSEP ? static_cast<const T *>(a.k) + row * a.ksb +
+                             (int64_t)(h / a.khd) * a.ksh + c + tb * a.kst
+                       : static_cast<const T *>(a.k) + row * a.sb + (int64_t)h * a.sh + c +
+                             tb * a.st;
     const int64_t dst = (int64_t)a.H * a.D;   // token stride of the dense outputs
     __nv_bfloat162 *xq = reinterpret_cast<__nv_bfloat162 *>(
         static_cast<__nv_bfloat16 *>(a.xq) + ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst);
     __nv_bfloat162 *yk = reinterpret_cast<__nv_bfloat162 *>(
         static_cast<__nv_bfloat16 *>(a.yk) + ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst);
-    const int64_t istep = ts * a.st, kstep = ts * a.kst, ostep = ts * dst / 2;
+    const int64_t istep = ts * a.st, kstep = KSEP ? ts * a.kst : istep, ostep = ts * dst / 2;
     const float2 sh0 = make_float2(off.x - r.x, off.y - r.y);
     // eight tokens' q, k pairs loaded together (indices clamped into the
     // group), then scaled and stored
@@ -225,9 +240,11 @@ __global__ void __launch_bounds__(PG * 64, 2) gla_prep_kernel(GlaPrepArgs a)
 // as the pre-pass formed them (the same definitions; the sums grouped
 // differently, so they may differ in the last bits: dq and dk take their
 // factor exp(b - r) from them, dg does not).
+// DKM: where dk goes -- 0 at q's offsets (k shares q's strides), 1 at k's
+// own strides, 2 to a.dk32 in fp32, in place of dk~ (grouped key/value heads).
 constexpr int UG = 16, UT = PC / UG, UCP = 8;   // token groups, tokens per group, channel pairs
-template <typename T>
-__global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
+template <typename T, int DKM>
+__global__ void __launch_bounds__(UG * UCP, 4) gla_undo_kernel(GlaPrepArgs a)
 {
     const int cg = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int cp = threadIdx.x % UCP, grp = threadIdx.x / UCP;
@@ -279,7 +296,6 @@ __global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
         const int64_t ts = rev ? -1 : 1;
         const float *gp = a.g + row * a.gsb + (int64_t)h * a.gsh + c + tb * a.gst;
         const int64_t qo = row * a.sb + (int64_t)h * a.sh + c + tb * a.st;
-        const int64_t ko = row * a.ksb + (int64_t)h * a.ksh + c + tb * a.kst;
         const int64_t fo = ((int64_t)row * a.T * a.H + h) * a.D + c + tb * dst;
         float2 b[UT], dqv[UT], dkv[UT], qv[UT], kv[UT];
 #pragma unroll
@@ -331,7 +347,10 @@ __global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
         // dq, dk, and the terms q~ dq~ - k~ dk~ (the rounded operands and
         // their own gradients) into b[]
         T *dqp = static_cast<T *>(a.dq) + qo;
-        T *dkp = a.dk32 ? nullptr : static_cast<T *>(a.dk) + ko;
+        T *dkp = DKM == 2   ? nullptr
+                 : DKM == 1 ? static_cast<T *>(a.dk) + row * a.ksb + (int64_t)h * a.ksh + c +
+                                  tb * a.kst
+                            : static_cast<T *>(a.dk) + qo;
         float2 gt = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < UT; ++j) {
@@ -341,10 +360,10 @@ __global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
                 Pair<T>::store(dqp + j * ts * a.st,
                                make_float2(dqv[j].x * __expf(ex), dqv[j].y * __expf(ey)));
                 const float2 dkj = make_float2(dkv[j].x * __expf(-ex), dkv[j].y * __expf(-ey));
-                if (dkp)
-                    Pair<T>::store(dkp + j * ts * a.kst, dkj);
-                else   // this thread read dk~ here above: overwritten in place
+                if (DKM == 2)   // this thread read dk~ here above: overwritten in place
                     *reinterpret_cast<float2 *>(a.dk32 + fo + j * ts * dst) = dkj;
+                else
+                    Pair<T>::store(dkp + j * ts * (DKM == 1 ? a.kst : a.st), dkj);
                 tm = make_float2(qv[j].x * dqv[j].x - kv[j].x * dkv[j].x,
                                  qv[j].y * dqv[j].y - kv[j].y * dkv[j].y);
             }
@@ -382,7 +401,34 @@ __global__ void __launch_bounds__(UG * UCP) gla_undo_kernel(GlaPrepArgs a)
     }
 }
 
+// One CTA per (segment, head), one thread per key channel: the segment's
+// chunk totals summed in chunk order.
+__global__ void __launch_bounds__(256) seg_decay_kernel(SegDecayArgs a)
+{
+    const int seg = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+    if (c >= a.D)
+        return;
+    const int64_t len = (int64_t)a.seg_cu[seg + 1] - a.seg_cu[seg];
+    const int nc = (int)((len + PC - 1) / PC);
+    const float *bp = a.btot + ((int64_t)seg * a.H + h) * a.ncmax * a.D + c;
+    float acc = 0.f;
+    for (int pc = 0; pc < nc && pc < a.ncmax; ++pc)
+        acc += bp[(int64_t)pc * a.D];
+    a.lam[((int64_t)seg * a.H + h) * a.D + c] = acc;
+}
+
 }  // namespace
+
+cudaError_t gla_segment_decay(const SegDecayArgs &a, cudaStream_t s)
+{
+    if (a.NS == 0 || a.H == 0)
+        return cudaSuccess;
+    if (a.D > 256 || a.H > 65535)
+        return cudaErrorNotSupported;
+    seg_decay_kernel<<<dim3((unsigned)a.NS, (unsigned)a.H), (a.D + 31) / 32 * 32, 0, s>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s)
 {
@@ -392,10 +438,15 @@ cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s)
         return cudaErrorNotSupported;
     dim3 grid((unsigned)a.ncmax, (unsigned)a.H, (unsigned)a.N);
     const int threads = PG * 64;
-    if (a.bf16)
-        gla_prep_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(a);
+    const bool ksep = a.khd != 1 || a.ksb != a.sb || a.kst != a.st || a.ksh != a.sh;
+    if (a.bf16 && ksep)
+        gla_prep_kernel<__nv_bfloat16, true><<<grid, threads, 0, s>>>(a);
+    else if (a.bf16)
+        gla_prep_kernel<__nv_bfloat16, false><<<grid, threads, 0, s>>>(a);
+    else if (ksep)
+        gla_prep_kernel<float, true><<<grid, threads, 0, s>>>(a);
     else
-        gla_prep_kernel<float><<<grid, threads, 0, s>>>(a);
+        gla_prep_kernel<float, false><<<grid, threads, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }
@@ -407,10 +458,16 @@ cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s)
     if (a.D != 128 || a.N > 65535 || a.H > 65535)
         return cudaErrorNotSupported;
     dim3 grid((unsigned)(a.D / (2 * UCP)), (unsigned)a.H, (unsigned)a.N);
+    const int dkm = a.dk32 ? 2 : (a.ksb != a.sb || a.kst != a.st || a.ksh != a.sh) ? 1 : 0;
+    auto launch = [&](auto kern) { kern<<<grid, UG * UCP, 0, s>>>(a); };
     if (a.bf16)
-        gla_undo_kernel<__nv_bfloat16><<<grid, UG * UCP, 0, s>>>(a);
+        dkm == 2   ? launch(gla_undo_kernel<__nv_bfloat16, 2>)
+        : dkm == 1 ? launch(gla_undo_kernel<__nv_bfloat16, 1>)
+                   : launch(gla_undo_kernel<__nv_bfloat16, 0>);
     else
-        gla_undo_kernel<float><<<grid, UG * UCP, 0, s>>>(a);
+        dkm == 2   ? launch(gla_undo_kernel<float, 2>)
+        : dkm == 1 ? launch(gla_undo_kernel<float, 1>)
+                   : launch(gla_undo_kernel<float, 0>);
     note_launch();
     return cudaGetLastError();
 }

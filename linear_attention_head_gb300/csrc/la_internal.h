@@ -103,6 +103,8 @@ struct GlaPrepArgs {
     void *xq, *yk;            // bf16 [rows][T][H][D]: q~ and k~
     float *er, *u;            // [N][H][ncmax][D]
     int *flags;               // [N H], zeroed beforehand
+    float *btot = nullptr;    // gla_prepare, when set: each chunk's total log-decay
+                              // per channel, [N][H][ncmax][D]
     float lim;                // largest |b - r| (and |r|) the chunked form takes
     void *dq, *dk;            // gla_undo: dq, dk out (token dtype, their strides)
     const float *dqf, *dkf;   // gla_undo: dq~, dk~ in (fp32, dense [rows][T][H][D])
@@ -119,6 +121,18 @@ cudaError_t gla_prepare(const GlaPrepArgs &a, cudaStream_t s);
 // the (sequence, head) pairs not flagged: one pass over each sequence against
 // the processing order, the later chunks' terms carried in registers.
 cudaError_t gla_undo(const GlaPrepArgs &a, cudaStream_t s);
+// Each segment's total log-decay per key channel (the gated form's sequence
+// split): lam[seg][h][c] = the sum over the segment's chunks of their totals
+// btot[seg][h][chunk][c] (gla_prepare over the segments: len * g_gamma[h]
+// plus the segment's gates).  D <= 256.
+struct SegDecayArgs {
+    int NS, H, D;
+    const int32_t *seg_cu;
+    const float *btot;
+    int64_t ncmax;
+    float *lam;
+};
+cudaError_t gla_segment_decay(const SegDecayArgs &a, cudaStream_t s);
 // A tensor-core sweep of the gated form on rescaled operands (la_gla_prep.cu)
 // with tile roles X, Y, Z given (bf16, D = 128 X and Y width): forward-type or
 // backward-type (bwd), the gated key channels being the state's rows or its
@@ -216,6 +230,10 @@ cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s);
 // seg_cu[s+1] - seg_cu[s], visited in token order (or reversed).  start is the
 // sequence's initial state (zero when null) and fin receives its final state
 // (skipped when null), both with the StateIn / StateOut indexing.
+// With lam set (the gated form) a segment's decay is per key channel:
+// element (r, c) takes exp(lam[seg][h][r]) (lam_cols == 0: the key channels
+// are the rows, lam [NS][H][D]) or exp(lam[seg][h][c]) (lam_cols: columns,
+// lam [NS][H][E]) instead of gamma^L.
 struct SplitScanArgs {
     int N, H, D, E;
     const int32_t *seg_cu;      // device [NS + 1]
@@ -225,6 +243,8 @@ struct SplitScanArgs {
     StateIn start;
     StateOut fin;
     int descending;
+    const float *lam = nullptr;
+    int lam_cols = 0;
 };
 cudaError_t split_scan(const SplitScanArgs &a, cudaStream_t s);
 

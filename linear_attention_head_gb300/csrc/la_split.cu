@@ -11,7 +11,10 @@
 // first pass computes F for every segment (zero initial states, all segments
 // in parallel), this scan turns the F into each segment's true initial state
 // and the sequence's final state, and a second pass runs every segment again
-// from its initial state.  The scan is elementwise in the state, so one
+// from its initial state.  With the gated form's per-key gate the segment's
+// decay is a diagonal, exp(lam) per key channel (the sum of the log-decays
+// over the segment), on the state's rows or columns: still elementwise.
+// The scan is elementwise in the state, so one
 // thread owns one state element of one (sequence, head) and walks that
 // sequence's segments in visiting order.
 
@@ -40,7 +43,11 @@ __global__ void __launch_bounds__(256) split_scan_kernel(SplitScanArgs a)
         const float f = *w;
         *w = carry;   // the segment's initial state
         const int len = a.seg_cu[seg + 1] - a.seg_cu[seg];
-        carry = fmaf(expf(g * (float)len), carry, f);
+        const float decay =
+            a.lam ? expf(a.lam[((int64_t)seg * a.H + h) * (a.lam_cols ? a.E : a.D) +
+                               (a.lam_cols ? c : r)])
+                  : expf(g * (float)len);
+        carry = fmaf(decay, carry, f);
     }
     if (a.fin.p)
         a.fin.p[user + r * a.fin.rs + c * a.fin.cs] = carry;

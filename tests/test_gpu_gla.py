@@ -345,3 +345,55 @@ def test_gated_grouped_heads_autograd():
     ref = _group_sums(dict(o=ro, dq=rq, dk=rk, dv=rv, dg=rg), G)
     compare(dict(o=o.detach().cpu(), dq=q.grad.cpu(), dk=k.grad.cpu(), dv=v.grad.cpu(),
                  dg=g.grad.cpu()), ref, TOL[torch.bfloat16], label="gated grouped autograd")
+
+
+def test_gated_keys_with_strides_of_their_own_through_the_c_abi():
+    # kv_heads = H with k (and dk) head-major while q is token-major: the
+    # pre-pass reads k, and the rescaling pass writes dk, at k's own strides.
+    # Same values as the call on a token-major k, bit for bit.
+    import ctypes
+    from linear_attention_head_gb300 import api as A
+    x = _inputs(2, 300, 3, 128, 128, torch.bfloat16, seed=31)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    ref_o, ref_f = la.gla_fwd(d["q"], d["k"], d["v"], d["g"], d["g_gamma"], d["scale"],
+                              d["initial_state"])
+    ref_b = la.gla_bwd(d["q"], d["k"], d["v"], d["do"], d["g"], d["g_gamma"], d["scale"],
+                       d["initial_state"], d["d_final_state"])
+    B, T, H, D = d["q"].shape
+    k_hm = d["k"].permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)   # [B,T,H,D] view
+    dk_hm = torch.empty((B, H, T, D), dtype=torch.bfloat16, device="cuda").permute(0, 2, 1, 3)
+    dims = N.LaDims()
+    dims.batch, dims.seq_len, dims.heads, dims.dim_qk, dims.dim_v = B, T, H, D, 128
+    dims.num_seqs, dims.kv_heads = 0, H
+    for i in range(3):
+        dims.qk_strides[i] = d["q"].stride(i)
+        dims.v_strides[i] = d["v"].stride(i)
+        dims.k_strides[i] = k_hm.stride(i)
+        dims.kv_v_strides[i] = d["v"].stride(i)
+    lib, st = N.lib(), A._stream(torch.device("cuda"))
+    o, fin = torch.empty_like(d["v"]), torch.empty_like(ref_f)
+    nb = int(lib.la_gla_fwd_workspace_size(ctypes.byref(dims), N.LA_DTYPE_BF16, None))
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    written = ctypes.c_int32(0)
+    N.check(lib.la_gla_fwd(ctypes.byref(dims), N.LA_DTYPE_BF16, A._ptr(d["q"]), A._ptr(k_hm),
+                           A._ptr(d["v"]), A._ptr(d["g"]), A._strides3(d["g"]),
+                           A._ptr(d["g_gamma"]), float(d["scale"]), A._ptr(d["initial_state"]),
+                           0, None, None, A._ptr(o), A._ptr(fin), A._ptr(ws), nb,
+                           ctypes.byref(written), st))
+    assert written.value == 1
+    dq, dv = torch.empty_like(d["q"]), torch.empty_like(d["v"])
+    dg, dinit = torch.empty_like(d["g"]), torch.empty_like(ref_f)
+    nb2 = int(lib.la_gla_workspace_size(ctypes.byref(dims), N.LA_DTYPE_BF16, None, 0))
+    ws2 = torch.empty(nb2, dtype=torch.uint8, device="cuda")
+    N.check(lib.la_gla_bwd(ctypes.byref(dims), N.LA_DTYPE_BF16, A._ptr(d["q"]), A._ptr(k_hm),
+                           A._ptr(d["v"]), A._ptr(d["do"]), A._ptr(d["g"]), A._strides3(d["g"]),
+                           A._ptr(d["g_gamma"]), float(d["scale"]), A._ptr(d["initial_state"]),
+                           A._ptr(d["d_final_state"]), 0, None, None, A._ptr(dq), A._ptr(dk_hm),
+                           A._ptr(dv), A._ptr(dg), A._ptr(dinit), A._ptr(ws2), nb2, None, 0, st))
+    torch.cuda.synchronize()
+    la.get_device_error()
+    got = dict(o=o, final_state=fin, dq=dq, dk=dk_hm, dv=dv, dg=dg, d_initial_state=dinit)
+    ref = dict(o=ref_o, final_state=ref_f, dq=ref_b[0], dk=ref_b[1], dv=ref_b[2], dg=ref_b[3],
+               d_initial_state=ref_b[4])
+    for name in got:
+        assert torch.equal(got[name], ref[name]), name

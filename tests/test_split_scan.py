@@ -81,3 +81,56 @@ def test_split_passes_around_a_state_scan_equal_the_unsplit_run(seg, reverse):
         r = np.asarray(r)
         err = np.max(np.abs(got[name] - r)) / np.max(np.abs(r))
         assert err <= 1e-12, (name, err)
+
+
+def _gated_split_forward(x, seg, reverse, gates_in_decay=True):
+    """The gated forward split: per segment, its state from zero (oracle) and
+    its log-decay per key channel (len * g_gamma + the sum of its gates); the
+    scan carry <- diag(exp(lam)) carry + F in visiting order; pass 2 from the
+    scanned states.  gates_in_decay=False plants a mistake: the scan's decay
+    without the gates' sum."""
+    q, k, v, gt = (x[n] for n in ("q", "k", "v", "g"))
+    gg, s, S0 = x["g_gamma"], x["scale"], x["initial_state"]
+    T = q.shape[1]
+    segs = _seg_bounds(T, seg)
+    visit = segs[::-1] if reverse else segs
+    part = lambda t, a, b: t[:, a:b].contiguous()
+    F, lam = {}, {}
+    for a, b in segs:
+        _, F[a] = oracle.gla_forward(part(q, a, b), part(k, a, b), part(v, a, b),
+                                     part(gt, a, b), gg, s, None, reverse)
+        lam[a] = (b - a) * gg.double()[None, :, None] + \
+            (gt[:, a:b].double().sum(1) if gates_in_decay else 0.0)   # [B, H, d]
+    Win, carry = {}, S0.double()
+    for a, b in visit:
+        Win[a] = carry
+        carry = torch.exp(lam[a])[..., None] * carry + torch.as_tensor(F[a])
+    o = np.zeros(q.shape[:3] + v.shape[3:])
+    for a, b in segs:
+        o[:, a:b], _ = oracle.gla_forward(part(q, a, b), part(k, a, b), part(v, a, b),
+                                          part(gt, a, b), gg, s, Win[a], reverse)
+    return o, carry.numpy()
+
+
+@pytest.mark.parametrize("seg", [1, 6, 16])
+@pytest.mark.parametrize("reverse", [False, True])
+def test_gated_split_scans_with_per_channel_decays(seg, reverse):
+    # the gated form's segment decay is a diagonal (one factor per key
+    # channel, the state's rows), so the scan stays elementwise
+    x = W.random_small(13, 2, 40, 3, 4, 5, g_lo=-0.5, g_hi=0.0)
+    gen = torch.Generator().manual_seed(14)
+    x["g"] = -0.6 * torch.rand(x["q"].shape, generator=gen, dtype=torch.float64)
+    x["initial_state"] = torch.randn((2, 3, 4, 5), generator=gen, dtype=torch.float64)
+    x["scale"] = 0.8
+    o, fin = _gated_split_forward(x, seg, reverse)
+    ro, rfin = oracle.gla_forward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"], x["scale"],
+                                  x["initial_state"], reverse)
+    assert np.abs(o - np.asarray(ro)).max() <= 1e-12 * max(1.0, np.abs(ro).max())
+    assert np.abs(fin - np.asarray(rfin)).max() <= 1e-12 * max(1.0, np.abs(rfin).max())
+    # the scan with the head's decay gamma^L alone (the gates left out) fails
+    if len(_seg_bounds(40, seg)) > 1:
+        o_bad, fin_bad = _gated_split_forward(x, seg, reverse, gates_in_decay=False)
+        # (the older state has mostly decayed over a segment, so the outputs
+        # move by 1e-3 of their maximum or less: far above the 1e-12 match)
+        assert np.abs(o_bad - np.asarray(ro)).max() > 1e-6 * np.abs(ro).max()
+        assert np.abs(fin_bad - np.asarray(rfin)).max() > 1e-6 * np.abs(rfin).max()
