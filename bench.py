@@ -788,33 +788,44 @@ def gla_bench(la, torch, dev, stream, peak):
            "tokens_per_s": B * T / (s_ms * 1e-3),
            "fwd_frac_of_peak": (4 * unit + 2 * unit) / (f_ms * 1e-3) / 1e9 / peak,
            "bwd_frac_of_peak": (7 * unit + 4 * unit) / (b_ms * 1e-3) / 1e9 / peak}
-    out["long_sequence_fwd"] = gla_long_bench(la, torch, dev, timed, peak)
+    out["long_sequence"] = gla_long_bench(la, torch, dev, timed, peak)
     return out
 
 
 def gla_long_bench(la, torch, dev, timed, peak):
-    """The gated forward on one long sequence with few heads (b1 h8 n262144
+    """The gated form on one long sequence with few heads (b1 h8 n262144
     d=e=128 bf16, fp32 gate): 8 (sequence, head) pairs for 152 SMs, with the
-    sequence split (segment decays, pre-pass, two passes around the scan with
-    per-channel decays) and without it.  Algorithmic bytes: q, k, v, g read
-    (the gate fp32), o written."""
+    sequence split (segment decays, pre-pass, passes around scans with
+    per-channel decays, dg offsets per segment) and without it.  gla_fwd alone,
+    and a training step: gla_fwd then gla_bwd (unsplit, the backward reuses
+    the forward's operands; split, it computes its own).  Algorithmic bytes:
+    forward q, k, v, g read (the gate fp32), o written; backward q, k, v, do,
+    g read, dq, dk, dv, dg written."""
     import workloads as W
     from linear_attention_head_gb300 import _native
     B, T, H, D = 1, 262144, 8, 128
     gg = W.alibi_g_gamma(H).to(dev)
     gen = torch.Generator(device=dev).manual_seed(23)
-    q, k, v = (torch.randn((B, T, H, D), generator=gen, device=dev).bfloat16() for _ in range(3))
+    q, k, v, do = (torch.randn((B, T, H, D), generator=gen, device=dev).bfloat16()
+                   for _ in range(4))
     g = -0.3 * torch.rand((B, T, H, D), generator=gen, device=dev)
-    out = {"workload": "gla_fwd b1 h8 n262144 d=e=128 bf16 tokens, fp32 per-key gate"}
-    nbytes = 6 * B * T * H * D * 2
+
+    def step():
+        o, fin, ops = la.gla_fwd(q, k, v, g, gg, 1.0, keep_operands=True)
+        la.gla_bwd(q, k, v, do, g, gg, 1.0, want_d_initial_state=False, operands=ops)
+
+    out = {"workload": "gla_fwd + gla_bwd b1 h8 n262144 d=e=128 bf16 tokens, fp32 per-key gate"}
+    unit = B * T * H * D * 2
     for name, mode in (("split", 1), ("unsplit", 0)):
         _native.check(_native.lib().la_set_sequence_split(mode, 0))
-        ms = timed(lambda: la.gla_fwd(q, k, v, g, gg, 1.0))
-        out[name] = {"ms": ms, "tokens_per_s": B * T / (ms * 1e-3),
-                     "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak}
+        f_ms = timed(lambda: la.gla_fwd(q, k, v, g, gg, 1.0))
+        s_ms = timed(step)
+        out[name] = {"fwd_ms": f_ms, "step_ms": s_ms, "tokens_per_s": B * T / (s_ms * 1e-3),
+                     "fwd_frac_of_peak": 6 * unit / (f_ms * 1e-3) / 1e9 / peak,
+                     "bwd_frac_of_peak": 11 * unit / ((s_ms - f_ms) * 1e-3) / 1e9 / peak}
     _native.check(_native.lib().la_set_sequence_split(1, 0))
     la.get_device_error(dev)
-    del q, k, v, g
+    del q, k, v, do, g
     return out
 
 

@@ -1181,6 +1181,288 @@ GlaBwdWs gla_bwd_layout(const Problem &P, const la_dims *d, int32_t dtype)
     return w;
 }
 
+// Whether the gated backward's chunked form can take these tensors: 16-byte
+// aligned token rows for its tensor maps and 8-byte gate pairs.
+bool gla_bwd_chunkable(const Problem &P, const la_dims *d, const void *q, const void *k,
+                       const void *v, const void *d_o, const void *dq, const void *dk,
+                       const void *dv, const float *g, const int64_t *gs, const float *dg)
+{
+    auto al = [](const void *p, const int64_t *st) {
+        return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && st[0] % 8 == 0 && st[1] % 8 == 0 &&
+               st[2] % 8 == 0;
+    };
+    const bool aligned = al(q, d->qk_strides) && al(k, P.k_st) && al(dq, d->qk_strides) &&
+                         al(dk, P.k_st) && al(v, P.kv_v_st) && al(d_o, d->v_strides) &&
+                         al(dv, P.kv_v_st);
+    const bool gate_pairs = (reinterpret_cast<uintptr_t>(g) & 7) == 0 &&
+                            (reinterpret_cast<uintptr_t>(dg) & 7) == 0 && gs[0] % 2 == 0 &&
+                            gs[1] % 2 == 0 && gs[2] % 2 == 0;
+    return aligned && gate_pairs;
+}
+
+// Workspace of the gated backward's split: the split tables and one state per
+// (segment, head) (W: the dq~ sweep's, then dv's, whose transposes dk~ takes),
+// the segments' log-decays, their chunks' totals, each segment's sum of dg's
+// terms and its dg offset, the gate gradient's block sums per segment, the
+// per-sequence part of la_gla_bwd's own layout (final state, fp32 dq, dk,
+// grouped dv parts; base) and the pre-pass buffers for the segments (prep).
+struct GlaBwdSplitWs {
+    SplitPlan S;
+    GlaFwdWs w;
+    GlaBwdWs bw;
+    int64_t nblk = 0;
+    size_t lam = 0, btot = 0, segtot = 0, off = 0, bsum = 0, base = 0, prep = 0, total = 0;
+};
+GlaBwdSplitWs gla_bwd_split_layout(const Problem &P, const la_dims *d, int32_t dtype,
+                                   const int64_t *gs)
+{
+    GlaBwdSplitWs x;
+    if (gs && !(P.packed || P.B == 1 || gs[0] == (int64_t)P.T * gs[1]))
+        return x;
+    x.S = plan_split(P, d);
+    if (x.S.NS == 0)
+        return x;
+    x.w = gla_layout(P, dtype, x.S.NS, x.S.seg_len);
+    if (!x.w.total) {
+        x.S = SplitPlan{};
+        return x;
+    }
+    x.bw = gla_bwd_layout(P, d, dtype);
+    x.nblk = (x.S.seg_len + la::DG_TB - 1) / la::DG_TB;
+    const size_t vec = round256((size_t)x.S.NS * P.H * P.D * 4);
+    x.lam = round256(x.S.bytes);
+    x.btot = x.lam + vec;
+    x.segtot = x.btot + round256((size_t)x.S.NS * P.H * x.w.ncmax * P.D * 4);
+    x.off = x.segtot + vec;
+    x.bsum = x.off + vec;
+    x.base = x.bsum + round256((size_t)x.S.NS * P.H * x.nblk * P.D * 4);
+    x.prep = x.base + x.bw.total;
+    x.total = x.prep + x.w.total;
+    return x;
+}
+
+// The gated backward split into segments: the pre-pass over the segments
+// (with the chunk totals) and the segments' log-decays; dq~ in two passes
+// around a scan with column decays (which gives the final state, transposed,
+// for dg); dv in two passes around a scan against the processing order with
+// row decays (which gives d_initial_state); dk~ in one pass from the scanned
+// G, transposed; the rescaling pass per segment (dq, dk, and dg from the
+// segment's own terms, with each segment's total); the flagged segments'
+// dg from the block scan; then each segment's dg offset (the later
+// segments' totals and the final state's term) added.  Flagged segments run
+// token by token in every pass.
+la_status gla_bwd_split(const Problem &P, const la_dims *d, int32_t dtype, const GlaBwdSplitWs &sx,
+                        la::SweepArgs a, const void *q, const void *k, const void *v,
+                        const void *d_o, const float *g, const int64_t *gs, const float *g_gamma,
+                        const float *initial_state, const float *d_final_state, int32_t reverse,
+                        void *dq, void *dk, void *dv, float *dg, float *d_initial_state,
+                        uint8_t *ws, cudaStream_t s)
+{
+    SplitBufs b;
+    la_status st = split_setup(P, sx.S, ws, 0, s, &b);
+    if (st != LA_OK)
+        return st;
+    float *lam = reinterpret_cast<float *>(ws + sx.lam);
+    uint8_t *base = ws + sx.base;
+    float *Ft = reinterpret_cast<float *>(base);
+    float *dqf = reinterpret_cast<float *>(base + sx.bw.dqf);
+    float *dkf = reinterpret_cast<float *>(base + sx.bw.dkf);
+    const bool grouped = P.G > 1;
+    to_segments(&a, P, sx.S, b);   // the one-row view, segments as sequences
+    const int64_t fsh = P.D, fst = (int64_t)P.H * P.D, fsb = fst * a.T;
+    const int64_t vsh = P.E, vst = (int64_t)P.H * P.E, vsb = vst * a.T;
+    const la::TokOut dvo =
+        grouped ? la::TokOut{base + sx.bw.cv, vsb, vst, vsh} : tok_out(dv, P.kv_v_st);
+    uint8_t *pw = ws + sx.prep;
+    cudaError_t e = cudaMemsetAsync(pw + sx.w.flags, 0, (size_t)sx.S.NS * P.H * 4, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "gated backward flags");
+    la::GlaPrepArgs pa = gla_prep_args(P, d, q, k, g, gs, g_gamma, reverse, pw, sx.w, sx.S.NS,
+                                       a.T, b.seg_cu);
+    pa.btot = reinterpret_cast<float *>(ws + sx.btot);
+    if ((e = la::gla_prepare(pa, s)) != cudaSuccess)
+        return cuda_fail(e, "gated backward operands");
+    la::SegDecayArgs sd{};
+    sd.NS = sx.S.NS;
+    sd.H = P.H;
+    sd.D = P.D;
+    sd.seg_cu = b.seg_cu;
+    sd.btot = pa.btot;
+    sd.ncmax = sx.w.ncmax;
+    sd.lam = lam;
+    if ((e = la::gla_segment_decay(sd, s)) != cudaSuccess)
+        return cuda_fail(e, "gated segment decays");
+    const int64_t dsh = P.D, dst = (int64_t)P.H * P.D, dsb = dst * a.T;
+    const la::Tok tq{pa.xq, dsb, dst, dsh, 1}, tk{pa.yk, dsb, dst, dsh, 1};
+    const la::Tok tdo = tok(d_o, d->v_strides), tv = tok(v, P.kv_v_st, P.G);
+    // one sweep: the chunked form (x, y, z tiles) for the pairs in range, the
+    // token-by-token kernels (u's tiles and gate) for the flagged ones
+    auto sweep = [&](la::SweepArgs t, la::SweepArgs u, bool bwd, bool cols, const la::Tok &x,
+                     const la::Tok &y, const la::Tok &z) -> la_status {
+        t.gate = la::Gate{};
+        t.gla_er = pa.er;
+        t.gla_u = pa.u;
+        t.gla_ncmax = sx.w.ncmax;
+        t.gla_flags = pa.flags;
+        t.gla_flag_run = 0;
+        cudaError_t err = la::tc_gla_sweep(t, bwd, cols, x, y, z, s);
+        if (err != cudaSuccess)
+            return cuda_fail(err, "gated tensor-core sweep launch");
+        u.gla_flags = pa.flags;
+        u.gla_flag_run = 1;
+        return short_run(u, bwd, s);
+    };
+    la::SweepArgs t = a, u = a;
+    // dq~ (fp32): forward-type (do, v, k~); S^T with gated columns
+    t.D = u.D = P.E;
+    t.E = u.E = P.D;
+    t.out = u.out = la::TokOut{dqf, fsb, fst, fsh};
+    u.out_f32 = 1;
+    u.q = tdo;
+    u.k = tv;
+    u.v = tok(k, P.k_st, P.G);
+    u.gate = gate_of(g, gs, true);
+    for (int pass = 0; pass < 2; ++pass) {
+        t.s_in = u.s_in = pass ? la::StateIn{b.W, P.D, 1} : la::StateIn{nullptr, 0, 0};
+        t.s_out = u.s_out = pass ? la::StateOut{nullptr, 0, 0} : la::StateOut{b.W, P.D, 1};
+        if ((st = sweep(t, u, false, true, tdo, tv, tk)))
+            return st;
+        if (pass == 0) {
+            la::SplitScanArgs sc =
+                scan_args(P, b, g_gamma, P.E, P.D, la::StateIn{initial_state, 1, P.E},
+                          la::StateOut{Ft, P.D, 1}, reverse != 0);
+            sc.lam = lam;
+            sc.lam_cols = 1;   // the key channels are S^T's columns
+            if ((st = scan(sc, s)))
+                return st;
+        }
+    }
+    // dv: backward-type (k~, q~, do); G with gated rows, scanned against the
+    // processing order from d_final_state
+    t = a;
+    u = a;
+    t.D = u.D = P.D;
+    t.E = u.E = P.E;
+    t.out = u.out = dvo;
+    u.q = tok(q, d->qk_strides);
+    u.k = tok(k, P.k_st, P.G);
+    u.v = tdo;
+    u.gate = gate_of(g, gs, false);
+    for (int pass = 0; pass < 2; ++pass) {
+        t.s_in = u.s_in = pass ? la::StateIn{b.W, P.E, 1} : la::StateIn{nullptr, 0, 0};
+        t.s_out = u.s_out = pass ? la::StateOut{nullptr, 0, 0} : la::StateOut{b.W, P.E, 1};
+        if ((st = sweep(t, u, true, false, tk, tq, tdo)))
+            return st;
+        if (pass == 0) {
+            la::SplitScanArgs sc =
+                scan_args(P, b, g_gamma, P.D, P.E, la::StateIn{d_final_state, P.E, 1},
+                          la::StateOut{d_initial_state, P.E, 1}, reverse == 0);
+            sc.lam = lam;   // the key channels are G's rows
+            if ((st = scan(sc, s)))
+                return st;
+        }
+    }
+    // dk~ (fp32): backward-type (v, do, q~) from each segment's G, transposed
+    t = a;
+    u = a;
+    t.D = u.D = P.E;
+    t.E = u.E = P.D;
+    t.out = u.out = la::TokOut{dkf, fsb, fst, fsh};
+    u.out_f32 = 1;
+    u.q = tdo;
+    u.k = tv;
+    u.v = tok(q, d->qk_strides);
+    u.gate = gate_of(g, gs, true);
+    t.s_in = u.s_in = la::StateIn{b.W, 1, P.E};
+    t.s_out = u.s_out = la::StateOut{nullptr, 0, 0};
+    if ((st = sweep(t, u, true, true, tv, tdo, tq)))
+        return st;
+    // dq, dk and each segment's own dg (no final-state term) with its total
+    float *segtot = reinterpret_cast<float *>(ws + sx.segtot);
+    pa.dq = dq;
+    pa.dk = dk;
+    pa.dk32 = grouped ? dkf : nullptr;
+    pa.dqf = dqf;
+    pa.dkf = dkf;
+    pa.dg = dg;
+    pa.Ft = nullptr;
+    pa.dF = nullptr;
+    pa.E = P.E;
+    pa.segtot = segtot;
+    if ((e = la::gla_undo(pa, s)) != cudaSuccess)
+        return cuda_fail(e, "gated backward rescale");
+    float *bsum = reinterpret_cast<float *>(ws + sx.bsum);
+    la::GateGradArgs gg{};
+    gg.N = sx.S.NS;
+    gg.H = P.H;
+    gg.D = P.D;
+    gg.E = P.E;
+    gg.T = a.T;
+    gg.nblk = sx.nblk;
+    gg.cu = b.seg_cu;
+    gg.reverse = reverse ? 1 : 0;
+    gg.bf16 = dtype == LA_DTYPE_BF16;
+    gg.q = q;
+    gg.k = k;
+    gg.sb = d->qk_strides[0];
+    gg.st = d->qk_strides[1];
+    gg.sh = d->qk_strides[2];
+    gg.ksb = P.k_st[0];
+    gg.kst = P.k_st[1];
+    gg.ksh = P.k_st[2];
+    gg.khd = P.G;
+    gg.dqf = dqf;
+    gg.dkf = dkf;
+    gg.fsb = fsb;
+    gg.fst = fst;
+    gg.fsh = fsh;
+    gg.dq = dq;
+    gg.dk = grouped ? nullptr : dk;
+    gg.dg = dg;
+    gg.gsb = gs[0];
+    gg.gst = gs[1];
+    gg.gsh = gs[2];
+    gg.Ft = nullptr;
+    gg.dF = nullptr;
+    gg.bsum = bsum;
+    gg.flags = pa.flags;
+    if ((e = la::gate_grad(gg, s)) != cudaSuccess)
+        return cuda_fail(e, "gate gradient");
+    la::SplitDgArgs sg{};
+    sg.N = P.N;
+    sg.NS = sx.S.NS;
+    sg.H = P.H;
+    sg.D = P.D;
+    sg.E = P.E;
+    sg.seg_cu = b.seg_cu;
+    sg.seq_first = b.seq_first;
+    sg.reverse = reverse ? 1 : 0;
+    sg.flags = pa.flags;
+    sg.segtot = segtot;
+    sg.bsum = bsum;
+    sg.nblk = sx.nblk;
+    sg.Ft = Ft;
+    sg.dF = d_final_state;
+    sg.off = reinterpret_cast<float *>(ws + sx.off);
+    sg.dg = dg;
+    sg.gst = gs[1];
+    sg.gsh = gs[2];
+    sg.max_seg_len = sx.S.seg_len;
+    if ((e = la::split_dg(sg, s)) != cudaSuccess)
+        return cuda_fail(e, "gate gradient of the split");
+    if (grouped) {
+        const int rows = P.packed ? 1 : P.B;
+        const int bf16 = dtype == LA_DTYPE_BF16;
+        e = la::gqa_reduce(dkf, tok_out(dk, P.k_st), rows, P.T, P.Hkv, P.G, P.D, bf16, s, true);
+        if (e == cudaSuccess)
+            e = la::gqa_reduce(dvo.p, tok_out(dv, P.kv_v_st), rows, P.T, P.Hkv, P.G, P.E, bf16,
+                               s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "grouped key/value gradient sum");
+    }
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1273,8 +1555,11 @@ size_t la_gla_workspace_size(const la_dims *dims, int32_t dtype, const int32_t *
     g_msg = keep;
     if (st != LA_OK)
         return 0;
-    return gla_bwd_layout(P, dims, dtype).total +
-           (with_forward_operands ? 0 : gla_fwd_layout(P, dtype).total);
+    const size_t t = gla_bwd_layout(P, dims, dtype).total +
+                     (with_forward_operands ? 0 : gla_fwd_layout(P, dtype).total);
+    // without the forward's operands, enough for the split where it applies
+    return with_forward_operands ? t
+                                 : std::max(t, gla_bwd_split_layout(P, dims, dtype, nullptr).total);
 }
 
 la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const void *k,
@@ -1321,6 +1606,17 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     const la::TokOut dvo =
         grouped ? la::TokOut{wsb + bw.cv, vsb, vst, vsh} : tok_out(dv, P.kv_v_st);
     la::SweepArgs a = base_args(P, dtype, cu_seqlens, g_gamma, scale, reverse);
+    const bool chunkable = gla_bwd_chunkable(P, dims, q, k, v, d_o, dq, dk, dv, g, g_strides, dg);
+    // Few long sequences: the split, when the chunked form applies and the
+    // workspace holds it (the forward's operands, laid out per sequence, are
+    // not used there).
+    {
+        const GlaBwdSplitWs sx = gla_bwd_split_layout(P, dims, dtype, g_strides);
+        if (chunkable && sx.total && workspace_bytes >= sx.total)
+            return gla_bwd_split(P, dims, dtype, sx, a, q, k, v, d_o, g, g_strides, g_gamma,
+                                 initial_state, d_final_state, reverse, dq, dk, dv, dg,
+                                 d_initial_state, wsb, s);
+    }
     // The chunked form on the tensor cores, when it applies and the workspace
     // also holds its operands: the three sweeps on q~, k~ for the (sequence,
     // head) pairs in range (dq~, dk~ in fp32 into the workspace), then dq~,
@@ -1330,23 +1626,11 @@ la_status la_gla_bwd(const la_dims *dims, int32_t dtype, const void *q, const vo
     la::GlaPrepArgs pa{};
     {
         const GlaFwdWs w = gla_fwd_layout(P, dtype);
-        auto al = [](const void *p, const int64_t *st) {
-            return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && st[0] % 8 == 0 && st[1] % 8 == 0 &&
-                   st[2] % 8 == 0;
-        };
-        const bool aligned = al(q, dims->qk_strides) && al(k, P.k_st) &&
-                             al(dq, dims->qk_strides) && al(dk, P.k_st) &&
-                             al(v, P.kv_v_st) && al(d_o, dims->v_strides) &&
-                             al(dv, P.kv_v_st);
-        const bool gate_pairs = (reinterpret_cast<uintptr_t>(g) & 7) == 0 &&
-                                (reinterpret_cast<uintptr_t>(dg) & 7) == 0 &&
-                                g_strides[0] % 2 == 0 && g_strides[1] % 2 == 0 &&
-                                g_strides[2] % 2 == 0;
         // the forward's operands, when the caller kept them
         const bool ready = w.total && fwd_workspace &&
                            (reinterpret_cast<uintptr_t>(fwd_workspace) & 255) == 0 &&
                            fwd_workspace_bytes >= w.total;
-        if (w.total && (ready || workspace_bytes >= need_ws + w.total) && aligned && gate_pairs) {
+        if (w.total && (ready || workspace_bytes >= need_ws + w.total) && chunkable) {
             uint8_t *ws = ready ? static_cast<uint8_t *>(fwd_workspace)
                                 : static_cast<uint8_t *>(workspace) + need_ws;
             int *fl = reinterpret_cast<int *>(ws + w.flags);

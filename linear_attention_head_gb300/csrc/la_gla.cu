@@ -124,7 +124,76 @@ template <typename T> __global__ void __launch_bounds__(256) block_scan(GateGrad
     }
 }
 
+// One thread per (sequence, head, channel): the offsets of the sequence's
+// segments, walked from the one processed last (whose offset is the final
+// state's term) to the one processed first.
+__global__ void __launch_bounds__(256) split_dg_offsets(SplitDgArgs a)
+{
+    const int n = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+    if (c >= a.D)
+        return;
+    float carry = 0.f;
+    if (a.dF && a.Ft) {
+        const int64_t sidx = ((int64_t)n * a.H + h) * (int64_t)a.D * a.E;
+        for (int e = 0; e < a.E; ++e)
+            carry += a.Ft[sidx + (int64_t)e * a.D + c] * a.dF[sidx + (int64_t)c * a.E + e];
+    }
+    const int first = a.seq_first[n], count = a.seq_first[n + 1] - first;
+    for (int j = 0; j < count; ++j) {
+        // processing order: ascending segments going forward, descending in
+        // reverse; walked here from the last processed
+        const int seg = first + (a.reverse ? j : count - 1 - j);
+        const int64_t sh = (int64_t)seg * a.H + h;
+        a.off[sh * a.D + c] = carry;
+        float tot = 0.f;
+        if (a.flags[sh]) {
+            const int64_t len = (int64_t)a.seg_cu[seg + 1] - a.seg_cu[seg];
+            const int nb = (int)((len + DG_TB - 1) / DG_TB);
+            for (int b = 0; b < nb && b < a.nblk; ++b)
+                tot += a.bsum[(sh * a.nblk + b) * a.D + c];
+        } else {
+            tot = a.segtot[sh * a.D + c];
+        }
+        carry += tot;
+    }
+}
+
+// Grid (segment, head, slice of DG_TB tokens); thread = channel.
+__global__ void __launch_bounds__(256) split_dg_add(SplitDgArgs a)
+{
+    const int seg = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+    if (c >= a.D)
+        return;
+    const int64_t t0 = a.seg_cu[seg] + (int64_t)blockIdx.z * DG_TB, t1 = a.seg_cu[seg + 1];
+    if (t0 >= t1)
+        return;
+    const float o = a.off[((int64_t)seg * a.H + h) * a.D + c];
+    float *p = a.dg + (int64_t)h * a.gsh + c;
+    const int64_t te = t1 - t0 < DG_TB ? t1 : t0 + DG_TB;
+#pragma unroll 8
+    for (int64_t t = t0; t < te; ++t)
+        p[t * a.gst] += o;
+}
+
 }  // namespace
+
+cudaError_t split_dg(const SplitDgArgs &a, cudaStream_t s)
+{
+    if (a.N == 0 || a.NS == 0 || a.H == 0)
+        return cudaSuccess;
+    if (a.D > 256 || a.N > 65535 || a.NS > 0x7fffffff || a.H > 65535)
+        return cudaErrorNotSupported;
+    const int threads = (a.D + 31) / 32 * 32;
+    split_dg_offsets<<<dim3((unsigned)a.N, (unsigned)a.H), threads, 0, s>>>(a);
+    note_launch();
+    // the longest segment's tokens in DG_TB slices
+    const int64_t slices = (a.max_seg_len + DG_TB - 1) / DG_TB;
+    if (slices < 1 || slices > 65535)
+        return cudaErrorNotSupported;
+    split_dg_add<<<dim3((unsigned)a.NS, (unsigned)a.H, (unsigned)slices), threads, 0, s>>>(a);
+    note_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s)
 {

@@ -399,6 +399,8 @@ __global__ void __launch_bounds__(UG * UCP, 4) gla_undo_kernel(GlaPrepArgs a)
         carry.y += tot.y;
         __syncthreads();   // s_tm read by all before the next chunk writes it
     }
+    if (a.segtot && grp == 0)
+        *reinterpret_cast<float2 *>(a.segtot + hv * a.D + c) = carry;
 }
 
 // One CTA per (segment, head), one thread per key channel: the segment's

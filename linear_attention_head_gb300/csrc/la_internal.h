@@ -110,6 +110,8 @@ struct GlaPrepArgs {
     const float *dqf, *dkf;   // gla_undo: dq~, dk~ in (fp32, dense [rows][T][H][D])
     float *dk32;              // gla_undo: when set, dk goes there in fp32, in
                               // place of dk~ (per query head), not to dk
+    float *segtot = nullptr;  // gla_undo, when set: each pair's sum of the terms
+                              // (with the final state's, if dF), [N][H][D]
     float *dg;                // gla_undo: the gate's gradient (the gate's strides)
     const float *Ft, *dF;     // gla_undo: final state (transposed, [E][D] per
                               // pair) and its gradient ([D][E]), or dF null
@@ -222,6 +224,29 @@ struct GateGradArgs {
     const int *flags = nullptr;
 };
 cudaError_t gate_grad(const GateGradArgs &a, cudaStream_t s);
+
+// dg of the sequence split (gated backward): each segment's dg was formed
+// from its own terms alone (gla_undo with segtot, or gate_grad's block sums
+// for the flagged pairs); this adds to every token of segment s the sum of
+// the terms of the segments processed after it, plus the final state's term
+// sum_e F dF (Ft transposed [N][H][E][D], dF [N][H][D][E], either may be
+// null).  Segments of sequence n: [seq_first[n], seq_first[n + 1]) over the
+// one-row token view (seg_cu); dg strides gst, gsh.  off: scratch [NS][H][D].
+struct SplitDgArgs {
+    int N, NS, H, D, E;
+    const int32_t *seg_cu, *seq_first;
+    int reverse;
+    const int *flags;          // [NS][H]: flagged pairs take their total from bsum
+    const float *segtot;       // [NS][H][D]
+    const float *bsum;         // [NS][H][nblk][D]
+    int64_t nblk;
+    const float *Ft, *dF;
+    float *off;
+    float *dg;
+    int64_t gst, gsh;
+    int64_t max_seg_len;       // the longest segment's tokens
+};
+cudaError_t split_dg(const SplitDgArgs &a, cudaStream_t s);
 
 // State scan of the sequence split (la_split.cu).  W holds one D x E fp32
 // state per (segment, head), [NS][H][D][E]; on entry the segments' results

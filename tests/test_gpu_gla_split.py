@@ -145,3 +145,93 @@ def test_gated_split_training_step():
                  dk=k.grad.cpu(), dv=v.grad.cpu(), dg=g.grad.cpu()),
             dict(o=ro, final_state=rf, dq=rq, dk=rk, dv=rv, dg=rg), TOL[torch.bfloat16],
             label="gated split training step")
+
+
+def _bwd_ws_bytes(x, split):
+    d = N.LaDims()
+    B, T, H, D = x["q"].shape
+    E = x["v"].shape[3]
+    cu = x["cu_seqlens"]
+    d.batch, d.seq_len, d.heads, d.dim_qk, d.dim_v = B, T, H, D, E
+    d.num_seqs = 0 if cu is None else len(cu) - 1
+    for i in range(3):
+        d.qk_strides[i] = x["q"].stride(i)
+        d.v_strides[i] = x["v"].stride(i)
+    keep = None if cu is None else cu.to(torch.int32).contiguous()
+    host = None if keep is None else ctypes.c_void_p(keep.data_ptr())
+    lib = N.lib()
+    N.check(lib.la_set_sequence_split(1 if split else 0, 256))
+    try:
+        return int(lib.la_gla_workspace_size(ctypes.byref(d), N.LA_DTYPE_BF16, host, 0))
+    finally:
+        N.check(lib.la_set_sequence_split(1, 256))
+
+
+def _full(x, reverse):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o, fin = la.gla_fwd(d["q"], d["k"], d["v"], d["g"], d["g_gamma"], d["scale"],
+                        d["initial_state"], reverse, x["cu_seqlens"])
+    dq, dk, dv, dg, dinit = la.gla_bwd(d["q"], d["k"], d["v"], d["do"], d["g"], d["g_gamma"],
+                                       d["scale"], d["initial_state"], d["d_final_state"],
+                                       reverse, x["cu_seqlens"])
+    torch.cuda.synchronize()
+    la.get_device_error()
+    out = dict(o=o, final_state=fin, dq=dq, dk=dk, dv=dv, dg=dg, d_initial_state=dinit)
+    return {k: v.cpu() for k, v in out.items()}
+
+
+def _full_ref(x, reverse):
+    ref = _ref(x, reverse)
+    dq, dk, dv, dg, dinit = oracle.gla_backward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"],
+                                                x["scale"], x["do"], x["initial_state"],
+                                                x["d_final_state"], reverse, x["cu_seqlens"])
+    ref.update(dq=dq, dk=dk, dv=dv, dg=dg, d_initial_state=dinit)
+    return ref
+
+
+# The backward split: dq~ in two passes around a scan with column decays,
+# dv around a scan against the processing order (which gives d_initial_state),
+# dk~ from the scanned G transposed, and dg per segment plus each segment's
+# offset (the later segments' terms and the final state's term).
+@pytest.mark.parametrize("B,T,E", [(1, 3000, 128), (2, 1500, 128), (1, 2500, 64)])
+def test_gated_split_backward_matches_oracle(B, T, E):
+    x = _inputs(B, T, 2, E, seed=2 * T + E)
+    assert _bwd_ws_bytes(x, True) > _bwd_ws_bytes(x, False) > 0
+    for reverse in (False, True):
+        compare(_full(x, reverse), _full_ref(x, reverse), TOL[torch.bfloat16],
+                label="gated split fwd+bwd B=%d T=%d E=%d rev=%d" % (B, T, E, reverse))
+
+
+def test_gated_split_backward_packed_with_out_of_range_segments():
+    # flagged segments (head 1, tokens 300-900 of the first sequence) take
+    # their dg from the block scan and their totals from its block sums
+    x = _inputs(1, 0, 2, 128, seqlens=[2100, 0, 700, 100, 37], seed=6)
+    x["g"][0, 300:900, 1] = -3.0
+    assert _bwd_ws_bytes(x, True) > _bwd_ws_bytes(x, False)
+    for reverse in (False, True):
+        compare(_full(x, reverse), _full_ref(x, reverse), TOL[torch.bfloat16],
+                cu=x["cu_seqlens"], label="gated split packed fwd+bwd rev=%d" % reverse)
+
+
+def test_gated_split_backward_grouped_heads():
+    x = _inputs(1, 3000, 4, 128, seed=7)
+    G = 2
+    kv = dict(x, k=x["k"][:, :, ::G].contiguous(), v=x["v"][:, :, ::G].contiguous())
+    rep = dict(x, k=kv["k"].repeat_interleave(G, dim=2), v=kv["v"].repeat_interleave(G, dim=2))
+    for reverse in (False, True):
+        ref = _full_ref(rep, reverse)
+        for name in ("dk", "dv"):
+            t = torch.as_tensor(ref[name])
+            ref[name] = t.reshape(t.shape[0], t.shape[1], -1, G, t.shape[3]).sum(3)
+        compare(_full(kv, reverse), ref, TOL[torch.bfloat16],
+                label="gated split grouped rev=%d" % reverse)
+
+
+def test_gated_split_backward_equals_unsplit_closely():
+    x = _inputs(1, 3000, 2, 128, seed=8)
+    got = _full(x, False)
+    N.check(N.lib().la_set_sequence_split(0, 0))
+    whole = _full(x, False)
+    for name in got:
+        ref = whole[name].float()
+        assert (got[name].float() - ref).abs().max() <= 2e-2 * ref.abs().max(), name
