@@ -346,6 +346,12 @@ size_t la_gla_fwd_workspace_size(const la_dims *dims, int32_t dtype,
  * grouping; dk and dv are the sums over each group's query heads, formed
  * from every query head's part (dk's in fp32, dv's in the token dtype, both
  * in the workspace) in fp32 and written in the token dtype.
+ * Sequence split (as la_gla_fwd's; a workspace of la_gla_workspace_size(...,
+ * 0) bytes): the operands are computed per segment (fwd_workspace is not
+ * used), dq~ and dv run in two passes around scans with per-channel decays
+ * (the latter giving d_initial_state), dk~ from the scanned gradients, and
+ * dg per segment plus each segment's offset: the sum of the terms of the
+ * segments processed after it and the final state's term.
  *   fwd_workspace  the workspace of a la_gla_fwd call on the same q, k, g,
  *              g_gamma, reverse and cu_seqlens that reported operands_written
  *              = 1, untouched since; or NULL.  The backward then uses the
