@@ -158,7 +158,8 @@ __global__ void __launch_bounds__(256) split_dg_offsets(SplitDgArgs a)
     }
 }
 
-// Grid (segment, head, slice of DG_TB tokens); thread = channel.
+// Grid (segment, head, slice of DG_TB tokens); thread = channel, one token
+// at a time (any strides).
 __global__ void __launch_bounds__(256) split_dg_add(SplitDgArgs a)
 {
     const int seg = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
@@ -173,6 +174,35 @@ __global__ void __launch_bounds__(256) split_dg_add(SplitDgArgs a)
 #pragma unroll 8
     for (int64_t t = t0; t < te; ++t)
         p[t * a.gst] += o;
+}
+
+// The same with four channels per thread (16-byte aligned rows, D % 4 == 0):
+// thread (token lane, channel quad) walks the slice's tokens DG_TB / TL at a
+// time apart.
+constexpr int TL = 4;   // token lanes per CTA
+__global__ void __launch_bounds__(256) split_dg_add4(SplitDgArgs a)
+{
+    const int seg = blockIdx.x, h = blockIdx.y;
+    const int D4 = a.D / 4, q = (int)threadIdx.x % D4, lane = (int)threadIdx.x / D4;
+    if (lane >= TL)
+        return;
+    const int64_t t0 = a.seg_cu[seg] + (int64_t)blockIdx.z * DG_TB, t1 = a.seg_cu[seg + 1];
+    if (t0 >= t1)
+        return;
+    const float4 o =
+        *reinterpret_cast<const float4 *>(a.off + ((int64_t)seg * a.H + h) * a.D + 4 * q);
+    float *p = a.dg + (int64_t)h * a.gsh + 4 * q;
+    const int64_t te = t1 - t0 < DG_TB ? t1 : t0 + DG_TB;
+#pragma unroll 4
+    for (int64_t t = t0 + lane; t < te; t += TL) {
+        float4 *x = reinterpret_cast<float4 *>(p + t * a.gst);
+        float4 v = *x;
+        v.x += o.x;
+        v.y += o.y;
+        v.z += o.z;
+        v.w += o.w;
+        *x = v;
+    }
 }
 
 }  // namespace
@@ -190,7 +220,13 @@ cudaError_t split_dg(const SplitDgArgs &a, cudaStream_t s)
     const int64_t slices = (a.max_seg_len + DG_TB - 1) / DG_TB;
     if (slices < 1 || slices > 65535)
         return cudaErrorNotSupported;
-    split_dg_add<<<dim3((unsigned)a.NS, (unsigned)a.H, (unsigned)slices), threads, 0, s>>>(a);
+    const dim3 grid((unsigned)a.NS, (unsigned)a.H, (unsigned)slices);
+    const bool vec = a.D % 4 == 0 && a.D / 4 * TL <= 256 && a.gst % 4 == 0 && a.gsh % 4 == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.dg) & 15) == 0;
+    if (vec)
+        split_dg_add4<<<grid, a.D / 4 * TL, 0, s>>>(a);
+    else
+        split_dg_add<<<grid, threads, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }

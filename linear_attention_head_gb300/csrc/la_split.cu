@@ -37,17 +37,31 @@ __global__ void __launch_bounds__(256) split_scan_kernel(SplitScanArgs a)
     float carry = a.start.p ? a.start.p[user + r * a.start.rs + c * a.start.cs] : 0.f;
     const float g = a.g[h];
     const int first = a.seq_first[n], count = a.seq_first[n + 1] - first;
-    for (int j = 0; j < count; ++j) {
-        const int seg = first + (a.descending ? count - 1 - j : j);
-        float *w = a.W + ((int64_t)seg * a.H + h) * de + idx;
-        const float f = *w;
-        *w = carry;   // the segment's initial state
-        const int len = a.seg_cu[seg + 1] - a.seg_cu[seg];
-        const float decay =
-            a.lam ? expf(a.lam[((int64_t)seg * a.H + h) * (a.lam_cols ? a.E : a.D) +
-                               (a.lam_cols ? c : r)])
-                  : expf(g * (float)len);
-        carry = fmaf(decay, carry, f);
+    const int64_t lw = a.lam_cols ? a.E : a.D, li = a.lam_cols ? c : r;
+    // eight segments' contributions and decays loaded together, then the
+    // carries formed in visiting order and stored
+    constexpr int BATCH = 8;
+    for (int j0 = 0; j0 < count; j0 += BATCH) {
+        float f[BATCH], dec[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            f[u] = 0.f;
+            dec[u] = 1.f;
+            if (j0 + u < count) {
+                const int seg = first + (a.descending ? count - 1 - (j0 + u) : j0 + u);
+                f[u] = a.W[((int64_t)seg * a.H + h) * de + idx];
+                const int len = a.seg_cu[seg + 1] - a.seg_cu[seg];
+                dec[u] = a.lam ? a.lam[((int64_t)seg * a.H + h) * lw + li] : g * (float)len;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            if (j0 + u < count) {
+                const int seg = first + (a.descending ? count - 1 - (j0 + u) : j0 + u);
+                a.W[((int64_t)seg * a.H + h) * de + idx] = carry;   // the segment's initial state
+                carry = fmaf(expf(dec[u]), carry, f[u]);
+            }
+        }
     }
     if (a.fin.p)
         a.fin.p[user + r * a.fin.rs + c * a.fin.cs] = carry;
