@@ -235,3 +235,28 @@ def test_gated_split_backward_equals_unsplit_closely():
     for name in got:
         ref = whole[name].float()
         assert (got[name].float() - ref).abs().max() <= 2e-2 * ref.abs().max(), name
+
+
+def test_gated_split_grouped_packed_out_of_range_both_directions():
+    # everything at once: packed sequences (one empty), two query heads per
+    # key/value head, one query head's gates out of range over part of the
+    # longest sequence, both directions, forward and backward
+    x = _inputs(1, 0, 4, 128, seqlens=[2600, 0, 900, 33], seed=15)
+    x["g"][0, 1000:1600, 3] = -3.0
+    G = 2
+    kv = dict(x, k=x["k"][:, :, ::G].contiguous(), v=x["v"][:, :, ::G].contiguous())
+    rep = dict(x, k=kv["k"].repeat_interleave(G, dim=2), v=kv["v"].repeat_interleave(G, dim=2))
+    for reverse in (False, True):
+        ref = _full_ref(rep, reverse)
+        for name in ("dk", "dv"):
+            t = torch.as_tensor(ref[name])
+            ref[name] = t.reshape(t.shape[0], t.shape[1], -1, G, t.shape[3]).sum(3)
+        compare(_full(kv, reverse), ref, TOL[torch.bfloat16], cu=x["cu_seqlens"],
+                label="gated split grouped packed rev=%d" % reverse)
+
+
+def test_gated_split_packed_value_width_64():
+    x = _inputs(1, 0, 2, 64, seqlens=[1800, 300, 0, 2500], seed=16)
+    for reverse in (False, True):
+        compare(_full(x, reverse), _full_ref(x, reverse), TOL[torch.bfloat16],
+                cu=x["cu_seqlens"], label="gated split packed E=64 rev=%d" % reverse)
