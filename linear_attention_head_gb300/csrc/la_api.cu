@@ -1063,9 +1063,10 @@ la::GlaPrepArgs gla_prep_args(const Problem &P, const la_dims *d, const void *q,
 
 // The chunked form's forward sweep on the pre-pass's operands: X = q~,
 // Y = k~ (dense [rows][T][H][D]), Z = v, the state's rows gated; pairs the
-// pre-pass flagged are left to the token-by-token kernels.
+// pre-pass flagged are left to the token-by-token kernels.  so: the final
+// states alone.
 cudaError_t gla_chunked_sweep(const la::SweepArgs &a, const la::GlaPrepArgs &pa, int64_t ncmax,
-                              cudaStream_t s)
+                              cudaStream_t s, bool so = false)
 {
     la::SweepArgs t = a;
     t.gate = la::Gate{};
@@ -1076,12 +1077,12 @@ cudaError_t gla_chunked_sweep(const la::SweepArgs &a, const la::GlaPrepArgs &pa,
     t.gla_flag_run = 0;
     const int64_t dsh = a.D, dst = (int64_t)a.H * a.D, dsb = dst * a.T;
     return la::tc_gla_sweep(t, false, false, la::Tok{pa.xq, dsb, dst, dsh, 1},
-                            la::Tok{pa.yk, dsb, dst, dsh, 1}, t.v, s);
+                            la::Tok{pa.yk, dsb, dst, dsh, 1}, t.v, s, so);
 }
 
 // The gated forward split into segments (few long sequences): the pre-pass
 // over the segments (also giving each chunk's total log-decay), the
-// segments' log-decays from those, the sweep from zero states
+// segments' log-decays from those, the sweep's state-only mode from zero states
 // (chunked, flagged segments token by token) into the per-segment states,
 // the scan with per-channel decays (which writes the final state), and the
 // sweep again from the scanned states for the outputs.  The operands are
@@ -1124,7 +1125,7 @@ la_status gla_fwd_split(const Problem &P, const la_dims *d, const GlaSplitWs &sw
         t.s_in = pass ? la::StateIn{b.W, P.E, 1} : la::StateIn{nullptr, 0, 0};
         t.s_out = pass ? la::StateOut{nullptr, 0, 0} : la::StateOut{b.W, P.E, 1};
         if (tc) {
-            e = gla_chunked_sweep(t, pa, sw.w.ncmax, s);
+            e = gla_chunked_sweep(t, pa, sw.w.ncmax, s, pass == 0);
             if (e == cudaErrorNotSupported && pass == 0)
                 tc = false;   // every segment token by token, in both passes
             else if (e != cudaSuccess)
@@ -1297,15 +1298,16 @@ la_status gla_bwd_split(const Problem &P, const la_dims *d, int32_t dtype, const
     const la::Tok tdo = tok(d_o, d->v_strides), tv = tok(v, P.kv_v_st, P.G);
     // one sweep: the chunked form (x, y, z tiles) for the pairs in range, the
     // token-by-token kernels (u's tiles and gate) for the flagged ones
+    // (so: the tensor-core sweep's state-only mode, for the first passes)
     auto sweep = [&](la::SweepArgs t, la::SweepArgs u, bool bwd, bool cols, const la::Tok &x,
-                     const la::Tok &y, const la::Tok &z) -> la_status {
+                     const la::Tok &y, const la::Tok &z, bool so) -> la_status {
         t.gate = la::Gate{};
         t.gla_er = pa.er;
         t.gla_u = pa.u;
         t.gla_ncmax = sx.w.ncmax;
         t.gla_flags = pa.flags;
         t.gla_flag_run = 0;
-        cudaError_t err = la::tc_gla_sweep(t, bwd, cols, x, y, z, s);
+        cudaError_t err = la::tc_gla_sweep(t, bwd, cols, x, y, z, s, so);
         if (err != cudaSuccess)
             return cuda_fail(err, "gated tensor-core sweep launch");
         u.gla_flags = pa.flags;
@@ -1325,7 +1327,7 @@ la_status gla_bwd_split(const Problem &P, const la_dims *d, int32_t dtype, const
     for (int pass = 0; pass < 2; ++pass) {
         t.s_in = u.s_in = pass ? la::StateIn{b.W, P.D, 1} : la::StateIn{nullptr, 0, 0};
         t.s_out = u.s_out = pass ? la::StateOut{nullptr, 0, 0} : la::StateOut{b.W, P.D, 1};
-        if ((st = sweep(t, u, false, true, tdo, tv, tk)))
+        if ((st = sweep(t, u, false, true, tdo, tv, tk, pass == 0)))
             return st;
         if (pass == 0) {
             la::SplitScanArgs sc =
@@ -1351,7 +1353,7 @@ la_status gla_bwd_split(const Problem &P, const la_dims *d, int32_t dtype, const
     for (int pass = 0; pass < 2; ++pass) {
         t.s_in = u.s_in = pass ? la::StateIn{b.W, P.E, 1} : la::StateIn{nullptr, 0, 0};
         t.s_out = u.s_out = pass ? la::StateOut{nullptr, 0, 0} : la::StateOut{b.W, P.E, 1};
-        if ((st = sweep(t, u, true, false, tk, tq, tdo)))
+        if ((st = sweep(t, u, true, false, tk, tq, tdo, pass == 0)))
             return st;
         if (pass == 0) {
             la::SplitScanArgs sc =
@@ -1375,7 +1377,7 @@ la_status gla_bwd_split(const Problem &P, const la_dims *d, int32_t dtype, const
     u.gate = gate_of(g, gs, true);
     t.s_in = u.s_in = la::StateIn{b.W, 1, P.E};
     t.s_out = u.s_out = la::StateOut{nullptr, 0, 0};
-    if ((st = sweep(t, u, true, true, tv, tdo, tq)))
+    if ((st = sweep(t, u, true, true, tv, tdo, tq, false)))
         return st;
     // dq, dk and each segment's own dg (no final-state term) with its total
     float *segtot = reinterpret_cast<float *>(ws + sx.segtot);

@@ -136,13 +136,15 @@ struct SegDecayArgs {
 };
 cudaError_t gla_segment_decay(const SegDecayArgs &a, cudaStream_t s);
 // A tensor-core sweep of the gated form on rescaled operands (la_gla_prep.cu)
-// with tile roles X, Y, Z given (bf16, D = 128 X and Y width): forward-type or
-// backward-type (bwd), the gated key channels being the state's rows or its
-// columns (cols, needs E = 128); a.gla_* set, a.out the output: bf16 rows,
-// or with cols (the sweeps giving dq~ and dk~) fp32 rows, 16-byte aligned.
+// with tile roles X, Y, Z given: forward-type or backward-type (bwd), the 128
+// gated key channels being the state's rows (D = 128, E in {64, 128}) or its
+// columns (cols: E = 128, D in {64, 128}); a.gla_* set, a.out the output:
+// bf16 rows, or with cols (the sweeps giving dq~ and dk~) fp32 rows, 16-byte
+// aligned.  so: the final states alone (the state-only mode; X and the output
+// are not touched), for the sequence split's first pass.
 // cudaErrorNotSupported when the tensor maps cannot be built.
 cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, const Tok &y,
-                         const Tok &z, cudaStream_t s);
+                         const Tok &z, cudaStream_t s, bool so = false);
 // The final states of a sweep alone (its outputs are not written; X is not
 // read): the tensor-core kernel's state-only mode, for the sequence split's
 // first pass.  Eligibility as tc_sweep_supported.

@@ -479,13 +479,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_sweep_kernel(const __grid_co
                     break;
                 tc_fence_after();
                 if (SO) {
-                    // column factor for the state update, applied to row i of Y
-                    float lc = 0.f;
-                    if (i < Lc) {
-                        const int pi = rev ? Lc - 1 - i : i;
-                        lc = BWD ? scale * pw[pi + 1] : pw[Lc - 1 - pi];
+                    if (GLA) {
+                        // Y carries its factors (backward-type: times s);
+                        // rows past the sequence's end cleared, as below
+                        uint8_t *yrow = sm + s * L::STAGE + L::XB + hh * (TC_C * 128) + i * 128;
+                        if (i >= Lc)
+                            zero_row(yrow);
+                        else if (BWD)
+                            scale_row_sw128(yrow, i, scale);
+                    } else {
+                        // column factor for the state update, applied to row i of Y
+                        float lc = 0.f;
+                        if (i < Lc) {
+                            const int pi = rev ? Lc - 1 - i : i;
+                            lc = BWD ? scale * pw[pi + 1] : pw[Lc - 1 - pi];
+                        }
+                        scale_y(s, lc);
                     }
-                    scale_y(s, lc);
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(p_ready);
@@ -876,7 +886,7 @@ cudaError_t launch_tc(const SweepArgs &a, cudaStream_t s, const Tok *xyz = nullp
         return cudaErrorNotSupported;
     if (SO)
         p.mx = p.mo = p.my;
-    if (GLA == 2) {
+    if (GLA == 2 && !SO) {
         // fp32 output: 32-column tiles, or 16-byte row writes
         if ((reinterpret_cast<uintptr_t>(a.out.p) & 15) || a.out.sb % 4 || a.out.st % 4 ||
             a.out.sh % 4 ||
@@ -959,24 +969,34 @@ cudaError_t tc_forward_sweep(const SweepArgs &a, cudaStream_t s) { return tc_swe
 cudaError_t tc_backward_sweep(const SweepArgs &a, cudaStream_t s) { return tc_sweep<true>(a, s); }
 
 cudaError_t tc_gla_sweep(const SweepArgs &a, bool bwd, bool cols, const Tok &x, const Tok &y,
-                         const Tok &z, cudaStream_t s)
+                         const Tok &z, cudaStream_t s, bool so)
 {
     if (a.N == 0)
         return cudaSuccess;
     const Tok xyz[3] = {x, y, z};
     // one CTA per (sequence, head) with the 128 key channels as the state's
     // rows (D = 128, E in {64, 128}) or columns (E = 128, D in {64, 128})
+    // state only: the forward-type sweeps (rows and columns) and the
+    // backward-type one with gated rows (the split's first passes)
     if (cols) {
-        if (a.E != 128 || (a.D != 64 && a.D != 128))
+        if (a.E != 128 || (a.D != 64 && a.D != 128) || (so && bwd))
             return cudaErrorNotSupported;
         if (bwd)
             return a.D == 128 ? launch_tc<128, 128, true, 2>(a, s, xyz)
                               : launch_tc<64, 128, true, 2>(a, s, xyz);
+        if (so)
+            return a.D == 128 ? launch_tc<128, 128, false, 2, true>(a, s, xyz)
+                              : launch_tc<64, 128, false, 2, true>(a, s, xyz);
         return a.D == 128 ? launch_tc<128, 128, false, 2>(a, s, xyz)
                           : launch_tc<64, 128, false, 2>(a, s, xyz);
     }
     if (a.D != 128 || (a.E != 64 && a.E != 128))
         return cudaErrorNotSupported;
+    if (so)
+        return bwd ? (a.E == 128 ? launch_tc<128, 128, true, 1, true>(a, s, xyz)
+                                 : launch_tc<128, 64, true, 1, true>(a, s, xyz))
+                   : (a.E == 128 ? launch_tc<128, 128, false, 1, true>(a, s, xyz)
+                                 : launch_tc<128, 64, false, 1, true>(a, s, xyz));
     if (bwd)
         return a.E == 128 ? launch_tc<128, 128, true, 1>(a, s, xyz)
                           : launch_tc<128, 64, true, 1>(a, s, xyz);
