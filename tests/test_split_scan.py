@@ -134,3 +134,73 @@ def test_gated_split_scans_with_per_channel_decays(seg, reverse):
         # move by 1e-3 of their maximum or less: far above the 1e-12 match)
         assert np.abs(o_bad - np.asarray(ro)).max() > 1e-6 * np.abs(ro).max()
         assert np.abs(fin_bad - np.asarray(rfin)).max() > 1e-6 * np.abs(rfin).max()
+
+
+def _gated_split_backward(x, seg, reverse, g_decay_on_rows=True):
+    """The gated backward split through the oracle: pass 1 gives each
+    segment's state from zero (forward) and its dL/dS at entry from a zero
+    gradient at its end (backward); the scans carry S forward and G against
+    the visiting order, both with the segment's per-key-channel decay
+    diag(exp(lam)) on the key rows; pass 2 runs each segment's backward from
+    its entering S and the G that arrives from the segments after it.
+    g_decay_on_rows=False plants a mistake: G's decay on the value columns."""
+    q, k, v, gt, do = (x[n] for n in ("q", "k", "v", "g", "do"))
+    gg, s = x["g_gamma"], x["scale"]
+    S0, dF = x["initial_state"], x["d_final_state"]
+    B, T, H, d = q.shape
+    e = v.shape[3]
+    segs = _seg_bounds(T, seg)
+    visit = segs[::-1] if reverse else segs
+    part = lambda t, a, b: t[:, a:b].contiguous()
+    zero = torch.zeros((B, H, d, e), dtype=torch.float64)
+    F, Gc, lam = {}, {}, {}
+    for a, b in segs:
+        args = (part(q, a, b), part(k, a, b), part(v, a, b), part(gt, a, b), gg, s)
+        _, F[a] = oracle.gla_forward(*args, None, reverse)
+        *_, Gc[a] = oracle.gla_backward(*args, part(do, a, b), zero, zero, reverse)
+        lam[a] = torch.exp((b - a) * gg.double()[None, :, None] + gt[:, a:b].double().sum(1))
+    Win, carry = {}, S0.double()
+    for a, b in visit:
+        Win[a] = carry
+        carry = lam[a][..., None] * carry + torch.as_tensor(F[a])
+    Wout, carry = {}, dF.double()
+    for a, b in visit[::-1]:
+        Wout[a] = carry
+        dec = lam[a][..., None] if g_decay_on_rows else lam[a][..., None, :e]
+        carry = dec * carry + torch.as_tensor(Gc[a])
+    dinit = carry
+    out = {n: np.zeros(t.shape) for n, t in (("dq", q), ("dk", k), ("dv", v), ("dg", gt))}
+    for a, b in segs:
+        dq, dk, dv, dg, _ = oracle.gla_backward(part(q, a, b), part(k, a, b), part(v, a, b),
+                                                part(gt, a, b), gg, s, part(do, a, b), Win[a],
+                                                Wout[a], reverse)
+        for n, t in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg)):
+            out[n][:, a:b] = np.asarray(t)
+    out["d_initial_state"] = dinit.numpy()
+    return out
+
+
+@pytest.mark.parametrize("seg", [1, 6, 16])
+@pytest.mark.parametrize("reverse", [False, True])
+def test_gated_split_backward_scans_with_per_channel_decays(seg, reverse):
+    # dq, dk, dv, dg and d_initial_state of the whole sequence from the
+    # segments' backward runs around the two scans (per-key-channel decays
+    # on the key rows of S and of G = dL/dS)
+    x = W.random_small(17, 2, 40, 3, 4, 4, g_lo=-0.5, g_hi=0.0)
+    gen = torch.Generator().manual_seed(18)
+    x["g"] = -0.6 * torch.rand(x["q"].shape, generator=gen, dtype=torch.float64)
+    x["initial_state"] = torch.randn((2, 3, 4, 4), generator=gen, dtype=torch.float64)
+    x["d_final_state"] = torch.randn((2, 3, 4, 4), generator=gen, dtype=torch.float64)
+    x["scale"] = 0.8
+    got = _gated_split_backward(x, seg, reverse)
+    dq, dk, dv, dg, dinit = oracle.gla_backward(x["q"], x["k"], x["v"], x["g"], x["g_gamma"],
+                                                x["scale"], x["do"], x["initial_state"],
+                                                x["d_final_state"], reverse)
+    ref = dict(dq=dq, dk=dk, dv=dv, dg=dg, d_initial_state=dinit)
+    for name, r in ref.items():
+        r = np.asarray(r)
+        assert np.abs(got[name] - r).max() <= 1e-11 * max(1.0, np.abs(r).max()), name
+    # G's decay applied to its value columns instead of its key rows fails
+    if len(_seg_bounds(40, seg)) > 1:
+        bad = _gated_split_backward(x, seg, reverse, g_decay_on_rows=False)
+        assert np.abs(bad["dk"] - np.asarray(dk)).max() > 1e-6 * np.abs(np.asarray(dk)).max()
